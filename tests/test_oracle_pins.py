@@ -1,0 +1,499 @@
+"""Pins for the fp64 oracle: each check ties it to something other than itself -- a closed
+form, a hand-worked example, brute force, a library routine or an invariant -- so that a
+dropped term, a wrong sign or index, or a transposed operand fails one of them.
+
+Sources: the DiffusionGemma vLLM page ("DiffusionGemma: vLLM이 네이티브로 지원하는 최초의
+디퓨전 언어 모델(dLLM)"), sections "엔트로피 기반 디노이징" (entropy equation H(p), the
+entropy-bound rule, the convergence rule), "자기 조건화" (self-conditioning) and
+"DiffusionGemmaModelState와 DiffusionSampler" (Gumbel-max candidate, renoise, argmax canvas);
+Salmon et al., SC'11, for Philox-4x32.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import scipy.stats
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+NEG_INF = np.float32(-np.inf)
+
+
+# ----------------------------------------------------------------------------- Philox
+M0, M1 = 0xD2511F53, 0xCD9E8D57
+W0, W1 = 0x9E3779B9, 0xBB67AE85
+MASK = 0xFFFFFFFF
+
+
+def _philox_inverse(out, key, rounds):
+    """Undo Philox-4x32 round by round.  Each round is a bijection: the low halves of the
+    two products give back X0 and X2 through the multipliers' inverses mod 2^32, and the
+    high halves then unmask X1 and X3.  Round keys are replayed in reverse order."""
+    inv0, inv1 = pow(M0, -1, 1 << 32), pow(M1, -1, 1 << 32)
+    keys = []
+    k0, k1 = key
+    for r in range(rounds):
+        if r:
+            k0, k1 = (k0 + W0) & MASK, (k1 + W1) & MASK
+        keys.append((k0, k1))
+    y0, y1, y2, y3 = (int(v) for v in out)
+    for k0, k1 in reversed(keys):
+        x2 = (y1 * inv1) & MASK
+        x0 = (y3 * inv0) & MASK
+        hi1 = (M1 * x2) >> 32
+        hi0 = (M0 * x0) >> 32
+        x1 = y0 ^ hi1 ^ k0
+        x3 = y2 ^ hi0 ^ k1
+        y0, y1, y2, y3 = x0, x1, x2, x3
+    return [y0, y1, y2, y3]
+
+
+@pytest.mark.parametrize("rounds", [1, 2, 10])
+def test_philox_is_the_published_bijection(rounds):
+    rng = np.random.default_rng(1)
+    for _ in range(200):
+        ctr = rng.integers(0, 1 << 32, 4, dtype=np.uint64).astype(np.uint32)
+        key = rng.integers(0, 1 << 32, 2, dtype=np.uint64).astype(np.uint32)
+        out = oracle.philox4x32(ctr, key, rounds)
+        assert _philox_inverse(out, [int(k) for k in key], rounds) == [int(c) for c in ctr]
+
+
+def test_philox_statistics():
+    # byte histogram of 40000 outputs (160000 words) and single-bit avalanche
+    rng = np.random.default_rng(2)
+    words = []
+    for i in range(40000):
+        words.extend(oracle.philox4x32([i, 7, 3, 0], [0x1234, 0x5678]))
+    b = np.array(words, np.uint32).view(np.uint8)
+    chi2, p = scipy.stats.chisquare(np.bincount(b, minlength=256))
+    assert p > 1e-4, (chi2, p)
+    flips = []
+    for _ in range(300):
+        ctr = rng.integers(0, 1 << 32, 4, dtype=np.uint64).astype(np.uint32)
+        key = rng.integers(0, 1 << 32, 2, dtype=np.uint64).astype(np.uint32)
+        bit = int(rng.integers(0, 128))
+        c2 = ctr.copy()
+        c2[bit // 32] ^= np.uint32(1 << (bit % 32))
+        a = oracle.philox4x32(ctr, key)
+        z = oracle.philox4x32(c2, key)
+        flips.append(sum(bin(int(x) ^ int(y)).count("1") for x, y in zip(a, z)))
+    assert abs(np.mean(flips) - 64.0) < 2.0
+
+
+def test_uniform_mapping():
+    assert oracle.uniform(0) == 2.0 ** -24
+    assert oracle.uniform(0xFFFFFFFF) == 1.0 - 2.0 ** -24
+    rng = np.random.default_rng(3)
+    ws = np.sort(rng.integers(0, 1 << 32, 2000, dtype=np.uint64))
+    us = [oracle.uniform(int(w)) for w in ws]
+    assert all(a <= b for a, b in zip(us, us[1:]))
+    for u in us[:200]:
+        assert float(np.float32(u)) == u          # exact in fp32
+        assert 0.0 < u < 1.0
+
+
+def test_token_mapping():
+    for V in (2, 7, 1024, 262144, 152064):
+        assert oracle.token(0, 0, V) == 0
+        assert oracle.token(0xFFFFFFFF, 0xFFFFFFFF, V) == V - 1
+    # uniform over V = 7 on random words
+    rng = np.random.default_rng(4)
+    counts = np.zeros(7)
+    for _ in range(14000):
+        w0, w1 = (int(x) for x in rng.integers(0, 1 << 32, 2, dtype=np.uint64))
+        t = oracle.token(w0, w1, 7)
+        assert 0 <= t < 7
+        counts[t] += 1
+    assert scipy.stats.chisquare(counts).pvalue > 1e-4
+    # the token is the integer part of x * V / 2^64: monotone in x and splits [0, 2^64) evenly
+    assert oracle.token(0x80000000, 0, 2) == 1 and oracle.token(0x7FFFFFFF, 0xFFFFFFFF, 2) == 0
+    assert oracle.token(0x40000000, 0, 4) == 1 and oracle.token(0xC0000000, 0, 4) == 3
+
+
+def test_random_tokens_cover_vocab():
+    V = 5
+    seen = [oracle.random_token(9, 1, 0, i, oracle.STREAM_RENOISE, V) for i in range(5000)]
+    counts = np.bincount(seen, minlength=V)
+    assert scipy.stats.chisquare(counts).pvalue > 1e-4
+    # streams and steps give different draws
+    a = [oracle.random_token(9, 1, 0, i, oracle.STREAM_RENOISE, 1 << 30) for i in range(64)]
+    b = [oracle.random_token(9, 1, 0, i, oracle.STREAM_INIT, 1 << 30) for i in range(64)]
+    c = [oracle.random_token(9, 1, 1, i, oracle.STREAM_RENOISE, 1 << 30) for i in range(64)]
+    assert a != b and a != c
+
+
+# ----------------------------------------------------------------------------- entropy
+@pytest.mark.parametrize("V", [1024, 32768, 152064, 262144])
+def test_entropy_uniform_is_log_V(V):
+    row = np.full(V, 1.25, np.float32)
+    for T in (1.0, 0.3):
+        r = oracle.row_stats(row, T=T, sample=False)
+        # a sequential fp64 sum of V terms is exact to within V * 2^-53 relative
+        bound = V * 2.0 ** -53
+        assert r["entropy"] == pytest.approx(math.log(V), rel=bound)
+        assert r["entropy_alt"] == pytest.approx(math.log(V), rel=bound)
+        assert r["lse"] == pytest.approx(1.25 / T + math.log(V), rel=1e-12)
+        assert r["argmax"] == 0
+
+
+def test_entropy_one_hot_and_supports():
+    row = np.full(8, NEG_INF, np.float32)
+    row[5] = 3.0
+    r = oracle.row_stats(row, sample=True)
+    assert r["entropy"] == 0.0 and r["entropy_alt"] == 0.0
+    assert r["argmax"] == 5 and r["sample"] == 5
+    for j in range(4):   # uniform over 2^j of 8 entries -> j ln 2
+        row = np.full(8, NEG_INF, np.float32)
+        row[: 1 << j] = -2.0
+        assert oracle.row_stats(row, sample=False)["entropy"] == pytest.approx(j * math.log(2), abs=1e-15)
+
+
+def test_entropy_two_point_is_binary_entropy():
+    for a, b, T in [(0.0, 1.0, 1.0), (2.0, -3.0, 0.7), (5.0, 5.0, 2.0)]:
+        row = np.full(16, NEG_INF, np.float32)
+        row[3], row[11] = a, b
+        p = scipy.special.expit((a - b) / T)
+        ref = scipy.stats.entropy([p, 1 - p])
+        r = oracle.row_stats(row, T=T, sample=False)
+        assert r["entropy"] == pytest.approx(ref, rel=1e-12)
+
+
+def test_entropy_matches_library_and_alt_form():
+    rng = np.random.default_rng(5)
+    for s in (0.5, 2.0, 8.0, 40.0):
+        for T in (1.0, 0.5, 1.5):
+            row = (rng.standard_normal(4096) * s).astype(np.float32)
+            r = oracle.row_stats(row, T=T, sample=False)
+            p = scipy.special.softmax(row.astype(np.float64) / T)
+            # -p log p of a probability next to 1 carries an absolute rounding error of a
+            # few ulp(1) in either evaluation, hence the absolute floor
+            assert r["entropy"] == pytest.approx(scipy.stats.entropy(p), rel=1e-10, abs=1e-15)
+            assert r["lse"] == pytest.approx(scipy.special.logsumexp(row.astype(np.float64) / T), rel=1e-13)
+            if r["entropy"] > 1e-6:
+                assert r["entropy_alt"] == pytest.approx(r["entropy"], rel=1e-9)
+            assert 0.0 <= r["entropy"] <= math.log(4096) + 1e-12
+
+
+def test_entropy_near_one_hot_alt_form_is_accurate():
+    # one entry 30 above the rest: H = r (1 + 30) - ... with r = (V-1) e^-30; the split
+    # form keeps full relative accuracy where log(1 + r) in one sum would lose it
+    V = 1024
+    row = np.zeros(V, np.float32)
+    row[17] = 30.0
+    r = oracle.row_stats(row, sample=False)
+    rr = (V - 1) * math.exp(-30.0)
+    ref = math.log1p(rr) + 30.0 * rr / (1.0 + rr)
+    assert r["entropy_alt"] == pytest.approx(ref, rel=1e-12)
+    assert r["entropy"] == pytest.approx(ref, rel=1e-6)
+
+
+def test_entropy_increases_with_temperature():
+    rng = np.random.default_rng(6)
+    row = (rng.standard_normal(512) * 3).astype(np.float32)
+    Hs = [oracle.row_stats(row, T=T, sample=False)["entropy"] for T in (0.2, 0.5, 1.0, 2.0, 5.0)]
+    assert all(a < b for a, b in zip(Hs, Hs[1:]))
+
+
+def test_bf16_input_path():
+    rng = np.random.default_rng(7)
+    f = (rng.standard_normal(300) * 4).astype(np.float32)
+    bits = (f.view(np.uint32) >> 16).astype(np.uint16)          # truncation to bf16
+    widened = (bits.astype(np.uint32) << 16).view(np.float32)
+    a = oracle.row_stats(bits, T=0.8, seed=3, position=2)
+    b = oracle.row_stats(widened, T=0.8, seed=3, position=2)
+    assert a == b
+
+
+def test_argmax_ties_lowest_index():
+    row = np.zeros(10, np.float32)
+    row[[4, 7]] = 2.0
+    assert oracle.row_stats(row, sample=False)["argmax"] == 4
+    assert oracle.row_stats(np.zeros(10, np.float32), sample=False)["argmax"] == 0
+
+
+# ----------------------------------------------------------------------------- sampling
+def test_sample_one_hot_finite_margin():
+    row = np.zeros(64, np.float32)
+    row[40] = 1000.0
+    for pos in range(50):
+        r = oracle.row_stats(row, seed=11, position=pos)
+        assert r["sample"] == 40
+        assert r["score1"] - r["score2"] > 1000.0 - 16.7 - 2.9
+
+
+@pytest.mark.parametrize("T", [1.0, 0.5])
+def test_gumbel_max_samples_softmax(T):
+    x = np.array([0.0, 1.0, -1.0, 2.0, 0.5, -2.0, 1.5, 0.25], np.float32)
+    p = scipy.special.softmax(x.astype(np.float64) / T)
+    counts = np.zeros(8)
+    for pos in range(100):
+        for step in range(200):
+            counts[oracle.row_stats(x, T=T, seed=5, request_id=3, step=step, position=pos)["sample"]] += 1
+    res = scipy.stats.chisquare(counts, p * counts.sum())
+    assert res.pvalue > 1e-4, (counts, p)
+
+
+def test_gumbel_noise_range_and_distribution():
+    g = np.array([oracle.gumbel(1, 2, 3, 4, v) for v in range(20000)])
+    gmax = -math.log(-math.log(1 - 2.0 ** -24))
+    gmin = -math.log(-math.log(2.0 ** -24))
+    assert g.max() <= gmax and g.min() >= gmin
+    assert abs(g.mean() - np.euler_gamma) < 0.03              # Gumbel(0,1) mean
+    assert abs(g.var() - math.pi ** 2 / 6) < 0.08
+
+
+# ----------------------------------------------------------------------------- acceptance
+def _golden():
+    with open(os.path.join(GOLDEN, "acceptance_4x8.json")) as f:
+        return json.load(f)
+
+
+def _support_logits(g):
+    V = g["V"]
+    x = np.full((1, len(g["supports"]), V), NEG_INF, np.float32)
+    for i, sup in enumerate(g["supports"]):
+        x[0, i, sup] = 0.5
+    return x
+
+
+def _params(n, **kw):
+    p = {"temperature": np.ones(n, np.float32), "beta": np.ones(n, np.float32),
+         "tau": np.full(n, 0.5, np.float32), "k": np.full(n, 2, np.int32),
+         "max_steps": np.full(n, 64, np.int32), "min_accept": np.ones(n, np.int32),
+         "step": np.zeros(n, np.int32), "request_id": np.arange(n, dtype=np.uint32),
+         "flags": np.full(n, oracle.ACTIVE, np.uint32)}
+    for k, v in kw.items():
+        p[k] = np.broadcast_to(np.asarray(v, p[k].dtype), (n,)).copy()
+    return p
+
+
+def test_acceptance_hand_worked_4x8():
+    g = _golden()
+    x = _support_logits(g)
+    L = x.shape[1]
+    for case in g["cases"]:
+        p = _params(1, beta=case["beta"], min_accept=case["min_accept"])
+        out = oracle.denoise_step(x, p, seed=1, canvas=np.zeros((1, L)),
+                                  prev_argmax=np.full((1, L), -1), stable_count=np.zeros(1))
+        ln2 = math.log(2)
+        assert out["entropy"][0] == pytest.approx([e * ln2 for e in g["entropy_in_ln2"]], abs=1e-15)
+        assert list(out["argmax"][0]) == g["argmax"]
+        assert out["mean_entropy"][0] == pytest.approx(g["mean_entropy_in_ln2"] * ln2, rel=1e-14)
+        assert sorted(np.nonzero(out["accept_mask"][0])[0].tolist()) == case["accepted"], case
+        assert out["n_accept"][0] == len(case["accepted"])
+        # accepted positions keep their sample; samples lie in the support
+        for i in range(L):
+            assert out["sample"][0, i] in g["supports"][i]
+            if out["accept_mask"][0, i]:
+                assert out["canvas"][0, i] == out["sample"][0, i]
+
+
+def test_acceptance_entropy_only_cases():
+    for case in _golden()["entropy_only_cases"]:
+        r = oracle.accept(case["H"], case["beta"], case["min_accept"])
+        assert r["order"][: r["n_accept"]].tolist() == case["accepted_in_order"], case
+        assert r["mask"].sum() == len(case["accepted_in_order"])
+
+
+def test_acceptance_brute_force():
+    """For L <= 12: the accepted count is the largest size of any subset whose entropies
+    sum to <= beta, and the accepted set is the (H, index)-smallest subset of that size.
+    Entropies are multiples of 1/16 so every sum is exact."""
+    rng = np.random.default_rng(8)
+    for trial in range(300):
+        L = int(rng.integers(1, 13))
+        H = rng.integers(0, 48, L) / 16.0
+        if trial % 3 == 0:
+            H[rng.integers(0, L, L // 2)] = H[0]            # ties
+        beta = float(rng.integers(-2, 80)) / 16.0 + (0.0 if trial % 2 else 1.0 / 32)
+        best = 0
+        for m in range(L, 0, -1):
+            if any(sum(H[list(S)]) <= beta for S in itertools.combinations(range(L), m)):
+                best = m
+                break
+        r = oracle.accept(H, beta, min_accept=0)
+        assert r["n_accept"] == best, (H, beta)
+        keys = sorted((H[i], i) for i in range(L))
+        assert sorted(np.nonzero(r["mask"])[0].tolist()) == sorted(i for _, i in keys[:best])
+        r1 = oracle.accept(H, beta, min_accept=1)
+        assert r1["n_accept"] == max(best, 1)
+
+
+def test_acceptance_invariants():
+    rng = np.random.default_rng(9)
+    for _ in range(50):
+        H = rng.exponential(1.0, 64)
+        prev = -1
+        for beta in np.linspace(0, 80, 41):
+            r = oracle.accept(H, beta, 1)
+            assert r["n_accept"] >= prev
+            prev = r["n_accept"]
+            acc, rej = H[r["mask"] == 1], H[r["mask"] == 0]
+            if acc.size and rej.size:
+                assert acc.max() <= rej.min()
+
+
+# ----------------------------------------------------------------------------- full step
+def _random_logits(rng, n, L, V, s=3.0):
+    return (rng.standard_normal((n, L, V)) * rng.uniform(0.5, s, (n, L, 1))).astype(np.float32)
+
+
+def test_step_invariants_and_renoise():
+    rng = np.random.default_rng(10)
+    n, L, V = 3, 20, 50
+    x = _random_logits(rng, n, L, V)
+    p = _params(n, beta=[1.0, 5.0, 30.0], step=[0, 3, 7], request_id=[5, 6, 7])
+    out = oracle.denoise_step(x, p, seed=0xABCDEF0123, canvas=np.zeros((n, L)),
+                              prev_argmax=np.full((n, L), -1), stable_count=np.zeros(n))
+    for c in range(n):
+        for i in range(L):
+            if out["accept_mask"][c, i]:
+                assert out["canvas"][c, i] == out["sample"][c, i]
+            else:
+                assert out["canvas"][c, i] == oracle.random_token(
+                    0xABCDEF0123, p["request_id"][c], p["step"][c], i, oracle.STREAM_RENOISE, V)
+            r = oracle.row_stats(x[c, i], seed=0xABCDEF0123, request_id=int(p["request_id"][c]),
+                                 step=int(p["step"][c]), position=i)
+            assert r["sample"] == out["sample"][c, i] and r["argmax"] == out["argmax"][c, i]
+        acc = out["entropy"][c][out["accept_mask"][c] == 1]
+        rej = out["entropy"][c][out["accept_mask"][c] == 0]
+        if acc.size and rej.size:
+            assert acc.max() <= rej.min()
+    assert out["n_accept"][0] <= out["n_accept"][1] <= out["n_accept"][2]
+    assert (out["prev_argmax"] == out["argmax"]).all()
+
+
+def test_convergence_hand_sequences():
+    rng = np.random.default_rng(11)
+    L, V = 8, 16
+    sharp = np.zeros((1, L, V), np.float32)
+    sharp[0, np.arange(L), rng.integers(0, V, L)] = 40.0     # mean entropy ~ 0
+    flat = _random_logits(rng, 1, L, V, s=0.6)               # mean entropy ~ log V
+    for logits, tau, expect in [(sharp, 0.5, [0, 0, 1]), (flat, 0.5, [0, 0, 0])]:
+        p = _params(1, k=2, tau=tau, max_steps=64)
+        canvas, prev, stable = np.zeros((1, L)), np.full((1, L), -1), np.zeros(1)
+        stables, convs = [], []
+        for step in range(3):
+            p["step"][:] = step
+            out = oracle.denoise_step(logits, p, 1, canvas, prev, stable)
+            canvas, prev, stable = out["canvas"], out["prev_argmax"], out["stable_count"]
+            stables.append(int(stable[0]))
+            convs.append(int(out["converged"][0]))
+        assert stables == [0, 1, 2]
+        assert convs == expect
+    # a change of argmax resets the count
+    p = _params(1, k=2, tau=100.0)
+    out = oracle.denoise_step(sharp, p, 1, np.zeros((1, L)), np.full((1, L), -1), np.zeros(1))
+    prev = out["prev_argmax"].copy()
+    prev[0, 3] = (prev[0, 3] + 1) % V
+    out2 = oracle.denoise_step(sharp, p, 1, out["canvas"], prev, np.array([5]))
+    assert out2["stable_count"][0] == 0 and out2["converged"][0] == 0
+    # the step cap converges regardless: S = 1 at step 0, S = 4 at step 3
+    for S, step in [(1, 0), (4, 3)]:
+        q = _params(1, max_steps=S, step=step, tau=0.0)
+        o = oracle.denoise_step(flat, q, 1, np.zeros((1, L)), np.full((1, L), -1), np.zeros(1))
+        assert o["converged"][0] == 1
+    q = _params(1, max_steps=5, step=3, tau=0.0)
+    o = oracle.denoise_step(flat, q, 1, np.zeros((1, L)), np.full((1, L), -1), np.zeros(1))
+    assert o["converged"][0] == 0
+
+
+def test_read_only_and_inactive():
+    rng = np.random.default_rng(12)
+    n, L, V = 3, 6, 32
+    x = _random_logits(rng, n, L, V)
+    flags = [oracle.ACTIVE | oracle.READ_ONLY, 0, oracle.ACTIVE]
+    p = _params(n, max_steps=[1, 8, 8])
+    p["flags"] = np.array(flags, np.uint32)
+    canvas0 = rng.integers(0, V, (n, L)).astype(np.int32)
+    out = oracle.denoise_step(x, p, 2, canvas0, np.full((n, L), -1), np.zeros(n))
+    assert (out["canvas"][0] == canvas0[0]).all() and out["accept_mask"][0].sum() == 0
+    assert out["converged"][0] == 1 and (out["sample"][0] == -1).all()
+    assert (out["canvas"][1] == canvas0[1]).all() and (out["prev_argmax"][1] == -1).all()
+    assert out["entropy"][1].sum() == 0 and out["converged"][1] == 0
+
+
+def test_canvas_init_tokens():
+    n, L, V = 2, 300, 7
+    p = _params(n, step=[0, 0])
+    p["flags"] = np.array([oracle.ACTIVE, 0], np.uint32)
+    c = oracle.canvas_init(n, L, V, p, seed=77)
+    assert c[0].min() >= 0 and c[0].max() < V and (c[1] == 0).all()
+    assert scipy.stats.chisquare(np.bincount(c[0], minlength=V)).pvalue > 1e-4
+
+
+# ----------------------------------------------------------------------------- self-conditioning
+def _bf16(a):
+    a = np.asarray(a, np.float32)
+    return ((a.view(np.uint32) + 0x8000) >> 16).astype(np.uint16)   # round-half-up is fine here
+
+
+def _widen(b):
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def test_pe_one_hot_uniform_linear():
+    rng = np.random.default_rng(13)
+    V, d = 40, 12
+    E = _bf16(rng.standard_normal((V, d)) * 0.02)
+    Ef = _widen(E)
+    P = np.zeros((3, V))
+    P[0, 17] = 1.0
+    P[1, :] = 1.0 / V
+    P[2] = rng.dirichlet(np.ones(V))
+    pe = oracle.pe_from_probs(P, E)
+    assert (pe[0] == Ef[17]).all()
+    np.testing.assert_allclose(pe[1], Ef.mean(axis=0), rtol=1e-12, atol=1e-18)
+    Q = rng.dirichlet(np.ones(V), 2)
+    a, b = 0.3, 0.7
+    lhs = oracle.pe_from_probs(a * Q[:1] + b * Q[1:], E)
+    rhs = a * oracle.pe_from_probs(Q[:1], E) + b * oracle.pe_from_probs(Q[1:], E)
+    np.testing.assert_allclose(lhs, rhs, rtol=1e-12, atol=1e-18)
+    np.testing.assert_allclose(pe[2], P[2] @ Ef, rtol=1e-12, atol=1e-18)   # library matmul
+
+
+def test_gelu_tanh_properties():
+    assert oracle.gelu_tanh(0.0) == 0.0
+    for x in np.linspace(-6, 6, 121):
+        exact = 0.5 * x * (1.0 + scipy.special.erf(x / math.sqrt(2.0)))   # x * Phi(x)
+        assert abs(oracle.gelu_tanh(float(x)) - exact) < 1e-3
+    assert oracle.gelu_tanh(30.0) == pytest.approx(30.0)
+    assert abs(oracle.gelu_tanh(-30.0)) < 1e-12
+    assert oracle.gelu_tanh(1.0) > 0.8 and oracle.gelu_tanh(-1.0) < 0
+
+
+def test_gated_mlp_closed_forms():
+    rng = np.random.default_rng(14)
+    d, h = 6, 10
+    pe = rng.standard_normal((4, d))
+    Z = np.zeros((h, d), np.uint16)
+    Wd = _bf16(rng.standard_normal((d, h)))
+    assert (oracle.gated_mlp(pe, Z, _bf16(rng.standard_normal((h, d))), Wd) == 0).all()
+    # d = h = 1: delta = wd * gelu(wg z) * (wu z)
+    wg, wu, wd = _bf16([[0.75]]), _bf16([[-1.5]]), _bf16([[2.0]])
+    for z in (-2.0, 0.5, 3.0):
+        got = oracle.gated_mlp(np.array([[z]]), wg, wu, wd)[0, 0]
+        ref = 2.0 * oracle.gelu_tanh(0.75 * z) * (-1.5 * z)
+        assert got == pytest.approx(ref, rel=1e-14)
+    # the general case against library matmuls in fp64
+    Wg, Wu = _bf16(rng.standard_normal((h, d)) * 0.3), _bf16(rng.standard_normal((h, d)) * 0.3)
+    g = pe @ _widen(Wg).T
+    u = pe @ _widen(Wu).T
+    gelu = 0.5 * g * (1.0 + scipy.special.erf(g / math.sqrt(2.0)))
+    ref = (gelu * u) @ _widen(Wd).T
+    got = oracle.gated_mlp(pe, Wg, Wu, Wd)
+    np.testing.assert_allclose(got, ref, rtol=5e-3, atol=1e-3 * np.abs(ref).max())
+
+
+def test_probs_from_logits_is_softmax():
+    rng = np.random.default_rng(15)
+    x = (rng.standard_normal((3, 200)) * 5).astype(np.float32)
+    T = np.array([1.0, 0.4, 1.3])
+    P = oracle.probs_from_logits(x, T)
+    np.testing.assert_allclose(P, scipy.special.softmax(x.astype(np.float64) / T[:, None], axis=1),
+                               rtol=1e-12, atol=1e-300)

@@ -1,0 +1,415 @@
+"""Benchmark of the entropy-bounded denoising step on GB300.
+
+One step = the whole hot path over one batch: the denoise step (per-position softmax /
+entropy / argmax / Gumbel-max sample, entropy-bound acceptance, renoise, convergence) and the
+self-conditioning feedback (P.E on tensor cores with the softmax fused into the operand load,
+then the gated MLP).  Default workload: 8 canvases x 256 positions, V = 262144, d = 4096,
+h = 16384, bf16 logits (the batched full-vocabulary step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload batched|sweep|ragged|single]
+    python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs an independent replica on its
+own GPU (the path has no exchange step), the timed region is bracketed by barriers and the
+slowest rank's time counts.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "canvas positions/s per denoise step (V=262144, d=4096); % of HBM/TC roofline"
+UNIT = "positions/s"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"],
+                "bf16_tflops_sustained": pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _workload_arith(wl, n_sc_rows, n_read_rows):
+    """Algorithmic bytes and tensor-core FLOPs of one step."""
+    N = wl.n * wl.L
+    logits_b = 2 * n_read_rows * wl.V
+    e_b = 2 * wl.V * wl.d
+    w_b = 6 * wl.d * wl.h
+    out_b = 17 * N + 2 * N * wl.d
+    pe_flops = 2.0 * n_sc_rows * wl.V * wl.d
+    mlp_flops = 6.0 * n_sc_rows * wl.d * wl.h
+    return {"bytes": logits_b + e_b + w_b + out_b, "logits_bytes": logits_b, "pe_flops": pe_flops,
+            "mlp_flops": mlp_flops, "tc_flops": pe_flops + mlp_flops}
+
+
+def _profile_traffic(kernel_tag: str):
+    """Per-launch DRAM bytes recorded from an ncu capture in profiles/, if the kernel source
+    it was taken on is unchanged (else None)."""
+    src = os.path.join(ROOT, "entropy_bounded_denoising_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(src)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(src, f), "rb") as fh:
+                h.update(fh.read())
+    digest = h.hexdigest()[:16]
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    s = re.search(r"csrc_sha256_16:\s*([0-9a-f]{16})", txt)
+    if m and s and s.group(1) == digest:
+        return float(m.group(1))
+    return None
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def _oracle_sample(wl, x_canvas_host, weights_host, p, n_sc_rows: int, threads: int):
+    """Time the fp64 oracle on one canvas (denoise) and n_sc_rows rows (self-conditioning);
+    returns seconds per canvas position."""
+    import oracle
+    L = wl.L
+    p1 = {k: v[:1].copy() for k, v in p.items()}
+    t0 = time.perf_counter()
+    oracle.denoise_step(x_canvas_host[None], p1, 7, np.zeros((1, L), np.int32), np.full((1, L), -1, np.int32),
+                        np.zeros(1, np.int32), n_threads=threads)
+    t_dn = time.perf_counter() - t0
+    t_sc = 0.0
+    if n_sc_rows:
+        E, Wg, Wu, Wd = weights_host
+        rows = x_canvas_host[:n_sc_rows]
+        t0 = time.perf_counter()
+        oracle.self_cond_rows(rows, np.full(n_sc_rows, float(p["temperature"][0])), E, Wg, Wu, Wd, V=wl.V,
+                              n_threads=threads)
+        t_sc = time.perf_counter() - t0
+    per_pos = t_dn / L + (t_sc / n_sc_rows if n_sc_rows else 0.0)
+    return per_pos, t_dn, t_sc
+
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores, as the comparison arm."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import oracle
+    from entropy_bounded_denoising_gb300 import synth
+    import torch
+    wl = synth.WORKLOADS[args.workload]
+    threads = oracle.max_threads()
+    p = synth.canvas_params(wl, step=1)
+    x = synth.logits(1, wl.L, wl.V, seed=wl.seed, step=1, scale=wl.scale, spike_frac=wl.spike_frac,
+                     dtype=wl.dtype, canvases=[0])
+    xh = synth.host_logits(x)[0]
+    E, Wg, Wu, Wd = synth.weights(wl.V, wl.d, wl.h, seed=wl.seed)
+    wh = tuple(synth.bf16_bits(t) for t in (E, Wg, Wu, Wd))
+    n_sc = 2
+    for _ in range(args.warmup):
+        _oracle_sample(wl, xh, wh, p, n_sc, threads)
+    times = []
+    for _ in range(args.steps):
+        per_pos, _, _ = _oracle_sample(wl, xh, wh, p, n_sc, threads)
+        times.append(per_pos)
+    per_pos = float(np.mean(times))
+    value = 1.0 / per_pos
+    sample = (f"per step: denoise oracle on 1 canvas ({wl.L} positions x V={wl.V}) plus "
+              f"self-conditioning on {n_sc} rows, extrapolated per position")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_pos * wl.n * wl.L * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": _config(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(wl):
+    return {"workload": (f"{wl.name}: {wl.n} canvases x {wl.L} positions, V={wl.V}, d={wl.d}, h={wl.h}, "
+                         f"{wl.dtype} logits"),
+            "n_canvas": wl.n, "L": wl.L, "V": wl.V, "d": wl.d, "h": wl.h,
+            "l2": "no flush: each step reads inputs larger than L2 (logits + embedding table)",
+            "parallelism": "replicas (canvases independent, no exchange step)"}
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_ours(args):
+    import torch
+    import entropy_bounded_denoising_gb300 as dg
+    from entropy_bounded_denoising_gb300 import synth, build
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        build.build()
+    if ws > 1:
+        tdist.barrier()
+    dg.load()
+
+    def barrier():
+        if ws > 1:
+            tdist.barrier()
+
+    wl = synth.WORKLOADS[args.workload]
+    n, L, V, d, h = wl.n, wl.L, wl.V, wl.d, wl.h
+    p = synth.canvas_params(wl, step=1)
+    if wl.name in ("sweep", "single", "profile"):
+        p["flags"] |= dg.DG_SELF_COND
+    x = synth.logits(n, L, V, seed=wl.seed + 1000 * rank, step=1, scale=wl.scale, spike_frac=wl.spike_frac,
+                     dtype=wl.dtype, device=dev)
+    E, Wg, Wu, Wd = synth.weights(V, d, h, seed=wl.seed, device=dev)
+    params = dg.params_tensor(p, dev)
+
+    def z(shape, dt, v=0):
+        return torch.full(shape, v, dtype=dt, device=dev)
+
+    canvas, prev, stable = z((n, L), torch.int32), z((n, L), torch.int32, -1), z((n,), torch.int32)
+    acc, am, smp = z((n, L), torch.uint8), z((n, L), torch.int32), z((n, L), torch.int32)
+    ent, lse, conv = z((n, L), torch.float32), z((n, L), torch.float32), z((n,), torch.uint8)
+    delta = torch.empty((n, L, d), dtype=torch.bfloat16, device=dev)
+    wsp = torch.empty(dg.dg_self_cond_workspace_bytes(n, L, d, h), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    seed = 0x5EED0000 + rank
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        dg.dg_denoise_step(x, params, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv, stream=stream)
+        dg.dg_self_cond_prepare(params, conv, n, L, d, h, delta, wsp, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        dg.dg_self_cond_pe(x, lse, params, E, h, wsp, stream=stream)
+        if ev:
+            ev[2].record(stream)
+        dg.dg_self_cond_mlp(n, L, Wg, Wu, Wd, delta, wsp, stream=stream)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    dg.dg_clear_device_status()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    launches0 = dg.dg_launch_count()
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for k in range(args.steps):
+            step(evs[k])
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    launches = dg.dg_launch_count() - launches0
+    elapsed_ms = start.elapsed_time(end)
+    status = dg.dg_get_device_status()
+    if status:
+        raise RuntimeError(f"device status {status:#x} after the timed region")
+    n_conv = int(conv.sum().item())
+    flags = p["flags"]
+    active = (flags & dg.DG_ACTIVE) != 0
+    sc_on = active & ((flags & dg.DG_SELF_COND) != 0) & ((flags & dg.DG_READ_ONLY) == 0)
+    conv_h = conv.cpu().numpy().astype(bool)
+    n_sc_rows = int((sc_on & ~conv_h).sum()) * L
+    n_read_rows = int(active.sum()) * L
+    positions = n_read_rows
+    if ws > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_step = elapsed_ms / args.steps
+    value = positions * ws * args.steps / (elapsed_ms / 1e3)
+
+    t_dn = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    t_pe = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    t_mlp = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
+    ar = _workload_arith(wl, n_sc_rows, n_read_rows)
+    pk = _peaks()
+    peak_tc = pk["bf16_tflops_sustained"]
+    pe_tflops = ar["pe_flops"] / (t_pe * 1e-3) / 1e12 if t_pe > 0 else 0.0
+    t_roof = max(ar["bytes"] / (pk["hbm_gbs"] * 1e9), ar["tc_flops"] / (peak_tc * 1e12))
+    traffic = _profile_traffic("pe_gemm_batched")
+
+    # ---------------------------------------------------------------- e2e: host buffers
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        xh.copy_(x)
+        out_canvas = torch.empty((n, L), dtype=torch.int32, pin_memory=True)
+        out_conv = torch.empty((n,), dtype=torch.uint8, pin_memory=True)
+        out_delta = torch.empty((n, L, d), dtype=torch.bfloat16, pin_memory=True)
+        xdev = torch.empty_like(x)
+        h2d = xh.numel() * xh.element_size()
+        d2h = (out_canvas.numel() * 4 + out_conv.numel() + out_delta.numel() * 2)
+
+        def e2e_step():
+            xdev.copy_(xh, non_blocking=True)
+            dg.dg_denoise_step(xdev, params, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv,
+                               stream=stream)
+            dg.dg_self_cond_logits(xdev, lse, params, conv, E, Wg, Wu, Wd, delta, wsp, stream=stream)
+            out_canvas.copy_(canvas, non_blocking=True)
+            out_conv.copy_(conv, non_blocking=True)
+            out_delta.copy_(delta, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e2.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms2 = s2.elapsed_time(e2)
+        if ws > 1:
+            t = torch.tensor([ms2], device=dev)
+            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+            ms2 = float(t.item())
+        e2e = {"value": positions * ws * args.steps / (ms2 / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms2 / args.steps}
+
+    # ---------------------------------------------------------------- CPU baseline (oracle)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        threads = oracle.max_threads()
+        xh0 = synth.host_logits(x[0])
+        wh = tuple(synth.bf16_bits(t) for t in (E, Wg, Wu, Wd))
+        n_sc = 4
+        per_pos, t_dn_cpu, t_sc_cpu = _oracle_sample(wl, xh0, wh, p, n_sc, threads)
+        cpu = {"value": 1.0 / per_pos, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": (f"denoise oracle on canvas 0 ({L} positions x V={V}, {t_dn_cpu:.1f} s) plus "
+                          f"self-conditioning on {n_sc} rows ({t_sc_cpu:.1f} s), extrapolated per position")}
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(wl),
+        "roofline": {"bound": "tensor", "achieved": pe_tflops, "peak": peak_tc, "unit": "TFLOP/s",
+                     "frac": pe_tflops / peak_tc, "traffic": traffic,
+                     "kernel": "P.E contraction (k_gemm softmax-A, N-major B) + split-K fix-up",
+                     "peak_source": f"{pk['source']} sustained bf16"},
+        "step_roofline": {"t_roof_ms": t_roof * 1e3, "frac": (t_roof * 1e3) / ms_step,
+                          "alg_bytes": ar["bytes"], "tc_flops": ar["tc_flops"],
+                          "hbm_peak_gbs": pk["hbm_gbs"], "tc_peak_tflops": peak_tc},
+        "kernels_ms": {"denoise_and_prepare": t_dn, "pe": t_pe, "mlp": t_mlp,
+                       "denoise_hbm_frac": (ar["logits_bytes"] / (t_dn * 1e-3)) / (pk["hbm_gbs"] * 1e9),
+                       "mlp_tflops": ar["mlp_flops"] / (t_mlp * 1e-3) / 1e12 if t_mlp > 0 else 0.0},
+        "steps_per_s": 1e3 / ms_step, "self_cond_rows": n_sc_rows, "converged_canvases": n_conv,
+        "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        tdist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="batched", choices=["batched", "sweep", "ragged", "single", "profile"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,323 @@
+"""ctypes binding of libdg (include/dg.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and forwards torch tensors
+as raw device pointers on the current (or given) CUDA stream.  All arithmetic runs in the
+library's kernels; there is no fallback.  Loading fails loudly when the library has not been
+built (run ``entropy_bounded_denoising_gb300.build.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import struct
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+DG_OK, DG_ERR_INVALID_ARG, DG_ERR_ALIGNMENT, DG_ERR_WORKSPACE, DG_ERR_UNSUPPORTED, DG_ERR_CUDA = 0, -1, -2, -3, -4, -5
+DG_BF16, DG_FP32 = 0, 1
+DG_ACTIVE, DG_READ_ONLY, DG_SELF_COND = 1, 2, 4
+DG_DEV_NAN_INF_ROW, DG_DEV_EMPTY_ROW, DG_DEV_TIMEOUT, DG_DEV_BAD_PARAM = 1, 2, 4, 8
+
+PARAM_FIELDS = ("temperature", "beta", "tau", "k", "max_steps", "min_accept", "step",
+                "request_id", "flags")
+_PARAM_FMT = "<fffiiiiII"
+PARAM_BYTES = struct.calcsize(_PARAM_FMT)   # 36, sizeof(dg_canvas_params)
+
+_lib = None
+
+
+class DGError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {status_string(code)} ({code})")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load libdg.so (built in-tree).  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"libdg.so not found at {path}: build it with "
+                           "entropy_bounded_denoising_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, u32, u64, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32,
+                                  ctypes.c_uint64, ctypes.c_size_t)
+    st = ctypes.c_int
+    sig = {
+        "dg_denoise_workspace_bytes": (sz, [i64, i32, i64, ctypes.c_int]),
+        "dg_denoise_step": (st, [P, ctypes.c_int, i64, i64, i32, i64, P, u64] + [P] * 11 + [P, sz, P]),
+        "dg_accept_from_entropy": (st, [P, P, P, i64, i32, i64, P, u64] + [P] * 7 + [P]),
+        "dg_canvas_init": (st, [P, i64, i32, i64, P, u64, P]),
+        "dg_advance_params": (st, [P, P, i64, P]),
+        "dg_self_cond_workspace_bytes": (sz, [i64, i32, i32, i32]),
+        "dg_self_cond_logits": (st, [P, ctypes.c_int, i64, P, P, P, i64, i32, i64, i32, i32,
+                                     P, P, P, P, P, P, sz, P]),
+        "dg_self_cond_prepare": (st, [P, P, i64, i32, i32, i32, P, P, sz, P]),
+        "dg_self_cond_pe": (st, [P, ctypes.c_int, i64, P, P, i64, i32, i64, i32, i32, P, P, sz, P]),
+        "dg_self_cond_mlp": (st, [i64, i32, i32, i32, P, P, P, P, P, sz, P]),
+        "dg_self_cond_probs_workspace_bytes": (sz, [i64, i32, i32]),
+        "dg_self_cond_probs": (st, [P, i64, i64, i64, i32, i32, P, P, P, P, P, P, sz, P]),
+        "dg_gemm_workspace_bytes": (sz, [i64, i64]),
+        "dg_gemm_bf16": (st, [P, i64, P, i64, ctypes.c_int, P, i64, i64, i64, i64, P, sz, P]),
+        "dg_philox_words": (st, [u64, u32, u32, u32, u32, u32, i64, P, P]),
+        "dg_get_device_status": (st, [P, ctypes.POINTER(u32)]),
+        "dg_clear_device_status": (st, [P]),
+        "dg_status_string": (ctypes.c_char_p, [st]),
+        "dg_version": (i32, []),
+        "dg_launch_count": (u64, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def exported_symbols() -> list[str]:
+    lib = load()
+    return [n for n in ("dg_denoise_workspace_bytes", "dg_denoise_step", "dg_accept_from_entropy",
+                        "dg_canvas_init", "dg_advance_params", "dg_self_cond_workspace_bytes",
+                        "dg_self_cond_logits", "dg_self_cond_prepare", "dg_self_cond_pe",
+                        "dg_self_cond_mlp", "dg_self_cond_probs_workspace_bytes",
+                        "dg_self_cond_probs", "dg_gemm_workspace_bytes", "dg_gemm_bf16",
+                        "dg_philox_words", "dg_get_device_status", "dg_clear_device_status",
+                        "dg_status_string", "dg_version", "dg_launch_count") if hasattr(lib, n)]
+
+
+# ------------------------------------------------------------------ marshalling helpers
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("device tensor expected")
+    return t.data_ptr()
+
+
+def _s(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(fn: str, code: int) -> None:
+    if code != DG_OK:
+        raise DGError(fn, code)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return DG_BF16
+    if t.dtype == torch.float32:
+        return DG_FP32
+    raise TypeError("logits must be bfloat16 or float32")
+
+
+def status_string(code: int) -> str:
+    return load().dg_status_string(int(code)).decode()
+
+
+def version() -> int:
+    return int(load().dg_version())
+
+
+def dg_launch_count() -> int:
+    return int(load().dg_launch_count())
+
+
+def pack_params(p: dict) -> bytes:
+    """Pack per-canvas parameter arrays into dg_canvas_params records (host bytes)."""
+    n = len(p["flags"])
+    return b"".join(struct.pack(_PARAM_FMT, *(np.asarray(p[f])[i].item() for f in PARAM_FIELDS))
+                    for i in range(n))
+
+
+def params_tensor(p: dict, device="cuda") -> torch.Tensor:
+    """Per-canvas parameters as a device uint8 tensor [n * 36]."""
+    raw = np.frombuffer(pack_params(p), dtype=np.uint8).copy()
+    return torch.from_numpy(raw).to(device)
+
+
+def unpack_params(t: torch.Tensor) -> dict:
+    raw = t.detach().cpu().numpy().tobytes()
+    n = len(raw) // PARAM_BYTES
+    rows = [struct.unpack_from(_PARAM_FMT, raw, i * PARAM_BYTES) for i in range(n)]
+    return {f: np.array([r[j] for r in rows]) for j, f in enumerate(PARAM_FIELDS)}
+
+
+# ------------------------------------------------------------------ entry points
+def dg_denoise_workspace_bytes(n_canvas: int, L: int, V: int, dtype: int = DG_BF16) -> int:
+    return int(load().dg_denoise_workspace_bytes(n_canvas, L, V, dtype))
+
+
+def dg_denoise_step(logits, params, seed, canvas, prev_argmax, stable_count, accept_mask, argmax,
+                    sample, entropy, lse, converged, mean_entropy=None, n_accept=None,
+                    workspace=None, *, n_canvas=None, L=None, V=None, ld=None, stream=None,
+                    check=True) -> int:
+    n, Lx, ldx = logits.shape if logits.dim() == 3 else (n_canvas, L, ld)
+    n_canvas = n if n_canvas is None else n_canvas
+    L = Lx if L is None else L
+    ld = ldx if ld is None else ld
+    V = ld if V is None else V
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().dg_denoise_step(_p(logits), _dtype_code(logits), ld, n_canvas, L, V, _p(params),
+                                int(seed) & 0xFFFFFFFFFFFFFFFF, _p(canvas), _p(prev_argmax),
+                                _p(stable_count), _p(accept_mask), _p(argmax), _p(sample), _p(entropy),
+                                _p(lse), _p(converged), _p(mean_entropy), _p(n_accept),
+                                _p(workspace), ws_bytes, _s(stream))
+    if check:
+        _check("dg_denoise_step", rc)
+    return rc
+
+
+def dg_accept_from_entropy(entropy, sample, argmax, n_canvas, L, V, params, seed, canvas,
+                           prev_argmax, stable_count, accept_mask, converged, mean_entropy=None,
+                           n_accept=None, stream=None, check=True) -> int:
+    rc = load().dg_accept_from_entropy(_p(entropy), _p(sample), _p(argmax), n_canvas, L, V,
+                                       _p(params), int(seed) & 0xFFFFFFFFFFFFFFFF, _p(canvas),
+                                       _p(prev_argmax), _p(stable_count), _p(accept_mask),
+                                       _p(converged), _p(mean_entropy), _p(n_accept), _s(stream))
+    if check:
+        _check("dg_accept_from_entropy", rc)
+    return rc
+
+
+def dg_canvas_init(canvas, n_canvas, L, V, params, seed, stream=None, check=True) -> int:
+    rc = load().dg_canvas_init(_p(canvas), n_canvas, L, V, _p(params),
+                               int(seed) & 0xFFFFFFFFFFFFFFFF, _s(stream))
+    if check:
+        _check("dg_canvas_init", rc)
+    return rc
+
+
+def dg_advance_params(params, converged, n_canvas, stream=None, check=True) -> int:
+    rc = load().dg_advance_params(_p(params), _p(converged), n_canvas, _s(stream))
+    if check:
+        _check("dg_advance_params", rc)
+    return rc
+
+
+def dg_self_cond_workspace_bytes(n_canvas: int, L: int, d: int, h: int) -> int:
+    return int(load().dg_self_cond_workspace_bytes(n_canvas, L, d, h))
+
+
+def dg_self_cond_logits(logits, lse, params, converged, E, W_gate, W_up, W_down, delta_emb,
+                        workspace, *, n_canvas=None, L=None, V=None, ld=None, stream=None,
+                        check=True) -> int:
+    n, Lx, ldx = logits.shape if logits.dim() == 3 else (n_canvas, L, ld)
+    n_canvas = n if n_canvas is None else n_canvas
+    L = Lx if L is None else L
+    ld = ldx if ld is None else ld
+    V = ld if V is None else V
+    d = E.shape[1]
+    h = W_gate.shape[0]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = load().dg_self_cond_logits(_p(logits), _dtype_code(logits), ld, _p(lse), _p(params),
+                                    _p(converged), n_canvas, L, V, d, h, _p(E), _p(W_gate),
+                                    _p(W_up), _p(W_down), _p(delta_emb), _p(workspace), ws_bytes,
+                                    _s(stream))
+    if check:
+        _check("dg_self_cond_logits", rc)
+    return rc
+
+
+def dg_self_cond_prepare(params, converged, n_canvas, L, d, h, delta_emb, workspace, stream=None,
+                         check=True) -> int:
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = load().dg_self_cond_prepare(_p(params), _p(converged), n_canvas, L, d, h, _p(delta_emb),
+                                     _p(workspace), ws_bytes, _s(stream))
+    if check:
+        _check("dg_self_cond_prepare", rc)
+    return rc
+
+
+def dg_self_cond_pe(logits, lse, params, E, h, workspace, *, n_canvas=None, L=None, V=None, ld=None,
+                    stream=None, check=True) -> int:
+    n, Lx, ldx = logits.shape if logits.dim() == 3 else (n_canvas, L, ld)
+    n_canvas = n if n_canvas is None else n_canvas
+    L = Lx if L is None else L
+    ld = ldx if ld is None else ld
+    V = ld if V is None else V
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = load().dg_self_cond_pe(_p(logits), _dtype_code(logits), ld, _p(lse), _p(params), n_canvas, L, V,
+                                E.shape[1], h, _p(E), _p(workspace), ws_bytes, _s(stream))
+    if check:
+        _check("dg_self_cond_pe", rc)
+    return rc
+
+
+def dg_self_cond_mlp(n_canvas, L, W_gate, W_up, W_down, delta_emb, workspace, stream=None,
+                     check=True) -> int:
+    d = W_gate.shape[1]
+    h = W_gate.shape[0]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = load().dg_self_cond_mlp(n_canvas, L, d, h, _p(W_gate), _p(W_up), _p(W_down), _p(delta_emb),
+                                 _p(workspace), ws_bytes, _s(stream))
+    if check:
+        _check("dg_self_cond_mlp", rc)
+    return rc
+
+
+def dg_self_cond_probs_workspace_bytes(n_rows: int, d: int, h: int) -> int:
+    return int(load().dg_self_cond_probs_workspace_bytes(n_rows, d, h))
+
+
+def dg_self_cond_probs(P, E, W_gate, W_up, W_down, delta_emb, workspace, *, V=None, stream=None,
+                       check=True) -> int:
+    n_rows, ld = P.shape
+    V = ld if V is None else V
+    d = E.shape[1]
+    h = W_gate.shape[0]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = load().dg_self_cond_probs(_p(P), ld, n_rows, V, d, h, _p(E), _p(W_gate), _p(W_up),
+                                   _p(W_down), _p(delta_emb), _p(workspace), ws_bytes, _s(stream))
+    if check:
+        _check("dg_self_cond_probs", rc)
+    return rc
+
+
+def dg_gemm_workspace_bytes(M: int, N: int) -> int:
+    return int(load().dg_gemm_workspace_bytes(M, N))
+
+
+def dg_gemm_bf16(A, B, C, b_mn_major: bool, workspace, *, M=None, N=None, K=None, stream=None,
+                 check=True) -> int:
+    M = A.shape[0] if M is None else M
+    K = A.shape[1] if K is None else K
+    N = (B.shape[1] if b_mn_major else B.shape[0]) if N is None else N
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().dg_gemm_bf16(_p(A), A.stride(0), _p(B), B.stride(0), int(bool(b_mn_major)), _p(C),
+                             C.stride(0), M, N, K, _p(workspace), ws_bytes, _s(stream))
+    if check:
+        _check("dg_gemm_bf16", rc)
+    return rc
+
+
+def dg_philox_words(seed, request_id, step, position, stream_id, block0, n_blocks, out,
+                    stream=None, check=True) -> int:
+    rc = load().dg_philox_words(int(seed) & 0xFFFFFFFFFFFFFFFF, request_id, step, position,
+                                stream_id, block0, n_blocks, _p(out), _s(stream))
+    if check:
+        _check("dg_philox_words", rc)
+    return rc
+
+
+def dg_get_device_status(stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    _check("dg_get_device_status", load().dg_get_device_status(_s(stream), ctypes.byref(v)))
+    return int(v.value)
+
+
+def dg_clear_device_status(stream=None) -> None:
+    _check("dg_clear_device_status", load().dg_clear_device_status(_s(stream)))

@@ -1,0 +1,220 @@
+// dg_common.cuh -- device helpers shared by the libdg kernels (sm_103a only).
+//
+// Philox-4x32-10 follows Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
+// 1, 2, 3" (SC'11).  The PTX wrappers cover mbarriers, bulk / tensor copies (TMA) and the
+// fifth-generation tensor core (tcgen05) with its tensor memory (TMEM).  Every wait is
+// bounded: when a bound expires the caller sets DG_DEV_TIMEOUT in the status word and
+// unwinds instead of spinning forever.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dg.h"
+
+#define DG_DEVINL __device__ __forceinline__
+
+// ------------------------------------------------------------------ status word
+namespace dg {
+
+DG_DEVINL void raise_status(unsigned* status, unsigned bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// ------------------------------------------------------------------ Philox-4x32-10
+struct u4 { uint32_t x, y, z, w; };
+
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u;
+constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;
+constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
+
+// Random-number streams (counter word 3, low byte).
+constexpr uint32_t kStreamGumbel = 0u;
+constexpr uint32_t kStreamRenoise = 1u;
+constexpr uint32_t kStreamInit = 2u;
+
+// Ten rounds: each multiplies the even words, swaps halves and mixes in the round key,
+// the key advancing by the Weyl constants between rounds.
+DG_DEVINL u4 philox10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = (uint64_t)kPhiloxM0 * c0;
+        const uint64_t p1 = (uint64_t)kPhiloxM1 * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ (k0 + (uint32_t)r * kPhiloxW0);
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ (k1 + (uint32_t)r * kPhiloxW1);
+        c1 = (uint32_t)p1;
+        c3 = (uint32_t)p0;
+        c0 = n0;
+        c2 = n2;
+    }
+    return u4{c0, c1, c2, c3};
+}
+
+// Counter word 3: stream id in the low byte, bits 32..55 of the seed above it.
+DG_DEVINL uint32_t ctr_word3(uint64_t seed, uint32_t stream) {
+    return stream | ((uint32_t)((seed >> 32) & 0xFFFFFFu) << 8);
+}
+
+// u = (floor(w / 2^9) + 1/2) / 2^23, exact in fp32, 2^-24 <= u <= 1 - 2^-24.
+DG_DEVINL float uniform_from_word(uint32_t w) {
+    return __uint2float_rn((w >> 9) * 2u + 1u) * 5.9604644775390625e-8f;  // (2k + 1) / 2^24
+}
+
+// Uniform token in [0, V): floor((w0 << 32 | w1) * V / 2^64).
+DG_DEVINL uint32_t token_from_words(uint32_t w0, uint32_t w1, uint32_t V) {
+    const uint64_t x = ((uint64_t)w0 << 32) | w1;
+    return (uint32_t)__umul64hi(x, (uint64_t)V);
+}
+
+DG_DEVINL uint32_t random_token(uint64_t seed, uint32_t request_id, uint32_t step, uint32_t position,
+                                uint32_t stream, uint32_t V) {
+    const u4 w = philox10(0u, position, step, ctr_word3(seed, stream), (uint32_t)seed, request_id);
+    return token_from_words(w.x, w.y, V);
+}
+
+// ------------------------------------------------------------------ bounded waits
+// Roughly 2^22 polls with a ~1 us suspend hint each: a few seconds at most.
+constexpr uint32_t kWaitPolls = 1u << 22;
+
+DG_DEVINL uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+DG_DEVINL void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+DG_DEVINL void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+DG_DEVINL void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+DG_DEVINL void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+DG_DEVINL void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+DG_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(1000u)
+        : "memory");
+    return ok != 0;
+}
+
+// Returns false when the bound expired.
+DG_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitPolls; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// ------------------------------------------------------------------ bulk copies (TMA)
+// Plain bulk copy global -> shared; both addresses 16-byte aligned, bytes % 16 == 0.
+DG_DEVINL void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+DG_DEVINL void tma_load_2d(void* dst, const void* tmap, int32_t c0, int32_t c1, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+DG_DEVINL void tma_load_3d(void* dst, const void* tmap, int32_t c0, int32_t c1, int32_t c2, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+        "%4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+DG_DEVINL void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// ------------------------------------------------------------------ tcgen05 / TMEM
+DG_DEVINL void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {  // whole warp
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+DG_DEVINL void tmem_relinquish() {  // whole warp
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+DG_DEVINL void tmem_dealloc(uint32_t taddr, uint32_t ncols) {  // whole warp
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+DG_DEVINL void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+DG_DEVINL void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem], kind::f16 (bf16 inputs, fp32 accumulate), one thread.
+DG_DEVINL void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on an mbarrier once all previously issued tcgen05.mma of this thread completed.
+DG_DEVINL void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets lane (base + t).
+DG_DEVINL void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace dg
+
+// ------------------------------------------------------------------ host helpers
+namespace dghost {
+// Device address of the status word of the current device (set up on first use).
+unsigned* status_word();
+// Record one kernel launch made by the library (process-wide counter).
+void count_launch();
+// Streaming multiprocessor count of the current device.
+int sm_count();
+// Map a CUDA error to a dg_status (DG_OK when err == cudaSuccess).
+inline dg_status cuda_status(cudaError_t err) { return err == cudaSuccess ? DG_OK : DG_ERR_CUDA; }
+// Encode a tiled tensor map (driver entry point fetched once).  Returns false on failure.
+bool encode_tmap(void* tmap, int dtype_code, int rank, void* base, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box, int swizzle_bytes);
+}  // namespace dghost

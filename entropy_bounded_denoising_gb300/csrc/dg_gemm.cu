@@ -1,0 +1,946 @@
+// dg_gemm.cu -- tensor-core GEMM engine (tcgen05 + TMEM + TMA, sm_103a) and the
+// self-conditioning feedback built on it.
+//
+// Method (DiffusionGemma vLLM page, "DiffusionGemma: vLLM이 네이티브로 지원하는 최초의 디퓨전
+// 언어 모델(dLLM)", section "자기 조건화" (self-conditioning), and the state paragraph of
+// "DiffusionGemmaModelState와 DiffusionSampler"): the step's softmax P becomes the
+// probability-weighted mean of the token embeddings, pe = P . E, which a small gated MLP
+// turns into the feedback added to the next pass's canvas embeddings; the feedback is zero
+// for the encoder prefill and commit passes.  The MLP form (no bias, GELU-tanh gate) is a
+// reading; the pages only say "small gated MLP".
+//
+// Engine (one CTA per SM, persistent, warp-specialised):
+//   warp 0      TMA producer: A and B tiles into a ring of shared-memory stages;
+//   warp 1      tcgen05.mma issuer (one elected thread) and TMEM owner;
+//   warps 2..5  epilogue: TMEM -> registers -> global (tcgen05.ld), one TMEM lane quarter each;
+//   warps 6..9  (softmax A only) transform: the logits tile landed by TMA is turned in place
+//               into P = exp2(x * log2e / T - lse * log2e) in bf16, so P never leaves the SM.
+// Work items are (k-slice, n-tile, m-tile) with the m-tile fastest; item w runs on CTA
+// w mod P in round w / P.  All CTAs of a round therefore stream the same k-range, and the
+// B tile (embedding rows) and A tile (logit rows) they share are read from HBM once and
+// served from L2 to the others.  With more than one k-slice the fp32 partial tiles go to a
+// workspace slot per item and a fix-up kernel adds them in slice order (deterministic).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <math.h>
+
+#include <algorithm>
+
+#include "dg_common.cuh"
+
+namespace {
+
+constexpr int BM = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum AMode { A_TMA = 0, A_SOFTMAX_BF16 = 1, A_SOFTMAX_FP32 = 2 };
+enum BMode { B_KMAJOR = 0, B_MNMAJOR = 1, B_KMAJOR_GATEUP = 2 };
+enum Epi { EPI_F32 = 0, EPI_BF16 = 1, EPI_GELU_GATEUP = 2, EPI_SCATTER_BF16 = 3 };
+
+struct GemmArgs {
+    int32_t m_tiles;        // m-tiles when plan == nullptr; upper bound otherwise
+    const int32_t* plan;    // plan[0] = active canvases, plan[1..] = their ids (or nullptr)
+    int32_t tpc;            // m-tiles per canvas
+    int32_t n_tiles;
+    int32_t k_blocks;
+    int32_t splits;         // k-slices
+    int64_t K;              // true K extent (tail masking of the softmax operand)
+    int32_t L;              // rows per canvas
+    const float* lse;       // [n_canvas][L]
+    const dg_canvas_params* params;
+    int32_t epi;
+    void* out;
+    int64_t ldo;            // output row stride in elements
+    int32_t n_valid;        // valid output columns
+    int32_t m_valid;        // valid output rows (plain GEMMs)
+    float* partial;         // [items][BM * BN] when splits > 1
+    unsigned* status;
+};
+
+template <int AM, int BMD, int BN_, int BK_, int STAGES_>
+struct Cfg {
+    static constexpr int kAMode = AM;
+    static constexpr int kBMode = BMD;
+    static constexpr int BN = BN_;
+    static constexpr int BK = BK_;
+    static constexpr int STAGES = STAGES_;
+    static constexpr bool kXform = AM != A_TMA;
+    static constexpr int kAccCols = BN;                      // fp32 accumulator columns
+    static constexpr int kNAcc = (BN <= 256) ? 2 : 1;        // double-buffered when it fits
+    static constexpr int kTmemCols = kAccCols * kNAcc;       // 256 or 512
+    static constexpr int kThreads = kXform ? 320 : 192;
+    static constexpr int kATileBytes = BM * BK * 2;
+    static constexpr int kStageBytesFp32 = (AM == A_SOFTMAX_FP32) ? BM * BK * 4 : 0;
+    static constexpr int kBTileBytes = BK * BN * 2;
+    static constexpr int kStageBytes = kATileBytes + kBTileBytes + kStageBytesFp32;
+    static constexpr int kASwizzle = BK * 2;                 // 64 or 128 bytes: one swizzle row per tile row
+    static constexpr uint32_t kTxBytes = (uint32_t)(kBTileBytes + (AM == A_SOFTMAX_FP32 ? kStageBytesFp32 : kATileBytes));
+    static constexpr size_t kSmem = 1024 + (size_t)STAGES * kStageBytes + 1024;
+};
+
+// ------------------------------------------------------------------ descriptors
+// Shared-memory matrix descriptor (tcgen05): start >> 4 in bits 0..13, leading byte offset
+// >> 4 in 16..29, stride byte offset >> 4 in 32..45, version 1 in 46..47, layout in 61..63
+// (2 = 128-byte swizzle, 4 = 64-byte swizzle).
+DG_DEVINL uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, int swizzle_bytes) {
+    const uint64_t layout = swizzle_bytes == 128 ? 2ull : 4ull;
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (layout << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator (bit 4), bf16 A (bits 7..9 = 1) and
+// B (bits 10..12 = 1), A K-major (bit 15 = 0), B major in bit 16, N >> 3 in 17..22,
+// M >> 4 in 24..28.
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ scheduling
+struct Item {
+    int m, n, kb_lo, kb_hi;
+    int64_t w;
+};
+
+DG_DEVINL int active_m_tiles(const GemmArgs& a) {
+    if (!a.plan) return a.m_tiles;
+    return min(a.m_tiles, a.plan[0] * a.tpc);
+}
+
+DG_DEVINL Item decode(const GemmArgs& a, int mt, int64_t w) {
+    const int64_t T = (int64_t)mt * a.n_tiles;
+    const int s = (int)(w / T);
+    const int t = (int)(w % T);
+    Item it;
+    it.w = w;
+    it.n = t / mt;
+    it.m = t % mt;
+    it.kb_lo = (int)((int64_t)s * a.k_blocks / a.splits);
+    it.kb_hi = (int)((int64_t)(s + 1) * a.k_blocks / a.splits);
+    return it;
+}
+
+DG_DEVINL int canvas_of(const GemmArgs& a, int m) {
+    const int j = m / a.tpc;
+    return a.plan ? a.plan[1 + j] : j;
+}
+
+DG_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+DG_DEVINL float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+DG_DEVINL float gelu_tanh(float z) {
+    const float k = 0.7978845608028654f;  // sqrt(2 / pi)
+    return 0.5f * z * (1.f + tanhf(k * (z + 0.044715f * z * z * z)));
+}
+
+struct __align__(8) GemmShared {
+    uint64_t full[8];
+    uint64_t xform[8];
+    uint64_t empty[8];
+    uint64_t accf[2];
+    uint64_t acce[2];
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+DG_DEVINL bool aborted(const GemmShared& sh) { return *(volatile const int*)&sh.abort_flag != 0; }
+
+DG_DEVINL void do_abort(GemmShared& sh, unsigned* status) {
+    *(volatile int*)&sh.abort_flag = 1;
+    dg::raise_status(status, DG_DEV_TIMEOUT);
+}
+
+// Apply the epilogue to 32 consecutive accumulator columns [col0, col0 + 32) of one row.
+// `g` holds gate values for EPI_GELU_GATEUP (then `v` holds the matching up values).
+DG_DEVINL void epi_store(const GemmArgs& a, int epi, int m, int n_tile, int row, int col_in_tile, int BNv,
+                         const float (&v)[32], const float* g) {
+    if (epi == EPI_F32) {
+        const int64_t r = (int64_t)m * BM + row;
+        if (r >= a.m_valid) return;
+        const int c0 = n_tile * BNv + col_in_tile;
+        float* o = static_cast<float*>(a.out) + r * a.ldo + c0;
+        if (c0 + 32 <= a.n_valid && ((reinterpret_cast<uintptr_t>(o) & 15u) == 0)) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(o + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else {
+            for (int i = 0; i < 32; ++i)
+                if (c0 + i < a.n_valid) o[i] = v[i];
+        }
+        return;
+    }
+    uint32_t pk[16];
+    int c0;
+    int64_t r;
+    uint16_t* base;
+    if (epi == EPI_GELU_GATEUP) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(gelu_tanh(g[2 * i]) * v[2 * i], gelu_tanh(g[2 * i + 1]) * v[2 * i + 1]);
+        c0 = n_tile * (BNv / 2) + col_in_tile;
+        r = (int64_t)m * BM + row;
+        base = static_cast<uint16_t*>(a.out);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        c0 = n_tile * BNv + col_in_tile;
+        if (epi == EPI_SCATTER_BF16) {
+            const int pos = (m % a.tpc) * BM + row;
+            if (pos >= a.L) return;
+            r = (int64_t)canvas_of(a, m) * a.L + pos;
+        } else {
+            r = (int64_t)m * BM + row;
+        }
+        base = static_cast<uint16_t*>(a.out);
+    }
+    uint16_t* o = base + r * a.ldo + c0;
+    if (c0 + 32 <= a.n_valid && ((reinterpret_cast<uintptr_t>(o) & 15u) == 0)) {
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) *reinterpret_cast<uint4*>(o + 2 * i) = make_uint4(pk[i], pk[i + 1], pk[i + 2], pk[i + 3]);
+    } else {
+        for (int i = 0; i < 32; ++i)
+            if (c0 + i < a.n_valid) o[i] = (uint16_t)((i & 1) ? (pk[i >> 1] >> 16) : (pk[i >> 1] & 0xFFFFu));
+    }
+}
+
+// ------------------------------------------------------------------ the GEMM kernel
+template <class C>
+__global__ void __launch_bounds__(C::kThreads, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+           const __grid_constant__ CUtensorMap tmB1, const GemmArgs a) {
+    extern __shared__ __align__(1024) unsigned char g_smem_raw[];
+    // 1024-byte aligned stage ring after the barrier block
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(g_smem_raw) + 1023) & ~uintptr_t(1023));
+    GemmShared& sh = *reinterpret_cast<GemmShared*>(smem + (size_t)C::STAGES * C::kStageBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int mt = active_m_tiles(a);
+    const int64_t n_items = (int64_t)mt * a.n_tiles * a.splits;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            dg::mbar_init(&sh.full[s], 1);
+            dg::mbar_init(&sh.xform[s], 128);
+            dg::mbar_init(&sh.empty[s], 1);
+        }
+        for (int i = 0; i < C::kNAcc; ++i) {
+            dg::mbar_init(&sh.accf[i], 1);
+            dg::mbar_init(&sh.acce[i], 128);
+        }
+        sh.abort_flag = 0;
+        dg::fence_mbar_init();
+    }
+    if (warp == 1) {
+        dg::tmem_alloc(&sh.tmem_base, C::kTmemCols);
+        dg::tmem_relinquish();
+    }
+    dg::tc_fence_before();
+    __syncthreads();
+    dg::tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            dg::prefetch_tmap(&tmA);
+            dg::prefetch_tmap(&tmB0);
+            if (C::kBMode == B_KMAJOR_GATEUP) dg::prefetch_tmap(&tmB1);
+            uint32_t it = 0;
+            for (int64_t w = blockIdx.x; w < n_items && !aborted(sh); w += gridDim.x) {
+                const Item im = decode(a, mt, w);
+                int cz = 0, crow = 0;
+                if (C::kXform) {
+                    cz = canvas_of(a, im.m);
+                    crow = (im.m % a.tpc) * BM;
+                }
+                for (int kb = im.kb_lo; kb < im.kb_hi; ++kb, ++it) {
+                    const int s = (int)(it % C::STAGES);
+                    const uint32_t ph = (it / C::STAGES) & 1u;
+                    if (!dg::mbar_wait(&sh.empty[s], ph ^ 1u)) { do_abort(sh, a.status); break; }
+                    unsigned char* st = smem + (size_t)s * C::kStageBytes;
+                    unsigned char* sA = st;
+                    unsigned char* sB = st + C::kATileBytes;
+                    unsigned char* sF = st + C::kATileBytes + C::kBTileBytes;  // fp32 staging
+                    dg::mbar_arrive_expect_tx(&sh.full[s], C::kTxBytes);
+                    const int k0 = kb * C::BK;
+                    if (C::kAMode == A_TMA) {
+                        dg::tma_load_2d(sA, &tmA, k0, im.m * BM, &sh.full[s]);
+                    } else if (C::kAMode == A_SOFTMAX_BF16) {
+                        dg::tma_load_3d(sA, &tmA, k0, crow, cz, &sh.full[s]);
+                    } else {
+                        // fp32 logits: BK = 32 columns = one 128-byte swizzle row per tile row
+                        dg::tma_load_3d(sF, &tmA, k0, crow, cz, &sh.full[s]);
+                    }
+                    if (C::kBMode == B_MNMAJOR) {
+                        // [K][N] embedding rows: one 64-column (128-byte) atom column per load
+#pragma unroll
+                        for (int j = 0; j < C::BN / 64; ++j)
+                            dg::tma_load_2d(sB + j * (C::BK * 128), &tmB0, im.n * C::BN + j * 64, k0, &sh.full[s]);
+                    } else if (C::kBMode == B_KMAJOR) {
+                        dg::tma_load_2d(sB, &tmB0, k0, im.n * C::BN, &sh.full[s]);
+                    } else {
+                        // gate rows in the first half of the tile, up rows in the second
+                        dg::tma_load_2d(sB, &tmB0, k0, im.n * (C::BN / 2), &sh.full[s]);
+                        dg::tma_load_2d(sB + (C::BN / 2) * C::BK * 2, &tmB1, k0, im.n * (C::BN / 2), &sh.full[s]);
+                    }
+                }
+            }
+            // never leave with a copy still landing in this CTA's shared memory
+            if (aborted(sh)) {
+                for (int s = 0; s < C::STAGES; ++s) (void)dg::mbar_wait(&sh.full[s], 0);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_mn = instr_desc(BM, C::BN > 256 ? 256 : C::BN, true);
+            constexpr uint32_t idesc_k = instr_desc(BM, C::BN > 256 ? 256 : C::BN, false);
+            constexpr uint32_t idesc = (C::kBMode == B_MNMAJOR) ? idesc_mn : idesc_k;
+            uint32_t it = 0, acc_it = 0;
+            for (int64_t w = blockIdx.x; w < n_items && !aborted(sh); w += gridDim.x, ++acc_it) {
+                const Item im = decode(a, mt, w);
+                const int ab = (int)(acc_it % C::kNAcc);
+                const uint32_t aph = (acc_it / C::kNAcc) & 1u;
+                if (!dg::mbar_wait(&sh.acce[ab], aph ^ 1u)) { do_abort(sh, a.status); break; }
+                dg::tc_fence_after();
+                const uint32_t dacc = tmem + (uint32_t)(ab * C::kAccCols);
+                bool ok = true;
+                for (int kb = im.kb_lo; kb < im.kb_hi; ++kb, ++it) {
+                    const int s = (int)(it % C::STAGES);
+                    const uint32_t ph = (it / C::STAGES) & 1u;
+                    if (!dg::mbar_wait(&sh.full[s], ph)) { ok = false; break; }
+                    if (C::kXform && !dg::mbar_wait(&sh.xform[s], ph)) { ok = false; break; }
+                    dg::tc_fence_after();
+                    const uint32_t sA = dg::smem_u32(smem + (size_t)s * C::kStageBytes);
+                    const uint32_t sB = sA + C::kATileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < C::BK / 16; ++kk) {
+                        const uint64_t ad = smem_desc(sA + kk * 32, 16, 8 * C::BK * 2, C::kASwizzle);
+                        const uint32_t accum = (kb > im.kb_lo || kk > 0) ? 1u : 0u;
+                        if (C::kBMode == B_MNMAJOR) {
+                            // N-major B: LBO = distance between 64-column atom columns, SBO = 8 K rows
+#pragma unroll
+                            for (int h = 0; h < C::BN / 256; ++h) {
+                                const uint64_t bd = smem_desc(sB + h * 4 * (C::BK * 128) + kk * 16 * 128, C::BK * 128, 1024, 128);
+                                dg::tc_mma_f16(dacc + h * 256, ad, bd, idesc, accum);
+                            }
+                        } else {
+                            const uint64_t bd = smem_desc(sB + kk * 32, 16, 8 * C::BK * 2, C::kASwizzle);
+                            dg::tc_mma_f16(dacc, ad, bd, idesc, accum);
+                        }
+                    }
+                    dg::tc_commit(&sh.empty[s]);  // frees the stage once these MMAs have read it
+                }
+                if (!ok) { do_abort(sh, a.status); break; }
+                dg::tc_commit(&sh.accf[ab]);  // accumulator complete
+            }
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;
+        uint32_t acc_it = 0;
+        for (int64_t w = blockIdx.x; w < n_items && !aborted(sh); w += gridDim.x, ++acc_it) {
+            const Item im = decode(a, mt, w);
+            const int ab = (int)(acc_it % C::kNAcc);
+            const uint32_t aph = (acc_it / C::kNAcc) & 1u;
+            if (!dg::mbar_wait(&sh.accf[ab], aph)) { do_abort(sh, a.status); break; }
+            dg::tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * C::kAccCols);
+            if (a.splits > 1) {
+                float* dst = a.partial + (size_t)im.w * (BM * C::BN) + (size_t)row * C::BN;
+                for (int ch = 0; ch < C::BN / 32; ++ch) {
+                    float v[32];
+                    dg::tmem_ld32(tbase + ch * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(dst + ch * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                }
+            } else if (a.epi == EPI_GELU_GATEUP) {
+                for (int ch = 0; ch < C::BN / 64; ++ch) {
+                    float g[32], u[32];
+                    dg::tmem_ld32(tbase + ch * 32, g);
+                    dg::tmem_ld32(tbase + C::BN / 2 + ch * 32, u);
+                    epi_store(a, a.epi, im.m, im.n, row, ch * 32, C::BN, u, g);
+                }
+            } else {
+                for (int ch = 0; ch < C::BN / 32; ++ch) {
+                    float v[32];
+                    dg::tmem_ld32(tbase + ch * 32, v);
+                    epi_store(a, a.epi, im.m, im.n, row, ch * 32, C::BN, v, nullptr);
+                }
+            }
+            dg::tc_fence_before();
+            dg::mbar_arrive(&sh.acce[ab]);
+        }
+    } else {
+        // ------------------------------------------------ softmax transform (warps 6..9)
+        if (C::kXform) {
+            const int t = threadIdx.x - 192;  // tile row handled by this thread
+            uint32_t it = 0;
+            for (int64_t w = blockIdx.x; w < n_items && !aborted(sh); w += gridDim.x) {
+                const Item im = decode(a, mt, w);
+                const int cz = canvas_of(a, im.m);
+                const int pos = (im.m % a.tpc) * BM + t;
+                const dg_canvas_params pr = a.params[cz];
+                const float kx = kLog2e / pr.temperature;
+                const float lb = (pos < a.L) ? a.lse[(int64_t)cz * a.L + pos] * kLog2e : 0.f;
+                bool ok = true;
+                for (int kb = im.kb_lo; kb < im.kb_hi; ++kb, ++it) {
+                    const int s = (int)(it % C::STAGES);
+                    const uint32_t ph = (it / C::STAGES) & 1u;
+                    if (!dg::mbar_wait(&sh.full[s], ph)) { ok = false; break; }
+                    unsigned char* st = smem + (size_t)s * C::kStageBytes;
+                    unsigned char* rowA = st + t * (C::BK * 2);
+                    const int64_t kbase = (int64_t)kb * C::BK;
+                    const bool tail = kbase + C::BK > a.K;
+                    // one tile row = BK bf16 = BK/8 16-byte chunks; the swizzle permutes chunks
+                    // within the row, so chunk c of the row sits at c ^ ((t >> sh) & mask)
+                    constexpr int kChunks = C::BK / 8;
+                    const int sw = (C::kASwizzle == 128) ? (t & 7) : ((t >> 1) & 3);
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c) {
+                        const int pc = c ^ sw;
+                        float x[8];
+                        if (C::kAMode == A_SOFTMAX_BF16) {
+                            const uint4 qv = *reinterpret_cast<const uint4*>(rowA + pc * 16);
+                            x[0] = __uint_as_float(qv.x << 16); x[1] = __uint_as_float(qv.x & 0xffff0000u);
+                            x[2] = __uint_as_float(qv.y << 16); x[3] = __uint_as_float(qv.y & 0xffff0000u);
+                            x[4] = __uint_as_float(qv.z << 16); x[5] = __uint_as_float(qv.z & 0xffff0000u);
+                            x[6] = __uint_as_float(qv.w << 16); x[7] = __uint_as_float(qv.w & 0xffff0000u);
+                        } else {
+                            // fp32 staging row: 32 floats = 128 bytes, 128-byte swizzle
+                            const unsigned char* rowF = st + C::kATileBytes + C::kBTileBytes + t * 128;
+                            const float4 f0 = *reinterpret_cast<const float4*>(rowF + (((2 * c) ^ (t & 7)) * 16));
+                            const float4 f1 = *reinterpret_cast<const float4*>(rowF + (((2 * c + 1) ^ (t & 7)) * 16));
+                            x[0] = f0.x; x[1] = f0.y; x[2] = f0.z; x[3] = f0.w;
+                            x[4] = f1.x; x[5] = f1.y; x[6] = f1.z; x[7] = f1.w;
+                        }
+                        float pz[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) pz[j] = ex2(fmaf(x[j], kx, -lb));
+                        if (tail) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                if (kbase + c * 8 + j >= a.K) pz[j] = 0.f;
+                        }
+                        *reinterpret_cast<uint4*>(rowA + pc * 16) =
+                            make_uint4(pack_bf16x2(pz[0], pz[1]), pack_bf16x2(pz[2], pz[3]),
+                                       pack_bf16x2(pz[4], pz[5]), pack_bf16x2(pz[6], pz[7]));
+                    }
+                    dg::fence_proxy_async_smem();  // make the generic-proxy writes visible to tcgen05
+                    dg::mbar_arrive(&sh.xform[s]);
+                }
+                if (!ok) { do_abort(sh, a.status); break; }
+            }
+        }
+    }
+
+    dg::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        dg::tc_fence_after();
+        dg::tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ split-K fix-up
+// One CTA per tile: adds the k-slice partials in slice order and applies the epilogue.
+template <int BN>
+__global__ void __launch_bounds__(256) k_fixup(const GemmArgs a) {
+    const int mt = active_m_tiles(a);
+    const int64_t T = (int64_t)mt * a.n_tiles;
+    const int64_t t = blockIdx.x;
+    if (t >= T) return;
+    const int n = (int)(t / mt), m = (int)(t % mt);
+    constexpr int kGroups = BM * (BN / 32);  // (row, 32-column chunk) pairs
+    for (int gidx = threadIdx.x; gidx < kGroups; gidx += blockDim.x) {
+        const int row = gidx / (BN / 32);
+        const int ch = gidx % (BN / 32);
+        if (a.epi == EPI_GELU_GATEUP && ch >= BN / 64) continue;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        float g[32];
+        for (int s = 0; s < a.splits; ++s) {
+            const float* src = a.partial + (size_t)(s * T + t) * (BM * BN) + (size_t)row * BN;
+            if (a.epi == EPI_GELU_GATEUP) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    if (s == 0) g[i] = 0.f;
+                    g[i] += src[ch * 32 + i];
+                    v[i] += src[BN / 2 + ch * 32 + i];
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] += src[ch * 32 + i];
+            }
+        }
+        epi_store(a, a.epi, m, n, row, ch * 32, BN, v, a.epi == EPI_GELU_GATEUP ? g : nullptr);
+    }
+}
+
+// ------------------------------------------------------------------ self-conditioning helpers
+DG_DEVINL bool self_cond_on(const dg_canvas_params& p, const uint8_t* converged, int64_t c) {
+    return (p.flags & DG_ACTIVE) && (p.flags & DG_SELF_COND) && !(p.flags & DG_READ_ONLY) &&
+           !(converged && converged[c]) && p.temperature > 0.f;
+}
+
+// Compact list of the canvases whose feedback is computed this step (original order).
+__global__ void k_plan(const dg_canvas_params* __restrict__ params, const uint8_t* __restrict__ converged,
+                       int64_t n, int32_t* __restrict__ plan) {
+    __shared__ int count;
+    if (threadIdx.x == 0) count = 0;
+    __syncthreads();
+    for (int64_t base = 0; base < n; base += blockDim.x) {
+        const int64_t c = base + threadIdx.x;
+        const bool on = c < n && self_cond_on(params[c], converged, c);
+        const unsigned ballot = __ballot_sync(0xffffffffu, on);
+        // order-preserving compaction: one warp at a time
+        for (int wv = 0; wv < (int)(blockDim.x >> 5); ++wv) {
+            if ((int)(threadIdx.x >> 5) == wv) {
+                const int before = __popc(ballot & ((1u << (threadIdx.x & 31)) - 1u));
+                if (on) plan[1 + count + before] = (int32_t)c;
+                __syncwarp();
+                if ((threadIdx.x & 31) == 0) count += __popc(ballot);
+            }
+            __syncthreads();
+        }
+    }
+    if (threadIdx.x == 0) plan[0] = count;
+}
+
+// Zero the feedback rows of canvases that get none this step.
+__global__ void k_zero_rows(const dg_canvas_params* __restrict__ params, const uint8_t* __restrict__ converged,
+                            int32_t L, int32_t d, uint16_t* __restrict__ delta) {
+    const int64_t c = blockIdx.y;
+    if (self_cond_on(params[c], converged, c)) return;
+    const int64_t total = (int64_t)L * d;
+    uint16_t* row = delta + c * total;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x)
+        row[i] = 0;
+}
+
+// ------------------------------------------------------------------ host side
+using PEbf16 = Cfg<A_SOFTMAX_BF16, B_MNMAJOR, 512, 32, 5>;
+using PEfp32 = Cfg<A_SOFTMAX_FP32, B_MNMAJOR, 512, 32, 3>;
+using PEprob = Cfg<A_TMA, B_MNMAJOR, 512, 32, 5>;
+using GateUp = Cfg<A_TMA, B_KMAJOR_GATEUP, 256, 64, 4>;
+using Down = Cfg<A_TMA, B_KMAJOR, 256, 64, 4>;
+
+constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// k-slices: the fewest that keep the rounds at least 95 % full, with slices of at least
+// `min_slice` k-blocks so that the partial tiles stay cheap next to the MMA work.
+int choose_splits(int64_t T, int k_blocks, int P, int min_slice) {
+    int best = 1;
+    double best_eff = 0.0;
+    for (int s = 1; s <= 32; ++s) {
+        if (s > 1 && k_blocks / s < min_slice) break;
+        const int64_t items = T * s;
+        const int64_t rounds = (items + P - 1) / P;
+        const double eff = (double)items / (double)(rounds * P);
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = s;
+        }
+        if (eff >= 0.95) break;
+    }
+    return best;
+}
+
+template <class C>
+dg_status launch_gemm(const void* tmA, const void* tmB0, const void* tmB1, const GemmArgs& a, int64_t max_items,
+                      cudaStream_t stream) {
+    auto kern = k_gemm<C>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
+        return DG_ERR_CUDA;
+    const int P = dghost::sm_count();
+    if (P <= 0) return DG_ERR_CUDA;
+    const int grid = (int)std::min<int64_t>(P, std::max<int64_t>(1, max_items));
+    const CUtensorMap& A = *static_cast<const CUtensorMap*>(tmA);
+    const CUtensorMap& B0 = *static_cast<const CUtensorMap*>(tmB0);
+    const CUtensorMap& B1 = *static_cast<const CUtensorMap*>(tmB1);
+    kern<<<grid, C::kThreads, C::kSmem, stream>>>(A, B0, B1, a);
+    dghost::count_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return DG_ERR_CUDA;
+    if (a.splits > 1) {
+        const int64_t T = (int64_t)a.m_tiles * a.n_tiles;
+        k_fixup<C::BN><<<(unsigned)T, 256, 0, stream>>>(a);
+        dghost::count_launch();
+        e = cudaGetLastError();
+    }
+    return dghost::cuda_status(e);
+}
+
+struct TMaps {
+    alignas(64) unsigned char a[128];
+    alignas(64) unsigned char b0[128];
+    alignas(64) unsigned char b1[128];
+};
+
+// 2D bf16 (or fp32) row-major matrix [rows][cols] with row stride ld (elements).
+bool tmap_2d(void* tm, int dt, const void* base, int64_t cols, int64_t rows, int64_t ld, uint32_t box_cols,
+             uint32_t box_rows, int swz) {
+    const int es = dt == 0 ? 2 : 4;
+    uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
+    uint64_t strides[1] = {(uint64_t)(ld * es)};
+    uint32_t box[2] = {box_cols, box_rows};
+    return dghost::encode_tmap(tm, dt, 2, const_cast<void*>(base), dims, strides, box, swz);
+}
+
+// 3D logits [n][L][ld] as (V, L, n) with box (BK, 128, 1).
+bool tmap_logits(void* tm, int dt, const void* base, int64_t V, int32_t L, int64_t n, int64_t ld, uint32_t bk,
+                 int swz) {
+    const int es = dt == 0 ? 2 : 4;
+    uint64_t dims[3] = {(uint64_t)V, (uint64_t)L, (uint64_t)n};
+    uint64_t strides[2] = {(uint64_t)(ld * es), (uint64_t)(ld * es * L)};
+    uint32_t box[3] = {bk, (uint32_t)BM, 1};
+    return dghost::encode_tmap(tm, dt, 3, const_cast<void*>(base), dims, strides, box, swz);
+}
+
+struct SelfCondLayout {
+    size_t plan, pe, hmid, partial, total;
+    int64_t rows;  // compact rows (n * L_pad)
+};
+
+SelfCondLayout self_cond_layout(int64_t n, int32_t L, int32_t d, int32_t h, int P) {
+    SelfCondLayout l;
+    const int tpc = (L + BM - 1) / BM;
+    l.rows = n * tpc * BM;
+    l.plan = 0;
+    l.pe = align256(sizeof(int32_t) * (size_t)(n + 1));
+    l.hmid = l.pe + align256((size_t)l.rows * d * 2);
+    l.partial = l.hmid + align256((size_t)l.rows * h * 2);
+    // partial slots for the P.E GEMM (the only one that splits K)
+    const int64_t T = n * tpc * (int64_t)((d + 511) / 512);
+    const int64_t slots = T * 32 > 0 ? std::min<int64_t>(T * 32, std::max<int64_t>(T, 8LL * P)) : 0;
+    l.total = l.partial + align256((size_t)slots * BM * 512 * 4);
+    return l;
+}
+
+int64_t pe_partial_slots(int64_t n, int32_t L, int32_t d, int P) {
+    const int tpc = (L + BM - 1) / BM;
+    const int64_t T = n * tpc * (int64_t)((d + 511) / 512);
+    return T * 32 > 0 ? std::min<int64_t>(T * 32, std::max<int64_t>(T, 8LL * P)) : 0;
+}
+
+// The three GEMMs of the feedback on compact rows: pe = P.E (already in `pe`), then
+// hmid = gelu(pe W_gate^T) * (pe W_up^T), then delta = hmid W_down^T scattered to rows.
+dg_status run_mlp(const uint16_t* pe, uint16_t* hmid, int64_t rows, int32_t d, int32_t h, const uint16_t* W_gate,
+                  const uint16_t* W_up, const uint16_t* W_down, uint16_t* delta, int64_t delta_ld,
+                  const int32_t* plan, int tpc, int32_t L, int32_t m_valid_rows, cudaStream_t stream) {
+    const int P = dghost::sm_count();
+    TMaps t1, t2;
+    if (!tmap_2d(t1.a, 0, pe, d, rows, d, 64, BM, 128)) return DG_ERR_CUDA;
+    if (!tmap_2d(t1.b0, 0, W_gate, d, h, d, 64, 128, 128)) return DG_ERR_CUDA;
+    if (!tmap_2d(t1.b1, 0, W_up, d, h, d, 64, 128, 128)) return DG_ERR_CUDA;
+    GemmArgs g{};
+    g.m_tiles = (int32_t)(rows / BM);
+    g.plan = plan;
+    g.tpc = tpc;
+    g.n_tiles = (h + 127) / 128;
+    g.k_blocks = (d + 63) / 64;
+    g.splits = 1;
+    g.K = d;
+    g.L = L;
+    g.epi = EPI_GELU_GATEUP;
+    g.out = hmid;
+    g.ldo = h;
+    g.n_valid = h;
+    g.m_valid = (int32_t)rows;
+    g.status = dghost::status_word();
+    dg_status s = launch_gemm<GateUp>(t1.a, t1.b0, t1.b1, g, (int64_t)g.m_tiles * g.n_tiles, stream);
+    if (s != DG_OK) return s;
+
+    if (!tmap_2d(t2.a, 0, hmid, h, rows, h, 64, BM, 128)) return DG_ERR_CUDA;
+    if (!tmap_2d(t2.b0, 0, W_down, h, d, h, 64, 256, 128)) return DG_ERR_CUDA;
+    GemmArgs q = g;
+    q.n_tiles = (d + 255) / 256;
+    q.k_blocks = (h + 63) / 64;
+    q.K = h;
+    q.epi = EPI_SCATTER_BF16;
+    q.out = delta;
+    q.ldo = delta_ld;
+    q.n_valid = d;
+    q.m_valid = m_valid_rows;
+    (void)P;
+    return launch_gemm<Down>(t2.a, t2.b0, t2.b0, q, (int64_t)q.m_tiles * q.n_tiles, stream);
+}
+
+dg_status check_weights(int64_t V, int32_t d, int32_t h, const uint16_t* E, const uint16_t* Wg, const uint16_t* Wu,
+                        const uint16_t* Wd) {
+    if (d < 8 || d > 65536 || h < 8 || h > 65536 || (d % 8) || (h % 8) || V < 2 || V > 0x7fffffffLL)
+        return DG_ERR_INVALID_ARG;
+    if (!E || !Wg || !Wu || !Wd) return DG_ERR_INVALID_ARG;
+    if (!aligned16(E) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd)) return DG_ERR_ALIGNMENT;
+    return DG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dg_self_cond_workspace_bytes(int64_t n_canvas, int32_t L, int32_t d, int32_t h) {
+    if (n_canvas < 0 || L < 1 || d < 1 || h < 1) return 0;
+    const int P = std::max(1, dghost::sm_count());
+    return self_cond_layout(n_canvas, L, d, h, P).total;
+}
+
+static dg_status self_cond_dims(dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L, int64_t V, int32_t d,
+                                int32_t h) {
+    if (dtype != DG_BF16 && dtype != DG_FP32) return DG_ERR_INVALID_ARG;
+    if (n_canvas < 0 || n_canvas > 65535 || L < 1 || L > 1024 || ld < V || V < 2 || V > 0x7fffffffLL)
+        return DG_ERR_INVALID_ARG;
+    if (d < 8 || d > 65536 || h < 8 || h > 65536 || (d % 8) || (h % 8)) return DG_ERR_INVALID_ARG;
+    return DG_OK;
+}
+
+// Device-dependent part of the checks (the layout depends on the SM count).
+static dg_status self_cond_workspace(int64_t n_canvas, int32_t L, int32_t d, int32_t h, const void* workspace,
+                                     size_t workspace_bytes, SelfCondLayout* lay) {
+    const int P = dghost::sm_count();
+    if (P <= 0) return DG_ERR_CUDA;
+    *lay = self_cond_layout(n_canvas, L, d, h, P);
+    if (!workspace || workspace_bytes < lay->total) return DG_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DG_ERR_ALIGNMENT;
+    return DG_OK;
+}
+
+dg_status dg_self_cond_prepare(const dg_canvas_params* params, const uint8_t* converged, int64_t n_canvas,
+                               int32_t L, int32_t d, int32_t h, uint16_t* delta_emb, void* workspace,
+                               size_t workspace_bytes, dg_stream_t stream) {
+    dg_status s = self_cond_dims(DG_BF16, 2, n_canvas, L, 2, d, h);
+    if (s != DG_OK || n_canvas == 0) return s;
+    if (!params || !delta_emb) return DG_ERR_INVALID_ARG;
+    if (!aligned16(delta_emb)) return DG_ERR_ALIGNMENT;
+    SelfCondLayout lay;
+    s = self_cond_workspace(n_canvas, L, d, h, workspace, workspace_bytes, &lay);
+    if (s != DG_OK) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    int32_t* plan = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + lay.plan);
+    k_plan<<<1, 1024, 0, st>>>(params, converged, n_canvas, plan);
+    dghost::count_launch();
+    if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+    dim3 grid((unsigned)std::min<int64_t>(1024, ((int64_t)L * d + 255) / 256), (unsigned)n_canvas);
+    k_zero_rows<<<grid, 256, 0, st>>>(params, converged, L, d, delta_emb);
+    dghost::count_launch();
+    return dghost::cuda_status(cudaGetLastError());
+}
+
+dg_status dg_self_cond_pe(const void* logits, dg_dtype dtype, int64_t ld, const float* lse,
+                          const dg_canvas_params* params, int64_t n_canvas, int32_t L, int64_t V, int32_t d,
+                          int32_t h, const uint16_t* E, void* workspace, size_t workspace_bytes,
+                          dg_stream_t stream) {
+    dg_status s = self_cond_dims(dtype, ld, n_canvas, L, V, d, h);
+    if (s != DG_OK || n_canvas == 0) return s;
+    if (!logits || !lse || !params || !E) return DG_ERR_INVALID_ARG;
+    const int es = dtype == DG_BF16 ? 2 : 4;
+    if (!aligned16(logits) || (ld * es) % 16 != 0 || !aligned16(E)) return DG_ERR_ALIGNMENT;
+    SelfCondLayout lay;
+    s = self_cond_workspace(n_canvas, L, d, h, workspace, workspace_bytes, &lay);
+    if (s != DG_OK) return s;
+    const int P = dghost::sm_count();
+    cudaStream_t st = (cudaStream_t)stream;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    const int tpc = (L + BM - 1) / BM;
+    // pe = softmax(logits / T) . E  (P formed in shared memory)
+    TMaps tm;
+    const int bk = 32;
+    if (!tmap_logits(tm.a, dtype == DG_BF16 ? 0 : 1, logits, V, L, n_canvas, ld, bk, dtype == DG_BF16 ? 64 : 128))
+        return DG_ERR_CUDA;
+    if (!tmap_2d(tm.b0, 0, E, d, V, d, 64, bk, 128)) return DG_ERR_CUDA;
+    GemmArgs g{};
+    g.m_tiles = (int32_t)(n_canvas * tpc);
+    g.plan = reinterpret_cast<int32_t*>(ws + lay.plan);
+    g.tpc = tpc;
+    g.n_tiles = (d + 511) / 512;
+    g.k_blocks = (int32_t)((V + bk - 1) / bk);
+    const int64_t Tmax = (int64_t)g.m_tiles * g.n_tiles;
+    g.splits = choose_splits(Tmax, g.k_blocks, P, 256);
+    while (g.splits > 1 && Tmax * g.splits > pe_partial_slots(n_canvas, L, d, P)) --g.splits;
+    g.K = V;
+    g.L = L;
+    g.lse = lse;
+    g.params = params;
+    g.epi = EPI_BF16;
+    g.out = ws + lay.pe;
+    g.ldo = d;
+    g.n_valid = d;
+    g.m_valid = (int32_t)lay.rows;
+    g.partial = reinterpret_cast<float*>(ws + lay.partial);
+    g.status = dghost::status_word();
+    return dtype == DG_BF16 ? launch_gemm<PEbf16>(tm.a, tm.b0, tm.b0, g, Tmax * g.splits, st)
+                            : launch_gemm<PEfp32>(tm.a, tm.b0, tm.b0, g, Tmax * g.splits, st);
+}
+
+dg_status dg_self_cond_mlp(int64_t n_canvas, int32_t L, int32_t d, int32_t h, const uint16_t* W_gate,
+                           const uint16_t* W_up, const uint16_t* W_down, uint16_t* delta_emb, void* workspace,
+                           size_t workspace_bytes, dg_stream_t stream) {
+    dg_status s = self_cond_dims(DG_BF16, 2, n_canvas, L, 2, d, h);
+    if (s != DG_OK || n_canvas == 0) return s;
+    if (!W_gate || !W_up || !W_down || !delta_emb) return DG_ERR_INVALID_ARG;
+    if (!aligned16(W_gate) || !aligned16(W_up) || !aligned16(W_down) || !aligned16(delta_emb))
+        return DG_ERR_ALIGNMENT;
+    SelfCondLayout lay;
+    s = self_cond_workspace(n_canvas, L, d, h, workspace, workspace_bytes, &lay);
+    if (s != DG_OK) return s;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    const int tpc = (L + BM - 1) / BM;
+    return run_mlp(reinterpret_cast<uint16_t*>(ws + lay.pe), reinterpret_cast<uint16_t*>(ws + lay.hmid), lay.rows,
+                   d, h, W_gate, W_up, W_down, delta_emb, d, reinterpret_cast<int32_t*>(ws + lay.plan), tpc, L,
+                   (int32_t)lay.rows, (cudaStream_t)stream);
+}
+
+dg_status dg_self_cond_logits(const void* logits, dg_dtype dtype, int64_t ld, const float* lse,
+                              const dg_canvas_params* params, const uint8_t* converged, int64_t n_canvas, int32_t L,
+                              int64_t V, int32_t d, int32_t h, const uint16_t* E, const uint16_t* W_gate,
+                              const uint16_t* W_up, const uint16_t* W_down, uint16_t* delta_emb, void* workspace,
+                              size_t workspace_bytes, dg_stream_t stream) {
+    dg_status s = self_cond_dims(dtype, ld, n_canvas, L, V, d, h);
+    if (s != DG_OK) return s;
+    s = check_weights(V, d, h, E, W_gate, W_up, W_down);
+    if (s != DG_OK) return s;
+    if (n_canvas == 0) return DG_OK;
+    if (!logits || !lse || !params || !delta_emb) return DG_ERR_INVALID_ARG;
+    const int es = dtype == DG_BF16 ? 2 : 4;
+    if (!aligned16(logits) || (ld * es) % 16 != 0 || !aligned16(delta_emb)) return DG_ERR_ALIGNMENT;
+    SelfCondLayout lay;
+    s = self_cond_workspace(n_canvas, L, d, h, workspace, workspace_bytes, &lay);
+    if (s != DG_OK) return s;
+    s = dg_self_cond_prepare(params, converged, n_canvas, L, d, h, delta_emb, workspace, workspace_bytes, stream);
+    if (s != DG_OK) return s;
+    s = dg_self_cond_pe(logits, dtype, ld, lse, params, n_canvas, L, V, d, h, E, workspace, workspace_bytes, stream);
+    if (s != DG_OK) return s;
+    return dg_self_cond_mlp(n_canvas, L, d, h, W_gate, W_up, W_down, delta_emb, workspace, workspace_bytes, stream);
+}
+
+size_t dg_self_cond_probs_workspace_bytes(int64_t n_rows, int32_t d, int32_t h) {
+    if (n_rows < 0 || d < 1 || h < 1) return 0;
+    const int P = std::max(1, dghost::sm_count());
+    const int64_t tiles = (n_rows + BM - 1) / BM;
+    const int64_t rows = tiles * BM;
+    const int64_t T = tiles * ((d + 511) / 512);
+    const int64_t slots = T * 32 > 0 ? std::min<int64_t>(T * 32, std::max<int64_t>(T, 8LL * P)) : 0;
+    return align256((size_t)rows * d * 2) + align256((size_t)rows * h * 2) + align256((size_t)slots * BM * 512 * 4);
+}
+
+dg_status dg_self_cond_probs(const uint16_t* P_rows, int64_t ld, int64_t n_rows, int64_t V, int32_t d, int32_t h,
+                             const uint16_t* E, const uint16_t* W_gate, const uint16_t* W_up, const uint16_t* W_down,
+                             uint16_t* delta_emb, void* workspace, size_t workspace_bytes, dg_stream_t stream) {
+    if (n_rows < 0 || n_rows > (1LL << 24) || ld < V) return DG_ERR_INVALID_ARG;
+    dg_status s = check_weights(V, d, h, E, W_gate, W_up, W_down);
+    if (s != DG_OK) return s;
+    if (n_rows == 0) return DG_OK;
+    if (!P_rows || !delta_emb) return DG_ERR_INVALID_ARG;
+    if (!aligned16(P_rows) || (ld * 2) % 16 != 0 || !aligned16(delta_emb)) return DG_ERR_ALIGNMENT;
+    const size_t need = dg_self_cond_probs_workspace_bytes(n_rows, d, h);
+    if (!workspace || workspace_bytes < need) return DG_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DG_ERR_ALIGNMENT;
+    const int P = dghost::sm_count();
+    if (P <= 0) return DG_ERR_CUDA;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int64_t tiles = (n_rows + BM - 1) / BM;
+    const int64_t rows = tiles * BM;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    uint16_t* pe = reinterpret_cast<uint16_t*>(ws);
+    uint16_t* hmid = reinterpret_cast<uint16_t*>(ws + align256((size_t)rows * d * 2));
+    float* partial = reinterpret_cast<float*>(ws + align256((size_t)rows * d * 2) + align256((size_t)rows * h * 2));
+
+    TMaps tm;
+    const int bk = 32;
+    if (!tmap_2d(tm.a, 0, P_rows, V, n_rows, ld, bk, BM, 64)) return DG_ERR_CUDA;
+    if (!tmap_2d(tm.b0, 0, E, d, V, d, 64, bk, 128)) return DG_ERR_CUDA;
+    GemmArgs g{};
+    g.m_tiles = (int32_t)tiles;
+    g.plan = nullptr;
+    g.tpc = (int32_t)tiles;
+    g.n_tiles = (d + 511) / 512;
+    g.k_blocks = (int32_t)((V + bk - 1) / bk);
+    const int64_t T = (int64_t)g.m_tiles * g.n_tiles;
+    const int64_t slots = T * 32 > 0 ? std::min<int64_t>(T * 32, std::max<int64_t>(T, 8LL * P)) : 0;
+    g.splits = choose_splits(T, g.k_blocks, P, 256);
+    while (g.splits > 1 && T * g.splits > slots) --g.splits;
+    g.K = V;
+    g.L = (int32_t)n_rows;
+    g.epi = EPI_BF16;
+    g.out = pe;
+    g.ldo = d;
+    g.n_valid = d;
+    g.m_valid = (int32_t)rows;
+    g.partial = partial;
+    g.status = dghost::status_word();
+    s = launch_gemm<PEprob>(tm.a, tm.b0, tm.b0, g, T * g.splits, st);
+    if (s != DG_OK) return s;
+    return run_mlp(pe, hmid, rows, d, h, W_gate, W_up, W_down, delta_emb, d, nullptr, (int)tiles, (int32_t)n_rows,
+                   (int32_t)rows, st);
+}
+
+size_t dg_gemm_workspace_bytes(int64_t M, int64_t N) {
+    if (M < 1 || N < 1) return 0;
+    const int P = std::max(1, dghost::sm_count());
+    const int64_t T = ((M + BM - 1) / BM) * ((N + 255) / 256);
+    const int64_t slots = std::min<int64_t>(T * 32, std::max<int64_t>(T, 8LL * P));
+    return align256((size_t)slots * BM * 512 * 4);
+}
+
+dg_status dg_gemm_bf16(const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb, int b_mn_major, float* C,
+                       int64_t ldc, int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                       dg_stream_t stream) {
+    if (M < 0 || N < 0 || K < 0 || M > (1LL << 24) || N > (1LL << 24) || K > 0x7fffffffLL) return DG_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return DG_OK;
+    if (K == 0 || !A || !B || !C || lda < K || ldc < N) return DG_ERR_INVALID_ARG;
+    if (b_mn_major ? ldb < N : ldb < K) return DG_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || (lda % 8) || (ldb % 8)) return DG_ERR_ALIGNMENT;
+    const size_t need = dg_gemm_workspace_bytes(M, N);
+    if (workspace_bytes < need || (need && !workspace)) return DG_ERR_WORKSPACE;
+    const int P = dghost::sm_count();
+    if (P <= 0) return DG_ERR_CUDA;
+    cudaStream_t st = (cudaStream_t)stream;
+    TMaps tm;
+    GemmArgs g{};
+    g.m_tiles = (int32_t)((M + BM - 1) / BM);
+    g.tpc = g.m_tiles;
+    g.L = (int32_t)M;
+    g.epi = EPI_F32;
+    g.out = C;
+    g.ldo = ldc;
+    g.n_valid = (int32_t)N;
+    g.m_valid = (int32_t)M;
+    g.partial = static_cast<float*>(workspace);
+    g.status = dghost::status_word();
+    g.K = K;
+    const int64_t slots_cap = need / ((size_t)BM * 512 * 4);
+    if (b_mn_major) {
+        const int bk = 32;
+        if (!tmap_2d(tm.a, 0, A, K, M, lda, bk, BM, 64)) return DG_ERR_CUDA;
+        if (!tmap_2d(tm.b0, 0, B, N, K, ldb, 64, bk, 128)) return DG_ERR_CUDA;
+        g.n_tiles = (int32_t)((N + 511) / 512);
+        g.k_blocks = (int32_t)((K + bk - 1) / bk);
+        const int64_t T = (int64_t)g.m_tiles * g.n_tiles;
+        g.splits = choose_splits(T, g.k_blocks, P, 256);
+        while (g.splits > 1 && T * g.splits > slots_cap) --g.splits;
+        return launch_gemm<PEprob>(tm.a, tm.b0, tm.b0, g, T * g.splits, st);
+    }
+    const int bk = 64;
+    if (!tmap_2d(tm.a, 0, A, K, M, lda, bk, BM, 128)) return DG_ERR_CUDA;
+    if (!tmap_2d(tm.b0, 0, B, K, N, ldb, bk, 256, 128)) return DG_ERR_CUDA;
+    g.n_tiles = (int32_t)((N + 255) / 256);
+    g.k_blocks = (int32_t)((K + bk - 1) / bk);
+    const int64_t T = (int64_t)g.m_tiles * g.n_tiles;
+    g.splits = choose_splits(T, g.k_blocks, P, 256);
+    while (g.splits > 1 && T * g.splits > slots_cap) --g.splits;
+    return launch_gemm<Down>(tm.a, tm.b0, tm.b0, g, T * g.splits, st);
+}
+
+}  // extern "C"

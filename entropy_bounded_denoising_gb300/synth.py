@@ -21,7 +21,6 @@ reproducible) streams, and a test always hands the same bytes to both sides.
 from __future__ import annotations
 
 import dataclasses
-import struct
 
 import numpy as np
 import torch
@@ -66,6 +65,10 @@ WORKLOADS = {
     "sweep": Workload("sweep", 64, 256, 262144, 4096, 16384, "bf16", (0.5, 12.0), 3, steps=64),
     "ragged": Workload("ragged", 32, 256, 152064, 3584, 18944, "bf16", (0.5, 12.0), 4,
                        full_loop=False, steps=64),
+    # reduced case for profiler captures: the batched kernels' shapes with half the
+    # vocabulary and half the canvases (inputs still larger than L2, ~1.5 GB on the device)
+    "profile": Workload("profile", 4, 256, 131072, 4096, 16384, "bf16", (0.5, 12.0), 5,
+                        spike_frac=0.10, full_loop=False, steps=64),
 }
 
 
@@ -129,6 +132,9 @@ def canvas_params(wl: Workload, step: int = 0):
     elif wl.name == "batched":
         p["beta"][:] = rng.uniform(4.0, 16.0, n); p["tau"][:] = 0.3; p["k"][:] = 2
         p["max_steps"][:] = 64; p["flags"][:] = ACTIVE | SELF_COND
+    elif wl.name == "profile":
+        p["beta"][:] = rng.uniform(4.0, 16.0, n); p["tau"][:] = 0.3; p["k"][:] = 2
+        p["max_steps"][:] = 64; p["flags"][:] = ACTIVE | SELF_COND
     elif wl.name == "sweep":
         p["beta"][:] = 8.0; p["tau"][:] = 0.3; p["k"][:] = 3; p["max_steps"][:] = 64
     elif wl.name == "ragged":
@@ -154,18 +160,6 @@ def params_with(base: dict, **kw) -> dict:
     for k, v in kw.items():
         out[k] = np.broadcast_to(np.asarray(v, dtype=out[k].dtype), out[k].shape).copy()
     return out
-
-
-PARAM_FIELDS = ("temperature", "beta", "tau", "k", "max_steps", "min_accept", "step",
-                "request_id", "flags")
-_PARAM_FMT = "<fffiiiiII"   # 36 bytes, the dg_canvas_params record
-
-
-def pack_params(p: dict) -> bytes:
-    """Pack a parameter dict into the dg_canvas_params byte layout (host bytes)."""
-    n = len(p["flags"])
-    return b"".join(struct.pack(_PARAM_FMT, *(p[f][i].item() for f in PARAM_FIELDS))
-                    for i in range(n))
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:

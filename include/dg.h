@@ -1,0 +1,287 @@
+/*
+ * dg.h -- C ABI of libdg, the GB300 (sm_103a) entropy-bounded denoising step of a
+ * block-diffusion language model with fixed-length canvases.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [DG]  "DiffusionGemma: vLLM이 네이티브로 지원하는 최초의 디퓨전 언어 모델(dLLM)"
+ *         (discuss.pytorch.kr):
+ *           - "엔트로피 기반 디노이징" (entropy-based denoising): every step resamples all
+ *             canvas positions, keeps the confident ones and renoises the rest; the
+ *             entropy H(p) = -sum_i p_i log p_i; the entropy-bound acceptance rule; the
+ *             convergence rule (argmax unchanged for several steps AND mean entropy below
+ *             a threshold, or the step cap), after which the argmax canvas is committed.
+ *           - "자기 조건화" (self-conditioning): the previous step's softmax becomes a
+ *             probability-weighted mean of token embeddings, goes through a small gated
+ *             MLP and is added to the next pass's canvas embeddings; zero for the encoder
+ *             prefill and commit passes.
+ *           - "DiffusionGemmaModelState와 DiffusionSampler": the Prefill case (random
+ *             canvas), the Denoise case (logits / T, Gumbel-max candidates
+ *             argmax(logits / T + g), entropy-bound acceptance, renoise, argmax canvas,
+ *             convergence check) and the per-request state kept in pre-allocated GPU
+ *             tensors updated in place.
+ *   [SPR] "답은 한 번 읽는데 모델은 왜 두 번 돌까? DiffusionGemma의 실행 경로 합치기":
+ *         read-only requests take a single denoising pass and only read probabilities
+ *         (diffusion_read_only with diffusion_max_steps = 1).
+ *   [PHX] Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+ *         SC'11 (Philox-4x32, 10 rounds).
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked (device) are device pointers owned by the caller; the library never
+ *     allocates, frees or keeps them.  Pointers marked (host) are read during the call.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ *     and is asynchronous: outputs are valid once the stream has reached the call.
+ *   - The return value reports host-side validation and launch errors only.  On a
+ *     validation error nothing is launched and no output is touched.  Problems found in
+ *     device data (NaN / +inf logits, all -inf rows, an expired bounded wait) set bits in
+ *     a device status word, read with dg_get_device_status().  Kernels never trap.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - Layouts are row-major.  "[n][L]" means canvas-major, position-minor, contiguous.
+ *   - Kernels are compiled for sm_103a only; on another device every launch returns
+ *     DG_ERR_CUDA.
+ */
+#ifndef DG_H
+#define DG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported entry points (the library is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define DG_API __attribute__((visibility("default")))
+#else
+#define DG_API
+#endif
+
+typedef struct CUstream_st* dg_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    DG_OK = 0,
+    DG_ERR_INVALID_ARG = -1, /* null pointer, size out of range, bad dtype            */
+    DG_ERR_ALIGNMENT = -2,   /* a pointer or row stride breaks the alignment rules    */
+    DG_ERR_WORKSPACE = -3,   /* workspace null or smaller than *_workspace_bytes()    */
+    DG_ERR_UNSUPPORTED = -4, /* shape outside what the kernels handle (see each call) */
+    DG_ERR_CUDA = -5         /* a CUDA runtime call or launch failed                  */
+} dg_status;
+
+typedef enum { DG_BF16 = 0, DG_FP32 = 1 } dg_dtype;
+
+/* Per-canvas flags. */
+enum {
+    DG_ACTIVE = 1u,    /* the canvas takes part in this step; clear = already converged:
+                          its logits are never read and none of its outputs is written  */
+    DG_READ_ONLY = 2u, /* single-pass read [SPR]: statistics only (entropy, lse, argmax);
+                          nothing accepted, canvas unchanged, converged = 1              */
+    DG_SELF_COND = 4u  /* compute the self-conditioning feedback for this canvas [DG]    */
+};
+
+/* Bits of the device status word. */
+enum {
+    DG_DEV_NAN_INF_ROW = 1u, /* a row held NaN or +inf logits; its outputs are unspecified */
+    DG_DEV_EMPTY_ROW = 2u,   /* a row was all -inf; its outputs are unspecified           */
+    DG_DEV_TIMEOUT = 4u,     /* a bounded wait inside a kernel expired; outputs of that
+                                launch are unspecified and the context stays usable       */
+    DG_DEV_BAD_PARAM = 8u    /* a per-canvas parameter was out of range (T <= 0, k < 1,
+                                max_steps < 1, min_accept outside 0..L); that canvas is
+                                skipped                                                   */
+};
+
+/* Per-canvas parameters, one 36-byte record per canvas, in device memory.
+ * The Philox key for a canvas is (lo32(seed), request_id); the counter is
+ * (block, position, step, stream | bits 32..55 of seed << 8) with stream 0 = Gumbel noise,
+ * 1 = renoise tokens, 2 = canvas initialisation [PHX]. */
+typedef struct {
+    float temperature;   /* T > 0: logits are scaled by 1/T [DG Denoise case]            */
+    float beta;          /* entropy budget in nats [DG entropy-bound rule]                */
+    float tau;           /* mean-entropy threshold in nats [DG convergence rule]          */
+    int32_t k;           /* consecutive unchanged argmax steps required, >= 1             */
+    int32_t max_steps;   /* step cap S >= 1: converged once step + 1 >= S                 */
+    int32_t min_accept;  /* positions accepted even when the budget allows none (0..L)    */
+    int32_t step;        /* 0-based index of this denoising step for the canvas           */
+    uint32_t request_id; /* second Philox key word                                        */
+    uint32_t flags;      /* DG_ACTIVE | DG_READ_ONLY | DG_SELF_COND                        */
+} dg_canvas_params;
+
+/* ------------------------------------------------------------------------------------ */
+/* Denoise step [DG "엔트로피 기반 디노이징", "DiffusionGemmaModelState와 DiffusionSampler"]. */
+/* ------------------------------------------------------------------------------------ */
+
+/* Workspace needed by dg_denoise_step (currently 0: all reductions stay on chip). */
+DG_API size_t dg_denoise_workspace_bytes(int64_t n_canvas, int32_t L, int64_t V, dg_dtype dtype);
+
+/* One denoising step for n_canvas canvases of L positions over a vocabulary of V.
+ *
+ * For each position of each DG_ACTIVE canvas, with y = logits / T:
+ *   entropy = H(softmax(y)) = -sum p log p (nats), lse = log sum exp(y),
+ *   argmax  = smallest v with logits[v] = max (the raw logits),
+ *   sample  = smallest v maximising y_v + g_v, g_v = -log(-log u_v) Gumbel noise from
+ *             Philox stream 0 with block = v / 4, word = v % 4, and
+ *             u = (floor(w / 2^9) + 1/2) / 2^23.
+ * Then per canvas: positions are ordered by (entropy, position) ascending and accepted
+ * while the running sum of their entropies stays <= beta (at least min_accept, at most L);
+ * accepted positions take their sample, the others a uniform token over [0, V) from
+ * Philox stream 1 (block 0, token = floor((w0 << 32 | w1) * V / 2^64)).  Convergence:
+ * stable_count becomes stable_count + 1 when the whole argmax canvas equals prev_argmax,
+ * else 0; the canvas converges when (stable_count >= k and mean entropy < tau) or
+ * step + 1 >= max_steps; prev_argmax is then overwritten with argmax.  DG_READ_ONLY canvases compute entropy,
+ * lse and argmax only (sample = -1, accept_mask = 0, canvas unchanged, converged = 1).
+ *
+ *   logits        (device) [n_canvas][L][ld] of dtype; 16-byte aligned; ld >= V and
+ *                 ld * sizeof(dtype) a multiple of 16.  Columns V..ld-1 are never read.
+ *   params        (device) [n_canvas] dg_canvas_params.
+ *   seed          Philox seed (low 32 bits = key word 0, bits 32..55 in the counter).
+ *   canvas        (device, in/out) [n_canvas][L] int32: the next canvas, written in place.
+ *   prev_argmax   (device, in/out) [n_canvas][L] int32: previous argmax canvas; -1 = none.
+ *   stable_count  (device, in/out) [n_canvas] int32.
+ *   accept_mask   (device, out) [n_canvas][L] uint8 (1 = accepted).
+ *   argmax, sample(device, out) [n_canvas][L] int32.
+ *   entropy, lse  (device, out) [n_canvas][L] float.
+ *   converged     (device, out) [n_canvas] uint8.
+ *   mean_entropy  (device, out, may be NULL) [n_canvas] float.
+ *   n_accept      (device, out, may be NULL) [n_canvas] int32.
+ *   workspace     may be NULL when dg_denoise_workspace_bytes() is 0.
+ * Limits: 1 <= L <= 1024, 2 <= V < 2^31, n_canvas >= 0 (0 launches nothing), and
+ * V * sizeof(dtype) <= 1.5 MiB (else DG_ERR_UNSUPPORTED).
+ * Errors: DG_ERR_INVALID_ARG (null required pointer, sizes), DG_ERR_ALIGNMENT,
+ * DG_ERR_UNSUPPORTED, DG_ERR_CUDA. */
+DG_API dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld,
+                          int64_t n_canvas, int32_t L, int64_t V,
+                          const dg_canvas_params* params, uint64_t seed,
+                          int32_t* canvas, int32_t* prev_argmax, int32_t* stable_count,
+                          uint8_t* accept_mask, int32_t* argmax, int32_t* sample,
+                          float* entropy, float* lse, uint8_t* converged,
+                          float* mean_entropy, int32_t* n_accept,
+                          void* workspace, size_t workspace_bytes, dg_stream_t stream);
+
+/* The per-canvas half of the step (acceptance, renoise, convergence) on caller-given
+ * per-position entropy, sample and argmax, all (device) [n_canvas][L].  Same semantics and
+ * outputs as dg_denoise_step; used to test the acceptance rule on chosen entropies. */
+DG_API dg_status dg_accept_from_entropy(const float* entropy, const int32_t* sample,
+                                 const int32_t* argmax, int64_t n_canvas, int32_t L, int64_t V,
+                                 const dg_canvas_params* params, uint64_t seed,
+                                 int32_t* canvas, int32_t* prev_argmax, int32_t* stable_count,
+                                 uint8_t* accept_mask, uint8_t* converged,
+                                 float* mean_entropy, int32_t* n_accept, dg_stream_t stream);
+
+/* Prefill case [DG "DiffusionGemmaModelState와 DiffusionSampler"]: fill every DG_ACTIVE
+ * canvas with uniform tokens over [0, V) from Philox stream 2 (block 0, counter step =
+ * params.step).  canvas (device, out) [n_canvas][L] int32.  Same limits as above. */
+DG_API dg_status dg_canvas_init(int32_t* canvas, int64_t n_canvas, int32_t L, int64_t V,
+                         const dg_canvas_params* params, uint64_t seed, dg_stream_t stream);
+
+/* Between steps of a loop: for every canvas, clear DG_ACTIVE when converged[c] is 1 and
+ * advance step by one otherwise (the canvas then commits its argmax [DG convergence
+ * rule]).  params (device, in/out) [n_canvas]; converged (device) [n_canvas]. */
+DG_API dg_status dg_advance_params(dg_canvas_params* params, const uint8_t* converged,
+                            int64_t n_canvas, dg_stream_t stream);
+
+/* ------------------------------------------------------------------------------------ */
+/* Self-conditioning [DG "자기 조건화"]:                                                  */
+/*   pe    = P . E,  P = softmax(logits / T) per position, E the token embedding table;  */
+/*   delta = W_down (gelu_tanh(W_gate pe) * (W_up pe)), no bias (gated MLP).            */
+/* Computed on the tensor cores (tcgen05, bf16 operands, fp32 accumulation); P is formed */
+/* tile by tile in shared memory from the logits and the step's lse, never in HBM.      */
+/* ------------------------------------------------------------------------------------ */
+
+/* Workspace for dg_self_cond_logits with these sizes (bytes, 256-byte aligned use). */
+DG_API size_t dg_self_cond_workspace_bytes(int64_t n_canvas, int32_t L, int32_t d, int32_t h);
+
+/* delta_emb for every position of every canvas with DG_ACTIVE and DG_SELF_COND set, not
+ * DG_READ_ONLY and not converged in this step; all other rows of delta_emb are set to 0
+ * (the feedback is zero for the prefill and commit passes [DG "자기 조건화"]).
+ *   logits    (device) [n_canvas][L][ld] as in dg_denoise_step.
+ *   lse       (device) [n_canvas][L] float: the lse output of dg_denoise_step for these
+ *             logits and parameters.
+ *   params    (device) [n_canvas]; converged (device) [n_canvas] uint8 (may be NULL =
+ *             none converged).
+ *   E         (device) bf16 [V][d] token embeddings; W_gate, W_up (device) bf16 [h][d];
+ *             W_down (device) bf16 [d][h] (row = output unit).  All 16-byte aligned.
+ *   delta_emb (device, out) bf16 [n_canvas][L][d].
+ * Limits: d and h multiples of 8 in [8, 65536]; L <= 1024; V as in dg_denoise_step.
+ * Errors: DG_ERR_INVALID_ARG, DG_ERR_ALIGNMENT, DG_ERR_WORKSPACE, DG_ERR_CUDA. */
+DG_API dg_status dg_self_cond_logits(const void* logits, dg_dtype dtype, int64_t ld, const float* lse,
+                              const dg_canvas_params* params, const uint8_t* converged,
+                              int64_t n_canvas, int32_t L, int64_t V, int32_t d, int32_t h,
+                              const uint16_t* E, const uint16_t* W_gate, const uint16_t* W_up,
+                              const uint16_t* W_down, uint16_t* delta_emb,
+                              void* workspace, size_t workspace_bytes, dg_stream_t stream);
+
+/* The three stages dg_self_cond_logits runs, exposed so a caller can place events or work
+ * between them.  They must be called in this order, on one stream, with one workspace
+ * (sized by dg_self_cond_workspace_bytes) and the same n_canvas, L, d and h:
+ *   dg_self_cond_prepare: selects the canvases whose feedback is computed this step
+ *                         (the list lives in the workspace) and zeroes the delta_emb rows
+ *                         of all others;
+ *   dg_self_cond_pe:      pe = softmax(logits / T) . E for the selected canvases, into the
+ *                         workspace (the tensor-core contraction over the vocabulary);
+ *   dg_self_cond_mlp:     delta_emb rows of the selected canvases from pe.
+ * Arguments, limits and errors are those of dg_self_cond_logits. */
+DG_API dg_status dg_self_cond_prepare(const dg_canvas_params* params, const uint8_t* converged,
+                                      int64_t n_canvas, int32_t L, int32_t d, int32_t h,
+                                      uint16_t* delta_emb, void* workspace, size_t workspace_bytes,
+                                      dg_stream_t stream);
+DG_API dg_status dg_self_cond_pe(const void* logits, dg_dtype dtype, int64_t ld, const float* lse,
+                                 const dg_canvas_params* params, int64_t n_canvas, int32_t L,
+                                 int64_t V, int32_t d, int32_t h, const uint16_t* E,
+                                 void* workspace, size_t workspace_bytes, dg_stream_t stream);
+DG_API dg_status dg_self_cond_mlp(int64_t n_canvas, int32_t L, int32_t d, int32_t h,
+                                  const uint16_t* W_gate, const uint16_t* W_up,
+                                  const uint16_t* W_down, uint16_t* delta_emb, void* workspace,
+                                  size_t workspace_bytes, dg_stream_t stream);
+
+/* Workspace for dg_self_cond_probs. */
+DG_API size_t dg_self_cond_probs_workspace_bytes(int64_t n_rows, int32_t d, int32_t h);
+
+/* The same feedback from caller-given probability rows (each row sums to 1):
+ *   P (device) bf16 [n_rows][ld], ld >= V, ld * 2 a multiple of 16; delta_emb (device, out)
+ *   bf16 [n_rows][d].  E and W as above. */
+DG_API dg_status dg_self_cond_probs(const uint16_t* P, int64_t ld, int64_t n_rows, int64_t V,
+                             int32_t d, int32_t h, const uint16_t* E, const uint16_t* W_gate,
+                             const uint16_t* W_up, const uint16_t* W_down, uint16_t* delta_emb,
+                             void* workspace, size_t workspace_bytes, dg_stream_t stream);
+
+/* The tensor-core GEMM engine behind the self-conditioning on plain operands:
+ *   C[m][n] = sum_k A[m][k] * B(k, n), fp32 out, with B(k, n) = B[n][k] when b_mn_major = 0
+ *   (B stored [N][K]) and B[k][n] when b_mn_major = 1 (B stored [K][N]).
+ *   A (device) bf16 [M][lda]; B (device) bf16; C (device, out) float [M][ldc].
+ *   lda, ldb multiples of 8; all pointers 16-byte aligned.  Workspace from
+ *   dg_gemm_workspace_bytes(M, N). */
+DG_API size_t dg_gemm_workspace_bytes(int64_t M, int64_t N);
+DG_API dg_status dg_gemm_bf16(const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                       int b_mn_major, float* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                       void* workspace, size_t workspace_bytes, dg_stream_t stream);
+
+/* ------------------------------------------------------------------------------------ */
+/* Random numbers and status.                                                          */
+/* ------------------------------------------------------------------------------------ */
+
+/* Philox-4x32-10 words [PHX] for counters (block0 + b, position, step, stream | seed bits),
+ * b = 0..n_blocks-1, key (lo32(seed), request_id): out (device) uint32 [n_blocks][4]. */
+DG_API dg_status dg_philox_words(uint64_t seed, uint32_t request_id, uint32_t step, uint32_t position,
+                          uint32_t stream_id, uint32_t block0, int64_t n_blocks, uint32_t* out,
+                          dg_stream_t stream);
+
+/* Synchronises `stream`, then returns the device status word of the current device in
+ * *status (DG_DEV_* bits accumulated since the last clear). */
+DG_API dg_status dg_get_device_status(dg_stream_t stream, uint32_t* status);
+
+/* Synchronises `stream` and clears the status word of the current device. */
+DG_API dg_status dg_clear_device_status(dg_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+DG_API const char* dg_status_string(dg_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+DG_API int32_t dg_version(void);
+
+/* Number of kernel launches the library has enqueued in this process so far (all devices). */
+DG_API uint64_t dg_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_H */

@@ -1,0 +1,73 @@
+"""The C ABI: the library builds for sm_103a on this host (cross-compiled), loads, and
+exports every entry point include/dg.h declares; host-side validation rejects bad
+arguments without touching the GPU."""
+import os
+import re
+
+import pytest
+
+import entropy_bounded_denoising_gb300 as dg
+from entropy_bounded_denoising_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    txt = open(os.path.join(ROOT, "include", "dg.h")).read()
+    return sorted(set(re.findall(r"^DG_API [^()]*?\b(dg_\w+)\(", txt, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("dg_denoise_step", "dg_self_cond_logits", "dg_self_cond_probs",
+                     "dg_canvas_init", "dg_accept_from_entropy", "dg_get_device_status"):
+        assert required in names
+
+
+def test_library_builds_loads_and_exports_all():
+    build.build()
+    lib = dg.load()
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert dg.version() >= 100
+    assert dg.status_string(dg.DG_ERR_WORKSPACE) == "DG_ERR_WORKSPACE"
+
+
+def test_host_validation_without_gpu():
+    lib = dg.load()
+    # null / out-of-range arguments are refused before any CUDA call
+    assert lib.dg_denoise_step(None, 0, 8, 1, 16, 8, None, 0, *([None] * 11), None, 0, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_denoise_step(None, 0, 8, 1, 0, 8, None, 0, *([None] * 11), None, 0, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_denoise_step(None, 0, 8, 1, 2000, 8, None, 0, *([None] * 11), None, 0, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_denoise_step(None, 7, 8, 1, 16, 8, None, 0, *([None] * 11), None, 0, None) == dg.DG_ERR_INVALID_ARG
+    # ld < V
+    assert lib.dg_denoise_step(16, 0, 4, 1, 16, 8, 16, 0, *([16] * 11), None, 0, None) == dg.DG_ERR_INVALID_ARG
+    # misaligned logits / row stride
+    assert lib.dg_denoise_step(18, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), None, 0, None) == dg.DG_ERR_ALIGNMENT
+    assert lib.dg_denoise_step(16, 0, 12, 1, 16, 12, 16, 0, *([16] * 11), None, 0, None) == dg.DG_ERR_ALIGNMENT
+    # a row that does not fit the on-chip plan
+    assert lib.dg_denoise_step(16, 1, 1 << 20, 1, 16, 1 << 20, 16, 0, *([16] * 11), None, 0, None) == dg.DG_ERR_UNSUPPORTED
+    # empty batch is a no-op
+    assert lib.dg_denoise_step(None, 0, 8, 0, 16, 8, None, 0, *([None] * 11), None, 0, None) == dg.DG_OK
+    assert lib.dg_denoise_workspace_bytes(8, 256, 262144, 0) == 0
+    # self-conditioning: sizes and alignment
+    assert lib.dg_self_cond_logits(16, 0, 64, 16, 16, None, 1, 16, 64, 12, 128, 16, 16, 16, 16, 16, 16, 1 << 30, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_self_cond_logits(16, 0, 64, 16, 16, None, 1, 16, 64, 64, 128, 18, 16, 16, 16, 16, 16, 1 << 30, None) == dg.DG_ERR_ALIGNMENT
+    assert lib.dg_self_cond_probs(16, 64, 4, 64, 64, 128, 16, 16, 16, 16, 16, None, 0, None) == dg.DG_ERR_WORKSPACE
+    assert lib.dg_gemm_bf16(16, 8, 16, 8, 0, 16, 8, 4, 4, 0, None, 0, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_philox_words(0, 0, 0, 0, 300, 0, 4, 16, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_canvas_init(None, 1, 16, 8, None, 0, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_advance_params(None, None, -1, None) == dg.DG_ERR_INVALID_ARG
+
+
+def test_params_record_layout():
+    import numpy as np
+    p = {"temperature": np.float32([0.5]), "beta": np.float32([2.0]), "tau": np.float32([0.25]),
+         "k": np.int32([3]), "max_steps": np.int32([9]), "min_accept": np.int32([1]),
+         "step": np.int32([4]), "request_id": np.uint32([77]), "flags": np.uint32([5])}
+    raw = dg.pack_params(p)
+    assert len(raw) == dg.PARAM_BYTES == 36
+    import torch
+    back = dg.unpack_params(torch.frombuffer(bytearray(raw), dtype=torch.uint8))
+    for k, v in p.items():
+        assert back[k][0] == v[0]

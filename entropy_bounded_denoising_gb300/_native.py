@@ -68,6 +68,7 @@ def load(path: str | None = None):
         "dg_self_cond_probs": (st, [P, i64, i64, i64, i32, i32, P, P, P, P, P, P, sz, P]),
         "dg_gemm_workspace_bytes": (sz, [i64, i64]),
         "dg_gemm_bf16": (st, [P, i64, P, i64, ctypes.c_int, P, i64, i64, i64, i64, P, sz, P]),
+        "dg_gemm_bf16_noalloc": (st, [P, i64, P, i64, ctypes.c_int, P, i64, i64, i64, i64, P]),
         "dg_philox_words": (st, [u64, u32, u32, u32, u32, u32, i64, P, P]),
         "dg_get_device_status": (st, [P, ctypes.POINTER(u32)]),
         "dg_clear_device_status": (st, [P]),
@@ -90,6 +91,7 @@ def exported_symbols() -> list[str]:
                         "dg_self_cond_logits", "dg_self_cond_prepare", "dg_self_cond_pe",
                         "dg_self_cond_mlp", "dg_self_cond_probs_workspace_bytes",
                         "dg_self_cond_probs", "dg_gemm_workspace_bytes", "dg_gemm_bf16",
+                        "dg_gemm_bf16_noalloc",
                         "dg_philox_words", "dg_get_device_status", "dg_clear_device_status",
                         "dg_status_string", "dg_version", "dg_launch_count") if hasattr(lib, n)]
 
@@ -301,6 +303,18 @@ def dg_gemm_bf16(A, B, C, b_mn_major: bool, workspace, *, M=None, N=None, K=None
                              C.stride(0), M, N, K, _p(workspace), ws_bytes, _s(stream))
     if check:
         _check("dg_gemm_bf16", rc)
+    return rc
+
+
+def dg_gemm_bf16_noalloc(A, B, C, b_mn_major: bool, *, M=None, N=None, K=None, stream=None,
+                         check=True) -> int:
+    M = A.shape[0] if M is None else M
+    K = A.shape[1] if K is None else K
+    N = (B.shape[1] if b_mn_major else B.shape[0]) if N is None else N
+    rc = load().dg_gemm_bf16_noalloc(_p(A), A.stride(0), _p(B), B.stride(0), int(bool(b_mn_major)), _p(C),
+                                     C.stride(0), M, N, K, _s(stream))
+    if check:
+        _check("dg_gemm_bf16_noalloc", rc)
     return rc
 
 

@@ -26,6 +26,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "dg_common.cuh"
 
@@ -944,3 +945,78 @@ dg_status dg_gemm_bf16(const uint16_t* A, int64_t lda, const uint16_t* B, int64_
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ no-allocation GEMM
+// dg_gemm_bf16_noalloc keeps its split-K partial tiles in this file-scope array instead of a
+// caller workspace, for callers that cannot allocate device memory.  Every device that loads
+// the library holds the array until the process exits.  Host code must not hand the symbol
+// itself to a kernel (on the host it is only a stand-in): the device address is looked up
+// once per device with cudaGetSymbolAddress and passed to the kernels.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DG_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of the scratch array for the current device (looked up on first use).
+dg_status noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DG_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return DG_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return DG_OK;
+}
+}  // namespace
+
+extern "C" dg_status dg_gemm_bf16_noalloc(const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                                          int b_mn_major, float* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                          dg_stream_t stream) {
+    if (M < 0 || N < 0 || K < 0 || M > (1LL << 24) || N > (1LL << 24) || K > 0x7fffffffLL) return DG_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return DG_OK;
+    if (K == 0 || !A || !B || !C || lda < K || ldc < N) return DG_ERR_INVALID_ARG;
+    if (b_mn_major ? ldb < N : ldb < K) return DG_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || (lda % 8) || (ldb % 8)) return DG_ERR_ALIGNMENT;
+    const int P = dghost::sm_count();
+    if (P <= 0) return DG_ERR_CUDA;
+    // the same tiling and k-slices as dg_gemm_bf16, so the two give identical results
+    const int bn = b_mn_major ? 512 : 256;
+    const int bk = b_mn_major ? 32 : 64;
+    GemmArgs g{};
+    g.m_tiles = (int32_t)((M + BM - 1) / BM);
+    g.tpc = g.m_tiles;
+    g.L = (int32_t)M;
+    g.epi = EPI_F32;
+    g.out = C;
+    g.ldo = ldc;
+    g.n_valid = (int32_t)N;
+    g.m_valid = (int32_t)M;
+    g.status = dghost::status_word();
+    g.K = K;
+    g.n_tiles = (int32_t)((N + bn - 1) / bn);
+    g.k_blocks = (int32_t)((K + bk - 1) / bk);
+    const int64_t T = (int64_t)g.m_tiles * g.n_tiles;
+    const int64_t slots_cap = (int64_t)(dg_gemm_workspace_bytes(M, N) / ((size_t)BM * 512 * 4));
+    g.splits = choose_splits(T, g.k_blocks, P, 256);
+    while (g.splits > 1 && T * g.splits > slots_cap) --g.splits;
+    const size_t need = g.splits > 1 ? (size_t)T * g.splits * BM * bn * 4 : 0;
+    if (need > (size_t)DG_NOALLOC_SCRATCH_BYTES) return DG_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    dg_status s = noalloc_scratch(&scratch);
+    if (s != DG_OK) return s;
+    g.partial = static_cast<float*>(scratch);
+    cudaStream_t st = (cudaStream_t)stream;
+    TMaps tm;
+    if (b_mn_major) {
+        if (!tmap_2d(tm.a, 0, A, K, M, lda, bk, BM, 64)) return DG_ERR_CUDA;
+        if (!tmap_2d(tm.b0, 0, B, N, K, ldb, 64, bk, 128)) return DG_ERR_CUDA;
+        return launch_gemm<PEprob>(tm.a, tm.b0, tm.b0, g, T * g.splits, st);
+    }
+    if (!tmap_2d(tm.a, 0, A, K, M, lda, bk, BM, 128)) return DG_ERR_CUDA;
+    if (!tmap_2d(tm.b0, 0, B, K, N, ldb, bk, 256, 128)) return DG_ERR_CUDA;
+    return launch_gemm<Down>(tm.a, tm.b0, tm.b0, g, T * g.splits, st);
+}

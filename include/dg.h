@@ -254,6 +254,28 @@ DG_API dg_status dg_gemm_bf16(const uint16_t* A, int64_t lda, const uint16_t* B,
                        int b_mn_major, float* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
                        void* workspace, size_t workspace_bytes, dg_stream_t stream);
 
+/* dg_gemm_bf16 for callers that cannot allocate device memory (no counterpart in the
+ * method's description; this is a deployment aid).  Some callers may not call cudaMalloc at
+ * all: a plugin whose host program hands it only input and output buffers, or code on a
+ * path where an allocation (and the device synchronisation it can cause) is not allowed.
+ * This variant takes no workspace: its split-K partial tiles live in a fixed array of
+ * DG_NOALLOC_SCRATCH_BYTES (8 MiB) in the library's device memory, which every GPU that
+ * loads the library keeps until the process exits.  The call itself allocates nothing.
+ *   - Arguments, layouts, tiling and results are those of dg_gemm_bf16 (the same k-slices,
+ *     so the same sums); only the workspace is gone.
+ *   - Problems whose partial tiles need more than DG_NOALLOC_SCRATCH_BYTES are rejected with
+ *     DG_ERR_UNSUPPORTED before anything is launched (use dg_gemm_bf16 for those).
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream capture.
+ *   - Nothing in the array needs to start at zero: each partial tile is written in full
+ *     before it is read.  All calls share the one array and it keeps the last call's
+ *     contents, so calls that overlap on the GPU (other streams, other host threads) race:
+ *     serialise them. */
+#define DG_NOALLOC_SCRATCH_BYTES (8u << 20)
+DG_API dg_status dg_gemm_bf16_noalloc(const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                                      int b_mn_major, float* C, int64_t ldc, int64_t M, int64_t N,
+                                      int64_t K, dg_stream_t stream);
+
 /* ------------------------------------------------------------------------------------ */
 /* Random numbers and status.                                                          */
 /* ------------------------------------------------------------------------------------ */

@@ -121,6 +121,27 @@ DG_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return false;
 }
 
+// Whole-warp wait: lane 0 polls, the warp then synchronises (which also orders the data the
+// barrier guards for the other lanes).  Keeps 31 lanes from hammering shared memory.
+// Must be called by all 32 lanes, converged.  `sleep_ns` > 0 backs off between polls for
+// waits that are off the critical path.
+DG_DEVINL bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t sleep_ns = 0) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        ok = 0;
+        for (uint32_t i = 0; i < kWaitPolls; ++i) {
+            if (mbar_try_wait(bar, parity)) {
+                ok = 1;
+                break;
+            }
+            if (sleep_ns) __nanosleep(sleep_ns);
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
 // ------------------------------------------------------------------ bulk copies (TMA)
 // Plain bulk copy global -> shared; both addresses 16-byte aligned, bytes % 16 == 0.
 DG_DEVINL void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -136,6 +157,16 @@ DG_DEVINL void tma_load_2d(void* dst, const void* tmap, int32_t c0, int32_t c1, 
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
         "[%4];" ::"r"(smem_u32(dst)),
         "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Multicast: the box lands at the same shared-memory offset in every CTA of `mask`, and each
+// of those CTAs' mbarrier at `bar`'s offset receives the byte count.
+DG_DEVINL void tma_load_2d_mc(void* dst, const void* tmap, int32_t c0, int32_t c1, uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
+        "[%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask)
         : "memory");
 }
 
@@ -183,6 +214,15 @@ DG_DEVINL void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uin
 DG_DEVINL void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
+}
+
+// As tc_commit, arriving on the mbarrier at `bar`'s offset in every CTA of `mask`.
+DG_DEVINL void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets lane (base + t).

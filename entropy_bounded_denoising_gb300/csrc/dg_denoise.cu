@@ -10,31 +10,27 @@
 // canvases follow the single-pass-reads page ("답은 한 번 읽는데 모델은 왜 두 번 돌까?"):
 // one pass, statistics only.
 //
-// K1 design (GB300): one thread-block cluster per canvas position.  Each CTA pulls its
-// slice of the logit row into shared memory with bulk copies (TMA engine) in pieces, so the
-// row is read from HBM exactly once; pass A folds the slice into an online-softmax state
-// (max m, count c of entries equal to m, r = sum of the other e^z, t = sum e^z z) -- the
-// split keeps near-one-hot rows accurate in fp32 -- plus the argmax; CTAs merge through
-// distributed shared memory in rank order (a reduction tree fixed by V alone, so a row's
-// result does not depend on the batch it came in).  Pass B draws the Gumbel noise only for
-// entries that can still win: an entry with z + G_max below the best score so far cannot,
-// and a cheap bound on u rejects most of the rest before the two logarithms.
-#include <cooperative_groups.h>
+// K1 design (GB300): one CTA per canvas position streams its logit row once from HBM.  A
+// producer warp keeps a ring of shared-memory slots filled with bulk copies (the TMA
+// engine); eight consumer warps fold every piece into an online-softmax state (max m,
+// count c of entries equal to m, r = sum of the other e^z, t = sum e^z z -- the split keeps
+// near-one-hot rows accurate in fp32) and the argmax, and in the same pass look for the
+// Gumbel-max winner: an entry whose y + G_max (G_max the largest Gumbel value the uniform
+// mapping can produce) cannot reach the best score seen so far in the CTA is skipped
+// without drawing its noise; the others are queued per warp and drawn 32 groups at a time.
+// The reduction order depends only on V, so a row's result does not depend on its batch.
 #include <cuda_runtime.h>
 
 #include <math.h>
 
 #include "dg_common.cuh"
 
-namespace cg = cooperative_groups;
-
 namespace {
 
-constexpr int kK1Threads = 256;
-constexpr int kK1Warps = kK1Threads / 32;
-constexpr int kMaxPieces = 8;
-constexpr int kMaxCluster = 8;
-constexpr uint32_t kMaxChunkBytes = 192u * 1024u;
+constexpr int kK1Warps = 8;                        // consumer warps
+constexpr int kK1Threads = (kK1Warps + 1) * 32;    // + one producer warp
+constexpr int kSlots = 4;                          // ring of shared-memory slots
+constexpr uint32_t kPieceBytes = 16384;            // bytes per slot
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Largest Gumbel value the uniform mapping can produce, -log(-log(1 - 2^-24)) = 16.6355...,
@@ -53,16 +49,15 @@ struct RowState {  // online softmax state of a set of entries, z measured in lo
 };
 
 struct K1Shared {
-    uint64_t bar[kMaxPieces];
+    uint64_t full[kSlots];
+    uint64_t empty[kSlots];
     RowState warp_state[kK1Warps];
-    RowState cta_state;  // read by the other CTAs of the cluster
-    RowState row_state;
     float warp_best[kK1Warps];
     int warp_bidx[kK1Warps];
-    float cta_best;  // read by the other CTAs of the cluster
-    int cta_bidx;
+    unsigned best_key;  // CTA-wide best score so far, order-preserving integer encoding
     int bad;
     int timeout;
+    int queue[kK1Warps][96];  // per-warp candidate groups awaiting their Gumbel draw
 };
 
 DG_DEVINL float ex2(float x) {
@@ -76,6 +71,15 @@ DG_DEVINL float max_nan(float a, float b) {
     float y;
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
     return y;
+}
+
+// Float <-> unsigned keys with the same order (for atomicMax on scores).
+DG_DEVINL unsigned float_key(float f) {
+    const unsigned b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+DG_DEVINL float key_float(unsigned k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 // Merge two states; k2 = log2e / T.  Sides whose max is below the new max are rescaled and
@@ -117,6 +121,22 @@ DG_DEVINL RowState shfl_state(RowState s, int lane_mask) {
 
 DG_DEVINL bool better(float s, int i, float bs, int bi) { return s > bs || (s == bs && i < bi); }
 
+DG_DEVINL uint32_t word_of(const dg::u4& w, int i) {
+    return i == 0 ? w.x : i == 1 ? w.y : i == 2 ? w.z : w.w;
+}
+
+DG_DEVINL void warp_best(float& best, int& bidx) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+        if (better(ob, oi, best, bidx)) {
+            best = ob;
+            bidx = oi;
+        }
+    }
+}
+
 template <int DT>
 struct Vec;  // 16 bytes of logits as floats
 
@@ -148,272 +168,292 @@ struct Vec<1> {  // fp32: 4 entries
     }
 };
 
+// Gumbel draw for one group of 4 consecutive entries (one Philox block), entries
+// [e0, e0 + 4) of the row held in `slot` from row entry `slot_e0` on.  Keeps (best, bidx)
+// as the largest score y + g, y = x / T, ties to the lower index.  `bound` is a score some
+// entry of the row is known to reach; entries that cannot reach it are not drawn.
+template <int DT>
+DG_DEVINL void eval_group(const unsigned char* slot, int slot_e0, int e0, int64_t V, float invT, uint32_t pos,
+                          uint32_t step, uint32_t c3, uint32_t k0, uint32_t k1, float bound, float& best,
+                          int& bidx) {
+    constexpr int ES = DT == 0 ? 2 : 4;
+    float x[4];
+    const unsigned char* p = slot + (size_t)(e0 - slot_e0) * ES;
+    if (DT == 0) {
+        const uint2 q = *reinterpret_cast<const uint2*>(p);
+        x[0] = __uint_as_float(q.x << 16);
+        x[1] = __uint_as_float(q.x & 0xffff0000u);
+        x[2] = __uint_as_float(q.y << 16);
+        x[3] = __uint_as_float(q.y & 0xffff0000u);
+    } else {
+        const float4 q = *reinterpret_cast<const float4*>(p);
+        x[0] = q.x;
+        x[1] = q.y;
+        x[2] = q.z;
+        x[3] = q.w;
+    }
+    const dg::u4 w = dg::philox10((uint32_t)e0 >> 2, pos, step, c3, k0, k1);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (e0 + i >= V) continue;
+        const float y = x[i] * invT;
+        const float b = fmaxf(bound, best);
+        if (!(y >= b - kGumbelMax - kCandidateSlack)) continue;
+        const float u = dg::uniform_from_word(word_of(w, i));
+        // g > D = b - y needs u > exp(-e^-D) >= 1 - e^-D; keep a factor 2 of slack
+        const float eb = 2.f * ex2(-(b - y) * kLog2e);
+        if (!(u > 1.f - eb)) continue;
+        const float score = y + (-logf(-logf(u)));
+        if (better(score, e0 + i, best, bidx)) {
+            best = score;
+            bidx = e0 + i;
+        }
+    }
+}
+
 // ------------------------------------------------------------------------------------
-// K1: per-position statistics and Gumbel-max sample.  grid (CS, L, n), cluster (CS, 1, 1).
+// K1: per-position statistics and Gumbel-max sample.  grid (L, n), one CTA per position.
 // ------------------------------------------------------------------------------------
 template <int DT>
-__global__ void __launch_bounds__(kK1Threads) k1_row_stats(
+__global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
     const unsigned char* __restrict__ logits, int64_t ld_bytes, int64_t V, int32_t L,
-    const dg_canvas_params* __restrict__ params, uint64_t seed, int32_t chunk_elems,
-    int32_t* __restrict__ argmax_out, int32_t* __restrict__ sample_out, float* __restrict__ entropy_out,
-    float* __restrict__ lse_out, unsigned* status) {
+    const dg_canvas_params* __restrict__ params, uint64_t seed, int32_t* __restrict__ argmax_out,
+    int32_t* __restrict__ sample_out, float* __restrict__ entropy_out, float* __restrict__ lse_out,
+    unsigned* status) {
     constexpr int VN = Vec<DT>::N;
     constexpr int ES = DT == 0 ? 2 : 4;
+    constexpr int GPV = VN / 4;                    // Philox blocks per 16-byte vector
+    constexpr int kPieceElems = kPieceBytes / ES;
     extern __shared__ __align__(128) unsigned char k1_smem[];
     K1Shared& sh = *reinterpret_cast<K1Shared*>(k1_smem);
-    unsigned char* chunk = k1_smem + ((sizeof(K1Shared) + 127) / 128) * 128;
+    unsigned char* ring = k1_smem + ((sizeof(K1Shared) + 127) / 128) * 128;
 
-    cg::cluster_group cluster = cg::this_cluster();
-    const int rank = (int)cluster.block_rank();
-    const int ncta = (int)cluster.num_blocks();
-    const int pos = blockIdx.y;
-    const int64_t canvas = blockIdx.z;
+    const int pos = blockIdx.x;
+    const int64_t canvas = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     const dg_canvas_params p = params[canvas];
-    if (!(p.flags & DG_ACTIVE)) return;  // whole cluster leaves together
+    if (!(p.flags & DG_ACTIVE)) return;
     if (!(p.temperature > 0.f) || !isfinite(p.temperature)) {
-        if (rank == 0 && tid == 0 && pos == 0) dg::raise_status(status, DG_DEV_BAD_PARAM);
+        if (tid == 0 && pos == 0) dg::raise_status(status, DG_DEV_BAD_PARAM);
         return;
     }
     const bool do_sample = !(p.flags & DG_READ_ONLY);
     const float invT = 1.0f / p.temperature;
     const float k2 = kLog2e * invT;
-
     const int64_t row = canvas * L + pos;
-    const int64_t begin = (int64_t)rank * chunk_elems;
-    const int64_t end = min(V, begin + (int64_t)chunk_elems);
-    const int n_el = (int)max((int64_t)0, end - begin);
-    const uint32_t bytes = (uint32_t)n_el * ES;
+    const unsigned char* src = logits + row * ld_bytes;
+    const uint32_t bytes = (uint32_t)(V * ES);
     const uint32_t bulk = bytes & ~15u;
-    const int nvec = (n_el + VN - 1) / VN;
-    const unsigned char* src = logits + row * ld_bytes + begin * ES;
-
-    int npieces = (int)((bytes + 8191u) / 8192u);
-    npieces = max(1, min(kMaxPieces, npieces));
-    const int vpp = (nvec + npieces - 1) / npieces;
+    const int npieces = (int)((bytes + kPieceBytes - 1) / kPieceBytes);
 
     if (tid == 0) {
-        for (int i = 0; i < npieces; ++i) dg::mbar_init(&sh.bar[i], 1);
+        for (int i = 0; i < kSlots; ++i) {
+            dg::mbar_init(&sh.full[i], 1);
+            dg::mbar_init(&sh.empty[i], kK1Warps);
+        }
         dg::fence_mbar_init();
         sh.bad = 0;
         sh.timeout = 0;
+        sh.best_key = float_key(-INFINITY);
     }
-    __syncthreads();
-    if (tid == 0) {
-        for (int i = 0; i < npieces; ++i) {
-            const uint32_t lo = (uint32_t)min(nvec, i * vpp) * 16u;
-            const uint32_t hi = min(bulk, (uint32_t)min(nvec, (i + 1) * vpp) * 16u);
-            if (hi > lo) {
-                dg::mbar_arrive_expect_tx(&sh.bar[i], hi - lo);
-                dg::bulk_g2s(chunk + lo, src + lo, hi - lo, &sh.bar[i]);
-            } else {
-                dg::mbar_arrive(&sh.bar[i]);
-            }
-        }
-    }
-    // ragged tail (< 16 bytes) by plain loads
-    if (tid < (int)(bytes - bulk)) chunk[bulk + tid] = src[bulk + tid];
     __syncthreads();
 
-    // ---------------- pass A: online softmax state and argmax
-    RowState st{-INFINITY, 0.f, 0.f, 0.f, 0x7fffffff};
-    bool bad = false;
-    for (int pc = 0; pc < npieces; ++pc) {
-        if (!dg::mbar_wait(&sh.bar[pc], 0)) {
-            sh.timeout = 1;
-            break;
+    if (warp == kK1Warps) {
+        // ---------------- producer: keep the ring full
+        if (lane == 0) {
+            for (int q = 0; q < npieces; ++q) {
+                const int sl = q % kSlots;
+                if (q >= kSlots && !dg::mbar_wait(&sh.empty[sl], (uint32_t)((q / kSlots) - 1) & 1u)) {
+                    sh.timeout = 1;
+                    break;
+                }
+                unsigned char* dst = ring + (size_t)sl * kPieceBytes;
+                const uint32_t lo = (uint32_t)q * kPieceBytes;
+                const uint32_t hi = min(bytes, lo + kPieceBytes);
+                const uint32_t bhi = min(bulk, hi);
+                // the ragged tail (< 16 bytes) by plain copies, ordered before the arrive below
+                for (uint32_t b = max(bulk, lo); b < hi; ++b) dst[b - lo] = src[b];
+                dg::mbar_arrive_expect_tx(&sh.full[sl], bhi > lo ? bhi - lo : 0u);
+                if (bhi > lo) dg::bulk_g2s(dst, src + lo, bhi - lo, &sh.full[sl]);
+            }
+            if (sh.timeout) {  // never leave with a copy still landing in shared memory
+                for (int i = 0; i < kSlots; ++i) (void)dg::mbar_wait(&sh.full[i], 0);
+                for (int i = 0; i < kSlots; ++i) (void)dg::mbar_wait(&sh.full[i], 1);
+            }
         }
-        const int vlo = pc * vpp, vhi = min(nvec, vlo + vpp);
-        for (int j = vlo + tid; j < vhi; j += kK1Threads) {
-            float x[VN];
-            Vec<DT>::load(chunk + (size_t)j * 16, x);
-            const int base = j * VN;
-            if (base + VN > n_el) {
-#pragma unroll
-                for (int i = 0; i < VN; ++i)
-                    if (base + i >= n_el) x[i] = -INFINITY;
+    } else {
+        // ---------------- consumers
+        RowState st{-INFINITY, 0.f, 0.f, 0.f, 0x7fffffff};
+        bool bad = false;
+        float best = -INFINITY;    // this warp's best score and its entry
+        int bidx = 0x7fffffff;
+        float bound = -INFINITY;   // best score known anywhere in the CTA
+        const uint32_t k0 = (uint32_t)seed, k1 = p.request_id;
+        const uint32_t c3 = dg::ctr_word3(seed, dg::kStreamGumbel);
+        const uint32_t step = (uint32_t)p.step;
+        int* queue = sh.queue[warp];
+        const unsigned lt = (1u << lane) - 1u;
+        for (int q = 0; q < npieces; ++q) {
+            const int sl = q % kSlots;
+            if (!dg::mbar_wait(&sh.full[sl], (uint32_t)(q / kSlots) & 1u)) {
+                sh.timeout = 1;
+                break;
             }
-            float vmax = x[0];
+            const unsigned char* slot = ring + (size_t)sl * kPieceBytes;
+            const int e_lo = q * kPieceElems;
+            const int n_el = (int)min((int64_t)kPieceElems, V - e_lo);
+            const int nvec = (n_el + VN - 1) / VN;
+            // candidate threshold on the raw logit: x / T + G_max >= best - slack
+            float x_thr = (fmaxf(bound, best) - kGumbelMax - kCandidateSlack) * p.temperature;
+            int qn = 0;
+            for (int j0 = warp * 32; j0 < nvec; j0 += kK1Warps * 32) {
+                const int j = j0 + lane;
+                bool cand[GPV];
 #pragma unroll
-            for (int i = 1; i < VN; ++i) vmax = fmaxf(vmax, x[i]);
-            if (vmax > st.m) {
-                int i0 = VN - 1;
+                for (int g = 0; g < GPV; ++g) cand[g] = false;
+                if (j < nvec) {
+                    float x[VN];
+                    Vec<DT>::load(slot + (size_t)j * 16, x);
+                    const int base = j * VN;
+                    if (base + VN > n_el) {
 #pragma unroll
-                for (int i = VN - 1; i >= 0; --i)
-                    if (x[i] == vmax) i0 = i;
-                if (st.m == -INFINITY) {
-                    st.c = 0.f;
-                    st.r = 0.f;
-                    st.t = 0.f;
-                } else {
-                    const float d = (st.m - vmax) * k2, al = ex2(d), s = st.c + st.r;
-                    st.t = al * (st.t + d * s);
-                    st.r = al * s;
-                    st.c = 0.f;
-                }
-                st.m = vmax;
-                st.idx = (int)begin + base + i0;
-            }
-            if (vmax == st.m) {
-                if (vmax == -INFINITY) {
+                        for (int i = 0; i < VN; ++i)
+                            if (base + i >= n_el) x[i] = -INFINITY;
+                    }
+                    float gmax[GPV];
 #pragma unroll
-                    for (int i = 0; i < VN; ++i) bad |= (x[i] != x[i]);
-                    continue;
-                }
+                    for (int g = 0; g < GPV; ++g)
+                        gmax[g] = fmaxf(fmaxf(x[4 * g], x[4 * g + 1]), fmaxf(x[4 * g + 2], x[4 * g + 3]));
+                    float vmax = gmax[0];
 #pragma unroll
-                for (int i = 0; i < VN; ++i) {
-                    if (x[i] == st.m) {
-                        st.c += 1.f;
+                    for (int g = 1; g < GPV; ++g) vmax = fmaxf(vmax, gmax[g]);
+                    // online softmax state
+                    if (vmax > st.m) {
+                        int i0 = VN - 1;
+#pragma unroll
+                        for (int i = VN - 1; i >= 0; --i)
+                            if (x[i] == vmax) i0 = i;
+                        if (st.m == -INFINITY) {
+                            st.c = 0.f;
+                            st.r = 0.f;
+                            st.t = 0.f;
+                        } else {
+                            const float d = (st.m - vmax) * k2, al = ex2(d), s = st.c + st.r;
+                            st.t = al * (st.t + d * s);
+                            st.r = al * s;
+                            st.c = 0.f;
+                        }
+                        st.m = vmax;
+                        st.idx = e_lo + base + i0;
+                    }
+                    if (vmax == st.m) {
+                        if (vmax == -INFINITY) {
+#pragma unroll
+                            for (int i = 0; i < VN; ++i) bad |= (x[i] != x[i]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < VN; ++i) {
+                                if (x[i] == st.m) {
+                                    st.c += 1.f;
+                                } else {
+                                    // -inf entries (masked tail, or -inf logits) contribute e = 0;
+                                    // the clamp keeps e * d at 0 instead of 0 * -inf
+                                    const float d = max_nan((x[i] - st.m) * k2, kMinExponent), e = ex2(d);
+                                    st.r += e;
+                                    st.t = fmaf(e, d, st.t);
+                                }
+                            }
+                        }
                     } else {
-                        // -inf entries (masked tail, or -inf logits) contribute e = 0; the clamp
-                        // keeps e * d at 0 instead of 0 * -inf
-                        const float d = max_nan((x[i] - st.m) * k2, kMinExponent), e = ex2(d);
-                        st.r += e;
-                        st.t = fmaf(e, d, st.t);
+#pragma unroll
+                        for (int i = 0; i < VN; ++i) {
+                            const float d = max_nan((x[i] - st.m) * k2, kMinExponent), e = ex2(d);
+                            st.r += e;
+                            st.t = fmaf(e, d, st.t);
+                        }
+                    }
+                    if (do_sample) {
+#pragma unroll
+                        for (int g = 0; g < GPV; ++g) cand[g] = gmax[g] >= x_thr;
                     }
                 }
-            } else {
+                if (!do_sample) continue;
+                // queue the candidate groups (ballot-compacted) and draw 32 at a time
 #pragma unroll
-                for (int i = 0; i < VN; ++i) {
-                    const float d = max_nan((x[i] - st.m) * k2, kMinExponent), e = ex2(d);
-                    st.r += e;
-                    st.t = fmaf(e, d, st.t);
+                for (int g = 0; g < GPV; ++g) {
+                    const unsigned mk = __ballot_sync(0xffffffffu, cand[g]);
+                    if (cand[g]) queue[qn + __popc(mk & lt)] = e_lo + (j * GPV + g) * 4;
+                    qn += __popc(mk);
                 }
-            }
-        }
-    }
-    if (bad) sh.bad = 1;
-
-    // warp, CTA and cluster merges (fixed order)
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) st = merge(st, shfl_state(st, o), k2);
-    if (lane == 0) sh.warp_state[warp] = st;
-    __syncthreads();
-    if (tid == 0) {
-        RowState c = sh.warp_state[0];
-        for (int w = 1; w < kK1Warps; ++w) c = merge(c, sh.warp_state[w], k2);
-        sh.cta_state = c;
-    }
-    cluster.sync();
-    if (tid == 0) {
-        RowState rs = *cluster.map_shared_rank(&sh.cta_state, 0);
-        for (int q = 1; q < ncta; ++q) rs = merge(rs, *cluster.map_shared_rank(&sh.cta_state, q), k2);
-        int any_bad = 0;
-        for (int q = 0; q < ncta; ++q) any_bad |= cluster.map_shared_rank(&sh.bad, q)[0];
-        sh.row_state = rs;
-        sh.bad = any_bad;
-    }
-    __syncthreads();
-    const RowState rs = sh.row_state;
-    const bool empty = rs.m == -INFINITY;
-    const bool row_bad = sh.bad || rs.m == INFINITY || !isfinite(rs.r) || !isfinite(rs.t);
-
-    // ---------------- pass B: Gumbel-max over entries that can still win
-    float best = -INFINITY;
-    int bidx = 0x7fffffff;
-    const uint32_t k0 = (uint32_t)seed, k1 = p.request_id;
-    const uint32_t c3 = dg::ctr_word3(seed, dg::kStreamGumbel);
-    const uint32_t step = (uint32_t)p.step;
-    if (do_sample && !empty && !row_bad && !sh.timeout) {
-        {  // the argmax entry gives the first lower bound (z = 0 there)
-            const dg::u4 w = dg::philox10((uint32_t)rs.idx >> 2, (uint32_t)pos, step, c3, k0, k1);
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-            const float u = dg::uniform_from_word(ws[rs.idx & 3]);
-            best = 0.f + (-logf(-logf(u)));
-            bidx = rs.idx;
-        }
-        for (int j = tid; j < nvec; j += kK1Threads) {
-            float x[VN];
-            Vec<DT>::load(chunk + (size_t)j * 16, x);
-            const int base = j * VN;
-#pragma unroll
-            for (int h = 0; h < VN; h += 4) {
-                float z[4];
-                bool any = false;
-                const float thr = best - kGumbelMax - kCandidateSlack;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float xi = (base + h + i < n_el) ? x[h + i] : -INFINITY;
-                    z[i] = (xi - rs.m) * invT;
-                    any |= (z[i] >= thr);
-                }
-                if (!any) continue;
-                const int v0 = (int)begin + base + h;  // multiple of 4
-                const dg::u4 w = dg::philox10((uint32_t)v0 >> 2, (uint32_t)pos, step, c3, k0, k1);
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if (!(z[i] >= best - kGumbelMax - kCandidateSlack)) continue;
-                    const float u = dg::uniform_from_word(ws[i]);
-                    // g > D = best - z needs u > exp(-e^-D) >= 1 - e^-D; keep a factor 2 of slack
-                    const float eb = 2.f * ex2(-(best - z[i]) * kLog2e);
-                    if (!(u > 1.f - eb)) continue;
-                    const float score = z[i] + (-logf(-logf(u)));
-                    if (better(score, v0 + i, best, bidx)) {
-                        best = score;
-                        bidx = v0 + i;
+                __syncwarp();
+                while (qn >= 32) {  // at most 31 + 32 * GPV < 96 entries are queued
+                    eval_group<DT>(slot, e_lo, queue[lane], V, invT, (uint32_t)pos, step, c3, k0, k1, bound, best, bidx);
+                    __syncwarp();
+                    const int rest = qn - 32;  // move the unprocessed tail to the front
+                    for (int r0 = 0; r0 < rest; r0 += 32) {
+                        const int r = r0 + lane;
+                        const int v = r < rest ? queue[32 + r] : 0;
+                        __syncwarp();
+                        if (r < rest) queue[r] = v;
+                        __syncwarp();
                     }
+                    qn = rest;
+                    warp_best(best, bidx);
+                    x_thr = (fmaxf(bound, best) - kGumbelMax - kCandidateSlack) * p.temperature;
                 }
             }
+            if (do_sample) {
+                // the queue refers to this slot: drain it (fewer than 32 left) before the slot is released
+                if (lane < qn)
+                    eval_group<DT>(slot, e_lo, queue[lane], V, invT, (uint32_t)pos, step, c3, k0, k1, bound, best, bidx);
+                warp_best(best, bidx);
+                // share the best score with the other warps, take theirs
+                if (lane == 0 && best > -INFINITY) atomicMax(&sh.best_key, float_key(best));
+                __syncwarp();
+                bound = fmaxf(bound, key_float(*(volatile unsigned*)&sh.best_key));
+            }
+            __syncwarp();
+            if (lane == 0) dg::mbar_arrive(&sh.empty[sl]);
         }
-    }
+        if (bad) sh.bad = 1;
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
-        if (better(ob, oi, best, bidx)) {
-            best = ob;
-            bidx = oi;
+        for (int o = 16; o >= 1; o >>= 1) st = merge(st, shfl_state(st, o), k2);
+        warp_best(best, bidx);
+        if (lane == 0) {
+            sh.warp_state[warp] = st;
+            sh.warp_best[warp] = best;
+            sh.warp_bidx[warp] = bidx;
         }
-    }
-    if (lane == 0) {
-        sh.warp_best[warp] = best;
-        sh.warp_bidx[warp] = bidx;
     }
     __syncthreads();
-    if (tid == 0) {
-        float b = sh.warp_best[0];
-        int bi = sh.warp_bidx[0];
-        for (int w = 1; w < kK1Warps; ++w)
-            if (better(sh.warp_best[w], sh.warp_bidx[w], b, bi)) {
-                b = sh.warp_best[w];
-                bi = sh.warp_bidx[w];
-            }
-        sh.cta_best = b;
-        sh.cta_bidx = bi;
-    }
-    cluster.sync();
-    if (rank == 0 && tid == 0) {
-        float b = sh.cta_best;
-        int bi = sh.cta_bidx;
-        int any_timeout = sh.timeout;
-        for (int q = 1; q < ncta; ++q) {
-            const float ob = *cluster.map_shared_rank(&sh.cta_best, q);
-            const int oi = *cluster.map_shared_rank(&sh.cta_bidx, q);
-            any_timeout |= *cluster.map_shared_rank(&sh.timeout, q);
-            if (better(ob, oi, b, bi)) {
-                b = ob;
-                bi = oi;
-            }
+    if (warp == 0) {
+        // the sample: the best of the warps' own winners
+        float b = -INFINITY;
+        int bi = 0x7fffffff;
+        if (lane < kK1Warps) {
+            b = sh.warp_best[lane];
+            bi = sh.warp_bidx[lane];
         }
-        // H = log(c + r) - t ln2 / (c + r), with log1p where a single entry holds the max
-        const float s = rs.c + rs.r;
-        const float lns = (rs.c == 1.f) ? log1pf(rs.r) : logf(rs.c) + log1pf(rs.r / rs.c);
-        const float H = lns - rs.t * kLn2 / s;
-        entropy_out[row] = H;
-        lse_out[row] = rs.m * invT + lns;
-        argmax_out[row] = empty ? 0 : rs.idx;
-        sample_out[row] = (do_sample && !empty && !row_bad) ? bi : -1;
-        if (row_bad) dg::raise_status(status, DG_DEV_NAN_INF_ROW);
-        if (empty) dg::raise_status(status, DG_DEV_EMPTY_ROW);
-        if (any_timeout) dg::raise_status(status, DG_DEV_TIMEOUT);
+        warp_best(b, bi);
+        if (lane == 0) {
+            RowState rs = sh.warp_state[0];
+            for (int w = 1; w < kK1Warps; ++w) rs = merge(rs, sh.warp_state[w], k2);
+            const bool empty = rs.m == -INFINITY;
+            const bool row_bad = sh.bad || rs.m == INFINITY || !isfinite(rs.r) || !isfinite(rs.t);
+            // H = log(c + r) - t ln2 / (c + r), with log1p where a single entry holds the max
+            const float s = rs.c + rs.r;
+            const float lns = (rs.c == 1.f) ? log1pf(rs.r) : logf(rs.c) + log1pf(rs.r / rs.c);
+            const float H = lns - rs.t * kLn2 / s;
+            entropy_out[row] = H;
+            lse_out[row] = rs.m * invT + lns;
+            argmax_out[row] = empty ? 0 : rs.idx;
+            sample_out[row] = (do_sample && !empty && !row_bad) ? bi : -1;
+            if (row_bad) dg::raise_status(status, DG_DEV_NAN_INF_ROW);
+            if (empty) dg::raise_status(status, DG_DEV_EMPTY_ROW);
+            if (sh.timeout) dg::raise_status(status, DG_DEV_TIMEOUT);
+        }
     }
-    // keep every CTA's shared memory alive until the peers are done reading it, and make
-    // sure no bulk copy is still landing when the CTA exits
-    if (sh.timeout && tid == 0)
-        for (int pc = 0; pc < npieces; ++pc) (void)dg::mbar_wait(&sh.bar[pc], 0);
-    cluster.sync();
 }
 
 // ------------------------------------------------------------------------------------
@@ -550,51 +590,28 @@ dg_status check_canvas_dims(int64_t n, int32_t L, int64_t V) {
     return DG_OK;
 }
 
-struct K1Plan {
-    int cs;
-    int32_t chunk_elems;
-    size_t smem;
-};
-
-bool plan_k1(dg_dtype dt, int64_t V, K1Plan* pl) {
+// Rows stream through the ring, so any V works up to 2^31 bytes per row.
+bool k1_supported(dg_dtype dt, int64_t V) {
     const int64_t es = dt == DG_BF16 ? 2 : 4;
-    const int64_t vn = 16 / es;
-    const int64_t row_bytes = V * es;
-    int cs = 1;
-    while (cs < kMaxCluster && row_bytes > (int64_t)cs * 65536) cs *= 2;
-    int64_t chunk = (V + cs - 1) / cs;
-    chunk = (chunk + vn - 1) / vn * vn;
-    if (chunk * es > (int64_t)kMaxChunkBytes) return false;
-    pl->cs = cs;
-    pl->chunk_elems = (int32_t)chunk;
-    pl->smem = ((sizeof(K1Shared) + 127) / 128) * 128 + (size_t)((chunk * es + 127) / 128 * 128);
-    return true;
+    return V * es < (1LL << 31);
 }
+
+size_t k1_smem_bytes() { return ((sizeof(K1Shared) + 127) / 128) * 128 + (size_t)kSlots * kPieceBytes; }
 
 template <int DT>
 dg_status launch_k1(const void* logits, int64_t ld, int64_t n, int32_t L, int64_t V,
-                    const dg_canvas_params* params, uint64_t seed, const K1Plan& pl, int32_t* argmax, int32_t* sample,
-                    float* entropy, float* lse, cudaStream_t stream) {
+                    const dg_canvas_params* params, uint64_t seed, int32_t* argmax, int32_t* sample, float* entropy,
+                    float* lse, cudaStream_t stream) {
     auto kern = k1_row_stats<DT>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) != cudaSuccess)
+    const size_t smem = k1_smem_bytes();
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DG_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)pl.cs, (unsigned)L, (unsigned)n);
-    cfg.blockDim = dim3(kK1Threads, 1, 1);
-    cfg.dynamicSmemBytes = pl.smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)pl.cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     const int64_t ld_bytes = ld * (DT == 0 ? 2 : 4);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<const unsigned char*>(logits), ld_bytes, V, L, params,
-                                       seed, pl.chunk_elems, argmax, sample, entropy, lse, dghost::status_word());
+    kern<<<dim3((unsigned)L, (unsigned)n, 1), kK1Threads, smem, stream>>>(static_cast<const unsigned char*>(logits),
+                                                                          ld_bytes, V, L, params, seed, argmax,
+                                                                          sample, entropy, lse, dghost::status_word());
     dghost::count_launch();
-    return dghost::cuda_status(e);
+    return dghost::cuda_status(cudaGetLastError());
 }
 
 dg_status launch_k2(const float* entropy, const int32_t* sample, const int32_t* argmax, int64_t n, int32_t L,
@@ -632,11 +649,10 @@ dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld, int64_
         return DG_ERR_INVALID_ARG;
     const int64_t es = dtype == DG_BF16 ? 2 : 4;
     if (!aligned16(logits) || (ld * es) % 16 != 0) return DG_ERR_ALIGNMENT;
-    K1Plan pl;
-    if (!plan_k1(dtype, V, &pl)) return DG_ERR_UNSUPPORTED;
+    if (!k1_supported(dtype, V)) return DG_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
-    s = dtype == DG_BF16 ? launch_k1<0>(logits, ld, n_canvas, L, V, params, seed, pl, argmax, sample, entropy, lse, st)
-                         : launch_k1<1>(logits, ld, n_canvas, L, V, params, seed, pl, argmax, sample, entropy, lse, st);
+    s = dtype == DG_BF16 ? launch_k1<0>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, st)
+                         : launch_k1<1>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, st);
     if (s != DG_OK) return s;
     return launch_k2(entropy, sample, argmax, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
                      accept_mask, converged, mean_entropy, n_accept, st);

@@ -28,7 +28,11 @@
 #include <algorithm>
 #include <mutex>
 
+#include <cooperative_groups.h>
+
 #include "dg_common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace {
 
@@ -70,7 +74,8 @@ struct Cfg {
     static constexpr int kAccCols = BN;                      // fp32 accumulator columns
     static constexpr int kNAcc = (BN <= 256) ? 2 : 1;        // double-buffered when it fits
     static constexpr int kTmemCols = kAccCols * kNAcc;       // 256 or 512
-    static constexpr int kThreads = kXform ? 320 : 192;
+    static constexpr int kXformThreads = 256;                // two warpgroups, half a tile row each
+    static constexpr int kThreads = kXform ? 192 + kXformThreads : 192;
     static constexpr int kATileBytes = BM * BK * 2;
     static constexpr int kStageBytesFp32 = (AM == A_SOFTMAX_FP32) ? BM * BK * 4 : 0;
     static constexpr int kBTileBytes = BK * BN * 2;
@@ -101,7 +106,9 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool b_mn_major)
 // ------------------------------------------------------------------ scheduling
 struct Item {
     int m, n, kb_lo, kb_hi;
-    int64_t w;
+    int m_load;   // m-tile whose rows are loaded (a real tile even for padding members)
+    bool valid;   // false for the padding members of the last group of m-tiles
+    int64_t w;    // partial-tile slot: k-slice * T + n * mt + m
 };
 
 DG_DEVINL int active_m_tiles(const GemmArgs& a) {
@@ -109,16 +116,26 @@ DG_DEVINL int active_m_tiles(const GemmArgs& a) {
     return min(a.m_tiles, a.plan[0] * a.tpc);
 }
 
-DG_DEVINL Item decode(const GemmArgs& a, int mt, int64_t w) {
-    const int64_t T = (int64_t)mt * a.n_tiles;
-    const int s = (int)(w / T);
-    const int t = (int)(w % T);
+// Work is cut into groups of `cm` consecutive m-tiles sharing one (k-slice, n-tile); the cm
+// CTAs of a cluster run a group together (rank r takes m-tile mg * cm + r) so that they can
+// share the B tile.  Groups are ordered (k-slice, n-tile, m-group), m fastest.
+DG_DEVINL int64_t group_count(const GemmArgs& a, int mt, int cm) {
+    return (int64_t)a.splits * a.n_tiles * ((mt + cm - 1) / cm);
+}
+
+DG_DEVINL Item decode(const GemmArgs& a, int mt, int cm, int rank, int64_t G) {
+    const int64_t mgc = (mt + cm - 1) / cm;
+    const int64_t per_s = (int64_t)a.n_tiles * mgc;
+    const int s = (int)(G / per_s);
+    const int64_t rem = G % per_s;
     Item it;
-    it.w = w;
-    it.n = t / mt;
-    it.m = t % mt;
+    it.n = (int)(rem / mgc);
+    it.m = (int)(rem % mgc) * cm + rank;
+    it.valid = it.m < mt;
+    it.m_load = it.valid ? it.m : mt - 1;
     it.kb_lo = (int)((int64_t)s * a.k_blocks / a.splits);
     it.kb_hi = (int)((int64_t)(s + 1) * a.k_blocks / a.splits);
+    it.w = (int64_t)s * mt * a.n_tiles + (int64_t)it.n * mt + it.m;
     return it;
 }
 
@@ -155,6 +172,9 @@ struct __align__(8) GemmShared {
 };
 
 DG_DEVINL bool aborted(const GemmShared& sh) { return *(volatile const int*)&sh.abort_flag != 0; }
+
+// Warp-uniform form for loops whose body holds whole-warp operations.
+DG_DEVINL bool aborted_warp(const GemmShared& sh) { return __shfl_sync(0xffffffffu, (int)aborted(sh), 0) != 0; }
 
 DG_DEVINL void do_abort(GemmShared& sh, unsigned* status) {
     *(volatile int*)&sh.abort_flag = 1;
@@ -213,6 +233,9 @@ DG_DEVINL void epi_store(const GemmArgs& a, int epi, int m, int n_tile, int row,
 }
 
 // ------------------------------------------------------------------ the GEMM kernel
+// Launched as clusters of cm = gridDim.x / (clusters) CTAs (cm = 1, 2 or 4).  With cm > 1
+// (N-major B only) every CTA loads BN/64/cm of the B tile's 64-column atoms and multicasts
+// them to the whole cluster, and a stage is refilled only once all cm CTAs' MMAs have read it.
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
@@ -222,15 +245,20 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(g_smem_raw) + 1023) & ~uintptr_t(1023));
     GemmShared& sh = *reinterpret_cast<GemmShared*>(smem + (size_t)C::STAGES * C::kStageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int cm = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int64_t cid = blockIdx.x / cm, ncl = gridDim.x / cm;
+    const uint16_t mask = (uint16_t)((1u << cm) - 1u);
 
     const int mt = active_m_tiles(a);
-    const int64_t n_items = (int64_t)mt * a.n_tiles * a.splits;
+    const int64_t n_groups = mt > 0 ? group_count(a, mt, cm) : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             dg::mbar_init(&sh.full[s], 1);
-            dg::mbar_init(&sh.xform[s], 128);
-            dg::mbar_init(&sh.empty[s], 1);
+            dg::mbar_init(&sh.xform[s], C::kXform ? C::kXformThreads : 1);
+            dg::mbar_init(&sh.empty[s], (uint32_t)cm);  // one release per CTA of the cluster
         }
         for (int i = 0; i < C::kNAcc; ++i) {
             dg::mbar_init(&sh.accf[i], 1);
@@ -244,7 +272,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         dg::tmem_relinquish();
     }
     dg::tc_fence_before();
-    __syncthreads();
+    cluster.sync();  // peers' barriers are initialised before any multicast lands
     dg::tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
 
@@ -255,12 +283,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             dg::prefetch_tmap(&tmB0);
             if (C::kBMode == B_KMAJOR_GATEUP) dg::prefetch_tmap(&tmB1);
             uint32_t it = 0;
-            for (int64_t w = blockIdx.x; w < n_items && !aborted(sh); w += gridDim.x) {
-                const Item im = decode(a, mt, w);
+            for (int64_t G = cid; G < n_groups && !aborted(sh); G += ncl) {
+                const Item im = decode(a, mt, cm, rank, G);
                 int cz = 0, crow = 0;
                 if (C::kXform) {
-                    cz = canvas_of(a, im.m);
-                    crow = (im.m % a.tpc) * BM;
+                    cz = canvas_of(a, im.m_load);
+                    crow = (im.m_load % a.tpc) * BM;
                 }
                 for (int kb = im.kb_lo; kb < im.kb_hi; ++kb, ++it) {
                     const int s = (int)(it % C::STAGES);
@@ -273,7 +301,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     dg::mbar_arrive_expect_tx(&sh.full[s], C::kTxBytes);
                     const int k0 = kb * C::BK;
                     if (C::kAMode == A_TMA) {
-                        dg::tma_load_2d(sA, &tmA, k0, im.m * BM, &sh.full[s]);
+                        dg::tma_load_2d(sA, &tmA, k0, im.m_load * BM, &sh.full[s]);
                     } else if (C::kAMode == A_SOFTMAX_BF16) {
                         dg::tma_load_3d(sA, &tmA, k0, crow, cz, &sh.full[s]);
                     } else {
@@ -281,10 +309,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                         dg::tma_load_3d(sF, &tmA, k0, crow, cz, &sh.full[s]);
                     }
                     if (C::kBMode == B_MNMAJOR) {
-                        // [K][N] embedding rows: one 64-column (128-byte) atom column per load
+                        // [K][N] embedding rows: one 64-column (128-byte) atom column per load; with
+                        // a cluster each CTA fetches every cm-th atom for all of its peers
+                        if (cm == 1) {
 #pragma unroll
-                        for (int j = 0; j < C::BN / 64; ++j)
-                            dg::tma_load_2d(sB + j * (C::BK * 128), &tmB0, im.n * C::BN + j * 64, k0, &sh.full[s]);
+                            for (int j = 0; j < C::BN / 64; ++j)
+                                dg::tma_load_2d(sB + j * (C::BK * 128), &tmB0, im.n * C::BN + j * 64, k0, &sh.full[s]);
+                        } else {
+                            for (int j = rank; j < C::BN / 64; j += cm)
+                                dg::tma_load_2d_mc(sB + j * (C::BK * 128), &tmB0, im.n * C::BN + j * 64, k0,
+                                                   &sh.full[s], mask);
+                        }
                     } else if (C::kBMode == B_KMAJOR) {
                         dg::tma_load_2d(sB, &tmB0, k0, im.n * C::BN, &sh.full[s]);
                     } else {
@@ -306,8 +341,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             constexpr uint32_t idesc_k = instr_desc(BM, C::BN > 256 ? 256 : C::BN, false);
             constexpr uint32_t idesc = (C::kBMode == B_MNMAJOR) ? idesc_mn : idesc_k;
             uint32_t it = 0, acc_it = 0;
-            for (int64_t w = blockIdx.x; w < n_items && !aborted(sh); w += gridDim.x, ++acc_it) {
-                const Item im = decode(a, mt, w);
+            for (int64_t G = cid; G < n_groups && !aborted(sh); G += ncl, ++acc_it) {
+                const Item im = decode(a, mt, cm, rank, G);
                 const int ab = (int)(acc_it % C::kNAcc);
                 const uint32_t aph = (acc_it / C::kNAcc) & 1u;
                 if (!dg::mbar_wait(&sh.acce[ab], aph ^ 1u)) { do_abort(sh, a.status); break; }
@@ -338,7 +373,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                             dg::tc_mma_f16(dacc, ad, bd, idesc, accum);
                         }
                     }
-                    dg::tc_commit(&sh.empty[s]);  // frees the stage once these MMAs have read it
+                    // frees the stage (in every CTA of the cluster) once these MMAs have read it
+                    if (cm == 1) dg::tc_commit(&sh.empty[s]);
+                    else dg::tc_commit_mc(&sh.empty[s], mask);
                 }
                 if (!ok) { do_abort(sh, a.status); break; }
                 dg::tc_commit(&sh.accf[ab]);  // accumulator complete
@@ -349,14 +386,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;
         uint32_t acc_it = 0;
-        for (int64_t w = blockIdx.x; w < n_items && !aborted(sh); w += gridDim.x, ++acc_it) {
-            const Item im = decode(a, mt, w);
+        for (int64_t G = cid; G < n_groups && !aborted_warp(sh); G += ncl, ++acc_it) {
+            const Item im = decode(a, mt, cm, rank, G);
             const int ab = (int)(acc_it % C::kNAcc);
             const uint32_t aph = (acc_it / C::kNAcc) & 1u;
-            if (!dg::mbar_wait(&sh.accf[ab], aph)) { do_abort(sh, a.status); break; }
+            if (!dg::mbar_wait_warp(&sh.accf[ab], aph, 256)) { do_abort(sh, a.status); break; }
             dg::tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * C::kAccCols);
-            if (a.splits > 1) {
+            if (!im.valid) {
+                // padding member of the group: nothing to store
+            } else if (a.splits > 1) {
                 float* dst = a.partial + (size_t)im.w * (BM * C::BN) + (size_t)row * C::BN;
                 for (int ch = 0; ch < C::BN / 32; ++ch) {
                     float v[32];
@@ -383,14 +422,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             dg::mbar_arrive(&sh.acce[ab]);
         }
     } else {
-        // ------------------------------------------------ softmax transform (warps 6..9)
+        // ------------------------------------------------ softmax transform (warps 6..13)
         if (C::kXform) {
-            const int t = threadIdx.x - 192;  // tile row handled by this thread
+            const int t = (threadIdx.x - 192) & (BM - 1);    // tile row handled by this thread
+            const int half = (threadIdx.x - 192) / BM;        // which half of the row's chunks
             uint32_t it = 0;
-            for (int64_t w = blockIdx.x; w < n_items && !aborted(sh); w += gridDim.x) {
-                const Item im = decode(a, mt, w);
-                const int cz = canvas_of(a, im.m);
-                const int pos = (im.m % a.tpc) * BM + t;
+            for (int64_t G = cid; G < n_groups && !aborted_warp(sh); G += ncl) {
+                const Item im = decode(a, mt, cm, rank, G);
+                const int cz = canvas_of(a, im.m_load);
+                const int pos = (im.m_load % a.tpc) * BM + t;
                 const dg_canvas_params pr = a.params[cz];
                 const float kx = kLog2e / pr.temperature;
                 const float lb = (pos < a.L) ? a.lse[(int64_t)cz * a.L + pos] * kLog2e : 0.f;
@@ -406,9 +446,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     // one tile row = BK bf16 = BK/8 16-byte chunks; the swizzle permutes chunks
                     // within the row, so chunk c of the row sits at c ^ ((t >> sh) & mask)
                     constexpr int kChunks = C::BK / 8;
+                    constexpr int kHalf = kChunks / 2;
                     const int sw = (C::kASwizzle == 128) ? (t & 7) : ((t >> 1) & 3);
 #pragma unroll
-                    for (int c = 0; c < kChunks; ++c) {
+                    for (int cc = 0; cc < kHalf; ++cc) {
+                        const int c = half * kHalf + cc;
                         const int pc = c ^ sw;
                         float x[8];
                         if (C::kAMode == A_SOFTMAX_BF16) {
@@ -446,7 +488,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
 
     dg::tc_fence_before();
-    __syncthreads();
+    // no CTA leaves while a peer may still multicast into it or release its stages
+    cluster.sync();
     if (warp == 1) {
         dg::tc_fence_after();
         dg::tmem_dealloc(tmem, C::kTmemCols);
@@ -559,21 +602,78 @@ int choose_splits(int64_t T, int k_blocks, int P, int min_slice) {
     return best;
 }
 
+struct LaunchPlan {
+    int cm;        // CTAs per cluster
+    int clusters;  // concurrent clusters (persistent grid = clusters * cm CTAs)
+    int splits;    // k-slices
+};
+
+// Cluster size, persistent grid and k-slices for a GEMM.  The N-major B tile (embedding rows)
+// is shared by the 2 CTAs of a cluster on neighbouring m-tiles (pairs fill the GPCs better
+// than 4-CTA clusters, and measured as fast); the 4-CTA form stays available and is used
+// only while the GPU keeps at least 90 % of its SMs busy with it.  The k-slices are then
+// chosen for the number of clusters, within `max_slots` partial tiles.
 template <class C>
-dg_status launch_gemm(const void* tmA, const void* tmB0, const void* tmB1, const GemmArgs& a, int64_t max_items,
-                      cudaStream_t stream) {
+bool plan_gemm(const GemmArgs& a, int64_t max_slots, LaunchPlan* pl) {
     auto kern = k_gemm<C>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
-        return DG_ERR_CUDA;
+        return false;
     const int P = dghost::sm_count();
-    if (P <= 0) return DG_ERR_CUDA;
-    const int grid = (int)std::min<int64_t>(P, std::max<int64_t>(1, max_items));
-    const CUtensorMap& A = *static_cast<const CUtensorMap*>(tmA);
-    const CUtensorMap& B0 = *static_cast<const CUtensorMap*>(tmB0);
-    const CUtensorMap& B1 = *static_cast<const CUtensorMap*>(tmB1);
-    kern<<<grid, C::kThreads, C::kSmem, stream>>>(A, B0, B1, a);
+    if (P <= 0) return false;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int cm = 1;
+    if (C::kBMode == B_MNMAJOR && a.m_tiles >= 2) cm = 2;
+    int clusters = P;
+    while (cm > 1) {
+        attr[0].val.clusterDim.x = (unsigned)cm;
+        cfg.gridDim = dim3((unsigned)((P / cm) * cm), 1, 1);
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess) nc = 0;
+        if (nc > 0 && (cm < 4 || nc * 4 >= (P * 9) / 10)) {
+            clusters = nc;
+            break;
+        }
+        cm /= 2;
+    }
+    if (cm == 1) clusters = P;
+    const int64_t per_split = (int64_t)a.n_tiles * ((a.m_tiles + cm - 1) / cm);
+    int splits = choose_splits(per_split, a.k_blocks, clusters, 256);
+    while (splits > 1 && (int64_t)a.m_tiles * a.n_tiles * splits > max_slots) --splits;
+    pl->cm = cm;
+    pl->clusters = clusters;
+    pl->splits = splits;
+    return true;
+}
+
+template <class C>
+dg_status launch_gemm(const void* tmA, const void* tmB0, const void* tmB1, const GemmArgs& a, const LaunchPlan& pl,
+                      cudaStream_t stream) {
+    auto kern = k_gemm<C>;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)pl.cm;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    const int64_t groups = (int64_t)a.splits * a.n_tiles * ((a.m_tiles + pl.cm - 1) / pl.cm);
+    const int64_t ncl = std::max<int64_t>(1, std::min<int64_t>(pl.clusters, groups));
+    cfg.gridDim = dim3((unsigned)(ncl * pl.cm), 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, *static_cast<const CUtensorMap*>(tmA),
+                                       *static_cast<const CUtensorMap*>(tmB0), *static_cast<const CUtensorMap*>(tmB1), a);
     dghost::count_launch();
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return DG_ERR_CUDA;
     if (a.splits > 1) {
         const int64_t T = (int64_t)a.m_tiles * a.n_tiles;
@@ -582,6 +682,16 @@ dg_status launch_gemm(const void* tmA, const void* tmB0, const void* tmB1, const
         e = cudaGetLastError();
     }
     return dghost::cuda_status(e);
+}
+
+// Plan, then launch, with the planned k-slices.
+template <class C>
+dg_status plan_and_launch(const void* tmA, const void* tmB0, const void* tmB1, GemmArgs a, int64_t max_slots,
+                          cudaStream_t stream) {
+    LaunchPlan pl;
+    if (!plan_gemm<C>(a, max_slots, &pl)) return DG_ERR_CUDA;
+    a.splits = pl.splits;
+    return launch_gemm<C>(tmA, tmB0, tmB1, a, pl, stream);
 }
 
 struct TMaps {
@@ -661,7 +771,7 @@ dg_status run_mlp(const uint16_t* pe, uint16_t* hmid, int64_t rows, int32_t d, i
     g.n_valid = h;
     g.m_valid = (int32_t)rows;
     g.status = dghost::status_word();
-    dg_status s = launch_gemm<GateUp>(t1.a, t1.b0, t1.b1, g, (int64_t)g.m_tiles * g.n_tiles, stream);
+    dg_status s = plan_and_launch<GateUp>(t1.a, t1.b0, t1.b1, g, 0, stream);
     if (s != DG_OK) return s;
 
     if (!tmap_2d(t2.a, 0, hmid, h, rows, h, 64, BM, 128)) return DG_ERR_CUDA;
@@ -676,7 +786,7 @@ dg_status run_mlp(const uint16_t* pe, uint16_t* hmid, int64_t rows, int32_t d, i
     q.n_valid = d;
     q.m_valid = m_valid_rows;
     (void)P;
-    return launch_gemm<Down>(t2.a, t2.b0, t2.b0, q, (int64_t)q.m_tiles * q.n_tiles, stream);
+    return plan_and_launch<Down>(t2.a, t2.b0, t2.b0, q, 0, stream);
 }
 
 dg_status check_weights(int64_t V, int32_t d, int32_t h, const uint16_t* E, const uint16_t* Wg, const uint16_t* Wu,
@@ -768,8 +878,7 @@ dg_status dg_self_cond_pe(const void* logits, dg_dtype dtype, int64_t ld, const 
     g.n_tiles = (d + 511) / 512;
     g.k_blocks = (int32_t)((V + bk - 1) / bk);
     const int64_t Tmax = (int64_t)g.m_tiles * g.n_tiles;
-    g.splits = choose_splits(Tmax, g.k_blocks, P, 256);
-    while (g.splits > 1 && Tmax * g.splits > pe_partial_slots(n_canvas, L, d, P)) --g.splits;
+    g.splits = 1;  // set by the plan
     g.K = V;
     g.L = L;
     g.lse = lse;
@@ -781,8 +890,9 @@ dg_status dg_self_cond_pe(const void* logits, dg_dtype dtype, int64_t ld, const 
     g.m_valid = (int32_t)lay.rows;
     g.partial = reinterpret_cast<float*>(ws + lay.partial);
     g.status = dghost::status_word();
-    return dtype == DG_BF16 ? launch_gemm<PEbf16>(tm.a, tm.b0, tm.b0, g, Tmax * g.splits, st)
-                            : launch_gemm<PEfp32>(tm.a, tm.b0, tm.b0, g, Tmax * g.splits, st);
+    const int64_t max_slots = pe_partial_slots(n_canvas, L, d, P);
+    return dtype == DG_BF16 ? plan_and_launch<PEbf16>(tm.a, tm.b0, tm.b0, g, max_slots, st)
+                            : plan_and_launch<PEfp32>(tm.a, tm.b0, tm.b0, g, max_slots, st);
 }
 
 dg_status dg_self_cond_mlp(int64_t n_canvas, int32_t L, int32_t d, int32_t h, const uint16_t* W_gate,
@@ -870,8 +980,7 @@ dg_status dg_self_cond_probs(const uint16_t* P_rows, int64_t ld, int64_t n_rows,
     g.k_blocks = (int32_t)((V + bk - 1) / bk);
     const int64_t T = (int64_t)g.m_tiles * g.n_tiles;
     const int64_t slots = T * 32 > 0 ? std::min<int64_t>(T * 32, std::max<int64_t>(T, 8LL * P)) : 0;
-    g.splits = choose_splits(T, g.k_blocks, P, 256);
-    while (g.splits > 1 && T * g.splits > slots) --g.splits;
+    g.splits = 1;  // set by the plan
     g.K = V;
     g.L = (int32_t)n_rows;
     g.epi = EPI_BF16;
@@ -881,7 +990,7 @@ dg_status dg_self_cond_probs(const uint16_t* P_rows, int64_t ld, int64_t n_rows,
     g.m_valid = (int32_t)rows;
     g.partial = partial;
     g.status = dghost::status_word();
-    s = launch_gemm<PEprob>(tm.a, tm.b0, tm.b0, g, T * g.splits, st);
+    s = plan_and_launch<PEprob>(tm.a, tm.b0, tm.b0, g, slots, st);
     if (s != DG_OK) return s;
     return run_mlp(pe, hmid, rows, d, h, W_gate, W_up, W_down, delta_emb, d, nullptr, (int)tiles, (int32_t)n_rows,
                    (int32_t)rows, st);
@@ -929,9 +1038,7 @@ dg_status dg_gemm_bf16(const uint16_t* A, int64_t lda, const uint16_t* B, int64_
         g.n_tiles = (int32_t)((N + 511) / 512);
         g.k_blocks = (int32_t)((K + bk - 1) / bk);
         const int64_t T = (int64_t)g.m_tiles * g.n_tiles;
-        g.splits = choose_splits(T, g.k_blocks, P, 256);
-        while (g.splits > 1 && T * g.splits > slots_cap) --g.splits;
-        return launch_gemm<PEprob>(tm.a, tm.b0, tm.b0, g, T * g.splits, st);
+        return plan_and_launch<PEprob>(tm.a, tm.b0, tm.b0, g, slots_cap, st);
     }
     const int bk = 64;
     if (!tmap_2d(tm.a, 0, A, K, M, lda, bk, BM, 128)) return DG_ERR_CUDA;
@@ -939,9 +1046,7 @@ dg_status dg_gemm_bf16(const uint16_t* A, int64_t lda, const uint16_t* B, int64_
     g.n_tiles = (int32_t)((N + 255) / 256);
     g.k_blocks = (int32_t)((K + bk - 1) / bk);
     const int64_t T = (int64_t)g.m_tiles * g.n_tiles;
-    g.splits = choose_splits(T, g.k_blocks, P, 256);
-    while (g.splits > 1 && T * g.splits > slots_cap) --g.splits;
-    return launch_gemm<Down>(tm.a, tm.b0, tm.b0, g, T * g.splits, st);
+    return plan_and_launch<Down>(tm.a, tm.b0, tm.b0, g, slots_cap, st);
 }
 
 }  // extern "C"
@@ -1001,8 +1106,9 @@ extern "C" dg_status dg_gemm_bf16_noalloc(const uint16_t* A, int64_t lda, const 
     g.k_blocks = (int32_t)((K + bk - 1) / bk);
     const int64_t T = (int64_t)g.m_tiles * g.n_tiles;
     const int64_t slots_cap = (int64_t)(dg_gemm_workspace_bytes(M, N) / ((size_t)BM * 512 * 4));
-    g.splits = choose_splits(T, g.k_blocks, P, 256);
-    while (g.splits > 1 && T * g.splits > slots_cap) --g.splits;
+    LaunchPlan pl;
+    if (!(b_mn_major ? plan_gemm<PEprob>(g, slots_cap, &pl) : plan_gemm<Down>(g, slots_cap, &pl))) return DG_ERR_CUDA;
+    g.splits = pl.splits;
     const size_t need = g.splits > 1 ? (size_t)T * g.splits * BM * bn * 4 : 0;
     if (need > (size_t)DG_NOALLOC_SCRATCH_BYTES) return DG_ERR_UNSUPPORTED;
     void* scratch = nullptr;
@@ -1014,9 +1120,9 @@ extern "C" dg_status dg_gemm_bf16_noalloc(const uint16_t* A, int64_t lda, const 
     if (b_mn_major) {
         if (!tmap_2d(tm.a, 0, A, K, M, lda, bk, BM, 64)) return DG_ERR_CUDA;
         if (!tmap_2d(tm.b0, 0, B, N, K, ldb, 64, bk, 128)) return DG_ERR_CUDA;
-        return launch_gemm<PEprob>(tm.a, tm.b0, tm.b0, g, T * g.splits, st);
+        return launch_gemm<PEprob>(tm.a, tm.b0, tm.b0, g, pl, st);
     }
     if (!tmap_2d(tm.a, 0, A, K, M, lda, bk, BM, 128)) return DG_ERR_CUDA;
     if (!tmap_2d(tm.b0, 0, B, K, N, ldb, bk, 256, 128)) return DG_ERR_CUDA;
-    return launch_gemm<Down>(tm.a, tm.b0, tm.b0, g, T * g.splits, st);
+    return launch_gemm<Down>(tm.a, tm.b0, tm.b0, g, pl, st);
 }

@@ -143,8 +143,8 @@ DG_API size_t dg_denoise_workspace_bytes(int64_t n_canvas, int32_t L, int64_t V,
  *   mean_entropy  (device, out, may be NULL) [n_canvas] float.
  *   n_accept      (device, out, may be NULL) [n_canvas] int32.
  *   workspace     may be NULL when dg_denoise_workspace_bytes() is 0.
- * Limits: 1 <= L <= 1024, 2 <= V < 2^31, n_canvas >= 0 (0 launches nothing), and
- * V * sizeof(dtype) <= 1.5 MiB (else DG_ERR_UNSUPPORTED).
+ * Limits: 1 <= L <= 1024, 2 <= V < 2^31, 0 <= n_canvas <= 65535 (0 launches nothing), and
+ * V * sizeof(dtype) < 2^31 bytes (else DG_ERR_UNSUPPORTED).
  * Errors: DG_ERR_INVALID_ARG (null required pointer, sizes), DG_ERR_ALIGNMENT,
  * DG_ERR_UNSUPPORTED, DG_ERR_CUDA. */
 DG_API dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld,

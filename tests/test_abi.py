@@ -46,7 +46,7 @@ def test_host_validation_without_gpu():
     assert lib.dg_denoise_step(18, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), None, 0, None) == dg.DG_ERR_ALIGNMENT
     assert lib.dg_denoise_step(16, 0, 12, 1, 16, 12, 16, 0, *([16] * 11), None, 0, None) == dg.DG_ERR_ALIGNMENT
     # a row that does not fit the on-chip plan
-    assert lib.dg_denoise_step(16, 1, 1 << 20, 1, 16, 1 << 20, 16, 0, *([16] * 11), None, 0, None) == dg.DG_ERR_UNSUPPORTED
+    assert lib.dg_denoise_step(16, 1, 1 << 29, 1, 16, 1 << 29, 16, 0, *([16] * 11), None, 0, None) == dg.DG_ERR_UNSUPPORTED
     # empty batch is a no-op
     assert lib.dg_denoise_step(None, 0, 8, 0, 16, 8, None, 0, *([None] * 11), None, 0, None) == dg.DG_OK
     assert lib.dg_denoise_workspace_bytes(8, 256, 262144, 0) == 0

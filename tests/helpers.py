@@ -78,11 +78,13 @@ class Report:
 
 
 def compare_step(g: dict, o: dict, p: dict, V: int, seed: int, canvas_in: np.ndarray,
-                 prev_in: np.ndarray, stable_in: np.ndarray, rows=None) -> Report:
+                 prev_in: np.ndarray, stable_in: np.ndarray, rows=None, g_in: dict | None = None) -> Report:
     """Compare GPU outputs `g` (StepBuffers.host()) with oracle outputs `o`.
 
     `rows` (optional) restricts the per-position checks to these (canvas, position) pairs and
-    skips the per-canvas checks (for sampled parity at full size)."""
+    skips the per-canvas checks (for sampled parity at full size).  `g_in` (optional) holds
+    the GPU buffers before the step; inactive canvases must keep them (else the buffers'
+    initial fill values)."""
     rep = Report()
     flags = np.asarray(p["flags"])
     n, L = g["argmax"].shape
@@ -91,8 +93,12 @@ def compare_step(g: dict, o: dict, p: dict, V: int, seed: int, canvas_in: np.nda
             # inactive: nothing written
             assert (g["canvas"][c] == canvas_in[c]).all()
             assert (g["prev"][c] == prev_in[c]).all() and g["stable"][c] == stable_in[c]
-            assert (g["accept"][c] == 7).all() and (g["argmax"][c] == -7).all()
-            assert g["converged"][c] == 7
+            if g_in is None:
+                assert (g["accept"][c] == 7).all() and (g["argmax"][c] == -7).all()
+                assert g["converged"][c] == 7
+            else:
+                for k in ("accept", "argmax", "sample", "entropy", "lse", "converged"):
+                    assert np.array_equal(g[k][c], g_in[k][c]), k
             continue
         pos = range(L) if rows is None else [i for (cc, i) in rows if cc == c]
         ro = bool(flags[c] & oracle.READ_ONLY)

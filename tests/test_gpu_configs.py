@@ -1,0 +1,218 @@
+"""GPU parity on the five measured workloads, at their full sizes, against the fp64 oracle.
+
+* tiny (1x16, V=1024, fp32) and single (1x256, V=32768): the full denoising loop, GPU and
+  oracle each running their own loop from the same initial state (the canvas is renoised
+  from the same counters on both sides; logits are precomputed per step), every step
+  compared; self-conditioning compared on every row (tiny) or sampled rows (single).
+* batched (8x256, V=262144, d=4096, h=16384): one step plus self-conditioning; two whole
+  canvases and sampled feedback rows against the oracle.
+* sweep (64x256, V=262144): the full loop until every canvas converges or hits the step
+  cap, in the launch configuration the benchmark uses; two canvases followed by the oracle
+  over every step, feedback rows sampled at the first self-conditioned step.
+* ragged (32x256, V=152064, d=3584, h=18944): one step with converged (masked), read-only
+  and normal canvases at mixed temperatures; sampled canvases of every role.
+Decision outputs are bit-exact except counted boundary positions (1e-6 relative);
+entropies within 1e-5 relative; feedback rows within 2e-2 relative (bf16 tensor cores)."""
+import numpy as np
+import pytest
+import torch
+
+import entropy_bounded_denoising_gb300 as dg
+from entropy_bounded_denoising_gb300 import synth
+import oracle
+
+from helpers import DELTA_RTOL, StepBuffers, compare_step, delta_rel_err, run_step
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+SEED = 0x5EED1234ABCD
+
+
+def _subset(p, idx):
+    return {k: np.asarray(v)[idx].copy() for k, v in p.items()}
+
+
+def _weights(wl, device):
+    E, Wg, Wu, Wd = synth.weights(wl.V, wl.d, wl.h, seed=wl.seed, device=device)
+    bits = tuple(synth.bf16_bits(t) for t in (E, Wg, Wu, Wd))
+    return (E, Wg, Wu, Wd), bits
+
+
+def _self_cond(x_dev, b, pt, n, L, wts, V):
+    E, Wg, Wu, Wd = wts
+    d, h = E.shape[1], Wg.shape[0]
+    delta = torch.full((n, L, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(dg.dg_self_cond_workspace_bytes(n, L, d, h), dtype=torch.uint8, device=DEV)
+    dg.dg_self_cond_logits(x_dev, b.lse, pt, b.converged, E, Wg, Wu, Wd, delta, ws, V=V)
+    return delta
+
+
+def _loop(wl, sc_from_step, check_rows_per_step):
+    """Full loop for a single-canvas (or few-canvas) workload; returns steps run."""
+    n, L, V = wl.n, wl.L, wl.V
+    wts, bits = _weights(wl, DEV)
+    base = synth.canvas_params(wl, step=0)
+    canvas0 = oracle.canvas_init(n, L, V, base, SEED)
+    # GPU state
+    b = StepBuffers.make(n, L, DEV, canvas0)
+    pt_init = dg.params_tensor(base, DEV)
+    gcanvas = torch.zeros((n, L), dtype=torch.int32, device=DEV)
+    dg.dg_canvas_init(gcanvas, n, L, V, pt_init, SEED)
+    assert (gcanvas.cpu().numpy() == canvas0).all()
+    # oracle state
+    o_canvas, o_prev, o_stable = canvas0.copy(), np.full((n, L), -1, np.int32), np.zeros(n, np.int32)
+    active = np.ones(n, bool)
+    steps = 0
+    for t in range(int(base["max_steps"].max())):
+        if not active.any():
+            break
+        p = synth.params_with(base, step=t)
+        p["flags"] = np.where(active, dg.DG_ACTIVE | (dg.DG_SELF_COND if t >= sc_from_step else 0), 0).astype(np.uint32)
+        x = synth.logits(n, L, V, seed=wl.seed, step=t, scale=wl.scale, spike_frac=wl.spike_frac, dtype=wl.dtype)
+        xd = x.to(DEV)
+        pt = dg.params_tensor(p, DEV)
+        g_in = b.host()
+        run_step(xd, pt, SEED, b, V=V)
+        delta = _self_cond(xd, b, pt, n, L, wts, V) if t >= sc_from_step else None
+        torch.cuda.synchronize()
+        assert dg.dg_get_device_status() == 0
+        g = b.host()
+        hx = synth.host_logits(x)
+        o = oracle.denoise_step(hx, p, SEED, o_canvas, o_prev, o_stable)
+        rep = compare_step(g, o, p, V, SEED, g_in["canvas"], g_in["prev"], g_in["stable"], g_in=g_in)
+        o_canvas, o_prev, o_stable = o["canvas"], o["prev_argmax"], o["stable_count"]
+        if delta is not None:
+            dh = delta.float().cpu().numpy()
+            for c in range(n):
+                if not active[c]:
+                    continue
+                rows = range(L) if check_rows_per_step is None else \
+                    np.random.default_rng(t * 7 + c).choice(L, check_rows_per_step, replace=False)
+                rows = sorted(rows)
+                if o["converged"][c]:
+                    assert (dh[c] == 0).all()
+                    continue
+                ref = oracle.self_cond_rows(hx[c][rows], np.full(len(rows), float(p["temperature"][c])), *bits, V=V)
+                err = delta_rel_err(dh[c][rows], ref)
+                assert err.max() <= DELTA_RTOL, (t, c, err.max())
+        active &= ~o["converged"].astype(bool)
+        steps += 1
+        print(f"step {t}: {rep}")
+    return steps
+
+
+def test_tiny_full_loop():
+    wl = synth.WORKLOADS["tiny"]
+    steps = _loop(wl, sc_from_step=1, check_rows_per_step=None)
+    assert 1 <= steps <= wl.steps
+
+
+def test_single_full_loop():
+    wl = synth.WORKLOADS["single"]
+    steps = _loop(wl, sc_from_step=1, check_rows_per_step=4)
+    assert 1 <= steps <= wl.steps
+
+
+def _one_step(wl, check_canvases, sc_rows, params):
+    n, L, V = wl.n, wl.L, wl.V
+    x = synth.logits(n, L, V, seed=wl.seed, step=1, scale=wl.scale, spike_frac=wl.spike_frac, device=DEV)
+    wts, bits = _weights(wl, DEV)
+    rng = np.random.default_rng(wl.seed)
+    canvas0 = rng.integers(0, V, (n, L)).astype(np.int32)
+    b = StepBuffers.make(n, L, DEV, canvas0)
+    pt = dg.params_tensor(params, DEV)
+    dg.dg_clear_device_status()
+    run_step(x, pt, SEED, b)
+    delta = _self_cond(x, b, pt, n, L, wts, V)
+    torch.cuda.synchronize()
+    assert dg.dg_get_device_status() == 0
+    g = b.host()
+    dh = delta.float().cpu().numpy()
+    for c in check_canvases:
+        hx = synth.host_logits(x[c:c + 1])
+        pc = _subset(params, [c])
+        o = oracle.denoise_step(hx, pc, SEED, canvas0[c:c + 1], np.full((1, L), -1, np.int32), np.zeros(1, np.int32))
+        gc = {k: v[c:c + 1] for k, v in g.items()}
+        rep = compare_step(gc, o, pc, V, SEED, canvas0[c:c + 1], np.full((1, L), -1, np.int32), np.zeros(1, np.int32))
+        print(f"canvas {c} (flags {params['flags'][c]}): {rep}")
+    for (c, i) in sc_rows:
+        hx = synth.host_logits(x[c, i:i + 1])
+        ref = oracle.self_cond_rows(hx, np.array([float(params["temperature"][c])]), *bits, V=V)
+        err = delta_rel_err(dh[c, i:i + 1], ref)
+        assert err.max() <= DELTA_RTOL, (c, i, err.max())
+    return g, dh, canvas0
+
+
+def test_batched_full_size():
+    wl = synth.WORKLOADS["batched"]
+    p = synth.canvas_params(wl, step=1)
+    g, dh, _ = _one_step(wl, check_canvases=[0, 5], sc_rows=[(0, 3), (5, 200), (7, 255)], params=p)
+    assert (g["converged"] == 0).all() and np.isfinite(dh).all()
+
+
+def test_ragged_full_size():
+    wl = synth.WORKLOADS["ragged"]
+    p = synth.canvas_params(wl, step=1)
+    flags = p["flags"]
+    conv = [c for c in range(wl.n) if flags[c] == 0]
+    ro = [c for c in range(wl.n) if flags[c] & dg.DG_READ_ONLY]
+    normal = [c for c in range(wl.n) if (flags[c] & dg.DG_SELF_COND)]
+    g, dh, canvas0 = _one_step(wl, check_canvases=[normal[0], normal[-1], ro[0]],
+                               sc_rows=[(normal[0], 0), (normal[-1], 129)], params=p)
+    for c in conv:   # masked canvases: never read, nothing written, no feedback
+        assert (g["canvas"][c] == canvas0[c]).all() and (g["argmax"][c] == -7).all()
+        assert (dh[c] == 0).all()
+    for c in ro:     # single-pass reads: statistics only, converged, no feedback
+        assert g["converged"][c] == 1 and (g["accept"][c] == 0).all() and (g["sample"][c] == -1).all()
+        assert (g["canvas"][c] == canvas0[c]).all() and (dh[c] == 0).all()
+
+
+def test_sweep_full_loop():
+    """64 canvases to convergence on the GPU; canvases 0 and 37 followed by the oracle."""
+    wl = synth.WORKLOADS["sweep"]
+    n, L, V = wl.n, wl.L, wl.V
+    follow = [0, 37]
+    wts, bits = _weights(wl, DEV)
+    base = synth.canvas_params(wl, step=0)
+    base["flags"][:] = dg.DG_ACTIVE | dg.DG_SELF_COND
+    pt = dg.params_tensor(base, DEV)
+    b = StepBuffers.make(n, L, DEV)
+    dg.dg_canvas_init(b.canvas, n, L, V, pt, SEED)
+    canvas0 = b.canvas.cpu().numpy()
+    d, h = wl.d, wl.h
+    delta = torch.empty((n, L, d), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(dg.dg_self_cond_workspace_bytes(n, L, d, h), dtype=torch.uint8, device=DEV)
+    E, Wg, Wu, Wd = wts
+    pf = _subset(base, follow)
+    o_canvas, o_prev, o_stable = canvas0[follow].copy(), np.full((2, L), -1, np.int32), np.zeros(2, np.int32)
+    o_active = np.ones(2, bool)
+    steps = 0
+    for t in range(wl.steps):
+        flags_now = dg.unpack_params(pt)["flags"]
+        if not (flags_now & dg.DG_ACTIVE).any():
+            break
+        x = synth.logits(n, L, V, seed=wl.seed, step=t, scale=wl.scale, device=DEV)
+        g_in = {k: v[follow] for k, v in b.host().items()}
+        run_step(x, pt, SEED, b)
+        dg.dg_self_cond_logits(x, b.lse, pt, b.converged, E, Wg, Wu, Wd, delta, ws)
+        torch.cuda.synchronize()
+        assert dg.dg_get_device_status() == 0
+        g = {k: v[follow] for k, v in b.host().items()}
+        if o_active.any():
+            pf["step"][:] = t
+            pf["flags"] = np.where(o_active, dg.DG_ACTIVE | dg.DG_SELF_COND, 0).astype(np.uint32)
+            hx = synth.host_logits(x[follow])
+            o = oracle.denoise_step(hx, pf, SEED, o_canvas, o_prev, o_stable)
+            rep = compare_step(g, o, pf, V, SEED, g_in["canvas"], g_in["prev"], g_in["stable"], g_in=g_in)
+            print(f"step {t}: {rep}")
+            if t == 0:
+                dh = delta.float().cpu().numpy()
+                for j, c in enumerate(follow):
+                    ref = oracle.self_cond_rows(hx[j, [17]], np.array([float(pf["temperature"][j])]), *bits, V=V)
+                    assert delta_rel_err(dh[c, [17]], ref).max() <= DELTA_RTOL
+            o_canvas, o_prev, o_stable = o["canvas"], o["prev_argmax"], o["stable_count"]
+            o_active &= ~o["converged"].astype(bool)
+        dg.dg_advance_params(pt, b.converged, n)
+        steps += 1
+    print(f"sweep ran {steps} steps")
+    assert steps >= 2

@@ -56,7 +56,7 @@ def _dist():
 class ClockSampler:
     """nvidia-smi clock / throttle samples while the timed region runs."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -79,7 +79,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -90,18 +93,25 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        """Median SM clock and throttle reasons over the samples taken inside the timed
+        region (all samples if none fell inside)."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        t0, t1 = getattr(self, "t_start", None), getattr(self, "t_end", None)
+        rows = self.lines
+        if t0 is not None and t1 is not None:
+            inside = [r for r in rows if t0 <= r[0] <= t1 + 0.25]
+            rows = inside or rows
+        for _, ln in rows:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx = float(parts[1])
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
             except ValueError:
                 continue
-            for nm, v in zip(names, parts[4:8]):
+            for nm, v in zip(names, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
         if not sm:
@@ -168,14 +178,20 @@ def _oracle_sample(wl, x_canvas_host, weights_host, p, n_sc_rows: int, threads: 
 
 
 def run_reference(args):
-    """The oracle as it stands, on the host cores, as the comparison arm."""
+    """The oracle as it stands, on the host cores, as the comparison arm.
+
+    One step = the oracle's denoise step on a slice of positions of canvas 0 plus, in every
+    m-th step, its self-conditioning on one position; m and the slice are set from the
+    warm-up timings so that the K timed steps take about two minutes.  The value is
+    positions/s with the per-position cost = (denoise time / positions) + (feedback time /
+    feedback rows) over the timed steps."""
     ws, rank, _ = _dist()
     if rank != 0:
         return 0
     import oracle
     from entropy_bounded_denoising_gb300 import synth
-    import torch
     wl = synth.WORKLOADS[args.workload]
+    oracle.build()
     threads = oracle.max_threads()
     p = synth.canvas_params(wl, step=1)
     x = synth.logits(1, wl.L, wl.V, seed=wl.seed, step=1, scale=wl.scale, spike_frac=wl.spike_frac,
@@ -183,17 +199,40 @@ def run_reference(args):
     xh = synth.host_logits(x)[0]
     E, Wg, Wu, Wd = synth.weights(wl.V, wl.d, wl.h, seed=wl.seed)
     wh = tuple(synth.bf16_bits(t) for t in (E, Wg, Wu, Wd))
-    n_sc = 2
-    for _ in range(args.warmup):
-        _oracle_sample(wl, xh, wh, p, n_sc, threads)
-    times = []
-    for _ in range(args.steps):
-        per_pos, _, _ = _oracle_sample(wl, xh, wh, p, n_sc, threads)
-        times.append(per_pos)
-    per_pos = float(np.mean(times))
+    p1 = {k: v[:1].copy() for k, v in p.items()}
+
+    def denoise(rows):
+        t0 = time.perf_counter()
+        oracle.denoise_step(xh[None, :rows], p1, 7, np.zeros((1, rows), np.int32), np.full((1, rows), -1, np.int32),
+                            np.zeros(1, np.int32), n_threads=threads)
+        return time.perf_counter() - t0
+
+    def feedback():
+        t0 = time.perf_counter()
+        oracle.self_cond_rows(xh[:1], np.full(1, float(p["temperature"][0])), *wh, V=wl.V, n_threads=threads)
+        return time.perf_counter() - t0
+
+    # warm-up: unit costs
+    rows = min(wl.L, max(1, threads))
+    c_dn, c_sc = denoise(rows) / rows, feedback()
+    for _ in range(max(0, args.warmup - 1)):
+        c_dn = denoise(rows) / rows
+    budget = 120.0 / max(1, args.steps)               # seconds per timed step
+    rows = int(min(wl.L, max(1, (0.5 * budget) / max(c_dn, 1e-9))))
+    every = max(1, int(np.ceil(c_sc / max(0.5 * budget, 1e-9))))
+    t_dn = t_sc = 0.0
+    n_dn = n_sc = 0
+    for k in range(args.steps):
+        t_dn += denoise(rows)
+        n_dn += rows
+        if k % every == 0:
+            t_sc += feedback()
+            n_sc += 1
+    per_pos = t_dn / n_dn + t_sc / max(1, n_sc)
     value = 1.0 / per_pos
-    sample = (f"per step: denoise oracle on 1 canvas ({wl.L} positions x V={wl.V}) plus "
-              f"self-conditioning on {n_sc} rows, extrapolated per position")
+    sample = (f"per step: oracle denoise on {rows} positions of canvas 0 (V={wl.V}); oracle self-conditioning "
+              f"on one position every {every} step(s) ({n_sc} in total); per-position cost = denoise time / "
+              f"positions + feedback time / feedback rows")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_pos * wl.n * wl.L * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -276,18 +315,21 @@ def run_ours(args):
     dg.dg_clear_device_status()
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    launches0 = dg.dg_launch_count()
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        time.sleep(0.3)  # let nvidia-smi start sampling before the timed region
+        clk.mark("t_start")
+        launches0 = dg.dg_launch_count()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for k in range(args.steps):
             step(evs[k])
         end.record(stream)
+        launches = dg.dg_launch_count() - launches0
         torch.cuda.synchronize()
+        clk.mark("t_end")
     barrier()
-    launches = dg.dg_launch_count() - launches0
     elapsed_ms = start.elapsed_time(end)
     status = dg.dg_get_device_status()
     if status:
@@ -365,7 +407,7 @@ def run_ours(args):
         threads = oracle.max_threads()
         xh0 = synth.host_logits(x[0])
         wh = tuple(synth.bf16_bits(t) for t in (E, Wg, Wu, Wd))
-        n_sc = 4
+        n_sc = max(1, min(16, threads))
         per_pos, t_dn_cpu, t_sc_cpu = _oracle_sample(wl, xh0, wh, p, n_sc, threads)
         cpu = {"value": 1.0 / per_pos, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": (f"denoise oracle on canvas 0 ({L} positions x V={V}, {t_dn_cpu:.1f} s) plus "
@@ -399,10 +441,10 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="batched", choices=["batched", "sweep", "ragged", "single", "profile"])
+    ap.add_argument("--workload", default="batched", choices=["batched", "sweep", "ragged", "single", "tiny", "profile"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

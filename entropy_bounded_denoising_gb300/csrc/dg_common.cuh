@@ -34,17 +34,25 @@ constexpr uint32_t kStreamGumbel = 0u;
 constexpr uint32_t kStreamRenoise = 1u;
 constexpr uint32_t kStreamInit = 2u;
 
+// 32 x 32 -> 64-bit product as (lo, hi).
+DG_DEVINL void mul_wide(uint32_t a, uint32_t b, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b64 t;\n\tmul.wide.u32 t, %2, %3;\n\tmov.b64 {%0, %1}, t;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(a), "r"(b));
+}
+
 // Ten rounds: each multiplies the even words, swaps halves and mixes in the round key,
 // the key advancing by the Weyl constants between rounds.
 DG_DEVINL u4 philox10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        const uint64_t p0 = (uint64_t)kPhiloxM0 * c0;
-        const uint64_t p1 = (uint64_t)kPhiloxM1 * c2;
-        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ (k0 + (uint32_t)r * kPhiloxW0);
-        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ (k1 + (uint32_t)r * kPhiloxW1);
-        c1 = (uint32_t)p1;
-        c3 = (uint32_t)p0;
+        uint32_t lo0, hi0, lo1, hi1;
+        mul_wide(c0, kPhiloxM0, lo0, hi0);
+        mul_wide(c2, kPhiloxM1, lo1, hi1);
+        const uint32_t n0 = hi1 ^ c1 ^ (k0 + (uint32_t)r * kPhiloxW0);
+        const uint32_t n2 = hi0 ^ c3 ^ (k1 + (uint32_t)r * kPhiloxW1);
+        c1 = lo1;
+        c3 = lo0;
         c0 = n0;
         c2 = n2;
     }

@@ -48,7 +48,9 @@ struct RowState {  // online softmax state of a set of entries, z measured in lo
     int idx;       // smallest index attaining m
 };
 
+template <int DT>
 struct K1Shared {
+    static constexpr int kQW = DT == 0 ? 2 : 4;  // words per queued group (4 bf16 or 4 fp32)
     uint64_t full[kSlots];
     uint64_t empty[kSlots];
     RowState warp_state[kK1Warps];
@@ -57,7 +59,10 @@ struct K1Shared {
     unsigned best_key;  // CTA-wide best score so far, order-preserving integer encoding
     int bad;
     int timeout;
-    int queue[kK1Warps][96];  // per-warp candidate groups awaiting their Gumbel draw
+    // per-warp candidate groups awaiting their Gumbel draw: first entry index and the 4
+    // logits (as raw words), so a queued group outlives the ring slot it came from
+    int q_e0[kK1Warps][96];
+    uint32_t q_x[kK1Warps][96][kQW];
 };
 
 DG_DEVINL float ex2(float x) {
@@ -168,30 +173,12 @@ struct Vec<1> {  // fp32: 4 entries
     }
 };
 
-// Gumbel draw for one group of 4 consecutive entries (one Philox block), entries
-// [e0, e0 + 4) of the row held in `slot` from row entry `slot_e0` on.  Keeps (best, bidx)
-// as the largest score y + g, y = x / T, ties to the lower index.  `bound` is a score some
-// entry of the row is known to reach; entries that cannot reach it are not drawn.
-template <int DT>
-DG_DEVINL void eval_group(const unsigned char* slot, int slot_e0, int e0, int64_t V, float invT, uint32_t pos,
-                          uint32_t step, uint32_t c3, uint32_t k0, uint32_t k1, float bound, float& best,
-                          int& bidx) {
-    constexpr int ES = DT == 0 ? 2 : 4;
-    float x[4];
-    const unsigned char* p = slot + (size_t)(e0 - slot_e0) * ES;
-    if (DT == 0) {
-        const uint2 q = *reinterpret_cast<const uint2*>(p);
-        x[0] = __uint_as_float(q.x << 16);
-        x[1] = __uint_as_float(q.x & 0xffff0000u);
-        x[2] = __uint_as_float(q.y << 16);
-        x[3] = __uint_as_float(q.y & 0xffff0000u);
-    } else {
-        const float4 q = *reinterpret_cast<const float4*>(p);
-        x[0] = q.x;
-        x[1] = q.y;
-        x[2] = q.z;
-        x[3] = q.w;
-    }
+// Gumbel draw for one group of 4 consecutive entries (one Philox block) [e0, e0 + 4) with
+// logits x.  Keeps (best, bidx) as the largest score y + g, y = x / T, ties to the lower
+// index.  `bound` is a score some entry of the row is known to reach; entries that cannot
+// reach it are not drawn.
+DG_DEVINL void eval_group(const float (&x)[4], int e0, int64_t V, float invT, uint32_t pos, uint32_t step,
+                          uint32_t c3, uint32_t k0, uint32_t k1, float bound, float& best, int& bidx) {
     const dg::u4 w = dg::philox10((uint32_t)e0 >> 2, pos, step, c3, k0, k1);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -211,6 +198,33 @@ DG_DEVINL void eval_group(const unsigned char* slot, int slot_e0, int e0, int64_
     }
 }
 
+// Raw words <-> 4 logits of a group (bf16 pairs or fp32).
+template <int DT, int N>
+DG_DEVINL void group_words(const float (&x)[N], int g, uint32_t (&w)[4]) {
+    if (DT == 0) {
+        w[0] = (__float_as_uint(x[4 * g]) >> 16) | (__float_as_uint(x[4 * g + 1]) & 0xffff0000u);
+        w[1] = (__float_as_uint(x[4 * g + 2]) >> 16) | (__float_as_uint(x[4 * g + 3]) & 0xffff0000u);
+        w[2] = 0u;
+        w[3] = 0u;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = __float_as_uint(x[4 * g + i]);
+    }
+}
+
+template <int DT>
+DG_DEVINL void words_group(const uint32_t* w, float (&x)[4]) {
+    if (DT == 0) {
+        x[0] = __uint_as_float(w[0] << 16);
+        x[1] = __uint_as_float(w[0] & 0xffff0000u);
+        x[2] = __uint_as_float(w[1] << 16);
+        x[3] = __uint_as_float(w[1] & 0xffff0000u);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = __uint_as_float(w[i]);
+    }
+}
+
 // ------------------------------------------------------------------------------------
 // K1: per-position statistics and Gumbel-max sample.  grid (L, n), one CTA per position.
 // ------------------------------------------------------------------------------------
@@ -225,8 +239,10 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
     constexpr int GPV = VN / 4;                    // Philox blocks per 16-byte vector
     constexpr int kPieceElems = kPieceBytes / ES;
     extern __shared__ __align__(128) unsigned char k1_smem[];
-    K1Shared& sh = *reinterpret_cast<K1Shared*>(k1_smem);
-    unsigned char* ring = k1_smem + ((sizeof(K1Shared) + 127) / 128) * 128;
+    using Shared = K1Shared<DT>;
+    constexpr int QW = Shared::kQW;
+    Shared& sh = *reinterpret_cast<Shared*>(k1_smem);
+    unsigned char* ring = k1_smem + ((sizeof(Shared) + 127) / 128) * 128;
 
     const int pos = blockIdx.x;
     const int64_t canvas = blockIdx.y;
@@ -292,7 +308,9 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
         const uint32_t k0 = (uint32_t)seed, k1 = p.request_id;
         const uint32_t c3 = dg::ctr_word3(seed, dg::kStreamGumbel);
         const uint32_t step = (uint32_t)p.step;
-        int* queue = sh.queue[warp];
+        int* q_e0 = sh.q_e0[warp];
+        uint32_t(*q_x)[QW] = sh.q_x[warp];
+        int qn = 0;  // warp-uniform queue length, kept across pieces
         const unsigned lt = (1u << lane) - 1u;
         for (int q = 0; q < npieces; ++q) {
             const int sl = q % kSlots;
@@ -306,14 +324,13 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
             const int nvec = (n_el + VN - 1) / VN;
             // candidate threshold on the raw logit: x / T + G_max >= best - slack
             float x_thr = (fmaxf(bound, best) - kGumbelMax - kCandidateSlack) * p.temperature;
-            int qn = 0;
             for (int j0 = warp * 32; j0 < nvec; j0 += kK1Warps * 32) {
                 const int j = j0 + lane;
                 bool cand[GPV];
 #pragma unroll
                 for (int g = 0; g < GPV; ++g) cand[g] = false;
+                float x[VN], e[VN];  // logits and e = exp((x - m) / T) against the lane's running max m
                 if (j < nvec) {
-                    float x[VN];
                     Vec<DT>::load(slot + (size_t)j * 16, x);
                     const int base = j * VN;
                     if (base + VN > n_el) {
@@ -350,52 +367,118 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
                     if (vmax == st.m) {
                         if (vmax == -INFINITY) {
 #pragma unroll
-                            for (int i = 0; i < VN; ++i) bad |= (x[i] != x[i]);
+                            for (int i = 0; i < VN; ++i) {
+                                bad |= (x[i] != x[i]);
+                                e[i] = 0.f;
+                            }
                         } else {
 #pragma unroll
                             for (int i = 0; i < VN; ++i) {
                                 if (x[i] == st.m) {
                                     st.c += 1.f;
+                                    e[i] = 1.f;
                                 } else {
                                     // -inf entries (masked tail, or -inf logits) contribute e = 0;
                                     // the clamp keeps e * d at 0 instead of 0 * -inf
-                                    const float d = max_nan((x[i] - st.m) * k2, kMinExponent), e = ex2(d);
-                                    st.r += e;
-                                    st.t = fmaf(e, d, st.t);
+                                    const float d = max_nan((x[i] - st.m) * k2, kMinExponent);
+                                    e[i] = ex2(d);
+                                    st.r += e[i];
+                                    st.t = fmaf(e[i], d, st.t);
                                 }
                             }
                         }
                     } else {
 #pragma unroll
                         for (int i = 0; i < VN; ++i) {
-                            const float d = max_nan((x[i] - st.m) * k2, kMinExponent), e = ex2(d);
-                            st.r += e;
-                            st.t = fmaf(e, d, st.t);
+                            const float d = max_nan((x[i] - st.m) * k2, kMinExponent);
+                            e[i] = ex2(d);
+                            st.r += e[i];
+                            st.t = fmaf(e[i], d, st.t);
                         }
                     }
                     if (do_sample) {
 #pragma unroll
                         for (int g = 0; g < GPV; ++g) cand[g] = gmax[g] >= x_thr;
                     }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < VN; ++i) {
+                        x[i] = -INFINITY;
+                        e[i] = 0.f;
+                    }
+                }
+                if (!do_sample) continue;
+                const float bnd = fmaxf(bound, best);
+                bool any = false;
+#pragma unroll
+                for (int g = 0; g < GPV; ++g) any |= cand[g];
+                const unsigned dense_mk = __ballot_sync(0xffffffffu, any);
+                if (bnd > -INFINITY && __popc(dense_mk) >= 16) {
+                    // Dense: most lanes hold candidates, so every lane draws its own groups' noise.
+                    // exp(y - bnd) = e * exp(m / T - bnd) reuses the softmax term; entries with
+                    // u <= 1 - 2 exp(y - bnd) cannot beat the bound (see eval_group).
+                    const float cb = ex2((st.m * invT - bnd) * kLog2e);
+                    const float nscale = -2.f * cb;
+#pragma unroll
+                    for (int g = 0; g < GPV; ++g) {
+                        if (!cand[g]) continue;
+                        const int e0 = e_lo + (j * GPV + g) * 4;
+                        const dg::u4 w = dg::philox10((uint32_t)e0 >> 2, (uint32_t)pos, step, c3, k0, k1);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float u = dg::uniform_from_word(word_of(w, i));
+                            if (!(u > fmaf(nscale, e[4 * g + i], 1.f))) continue;
+                            if (e0 + i >= V) continue;
+                            const float score = x[4 * g + i] * invT + (-logf(-logf(u)));
+                            if (better(score, e0 + i, best, bidx)) {
+                                best = score;
+                                bidx = e0 + i;
+                            }
+                        }
+                    }
+                    warp_best(best, bidx);
+                    x_thr = (fmaxf(bound, best) - kGumbelMax - kCandidateSlack) * p.temperature;
+                    continue;
                 }
                 if (!do_sample) continue;
                 // queue the candidate groups (ballot-compacted) and draw 32 at a time
 #pragma unroll
                 for (int g = 0; g < GPV; ++g) {
                     const unsigned mk = __ballot_sync(0xffffffffu, cand[g]);
-                    if (cand[g]) queue[qn + __popc(mk & lt)] = e_lo + (j * GPV + g) * 4;
+                    if (cand[g]) {
+                        const int at = qn + __popc(mk & lt);
+                        uint32_t wv[4];
+                        group_words<DT>(x, g, wv);
+                        q_e0[at] = e_lo + (j * GPV + g) * 4;
+#pragma unroll
+                        for (int i = 0; i < QW; ++i) q_x[at][i] = wv[i];
+                    }
                     qn += __popc(mk);
                 }
                 __syncwarp();
                 while (qn >= 32) {  // at most 31 + 32 * GPV < 96 entries are queued
-                    eval_group<DT>(slot, e_lo, queue[lane], V, invT, (uint32_t)pos, step, c3, k0, k1, bound, best, bidx);
+                    {
+                        float xg[4];
+                        words_group<DT>(q_x[lane], xg);
+                        eval_group(xg, q_e0[lane], V, invT, (uint32_t)pos, step, c3, k0, k1, bound, best, bidx);
+                    }
                     __syncwarp();
                     const int rest = qn - 32;  // move the unprocessed tail to the front
                     for (int r0 = 0; r0 < rest; r0 += 32) {
                         const int r = r0 + lane;
-                        const int v = r < rest ? queue[32 + r] : 0;
+                        int e0v = 0;
+                        uint32_t wv[4] = {0u, 0u, 0u, 0u};
+                        if (r < rest) {
+                            e0v = q_e0[32 + r];
+#pragma unroll
+                            for (int i = 0; i < QW; ++i) wv[i] = q_x[32 + r][i];
+                        }
                         __syncwarp();
-                        if (r < rest) queue[r] = v;
+                        if (r < rest) {
+                            q_e0[r] = e0v;
+#pragma unroll
+                            for (int i = 0; i < QW; ++i) q_x[r][i] = wv[i];
+                        }
                         __syncwarp();
                     }
                     qn = rest;
@@ -404,10 +487,6 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
                 }
             }
             if (do_sample) {
-                // the queue refers to this slot: drain it (fewer than 32 left) before the slot is released
-                if (lane < qn)
-                    eval_group<DT>(slot, e_lo, queue[lane], V, invT, (uint32_t)pos, step, c3, k0, k1, bound, best, bidx);
-                warp_best(best, bidx);
                 // share the best score with the other warps, take theirs
                 if (lane == 0 && best > -INFINITY) atomicMax(&sh.best_key, float_key(best));
                 __syncwarp();
@@ -416,6 +495,12 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
             __syncwarp();
             if (lane == 0) dg::mbar_arrive(&sh.empty[sl]);
         }
+        if (do_sample && lane < qn) {  // the last (fewer than 32) queued groups
+            float xg[4];
+            words_group<DT>(q_x[lane], xg);
+            eval_group(xg, q_e0[lane], V, invT, (uint32_t)pos, step, c3, k0, k1, bound, best, bidx);
+        }
+        __syncwarp();
         if (bad) sh.bad = 1;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) st = merge(st, shfl_state(st, o), k2);
@@ -596,14 +681,15 @@ bool k1_supported(dg_dtype dt, int64_t V) {
     return V * es < (1LL << 31);
 }
 
-size_t k1_smem_bytes() { return ((sizeof(K1Shared) + 127) / 128) * 128 + (size_t)kSlots * kPieceBytes; }
+template <int DT>
+size_t k1_smem_bytes() { return ((sizeof(K1Shared<DT>) + 127) / 128) * 128 + (size_t)kSlots * kPieceBytes; }
 
 template <int DT>
 dg_status launch_k1(const void* logits, int64_t ld, int64_t n, int32_t L, int64_t V,
                     const dg_canvas_params* params, uint64_t seed, int32_t* argmax, int32_t* sample, float* entropy,
                     float* lse, cudaStream_t stream) {
     auto kern = k1_row_stats<DT>;
-    const size_t smem = k1_smem_bytes();
+    const size_t smem = k1_smem_bytes<DT>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DG_ERR_CUDA;
     const int64_t ld_bytes = ld * (DT == 0 ? 2 : 4);

@@ -497,7 +497,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 }
 
 // ------------------------------------------------------------------ split-K fix-up
-// One CTA per tile: adds the k-slice partials in slice order and applies the epilogue.
+// Adds the k-slice partials of each tile in slice order and applies the epilogue.  Plain
+// stores (fp32 / bf16): every thread owns 4 consecutive columns (float4 loads, coalesced
+// across the warp) and the tiles are spread over gridDim.y CTAs each.  The GELU and scatter
+// epilogues (32-column groups) take the generic loop.
 template <int BN>
 __global__ void __launch_bounds__(256) k_fixup(const GemmArgs a) {
     const int mt = active_m_tiles(a);
@@ -505,6 +508,46 @@ __global__ void __launch_bounds__(256) k_fixup(const GemmArgs a) {
     const int64_t t = blockIdx.x;
     if (t >= T) return;
     const int n = (int)(t / mt), m = (int)(t % mt);
+    if (a.epi == EPI_F32 || a.epi == EPI_BF16) {
+        constexpr int kQuads = BM * BN / 4;
+        const int per_cta = (kQuads + gridDim.y - 1) / gridDim.y;
+        const int q0 = blockIdx.y * per_cta, q1 = min(kQuads, q0 + per_cta);
+        for (int qd = q0 + threadIdx.x; qd < q1; qd += blockDim.x) {
+            const int row = qd / (BN / 4);
+            const int col = (qd % (BN / 4)) * 4;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s = 0; s < a.splits; ++s) {
+                const float4 v = *reinterpret_cast<const float4*>(
+                    a.partial + (size_t)(s * T + t) * (BM * BN) + (size_t)row * BN + col);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            const int64_t r = (int64_t)m * BM + row;
+            const int c0 = n * BN + col;
+            if (a.epi == EPI_F32) {
+                if (r >= a.m_valid) continue;
+                float* o = static_cast<float*>(a.out) + r * a.ldo + c0;
+                const float vv[4] = {acc.x, acc.y, acc.z, acc.w};
+                for (int i = 0; i < 4; ++i)
+                    if (c0 + i < a.n_valid) o[i] = vv[i];
+            } else {
+                uint16_t* o = static_cast<uint16_t*>(a.out) + r * a.ldo + c0;
+                const uint32_t p0 = pack_bf16x2(acc.x, acc.y), p1 = pack_bf16x2(acc.z, acc.w);
+                if (c0 + 4 <= a.n_valid && ((reinterpret_cast<uintptr_t>(o) & 7u) == 0)) {
+                    *reinterpret_cast<uint2*>(o) = make_uint2(p0, p1);
+                } else {
+                    const uint16_t hv[4] = {(uint16_t)(p0 & 0xFFFFu), (uint16_t)(p0 >> 16), (uint16_t)(p1 & 0xFFFFu),
+                                            (uint16_t)(p1 >> 16)};
+                    for (int i = 0; i < 4; ++i)
+                        if (c0 + i < a.n_valid) o[i] = hv[i];
+                }
+            }
+        }
+        return;
+    }
+    if (blockIdx.y != 0) return;
     constexpr int kGroups = BM * (BN / 32);  // (row, 32-column chunk) pairs
     for (int gidx = threadIdx.x; gidx < kGroups; gidx += blockDim.x) {
         const int row = gidx / (BN / 32);
@@ -677,7 +720,10 @@ dg_status launch_gemm(const void* tmA, const void* tmB0, const void* tmB1, const
     if (e != cudaSuccess) return DG_ERR_CUDA;
     if (a.splits > 1) {
         const int64_t T = (int64_t)a.m_tiles * a.n_tiles;
-        k_fixup<C::BN><<<(unsigned)T, 256, 0, stream>>>(a);
+        // spread each tile over enough CTAs to fill the GPU a few times
+        const int P = dghost::sm_count();
+        const unsigned per_tile = (unsigned)std::max<int64_t>(1, std::min<int64_t>(16, (4LL * P + T - 1) / T));
+        k_fixup<C::BN><<<dim3((unsigned)T, per_tile, 1), 256, 0, stream>>>(a);
         dghost::count_launch();
         e = cudaGetLastError();
     }

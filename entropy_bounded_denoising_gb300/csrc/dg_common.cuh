@@ -59,6 +59,52 @@ DG_DEVINL u4 philox10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32
     return u4{c0, c1, c2, c3};
 }
 
+// Philox-4x32-10 for many counters that differ only in word 0 (the Gumbel stream of one
+// position): the parts of the first two rounds that do not depend on word 0 are computed
+// once.  philox10_c0(c0, philox_pre(c1, c2, c3, k0, k1)) == philox10(c0, c1, c2, c3, k0, k1).
+struct PhiloxPre {
+    uint32_t c3k1;  // round 1: c3 ^ k1
+    uint32_t u1;    // round 2: lo(c2 * M1) ^ (k0 + W0)
+    uint32_t u2;    // round 2: hi(n0 * M0) ^ (k1 + W1), n0 = hi(c2 * M1) ^ c1 ^ k0
+    uint32_t w3;    // round 2: lo(n0 * M0), word 3 after the round
+    uint32_t k0, k1;
+};
+
+DG_DEVINL PhiloxPre philox_pre(uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0, uint32_t k1) {
+    PhiloxPre p;
+    uint32_t lo1, hi1, lo0, hi0;
+    mul_wide(c2, kPhiloxM1, lo1, hi1);
+    const uint32_t n0 = hi1 ^ c1 ^ k0;
+    mul_wide(n0, kPhiloxM0, lo0, hi0);
+    p.c3k1 = c3 ^ k1;
+    p.u1 = lo1 ^ (k0 + kPhiloxW0);
+    p.u2 = hi0 ^ (k1 + kPhiloxW1);
+    p.w3 = lo0;
+    p.k0 = k0;
+    p.k1 = k1;
+    return p;
+}
+
+DG_DEVINL u4 philox10_c0(uint32_t c0, const PhiloxPre& p) {
+    uint32_t lo0, hi0, lo1, hi1;
+    mul_wide(c0, kPhiloxM0, lo0, hi0);           // round 1, word 0 product
+    const uint32_t n2 = hi0 ^ p.c3k1;            // round 1, new word 2 (word 3 = lo0)
+    mul_wide(n2, kPhiloxM1, lo1, hi1);           // round 2, word 2 product
+    uint32_t c0r = hi1 ^ p.u1, c1r = lo1, c2r = p.u2 ^ lo0, c3r = p.w3;
+#pragma unroll
+    for (int r = 2; r < 10; ++r) {
+        mul_wide(c0r, kPhiloxM0, lo0, hi0);
+        mul_wide(c2r, kPhiloxM1, lo1, hi1);
+        const uint32_t n0 = hi1 ^ c1r ^ (p.k0 + (uint32_t)r * kPhiloxW0);
+        const uint32_t m2 = hi0 ^ c3r ^ (p.k1 + (uint32_t)r * kPhiloxW1);
+        c1r = lo1;
+        c3r = lo0;
+        c0r = n0;
+        c2r = m2;
+    }
+    return u4{c0r, c1r, c2r, c3r};
+}
+
 // Counter word 3: stream id in the low byte, bits 32..55 of the seed above it.
 DG_DEVINL uint32_t ctr_word3(uint64_t seed, uint32_t stream) {
     return stream | ((uint32_t)((seed >> 32) & 0xFFFFFFu) << 8);

@@ -12,16 +12,22 @@
 //
 // K1 design (GB300): one CTA per canvas position streams its logit row once from HBM.  A
 // producer warp keeps a ring of shared-memory slots filled with bulk copies (the TMA
-// engine); eight consumer warps fold every piece into an online-softmax state (max m,
-// count c of entries equal to m, r = sum of the other e^z, t = sum e^z z -- the split keeps
-// near-one-hot rows accurate in fp32) and the argmax, and in the same pass look for the
-// Gumbel-max winner: an entry whose y + G_max (G_max the largest Gumbel value the uniform
-// mapping can produce) cannot reach the best score seen so far in the CTA is skipped
-// without drawing its noise; the others are queued per warp and drawn 32 groups at a time.
+// engine); eight consumer warps read every piece twice from shared memory.  Pass 1 takes
+// vector maxima with packed bf16x2 instructions and queues the candidate groups of the
+// Gumbel-max search: an entry whose y + G_max (G_max the largest Gumbel value the uniform
+// mapping can produce) cannot reach the best score seen so far is skipped without drawing
+// its noise.  Pass 2 folds the piece into an online-softmax state (max m, count c of
+// entries equal to m, r = sum of the other e^z, t = sum e^z z -- the split keeps
+// near-one-hot rows accurate in fp32) against the warp's running max, which changes only
+// between passes, so no lane diverges on a new maximum.  Queued groups are drawn a warp's
+// worth at a time, with the Philox rounds that do not depend on the entry index computed
+// once per row.
 // The reduction order depends only on V, so a row's result does not depend on its batch.
 #include <cuda_runtime.h>
 
 #include <math.h>
+
+#include <type_traits>
 
 #include "dg_common.cuh"
 
@@ -31,17 +37,29 @@ constexpr int kK1Warps = 8;                        // consumer warps
 constexpr int kK1Threads = (kK1Warps + 1) * 32;    // + one producer warp
 constexpr int kSlots = 4;                          // ring of shared-memory slots
 constexpr uint32_t kPieceBytes = 16384;            // bytes per slot
+constexpr int kVecPerLane = (int)(kPieceBytes / 16) / (kK1Warps * 32);  // 16-byte vectors per lane per piece
+constexpr int kDrawPerLane = 1;                    // queued groups drawn per lane per round
+constexpr int kDraw = 32 * kDrawPerLane;           // groups drawn per round
+constexpr int kQueue = kDrawPerLane == 1 ? 64 : 96;  // per-warp ring of candidate groups awaiting their draw
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Largest Gumbel value the uniform mapping can produce, -log(-log(1 - 2^-24)) = 16.6355...,
 // rounded up; plus a margin for the candidate test.
 constexpr float kGumbelMax = 16.64f;
 constexpr float kCandidateSlack = 1e-3f;
+// Smallest Gumbel value, -log(-log(2^-24)) = -2.81153..., by magnitude, rounded up.
+constexpr float kGumbelLow = 2.8117f;
 // Exponents (log2 units) below this give 2^d = 0 in fp32 with flush-to-zero.
 constexpr float kMinExponent = -256.f;
+// bf16 pairs: -inf, and -2^64 (the floor applied to logits before the exponent, so that a
+// -inf logit gives e = 0 and e * d = 0 instead of 0 * -inf).
+constexpr uint32_t kBf16NegInf2 = 0xFF80FF80u;
+constexpr uint32_t kBf16NegFloor2 = 0xDF80DF80u;
+
+static_assert(kVecPerLane * kK1Warps * 32 * 16 == (int)kPieceBytes, "a piece splits evenly over the lanes");
 
 struct RowState {  // online softmax state of a set of entries, z measured in log2 units
-    float m;       // max raw logit (-inf = empty)
+    float m;       // reference: the largest raw logit seen by the warp (-inf = empty)
     float c;       // entries equal to m
     float r;       // sum of 2^d over the other entries, d = (x - m) * log2e / T
     float t;       // sum of 2^d * d
@@ -59,10 +77,10 @@ struct K1Shared {
     unsigned best_key;  // CTA-wide best score so far, order-preserving integer encoding
     int bad;
     int timeout;
-    // per-warp candidate groups awaiting their Gumbel draw: first entry index and the 4
-    // logits (as raw words), so a queued group outlives the ring slot it came from
-    int q_e0[kK1Warps][96];
-    uint32_t q_x[kK1Warps][96][kQW];
+    // per-warp ring of candidate groups: first entry index and the 4 logits (raw words), so
+    // a queued group outlives the ring slot it came from
+    int q_e0[kK1Warps][kQueue];
+    uint32_t q_x[kK1Warps][kQueue][kQW];
 };
 
 DG_DEVINL float ex2(float x) {
@@ -76,6 +94,70 @@ DG_DEVINL float max_nan(float a, float b) {
     float y;
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
     return y;
+}
+
+// Lane-wise max of two bf16 pairs, NaN-propagating.
+DG_DEVINL uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Either half of bf16 pair a >= (==) the same half of b.
+DG_DEVINL bool bge2_any(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("{\n\t.reg .pred p, q;\n\tsetp.ge.bf16x2 p|q, %1, %2;\n\tor.pred p, p, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(a), "r"(b));
+    return r != 0;
+}
+DG_DEVINL bool beq2_any(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("{\n\t.reg .pred p, q;\n\tsetp.eq.bf16x2 p|q, %1, %2;\n\tor.pred p, p, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(a), "r"(b));
+    return r != 0;
+}
+
+DG_DEVINL float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+DG_DEVINL float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// The largest bf16 value <= t, in both halves of a pair (a conservative candidate threshold).
+DG_DEVINL uint32_t bf16_floor2(float t) {
+    const uint32_t b = __float_as_uint(t);
+    uint32_t h = b >> 16;                                      // truncation: toward zero
+    if ((b & 0xffffu) != 0u && (b & 0x80000000u) != 0u && t == t) h += 1u;  // negative: one step down
+    if (t != t) h = 0xFF80u;
+    return h | (h << 16);
+}
+
+// Packed fp32 pairs (sm_100 f32x2 arithmetic, round to nearest like the scalar forms).
+DG_DEVINL uint64_t f2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+DG_DEVINL float f2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+DG_DEVINL float f2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+DG_DEVINL uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+DG_DEVINL uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+DG_DEVINL uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+DG_DEVINL uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
 }
 
 // Float <-> unsigned keys with the same order (for atomicMax on scores).
@@ -142,52 +224,83 @@ DG_DEVINL void warp_best(float& best, int& bidx) {
     }
 }
 
+// Index into a warp's candidate ring, for arguments below 2 * kQueue.
+DG_DEVINL int queue_slot(int i) { return (kQueue & (kQueue - 1)) == 0 ? (i & (kQueue - 1)) : (i >= kQueue ? i - kQueue : i); }
+static_assert(kDraw - 1 + 32 <= kQueue, "a round's worth of groups plus one vector's fit the ring");
+
 template <int DT>
-struct Vec;  // 16 bytes of logits as floats
-
-template <>
-struct Vec<0> {  // bf16: 8 entries
-    static constexpr int N = 8;
-    DG_DEVINL static void load(const unsigned char* p, float (&x)[8]) {
-        const uint4 q = *reinterpret_cast<const uint4*>(p);
-        x[0] = __uint_as_float(q.x << 16);
-        x[1] = __uint_as_float(q.x & 0xffff0000u);
-        x[2] = __uint_as_float(q.y << 16);
-        x[3] = __uint_as_float(q.y & 0xffff0000u);
-        x[4] = __uint_as_float(q.z << 16);
-        x[5] = __uint_as_float(q.z & 0xffff0000u);
-        x[6] = __uint_as_float(q.w << 16);
-        x[7] = __uint_as_float(q.w & 0xffff0000u);
-    }
+struct Vec {  // 16 bytes of logits: 8 bf16 or 4 fp32 entries
+    static constexpr int N = DT == 0 ? 8 : 4;
 };
 
-template <>
-struct Vec<1> {  // fp32: 4 entries
-    static constexpr int N = 4;
-    DG_DEVINL static void load(const unsigned char* p, float (&x)[4]) {
-        const float4 q = *reinterpret_cast<const float4*>(p);
-        x[0] = q.x;
-        x[1] = q.y;
-        x[2] = q.z;
-        x[3] = q.w;
-    }
-};
-
-// Gumbel draw for one group of 4 consecutive entries (one Philox block) [e0, e0 + 4) with
-// logits x.  Keeps (best, bidx) as the largest score y + g, y = x / T, ties to the lower
-// index.  `bound` is a score some entry of the row is known to reach; entries that cannot
-// reach it are not drawn.
-DG_DEVINL void eval_group(const float (&x)[4], int e0, int64_t V, float invT, uint32_t pos, uint32_t step,
-                          uint32_t c3, uint32_t k0, uint32_t k1, float bound, float& best, int& bidx) {
-    const dg::u4 w = dg::philox10((uint32_t)e0 >> 2, pos, step, c3, k0, k1);
+// The 16-byte vector j of a slot as raw words, entries past the row's end (or vectors past
+// the piece's end) set to -inf.  FULL: the piece is whole, no checks.
+template <int DT, bool FULL>
+DG_DEVINL uint4 load_raw(const unsigned char* slot, int j, int nvec, int n_el) {
+    constexpr int VN = Vec<DT>::N;
+    constexpr uint32_t kNegInf = DT == 0 ? kBf16NegInf2 : 0xFF800000u;
+    if (FULL) return *reinterpret_cast<const uint4*>(slot + (size_t)j * 16);
+    uint4 w = make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
+    if (j < nvec) {
+        w = *reinterpret_cast<const uint4*>(slot + (size_t)j * 16);
+        const int valid = n_el - j * VN;
+        if (valid < VN) {  // the row's ragged end
+            uint32_t a[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < VN; ++i) {
+                if (i < valid) continue;
+                if (DT == 0)
+                    a[i >> 1] = (i & 1) ? ((a[i >> 1] & 0x0000ffffu) | 0xFF800000u) : ((a[i >> 1] & 0xffff0000u) | 0xFF80u);
+                else
+                    a[i] = 0xFF800000u;
+            }
+            w = make_uint4(a[0], a[1], a[2], a[3]);
+        }
+    }
+    return w;
+}
+
+template <int DT>
+DG_DEVINL void unpack(const uint4& w, float (&x)[Vec<DT>::N]) {
+    if constexpr (DT == 0) {
+        x[0] = bf_lo(w.x); x[1] = bf_hi(w.x); x[2] = bf_lo(w.y); x[3] = bf_hi(w.y);
+        x[4] = bf_lo(w.z); x[5] = bf_hi(w.z); x[6] = bf_lo(w.w); x[7] = bf_hi(w.w);
+    } else {
+        x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+        x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+    }
+}
+
+template <int DT>
+DG_DEVINL void words_group(const uint32_t* w, float (&x)[4]) {
+    if (DT == 0) {
+        x[0] = bf_lo(w[0]); x[1] = bf_hi(w[0]); x[2] = bf_lo(w[1]); x[3] = bf_hi(w[1]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = __uint_as_float(w[i]);
+    }
+}
+
+// Gumbel draw for one group of 4 consecutive entries (one Philox block, words w) [e0, e0 + 4)
+// with logits x.  Keeps (best, bidx) as the largest score y + g, y = x / T, ties to the
+// lower index.  Entries that cannot reach max(bound, best) are not drawn: g > D needs
+// u > exp(-e^-D) >= 1 - e^-D, tested (with a factor 2 of slack) first for the whole group
+// against its largest uniform and largest logit, then per entry.
+DG_DEVINL void eval_words(const float (&x)[4], int e0, const dg::u4& w, int64_t V, float invT, float bound,
+                          float& best, int& bidx) {
+    {
+        const float b = fmaxf(bound, best);
+        const float ymax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])) * invT;
+        const float umax = dg::uniform_from_word(max(max(w.x, w.y), max(w.z, w.w)));
+        if (!(umax > 1.f - 2.f * ex2((ymax - b) * kLog2e))) return;
+    }
+#pragma unroll 1
+    for (int i = 0; i < 4; ++i) {  // rare (a few groups per row): kept rolled, small code
         if (e0 + i >= V) continue;
-        const float y = x[i] * invT;
+        const float y = (i == 0 ? x[0] : i == 1 ? x[1] : i == 2 ? x[2] : x[3]) * invT;
         const float b = fmaxf(bound, best);
         if (!(y >= b - kGumbelMax - kCandidateSlack)) continue;
         const float u = dg::uniform_from_word(word_of(w, i));
-        // g > D = b - y needs u > exp(-e^-D) >= 1 - e^-D; keep a factor 2 of slack
         const float eb = 2.f * ex2(-(b - y) * kLog2e);
         if (!(u > 1.f - eb)) continue;
         const float score = y + (-logf(-logf(u)));
@@ -198,35 +311,34 @@ DG_DEVINL void eval_group(const float (&x)[4], int e0, int64_t V, float invT, ui
     }
 }
 
-// Raw words <-> 4 logits of a group (bf16 pairs or fp32).
-template <int DT, int N>
-DG_DEVINL void group_words(const float (&x)[N], int g, uint32_t (&w)[4]) {
-    if (DT == 0) {
-        w[0] = (__float_as_uint(x[4 * g]) >> 16) | (__float_as_uint(x[4 * g + 1]) & 0xffff0000u);
-        w[1] = (__float_as_uint(x[4 * g + 2]) >> 16) | (__float_as_uint(x[4 * g + 3]) & 0xffff0000u);
-        w[2] = 0u;
-        w[3] = 0u;
-    } else {
+// Queued groups of one warp: kDraw at a time, kDrawPerLane per lane (independent Philox
+// chains), or the fewer left at the end of the row.  All 32 lanes call it (warp-uniform n).
+template <int DT, int QW>
+DG_DEVINL void draw_queued(const int* q_e0, const uint32_t (*q_x)[QW], int qh, int n, int lane, int64_t V,
+                           float invT, const dg::PhiloxPre& pre, float bound, float& best, int& bidx) {
+    float xs[kDrawPerLane][4];
+    int es[kDrawPerLane];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) w[i] = __float_as_uint(x[4 * g + i]);
+    for (int r = 0; r < kDrawPerLane; ++r) {
+        const int at = queue_slot(qh + 32 * r + lane);
+        words_group<DT>(q_x[at], xs[r]);
+        es[r] = q_e0[at];
     }
-}
-
-template <int DT>
-DG_DEVINL void words_group(const uint32_t* w, float (&x)[4]) {
-    if (DT == 0) {
-        x[0] = __uint_as_float(w[0] << 16);
-        x[1] = __uint_as_float(w[0] & 0xffff0000u);
-        x[2] = __uint_as_float(w[1] << 16);
-        x[3] = __uint_as_float(w[1] & 0xffff0000u);
-    } else {
+    __syncwarp();  // read before later groups reuse these entries
+    dg::u4 w[kDrawPerLane];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) x[i] = __uint_as_float(w[i]);
-    }
+    for (int r = 0; r < kDrawPerLane; ++r) w[r] = dg::philox10_c0((uint32_t)es[r] >> 2, pre);
+#pragma unroll
+    for (int r = 0; r < kDrawPerLane; ++r)
+        if (32 * r + lane < n) eval_words(xs[r], es[r], w[r], V, invT, bound, best, bidx);
 }
 
 // ------------------------------------------------------------------------------------
 // K1: per-position statistics and Gumbel-max sample.  grid (L, n), one CTA per position.
+// Each consumer warp takes kVecPerLane 16-byte vectors per lane of every piece, in two
+// passes over shared memory: (1) vector maxima, candidate groups into the warp's queue;
+// (2) the exponential sums against the warp's running max, which only grows between
+// pieces (a warp-uniform branch), so lanes do not diverge on new maxima.
 // ------------------------------------------------------------------------------------
 template <int DT>
 __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
@@ -302,19 +414,18 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
         // ---------------- consumers
         RowState st{-INFINITY, 0.f, 0.f, 0.f, 0x7fffffff};
         bool bad = false;
-        float best = -INFINITY;    // this warp's best score and its entry
+        float best = -INFINITY;    // this lane's best score and its entry
         int bidx = 0x7fffffff;
         float bound = -INFINITY;   // best score known anywhere in the CTA
-        const uint32_t k0 = (uint32_t)seed, k1 = p.request_id;
-        const uint32_t c3 = dg::ctr_word3(seed, dg::kStreamGumbel);
-        const uint32_t step = (uint32_t)p.step;
+        const dg::PhiloxPre pre = dg::philox_pre((uint32_t)pos, (uint32_t)p.step,
+                                                 dg::ctr_word3(seed, dg::kStreamGumbel), (uint32_t)seed, p.request_id);
         int* q_e0 = sh.q_e0[warp];
         uint32_t(*q_x)[QW] = sh.q_x[warp];
-        int qn = 0;  // warp-uniform queue length, kept across pieces
+        int qh = 0, qn = 0;  // warp-uniform queue head and length, kept across pieces
         const unsigned lt = (1u << lane) - 1u;
         for (int q = 0; q < npieces; ++q) {
             const int sl = q % kSlots;
-            if (!dg::mbar_wait(&sh.full[sl], (uint32_t)(q / kSlots) & 1u)) {
+            if (!__all_sync(0xffffffffu, dg::mbar_wait(&sh.full[sl], (uint32_t)(q / kSlots) & 1u))) {
                 sh.timeout = 1;
                 break;
             }
@@ -322,184 +433,179 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
             const int e_lo = q * kPieceElems;
             const int n_el = (int)min((int64_t)kPieceElems, V - e_lo);
             const int nvec = (n_el + VN - 1) / VN;
-            // candidate threshold on the raw logit: x / T + G_max >= best - slack
-            float x_thr = (fmaxf(bound, best) - kGumbelMax - kCandidateSlack) * p.temperature;
-            for (int j0 = warp * 32; j0 < nvec; j0 += kK1Warps * 32) {
-                const int j = j0 + lane;
-                bool cand[GPV];
+
+            // One piece in two passes; FULL: every vector of the piece is whole (all but the
+            // row's last piece), so the bounds checks drop out; SAMPLE: the Gumbel-max search
+            // runs (not for read-only canvases).
+            auto piece = [&](auto full_tag, auto sample_tag) {
+                constexpr bool FULL = decltype(full_tag)::value;
+                constexpr bool SAMPLE = decltype(sample_tag)::value;
+                // ---- pass 1: vector maxima, then the warp's max; a larger one rescales every
+                // lane's state (warp-uniform, so lanes never diverge on a new maximum)
+                uint32_t lm2 = kBf16NegInf2;  // lane max as a bf16 pair (max of even, odd entries)
+                float lane_max = -INFINITY;
 #pragma unroll
-                for (int g = 0; g < GPV; ++g) cand[g] = false;
-                float x[VN], e[VN];  // logits and e = exp((x - m) / T) against the lane's running max m
-                if (j < nvec) {
-                    Vec<DT>::load(slot + (size_t)j * 16, x);
-                    const int base = j * VN;
-                    if (base + VN > n_el) {
-#pragma unroll
-                        for (int i = 0; i < VN; ++i)
-                            if (base + i >= n_el) x[i] = -INFINITY;
+                for (int v = 0; v < kVecPerLane; ++v) {
+                    const int j = (v * kK1Warps + warp) * 32 + lane;
+                    const uint4 w = load_raw<DT, FULL>(slot, j, nvec, n_el);
+                    if constexpr (DT == 0) {
+                        lm2 = bmax2(lm2, bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w)));
+                    } else {
+                        const float vmax = max_nan(max_nan(__uint_as_float(w.x), __uint_as_float(w.y)),
+                                                   max_nan(__uint_as_float(w.z), __uint_as_float(w.w)));
+                        lane_max = max_nan(lane_max, vmax);
                     }
-                    float gmax[GPV];
+                }
+                if (DT == 0) lane_max = max_nan(bf_lo(lm2), bf_hi(lm2));
+                float wmax = lane_max;
 #pragma unroll
-                    for (int g = 0; g < GPV; ++g)
-                        gmax[g] = fmaxf(fmaxf(x[4 * g], x[4 * g + 1]), fmaxf(x[4 * g + 2], x[4 * g + 3]));
-                    float vmax = gmax[0];
-#pragma unroll
-                    for (int g = 1; g < GPV; ++g) vmax = fmaxf(vmax, gmax[g]);
-                    // online softmax state
-                    if (vmax > st.m) {
-                        int i0 = VN - 1;
-#pragma unroll
-                        for (int i = VN - 1; i >= 0; --i)
-                            if (x[i] == vmax) i0 = i;
-                        if (st.m == -INFINITY) {
-                            st.c = 0.f;
-                            st.r = 0.f;
-                            st.t = 0.f;
-                        } else {
-                            const float d = (st.m - vmax) * k2, al = ex2(d), s = st.c + st.r;
-                            st.t = al * (st.t + d * s);
-                            st.r = al * s;
-                            st.c = 0.f;
-                        }
-                        st.m = vmax;
-                        st.idx = e_lo + base + i0;
+                for (int o = 16; o >= 1; o >>= 1) wmax = max_nan(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+                if (wmax != wmax) {
+                    bad = true;
+                } else if (wmax > st.m) {
+                    if (st.m > -INFINITY) {
+                        const float d = (st.m - wmax) * k2, al = ex2(d), s = st.c + st.r;
+                        st.t = al * (st.t + d * s);
+                        st.r = al * s;
                     }
-                    if (vmax == st.m) {
-                        if (vmax == -INFINITY) {
-#pragma unroll
-                            for (int i = 0; i < VN; ++i) {
-                                bad |= (x[i] != x[i]);
-                                e[i] = 0.f;
-                            }
-                        } else {
-#pragma unroll
+                    st.c = 0.f;
+                    st.m = wmax;
+                    st.idx = 0x7fffffff;
+                }
+                if (!(st.m > -INFINITY && st.m < INFINITY)) return;  // nothing to add while m = -inf
+
+                // ---- pass 2: candidate groups and exponential sums.  Every score is at least
+                // its y plus the smallest Gumbel value, so m / T - kGumbelLow bounds the winner's
+                // score from below before any noise is drawn.  x - m is exact for bf16 entries,
+                // so d carries one rounding whatever the size of m / T.
+                const float ym = st.m * invT;
+                bound = fmaxf(bound, ym - kGumbelLow - fabsf(ym) * 2.4e-7f);
+                const float x_thr = (fmaxf(bound, best) - kGumbelMax - kCandidateSlack) * p.temperature;
+                const uint32_t thr2 = DT == 0 ? bf16_floor2(x_thr) : 0u;
+                const uint32_t m2 = DT == 0 ? (__float_as_uint(st.m) >> 16) * 0x10001u : 0u;
+                (void)thr2;
+                (void)m2;
+                const uint64_t mm = f2(st.m, st.m), kk = f2(k2, k2);
+                uint64_t racc[2] = {0ull, 0ull}, tacc[2] = {0ull, 0ull};  // pairs of partial sums
+                auto vec2 = [&](int v) {
+                    const int j = (v * kK1Warps + warp) * 32 + lane;
+                    const bool in = FULL || j < nvec;
+                    const uint4 w = load_raw<DT, FULL>(slot, j, nvec, n_el);
+                    bool cand[GPV], tie;
+                    if constexpr (DT == 0) {
+                        const uint32_t g0 = bmax2(w.x, w.y), g1 = bmax2(w.z, w.w);
+                        cand[0] = SAMPLE && in && bge2_any(g0, thr2);
+                        cand[GPV - 1] = SAMPLE && in && bge2_any(g1, thr2);
+                        tie = beq2_any(bmax2(g0, g1), m2);
+                    } else {
+                        const float vmax = max_nan(max_nan(__uint_as_float(w.x), __uint_as_float(w.y)),
+                                                   max_nan(__uint_as_float(w.z), __uint_as_float(w.w)));
+                        cand[0] = SAMPLE && in && vmax >= x_thr;
+                        tie = vmax == st.m;
+                    }
+                    if (in) {
+                        float x[VN];
+                        if (tie) {
+                            // the vector holds the max: count its copies, the rest as usual
+                            unpack<DT>(w, x);
+        #pragma unroll
                             for (int i = 0; i < VN; ++i) {
                                 if (x[i] == st.m) {
                                     st.c += 1.f;
-                                    e[i] = 1.f;
+                                    st.idx = min(st.idx, e_lo + j * VN + i);
                                 } else {
-                                    // -inf entries (masked tail, or -inf logits) contribute e = 0;
-                                    // the clamp keeps e * d at 0 instead of 0 * -inf
                                     const float d = max_nan((x[i] - st.m) * k2, kMinExponent);
-                                    e[i] = ex2(d);
-                                    st.r += e[i];
-                                    st.t = fmaf(e[i], d, st.t);
+                                    const float e = ex2(d);
+                                    st.r += e;
+                                    st.t = fmaf(e, d, st.t);
+                                }
+                            }
+                        } else if constexpr (DT == 0) {
+                            // entries floored at -2^64 (a -inf logit gives e = 0, e * d = 0), two per op
+                            const uint32_t fw[4] = {bmax2(w.x, kBf16NegFloor2), bmax2(w.y, kBf16NegFloor2),
+                                                    bmax2(w.z, kBf16NegFloor2), bmax2(w.w, kBf16NegFloor2)};
+        #pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const uint64_t d2 = f2_mul(f2_sub(f2(bf_lo(fw[k]), bf_hi(fw[k])), mm), kk);
+                                const uint64_t e2 = f2(ex2(f2_lo(d2)), ex2(f2_hi(d2)));
+                                racc[k & 1] = f2_add(racc[k & 1], e2);
+                                tacc[k & 1] = f2_fma(e2, d2, tacc[k & 1]);
+                            }
+                        } else {
+                            unpack<DT>(w, x);
+        #pragma unroll
+                            for (int i = 0; i < VN; ++i) {
+                                const float d = max_nan((x[i] - st.m) * k2, kMinExponent);
+                                const float e = ex2(d);
+                                st.r += e;
+                                st.t = fmaf(e, d, st.t);
+                            }
+                        }
+                    }
+                    if (!SAMPLE) return;
+                    bool any = false;
+        #pragma unroll
+                    for (int g = 0; g < GPV; ++g) any |= cand[g];
+                    if (__ballot_sync(0xffffffffu, any) == 0u) return;
+        #pragma unroll
+                    for (int g = 0; g < GPV; ++g) {
+                        const unsigned mk = __ballot_sync(0xffffffffu, cand[g]);
+                        if (cand[g]) {
+                            const int at = queue_slot(qh + qn + __popc(mk & lt));
+                            q_e0[at] = e_lo + (j * GPV + g) * 4;
+                            if (DT == 0) {
+                                q_x[at][0] = g == 0 ? w.x : w.z;
+                                q_x[at][1] = g == 0 ? w.y : w.w;
+                            } else {
+                                q_x[at][0] = w.x;
+                                q_x[at][1] = w.y;
+                                if (QW == 4) {
+                                    q_x[at][QW - 2] = w.z;
+                                    q_x[at][QW - 1] = w.w;
                                 }
                             }
                         }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < VN; ++i) {
-                            const float d = max_nan((x[i] - st.m) * k2, kMinExponent);
-                            e[i] = ex2(d);
-                            st.r += e[i];
-                            st.t = fmaf(e[i], d, st.t);
+                        qn += __popc(mk);
+                        __syncwarp();
+                        if (qn >= kDraw) {  // at most kDraw - 1 + 32 <= kQueue groups are queued
+                            draw_queued<DT, QW>(q_e0, q_x, qh, kDraw, lane, V, invT, pre, bound, best, bidx);
+                            qh = queue_slot(qh + kDraw);
+                            qn -= kDraw;
                         }
                     }
-                    if (do_sample) {
-#pragma unroll
-                        for (int g = 0; g < GPV; ++g) cand[g] = gmax[g] >= x_thr;
-                    }
+                };
+                if constexpr (SAMPLE) {
+#pragma unroll 1
+                    for (int v = 0; v < kVecPerLane; ++v) vec2(v);  // rolled: one copy of the draw code
                 } else {
 #pragma unroll
-                    for (int i = 0; i < VN; ++i) {
-                        x[i] = -INFINITY;
-                        e[i] = 0.f;
-                    }
+                    for (int v = 0; v < kVecPerLane; ++v) vec2(v);
                 }
-                if (!do_sample) continue;
-                const float bnd = fmaxf(bound, best);
-                bool any = false;
-#pragma unroll
-                for (int g = 0; g < GPV; ++g) any |= cand[g];
-                const unsigned dense_mk = __ballot_sync(0xffffffffu, any);
-                if (bnd > -INFINITY && __popc(dense_mk) >= 16) {
-                    // Dense: most lanes hold candidates, so every lane draws its own groups' noise.
-                    // exp(y - bnd) = e * exp(m / T - bnd) reuses the softmax term; entries with
-                    // u <= 1 - 2 exp(y - bnd) cannot beat the bound (see eval_group).
-                    const float cb = ex2((st.m * invT - bnd) * kLog2e);
-                    const float nscale = -2.f * cb;
-#pragma unroll
-                    for (int g = 0; g < GPV; ++g) {
-                        if (!cand[g]) continue;
-                        const int e0 = e_lo + (j * GPV + g) * 4;
-                        const dg::u4 w = dg::philox10((uint32_t)e0 >> 2, (uint32_t)pos, step, c3, k0, k1);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float u = dg::uniform_from_word(word_of(w, i));
-                            if (!(u > fmaf(nscale, e[4 * g + i], 1.f))) continue;
-                            if (e0 + i >= V) continue;
-                            const float score = x[4 * g + i] * invT + (-logf(-logf(u)));
-                            if (better(score, e0 + i, best, bidx)) {
-                                best = score;
-                                bidx = e0 + i;
-                            }
-                        }
-                    }
-                    warp_best(best, bidx);
-                    x_thr = (fmaxf(bound, best) - kGumbelMax - kCandidateSlack) * p.temperature;
-                    continue;
+                if (DT == 0) {
+                    st.r += (f2_lo(racc[0]) + f2_hi(racc[0])) + (f2_lo(racc[1]) + f2_hi(racc[1]));
+                    st.t += (f2_lo(tacc[0]) + f2_hi(tacc[0])) + (f2_lo(tacc[1]) + f2_hi(tacc[1]));
                 }
-                if (!do_sample) continue;
-                // queue the candidate groups (ballot-compacted) and draw 32 at a time
-#pragma unroll
-                for (int g = 0; g < GPV; ++g) {
-                    const unsigned mk = __ballot_sync(0xffffffffu, cand[g]);
-                    if (cand[g]) {
-                        const int at = qn + __popc(mk & lt);
-                        uint32_t wv[4];
-                        group_words<DT>(x, g, wv);
-                        q_e0[at] = e_lo + (j * GPV + g) * 4;
-#pragma unroll
-                        for (int i = 0; i < QW; ++i) q_x[at][i] = wv[i];
-                    }
-                    qn += __popc(mk);
-                }
-                __syncwarp();
-                while (qn >= 32) {  // at most 31 + 32 * GPV < 96 entries are queued
-                    {
-                        float xg[4];
-                        words_group<DT>(q_x[lane], xg);
-                        eval_group(xg, q_e0[lane], V, invT, (uint32_t)pos, step, c3, k0, k1, bound, best, bidx);
-                    }
-                    __syncwarp();
-                    const int rest = qn - 32;  // move the unprocessed tail to the front
-                    for (int r0 = 0; r0 < rest; r0 += 32) {
-                        const int r = r0 + lane;
-                        int e0v = 0;
-                        uint32_t wv[4] = {0u, 0u, 0u, 0u};
-                        if (r < rest) {
-                            e0v = q_e0[32 + r];
-#pragma unroll
-                            for (int i = 0; i < QW; ++i) wv[i] = q_x[32 + r][i];
-                        }
-                        __syncwarp();
-                        if (r < rest) {
-                            q_e0[r] = e0v;
-#pragma unroll
-                            for (int i = 0; i < QW; ++i) q_x[r][i] = wv[i];
-                        }
-                        __syncwarp();
-                    }
-                    qn = rest;
-                    warp_best(best, bidx);
-                    x_thr = (fmaxf(bound, best) - kGumbelMax - kCandidateSlack) * p.temperature;
-                }
+            };
+            if (do_sample) {
+                if (n_el == kPieceElems) piece(std::true_type{}, std::true_type{});
+                else piece(std::false_type{}, std::true_type{});
+            } else {
+                if (n_el == kPieceElems) piece(std::true_type{}, std::false_type{});
+                else piece(std::false_type{}, std::false_type{});
             }
+
             if (do_sample) {
                 // share the best score with the other warps, take theirs
-                if (lane == 0 && best > -INFINITY) atomicMax(&sh.best_key, float_key(best));
+                warp_best(best, bidx);
+                const float mine = fmaxf(best, bound);
+                if (lane == 0 && mine > -INFINITY) atomicMax(&sh.best_key, float_key(mine));
                 __syncwarp();
                 bound = fmaxf(bound, key_float(*(volatile unsigned*)&sh.best_key));
             }
             __syncwarp();
             if (lane == 0) dg::mbar_arrive(&sh.empty[sl]);
         }
-        if (do_sample && lane < qn) {  // the last (fewer than 32) queued groups
-            float xg[4];
-            words_group<DT>(q_x[lane], xg);
-            eval_group(xg, q_e0[lane], V, invT, (uint32_t)pos, step, c3, k0, k1, bound, best, bidx);
-        }
+        if (do_sample && qn > 0) draw_queued<DT, QW>(q_e0, q_x, qh, qn, lane, V, invT, pre, bound, best, bidx);
         __syncwarp();
         if (bad) sh.bad = 1;
 #pragma unroll

@@ -63,8 +63,11 @@ struct GemmArgs {
     unsigned* status;
 };
 
-template <int AM, int BMD, int BN_, int BK_, int STAGES_>
+// PAIR_: the CTA pair of a 2-CTA cluster computes one 256-row tile with cta_group::2 MMAs
+// (N-major B with the softmax transform only); each CTA then holds half of every B slab.
+template <int AM, int BMD, int BN_, int BK_, int STAGES_, bool PAIR_ = false>
 struct Cfg {
+    static constexpr bool kPair = PAIR_;
     static constexpr int kAMode = AM;
     static constexpr int kBMode = BMD;
     static constexpr int BN = BN_;
@@ -75,14 +78,16 @@ struct Cfg {
     static constexpr int kNAcc = (BN <= 256) ? 2 : 1;        // double-buffered when it fits
     static constexpr int kTmemCols = kAccCols * kNAcc;       // 256 or 512
     static constexpr int kXformThreads = 256;                // two warpgroups, half a tile row each
+    static constexpr int kXformWarps = kXformThreads / 32;
     static constexpr int kThreads = kXform ? 192 + kXformThreads : 192;
     static constexpr int kATileBytes = BM * BK * 2;
     static constexpr int kStageBytesFp32 = (AM == A_SOFTMAX_FP32) ? BM * BK * 4 : 0;
-    static constexpr int kBTileBytes = BK * BN * 2;
+    static constexpr int kBTileBytes = BK * BN * 2 / (PAIR_ ? 2 : 1);  // this CTA's part of the B tile
     static constexpr int kStageBytes = kATileBytes + kBTileBytes + kStageBytesFp32;
     static constexpr int kASwizzle = BK * 2;                 // 64 or 128 bytes: one swizzle row per tile row
     static constexpr uint32_t kTxBytes = (uint32_t)(kBTileBytes + (AM == A_SOFTMAX_FP32 ? kStageBytesFp32 : kATileBytes));
     static constexpr size_t kSmem = 1024 + (size_t)STAGES * kStageBytes + 1024;
+    static_assert(!PAIR_ || (BMD == B_MNMAJOR && AM != A_TMA && BN_ == 512), "pair mode: softmax A, N-major B, BN 512");
 };
 
 // ------------------------------------------------------------------ descriptors
@@ -250,6 +255,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const int rank = (int)cluster.block_rank();
     const int64_t cid = blockIdx.x / cm, ncl = gridDim.x / cm;
     const uint16_t mask = (uint16_t)((1u << cm) - 1u);
+    constexpr bool PAIR = C::kPair;
+    const bool leader = !PAIR || rank == 0;  // the pair's MMAs are issued by its first CTA
 
     const int mt = active_m_tiles(a);
     const int64_t n_groups = mt > 0 ? group_count(a, mt, cm) : 0;
@@ -257,19 +264,25 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             dg::mbar_init(&sh.full[s], 1);
-            dg::mbar_init(&sh.xform[s], C::kXform ? C::kXformThreads : 1);
-            dg::mbar_init(&sh.empty[s], (uint32_t)cm);  // one release per CTA of the cluster
+            // pair: one arrival per transform warp of both CTAs, in the first CTA's barrier
+            dg::mbar_init(&sh.xform[s], PAIR ? 2 * C::kXformWarps : (C::kXform ? C::kXformThreads : 1));
+            dg::mbar_init(&sh.empty[s], PAIR ? 1u : (uint32_t)cm);  // one release per CTA of the cluster
         }
         for (int i = 0; i < C::kNAcc; ++i) {
             dg::mbar_init(&sh.accf[i], 1);
-            dg::mbar_init(&sh.acce[i], 128);
+            dg::mbar_init(&sh.acce[i], PAIR ? 2 * 4 : 128);  // pair: one per epilogue warp of both CTAs
         }
         sh.abort_flag = 0;
         dg::fence_mbar_init();
     }
     if (warp == 1) {
-        dg::tmem_alloc(&sh.tmem_base, C::kTmemCols);
-        dg::tmem_relinquish();
+        if constexpr (PAIR) {
+            dg::tmem_alloc_pair(&sh.tmem_base, C::kTmemCols);
+            dg::tmem_relinquish_pair();
+        } else {
+            dg::tmem_alloc(&sh.tmem_base, C::kTmemCols);
+            dg::tmem_relinquish();
+        }
     }
     dg::tc_fence_before();
     cluster.sync();  // peers' barriers are initialised before any multicast lands
@@ -311,7 +324,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     if (C::kBMode == B_MNMAJOR) {
                         // [K][N] embedding rows: one 64-column (128-byte) atom column per load; with
                         // a cluster each CTA fetches every cm-th atom for all of its peers
-                        if (cm == 1) {
+                        if (PAIR) {
+                            // this CTA's half of each 256-column slab h: atoms 2h, 2h + 1
+#pragma unroll
+                            for (int h = 0; h < C::BN / 256; ++h)
+#pragma unroll
+                                for (int at = 0; at < 2; ++at)
+                                    dg::tma_load_2d(sB + (2 * h + at) * (C::BK * 128), &tmB0,
+                                                    im.n * C::BN + h * 256 + rank * 128 + at * 64, k0, &sh.full[s]);
+                        } else if (cm == 1) {
 #pragma unroll
                             for (int j = 0; j < C::BN / 64; ++j)
                                 dg::tma_load_2d(sB + j * (C::BK * 128), &tmB0, im.n * C::BN + j * 64, k0, &sh.full[s]);
@@ -336,7 +357,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc_pair = instr_desc(2 * BM, 256, true);
             constexpr uint32_t idesc_mn = instr_desc(BM, C::BN > 256 ? 256 : C::BN, true);
             constexpr uint32_t idesc_k = instr_desc(BM, C::BN > 256 ? 256 : C::BN, false);
             constexpr uint32_t idesc = (C::kBMode == B_MNMAJOR) ? idesc_mn : idesc_k;
@@ -345,15 +367,20 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 const Item im = decode(a, mt, cm, rank, G);
                 const int ab = (int)(acc_it % C::kNAcc);
                 const uint32_t aph = (acc_it / C::kNAcc) & 1u;
-                if (!dg::mbar_wait(&sh.acce[ab], aph ^ 1u)) { do_abort(sh, a.status); break; }
+                if (!dg::mbar_wait(&sh.acce[ab], aph ^ 1u)) {
+                    do_abort(sh, a.status);
+                    break;
+                }
                 dg::tc_fence_after();
                 const uint32_t dacc = tmem + (uint32_t)(ab * C::kAccCols);
                 bool ok = true;
                 for (int kb = im.kb_lo; kb < im.kb_hi; ++kb, ++it) {
                     const int s = (int)(it % C::STAGES);
                     const uint32_t ph = (it / C::STAGES) & 1u;
-                    if (!dg::mbar_wait(&sh.full[s], ph)) { ok = false; break; }
-                    if (C::kXform && !dg::mbar_wait(&sh.xform[s], ph)) { ok = false; break; }
+                    // pair: the transform warps of both CTAs report (after their own full waits)
+                    if (!PAIR && !dg::mbar_wait(&sh.full[s], ph)) { ok = false; break; }
+                    if (PAIR && !dg::mbar_wait(&sh.xform[s], ph)) { ok = false; break; }
+                    if (!PAIR && C::kXform && !dg::mbar_wait(&sh.xform[s], ph)) { ok = false; break; }
                     dg::tc_fence_after();
                     const uint32_t sA = dg::smem_u32(smem + (size_t)s * C::kStageBytes);
                     const uint32_t sB = sA + C::kATileBytes;
@@ -361,7 +388,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     for (int kk = 0; kk < C::BK / 16; ++kk) {
                         const uint64_t ad = smem_desc(sA + kk * 32, 16, 8 * C::BK * 2, C::kASwizzle);
                         const uint32_t accum = (kb > im.kb_lo || kk > 0) ? 1u : 0u;
-                        if (C::kBMode == B_MNMAJOR) {
+                        if constexpr (PAIR) {
+                            // two N = 256 slabs; this CTA's B holds 2 atom columns of each
+#pragma unroll
+                            for (int h = 0; h < C::BN / 256; ++h) {
+                                const uint64_t bd = smem_desc(sB + h * 2 * (C::BK * 128) + kk * 16 * 128, C::BK * 128, 1024, 128);
+                                dg::tc_mma_f16_pair(dacc + h * 256, ad, bd, idesc_pair, accum);
+                            }
+                        } else if (C::kBMode == B_MNMAJOR) {
                             // N-major B: LBO = distance between 64-column atom columns, SBO = 8 K rows
 #pragma unroll
                             for (int h = 0; h < C::BN / 256; ++h) {
@@ -374,11 +408,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                         }
                     }
                     // frees the stage (in every CTA of the cluster) once these MMAs have read it
-                    if (cm == 1) dg::tc_commit(&sh.empty[s]);
+                    if constexpr (PAIR) dg::tc_commit_pair_mc(&sh.empty[s], mask);
+                    else if (cm == 1) dg::tc_commit(&sh.empty[s]);
                     else dg::tc_commit_mc(&sh.empty[s], mask);
                 }
                 if (!ok) { do_abort(sh, a.status); break; }
-                dg::tc_commit(&sh.accf[ab]);  // accumulator complete
+                if constexpr (PAIR) dg::tc_commit_pair_mc(&sh.accf[ab], mask);  // both CTAs' accumulators complete
+                else dg::tc_commit(&sh.accf[ab]);                              // accumulator complete
             }
         }
     } else if (warp < 6) {
@@ -419,7 +455,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 }
             }
             dg::tc_fence_before();
-            dg::mbar_arrive(&sh.acce[ab]);
+            if (PAIR) {
+                __syncwarp();
+                if (lane == 0) dg::mbar_arrive_remote(dg::mapa_shared(&sh.acce[ab], 0));
+            } else {
+                dg::mbar_arrive(&sh.acce[ab]);
+            }
         }
     } else {
         // ------------------------------------------------ softmax transform (warps 6..13)
@@ -438,7 +479,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 for (int kb = im.kb_lo; kb < im.kb_hi; ++kb, ++it) {
                     const int s = (int)(it % C::STAGES);
                     const uint32_t ph = (it / C::STAGES) & 1u;
-                    if (!dg::mbar_wait(&sh.full[s], ph)) { ok = false; break; }
+                    // every lane polls; the outcome is made warp-uniform (the warp arrives as one)
+                    if (!__all_sync(0xffffffffu, dg::mbar_wait(&sh.full[s], ph))) { ok = false; break; }
                     unsigned char* st = smem + (size_t)s * C::kStageBytes;
                     unsigned char* rowA = st + t * (C::BK * 2);
                     const int64_t kbase = (int64_t)kb * C::BK;
@@ -480,7 +522,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                                        pack_bf16x2(pz[4], pz[5]), pack_bf16x2(pz[6], pz[7]));
                     }
                     dg::fence_proxy_async_smem();  // make the generic-proxy writes visible to tcgen05
-                    dg::mbar_arrive(&sh.xform[s]);
+                    if (PAIR) {
+                        __syncwarp();
+                        if (lane == 0) dg::mbar_arrive_remote(dg::mapa_shared(&sh.xform[s], 0));
+                    } else {
+                        dg::mbar_arrive(&sh.xform[s]);
+                    }
                 }
                 if (!ok) { do_abort(sh, a.status); break; }
             }
@@ -492,7 +539,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     cluster.sync();
     if (warp == 1) {
         dg::tc_fence_after();
-        dg::tmem_dealloc(tmem, C::kTmemCols);
+        if constexpr (PAIR) dg::tmem_dealloc_pair(tmem, C::kTmemCols);
+        else dg::tmem_dealloc(tmem, C::kTmemCols);
     }
 }
 
@@ -617,8 +665,8 @@ __global__ void k_zero_rows(const dg_canvas_params* __restrict__ params, const u
 }
 
 // ------------------------------------------------------------------ host side
-using PEbf16 = Cfg<A_SOFTMAX_BF16, B_MNMAJOR, 512, 32, 5>;
-using PEfp32 = Cfg<A_SOFTMAX_FP32, B_MNMAJOR, 512, 32, 3>;
+using PEbf16 = Cfg<A_SOFTMAX_BF16, B_MNMAJOR, 512, 32, 8, true>;
+using PEfp32 = Cfg<A_SOFTMAX_FP32, B_MNMAJOR, 512, 32, 5, true>;
 using PEprob = Cfg<A_TMA, B_MNMAJOR, 512, 32, 5>;
 using GateUp = Cfg<A_TMA, B_KMAJOR_GATEUP, 256, 64, 4>;
 using Down = Cfg<A_TMA, B_KMAJOR, 256, 64, 4>;
@@ -673,13 +721,14 @@ bool plan_gemm(const GemmArgs& a, int64_t max_slots, LaunchPlan* pl) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int cm = 1;
-    if (C::kBMode == B_MNMAJOR && a.m_tiles >= 2) cm = 2;
+    if (C::kPair || (C::kBMode == B_MNMAJOR && a.m_tiles >= 2)) cm = 2;
     int clusters = P;
     while (cm > 1) {
         attr[0].val.clusterDim.x = (unsigned)cm;
         cfg.gridDim = dim3((unsigned)((P / cm) * cm), 1, 1);
         int nc = 0;
         if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess) nc = 0;
+        if (C::kPair && nc <= 0) return false;  // a pair kernel runs only as 2-CTA clusters
         if (nc > 0 && (cm < 4 || nc * 4 >= (P * 9) / 10)) {
             clusters = nc;
             break;

@@ -63,8 +63,9 @@ struct GemmArgs {
     unsigned* status;
 };
 
-// PAIR_: the CTA pair of a 2-CTA cluster computes one 256-row tile with cta_group::2 MMAs
-// (N-major B with the softmax transform only); each CTA then holds half of every B slab.
+// PAIR_: the CTA pair of a 2-CTA cluster computes one 256-row tile with cta_group::2 MMAs;
+// each CTA then holds half of every 256-column B slab (for the gate/up tile: the first CTA
+// the gate rows, the second the up rows).
 template <int AM, int BMD, int BN_, int BK_, int STAGES_, bool PAIR_ = false>
 struct Cfg {
     static constexpr bool kPair = PAIR_;
@@ -87,7 +88,7 @@ struct Cfg {
     static constexpr int kASwizzle = BK * 2;                 // 64 or 128 bytes: one swizzle row per tile row
     static constexpr uint32_t kTxBytes = (uint32_t)(kBTileBytes + (AM == A_SOFTMAX_FP32 ? kStageBytesFp32 : kATileBytes));
     static constexpr size_t kSmem = 1024 + (size_t)STAGES * kStageBytes + 1024;
-    static_assert(!PAIR_ || (BMD == B_MNMAJOR && AM != A_TMA && BN_ == 512), "pair mode: softmax A, N-major B, BN 512");
+    static_assert(!PAIR_ || (BMD == B_MNMAJOR ? BN_ == 512 : BN_ == 256), "pair mode: BN 512 (N-major B) or 256");
 };
 
 // ------------------------------------------------------------------ descriptors
@@ -265,7 +266,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         for (int s = 0; s < C::STAGES; ++s) {
             dg::mbar_init(&sh.full[s], 1);
             // pair: one arrival per transform warp of both CTAs, in the first CTA's barrier
-            dg::mbar_init(&sh.xform[s], PAIR ? 2 * C::kXformWarps : (C::kXform ? C::kXformThreads : 1));
+            // (without a transform: the second CTA's relay, once its own stage has landed)
+            dg::mbar_init(&sh.xform[s], PAIR ? (C::kXform ? 2 * C::kXformWarps : 1) : (C::kXform ? C::kXformThreads : 1));
             dg::mbar_init(&sh.empty[s], PAIR ? 1u : (uint32_t)cm);  // one release per CTA of the cluster
         }
         for (int i = 0; i < C::kNAcc; ++i) {
@@ -342,7 +344,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                                                    &sh.full[s], mask);
                         }
                     } else if (C::kBMode == B_KMAJOR) {
-                        dg::tma_load_2d(sB, &tmB0, k0, im.n * C::BN, &sh.full[s]);
+                        // pair: this CTA's half of the tile's rows (box of BN / 2 rows)
+                        dg::tma_load_2d(sB, &tmB0, k0, im.n * C::BN + (PAIR ? rank * (C::BN / 2) : 0), &sh.full[s]);
+                    } else if (PAIR) {
+                        // gate rows from the first CTA, up rows from the second
+                        dg::tma_load_2d(sB, rank == 0 ? &tmB0 : &tmB1, k0, im.n * (C::BN / 2), &sh.full[s]);
                     } else {
                         // gate rows in the first half of the tile, up rows in the second
                         dg::tma_load_2d(sB, &tmB0, k0, im.n * (C::BN / 2), &sh.full[s]);
@@ -356,9 +362,23 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
+        // ------------------------------------------------ MMA issuer (relay in the pair's second CTA)
+        if (PAIR && !C::kXform && lane == 0 && !leader) {
+            // tell the first CTA when this CTA's part of each stage has landed
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t G = cid; G < n_groups && ok && !aborted(sh); G += ncl) {
+                const Item im = decode(a, mt, cm, rank, G);
+                for (int kb = im.kb_lo; kb < im.kb_hi; ++kb, ++it) {
+                    const int s = (int)(it % C::STAGES);
+                    if (!dg::mbar_wait(&sh.full[s], (it / C::STAGES) & 1u)) { ok = false; break; }
+                    dg::mbar_arrive_remote(dg::mapa_shared(&sh.xform[s], 0));
+                }
+            }
+            if (!ok) do_abort(sh, a.status);
+        }
         if (lane == 0 && leader) {
-            constexpr uint32_t idesc_pair = instr_desc(2 * BM, 256, true);
+            constexpr uint32_t idesc_pair = instr_desc(2 * BM, 256, C::kBMode == B_MNMAJOR);
             constexpr uint32_t idesc_mn = instr_desc(BM, C::BN > 256 ? 256 : C::BN, true);
             constexpr uint32_t idesc_k = instr_desc(BM, C::BN > 256 ? 256 : C::BN, false);
             constexpr uint32_t idesc = (C::kBMode == B_MNMAJOR) ? idesc_mn : idesc_k;
@@ -377,8 +397,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 for (int kb = im.kb_lo; kb < im.kb_hi; ++kb, ++it) {
                     const int s = (int)(it % C::STAGES);
                     const uint32_t ph = (it / C::STAGES) & 1u;
-                    // pair: the transform warps of both CTAs report (after their own full waits)
-                    if (!PAIR && !dg::mbar_wait(&sh.full[s], ph)) { ok = false; break; }
+                    // pair: the transform warps of both CTAs report (after their own full waits);
+                    // without a transform, this CTA's stage and the second CTA's relay
+                    if ((!PAIR || !C::kXform) && !dg::mbar_wait(&sh.full[s], ph)) { ok = false; break; }
                     if (PAIR && !dg::mbar_wait(&sh.xform[s], ph)) { ok = false; break; }
                     if (!PAIR && C::kXform && !dg::mbar_wait(&sh.xform[s], ph)) { ok = false; break; }
                     dg::tc_fence_after();
@@ -388,13 +409,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     for (int kk = 0; kk < C::BK / 16; ++kk) {
                         const uint64_t ad = smem_desc(sA + kk * 32, 16, 8 * C::BK * 2, C::kASwizzle);
                         const uint32_t accum = (kb > im.kb_lo || kk > 0) ? 1u : 0u;
-                        if constexpr (PAIR) {
+                        if constexpr (PAIR && C::kBMode == B_MNMAJOR) {
                             // two N = 256 slabs; this CTA's B holds 2 atom columns of each
 #pragma unroll
                             for (int h = 0; h < C::BN / 256; ++h) {
                                 const uint64_t bd = smem_desc(sB + h * 2 * (C::BK * 128) + kk * 16 * 128, C::BK * 128, 1024, 128);
                                 dg::tc_mma_f16_pair(dacc + h * 256, ad, bd, idesc_pair, accum);
                             }
+                        } else if constexpr (PAIR) {
+                            // K-major B: this CTA's BN / 2 rows
+                            const uint64_t bd = smem_desc(sB + kk * 32, 16, 8 * C::BK * 2, C::kASwizzle);
+                            dg::tc_mma_f16_pair(dacc, ad, bd, idesc_pair, accum);
                         } else if (C::kBMode == B_MNMAJOR) {
                             // N-major B: LBO = distance between 64-column atom columns, SBO = 8 K rows
 #pragma unroll
@@ -668,8 +693,9 @@ __global__ void k_zero_rows(const dg_canvas_params* __restrict__ params, const u
 using PEbf16 = Cfg<A_SOFTMAX_BF16, B_MNMAJOR, 512, 32, 8, true>;
 using PEfp32 = Cfg<A_SOFTMAX_FP32, B_MNMAJOR, 512, 32, 5, true>;
 using PEprob = Cfg<A_TMA, B_MNMAJOR, 512, 32, 5>;
-using GateUp = Cfg<A_TMA, B_KMAJOR_GATEUP, 256, 64, 4>;
-using Down = Cfg<A_TMA, B_KMAJOR, 256, 64, 4>;
+using GateUp = Cfg<A_TMA, B_KMAJOR_GATEUP, 256, 64, 6, true>;
+using Down = Cfg<A_TMA, B_KMAJOR, 256, 64, 6, true>;
+using DownSingle = Cfg<A_TMA, B_KMAJOR, 256, 64, 4>;  // plain GEMMs (K-major B) on one CTA per tile
 
 constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -870,7 +896,7 @@ dg_status run_mlp(const uint16_t* pe, uint16_t* hmid, int64_t rows, int32_t d, i
     if (s != DG_OK) return s;
 
     if (!tmap_2d(t2.a, 0, hmid, h, rows, h, 64, BM, 128)) return DG_ERR_CUDA;
-    if (!tmap_2d(t2.b0, 0, W_down, h, d, h, 64, 256, 128)) return DG_ERR_CUDA;
+    if (!tmap_2d(t2.b0, 0, W_down, h, d, h, 64, Down::kPair ? 128 : 256, 128)) return DG_ERR_CUDA;
     GemmArgs q = g;
     q.n_tiles = (d + 255) / 256;
     q.k_blocks = (h + 63) / 64;
@@ -972,7 +998,6 @@ dg_status dg_self_cond_pe(const void* logits, dg_dtype dtype, int64_t ld, const 
     g.tpc = tpc;
     g.n_tiles = (d + 511) / 512;
     g.k_blocks = (int32_t)((V + bk - 1) / bk);
-    const int64_t Tmax = (int64_t)g.m_tiles * g.n_tiles;
     g.splits = 1;  // set by the plan
     g.K = V;
     g.L = L;
@@ -1132,7 +1157,6 @@ dg_status dg_gemm_bf16(const uint16_t* A, int64_t lda, const uint16_t* B, int64_
         if (!tmap_2d(tm.b0, 0, B, N, K, ldb, 64, bk, 128)) return DG_ERR_CUDA;
         g.n_tiles = (int32_t)((N + 511) / 512);
         g.k_blocks = (int32_t)((K + bk - 1) / bk);
-        const int64_t T = (int64_t)g.m_tiles * g.n_tiles;
         return plan_and_launch<PEprob>(tm.a, tm.b0, tm.b0, g, slots_cap, st);
     }
     const int bk = 64;
@@ -1140,8 +1164,7 @@ dg_status dg_gemm_bf16(const uint16_t* A, int64_t lda, const uint16_t* B, int64_
     if (!tmap_2d(tm.b0, 0, B, K, N, ldb, bk, 256, 128)) return DG_ERR_CUDA;
     g.n_tiles = (int32_t)((N + 255) / 256);
     g.k_blocks = (int32_t)((K + bk - 1) / bk);
-    const int64_t T = (int64_t)g.m_tiles * g.n_tiles;
-    return plan_and_launch<Down>(tm.a, tm.b0, tm.b0, g, slots_cap, st);
+    return plan_and_launch<DownSingle>(tm.a, tm.b0, tm.b0, g, slots_cap, st);
 }
 
 }  // extern "C"
@@ -1202,7 +1225,7 @@ extern "C" dg_status dg_gemm_bf16_noalloc(const uint16_t* A, int64_t lda, const 
     const int64_t T = (int64_t)g.m_tiles * g.n_tiles;
     const int64_t slots_cap = (int64_t)(dg_gemm_workspace_bytes(M, N) / ((size_t)BM * 512 * 4));
     LaunchPlan pl;
-    if (!(b_mn_major ? plan_gemm<PEprob>(g, slots_cap, &pl) : plan_gemm<Down>(g, slots_cap, &pl))) return DG_ERR_CUDA;
+    if (!(b_mn_major ? plan_gemm<PEprob>(g, slots_cap, &pl) : plan_gemm<DownSingle>(g, slots_cap, &pl))) return DG_ERR_CUDA;
     g.splits = pl.splits;
     const size_t need = g.splits > 1 ? (size_t)T * g.splits * BM * bn * 4 : 0;
     if (need > (size_t)DG_NOALLOC_SCRATCH_BYTES) return DG_ERR_UNSUPPORTED;
@@ -1219,5 +1242,5 @@ extern "C" dg_status dg_gemm_bf16_noalloc(const uint16_t* A, int64_t lda, const 
     }
     if (!tmap_2d(tm.a, 0, A, K, M, lda, bk, BM, 128)) return DG_ERR_CUDA;
     if (!tmap_2d(tm.b0, 0, B, K, N, ldb, bk, 256, 128)) return DG_ERR_CUDA;
-    return launch_gemm<Down>(tm.a, tm.b0, tm.b0, g, pl, st);
+    return launch_gemm<DownSingle>(tm.a, tm.b0, tm.b0, g, pl, st);
 }

@@ -69,6 +69,11 @@ def _load():
         lib.orc_pe_from_probs.argtypes = [P, i64, i64, i32, P, P, ctypes.c_int]
         lib.orc_gated_mlp.argtypes = [P, i64, i32, i32, P, P, P, P, ctypes.c_int]
         lib.orc_probs_from_logits.argtypes = [P, ctypes.c_int, i64, i64, i64, P, P, ctypes.c_int]
+        lib.orc_choice_probs.argtypes = [P, ctypes.c_int, i64, i64, i64, P, P, i32, P, ctypes.c_int]
+        lib.orc_bf16_round.argtypes = [ctypes.c_float]
+        lib.orc_bf16_round.restype = ctypes.c_uint16
+        lib.orc_embed_canvas.argtypes = [P, i64, i64, P, i32, P, ctypes.c_float, P]
+        lib.orc_commit.argtypes = [P, P, P, i64, i32, P, P, P, P]
         lib.orc_max_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -262,3 +267,53 @@ def self_cond_rows(rows, T_rows, E_bf16, W_gate, W_up, W_down, V: int | None = N
     """Self-conditioning delta for logit rows: gated MLP of softmax(x / T) . E."""
     P = probs_from_logits(rows, T_rows, V=V, n_threads=n_threads)
     return gated_mlp(pe_from_probs(P, E_bf16, n_threads), W_gate, W_up, W_down, n_threads)
+
+
+# ---------------------------------------------------------------- single-pass reads
+def choice_probs(rows, T_rows, choices, V: int | None = None, n_threads: int = 0) -> np.ndarray:
+    """p = exp(x_tok / T - lse) for caller-given tokens per row (fp64); tokens outside
+    [0, V) give 0.  rows: [r, ld] bf16 bits or float32; choices: [r, C] int32."""
+    lib = _load()
+    x = np.ascontiguousarray(rows)
+    r, ld = x.shape
+    V = ld if V is None else V
+    T = _c(np.broadcast_to(np.asarray(T_rows, np.float64), (r,)), np.float64)
+    ch = _c(choices, np.int32)
+    C = ch.shape[1]
+    assert ch.shape[0] == r
+    out = np.zeros((r, C), np.float64)
+    lib.orc_choice_probs(_ptr(x), _dtype_code(x), ld, r, V, _ptr(T), _ptr(ch), C, _ptr(out), int(n_threads))
+    return out
+
+
+# ---------------------------------------------------------------- step-after glue
+def bf16_round(f: float) -> int:
+    """Round-to-nearest-even of an fp32 value to a bf16 bit pattern."""
+    return int(_load().orc_bf16_round(float(np.float32(f))))
+
+
+def embed_canvas(canvas, E_bf16, delta_bf16=None, scale: float = 1.0) -> np.ndarray:
+    """emb = bf16(fma(scale, E[canvas], delta)) as bf16 bit patterns [rows, d]."""
+    lib = _load()
+    cv = _c(canvas, np.int32).reshape(-1)
+    E = _c(E_bf16, np.uint16)
+    V, d = E.shape
+    dl = None if delta_bf16 is None else _c(delta_bf16, np.uint16).reshape(-1, d)
+    out = np.zeros((cv.shape[0], d), np.uint16)
+    lib.orc_embed_canvas(_ptr(cv), cv.shape[0], V, _ptr(E), d, _ptr(dl), float(scale), _ptr(out))
+    return out
+
+
+def commit(converged, active, argmax, tokens, prev_argmax, stable_count) -> dict:
+    """Commit of converged active canvases: tokens = argmax, state reset (copies returned)."""
+    lib = _load()
+    cv = _c(converged, np.uint8)
+    ac = _c(active, np.uint8)
+    am = _c(argmax, np.int32)
+    n, L = am.shape
+    tok = _c(tokens, np.int32).copy()
+    prev = _c(prev_argmax, np.int32).copy()
+    st = _c(stable_count, np.int32).copy()
+    committed = np.zeros(n, np.uint8)
+    lib.orc_commit(_ptr(cv), _ptr(ac), _ptr(am), n, L, _ptr(tok), _ptr(prev), _ptr(st), _ptr(committed))
+    return {"tokens": tok, "prev_argmax": prev, "stable_count": st, "committed": committed}

@@ -19,9 +19,10 @@
  *         as 1, 2, 3", SC'11 -- the Philox-4x32 bijection with 10 rounds.
  *   [GELU] D. Hendrycks, K. Gimpel, "Gaussian Error Linear Units" -- tanh form.
  *
- * Readings where the pages are silent are listed in the design doc and restated at the
- * function that takes them.  Everything is fp64 and follows the definitions in the
- * order the pages give them; nothing is blocked, fused or reordered.
+ * Where the pages are silent, the reading taken is stated at the function that takes
+ * it.  Everything is fp64 (except where an output is a rounded bf16 bit pattern, whose
+ * definition fixes the rounding) and follows the definitions in the order the pages
+ * give them; nothing is blocked, fused or reordered.
  *
  * Pins: every function here is checked by tests/test_oracle_*.py against closed
  * forms, hand-worked examples, brute force and invariants (see those files).
@@ -486,6 +487,101 @@ void orc_probs_from_logits(const void* logits, int dtype, int64_t ld, int64_t n_
         for (int64_t v = 0; v < V; ++v) s += exp(orc_logit(row, dtype, v) / T - m);
         double lse = m + log(s);
         for (int64_t v = 0; v < V; ++v) P[r * V + v] = exp(orc_logit(row, dtype, v) / T - lse);
+    }
+}
+
+/* ------------------------------------------------------------------------------- */
+/* Single-pass reads [SPR], sections "답의 내용은 몰라도 답을 담을 자리는 안다" and     */
+/* "12개 입력과 4개 캔버스를 예산에 넣어 보면": a read-only request wants the        */
+/* probability of fixed answer tokens at its answer slots.  Reading: the probability */
+/* under the step's distribution softmax(x / T), p = exp(x_tok / T - lse), with lse   */
+/* from the definition; slots with a token outside [0, V) (unused: -1) give 0.        */
+/* ------------------------------------------------------------------------------- */
+void orc_choice_probs(const void* logits, int dtype, int64_t ld, int64_t n_rows, int64_t V,
+                      const double* T_rows, const int32_t* choices, int32_t C, double* probs,
+                      int n_threads)
+{
+    size_t esize = dtype == 0 ? 2 : 4;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        const char* row = (const char*)logits + (size_t)r * (size_t)ld * esize;
+        double T = T_rows[r];
+        double m = -INFINITY;
+        for (int64_t v = 0; v < V; ++v) {
+            double y = orc_logit(row, dtype, v) / T;
+            if (y > m) m = y;
+        }
+        double s = 0.0;
+        for (int64_t v = 0; v < V; ++v) s += exp(orc_logit(row, dtype, v) / T - m);
+        double lse = m + log(s);
+        for (int32_t k = 0; k < C; ++k) {
+            int32_t tok = choices[r * C + k];
+            probs[r * C + k] = (tok >= 0 && tok < V) ? exp(orc_logit(row, dtype, tok) / T - lse) : 0.0;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------------- */
+/* Step-after glue [DG], section "DiffusionGemmaModelState와 DiffusionSampler" (the   */
+/* input-preparation hook adds the stored feedback to the canvas embeddings) and     */
+/* "자기 조건화" (the feedback is added to the next pass's canvas embeddings):       */
+/*   emb[r] = bf16( fma(scale, E[canvas[r]], delta[r]) )                            */
+/* The output is a bf16 bit pattern, so its definition fixes the rounding: one fp32  */
+/* fused multiply-add, then round-to-nearest-even to bf16.  `scale` is the model's    */
+/* embedding scale (1 for a plain lookup); delta NULL (prefill / commit passes: no   */
+/* feedback) adds nothing.  A token outside [0, V) gives a zero row.                 */
+/* ------------------------------------------------------------------------------- */
+uint16_t orc_bf16_round(float f)
+{
+    uint32_t b;
+    memcpy(&b, &f, sizeof b);
+    if ((b & 0x7f800000u) == 0x7f800000u && (b & 0x007fffffu) != 0u)
+        return (uint16_t)((b >> 16) | 0x0040u);          /* NaN stays NaN (quiet) */
+    uint32_t lsb = (b >> 16) & 1u;                       /* ties go to the even neighbour */
+    return (uint16_t)((b + 0x7fffu + lsb) >> 16);
+}
+
+void orc_embed_canvas(const int32_t* canvas, int64_t n_rows, int64_t V, const uint16_t* E,
+                      int32_t d, const uint16_t* delta, float scale, uint16_t* out)
+{
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int32_t tok = canvas[r];
+        for (int32_t j = 0; j < d; ++j) {
+            if (tok < 0 || tok >= V) {
+                out[r * d + j] = 0;
+                continue;
+            }
+            float e = (float)orc_bf16(E[(int64_t)tok * d + j]);
+            float a = delta ? (float)orc_bf16(delta[r * d + j]) : 0.0f;
+            out[r * d + j] = orc_bf16_round(fmaf(scale, e, a));
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------------- */
+/* Commit [DG], section "DiffusionGemmaModelState와 DiffusionSampler", Commit case:  */
+/* a converged canvas emits its argmax as the block's tokens.  Reading: only         */
+/* canvases still active this step commit (a canvas commits once); their loop state  */
+/* is reset for the next block (no previous argmax, stable count 0).                  */
+/* ------------------------------------------------------------------------------- */
+void orc_commit(const uint8_t* converged, const uint8_t* active, const int32_t* argmax, int64_t n,
+                int32_t L, int32_t* tokens, int32_t* prev_argmax, int32_t* stable_count,
+                uint8_t* committed)
+{
+    for (int64_t c = 0; c < n; ++c) {
+        int go = active[c] && converged[c];
+        committed[c] = (uint8_t)(go ? 1 : 0);
+        if (!go) continue;
+        for (int32_t i = 0; i < L; ++i) {
+            tokens[c * L + i] = argmax[c * L + i];
+            prev_argmax[c * L + i] = -1;
+        }
+        stable_count[c] = 0;
     }
 }
 

@@ -134,19 +134,20 @@ def _workload_arith(wl, n_sc_rows, n_read_rows):
 
 
 def _profile_traffic(kernel_tag: str):
-    """Per-launch DRAM bytes recorded from an ncu capture in profiles/, if the kernel source
-    it was taken on is unchanged (else None)."""
-    src = os.path.join(ROOT, "entropy_bounded_denoising_gb300", "csrc")
-    h = hashlib.sha256()
-    for f in sorted(os.listdir(src)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(src, f), "rb") as fh:
-                h.update(fh.read())
-    digest = h.hexdigest()[:16]
+    """Per-launch DRAM bytes recorded from an ncu capture in profiles/, if the kernel sources
+    it was taken on (the files its `csrc_files:` line lists) are unchanged (else None)."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
+    src = os.path.join(ROOT, "entropy_bounded_denoising_gb300", "csrc")
+    f = re.search(r"csrc_files:\s*([^\n]+)", txt)
+    files = f.group(1).split() if f else sorted(x for x in os.listdir(src) if x.endswith((".cu", ".cuh")))
+    h = hashlib.sha256()
+    for name in files:
+        with open(os.path.join(src, name), "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()[:16]
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
     s = re.search(r"csrc_sha256_16:\s*([0-9a-f]{16})", txt)
     if m and s and s.group(1) == digest:
@@ -422,6 +423,51 @@ def run_ours(args):
                "d2h_bytes_per_step": d2h, "ms_per_step": ms2 / args.steps,
                "pipelining": "next step's H2D overlaps this step's compute (two device input buffers)"}
 
+    # ---------------------------------------------------------------- rows around the step
+    # Timed alone (not part of the step): the next pass's embeddings (token rows + feedback),
+    # single-pass-read choice probabilities (4 slots per position) and the commit, each
+    # against the HBM roofline of its algorithmic bytes.
+    around = None
+    if not args.no_extras:
+        rng = np.random.default_rng(5)
+        emb = torch.empty((n * L, d), dtype=torch.bfloat16, device=dev)
+        C = 4
+        choices = torch.from_numpy(rng.integers(0, V, (n, L, C)).astype(np.int32)).to(dev)
+        probs = torch.empty((n, L, C), dtype=torch.float32, device=dev)
+        tokens = torch.empty((n, L), dtype=torch.int32, device=dev)
+        committed = torch.empty((n,), dtype=torch.uint8, device=dev)
+
+        def _time(fn, reps=50):
+            for _ in range(5):
+                fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / reps
+
+        def _entry(ms, nbytes):
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            return {"ms": ms, "alg_bytes": nbytes, "achieved_gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"]}
+
+        around = {
+            "embed_canvas": _entry(_time(lambda: dg.dg_embed_canvas(canvas, E, delta.view(n * L, d), emb, 1.0,
+                                                                    stream=stream)),
+                                   n * L * (3 * d * 2 + 4)),
+            "choice_probs": _entry(_time(lambda: dg.dg_choice_probs(x, lse, params, choices, probs, stream=stream)),
+                                   n * L * (C * (4 + 4 + 2) + 4)),
+            "commit": _entry(_time(lambda: dg.dg_commit(params, conv, am, tokens, prev, stable, committed,
+                                                        stream=stream)),
+                             n * L * 4 * 2 + n * 10),
+            "note": "timed alone, not part of the step; alg_bytes: embed = E rows gathered + feedback + "
+                    "output; choice_probs = 4 slots x (token + probability + logit) + lse; commit = argmax + tokens",
+        }
+        torch.cuda.synchronize()
+        if dg.dg_get_device_status():
+            raise RuntimeError("device status set by the rows around the step")
+
     # ---------------------------------------------------------------- CPU baseline (oracle)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -454,6 +500,7 @@ def run_ours(args):
                        "mlp_tflops": ar["mlp_flops"] / (t_mlp * 1e-3) / 1e12 if t_mlp > 0 else 0.0},
         "steps_per_s": 1e3 / ms_step, "self_cond_rows": n_sc_rows, "converged_canvases": n_conv,
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clk.summary(),
+        "around_step": around,
     }
     print(json.dumps(line), flush=True)
     if ws > 1:
@@ -469,6 +516,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="batched", choices=["batched", "sweep", "ragged", "single", "tiny", "profile"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip timing the rows around the step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":

@@ -69,6 +69,9 @@ def load(path: str | None = None):
         "dg_gemm_workspace_bytes": (sz, [i64, i64]),
         "dg_gemm_bf16": (st, [P, i64, P, i64, ctypes.c_int, P, i64, i64, i64, i64, P, sz, P]),
         "dg_gemm_bf16_noalloc": (st, [P, i64, P, i64, ctypes.c_int, P, i64, i64, i64, i64, P]),
+        "dg_choice_probs": (st, [P, ctypes.c_int, i64, P, P, i64, i32, i64, P, i32, P, P]),
+        "dg_embed_canvas": (st, [P, i64, i64, P, i32, P, ctypes.c_float, P, P]),
+        "dg_commit": (st, [P, P, P, i64, i32, P, P, P, P, P]),
         "dg_philox_words": (st, [u64, u32, u32, u32, u32, u32, i64, P, P]),
         "dg_get_device_status": (st, [P, ctypes.POINTER(u32)]),
         "dg_clear_device_status": (st, [P]),
@@ -91,7 +94,7 @@ def exported_symbols() -> list[str]:
                         "dg_self_cond_logits", "dg_self_cond_prepare", "dg_self_cond_pe",
                         "dg_self_cond_mlp", "dg_self_cond_probs_workspace_bytes",
                         "dg_self_cond_probs", "dg_gemm_workspace_bytes", "dg_gemm_bf16",
-                        "dg_gemm_bf16_noalloc",
+                        "dg_gemm_bf16_noalloc", "dg_choice_probs", "dg_embed_canvas", "dg_commit",
                         "dg_philox_words", "dg_get_device_status", "dg_clear_device_status",
                         "dg_status_string", "dg_version", "dg_launch_count") if hasattr(lib, n)]
 
@@ -207,6 +210,37 @@ def dg_advance_params(params, converged, n_canvas, stream=None, check=True) -> i
     rc = load().dg_advance_params(_p(params), _p(converged), n_canvas, _s(stream))
     if check:
         _check("dg_advance_params", rc)
+    return rc
+
+
+def dg_choice_probs(logits, lse, params, choices, probs, *, V=None, stream=None, check=True) -> int:
+    """probs[c, i, k] = exp(logits[c, i, choices[c, i, k]] / T - lse[c, i]); logits [n, L, ld]."""
+    n, L, ld = logits.shape
+    C = choices.shape[-1]
+    rc = load().dg_choice_probs(_p(logits), _dtype_code(logits), ld, _p(lse), _p(params), n, L,
+                                ld if V is None else V, _p(choices), C, _p(probs), _s(stream))
+    if check:
+        _check("dg_choice_probs", rc)
+    return rc
+
+
+def dg_embed_canvas(canvas, E, delta_emb, out, scale: float = 1.0, stream=None, check=True) -> int:
+    """out = bf16(fma(scale, E[canvas], delta_emb)); canvas [..] int32, E [V, d], out [.., d]."""
+    V, d = E.shape
+    rc = load().dg_embed_canvas(_p(canvas), canvas.numel(), V, _p(E), d, _p(delta_emb), float(scale),
+                                _p(out), _s(stream))
+    if check:
+        _check("dg_embed_canvas", rc)
+    return rc
+
+
+def dg_commit(params, converged, argmax, tokens, prev_argmax, stable_count, committed, stream=None,
+              check=True) -> int:
+    n, L = argmax.shape
+    rc = load().dg_commit(_p(params), _p(converged), _p(argmax), n, L, _p(tokens), _p(prev_argmax),
+                          _p(stable_count), _p(committed), _s(stream))
+    if check:
+        _check("dg_commit", rc)
     return rc
 
 

@@ -277,6 +277,57 @@ DG_API dg_status dg_gemm_bf16_noalloc(const uint16_t* A, int64_t lda, const uint
                                       int64_t K, dg_stream_t stream);
 
 /* ------------------------------------------------------------------------------------ */
+/* Around the step: single-pass reads, the next pass's inputs, commit.                  */
+/* ------------------------------------------------------------------------------------ */
+
+/* Single-pass reads [SPR, "답의 내용은 몰라도 답을 담을 자리는 안다"]: a read-only request
+ * reads the probability of fixed answer tokens at its answer slots.  For every position of
+ * every DG_ACTIVE canvas and every slot k < C:
+ *   probs[c][i][k] = exp(logits[c][i][tok] / T - lse[c][i]),  tok = choices[c][i][k],
+ * the probability under the step's distribution softmax(logits / T) (T of the canvas; 1
+ * for plain probabilities), with lse from dg_denoise_step of the same logits.  A slot with a
+ * token outside [0, V) gives 0 (use -1 for unused slots).  Inactive canvases are skipped.
+ *   logits  (device) [n_canvas][L][ld] bf16 or fp32, as for dg_denoise_step.
+ *   lse     (device) [n_canvas][L] float.
+ *   choices (device) [n_canvas][L][C] int32.
+ *   probs   (device, out) [n_canvas][L][C] float.
+ * Limits: 1 <= C <= 1024, L and V as dg_denoise_step.
+ * Errors: DG_ERR_INVALID_ARG, DG_ERR_ALIGNMENT (logits not 16-byte aligned), DG_ERR_CUDA. */
+DG_API dg_status dg_choice_probs(const void* logits, dg_dtype dtype, int64_t ld, const float* lse,
+                          const dg_canvas_params* params, int64_t n_canvas, int32_t L, int64_t V,
+                          const int32_t* choices, int32_t C, float* probs, dg_stream_t stream);
+
+/* The next pass's canvas embeddings [DG "DiffusionGemmaModelState와 DiffusionSampler", the
+ * input-preparation hook; "자기 조건화": the feedback is added to the canvas embeddings]:
+ *   out[r] = bf16( fma(scale, E[canvas[r]], delta_emb[r]) )   for r < n_rows,
+ * one fp32 fused multiply-add per element, rounded to nearest even.  delta_emb NULL (the
+ * prefill and commit passes, no feedback) adds nothing; `scale` is the model's embedding
+ * scale (1 for a plain lookup).  A token outside [0, V) gives a zero row.
+ *   canvas    (device) [n_rows] int32 (e.g. the [n][L] canvas, n_rows = n * L).
+ *   E         (device) [V][d] bf16.
+ *   delta_emb (device, may be NULL) [n_rows][d] bf16.
+ *   out       (device, out) [n_rows][d] bf16; must not overlap E or delta_emb.
+ * Limits: d % 8 == 0, 8 <= d <= 65536, 0 <= n_rows < 2^31, 2 <= V < 2^31.
+ * Errors: DG_ERR_INVALID_ARG, DG_ERR_ALIGNMENT (E, delta_emb, out not 16-byte aligned),
+ * DG_ERR_CUDA. */
+DG_API dg_status dg_embed_canvas(const int32_t* canvas, int64_t n_rows, int64_t V, const uint16_t* E,
+                          int32_t d, const uint16_t* delta_emb, float scale, uint16_t* out,
+                          dg_stream_t stream);
+
+/* Commit case [DG "DiffusionGemmaModelState와 DiffusionSampler"]: every canvas that is
+ * DG_ACTIVE and converged this step emits its argmax canvas as the block's tokens, and its
+ * loop state is reset for the next block (prev_argmax = -1, stable_count = 0);
+ * committed[c] = 1 for those canvases and 0 for every other (whose tokens and state are
+ * left unchanged).  Call it after dg_denoise_step and before dg_advance_params.
+ *   converged (device) [n_canvas] uint8, argmax (device) [n_canvas][L] int32.
+ *   tokens, prev_argmax (device, in/out) [n_canvas][L] int32; stable_count (device, in/out)
+ *   [n_canvas] int32; committed (device, out) [n_canvas] uint8.
+ * Limits: 1 <= L <= 1024, 0 <= n_canvas <= 65535.  Errors: DG_ERR_INVALID_ARG, DG_ERR_CUDA. */
+DG_API dg_status dg_commit(const dg_canvas_params* params, const uint8_t* converged, const int32_t* argmax,
+                    int64_t n_canvas, int32_t L, int32_t* tokens, int32_t* prev_argmax,
+                    int32_t* stable_count, uint8_t* committed, dg_stream_t stream);
+
+/* ------------------------------------------------------------------------------------ */
 /* Random numbers and status.                                                          */
 /* ------------------------------------------------------------------------------------ */
 

@@ -452,7 +452,20 @@ def run_ours(args):
             gbs = nbytes / (ms * 1e-3) / 1e9
             return {"ms": ms, "alg_bytes": nbytes, "achieved_gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"]}
 
+        p_all = dict(p)
+        p_all["flags"] = p["flags"] | dg.DG_SAMPLE_ALL
+        params_all = dg.params_tensor(p_all, dev)
+
+        def _denoise(prm):
+            return lambda: dg.dg_denoise_step(x, prm, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv,
+                                              stream=stream)
+
         around = {
+            "denoise_step": {"ms": _time(_denoise(params), reps=20),
+                             "note": "dg_denoise_step as in the step: samples drawn at the accepted positions"},
+            "denoise_step_sample_all": {"ms": _time(_denoise(params_all), reps=20),
+                                        "note": "dg_denoise_step with DG_SAMPLE_ALL: every position draws its "
+                                                "sample in the statistics pass"},
             "embed_canvas": _entry(_time(lambda: dg.dg_embed_canvas(canvas, E, delta.view(n * L, d), emb, 1.0,
                                                                     stream=stream)),
                                    n * L * (3 * d * 2 + 4)),

@@ -18,7 +18,7 @@ from . import build as _build
 
 DG_OK, DG_ERR_INVALID_ARG, DG_ERR_ALIGNMENT, DG_ERR_WORKSPACE, DG_ERR_UNSUPPORTED, DG_ERR_CUDA = 0, -1, -2, -3, -4, -5
 DG_BF16, DG_FP32 = 0, 1
-DG_ACTIVE, DG_READ_ONLY, DG_SELF_COND = 1, 2, 4
+DG_ACTIVE, DG_READ_ONLY, DG_SELF_COND, DG_SAMPLE_ALL = 1, 2, 4, 8
 DG_DEV_NAN_INF_ROW, DG_DEV_EMPTY_ROW, DG_DEV_TIMEOUT, DG_DEV_BAD_PARAM = 1, 2, 4, 8
 
 PARAM_FIELDS = ("temperature", "beta", "tau", "k", "max_steps", "min_accept", "step",

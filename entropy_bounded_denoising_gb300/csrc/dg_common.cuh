@@ -21,6 +21,12 @@ DG_DEVINL void raise_status(unsigned* status, unsigned bits) {
     if (status) atomicOr(status, bits);
 }
 
+// Per-canvas parameters the acceptance kernel works with (else DG_DEV_BAD_PARAM, canvas skipped).
+DG_DEVINL bool canvas_params_ok(const dg_canvas_params& p, int32_t L) {
+    return p.temperature > 0.f && isfinite(p.temperature) && p.k >= 1 && p.max_steps >= 1 && p.min_accept >= 0 &&
+           p.min_accept <= L;
+}
+
 // ------------------------------------------------------------------ Philox-4x32-10
 struct u4 { uint32_t x, y, z, w; };
 

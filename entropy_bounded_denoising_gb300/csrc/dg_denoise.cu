@@ -22,6 +22,10 @@
 // between passes, so no lane diverges on a new maximum.  Queued groups are drawn a warp's
 // worth at a time, with the Philox rounds that do not depend on the entry index computed
 // once per row.
+// A sample is kept only at an accepted position (a rejected one is renoised in the same
+// step), so canvases without DG_SAMPLE_ALL skip the search in the statistics pass; after the
+// acceptance the same kernel runs again in its deferred mode over the accepted rows only,
+// with the row maximum already known (no statistics, no pass 1).
 // The reduction order depends only on V, so a row's result does not depend on its batch.
 #include <cuda_runtime.h>
 
@@ -340,12 +344,12 @@ DG_DEVINL void draw_queued(const int* q_e0, const uint32_t (*q_x)[QW], int qh, i
 // (2) the exponential sums against the warp's running max, which only grows between
 // pieces (a warp-uniform branch), so lanes do not diverge on new maxima.
 // ------------------------------------------------------------------------------------
-template <int DT>
+template <int DT, bool kDeferred>
 __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
     const unsigned char* __restrict__ logits, int64_t ld_bytes, int64_t V, int32_t L,
     const dg_canvas_params* __restrict__ params, uint64_t seed, int32_t* __restrict__ argmax_out,
     int32_t* __restrict__ sample_out, float* __restrict__ entropy_out, float* __restrict__ lse_out,
-    unsigned* status) {
+    const uint8_t* __restrict__ accept_mask, int32_t* __restrict__ canvas_out, unsigned* status) {
     constexpr int VN = Vec<DT>::N;
     constexpr int ES = DT == 0 ? 2 : 4;
     constexpr int GPV = VN / 4;                    // Philox blocks per 16-byte vector
@@ -362,15 +366,35 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
 
     const dg_canvas_params p = params[canvas];
     if (!(p.flags & DG_ACTIVE)) return;
-    if (!(p.temperature > 0.f) || !isfinite(p.temperature)) {
-        if (tid == 0 && pos == 0) dg::raise_status(status, DG_DEV_BAD_PARAM);
-        return;
-    }
-    const bool do_sample = !(p.flags & DG_READ_ONLY);
-    const float invT = 1.0f / p.temperature;
-    const float k2 = kLog2e * invT;
     const int64_t row = canvas * L + pos;
     const unsigned char* src = logits + row * ld_bytes;
+    float m_known = -INFINITY;  // deferred mode: the row's largest raw logit
+    if constexpr (kDeferred) {
+        // only accepted positions of canvases that did not sample in the statistics pass
+        // (parameters the acceptance kernel rejected leave accept_mask unwritten)
+        if ((p.flags & (DG_READ_ONLY | DG_SAMPLE_ALL)) || !dg::canvas_params_ok(p, L)) return;
+        if (!accept_mask[row]) return;
+        const int32_t a = argmax_out[row];
+        const float l = lse_out[row];
+        if (a >= 0 && a < V)
+            m_known = DT == 0 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(src)[a] << 16)
+                              : reinterpret_cast<const float*>(src)[a];
+        if (!(isfinite(m_known) && isfinite(l))) {  // a NaN / inf / empty row: flagged by the statistics pass
+            if (tid == 0) {
+                sample_out[row] = -1;
+                canvas_out[row] = -1;
+            }
+            return;
+        }
+    } else {
+        if (!(p.temperature > 0.f) || !isfinite(p.temperature)) {
+            if (tid == 0 && pos == 0) dg::raise_status(status, DG_DEV_BAD_PARAM);
+            return;
+        }
+    }
+    const bool do_sample = kDeferred || ((p.flags & DG_SAMPLE_ALL) && !(p.flags & DG_READ_ONLY));
+    const float invT = 1.0f / p.temperature;
+    const float k2 = kLog2e * invT;
     const uint32_t bytes = (uint32_t)(V * ES);
     const uint32_t bulk = bytes & ~15u;
     const int npieces = (int)((bytes + kPieceBytes - 1) / kPieceBytes);
@@ -412,7 +436,7 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
         }
     } else {
         // ---------------- consumers
-        RowState st{-INFINITY, 0.f, 0.f, 0.f, 0x7fffffff};
+        RowState st{m_known, 0.f, 0.f, 0.f, 0x7fffffff};
         bool bad = false;
         float best = -INFINITY;    // this lane's best score and its entry
         int bidx = 0x7fffffff;
@@ -440,12 +464,13 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
             auto piece = [&](auto full_tag, auto sample_tag) {
                 constexpr bool FULL = decltype(full_tag)::value;
                 constexpr bool SAMPLE = decltype(sample_tag)::value;
+                constexpr bool STATS = !kDeferred;
                 // ---- pass 1: vector maxima, then the warp's max; a larger one rescales every
                 // lane's state (warp-uniform, so lanes never diverge on a new maximum)
                 uint32_t lm2 = kBf16NegInf2;  // lane max as a bf16 pair (max of even, odd entries)
                 float lane_max = -INFINITY;
 #pragma unroll
-                for (int v = 0; v < kVecPerLane; ++v) {
+                for (int v = 0; v < (STATS ? kVecPerLane : 0); ++v) {
                     const int j = (v * kK1Warps + warp) * 32 + lane;
                     const uint4 w = load_raw<DT, FULL>(slot, j, nvec, n_el);
                     if constexpr (DT == 0) {
@@ -459,8 +484,11 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
                 if (DT == 0) lane_max = max_nan(bf_lo(lm2), bf_hi(lm2));
                 float wmax = lane_max;
 #pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) wmax = max_nan(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
-                if (wmax != wmax) {
+                for (int o = 16; o >= 1; o >>= 1)
+                    if (STATS) wmax = max_nan(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+                if (!STATS) {
+                    // the row maximum is known: nothing to rescale
+                } else if (wmax != wmax) {
                     bad = true;
                 } else if (wmax > st.m) {
                     if (st.m > -INFINITY) {
@@ -503,7 +531,7 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
                         cand[0] = SAMPLE && in && vmax >= x_thr;
                         tie = vmax == st.m;
                     }
-                    if (in) {
+                    if (STATS && in) {
                         float x[VN];
                         if (tie) {
                             // the vector holds the max: count its copies, the rest as usual
@@ -581,7 +609,7 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
 #pragma unroll
                     for (int v = 0; v < kVecPerLane; ++v) vec2(v);
                 }
-                if (DT == 0) {
+                if (DT == 0 && STATS) {
                     st.r += (f2_lo(racc[0]) + f2_hi(racc[0])) + (f2_lo(racc[1]) + f2_hi(racc[1]));
                     st.t += (f2_lo(tacc[0]) + f2_hi(tacc[0])) + (f2_lo(tacc[1]) + f2_hi(tacc[1]));
                 }
@@ -608,8 +636,10 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
         if (do_sample && qn > 0) draw_queued<DT, QW>(q_e0, q_x, qh, qn, lane, V, invT, pre, bound, best, bidx);
         __syncwarp();
         if (bad) sh.bad = 1;
+        if constexpr (!kDeferred) {
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) st = merge(st, shfl_state(st, o), k2);
+            for (int o = 16; o >= 1; o >>= 1) st = merge(st, shfl_state(st, o), k2);
+        }
         warp_best(best, bidx);
         if (lane == 0) {
             sh.warp_state[warp] = st;
@@ -627,7 +657,12 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
             bi = sh.warp_bidx[lane];
         }
         warp_best(b, bi);
-        if (lane == 0) {
+        if (kDeferred && lane == 0) {
+            // the kept sample becomes the position's next token
+            sample_out[row] = bi;
+            canvas_out[row] = bi;
+            if (sh.timeout) dg::raise_status(status, DG_DEV_TIMEOUT);
+        } else if (lane == 0) {
             RowState rs = sh.warp_state[0];
             for (int w = 1; w < kK1Warps; ++w) rs = merge(rs, sh.warp_state[w], k2);
             const bool empty = rs.m == -INFINITY;
@@ -655,7 +690,7 @@ __global__ void __launch_bounds__(1024) k2_accept(
     int32_t L, int64_t V, const dg_canvas_params* __restrict__ params, uint64_t seed, int32_t* __restrict__ canvas,
     int32_t* __restrict__ prev_argmax, int32_t* __restrict__ stable_count, uint8_t* __restrict__ accept_mask,
     uint8_t* __restrict__ converged, float* __restrict__ mean_entropy, int32_t* __restrict__ n_accept,
-    unsigned* status) {
+    bool allow_deferred, unsigned* status) {
     __shared__ float sH[1024];
     __shared__ double sSorted[1024];
     __shared__ double sWarp[32];
@@ -665,12 +700,14 @@ __global__ void __launch_bounds__(1024) k2_accept(
     const int i = threadIdx.x, lane = i & 31, warp = i >> 5, nwarps = blockDim.x >> 5;
     const dg_canvas_params p = params[c];
     if (!(p.flags & DG_ACTIVE)) return;
-    if (!(p.temperature > 0.f) || !isfinite(p.temperature) || p.k < 1 || p.max_steps < 1 || p.min_accept < 0 ||
-        p.min_accept > L) {
+    if (!dg::canvas_params_ok(p, L)) {
         if (i == 0) dg::raise_status(status, DG_DEV_BAD_PARAM);
         return;
     }
     const bool read_only = (p.flags & DG_READ_ONLY) != 0;
+    // accepted positions of a deferred canvas get their sample (and token) from the
+    // deferred sampling pass that follows
+    const bool deferred = allow_deferred && !(p.flags & DG_SAMPLE_ALL);
     const bool valid = i < L;
     const int64_t q = c * L + i;
     const float H = valid ? entropy[q] : 0.f;
@@ -723,10 +760,13 @@ __global__ void __launch_bounds__(1024) k2_accept(
     if (valid) {
         const bool acc = rk < nacc;
         accept_mask[q] = acc ? 1 : 0;
-        if (!read_only)
-            canvas[q] = acc ? sample[q]
-                            : (int32_t)dg::random_token(seed, p.request_id, (uint32_t)p.step, (uint32_t)i,
-                                                        dg::kStreamRenoise, (uint32_t)V);
+        if (!read_only) {
+            if (!acc)
+                canvas[q] = (int32_t)dg::random_token(seed, p.request_id, (uint32_t)p.step, (uint32_t)i,
+                                                      dg::kStreamRenoise, (uint32_t)V);
+            else if (!deferred)
+                canvas[q] = sample[q];
+        }
         prev_argmax[q] = am;
     }
     if (i == 0) {
@@ -790,18 +830,21 @@ bool k1_supported(dg_dtype dt, int64_t V) {
 template <int DT>
 size_t k1_smem_bytes() { return ((sizeof(K1Shared<DT>) + 127) / 128) * 128 + (size_t)kSlots * kPieceBytes; }
 
-template <int DT>
+// kDeferred = false: statistics of every active row (+ samples of DG_SAMPLE_ALL canvases);
+// kDeferred = true: samples and tokens of the accepted positions of the other canvases.
+template <int DT, bool kDeferred>
 dg_status launch_k1(const void* logits, int64_t ld, int64_t n, int32_t L, int64_t V,
                     const dg_canvas_params* params, uint64_t seed, int32_t* argmax, int32_t* sample, float* entropy,
-                    float* lse, cudaStream_t stream) {
-    auto kern = k1_row_stats<DT>;
+                    float* lse, const uint8_t* accept_mask, int32_t* canvas, cudaStream_t stream) {
+    auto kern = k1_row_stats<DT, kDeferred>;
     const size_t smem = k1_smem_bytes<DT>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DG_ERR_CUDA;
     const int64_t ld_bytes = ld * (DT == 0 ? 2 : 4);
     kern<<<dim3((unsigned)L, (unsigned)n, 1), kK1Threads, smem, stream>>>(static_cast<const unsigned char*>(logits),
                                                                           ld_bytes, V, L, params, seed, argmax,
-                                                                          sample, entropy, lse, dghost::status_word());
+                                                                          sample, entropy, lse, accept_mask, canvas,
+                                                                          dghost::status_word());
     dghost::count_launch();
     return dghost::cuda_status(cudaGetLastError());
 }
@@ -809,11 +852,11 @@ dg_status launch_k1(const void* logits, int64_t ld, int64_t n, int32_t L, int64_
 dg_status launch_k2(const float* entropy, const int32_t* sample, const int32_t* argmax, int64_t n, int32_t L,
                     int64_t V, const dg_canvas_params* params, uint64_t seed, int32_t* canvas, int32_t* prev_argmax,
                     int32_t* stable_count, uint8_t* accept_mask, uint8_t* converged, float* mean_entropy,
-                    int32_t* n_accept, cudaStream_t stream) {
+                    int32_t* n_accept, bool allow_deferred, cudaStream_t stream) {
     const unsigned threads = (unsigned)((L + 31) / 32 * 32);
     k2_accept<<<(unsigned)n, threads, 0, stream>>>(entropy, sample, argmax, L, V, params, seed, canvas, prev_argmax,
                                                    stable_count, accept_mask, converged, mean_entropy, n_accept,
-                                                   dghost::status_word());
+                                                   allow_deferred, dghost::status_word());
     dghost::count_launch();
     return dghost::cuda_status(cudaGetLastError());
 }
@@ -843,11 +886,19 @@ dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld, int64_
     if (!aligned16(logits) || (ld * es) % 16 != 0) return DG_ERR_ALIGNMENT;
     if (!k1_supported(dtype, V)) return DG_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
-    s = dtype == DG_BF16 ? launch_k1<0>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, st)
-                         : launch_k1<1>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, st);
+    s = dtype == DG_BF16
+            ? launch_k1<0, false>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, nullptr,
+                                  nullptr, st)
+            : launch_k1<1, false>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, nullptr,
+                                  nullptr, st);
     if (s != DG_OK) return s;
-    return launch_k2(entropy, sample, argmax, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
-                     accept_mask, converged, mean_entropy, n_accept, st);
+    s = launch_k2(entropy, sample, argmax, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
+                  accept_mask, converged, mean_entropy, n_accept, true, st);
+    if (s != DG_OK) return s;
+    return dtype == DG_BF16 ? launch_k1<0, true>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy,
+                                                 lse, accept_mask, canvas, st)
+                            : launch_k1<1, true>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy,
+                                                 lse, accept_mask, canvas, st);
 }
 
 dg_status dg_accept_from_entropy(const float* entropy, const int32_t* sample, const int32_t* argmax,
@@ -862,7 +913,7 @@ dg_status dg_accept_from_entropy(const float* entropy, const int32_t* sample, co
         !converged)
         return DG_ERR_INVALID_ARG;
     return launch_k2(entropy, sample, argmax, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
-                     accept_mask, converged, mean_entropy, n_accept, (cudaStream_t)stream);
+                     accept_mask, converged, mean_entropy, n_accept, false, (cudaStream_t)stream);
 }
 
 dg_status dg_canvas_init(int32_t* canvas, int64_t n_canvas, int32_t L, int64_t V, const dg_canvas_params* params,

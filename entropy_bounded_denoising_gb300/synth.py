@@ -25,7 +25,7 @@ import dataclasses
 import numpy as np
 import torch
 
-ACTIVE, READ_ONLY, SELF_COND = 1, 2, 4
+ACTIVE, READ_ONLY, SELF_COND, SAMPLE_ALL = 1, 2, 4, 8
 
 # purposes for seeding (arbitrary distinct constants)
 _P_BASE, _P_SCALE, _P_NOISE, _P_SPIKE, _P_WEIGHT, _P_PARAMS = 11, 23, 37, 41, 53, 67

@@ -75,7 +75,9 @@ enum {
                           its logits are never read and none of its outputs is written  */
     DG_READ_ONLY = 2u, /* single-pass read [SPR]: statistics only (entropy, lse, argmax);
                           nothing accepted, canvas unchanged, converged = 1              */
-    DG_SELF_COND = 4u  /* compute the self-conditioning feedback for this canvas [DG]    */
+    DG_SELF_COND = 4u, /* compute the self-conditioning feedback for this canvas [DG]    */
+    DG_SAMPLE_ALL = 8u /* draw the Gumbel-max sample at every position; clear = only at
+                          the accepted positions, the only ones whose sample is kept      */
 };
 
 /* Bits of the device status word. */
@@ -102,7 +104,7 @@ typedef struct {
     int32_t min_accept;  /* positions accepted even when the budget allows none (0..L)    */
     int32_t step;        /* 0-based index of this denoising step for the canvas           */
     uint32_t request_id; /* second Philox key word                                        */
-    uint32_t flags;      /* DG_ACTIVE | DG_READ_ONLY | DG_SELF_COND                        */
+    uint32_t flags;      /* DG_ACTIVE | DG_READ_ONLY | DG_SELF_COND | DG_SAMPLE_ALL        */
 } dg_canvas_params;
 
 /* ------------------------------------------------------------------------------------ */
@@ -129,6 +131,14 @@ DG_API size_t dg_denoise_workspace_bytes(int64_t n_canvas, int32_t L, int64_t V,
  * step + 1 >= max_steps; prev_argmax is then overwritten with argmax.  DG_READ_ONLY canvases compute entropy,
  * lse and argmax only (sample = -1, accept_mask = 0, canvas unchanged, converged = 1).
  *
+ * Where the sample is drawn: a rejected position's sample is replaced by its renoise token
+ * in the same step, so by default the sample is drawn only after the acceptance, at the
+ * accepted positions (a second read of those rows); sample = -1 at the rejected ones.  The
+ * canvas, accept mask and every other output are the same either way.  With DG_SAMPLE_ALL
+ * set on a canvas, every position of it draws its sample in the statistics pass (sample
+ * defined everywhere).  The launches are: statistics (+ samples of DG_SAMPLE_ALL canvases),
+ * acceptance / renoise / convergence, then the samples of the accepted positions.
+ *
  *   logits        (device) [n_canvas][L][ld] of dtype; 16-byte aligned; ld >= V and
  *                 ld * sizeof(dtype) a multiple of 16.  Columns V..ld-1 are never read.
  *   params        (device) [n_canvas] dg_canvas_params.
@@ -137,7 +147,7 @@ DG_API size_t dg_denoise_workspace_bytes(int64_t n_canvas, int32_t L, int64_t V,
  *   prev_argmax   (device, in/out) [n_canvas][L] int32: previous argmax canvas; -1 = none.
  *   stable_count  (device, in/out) [n_canvas] int32.
  *   accept_mask   (device, out) [n_canvas][L] uint8 (1 = accepted).
- *   argmax, sample(device, out) [n_canvas][L] int32.
+ *   argmax, sample(device, out) [n_canvas][L] int32 (sample: -1 where not drawn, see above).
  *   entropy, lse  (device, out) [n_canvas][L] float.
  *   converged     (device, out) [n_canvas] uint8.
  *   mean_entropy  (device, out, may be NULL) [n_canvas] float.
@@ -158,7 +168,8 @@ DG_API dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld,
 
 /* The per-canvas half of the step (acceptance, renoise, convergence) on caller-given
  * per-position entropy, sample and argmax, all (device) [n_canvas][L].  Same semantics and
- * outputs as dg_denoise_step; used to test the acceptance rule on chosen entropies. */
+ * outputs as dg_denoise_step, except that every accepted position takes the given sample
+ * (DG_SAMPLE_ALL plays no part); used to test the acceptance rule on chosen entropies. */
 DG_API dg_status dg_accept_from_entropy(const float* entropy, const int32_t* sample,
                                  const int32_t* argmax, int64_t n_canvas, int32_t L, int64_t V,
                                  const dg_canvas_params* params, uint64_t seed,

@@ -102,6 +102,7 @@ def compare_step(g: dict, o: dict, p: dict, V: int, seed: int, canvas_in: np.nda
             continue
         pos = range(L) if rows is None else [i for (cc, i) in rows if cc == c]
         ro = bool(flags[c] & oracle.READ_ONLY)
+        sample_all = bool(flags[c] & synth.SAMPLE_ALL)
         for i in pos:
             rep.positions += 1
             assert g["argmax"][c, i] == o["argmax"][c, i], (c, i)
@@ -111,8 +112,10 @@ def compare_step(g: dict, o: dict, p: dict, V: int, seed: int, canvas_in: np.nda
                 rep.max_h_rel = max(rep.max_h_rel, abs(h - hr) / hr)
             l, lr = float(g["lse"][c, i]), float(o["lse"][c, i])
             assert abs(l - lr) <= LSE_RTOL * max(abs(lr), 1.0), (c, i, l, lr)
-            if ro:
-                assert g["sample"][c, i] == -1
+            if ro or (not sample_all and not g["accept"][c, i]):
+                # read-only canvases draw nothing; other canvases without DG_SAMPLE_ALL draw
+                # only at accepted positions (a rejected sample is renoised in the same step)
+                assert g["sample"][c, i] == -1, (c, i, g["sample"][c, i])
             elif g["sample"][c, i] != o["sample"][c, i]:
                 assert o["sample_gap"][c, i] < BOUNDARY, (c, i, g["sample"][c, i], o["sample"][c, i])
                 rep.sample_boundary += 1

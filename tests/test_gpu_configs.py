@@ -67,7 +67,10 @@ def _loop(wl, sc_from_step, check_rows_per_step):
         if not active.any():
             break
         p = synth.params_with(base, step=t)
-        p["flags"] = np.where(active, dg.DG_ACTIVE | (dg.DG_SELF_COND if t >= sc_from_step else 0), 0).astype(np.uint32)
+        # odd steps draw every position's sample, even steps only the accepted positions'
+        mode = dg.DG_SAMPLE_ALL if t % 2 else 0
+        p["flags"] = np.where(active, dg.DG_ACTIVE | mode | (dg.DG_SELF_COND if t >= sc_from_step else 0),
+                              0).astype(np.uint32)
         x = synth.logits(n, L, V, seed=wl.seed, step=t, scale=wl.scale, spike_frac=wl.spike_frac, dtype=wl.dtype)
         xd = x.to(DEV)
         pt = dg.params_tensor(p, DEV)
@@ -143,11 +146,16 @@ def _one_step(wl, check_canvases, sc_rows, params):
     return g, dh, canvas0
 
 
-def test_batched_full_size():
+@pytest.mark.parametrize("sample_all", [False, True])
+def test_batched_full_size(sample_all):
     wl = synth.WORKLOADS["batched"]
     p = synth.canvas_params(wl, step=1)
+    if sample_all:
+        p["flags"] |= dg.DG_SAMPLE_ALL
     g, dh, _ = _one_step(wl, check_canvases=[0, 5], sc_rows=[(0, 3), (5, 200), (7, 255)], params=p)
     assert (g["converged"] == 0).all() and np.isfinite(dh).all()
+    drawn = g["sample"] >= 0
+    assert drawn.all() if sample_all else np.array_equal(drawn, g["accept"] == 1)
 
 
 def test_ragged_full_size():

@@ -48,17 +48,24 @@ def _check_case(x, p, seed, V, canvas0=None, prev0=None, stable0=None):
     return g, o, rep
 
 
+@pytest.mark.parametrize("sample_all", [False, True])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("V,ld", [(5003, 5008), (1024, 1024), (40000, 40000), (70001, 70008)])
-def test_step_small_ragged(dtype, V, ld):
+def test_step_small_ragged(dtype, V, ld, sample_all):
+    """Canvases 0 and 3 draw their samples in opposite ways (every position / accepted
+    positions only, after the acceptance); canvas 1 is read-only, canvas 2 inactive."""
     rng = np.random.default_rng(V + (dtype == "fp32"))
-    n, L = 3, 200
+    n, L = 4, 200
     x = synth.logits(n, L, V, seed=V, step=1, scale=(0.5, 12.0), spike_frac=0.1, dtype=dtype, ld=ld)
     p = _params(n, rng)
     p["flags"][1] = dg.DG_ACTIVE | dg.DG_READ_ONLY
     p["max_steps"][1] = 1
     p["flags"][2] = 0
-    _check_case(x, p, 0xDEADBEEF12345, V, canvas0=rng.integers(0, V, (n, L)).astype(np.int32))
+    p["flags"][0 if sample_all else 3] |= dg.DG_SAMPLE_ALL
+    g, o, _ = _check_case(x, p, 0xDEADBEEF12345, V, canvas0=rng.integers(0, V, (n, L)).astype(np.int32))
+    deferred = 3 if sample_all else 0
+    assert (g["sample"][deferred][g["accept"][deferred] == 0] == -1).all()
+    assert g["accept"][deferred].any()
 
 
 def test_step_convergence_sequence():
@@ -184,7 +191,7 @@ def test_nan_and_empty_rows_set_status():
     x[0, 2, :] = float("-inf")
     x[0, 3, 7] = float("inf")
     x[0, 4, 10:20] = float("-inf")      # some -inf entries are fine
-    p = _params(n, np.random.default_rng(9), temperature=1.0)
+    p = _params(n, np.random.default_rng(9), temperature=1.0, flags=dg.DG_ACTIVE | dg.DG_SAMPLE_ALL)
     b = StepBuffers.make(n, L, DEV)
     dg.dg_clear_device_status()
     run_step(x.to(DEV), dg.params_tensor(p, DEV), 1, b)

@@ -293,13 +293,16 @@ def run_ours(args):
     ent, lse, conv = z((n, L), torch.float32), z((n, L), torch.float32), z((n,), torch.uint8)
     delta = torch.empty((n, L, d), dtype=torch.bfloat16, device=dev)
     wsp = torch.empty(dg.dg_self_cond_workspace_bytes(n, L, d, h), dtype=torch.uint8, device=dev)
+    dws = torch.empty(dg.dg_denoise_workspace_bytes(n, L, V, dg.DG_BF16 if wl.dtype == "bf16" else dg.DG_FP32),
+                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     seed = 0x5EED0000 + rank
 
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        dg.dg_denoise_step(x, params, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv, stream=stream)
+        dg.dg_denoise_step(x, params, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv, workspace=dws,
+                           stream=stream)
         dg.dg_self_cond_prepare(params, conv, n, L, d, h, delta, wsp, stream=stream)
         if ev:
             ev[1].record(stream)
@@ -389,7 +392,7 @@ def run_ours(args):
             b = k % 2
             stream.wait_event(h2d_done[b])
             dg.dg_denoise_step(xdev[b], params, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv,
-                               stream=stream)
+                               workspace=dws, stream=stream)
             dg.dg_self_cond_logits(xdev[b], lse, params, conv, E, Wg, Wu, Wd, delta, wsp, stream=stream)
             buf_free[b].record(stream)
             out_canvas.copy_(canvas, non_blocking=True)
@@ -458,7 +461,7 @@ def run_ours(args):
 
         def _denoise(prm):
             return lambda: dg.dg_denoise_step(x, prm, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv,
-                                              stream=stream)
+                                              workspace=dws, stream=stream)
 
         around = {
             "denoise_step": {"ms": _time(_denoise(params), reps=20),

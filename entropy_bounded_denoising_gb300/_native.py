@@ -175,7 +175,10 @@ def dg_denoise_step(logits, params, seed, canvas, prev_argmax, stable_count, acc
     L = Lx if L is None else L
     ld = ldx if ld is None else ld
     V = ld if V is None else V
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if workspace is None:  # the caller gave none: one sized by the library, on the logits' device
+        workspace = torch.empty(dg_denoise_workspace_bytes(n_canvas, L, V, _dtype_code(logits)),
+                                dtype=torch.uint8, device=logits.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
     rc = load().dg_denoise_step(_p(logits), _dtype_code(logits), ld, n_canvas, L, V, _p(params),
                                 int(seed) & 0xFFFFFFFFFFFFFFFF, _p(canvas), _p(prev_argmax),
                                 _p(stable_count), _p(accept_mask), _p(argmax), _p(sample), _p(entropy),

@@ -23,14 +23,17 @@
 // worth at a time, with the Philox rounds that do not depend on the entry index computed
 // once per row.
 // A sample is kept only at an accepted position (a rejected one is renoised in the same
-// step), so canvases without DG_SAMPLE_ALL skip the search in the statistics pass; after the
-// acceptance the same kernel runs again in its deferred mode over the accepted rows only,
-// with the row maximum already known (no statistics, no pass 1).
+// step), so canvases without DG_SAMPLE_ALL skip the search in the statistics pass; the
+// acceptance kernel lists their accepted rows (with each row's maximum, recorded by the
+// statistics pass), and a third kernel searches those rows in 16 KB chunks, one warp per
+// chunk, reading global memory directly: few rows are left, so the work is cut finer than a
+// row to keep every SM busy.
 // The reduction order depends only on V, so a row's result does not depend on its batch.
 #include <cuda_runtime.h>
 
 #include <math.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "dg_common.cuh"
@@ -40,6 +43,9 @@ namespace {
 constexpr int kK1Warps = 8;                        // consumer warps
 constexpr int kK1Threads = (kK1Warps + 1) * 32;    // + one producer warp
 constexpr int kSlots = 4;                          // ring of shared-memory slots
+constexpr uint32_t kChunkBytes = 16384;            // deferred sampling: bytes of a row per warp item
+constexpr int kDWarps = 8;                         // deferred sampling: warps per CTA
+constexpr int kDBatch = 4;                         // 16-byte loads in flight per lane
 constexpr uint32_t kPieceBytes = 16384;            // bytes per slot
 constexpr int kVecPerLane = (int)(kPieceBytes / 16) / (kK1Warps * 32);  // 16-byte vectors per lane per piece
 constexpr int kDrawPerLane = 1;                    // queued groups drawn per lane per round
@@ -68,6 +74,16 @@ struct RowState {  // online softmax state of a set of entries, z measured in lo
     float r;       // sum of 2^d over the other entries, d = (x - m) * log2e / T
     float t;       // sum of 2^d * d
     int idx;       // smallest index attaining m
+};
+
+// The deferred-sampling workspace (caller memory, carved by dg_denoise_step): the list of
+// accepted rows of canvases without DG_SAMPLE_ALL, filled by the acceptance kernel.
+struct DeferredWs {
+    int32_t* count;  // entries listed
+    int2* entry;     // [n * L]: (row, bits of the row's largest raw logit)
+    unsigned long long* key;  // [n * L]: best (score, entry) of the row so far, see score_key
+    int32_t* done;   // [n * L]: chunks of the row searched so far
+    float* row_max;  // [n * L] by row: written by the statistics pass
 };
 
 template <int DT>
@@ -344,12 +360,14 @@ DG_DEVINL void draw_queued(const int* q_e0, const uint32_t (*q_x)[QW], int qh, i
 // (2) the exponential sums against the warp's running max, which only grows between
 // pieces (a warp-uniform branch), so lanes do not diverge on new maxima.
 // ------------------------------------------------------------------------------------
-template <int DT, bool kDeferred>
+// ws (may be null): the deferred-sampling workspace; its list count is cleared here (before
+// any CTA returns) and each row's largest raw logit recorded (NaN for a NaN / inf / empty row).
+template <int DT>
 __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
     const unsigned char* __restrict__ logits, int64_t ld_bytes, int64_t V, int32_t L,
     const dg_canvas_params* __restrict__ params, uint64_t seed, int32_t* __restrict__ argmax_out,
     int32_t* __restrict__ sample_out, float* __restrict__ entropy_out, float* __restrict__ lse_out,
-    const uint8_t* __restrict__ accept_mask, int32_t* __restrict__ canvas_out, unsigned* status) {
+    DeferredWs ws, unsigned* status) {
     constexpr int VN = Vec<DT>::N;
     constexpr int ES = DT == 0 ? 2 : 4;
     constexpr int GPV = VN / 4;                    // Philox blocks per 16-byte vector
@@ -364,35 +382,16 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
     const int64_t canvas = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+    if (ws.count && pos == 0 && canvas == 0 && tid == 0) *ws.count = 0;
     const dg_canvas_params p = params[canvas];
     if (!(p.flags & DG_ACTIVE)) return;
+    if (!(p.temperature > 0.f) || !isfinite(p.temperature)) {
+        if (tid == 0 && pos == 0) dg::raise_status(status, DG_DEV_BAD_PARAM);
+        return;
+    }
     const int64_t row = canvas * L + pos;
     const unsigned char* src = logits + row * ld_bytes;
-    float m_known = -INFINITY;  // deferred mode: the row's largest raw logit
-    if constexpr (kDeferred) {
-        // only accepted positions of canvases that did not sample in the statistics pass
-        // (parameters the acceptance kernel rejected leave accept_mask unwritten)
-        if ((p.flags & (DG_READ_ONLY | DG_SAMPLE_ALL)) || !dg::canvas_params_ok(p, L)) return;
-        if (!accept_mask[row]) return;
-        const int32_t a = argmax_out[row];
-        const float l = lse_out[row];
-        if (a >= 0 && a < V)
-            m_known = DT == 0 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(src)[a] << 16)
-                              : reinterpret_cast<const float*>(src)[a];
-        if (!(isfinite(m_known) && isfinite(l))) {  // a NaN / inf / empty row: flagged by the statistics pass
-            if (tid == 0) {
-                sample_out[row] = -1;
-                canvas_out[row] = -1;
-            }
-            return;
-        }
-    } else {
-        if (!(p.temperature > 0.f) || !isfinite(p.temperature)) {
-            if (tid == 0 && pos == 0) dg::raise_status(status, DG_DEV_BAD_PARAM);
-            return;
-        }
-    }
-    const bool do_sample = kDeferred || ((p.flags & DG_SAMPLE_ALL) && !(p.flags & DG_READ_ONLY));
+    const bool do_sample = (p.flags & DG_SAMPLE_ALL) && !(p.flags & DG_READ_ONLY);
     const float invT = 1.0f / p.temperature;
     const float k2 = kLog2e * invT;
     const uint32_t bytes = (uint32_t)(V * ES);
@@ -436,7 +435,7 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
         }
     } else {
         // ---------------- consumers
-        RowState st{m_known, 0.f, 0.f, 0.f, 0x7fffffff};
+        RowState st{-INFINITY, 0.f, 0.f, 0.f, 0x7fffffff};
         bool bad = false;
         float best = -INFINITY;    // this lane's best score and its entry
         int bidx = 0x7fffffff;
@@ -464,13 +463,12 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
             auto piece = [&](auto full_tag, auto sample_tag) {
                 constexpr bool FULL = decltype(full_tag)::value;
                 constexpr bool SAMPLE = decltype(sample_tag)::value;
-                constexpr bool STATS = !kDeferred;
                 // ---- pass 1: vector maxima, then the warp's max; a larger one rescales every
                 // lane's state (warp-uniform, so lanes never diverge on a new maximum)
                 uint32_t lm2 = kBf16NegInf2;  // lane max as a bf16 pair (max of even, odd entries)
                 float lane_max = -INFINITY;
 #pragma unroll
-                for (int v = 0; v < (STATS ? kVecPerLane : 0); ++v) {
+                for (int v = 0; v < kVecPerLane; ++v) {
                     const int j = (v * kK1Warps + warp) * 32 + lane;
                     const uint4 w = load_raw<DT, FULL>(slot, j, nvec, n_el);
                     if constexpr (DT == 0) {
@@ -484,11 +482,8 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
                 if (DT == 0) lane_max = max_nan(bf_lo(lm2), bf_hi(lm2));
                 float wmax = lane_max;
 #pragma unroll
-                for (int o = 16; o >= 1; o >>= 1)
-                    if (STATS) wmax = max_nan(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
-                if (!STATS) {
-                    // the row maximum is known: nothing to rescale
-                } else if (wmax != wmax) {
+                for (int o = 16; o >= 1; o >>= 1) wmax = max_nan(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+                if (wmax != wmax) {
                     bad = true;
                 } else if (wmax > st.m) {
                     if (st.m > -INFINITY) {
@@ -531,7 +526,7 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
                         cand[0] = SAMPLE && in && vmax >= x_thr;
                         tie = vmax == st.m;
                     }
-                    if (STATS && in) {
+                    if (in) {
                         float x[VN];
                         if (tie) {
                             // the vector holds the max: count its copies, the rest as usual
@@ -609,7 +604,7 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
 #pragma unroll
                     for (int v = 0; v < kVecPerLane; ++v) vec2(v);
                 }
-                if (DT == 0 && STATS) {
+                if (DT == 0) {
                     st.r += (f2_lo(racc[0]) + f2_hi(racc[0])) + (f2_lo(racc[1]) + f2_hi(racc[1]));
                     st.t += (f2_lo(tacc[0]) + f2_hi(tacc[0])) + (f2_lo(tacc[1]) + f2_hi(tacc[1]));
                 }
@@ -636,10 +631,8 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
         if (do_sample && qn > 0) draw_queued<DT, QW>(q_e0, q_x, qh, qn, lane, V, invT, pre, bound, best, bidx);
         __syncwarp();
         if (bad) sh.bad = 1;
-        if constexpr (!kDeferred) {
 #pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) st = merge(st, shfl_state(st, o), k2);
-        }
+        for (int o = 16; o >= 1; o >>= 1) st = merge(st, shfl_state(st, o), k2);
         warp_best(best, bidx);
         if (lane == 0) {
             sh.warp_state[warp] = st;
@@ -657,12 +650,7 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
             bi = sh.warp_bidx[lane];
         }
         warp_best(b, bi);
-        if (kDeferred && lane == 0) {
-            // the kept sample becomes the position's next token
-            sample_out[row] = bi;
-            canvas_out[row] = bi;
-            if (sh.timeout) dg::raise_status(status, DG_DEV_TIMEOUT);
-        } else if (lane == 0) {
+        if (lane == 0) {
             RowState rs = sh.warp_state[0];
             for (int w = 1; w < kK1Warps; ++w) rs = merge(rs, sh.warp_state[w], k2);
             const bool empty = rs.m == -INFINITY;
@@ -675,10 +663,143 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
             lse_out[row] = rs.m * invT + lns;
             argmax_out[row] = empty ? 0 : rs.idx;
             sample_out[row] = (do_sample && !empty && !row_bad) ? bi : -1;
+            if (ws.row_max) ws.row_max[row] = (empty || row_bad) ? __int_as_float(0x7fc00000) : rs.m;
             if (row_bad) dg::raise_status(status, DG_DEV_NAN_INF_ROW);
             if (empty) dg::raise_status(status, DG_DEV_EMPTY_ROW);
             if (sh.timeout) dg::raise_status(status, DG_DEV_TIMEOUT);
         }
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// Deferred sampling: the Gumbel-max samples of the listed accepted rows.  Work items are
+// (list entry, 16 KB chunk of its row), taken one per warp in a grid-stride loop; a lane
+// loads kDBatch 16-byte vectors at a time straight from global memory and draws the noise
+// only for 4-entry groups whose largest y + G_max reaches the bound m / T - kGumbelLow (m
+// the row's largest logit) or the warp's best so far.  A chunk's winner joins the row's
+// 64-bit key by atomicMax (order-independent, so the result is deterministic); the warp that
+// completes the row's last chunk writes its sample and token.
+// ------------------------------------------------------------------------------------
+// Order-preserving key of (score, entry): larger score first, then the smaller entry.
+DG_DEVINL unsigned long long score_key(float score, int idx) {
+    return ((unsigned long long)float_key(score) << 32) | (unsigned long long)(0xffffffffu - (uint32_t)idx);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kDWarps * 32, 3) k1_sample_listed(
+    const unsigned char* __restrict__ logits, int64_t ld_bytes, int64_t V, int32_t L,
+    const dg_canvas_params* __restrict__ params, uint64_t seed, DeferredWs ws, int32_t* __restrict__ sample_out,
+    int32_t* __restrict__ canvas_out) {
+    constexpr int VN = Vec<DT>::N;
+    constexpr int ES = DT == 0 ? 2 : 4;
+    constexpr int GPV = VN / 4;
+    constexpr int kChunkElems = (int)(kChunkBytes / ES);
+    constexpr int kChunkVecs = (int)(kChunkBytes / 16);
+    static_assert(kChunkVecs % (32 * kDBatch) == 0, "a chunk splits into whole batches");
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * kDWarps + (threadIdx.x >> 5);
+    const int64_t nw = (int64_t)gridDim.x * kDWarps;
+    const int count = *ws.count;
+    const int cpr = (int)((V * ES + kChunkBytes - 1) / kChunkBytes);  // chunks per row
+    const int64_t items = (int64_t)count * cpr;
+    for (int64_t it = gw; it < items; it += nw) {
+        const int w = (int)(it / cpr);
+        const int chunk = (int)(it - (int64_t)w * cpr);
+        const int2 e = ws.entry[w];
+        const int64_t row = e.x;
+        const float m = __int_as_float(e.y);
+        const int64_t canvas = row / L;
+        const dg_canvas_params p = params[canvas];
+        const bool ok = isfinite(m);  // else a NaN / inf / empty row (flagged by the statistics pass)
+        float best = -INFINITY;
+        int bidx = 0x7fffffff;
+        if (ok) {
+            const int pos = (int)(row - canvas * L);
+            const float invT = 1.0f / p.temperature;
+            const float ym = m * invT;
+            const float bound = ym - kGumbelLow - fabsf(ym) * 2.4e-7f;
+            const dg::PhiloxPre pre = dg::philox_pre((uint32_t)pos, (uint32_t)p.step,
+                                                     dg::ctr_word3(seed, dg::kStreamGumbel), (uint32_t)seed,
+                                                     p.request_id);
+            const uint4* src = reinterpret_cast<const uint4*>(logits + row * ld_bytes + (int64_t)chunk * kChunkBytes);
+            const int e_lo = chunk * kChunkElems;
+            const int n_el = (int)min((int64_t)kChunkElems, V - e_lo);
+            const int nvec = (n_el + VN - 1) / VN;
+            float x_thr = (bound - kGumbelMax - kCandidateSlack) * p.temperature;
+            uint32_t thr2 = DT == 0 ? bf16_floor2(x_thr) : 0u;
+            // two register batches: the next one is loading while this one is tested
+            uint4 cur[kDBatch], nxt[kDBatch];
+            auto load = [&](uint4 (&buf)[kDBatch], int b0) {
+#pragma unroll
+                for (int k = 0; k < kDBatch; ++k) {
+                    const int j = b0 + k * 32 + lane;
+                    buf[k] = j < nvec ? __ldcs(src + j) : make_uint4(0, 0, 0, 0);
+                }
+            };
+            load(cur, 0);
+#pragma unroll 1
+            for (int b0 = 0; b0 < nvec; b0 += 32 * kDBatch) {
+                if (b0 + 32 * kDBatch < nvec) load(nxt, b0 + 32 * kDBatch);
+                const float best0 = best;
+#pragma unroll
+                for (int k = 0; k < kDBatch; ++k) {
+                    const int j = b0 + k * 32 + lane;
+                    if (j >= nvec) continue;
+                    const uint4 v = cur[k];
+                    const int valid = n_el - j * VN;  // entries of this vector inside the row
+                    bool cand[GPV];
+                    if (DT == 0 && valid >= VN) {
+                        // whole vector: packed test of each 4-entry group's max
+                        cand[0] = bge2_any(bmax2(v.x, v.y), thr2);
+                        cand[GPV - 1] = bge2_any(bmax2(v.z, v.w), thr2);
+                    } else {
+                        float x[VN];
+                        unpack<DT>(v, x);
+#pragma unroll
+                        for (int i = 0; i < VN; ++i)
+                            if (i >= valid) x[i] = -INFINITY;
+#pragma unroll
+                        for (int g = 0; g < GPV; ++g)
+                            cand[g] = fmaxf(fmaxf(x[4 * g], x[4 * g + 1]), fmaxf(x[4 * g + 2], x[4 * g + 3])) >= x_thr;
+                    }
+#pragma unroll
+                    for (int g = 0; g < GPV; ++g) {
+                        if (!cand[g]) continue;  // rare: a candidate group is drawn where found
+                        float x[VN];
+                        unpack<DT>(v, x);
+#pragma unroll
+                        for (int i = 0; i < VN; ++i)
+                            if (i >= valid) x[i] = -INFINITY;
+                        const int e0 = e_lo + (j * GPV + g) * 4;
+                        const float xg[4] = {x[4 * g], x[4 * g + 1], x[4 * g + 2], x[4 * g + 3]};
+                        const dg::u4 r = dg::philox10_c0((uint32_t)e0 >> 2, pre);
+                        eval_words(xg, e0, r, V, invT, bound, best, bidx);
+                    }
+                }
+                // a lane's new best tightens every lane's threshold for the next batch
+                if (__any_sync(0xffffffffu, best != best0)) {
+                    warp_best(best, bidx);
+                    x_thr = (fmaxf(bound, best) - kGumbelMax - kCandidateSlack) * p.temperature;
+                    thr2 = DT == 0 ? bf16_floor2(x_thr) : 0u;
+                }
+#pragma unroll
+                for (int k = 0; k < kDBatch; ++k) cur[k] = nxt[k];
+            }
+            warp_best(best, bidx);
+        }
+        if (lane == 0) {
+            if (ok && best > -INFINITY) atomicMax(ws.key + w, score_key(best, bidx));
+            __threadfence();
+            if (atomicAdd(ws.done + w, 1) == cpr - 1) {
+                // every chunk of the row is in: its winner is the position's sample and token
+                __threadfence();
+                const unsigned long long k = atomicMax(ws.key + w, 0ull);
+                const int32_t tok = (ok && k != 0ull) ? (int32_t)(0xffffffffu - (uint32_t)(k & 0xffffffffull)) : -1;
+                sample_out[row] = tok;
+                canvas_out[row] = tok;
+            }
+        }
+        __syncwarp();
     }
 }
 
@@ -690,11 +811,12 @@ __global__ void __launch_bounds__(1024) k2_accept(
     int32_t L, int64_t V, const dg_canvas_params* __restrict__ params, uint64_t seed, int32_t* __restrict__ canvas,
     int32_t* __restrict__ prev_argmax, int32_t* __restrict__ stable_count, uint8_t* __restrict__ accept_mask,
     uint8_t* __restrict__ converged, float* __restrict__ mean_entropy, int32_t* __restrict__ n_accept,
-    bool allow_deferred, unsigned* status) {
+    DeferredWs ws, unsigned* status) {
     __shared__ float sH[1024];
     __shared__ double sSorted[1024];
     __shared__ double sWarp[32];
     __shared__ int sCut;
+    __shared__ int sBase;
 
     const int64_t c = blockIdx.x;
     const int i = threadIdx.x, lane = i & 31, warp = i >> 5, nwarps = blockDim.x >> 5;
@@ -705,9 +827,10 @@ __global__ void __launch_bounds__(1024) k2_accept(
         return;
     }
     const bool read_only = (p.flags & DG_READ_ONLY) != 0;
-    // accepted positions of a deferred canvas get their sample (and token) from the
-    // deferred sampling pass that follows
-    const bool deferred = allow_deferred && !(p.flags & DG_SAMPLE_ALL);
+    // ws.count null (the acceptance hook): no deferred sampling.  Else accepted positions of
+    // a canvas without DG_SAMPLE_ALL are listed for the deferred sampling pass, which writes
+    // their sample and token
+    const bool deferred = ws.count && !(p.flags & DG_SAMPLE_ALL);
     const bool valid = i < L;
     const int64_t q = c * L + i;
     const float H = valid ? entropy[q] : 0.f;
@@ -756,9 +879,16 @@ __global__ void __launch_bounds__(1024) k2_accept(
     nacc = min(nacc, L);
     if (read_only) nacc = 0;
 
+    if (i == 0 && deferred && nacc > 0) sBase = atomicAdd(ws.count, nacc);
     const bool same = __syncthreads_and(!valid || am == prev_argmax[q]) != 0;
     if (valid) {
         const bool acc = rk < nacc;
+        if (deferred && acc) {  // accepted ranks are 0..nacc-1
+            const int at = sBase + rk;
+            ws.entry[at] = make_int2((int)q, __float_as_int(ws.row_max[q]));
+            ws.key[at] = 0ull;
+            ws.done[at] = 0;
+        }
         accept_mask[q] = acc ? 1 : 0;
         if (!read_only) {
             if (!acc)
@@ -830,21 +960,40 @@ bool k1_supported(dg_dtype dt, int64_t V) {
 template <int DT>
 size_t k1_smem_bytes() { return ((sizeof(K1Shared<DT>) + 127) / 128) * 128 + (size_t)kSlots * kPieceBytes; }
 
-// kDeferred = false: statistics of every active row (+ samples of DG_SAMPLE_ALL canvases);
-// kDeferred = true: samples and tokens of the accepted positions of the other canvases.
-template <int DT, bool kDeferred>
+// Statistics of every active row (+ samples of DG_SAMPLE_ALL canvases); clears the list.
+template <int DT>
 dg_status launch_k1(const void* logits, int64_t ld, int64_t n, int32_t L, int64_t V,
                     const dg_canvas_params* params, uint64_t seed, int32_t* argmax, int32_t* sample, float* entropy,
-                    float* lse, const uint8_t* accept_mask, int32_t* canvas, cudaStream_t stream) {
-    auto kern = k1_row_stats<DT, kDeferred>;
+                    float* lse, const DeferredWs& ws, cudaStream_t stream) {
+    auto kern = k1_row_stats<DT>;
     const size_t smem = k1_smem_bytes<DT>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DG_ERR_CUDA;
     const int64_t ld_bytes = ld * (DT == 0 ? 2 : 4);
     kern<<<dim3((unsigned)L, (unsigned)n, 1), kK1Threads, smem, stream>>>(static_cast<const unsigned char*>(logits),
                                                                           ld_bytes, V, L, params, seed, argmax,
-                                                                          sample, entropy, lse, accept_mask, canvas,
+                                                                          sample, entropy, lse, ws,
                                                                           dghost::status_word());
+    dghost::count_launch();
+    return dghost::cuda_status(cudaGetLastError());
+}
+
+// Samples and tokens of the listed accepted rows: three CTAs of kDWarps warps per SM, one warp
+// per 16 KB chunk (the list length is only known on the device).
+template <int DT>
+dg_status launch_kd(const void* logits, int64_t ld, int64_t n, int32_t L, int64_t V,
+                    const dg_canvas_params* params, uint64_t seed, const DeferredWs& ws, int32_t* sample,
+                    int32_t* canvas, cudaStream_t stream) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return DG_ERR_CUDA;
+    const int64_t cpr = (V * (DT == 0 ? 2 : 4) + kChunkBytes - 1) / kChunkBytes;
+    const int64_t max_items = n * (int64_t)L * cpr;
+    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(3LL * sms, (max_items + kDWarps - 1) / kDWarps));
+    const int64_t ld_bytes = ld * (DT == 0 ? 2 : 4);
+    k1_sample_listed<DT><<<grid, kDWarps * 32, 0, stream>>>(static_cast<const unsigned char*>(logits), ld_bytes, V, L,
+                                                           params, seed, ws, sample, canvas);
     dghost::count_launch();
     return dghost::cuda_status(cudaGetLastError());
 }
@@ -852,28 +1001,44 @@ dg_status launch_k1(const void* logits, int64_t ld, int64_t n, int32_t L, int64_
 dg_status launch_k2(const float* entropy, const int32_t* sample, const int32_t* argmax, int64_t n, int32_t L,
                     int64_t V, const dg_canvas_params* params, uint64_t seed, int32_t* canvas, int32_t* prev_argmax,
                     int32_t* stable_count, uint8_t* accept_mask, uint8_t* converged, float* mean_entropy,
-                    int32_t* n_accept, bool allow_deferred, cudaStream_t stream) {
+                    int32_t* n_accept, const DeferredWs& ws, cudaStream_t stream) {
     const unsigned threads = (unsigned)((L + 31) / 32 * 32);
     k2_accept<<<(unsigned)n, threads, 0, stream>>>(entropy, sample, argmax, L, V, params, seed, canvas, prev_argmax,
                                                    stable_count, accept_mask, converged, mean_entropy, n_accept,
-                                                   allow_deferred, dghost::status_word());
+                                                   ws, dghost::status_word());
     dghost::count_launch();
     return dghost::cuda_status(cudaGetLastError());
+}
+
+// The deferred-sampling workspace: a count (padded to 256 bytes), then per listed row an
+// entry (8 bytes), a key (8) and a chunk counter (4), and per row its maximum (4).
+size_t denoise_ws_bytes(int64_t rows) { return (size_t)256 + (size_t)rows * 24; }
+
+DeferredWs carve_ws(void* workspace, int64_t rows) {
+    unsigned char* b = static_cast<unsigned char*>(workspace);
+    DeferredWs ws;
+    ws.count = reinterpret_cast<int32_t*>(b);
+    ws.entry = reinterpret_cast<int2*>(b + 256);
+    ws.key = reinterpret_cast<unsigned long long*>(b + 256 + 8 * rows);
+    ws.done = reinterpret_cast<int32_t*>(b + 256 + 16 * rows);
+    ws.row_max = reinterpret_cast<float*>(b + 256 + 20 * rows);
+    return ws;
 }
 
 }  // namespace
 
 extern "C" {
 
-size_t dg_denoise_workspace_bytes(int64_t, int32_t, int64_t, dg_dtype) { return 0; }
+size_t dg_denoise_workspace_bytes(int64_t n_canvas, int32_t L, int64_t, dg_dtype) {
+    if (n_canvas < 0 || L < 0) return 0;
+    return (denoise_ws_bytes(n_canvas * (int64_t)L) + 255) / 256 * 256;
+}
 
 dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L, int64_t V,
                           const dg_canvas_params* params, uint64_t seed, int32_t* canvas, int32_t* prev_argmax,
                           int32_t* stable_count, uint8_t* accept_mask, int32_t* argmax, int32_t* sample,
                           float* entropy, float* lse, uint8_t* converged, float* mean_entropy, int32_t* n_accept,
                           void* workspace, size_t workspace_bytes, dg_stream_t stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     if (dtype != DG_BF16 && dtype != DG_FP32) return DG_ERR_INVALID_ARG;
     dg_status s = check_canvas_dims(n_canvas, L, V);
     if (s != DG_OK) return s;
@@ -885,20 +1050,18 @@ dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld, int64_
     const int64_t es = dtype == DG_BF16 ? 2 : 4;
     if (!aligned16(logits) || (ld * es) % 16 != 0) return DG_ERR_ALIGNMENT;
     if (!k1_supported(dtype, V)) return DG_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < dg_denoise_workspace_bytes(n_canvas, L, V, dtype)) return DG_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 7u) != 0) return DG_ERR_ALIGNMENT;
+    const DeferredWs ws = carve_ws(workspace, n_canvas * (int64_t)L);
     cudaStream_t st = (cudaStream_t)stream;
-    s = dtype == DG_BF16
-            ? launch_k1<0, false>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, nullptr,
-                                  nullptr, st)
-            : launch_k1<1, false>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, nullptr,
-                                  nullptr, st);
+    s = dtype == DG_BF16 ? launch_k1<0>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, ws, st)
+                         : launch_k1<1>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, ws, st);
     if (s != DG_OK) return s;
     s = launch_k2(entropy, sample, argmax, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
-                  accept_mask, converged, mean_entropy, n_accept, true, st);
+                  accept_mask, converged, mean_entropy, n_accept, ws, st);
     if (s != DG_OK) return s;
-    return dtype == DG_BF16 ? launch_k1<0, true>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy,
-                                                 lse, accept_mask, canvas, st)
-                            : launch_k1<1, true>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy,
-                                                 lse, accept_mask, canvas, st);
+    return dtype == DG_BF16 ? launch_kd<0>(logits, ld, n_canvas, L, V, params, seed, ws, sample, canvas, st)
+                            : launch_kd<1>(logits, ld, n_canvas, L, V, params, seed, ws, sample, canvas, st);
 }
 
 dg_status dg_accept_from_entropy(const float* entropy, const int32_t* sample, const int32_t* argmax,
@@ -913,7 +1076,7 @@ dg_status dg_accept_from_entropy(const float* entropy, const int32_t* sample, co
         !converged)
         return DG_ERR_INVALID_ARG;
     return launch_k2(entropy, sample, argmax, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
-                     accept_mask, converged, mean_entropy, n_accept, false, (cudaStream_t)stream);
+                     accept_mask, converged, mean_entropy, n_accept, DeferredWs{}, (cudaStream_t)stream);
 }
 
 dg_status dg_canvas_init(int32_t* canvas, int64_t n_canvas, int32_t L, int64_t V, const dg_canvas_params* params,

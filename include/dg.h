@@ -111,7 +111,8 @@ typedef struct {
 /* Denoise step [DG "엔트로피 기반 디노이징", "DiffusionGemmaModelState와 DiffusionSampler"]. */
 /* ------------------------------------------------------------------------------------ */
 
-/* Workspace needed by dg_denoise_step (currently 0: all reductions stay on chip). */
+/* Workspace needed by dg_denoise_step: the list of accepted positions that the deferred
+ * sampling launch works through (256 bytes + 24 bytes per position, rounded up to 256). */
 DG_API size_t dg_denoise_workspace_bytes(int64_t n_canvas, int32_t L, int64_t V, dg_dtype dtype);
 
 /* One denoising step for n_canvas canvases of L positions over a vocabulary of V.
@@ -137,7 +138,9 @@ DG_API size_t dg_denoise_workspace_bytes(int64_t n_canvas, int32_t L, int64_t V,
  * canvas, accept mask and every other output are the same either way.  With DG_SAMPLE_ALL
  * set on a canvas, every position of it draws its sample in the statistics pass (sample
  * defined everywhere).  The launches are: statistics (+ samples of DG_SAMPLE_ALL canvases),
- * acceptance / renoise / convergence, then the samples of the accepted positions.
+ * acceptance / renoise / convergence (which lists the accepted positions of the other
+ * canvases in the workspace), then the samples of the listed positions (16 KB of a row per
+ * warp; results do not depend on which warp finishes first).
  *
  *   logits        (device) [n_canvas][L][ld] of dtype; 16-byte aligned; ld >= V and
  *                 ld * sizeof(dtype) a multiple of 16.  Columns V..ld-1 are never read.
@@ -152,11 +155,13 @@ DG_API size_t dg_denoise_workspace_bytes(int64_t n_canvas, int32_t L, int64_t V,
  *   converged     (device, out) [n_canvas] uint8.
  *   mean_entropy  (device, out, may be NULL) [n_canvas] float.
  *   n_accept      (device, out, may be NULL) [n_canvas] int32.
- *   workspace     may be NULL when dg_denoise_workspace_bytes() is 0.
+ *   workspace     (device) at least dg_denoise_workspace_bytes() bytes, 8-byte aligned;
+ *                 scratch owned by the call until the stream passes it (no initial
+ *                 contents needed); calls that overlap on the GPU need their own.
  * Limits: 1 <= L <= 1024, 2 <= V < 2^31, 0 <= n_canvas <= 65535 (0 launches nothing), and
  * V * sizeof(dtype) < 2^31 bytes (else DG_ERR_UNSUPPORTED).
  * Errors: DG_ERR_INVALID_ARG (null required pointer, sizes), DG_ERR_ALIGNMENT,
- * DG_ERR_UNSUPPORTED, DG_ERR_CUDA. */
+ * DG_ERR_WORKSPACE (workspace null or too small), DG_ERR_UNSUPPORTED, DG_ERR_CUDA. */
 DG_API dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld,
                           int64_t n_canvas, int32_t L, int64_t V,
                           const dg_canvas_params* params, uint64_t seed,

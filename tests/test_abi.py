@@ -47,9 +47,15 @@ def test_host_validation_without_gpu():
     assert lib.dg_denoise_step(16, 0, 12, 1, 16, 12, 16, 0, *([16] * 11), None, 0, None) == dg.DG_ERR_ALIGNMENT
     # a row that does not fit the on-chip plan
     assert lib.dg_denoise_step(16, 1, 1 << 29, 1, 16, 1 << 29, 16, 0, *([16] * 11), None, 0, None) == dg.DG_ERR_UNSUPPORTED
+    # the deferred-sampling list needs a workspace of 256 + 24 bytes per position, 256-byte
+    # granular and 8-byte aligned
+    assert lib.dg_denoise_step(16, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), None, 0, None) == dg.DG_ERR_WORKSPACE
+    assert lib.dg_denoise_step(16, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), 256, 640, None) == dg.DG_ERR_WORKSPACE
+    assert lib.dg_denoise_step(16, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), 260, 768, None) == dg.DG_ERR_ALIGNMENT
     # empty batch is a no-op
     assert lib.dg_denoise_step(None, 0, 8, 0, 16, 8, None, 0, *([None] * 11), None, 0, None) == dg.DG_OK
-    assert lib.dg_denoise_workspace_bytes(8, 256, 262144, 0) == 0
+    assert lib.dg_denoise_workspace_bytes(8, 256, 262144, 0) == 256 + 24 * 8 * 256
+    assert lib.dg_denoise_workspace_bytes(1, 16, 1024, 1) == 768
     # self-conditioning: sizes and alignment
     assert lib.dg_self_cond_logits(16, 0, 64, 16, 16, None, 1, 16, 64, 12, 128, 16, 16, 16, 16, 16, 16, 1 << 30, None) == dg.DG_ERR_INVALID_ARG
     assert lib.dg_self_cond_logits(16, 0, 64, 16, 16, None, 1, 16, 64, 64, 128, 18, 16, 16, 16, 16, 16, 1 << 30, None) == dg.DG_ERR_ALIGNMENT

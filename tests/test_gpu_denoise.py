@@ -204,3 +204,18 @@ def test_nan_and_empty_rows_set_status():
     assert int(b.argmax[0, 4]) == o["argmax"] and int(b.sample[0, 4]) == o["sample"]
     assert abs(float(b.entropy[0, 4]) - o["entropy"]) <= 1e-5 * o["entropy"]
     assert dg.dg_get_device_status() == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_deferred_sampling_every_position_accepted(dtype):
+    """A budget that accepts every position: the deferred sampling launch draws every row
+    (about ten rows per CTA, flat rows included) and matches the oracle's samples at all of
+    them; one canvas samples in the statistics pass instead (DG_SAMPLE_ALL)."""
+    rng = np.random.default_rng(12)
+    n, L, V = 6, 256, 40000
+    x = synth.logits(n, L, V, seed=12, step=0, scale=(0.5, 12.0), spike_frac=0.1, dtype=dtype)
+    p = _params(n, rng, beta=1e9)
+    p["flags"][4] |= dg.DG_SAMPLE_ALL
+    g, o, _ = _check_case(x, p, 77, V)
+    assert (g["accept"] == 1).all() and (g["sample"] >= 0).all()
+    assert (g["canvas"] == g["sample"]).all()

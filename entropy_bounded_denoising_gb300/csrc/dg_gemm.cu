@@ -89,6 +89,8 @@ struct Cfg {
     static constexpr uint32_t kTxBytes = (uint32_t)(kBTileBytes + (AM == A_SOFTMAX_FP32 ? kStageBytesFp32 : kATileBytes));
     static constexpr size_t kSmem = 1024 + (size_t)STAGES * kStageBytes + 1024;
     static_assert(!PAIR_ || (BMD == B_MNMAJOR ? BN_ == 512 : BN_ == 256), "pair mode: BN 512 (N-major B) or 256");
+    static_assert(STAGES_ <= 12, "stage barriers");
+    static_assert(kSmem <= 232448, "fits the opt-in shared memory of an SM");
 };
 
 // ------------------------------------------------------------------ descriptors
@@ -167,10 +169,12 @@ DG_DEVINL float gelu_tanh(float z) {
     return 0.5f * z * (1.f + tanhf(k * (z + 0.044715f * z * z * z)));
 }
 
+constexpr int kMaxStages = 12;
+
 struct __align__(8) GemmShared {
-    uint64_t full[8];
-    uint64_t xform[8];
-    uint64_t empty[8];
+    uint64_t full[kMaxStages];
+    uint64_t xform[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t accf[2];
     uint64_t acce[2];
     uint32_t tmem_base;
@@ -690,11 +694,18 @@ __global__ void k_zero_rows(const dg_canvas_params* __restrict__ params, const u
 }
 
 // ------------------------------------------------------------------ host side
-using PEbf16 = Cfg<A_SOFTMAX_BF16, B_MNMAJOR, 512, 32, 8, true>;
+// Pipeline depths (shared-memory stages) of the self-conditioning GEMMs.
+#ifndef DG_PE_STAGES
+#define DG_PE_STAGES 8
+#endif
+#ifndef DG_MLP_STAGES
+#define DG_MLP_STAGES 6
+#endif
+using PEbf16 = Cfg<A_SOFTMAX_BF16, B_MNMAJOR, 512, 32, DG_PE_STAGES, true>;
 using PEfp32 = Cfg<A_SOFTMAX_FP32, B_MNMAJOR, 512, 32, 5, true>;
 using PEprob = Cfg<A_TMA, B_MNMAJOR, 512, 32, 5>;
-using GateUp = Cfg<A_TMA, B_KMAJOR_GATEUP, 256, 64, 6, true>;
-using Down = Cfg<A_TMA, B_KMAJOR, 256, 64, 6, true>;
+using GateUp = Cfg<A_TMA, B_KMAJOR_GATEUP, 256, 64, DG_MLP_STAGES, true>;
+using Down = Cfg<A_TMA, B_KMAJOR, 256, 64, DG_MLP_STAGES, true>;
 using DownSingle = Cfg<A_TMA, B_KMAJOR, 256, 64, 4>;  // plain GEMMs (K-major B) on one CTA per tile
 
 constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }

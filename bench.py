@@ -182,10 +182,10 @@ def run_reference(args):
     """The oracle as it stands, on the host cores, as the comparison arm.
 
     One step = the oracle's denoise step on a slice of positions of canvas 0 plus, in every
-    m-th step, its self-conditioning on one position; m and the slice are set from the
-    warm-up timings so that the K timed steps take about two minutes.  The value is
-    positions/s with the per-position cost = (denoise time / positions) + (feedback time /
-    feedback rows) over the timed steps."""
+    m-th step, its self-conditioning on one position per host thread (the oracle runs rows
+    in parallel); m and the slice are set from the warm-up timings so that the K timed steps
+    take about two minutes.  The value is positions/s with the per-position cost =
+    (denoise time / positions) + (feedback time / feedback rows) over the timed steps."""
     ws, rank, _ = _dist()
     if rank != 0:
         return 0
@@ -208,9 +208,11 @@ def run_reference(args):
                             np.zeros(1, np.int32), n_threads=threads)
         return time.perf_counter() - t0
 
+    n_fb = min(wl.L, max(1, threads))  # feedback rows per call: one per host thread
+
     def feedback():
         t0 = time.perf_counter()
-        oracle.self_cond_rows(xh[:1], np.full(1, float(p["temperature"][0])), *wh, V=wl.V, n_threads=threads)
+        oracle.self_cond_rows(xh[:n_fb], np.full(n_fb, float(p["temperature"][0])), *wh, V=wl.V, n_threads=threads)
         return time.perf_counter() - t0
 
     # warm-up: unit costs
@@ -228,12 +230,12 @@ def run_reference(args):
         n_dn += rows
         if k % every == 0:
             t_sc += feedback()
-            n_sc += 1
+            n_sc += n_fb
     per_pos = t_dn / n_dn + t_sc / max(1, n_sc)
     value = 1.0 / per_pos
     sample = (f"per step: oracle denoise on {rows} positions of canvas 0 (V={wl.V}); oracle self-conditioning "
-              f"on one position every {every} step(s) ({n_sc} in total); per-position cost = denoise time / "
-              f"positions + feedback time / feedback rows")
+              f"on {n_fb} positions every {every} step(s) ({n_sc} rows in total); per-position cost = denoise "
+              f"time / positions + feedback time / feedback rows")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_pos * wl.n * wl.L * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",

@@ -46,6 +46,22 @@ def _peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest of the ranks' values (the slowest rank's time); x itself on one rank."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(positions_per_rank: int, world: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job positions/s: every rank's positions over the slowest rank's time."""
+    return positions_per_rank * world * steps / (elapsed_ms / 1e3)
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -348,12 +364,9 @@ def run_ours(args):
     n_sc_rows = int((sc_on & ~conv_h).sum()) * L
     n_read_rows = int(active.sum()) * L
     positions = n_read_rows
-    if ws > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
     ms_step = elapsed_ms / args.steps
-    value = positions * ws * args.steps / (elapsed_ms / 1e3)
+    value = job_throughput(positions, ws, args.steps, elapsed_ms)
 
     t_dn = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     t_pe = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
@@ -419,12 +432,8 @@ def run_ours(args):
         e2e_run(args.steps, s2, e2)
         torch.cuda.synchronize()
         barrier()
-        ms2 = s2.elapsed_time(e2)
-        if ws > 1:
-            t = torch.tensor([ms2], device=dev)
-            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-            ms2 = float(t.item())
-        e2e = {"value": positions * ws * args.steps / (ms2 / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        ms2 = max_over_ranks(s2.elapsed_time(e2), dev)
+        e2e = {"value": job_throughput(positions, ws, args.steps, ms2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ms2 / args.steps,
                "pipelining": "next step's H2D overlaps this step's compute (two device input buffers)"}
 

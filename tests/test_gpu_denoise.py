@@ -219,3 +219,19 @@ def test_deferred_sampling_every_position_accepted(dtype):
     g, o, _ = _check_case(x, p, 77, V)
     assert (g["accept"] == 1).all() and (g["sample"] >= 0).all()
     assert (g["canvas"] == g["sample"]).all()
+
+
+@pytest.mark.parametrize("sample_all", [False, True])
+@pytest.mark.parametrize("dtype,V,ld,L", [("bf16", 2, 8, 33), ("bf16", 7, 8, 1), ("bf16", 9, 16, 64),
+                                          ("fp32", 3, 4, 33), ("fp32", 5, 8, 1024), ("bf16", 8200, 8200, 1024)])
+def test_step_edge_sizes(dtype, V, ld, L, sample_all):
+    """The smallest vocabularies (one partial 16-byte vector per row, most of it padding that
+    holds +1000 and must never be read as data), a one-position canvas and the largest canvas
+    (L = 1024, one acceptance CTA of 1024 threads), in both sampling modes."""
+    rng = np.random.default_rng(V * 7 + L)
+    n = 2
+    x = synth.logits(n, L, V, seed=V + L, step=1, scale=(0.5, 12.0), spike_frac=0.1, dtype=dtype, ld=ld)
+    p = _params(n, rng)
+    if sample_all:
+        p["flags"] |= dg.DG_SAMPLE_ALL
+    _check_case(x, p, 0xE06E + V, V, canvas0=rng.integers(0, V, (n, L)).astype(np.int32))

@@ -7,6 +7,7 @@ then the gated MLP).  Default workload: 8 canvases x 256 positions, V = 262144, 
 h = 16384, bf16 logits (the batched full-vocabulary step).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload batched|sweep|ragged|single]
+    python bench.py --workload sweep --loop --warmup 1   # the whole loop to convergence
     python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
 
 Prints one JSON line (rank 0).  Under torchrun every rank runs an independent replica on its
@@ -535,6 +536,115 @@ def run_ours(args):
     return 0
 
 
+# --------------------------------------------------------------------------- full loop
+def run_loop(args):
+    """The denoising loop of a workload from the Prefill case to convergence: every step runs
+    dg_denoise_step, the feedback stages and dg_advance_params on the canvases still active
+    (converged canvases drop out).  Each step's logits are generated between steps, outside
+    the timed region; the value is positions/s over the timed library work (active positions
+    summed over the steps), with steps/s and the loop's roofline fraction beside it."""
+    import torch
+    import entropy_bounded_denoising_gb300 as dg
+    from entropy_bounded_denoising_gb300 import synth, build
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        build.build()
+    if ws > 1:
+        tdist.barrier()
+    dg.load()
+    wl = synth.WORKLOADS[args.workload]
+    n, L, V, d, h = wl.n, wl.L, wl.V, wl.d, wl.h
+    base = synth.canvas_params(wl, step=0)
+    base["flags"] = np.where(base["flags"] & dg.DG_ACTIVE, base["flags"] | dg.DG_SELF_COND, base["flags"]).astype(np.uint32)
+    E, Wg, Wu, Wd = synth.weights(V, d, h, seed=wl.seed, device=dev)
+    dt = dg.DG_BF16 if wl.dtype == "bf16" else dg.DG_FP32
+    z = lambda shape, t, v=0: torch.full(shape, v, dtype=t, device=dev)
+    canvas, prev, stable = z((n, L), torch.int32), z((n, L), torch.int32, -1), z((n,), torch.int32)
+    acc, am, smp = z((n, L), torch.uint8), z((n, L), torch.int32), z((n, L), torch.int32)
+    ent, lse, conv = z((n, L), torch.float32), z((n, L), torch.float32), z((n,), torch.uint8)
+    delta = torch.empty((n, L, d), dtype=torch.bfloat16, device=dev)
+    wsp = torch.empty(dg.dg_self_cond_workspace_bytes(n, L, d, h), dtype=torch.uint8, device=dev)
+    dws = torch.empty(dg.dg_denoise_workspace_bytes(n, L, V, dt), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    seed = 0x5EED0000 + rank
+    pk = _peaks()
+
+    def one_loop(timed):
+        params = dg.params_tensor(base, dev)
+        dg.dg_canvas_init(canvas, n, L, V, params, seed, stream=stream)
+        prev.fill_(-1)
+        stable.zero_()
+        total_ms, positions, steps, t_roof = 0.0, 0, 0, 0.0
+        for t in range(int(base["max_steps"].max())):
+            flags = dg.unpack_params(params)["flags"]
+            active = (flags & dg.DG_ACTIVE) != 0
+            if not active.any():
+                break
+            x = synth.logits(n, L, V, seed=wl.seed + 1000 * rank, step=t, scale=wl.scale,
+                             spike_frac=wl.spike_frac, dtype=wl.dtype, device=dev)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dg.dg_denoise_step(x, params, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv,
+                               workspace=dws, stream=stream)
+            dg.dg_self_cond_prepare(params, conv, n, L, d, h, delta, wsp, stream=stream)
+            dg.dg_self_cond_pe(x, lse, params, E, h, wsp, stream=stream)
+            dg.dg_self_cond_mlp(n, L, Wg, Wu, Wd, delta, wsp, stream=stream)
+            dg.dg_advance_params(params, conv, n, stream=stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            del x
+            if timed:
+                conv_h = conv.cpu().numpy().astype(bool)
+                rows = int(active.sum()) * L
+                sc_rows = int((active & ~conv_h).sum()) * L
+                ar = _workload_arith(wl, sc_rows, rows)
+                t_roof += max(ar["bytes"] / (pk["hbm_gbs"] * 1e9), ar["tc_flops"] / (pk["bf16_tflops_sustained"] * 1e12))
+                total_ms += a.elapsed_time(b)
+                positions += rows
+                steps += 1
+        return total_ms, positions, steps, t_roof
+
+    for _ in range(max(0, args.warmup)):
+        one_loop(False)   # whole warm-up loops (the first builds kernels' tensor maps and caches)
+    if dg.dg_get_device_status():
+        raise RuntimeError("device status set during the warm-up loop")
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        clk.mark("t_start")
+        launches0 = dg.dg_launch_count()
+        total_ms, positions, steps, t_roof = one_loop(True)
+        launches = dg.dg_launch_count() - launches0
+        clk.mark("t_end")
+    if dg.dg_get_device_status():
+        raise RuntimeError("device status set during the timed loop")
+    total_ms = max_over_ranks(total_ms, dev)
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": job_throughput(positions, ws, 1, total_ms), "unit": UNIT, "n_gpus": ws,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": total_ms / max(1, steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(_config(wl), mode="full loop from the Prefill case until every canvas converges or "
+                       "reaches its step cap; converged canvases drop out; logits generated between steps, "
+                       "outside the timed region"),
+        "steps_per_s": 1e3 * steps / total_ms, "positions": positions,
+        "loop_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof * 1e3 / total_ms},
+        "gpu_launches": launches, "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        tdist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -545,9 +655,13 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip timing the rows around the step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--loop", action="store_true",
+                    help="time the workload's whole denoising loop (e.g. --workload sweep) instead of repeated steps")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.loop:
+        return run_loop(args)
     return run_ours(args)
 
 

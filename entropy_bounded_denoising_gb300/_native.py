@@ -55,6 +55,8 @@ def load(path: str | None = None):
     sig = {
         "dg_denoise_workspace_bytes": (sz, [i64, i32, i64, ctypes.c_int]),
         "dg_denoise_step": (st, [P, ctypes.c_int, i64, i64, i32, i64, P, u64] + [P] * 11 + [P, sz, P]),
+        "dg_denoise_stats": (st, [P, ctypes.c_int, i64, i64, i32, i64, P, u64] + [P] * 11 + [P, sz, P]),
+        "dg_denoise_samples": (st, [P, ctypes.c_int, i64, i64, i32, i64, P, u64, P, P, P, sz, P]),
         "dg_accept_from_entropy": (st, [P, P, P, i64, i32, i64, P, u64] + [P] * 7 + [P]),
         "dg_canvas_init": (st, [P, i64, i32, i64, P, u64, P]),
         "dg_advance_params": (st, [P, P, i64, P]),
@@ -89,7 +91,8 @@ def load(path: str | None = None):
 
 def exported_symbols() -> list[str]:
     lib = load()
-    return [n for n in ("dg_denoise_workspace_bytes", "dg_denoise_step", "dg_accept_from_entropy",
+    return [n for n in ("dg_denoise_workspace_bytes", "dg_denoise_step", "dg_denoise_stats",
+                        "dg_denoise_samples", "dg_accept_from_entropy",
                         "dg_canvas_init", "dg_advance_params", "dg_self_cond_workspace_bytes",
                         "dg_self_cond_logits", "dg_self_cond_prepare", "dg_self_cond_pe",
                         "dg_self_cond_mlp", "dg_self_cond_probs_workspace_bytes",
@@ -166,26 +169,68 @@ def dg_denoise_workspace_bytes(n_canvas: int, L: int, V: int, dtype: int = DG_BF
     return int(load().dg_denoise_workspace_bytes(n_canvas, L, V, dtype))
 
 
-def dg_denoise_step(logits, params, seed, canvas, prev_argmax, stable_count, accept_mask, argmax,
-                    sample, entropy, lse, converged, mean_entropy=None, n_accept=None,
-                    workspace=None, *, n_canvas=None, L=None, V=None, ld=None, stream=None,
-                    check=True) -> int:
+def _denoise_dims(logits, n_canvas, L, V, ld):
     n, Lx, ldx = logits.shape if logits.dim() == 3 else (n_canvas, L, ld)
     n_canvas = n if n_canvas is None else n_canvas
     L = Lx if L is None else L
     ld = ldx if ld is None else ld
     V = ld if V is None else V
+    return n_canvas, L, V, ld
+
+
+def _denoise_ws(workspace, logits, n_canvas, L, V):
     if workspace is None:  # the caller gave none: one sized by the library, on the logits' device
         workspace = torch.empty(dg_denoise_workspace_bytes(n_canvas, L, V, _dtype_code(logits)),
                                 dtype=torch.uint8, device=logits.device)
-    ws_bytes = workspace.numel() * workspace.element_size()
-    rc = load().dg_denoise_step(_p(logits), _dtype_code(logits), ld, n_canvas, L, V, _p(params),
-                                int(seed) & 0xFFFFFFFFFFFFFFFF, _p(canvas), _p(prev_argmax),
-                                _p(stable_count), _p(accept_mask), _p(argmax), _p(sample), _p(entropy),
-                                _p(lse), _p(converged), _p(mean_entropy), _p(n_accept),
-                                _p(workspace), ws_bytes, _s(stream))
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def _denoise_full(fn, logits, params, seed, canvas, prev_argmax, stable_count, accept_mask, argmax,
+                  sample, entropy, lse, converged, mean_entropy, n_accept, workspace, n_canvas, L, V,
+                  ld, stream, check):
+    n_canvas, L, V, ld = _denoise_dims(logits, n_canvas, L, V, ld)
+    workspace, ws_bytes = _denoise_ws(workspace, logits, n_canvas, L, V)
+    rc = getattr(load(), fn)(_p(logits), _dtype_code(logits), ld, n_canvas, L, V, _p(params),
+                             int(seed) & 0xFFFFFFFFFFFFFFFF, _p(canvas), _p(prev_argmax),
+                             _p(stable_count), _p(accept_mask), _p(argmax), _p(sample), _p(entropy),
+                             _p(lse), _p(converged), _p(mean_entropy), _p(n_accept),
+                             _p(workspace), ws_bytes, _s(stream))
     if check:
-        _check("dg_denoise_step", rc)
+        _check(fn, rc)
+    return rc
+
+
+def dg_denoise_step(logits, params, seed, canvas, prev_argmax, stable_count, accept_mask, argmax,
+                    sample, entropy, lse, converged, mean_entropy=None, n_accept=None,
+                    workspace=None, *, n_canvas=None, L=None, V=None, ld=None, stream=None,
+                    check=True) -> int:
+    return _denoise_full("dg_denoise_step", logits, params, seed, canvas, prev_argmax, stable_count,
+                         accept_mask, argmax, sample, entropy, lse, converged, mean_entropy, n_accept,
+                         workspace, n_canvas, L, V, ld, stream, check)
+
+
+def dg_denoise_stats(logits, params, seed, canvas, prev_argmax, stable_count, accept_mask, argmax,
+                     sample, entropy, lse, converged, mean_entropy=None, n_accept=None,
+                     workspace=None, *, n_canvas=None, L=None, V=None, ld=None, stream=None,
+                     check=True) -> int:
+    """The statistics / acceptance half of dg_denoise_step (pass the same workspace to
+    dg_denoise_samples afterwards)."""
+    if workspace is None:
+        raise ValueError("dg_denoise_stats needs the workspace that dg_denoise_samples will read")
+    return _denoise_full("dg_denoise_stats", logits, params, seed, canvas, prev_argmax, stable_count,
+                         accept_mask, argmax, sample, entropy, lse, converged, mean_entropy, n_accept,
+                         workspace, n_canvas, L, V, ld, stream, check)
+
+
+def dg_denoise_samples(logits, params, seed, canvas, sample, workspace, *, n_canvas=None, L=None,
+                       V=None, ld=None, stream=None, check=True) -> int:
+    n_canvas, L, V, ld = _denoise_dims(logits, n_canvas, L, V, ld)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = load().dg_denoise_samples(_p(logits), _dtype_code(logits), ld, n_canvas, L, V, _p(params),
+                                   int(seed) & 0xFFFFFFFFFFFFFFFF, _p(canvas), _p(sample),
+                                   _p(workspace), ws_bytes, _s(stream))
+    if check:
+        _check("dg_denoise_samples", rc)
     return rc
 
 

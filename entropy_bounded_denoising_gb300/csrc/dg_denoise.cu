@@ -978,19 +978,20 @@ dg_status launch_k1(const void* logits, int64_t ld, int64_t n, int32_t L, int64_
     return dghost::cuda_status(cudaGetLastError());
 }
 
-// Samples and tokens of the listed accepted rows: three CTAs of kDWarps warps per SM, one warp
-// per 16 KB chunk (the list length is only known on the device).
+// Samples and tokens of the listed accepted rows: ctas_per_sm CTAs of kDWarps warps per SM,
+// one warp per 16 KB chunk (the list length is only known on the device).
 template <int DT>
 dg_status launch_kd(const void* logits, int64_t ld, int64_t n, int32_t L, int64_t V,
                     const dg_canvas_params* params, uint64_t seed, const DeferredWs& ws, int32_t* sample,
-                    int32_t* canvas, cudaStream_t stream) {
+                    int32_t* canvas, int ctas_per_sm, cudaStream_t stream) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return DG_ERR_CUDA;
     const int64_t cpr = (V * (DT == 0 ? 2 : 4) + kChunkBytes - 1) / kChunkBytes;
     const int64_t max_items = n * (int64_t)L * cpr;
-    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(3LL * sms, (max_items + kDWarps - 1) / kDWarps));
+    const unsigned grid =
+        (unsigned)std::max<int64_t>(1, std::min<int64_t>((int64_t)ctas_per_sm * sms, (max_items + kDWarps - 1) / kDWarps));
     const int64_t ld_bytes = ld * (DT == 0 ? 2 : 4);
     k1_sample_listed<DT><<<grid, kDWarps * 32, 0, stream>>>(static_cast<const unsigned char*>(logits), ld_bytes, V, L,
                                                            params, seed, ws, sample, canvas);
@@ -1034,11 +1035,11 @@ size_t dg_denoise_workspace_bytes(int64_t n_canvas, int32_t L, int64_t, dg_dtype
     return (denoise_ws_bytes(n_canvas * (int64_t)L) + 255) / 256 * 256;
 }
 
-dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L, int64_t V,
-                          const dg_canvas_params* params, uint64_t seed, int32_t* canvas, int32_t* prev_argmax,
-                          int32_t* stable_count, uint8_t* accept_mask, int32_t* argmax, int32_t* sample,
-                          float* entropy, float* lse, uint8_t* converged, float* mean_entropy, int32_t* n_accept,
-                          void* workspace, size_t workspace_bytes, dg_stream_t stream) {
+dg_status dg_denoise_stats(const void* logits, dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L, int64_t V,
+                           const dg_canvas_params* params, uint64_t seed, int32_t* canvas, int32_t* prev_argmax,
+                           int32_t* stable_count, uint8_t* accept_mask, int32_t* argmax, int32_t* sample,
+                           float* entropy, float* lse, uint8_t* converged, float* mean_entropy, int32_t* n_accept,
+                           void* workspace, size_t workspace_bytes, dg_stream_t stream) {
     if (dtype != DG_BF16 && dtype != DG_FP32) return DG_ERR_INVALID_ARG;
     dg_status s = check_canvas_dims(n_canvas, L, V);
     if (s != DG_OK) return s;
@@ -1057,11 +1058,50 @@ dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld, int64_
     s = dtype == DG_BF16 ? launch_k1<0>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, ws, st)
                          : launch_k1<1>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, ws, st);
     if (s != DG_OK) return s;
-    s = launch_k2(entropy, sample, argmax, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
-                  accept_mask, converged, mean_entropy, n_accept, ws, st);
+    return launch_k2(entropy, sample, argmax, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
+                     accept_mask, converged, mean_entropy, n_accept, ws, st);
+}
+
+static dg_status denoise_samples(const void* logits, dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L,
+                                 int64_t V, const dg_canvas_params* params, uint64_t seed, int32_t* canvas,
+                                 int32_t* sample, void* workspace, size_t workspace_bytes, int ctas_per_sm,
+                                 cudaStream_t st) {
+    if (dtype != DG_BF16 && dtype != DG_FP32) return DG_ERR_INVALID_ARG;
+    dg_status s = check_canvas_dims(n_canvas, L, V);
     if (s != DG_OK) return s;
-    return dtype == DG_BF16 ? launch_kd<0>(logits, ld, n_canvas, L, V, params, seed, ws, sample, canvas, st)
-                            : launch_kd<1>(logits, ld, n_canvas, L, V, params, seed, ws, sample, canvas, st);
+    if (ld < V) return DG_ERR_INVALID_ARG;
+    if (n_canvas == 0) return DG_OK;
+    if (!logits || !params || !canvas || !sample) return DG_ERR_INVALID_ARG;
+    const int64_t es = dtype == DG_BF16 ? 2 : 4;
+    if (!aligned16(logits) || (ld * es) % 16 != 0) return DG_ERR_ALIGNMENT;
+    if (!k1_supported(dtype, V)) return DG_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < dg_denoise_workspace_bytes(n_canvas, L, V, dtype)) return DG_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 7u) != 0) return DG_ERR_ALIGNMENT;
+    const DeferredWs ws = carve_ws(workspace, n_canvas * (int64_t)L);
+    return dtype == DG_BF16
+               ? launch_kd<0>(logits, ld, n_canvas, L, V, params, seed, ws, sample, canvas, ctas_per_sm, st)
+               : launch_kd<1>(logits, ld, n_canvas, L, V, params, seed, ws, sample, canvas, ctas_per_sm, st);
+}
+
+dg_status dg_denoise_samples(const void* logits, dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L, int64_t V,
+                             const dg_canvas_params* params, uint64_t seed, int32_t* canvas, int32_t* sample,
+                             void* workspace, size_t workspace_bytes, dg_stream_t stream) {
+    return denoise_samples(logits, dtype, ld, n_canvas, L, V, params, seed, canvas, sample, workspace,
+                           workspace_bytes, 1, (cudaStream_t)stream);
+}
+
+dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L, int64_t V,
+                          const dg_canvas_params* params, uint64_t seed, int32_t* canvas, int32_t* prev_argmax,
+                          int32_t* stable_count, uint8_t* accept_mask, int32_t* argmax, int32_t* sample,
+                          float* entropy, float* lse, uint8_t* converged, float* mean_entropy, int32_t* n_accept,
+                          void* workspace, size_t workspace_bytes, dg_stream_t stream) {
+    dg_status s = dg_denoise_stats(logits, dtype, ld, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
+                                   accept_mask, argmax, sample, entropy, lse, converged, mean_entropy, n_accept,
+                                   workspace, workspace_bytes, stream);
+    if (s != DG_OK || n_canvas == 0) return s;
+    // alone on its stream: three CTAs per SM hide more of the load latency
+    return denoise_samples(logits, dtype, ld, n_canvas, L, V, params, seed, canvas, sample, workspace,
+                           workspace_bytes, 3, (cudaStream_t)stream);
 }
 
 dg_status dg_accept_from_entropy(const float* entropy, const int32_t* sample, const int32_t* argmax,

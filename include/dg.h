@@ -171,6 +171,35 @@ DG_API dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld,
                           float* mean_entropy, int32_t* n_accept,
                           void* workspace, size_t workspace_bytes, dg_stream_t stream);
 
+/* dg_denoise_step in two calls, so that the samples can run on another stream (e.g. beside
+ * the self-conditioning GEMMs, which do not read them):
+ *   dg_denoise_stats:   statistics, acceptance, renoise of the rejected positions and
+ *                       convergence; lists the accepted positions of canvases without
+ *                       DG_SAMPLE_ALL in the workspace (their sample and canvas entries are
+ *                       written by dg_denoise_samples);
+ *   dg_denoise_samples: the Gumbel-max samples of the listed positions, written to sample
+ *                       and canvas.  It launches at most one CTA per SM (of 256 threads and
+ *                       80 registers, no shared memory), so that it can share SMs with a
+ *                       GEMM running on another stream.
+ * dg_denoise_samples must follow dg_denoise_stats of the same step (an event on the stats'
+ * stream when it runs on another stream), with the same logits, params, seed, sizes and
+ * workspace, and complete before the canvas or the workspace is used again (by the caller or
+ * the next step).  Arguments, limits and errors are those of dg_denoise_step; together the
+ * two calls produce exactly its outputs. */
+DG_API dg_status dg_denoise_stats(const void* logits, dg_dtype dtype, int64_t ld,
+                                  int64_t n_canvas, int32_t L, int64_t V,
+                                  const dg_canvas_params* params, uint64_t seed,
+                                  int32_t* canvas, int32_t* prev_argmax, int32_t* stable_count,
+                                  uint8_t* accept_mask, int32_t* argmax, int32_t* sample,
+                                  float* entropy, float* lse, uint8_t* converged,
+                                  float* mean_entropy, int32_t* n_accept,
+                                  void* workspace, size_t workspace_bytes, dg_stream_t stream);
+DG_API dg_status dg_denoise_samples(const void* logits, dg_dtype dtype, int64_t ld,
+                                    int64_t n_canvas, int32_t L, int64_t V,
+                                    const dg_canvas_params* params, uint64_t seed,
+                                    int32_t* canvas, int32_t* sample,
+                                    void* workspace, size_t workspace_bytes, dg_stream_t stream);
+
 /* The per-canvas half of the step (acceptance, renoise, convergence) on caller-given
  * per-position entropy, sample and argmax, all (device) [n_canvas][L].  Same semantics and
  * outputs as dg_denoise_step, except that every accepted position takes the given sample

@@ -52,6 +52,13 @@ def test_host_validation_without_gpu():
     assert lib.dg_denoise_step(16, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), None, 0, None) == dg.DG_ERR_WORKSPACE
     assert lib.dg_denoise_step(16, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), 256, 640, None) == dg.DG_ERR_WORKSPACE
     assert lib.dg_denoise_step(16, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), 260, 768, None) == dg.DG_ERR_ALIGNMENT
+    # the two halves of the step validate like the whole
+    assert lib.dg_denoise_stats(16, 0, 8, 1, 16, 8, None, 0, *([16] * 11), 256, 768, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_denoise_stats(16, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), None, 0, None) == dg.DG_ERR_WORKSPACE
+    assert lib.dg_denoise_samples(16, 0, 8, 1, 16, 8, 16, 0, None, 16, 256, 768, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_denoise_samples(16, 0, 8, 1, 16, 8, 16, 0, 16, 16, 256, 640, None) == dg.DG_ERR_WORKSPACE
+    assert lib.dg_denoise_samples(18, 0, 8, 1, 16, 8, 16, 0, 16, 16, 256, 768, None) == dg.DG_ERR_ALIGNMENT
+    assert lib.dg_denoise_samples(None, 0, 8, 0, 16, 8, None, 0, None, None, None, 0, None) == dg.DG_OK
     # empty batch is a no-op
     assert lib.dg_denoise_step(None, 0, 8, 0, 16, 8, None, 0, *([None] * 11), None, 0, None) == dg.DG_OK
     assert lib.dg_denoise_workspace_bytes(8, 256, 262144, 0) == 256 + 24 * 8 * 256

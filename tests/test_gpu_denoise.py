@@ -235,3 +235,38 @@ def test_step_edge_sizes(dtype, V, ld, L, sample_all):
     if sample_all:
         p["flags"] |= dg.DG_SAMPLE_ALL
     _check_case(x, p, 0xE06E + V, V, canvas0=rng.integers(0, V, (n, L)).astype(np.int32))
+
+
+def test_split_step_on_two_streams_matches_one_call():
+    """dg_denoise_stats on one stream and dg_denoise_samples on another (after an event, as
+    the benchmark runs them beside the feedback GEMMs) give bit-identical outputs to
+    dg_denoise_step, over three steps of a loop with mixed sampling modes."""
+    rng = np.random.default_rng(21)
+    n, L, V = 5, 256, 70001
+    p = _params(n, rng, beta=12.0)
+    p["flags"][1] |= dg.DG_SAMPLE_ALL
+    p["flags"][3] = dg.DG_ACTIVE | dg.DG_READ_ONLY
+    p["max_steps"][3] = 1
+    canvas0 = rng.integers(0, V, (n, L)).astype(np.int32)
+    one, two = StepBuffers.make(n, L, DEV, canvas0), StepBuffers.make(n, L, DEV, canvas0)
+    ws1 = torch.empty(dg.dg_denoise_workspace_bytes(n, L, V), dtype=torch.uint8, device=DEV)
+    ws2 = torch.empty_like(ws1)
+    main, side = torch.cuda.Stream(), torch.cuda.Stream()
+    done = torch.cuda.Event()
+    for t in range(3):
+        p["step"][:] = t
+        pt = dg.params_tensor(p, DEV)
+        x = synth.logits(n, L, V, seed=21, step=t, scale=(0.5, 12.0), spike_frac=0.1, ld=70008, device=DEV)
+        torch.cuda.synchronize()
+        run_step(x, pt, 4242, one, V=V)
+        b = two
+        dg.dg_denoise_stats(x, pt, 4242, b.canvas, b.prev, b.stable, b.accept, b.argmax, b.sample, b.entropy,
+                            b.lse, b.converged, b.mean_entropy, b.n_accept, workspace=ws2, V=V, stream=main)
+        done.record(main)
+        side.wait_event(done)
+        dg.dg_denoise_samples(x, pt, 4242, b.canvas, b.sample, ws2, V=V, stream=side)
+        torch.cuda.synchronize()
+        h1, h2 = one.host(), two.host()
+        for k in h1:
+            assert np.array_equal(h1[k], h2[k]), (t, k)
+        assert (h2["sample"][0][h2["accept"][0] == 1] >= 0).all()

@@ -574,10 +574,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 }
 
 // ------------------------------------------------------------------ split-K fix-up
-// Adds the k-slice partials of each tile in slice order and applies the epilogue.  Plain
-// stores (fp32 / bf16): every thread owns 4 consecutive columns (float4 loads, coalesced
-// across the warp) and the tiles are spread over gridDim.y CTAs each.  The GELU and scatter
-// epilogues (32-column groups) take the generic loop.
+// Adds the k-slice partials of each tile in slice order and applies the epilogue.  Every
+// thread owns 4 consecutive output columns of a row (float4 loads, coalesced across the warp)
+// and the tiles are spread over gridDim.y CTAs each.  For the gate/up epilogue the output
+// columns are the tile's first BN/2 (gate) columns, each paired with the up column BN/2 later.
 template <int BN>
 __global__ void __launch_bounds__(256) k_fixup(const GemmArgs a) {
     const int mt = active_m_tiles(a);
@@ -585,70 +585,65 @@ __global__ void __launch_bounds__(256) k_fixup(const GemmArgs a) {
     const int64_t t = blockIdx.x;
     if (t >= T) return;
     const int n = (int)(t / mt), m = (int)(t % mt);
-    if (a.epi == EPI_F32 || a.epi == EPI_BF16) {
-        constexpr int kQuads = BM * BN / 4;
-        const int per_cta = (kQuads + gridDim.y - 1) / gridDim.y;
-        const int q0 = blockIdx.y * per_cta, q1 = min(kQuads, q0 + per_cta);
-        for (int qd = q0 + threadIdx.x; qd < q1; qd += blockDim.x) {
-            const int row = qd / (BN / 4);
-            const int col = (qd % (BN / 4)) * 4;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s = 0; s < a.splits; ++s) {
-                const float4 v = *reinterpret_cast<const float4*>(
-                    a.partial + (size_t)(s * T + t) * (BM * BN) + (size_t)row * BN + col);
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
-            }
-            const int64_t r = (int64_t)m * BM + row;
-            const int c0 = n * BN + col;
-            if (a.epi == EPI_F32) {
-                if (r >= a.m_valid) continue;
-                float* o = static_cast<float*>(a.out) + r * a.ldo + c0;
-                const float vv[4] = {acc.x, acc.y, acc.z, acc.w};
-                for (int i = 0; i < 4; ++i)
-                    if (c0 + i < a.n_valid) o[i] = vv[i];
-            } else {
-                uint16_t* o = static_cast<uint16_t*>(a.out) + r * a.ldo + c0;
-                const uint32_t p0 = pack_bf16x2(acc.x, acc.y), p1 = pack_bf16x2(acc.z, acc.w);
-                if (c0 + 4 <= a.n_valid && ((reinterpret_cast<uintptr_t>(o) & 7u) == 0)) {
-                    *reinterpret_cast<uint2*>(o) = make_uint2(p0, p1);
-                } else {
-                    const uint16_t hv[4] = {(uint16_t)(p0 & 0xFFFFu), (uint16_t)(p0 >> 16), (uint16_t)(p1 & 0xFFFFu),
-                                            (uint16_t)(p1 >> 16)};
-                    for (int i = 0; i < 4; ++i)
-                        if (c0 + i < a.n_valid) o[i] = hv[i];
-                }
-            }
-        }
-        return;
-    }
-    if (blockIdx.y != 0) return;
-    constexpr int kGroups = BM * (BN / 32);  // (row, 32-column chunk) pairs
-    for (int gidx = threadIdx.x; gidx < kGroups; gidx += blockDim.x) {
-        const int row = gidx / (BN / 32);
-        const int ch = gidx % (BN / 32);
-        if (a.epi == EPI_GELU_GATEUP && ch >= BN / 64) continue;
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.f;
-        float g[32];
+    const bool gu = a.epi == EPI_GELU_GATEUP;
+    const int out_cols = gu ? BN / 2 : BN;
+    const int quads = BM * out_cols / 4;
+    const int per_cta = (quads + gridDim.y - 1) / gridDim.y;
+    const int q0 = blockIdx.y * per_cta, q1 = min(quads, q0 + per_cta);
+    for (int qd = q0 + threadIdx.x; qd < q1; qd += blockDim.x) {
+        const int row = qd / (out_cols / 4);
+        const int col = (qd % (out_cols / 4)) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), up = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s = 0; s < a.splits; ++s) {
-            const float* src = a.partial + (size_t)(s * T + t) * (BM * BN) + (size_t)row * BN;
-            if (a.epi == EPI_GELU_GATEUP) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    if (s == 0) g[i] = 0.f;
-                    g[i] += src[ch * 32 + i];
-                    v[i] += src[BN / 2 + ch * 32 + i];
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] += src[ch * 32 + i];
+            const float* src = a.partial + (size_t)(s * T + t) * (BM * BN) + (size_t)row * BN + col;
+            const float4 v = *reinterpret_cast<const float4*>(src);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+            if (gu) {
+                const float4 u = *reinterpret_cast<const float4*>(src + BN / 2);
+                up.x += u.x;
+                up.y += u.y;
+                up.z += u.z;
+                up.w += u.w;
             }
         }
-        epi_store(a, a.epi, m, n, row, ch * 32, BN, v, a.epi == EPI_GELU_GATEUP ? g : nullptr);
+        int64_t r;
+        int c0;
+        if (a.epi == EPI_SCATTER_BF16) {
+            const int pos = (m % a.tpc) * BM + row;
+            if (pos >= a.L) continue;
+            r = (int64_t)canvas_of(a, m) * a.L + pos;
+            c0 = n * BN + col;
+        } else {
+            r = (int64_t)m * BM + row;
+            c0 = n * out_cols + col;
+        }
+        if (a.epi == EPI_F32) {
+            if (r >= a.m_valid) continue;
+            float* o = static_cast<float*>(a.out) + r * a.ldo + c0;
+            const float vv[4] = {acc.x, acc.y, acc.z, acc.w};
+            for (int i = 0; i < 4; ++i)
+                if (c0 + i < a.n_valid) o[i] = vv[i];
+            continue;
+        }
+        if (gu) {
+            acc.x = gelu_tanh(acc.x) * up.x;
+            acc.y = gelu_tanh(acc.y) * up.y;
+            acc.z = gelu_tanh(acc.z) * up.z;
+            acc.w = gelu_tanh(acc.w) * up.w;
+        }
+        uint16_t* o = static_cast<uint16_t*>(a.out) + r * a.ldo + c0;
+        const uint32_t p0 = pack_bf16x2(acc.x, acc.y), p1 = pack_bf16x2(acc.z, acc.w);
+        if (c0 + 4 <= a.n_valid && ((reinterpret_cast<uintptr_t>(o) & 7u) == 0)) {
+            *reinterpret_cast<uint2*>(o) = make_uint2(p0, p1);
+        } else {
+            const uint16_t hv[4] = {(uint16_t)(p0 & 0xFFFFu), (uint16_t)(p0 >> 16), (uint16_t)(p1 & 0xFFFFu),
+                                    (uint16_t)(p1 >> 16)};
+            for (int i = 0; i < 4; ++i)
+                if (c0 + i < a.n_valid) o[i] = hv[i];
+        }
     }
 }
 
@@ -740,9 +735,11 @@ struct LaunchPlan {
 // is shared by the 2 CTAs of a cluster on neighbouring m-tiles (pairs fill the GPCs better
 // than 4-CTA clusters, and measured as fast); the 4-CTA form stays available and is used
 // only while the GPU keeps at least 90 % of its SMs busy with it.  The k-slices are then
-// chosen for the number of clusters, within `max_slots` partial tiles.
+// chosen for the number of clusters, within `max_slots` partial tiles, with slices of at
+// least `min_slice` k-blocks, and only when the unsplit work would fill less than
+// `split_below` of the clusters' last round.
 template <class C>
-bool plan_gemm(const GemmArgs& a, int64_t max_slots, LaunchPlan* pl) {
+bool plan_gemm(const GemmArgs& a, int64_t max_slots, LaunchPlan* pl, int min_slice = 256, double split_below = 1.01) {
     auto kern = k_gemm<C>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
         return false;
@@ -774,7 +771,9 @@ bool plan_gemm(const GemmArgs& a, int64_t max_slots, LaunchPlan* pl) {
     }
     if (cm == 1) clusters = P;
     const int64_t per_split = (int64_t)a.n_tiles * ((a.m_tiles + cm - 1) / cm);
-    int splits = choose_splits(per_split, a.k_blocks, clusters, 256);
+    const int64_t rounds1 = (per_split + clusters - 1) / clusters;
+    const double eff1 = (double)per_split / (double)(rounds1 * clusters);
+    int splits = eff1 < split_below ? choose_splits(per_split, a.k_blocks, clusters, std::max(1, min_slice)) : 1;
     while (splits > 1 && (int64_t)a.m_tiles * a.n_tiles * splits > max_slots) --splits;
     pl->cm = cm;
     pl->clusters = clusters;
@@ -819,9 +818,9 @@ dg_status launch_gemm(const void* tmA, const void* tmB0, const void* tmB1, const
 // Plan, then launch, with the planned k-slices.
 template <class C>
 dg_status plan_and_launch(const void* tmA, const void* tmB0, const void* tmB1, GemmArgs a, int64_t max_slots,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, int min_slice = 256, double split_below = 1.01) {
     LaunchPlan pl;
-    if (!plan_gemm<C>(a, max_slots, &pl)) return DG_ERR_CUDA;
+    if (!plan_gemm<C>(a, max_slots, &pl, min_slice, split_below)) return DG_ERR_CUDA;
     a.splits = pl.splits;
     return launch_gemm<C>(tmA, tmB0, tmB1, a, pl, stream);
 }
@@ -878,11 +877,19 @@ int64_t pe_partial_slots(int64_t n, int32_t L, int32_t d, int P) {
     return T * 32 > 0 ? std::min<int64_t>(T * 32, std::max<int64_t>(T, 8LL * P)) : 0;
 }
 
+// Smallest k-slice of the self-conditioning GEMMs, in elements of K: a slice of 1024 still
+// keeps the tensor cores busy about ten times longer than its partial tile takes to write.
+constexpr int kMinSliceK = 1024;
+
 // The three GEMMs of the feedback on compact rows: pe = P.E (already in `pe`), then
 // hmid = gelu(pe W_gate^T) * (pe W_up^T), then delta = hmid W_down^T scattered to rows.
+// `partial` holds `pe_slots` P.E partial tiles (128 x 512 fp32), i.e. twice as many of the
+// MLP's 128 x 256 tiles: a GEMM too small to fill the GPU (under 60 % of its pairs in the
+// last round) splits K into them.
 dg_status run_mlp(const uint16_t* pe, uint16_t* hmid, int64_t rows, int32_t d, int32_t h, const uint16_t* W_gate,
                   const uint16_t* W_up, const uint16_t* W_down, uint16_t* delta, int64_t delta_ld,
-                  const int32_t* plan, int tpc, int32_t L, int32_t m_valid_rows, cudaStream_t stream) {
+                  const int32_t* plan, int tpc, int32_t L, int32_t m_valid_rows, float* partial, int64_t pe_slots,
+                  cudaStream_t stream) {
     const int P = dghost::sm_count();
     TMaps t1, t2;
     if (!tmap_2d(t1.a, 0, pe, d, rows, d, 64, BM, 128)) return DG_ERR_CUDA;
@@ -902,8 +909,10 @@ dg_status run_mlp(const uint16_t* pe, uint16_t* hmid, int64_t rows, int32_t d, i
     g.ldo = h;
     g.n_valid = h;
     g.m_valid = (int32_t)rows;
+    g.partial = partial;
     g.status = dghost::status_word();
-    dg_status s = plan_and_launch<GateUp>(t1.a, t1.b0, t1.b1, g, 0, stream);
+    const int64_t mlp_slots = partial ? 2 * pe_slots : 0;
+    dg_status s = plan_and_launch<GateUp>(t1.a, t1.b0, t1.b1, g, mlp_slots, stream, kMinSliceK / 64, 0.6);
     if (s != DG_OK) return s;
 
     if (!tmap_2d(t2.a, 0, hmid, h, rows, h, 64, BM, 128)) return DG_ERR_CUDA;
@@ -918,7 +927,7 @@ dg_status run_mlp(const uint16_t* pe, uint16_t* hmid, int64_t rows, int32_t d, i
     q.n_valid = d;
     q.m_valid = m_valid_rows;
     (void)P;
-    return plan_and_launch<Down>(t2.a, t2.b0, t2.b0, q, 0, stream);
+    return plan_and_launch<Down>(t2.a, t2.b0, t2.b0, q, mlp_slots, stream, kMinSliceK / 64, 0.6);
 }
 
 dg_status check_weights(int64_t V, int32_t d, int32_t h, const uint16_t* E, const uint16_t* Wg, const uint16_t* Wu,
@@ -1022,8 +1031,8 @@ dg_status dg_self_cond_pe(const void* logits, dg_dtype dtype, int64_t ld, const 
     g.partial = reinterpret_cast<float*>(ws + lay.partial);
     g.status = dghost::status_word();
     const int64_t max_slots = pe_partial_slots(n_canvas, L, d, P);
-    return dtype == DG_BF16 ? plan_and_launch<PEbf16>(tm.a, tm.b0, tm.b0, g, max_slots, st)
-                            : plan_and_launch<PEfp32>(tm.a, tm.b0, tm.b0, g, max_slots, st);
+    return dtype == DG_BF16 ? plan_and_launch<PEbf16>(tm.a, tm.b0, tm.b0, g, max_slots, st, kMinSliceK / bk)
+                            : plan_and_launch<PEfp32>(tm.a, tm.b0, tm.b0, g, max_slots, st, kMinSliceK / bk);
 }
 
 dg_status dg_self_cond_mlp(int64_t n_canvas, int32_t L, int32_t d, int32_t h, const uint16_t* W_gate,
@@ -1039,9 +1048,11 @@ dg_status dg_self_cond_mlp(int64_t n_canvas, int32_t L, int32_t d, int32_t h, co
     if (s != DG_OK) return s;
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     const int tpc = (L + BM - 1) / BM;
+    const int P = dghost::sm_count();
     return run_mlp(reinterpret_cast<uint16_t*>(ws + lay.pe), reinterpret_cast<uint16_t*>(ws + lay.hmid), lay.rows,
                    d, h, W_gate, W_up, W_down, delta_emb, d, reinterpret_cast<int32_t*>(ws + lay.plan), tpc, L,
-                   (int32_t)lay.rows, (cudaStream_t)stream);
+                   (int32_t)lay.rows, reinterpret_cast<float*>(ws + lay.partial), pe_partial_slots(n_canvas, L, d, P),
+                   (cudaStream_t)stream);
 }
 
 dg_status dg_self_cond_logits(const void* logits, dg_dtype dtype, int64_t ld, const float* lse,
@@ -1124,7 +1135,7 @@ dg_status dg_self_cond_probs(const uint16_t* P_rows, int64_t ld, int64_t n_rows,
     s = plan_and_launch<PEprob>(tm.a, tm.b0, tm.b0, g, slots, st);
     if (s != DG_OK) return s;
     return run_mlp(pe, hmid, rows, d, h, W_gate, W_up, W_down, delta_emb, d, nullptr, (int)tiles, (int32_t)n_rows,
-                   (int32_t)rows, st);
+                   (int32_t)rows, partial, slots, st);
 }
 
 size_t dg_gemm_workspace_bytes(int64_t M, int64_t N) {

@@ -314,7 +314,10 @@ def run_ours(args):
     wsp = torch.empty(dg.dg_self_cond_workspace_bytes(n, L, d, h), dtype=torch.uint8, device=dev)
     dws = torch.empty(dg.dg_denoise_workspace_bytes(n, L, V, dg.DG_BF16 if wl.dtype == "bf16" else dg.DG_FP32),
                       dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
+    # --graph captures the step once as a CUDA graph (on a side stream, as capture requires)
+    # and times its replays; otherwise every step is enqueued call by call.
+    stream = torch.cuda.Stream(device=dev) if args.graph else torch.cuda.current_stream()
+    stream.wait_stream(torch.cuda.current_stream())
     seed = 0x5EED0000 + rank
 
     def step(ev=None):
@@ -336,6 +339,18 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
     dg.dg_clear_device_status()
+    graph = None
+    launches_per_step = 0
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        c0 = dg.dg_launch_count()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        launches_per_step = dg.dg_launch_count() - c0
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                graph.replay()
+        torch.cuda.synchronize()
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     barrier()
@@ -346,8 +361,13 @@ def run_ours(args):
         launches0 = dg.dg_launch_count()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
-        for k in range(args.steps):
-            step(evs[k])
+        if graph is not None:
+            with torch.cuda.stream(stream):
+                for k in range(args.steps):
+                    graph.replay()
+        else:
+            for k in range(args.steps):
+                step(evs[k])
         end.record(stream)
         launches = dg.dg_launch_count() - launches0
         torch.cuda.synchronize()
@@ -369,6 +389,14 @@ def run_ours(args):
     ms_step = elapsed_ms / args.steps
     value = job_throughput(positions, ws, args.steps, elapsed_ms)
 
+    if graph is not None:
+        # the per-phase split from eager steps (the replays carry no events); launches per
+        # replay are the captured step's
+        launches = launches_per_step * args.steps
+        for k in range(min(20, args.steps)):
+            step(evs[k])
+        torch.cuda.synchronize()
+        evs = evs[:min(20, args.steps)]
     t_dn = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     t_pe = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
     t_mlp = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
@@ -515,7 +543,9 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(wl),
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(_config(wl), launch=("CUDA graph replays of the captured step" if graph is not None
+                                            else "eager: every call enqueued each step")),
         "roofline": {"bound": "tensor", "achieved": pe_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                      "frac": pe_tflops / peak_tc, "traffic": traffic,
                      "kernel": "P.E contraction (k_gemm softmax-A, N-major B) + split-K fix-up",
@@ -655,6 +685,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip timing the rows around the step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true", help="time replays of the step captured as a CUDA graph")
     ap.add_argument("--loop", action="store_true",
                     help="time the workload's whole denoising loop (e.g. --workload sweep) instead of repeated steps")
     args = ap.parse_args()

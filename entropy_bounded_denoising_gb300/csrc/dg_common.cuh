@@ -21,6 +21,14 @@ DG_DEVINL void raise_status(unsigned* status, unsigned bits) {
     if (status) atomicOr(status, bits);
 }
 
+// Programmatic dependent launch.  Kernels of the library are launched so that they may start
+// while the previous kernel on the stream drains; each calls pdl_wait() before its first
+// global-memory access (and before any early exit, so that completion stays ordered along the
+// stream), then pdl_release() to let the next kernel start in turn.  Without the launch
+// attribute both are no-ops.
+DG_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+DG_DEVINL void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Per-canvas parameters the acceptance kernel works with (else DG_DEV_BAD_PARAM, canvas skipped).
 DG_DEVINL bool canvas_params_ok(const dg_canvas_params& p, int32_t L) {
     return p.temperature > 0.f && isfinite(p.temperature) && p.k >= 1 && p.max_steps >= 1 && p.min_accept >= 0 &&
@@ -388,4 +396,26 @@ inline dg_status cuda_status(cudaError_t err) { return err == cudaSuccess ? DG_O
 // Encode a tiled tensor map (driver entry point fetched once).  Returns false on failure.
 bool encode_tmap(void* tmap, int dtype_code, int rank, void* base, const uint64_t* dims,
                  const uint64_t* strides_bytes, const uint32_t* box, int swizzle_bytes);
+// Programmatic dependent launch on (build with -DDG_NO_PDL for plain stream order).
+#ifdef DG_NO_PDL
+constexpr bool kPdl = false;
+#else
+constexpr bool kPdl = true;
+#endif
+// Launch with programmatic stream serialisation (the kernel calls dg::pdl_wait first).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = kPdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
 }  // namespace dghost

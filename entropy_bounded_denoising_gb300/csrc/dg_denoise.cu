@@ -382,6 +382,8 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
     const int64_t canvas = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+    dg::pdl_wait();
+    dg::pdl_release();
     if (ws.count && pos == 0 && canvas == 0 && tid == 0) *ws.count = 0;
     const dg_canvas_params p = params[canvas];
     if (!(p.flags & DG_ACTIVE)) return;
@@ -699,6 +701,8 @@ __global__ void __launch_bounds__(kDWarps * 32, 3) k1_sample_listed(
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * kDWarps + (threadIdx.x >> 5);
     const int64_t nw = (int64_t)gridDim.x * kDWarps;
+    dg::pdl_wait();
+    dg::pdl_release();
     const int count = *ws.count;
     const int cpr = (int)((V * ES + kChunkBytes - 1) / kChunkBytes);  // chunks per row
     const int64_t items = (int64_t)count * cpr;
@@ -820,6 +824,8 @@ __global__ void __launch_bounds__(1024) k2_accept(
 
     const int64_t c = blockIdx.x;
     const int i = threadIdx.x, lane = i & 31, warp = i >> 5, nwarps = blockDim.x >> 5;
+    dg::pdl_wait();
+    dg::pdl_release();
     const dg_canvas_params p = params[c];
     if (!(p.flags & DG_ACTIVE)) return;
     if (!dg::canvas_params_ok(p, L)) {
@@ -970,12 +976,11 @@ dg_status launch_k1(const void* logits, int64_t ld, int64_t n, int32_t L, int64_
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DG_ERR_CUDA;
     const int64_t ld_bytes = ld * (DT == 0 ? 2 : 4);
-    kern<<<dim3((unsigned)L, (unsigned)n, 1), kK1Threads, smem, stream>>>(static_cast<const unsigned char*>(logits),
-                                                                          ld_bytes, V, L, params, seed, argmax,
-                                                                          sample, entropy, lse, ws,
-                                                                          dghost::status_word());
+    const cudaError_t e = dghost::launch_pdl(kern, dim3((unsigned)L, (unsigned)n, 1), dim3(kK1Threads), smem, stream,
+                                             static_cast<const unsigned char*>(logits), ld_bytes, V, L, params, seed,
+                                             argmax, sample, entropy, lse, ws, dghost::status_word());
     dghost::count_launch();
-    return dghost::cuda_status(cudaGetLastError());
+    return dghost::cuda_status(e);
 }
 
 // Samples and tokens of the listed accepted rows: ctas_per_sm CTAs of kDWarps warps per SM,
@@ -993,10 +998,11 @@ dg_status launch_kd(const void* logits, int64_t ld, int64_t n, int32_t L, int64_
     const unsigned grid =
         (unsigned)std::max<int64_t>(1, std::min<int64_t>((int64_t)ctas_per_sm * sms, (max_items + kDWarps - 1) / kDWarps));
     const int64_t ld_bytes = ld * (DT == 0 ? 2 : 4);
-    k1_sample_listed<DT><<<grid, kDWarps * 32, 0, stream>>>(static_cast<const unsigned char*>(logits), ld_bytes, V, L,
-                                                           params, seed, ws, sample, canvas);
+    const cudaError_t e = dghost::launch_pdl(k1_sample_listed<DT>, dim3(grid), dim3(kDWarps * 32), 0, stream,
+                                             static_cast<const unsigned char*>(logits), ld_bytes, V, L, params, seed,
+                                             ws, sample, canvas);
     dghost::count_launch();
-    return dghost::cuda_status(cudaGetLastError());
+    return dghost::cuda_status(e);
 }
 
 dg_status launch_k2(const float* entropy, const int32_t* sample, const int32_t* argmax, int64_t n, int32_t L,
@@ -1004,11 +1010,12 @@ dg_status launch_k2(const float* entropy, const int32_t* sample, const int32_t* 
                     int32_t* stable_count, uint8_t* accept_mask, uint8_t* converged, float* mean_entropy,
                     int32_t* n_accept, const DeferredWs& ws, cudaStream_t stream) {
     const unsigned threads = (unsigned)((L + 31) / 32 * 32);
-    k2_accept<<<(unsigned)n, threads, 0, stream>>>(entropy, sample, argmax, L, V, params, seed, canvas, prev_argmax,
-                                                   stable_count, accept_mask, converged, mean_entropy, n_accept,
-                                                   ws, dghost::status_word());
+    const cudaError_t e = dghost::launch_pdl(k2_accept, dim3((unsigned)n), dim3(threads), 0, stream, entropy, sample,
+                                             argmax, L, V, params, seed, canvas, prev_argmax, stable_count,
+                                             accept_mask, converged, mean_entropy, n_accept, ws,
+                                             dghost::status_word());
     dghost::count_launch();
-    return dghost::cuda_status(cudaGetLastError());
+    return dghost::cuda_status(e);
 }
 
 // The deferred-sampling workspace: a count (padded to 256 bytes), then per listed row an

@@ -263,9 +263,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     constexpr bool PAIR = C::kPair;
     const bool leader = !PAIR || rank == 0;  // the pair's MMAs are issued by its first CTA
 
-    const int mt = active_m_tiles(a);
-    const int64_t n_groups = mt > 0 ? group_count(a, mt, cm) : 0;
-
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             dg::mbar_init(&sh.full[s], 1);
@@ -294,6 +291,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     cluster.sync();  // peers' barriers are initialised before any multicast lands
     dg::tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
+    // the prologue above overlaps the previous kernel; its outputs (plan, lse, A, B) are read below
+    dg::pdl_wait();
+    dg::pdl_release();
+    const int mt = active_m_tiles(a);
+    const int64_t n_groups = mt > 0 ? group_count(a, mt, cm) : 0;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -580,6 +582,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 // columns are the tile's first BN/2 (gate) columns, each paired with the up column BN/2 later.
 template <int BN>
 __global__ void __launch_bounds__(256) k_fixup(const GemmArgs a) {
+    dg::pdl_wait();
+    dg::pdl_release();
     const int mt = active_m_tiles(a);
     const int64_t T = (int64_t)mt * a.n_tiles;
     const int64_t t = blockIdx.x;
@@ -656,6 +660,8 @@ DG_DEVINL bool self_cond_on(const dg_canvas_params& p, const uint8_t* converged,
 // Compact list of the canvases whose feedback is computed this step (original order).
 __global__ void k_plan(const dg_canvas_params* __restrict__ params, const uint8_t* __restrict__ converged,
                        int64_t n, int32_t* __restrict__ plan) {
+    dg::pdl_wait();
+    dg::pdl_release();
     __shared__ int count;
     if (threadIdx.x == 0) count = 0;
     __syncthreads();
@@ -680,6 +686,8 @@ __global__ void k_plan(const dg_canvas_params* __restrict__ params, const uint8_
 // Zero the feedback rows of canvases that get none this step.
 __global__ void k_zero_rows(const dg_canvas_params* __restrict__ params, const uint8_t* __restrict__ converged,
                             int32_t L, int32_t d, uint16_t* __restrict__ delta) {
+    dg::pdl_wait();
+    dg::pdl_release();
     const int64_t c = blockIdx.y;
     if (self_cond_on(params[c], converged, c)) return;
     const int64_t total = (int64_t)L * d;
@@ -786,11 +794,13 @@ dg_status launch_gemm(const void* tmA, const void* tmB0, const void* tmB1, const
                       cudaStream_t stream) {
     auto kern = k_gemm<C>;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)pl.cm;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // the kernel waits after its prologue
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     const int64_t groups = (int64_t)a.splits * a.n_tiles * ((a.m_tiles + pl.cm - 1) / pl.cm);
     const int64_t ncl = std::max<int64_t>(1, std::min<int64_t>(pl.clusters, groups));
     cfg.gridDim = dim3((unsigned)(ncl * pl.cm), 1, 1);
@@ -798,7 +808,7 @@ dg_status launch_gemm(const void* tmA, const void* tmB0, const void* tmB1, const
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = dghost::kPdl ? 2 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, *static_cast<const CUtensorMap*>(tmA),
                                        *static_cast<const CUtensorMap*>(tmB0), *static_cast<const CUtensorMap*>(tmB1), a);
     dghost::count_launch();
@@ -808,9 +818,8 @@ dg_status launch_gemm(const void* tmA, const void* tmB0, const void* tmB1, const
         // spread each tile over enough CTAs to fill the GPU a few times
         const int P = dghost::sm_count();
         const unsigned per_tile = (unsigned)std::max<int64_t>(1, std::min<int64_t>(16, (4LL * P + T - 1) / T));
-        k_fixup<C::BN><<<dim3((unsigned)T, per_tile, 1), 256, 0, stream>>>(a);
+        e = dghost::launch_pdl(k_fixup<C::BN>, dim3((unsigned)T, per_tile, 1), dim3(256), 0, stream, a);
         dghost::count_launch();
-        e = cudaGetLastError();
     }
     return dghost::cuda_status(e);
 }
@@ -981,13 +990,13 @@ dg_status dg_self_cond_prepare(const dg_canvas_params* params, const uint8_t* co
     if (s != DG_OK) return s;
     cudaStream_t st = (cudaStream_t)stream;
     int32_t* plan = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + lay.plan);
-    k_plan<<<1, 1024, 0, st>>>(params, converged, n_canvas, plan);
+    cudaError_t e = dghost::launch_pdl(k_plan, dim3(1), dim3(1024), 0, st, params, converged, n_canvas, plan);
     dghost::count_launch();
-    if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+    if (e != cudaSuccess) return DG_ERR_CUDA;
     dim3 grid((unsigned)std::min<int64_t>(1024, ((int64_t)L * d + 255) / 256), (unsigned)n_canvas);
-    k_zero_rows<<<grid, 256, 0, st>>>(params, converged, L, d, delta_emb);
+    e = dghost::launch_pdl(k_zero_rows, grid, dim3(256), 0, st, params, converged, L, d, delta_emb);
     dghost::count_launch();
-    return dghost::cuda_status(cudaGetLastError());
+    return dghost::cuda_status(e);
 }
 
 dg_status dg_self_cond_pe(const void* logits, dg_dtype dtype, int64_t ld, const float* lse,

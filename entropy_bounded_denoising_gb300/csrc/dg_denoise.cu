@@ -43,7 +43,8 @@ namespace {
 constexpr int kK1Warps = 8;                        // consumer warps
 constexpr int kK1Threads = (kK1Warps + 1) * 32;    // + one producer warp
 constexpr int kSlots = 4;                          // ring of shared-memory slots
-constexpr uint32_t kChunkBytes = 16384;            // deferred sampling: bytes of a row per warp item
+constexpr uint32_t kChunkBytes = 16384;            // deferred sampling: largest bytes of a row per warp item
+constexpr uint32_t kChunkMin = 2048;               // and smallest (one batch of loads per lane)
 constexpr int kDWarps = 8;                         // deferred sampling: warps per CTA
 constexpr int kDBatch = 4;                         // 16-byte loads in flight per lane
 constexpr uint32_t kPieceBytes = 16384;            // bytes per slot
@@ -675,7 +676,8 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
 
 // ------------------------------------------------------------------------------------
 // Deferred sampling: the Gumbel-max samples of the listed accepted rows.  Work items are
-// (list entry, 16 KB chunk of its row), taken one per warp in a grid-stride loop; a lane
+// (list entry, chunk of its row), taken one per warp in a grid-stride loop; chunks are 16 KB,
+// or shorter (down to 2 KB) when the listed rows are too few to give every warp two; a lane
 // loads kDBatch 16-byte vectors at a time straight from global memory and draws the noise
 // only for 4-entry groups whose largest y + G_max reaches the bound m / T - kGumbelLow (m
 // the row's largest logit) or the warp's best so far.  A chunk's winner joins the row's
@@ -695,16 +697,20 @@ __global__ void __launch_bounds__(kDWarps * 32, 3) k1_sample_listed(
     constexpr int VN = Vec<DT>::N;
     constexpr int ES = DT == 0 ? 2 : 4;
     constexpr int GPV = VN / 4;
-    constexpr int kChunkElems = (int)(kChunkBytes / ES);
-    constexpr int kChunkVecs = (int)(kChunkBytes / 16);
-    static_assert(kChunkVecs % (32 * kDBatch) == 0, "a chunk splits into whole batches");
+    static_assert(kChunkMin % (32 * kDBatch * 16) == 0 && kChunkBytes % kChunkMin == 0, "whole batches per chunk");
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * kDWarps + (threadIdx.x >> 5);
     const int64_t nw = (int64_t)gridDim.x * kDWarps;
     dg::pdl_wait();
     dg::pdl_release();
     const int count = *ws.count;
-    const int cpr = (int)((V * ES + kChunkBytes - 1) / kChunkBytes);  // chunks per row
+    // chunk size: every warp computes the same one from the list length
+    const int64_t row_bytes = V * ES;
+    const int64_t want = ((int64_t)count * row_bytes) / (2 * nw);
+    const uint32_t chunk_bytes =
+        (uint32_t)min((int64_t)kChunkBytes, max((int64_t)kChunkMin, (want + kChunkMin - 1) / kChunkMin * kChunkMin));
+    const int kChunkElems = (int)(chunk_bytes / ES);
+    const int cpr = (int)((row_bytes + chunk_bytes - 1) / chunk_bytes);  // chunks per row
     const int64_t items = (int64_t)count * cpr;
     for (int64_t it = gw; it < items; it += nw) {
         const int w = (int)(it / cpr);
@@ -725,7 +731,7 @@ __global__ void __launch_bounds__(kDWarps * 32, 3) k1_sample_listed(
             const dg::PhiloxPre pre = dg::philox_pre((uint32_t)pos, (uint32_t)p.step,
                                                      dg::ctr_word3(seed, dg::kStreamGumbel), (uint32_t)seed,
                                                      p.request_id);
-            const uint4* src = reinterpret_cast<const uint4*>(logits + row * ld_bytes + (int64_t)chunk * kChunkBytes);
+            const uint4* src = reinterpret_cast<const uint4*>(logits + row * ld_bytes + (int64_t)chunk * chunk_bytes);
             const int e_lo = chunk * kChunkElems;
             const int n_el = (int)min((int64_t)kChunkElems, V - e_lo);
             const int nvec = (n_el + VN - 1) / VN;

@@ -598,19 +598,30 @@ __global__ void __launch_bounds__(256) k_fixup(const GemmArgs a) {
         const int row = qd / (out_cols / 4);
         const int col = (qd % (out_cols / 4)) * 4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), up = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < a.splits; ++s) {
-            const float* src = a.partial + (size_t)(s * T + t) * (BM * BN) + (size_t)row * BN + col;
-            const float4 v = *reinterpret_cast<const float4*>(src);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
-            if (gu) {
-                const float4 u = *reinterpret_cast<const float4*>(src + BN / 2);
-                up.x += u.x;
-                up.y += u.y;
-                up.z += u.z;
-                up.w += u.w;
+        // kU slices' loads in flight at once, added in slice order (read once: streaming loads)
+        constexpr int kU = 8;
+        for (int s0 = 0; s0 < a.splits; s0 += kU) {
+            float4 v[kU], u[kU];
+#pragma unroll
+            for (int j = 0; j < kU; ++j) {
+                if (s0 + j >= a.splits) continue;
+                const float* src = a.partial + (size_t)((s0 + j) * T + t) * (BM * BN) + (size_t)row * BN + col;
+                v[j] = __ldcs(reinterpret_cast<const float4*>(src));
+                if (gu) u[j] = __ldcs(reinterpret_cast<const float4*>(src + BN / 2));
+            }
+#pragma unroll
+            for (int j = 0; j < kU; ++j) {
+                if (s0 + j >= a.splits) continue;
+                acc.x += v[j].x;
+                acc.y += v[j].y;
+                acc.z += v[j].z;
+                acc.w += v[j].w;
+                if (gu) {
+                    up.x += u[j].x;
+                    up.y += u[j].y;
+                    up.z += u[j].z;
+                    up.w += u[j].w;
+                }
             }
         }
         int64_t r;
@@ -657,28 +668,37 @@ DG_DEVINL bool self_cond_on(const dg_canvas_params& p, const uint8_t* converged,
            !(converged && converged[c]) && p.temperature > 0.f;
 }
 
-// Compact list of the canvases whose feedback is computed this step (original order).
+// Compact list of the canvases whose feedback is computed this step (original order): per
+// chunk of blockDim.x canvases, warp ballots, an exclusive prefix over the warps' counts.
 __global__ void k_plan(const dg_canvas_params* __restrict__ params, const uint8_t* __restrict__ converged,
                        int64_t n, int32_t* __restrict__ plan) {
     dg::pdl_wait();
     dg::pdl_release();
-    __shared__ int count;
-    if (threadIdx.x == 0) count = 0;
-    __syncthreads();
+    __shared__ int warp_base[32];
+    __shared__ int total;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    int count = 0;  // canvases listed before this chunk (same in every thread)
     for (int64_t base = 0; base < n; base += blockDim.x) {
         const int64_t c = base + threadIdx.x;
         const bool on = c < n && self_cond_on(params[c], converged, c);
         const unsigned ballot = __ballot_sync(0xffffffffu, on);
-        // order-preserving compaction: one warp at a time
-        for (int wv = 0; wv < (int)(blockDim.x >> 5); ++wv) {
-            if ((int)(threadIdx.x >> 5) == wv) {
-                const int before = __popc(ballot & ((1u << (threadIdx.x & 31)) - 1u));
-                if (on) plan[1 + count + before] = (int32_t)c;
-                __syncwarp();
-                if ((threadIdx.x & 31) == 0) count += __popc(ballot);
+        if (lane == 0) warp_base[warp] = __popc(ballot);
+        __syncthreads();
+        if (warp == 0) {
+            const int v = lane < nwarps ? warp_base[lane] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
             }
-            __syncthreads();
+            if (lane < nwarps) warp_base[lane] = incl - v;
+            if (lane == 31) total = incl;
         }
+        __syncthreads();
+        if (on) plan[1 + count + warp_base[warp] + __popc(ballot & ((1u << lane) - 1u))] = (int32_t)c;
+        count += total;
+        __syncthreads();  // warp_base and total are rewritten by the next chunk
     }
     if (threadIdx.x == 0) plan[0] = count;
 }

@@ -703,17 +703,18 @@ __global__ void k_plan(const dg_canvas_params* __restrict__ params, const uint8_
     if (threadIdx.x == 0) plan[0] = count;
 }
 
-// Zero the feedback rows of canvases that get none this step.
+// Zero the feedback rows of canvases that get none this step: grid (CTAs per canvas, canvases),
+// 16-byte stores (d is a multiple of 8 and delta_emb 16-byte aligned).
 __global__ void k_zero_rows(const dg_canvas_params* __restrict__ params, const uint8_t* __restrict__ converged,
                             int32_t L, int32_t d, uint16_t* __restrict__ delta) {
     dg::pdl_wait();
     dg::pdl_release();
     const int64_t c = blockIdx.y;
     if (self_cond_on(params[c], converged, c)) return;
-    const int64_t total = (int64_t)L * d;
-    uint16_t* row = delta + c * total;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x)
-        row[i] = 0;
+    const int64_t vecs = (int64_t)L * d / 8;
+    uint4* row = reinterpret_cast<uint4*>(delta + c * (int64_t)L * d);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < vecs; i += (int64_t)gridDim.x * blockDim.x)
+        row[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1013,7 +1014,11 @@ dg_status dg_self_cond_prepare(const dg_canvas_params* params, const uint8_t* co
     cudaError_t e = dghost::launch_pdl(k_plan, dim3(1), dim3(1024), 0, st, params, converged, n_canvas, plan);
     dghost::count_launch();
     if (e != cudaSuccess) return DG_ERR_CUDA;
-    dim3 grid((unsigned)std::min<int64_t>(1024, ((int64_t)L * d + 255) / 256), (unsigned)n_canvas);
+    // about four CTAs per SM over all canvases (most of them exit at once when feedback is on)
+    const int P = std::max(1, dghost::sm_count());
+    const int64_t per_canvas = std::max<int64_t>(1, std::min<int64_t>(((int64_t)L * d / 8 + 255) / 256,
+                                                                      (4LL * P + n_canvas - 1) / n_canvas));
+    dim3 grid((unsigned)per_canvas, (unsigned)n_canvas);
     e = dghost::launch_pdl(k_zero_rows, grid, dim3(256), 0, st, params, converged, L, d, delta_emb);
     dghost::count_launch();
     return dghost::cuda_status(e);

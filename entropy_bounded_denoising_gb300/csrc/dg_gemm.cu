@@ -13,8 +13,9 @@
 //   warp 0      TMA producer: A and B tiles into a ring of shared-memory stages;
 //   warp 1      tcgen05.mma issuer (one elected thread) and TMEM owner;
 //   warps 2..5  epilogue: TMEM -> registers -> global (tcgen05.ld), one TMEM lane quarter each;
-//   warps 6..9  (softmax A only) transform: the logits tile landed by TMA is turned in place
-//               into P = exp2(x * log2e / T - lse * log2e) in bf16, so P never leaves the SM.
+//   warps 6..13 (softmax A only) transform: the logits tile landed by TMA is turned in place
+//               into P = exp2(x * log2e / T - lse * log2e) in bf16, so P never leaves the SM;
+//               two groups of four warps take the stages in turn.
 // Work items are (k-slice, n-tile, m-tile) with the m-tile fastest; item w runs on CTA
 // w mod P in round w / P.  All CTAs of a round therefore stream the same k-range, and the
 // B tile (embedding rows) and A tile (logit rows) they share are read from HBM once and
@@ -78,7 +79,7 @@ struct Cfg {
     static constexpr int kAccCols = BN;                      // fp32 accumulator columns
     static constexpr int kNAcc = (BN <= 256) ? 2 : 1;        // double-buffered when it fits
     static constexpr int kTmemCols = kAccCols * kNAcc;       // 256 or 512
-    static constexpr int kXformThreads = 256;                // two warpgroups, half a tile row each
+    static constexpr int kXformThreads = 256;                // DG_XFORM_GROUPS groups taking stages in turn
     static constexpr int kXformWarps = kXformThreads / 32;
     static constexpr int kThreads = kXform ? 192 + kXformThreads : 192;
     static constexpr int kATileBytes = BM * BK * 2;
@@ -168,6 +169,12 @@ DG_DEVINL float gelu_tanh(float z) {
     const float k = 0.7978845608028654f;  // sqrt(2 / pi)
     return 0.5f * z * (1.f + tanhf(k * (z + 0.044715f * z * z * z)));
 }
+
+// Groups of softmax-transform threads that take the P.E stages in turn (2: measured fastest
+// against 1, 4 and 8 on the batched workload; see the transform loop).
+#ifndef DG_XFORM_GROUPS
+#define DG_XFORM_GROUPS 2
+#endif
 
 constexpr int kMaxStages = 12;
 
@@ -266,9 +273,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             dg::mbar_init(&sh.full[s], 1);
-            // pair: one arrival per transform warp of both CTAs, in the first CTA's barrier
+            // pair: one arrival per transform warp of the stage's group in both CTAs, in the
+            // first CTA's barrier
             // (without a transform: the second CTA's relay, once its own stage has landed)
-            dg::mbar_init(&sh.xform[s], PAIR ? (C::kXform ? 2 * C::kXformWarps : 1) : (C::kXform ? C::kXformThreads : 1));
+            dg::mbar_init(&sh.xform[s], PAIR ? (C::kXform ? 2 * (C::kXformWarps / DG_XFORM_GROUPS) : 1)
+                                              : (C::kXform ? C::kXformThreads / DG_XFORM_GROUPS : 1));
             dg::mbar_init(&sh.empty[s], PAIR ? 1u : (uint32_t)cm);  // one release per CTA of the cluster
         }
         for (int i = 0; i < C::kNAcc; ++i) {
@@ -496,62 +505,80 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     } else {
         // ------------------------------------------------ softmax transform (warps 6..13)
         if (C::kXform) {
-            const int t = (threadIdx.x - 192) & (BM - 1);    // tile row handled by this thread
-            const int half = (threadIdx.x - 192) / BM;        // which half of the row's chunks
+            // kXG groups of transform threads take the stages in turn (stage it goes to group
+            // it % kXG), so each group has kXG stages' worth of MMA time for one stage's chain
+            // (barrier wait, shared loads, exponentials, stores, proxy fence, arrival); a
+            // thread converts kRows whole tile rows of its group's stages
+            constexpr int kXG = DG_XFORM_GROUPS;
+            constexpr int kGT = C::kXformThreads / kXG;       // threads per group
+            constexpr int kRows = BM / kGT;                    // tile rows per thread
+            static_assert(kGT >= 32 && kGT <= BM && BM % kGT == 0, "whole warps, whole rows per group");
+            const int xt = threadIdx.x - 192;
+            const int grp = xt / kGT;
+            const int t0 = xt % kGT;
             uint32_t it = 0;
             for (int64_t G = cid; G < n_groups && !aborted_warp(sh); G += ncl) {
                 const Item im = decode(a, mt, cm, rank, G);
                 const int cz = canvas_of(a, im.m_load);
-                const int pos = (im.m_load % a.tpc) * BM + t;
                 const dg_canvas_params pr = a.params[cz];
                 const float kx = kLog2e / pr.temperature;
-                const float lb = (pos < a.L) ? a.lse[(int64_t)cz * a.L + pos] * kLog2e : 0.f;
+                float lbs[kRows];
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) {
+                    const int pos = (im.m_load % a.tpc) * BM + t0 + r * kGT;
+                    lbs[r] = (pos < a.L) ? a.lse[(int64_t)cz * a.L + pos] * kLog2e : 0.f;
+                }
                 bool ok = true;
                 for (int kb = im.kb_lo; kb < im.kb_hi; ++kb, ++it) {
+                    if ((int)(it % kXG) != grp) continue;
                     const int s = (int)(it % C::STAGES);
                     const uint32_t ph = (it / C::STAGES) & 1u;
                     // every lane polls; the outcome is made warp-uniform (the warp arrives as one)
                     if (!__all_sync(0xffffffffu, dg::mbar_wait(&sh.full[s], ph))) { ok = false; break; }
                     unsigned char* st = smem + (size_t)s * C::kStageBytes;
-                    unsigned char* rowA = st + t * (C::BK * 2);
                     const int64_t kbase = (int64_t)kb * C::BK;
                     const bool tail = kbase + C::BK > a.K;
-                    // one tile row = BK bf16 = BK/8 16-byte chunks; the swizzle permutes chunks
-                    // within the row, so chunk c of the row sits at c ^ ((t >> sh) & mask)
-                    constexpr int kChunks = C::BK / 8;
-                    constexpr int kHalf = kChunks / 2;
-                    const int sw = (C::kASwizzle == 128) ? (t & 7) : ((t >> 1) & 3);
 #pragma unroll
-                    for (int cc = 0; cc < kHalf; ++cc) {
-                        const int c = half * kHalf + cc;
-                        const int pc = c ^ sw;
-                        float x[8];
-                        if (C::kAMode == A_SOFTMAX_BF16) {
-                            const uint4 qv = *reinterpret_cast<const uint4*>(rowA + pc * 16);
-                            x[0] = __uint_as_float(qv.x << 16); x[1] = __uint_as_float(qv.x & 0xffff0000u);
-                            x[2] = __uint_as_float(qv.y << 16); x[3] = __uint_as_float(qv.y & 0xffff0000u);
-                            x[4] = __uint_as_float(qv.z << 16); x[5] = __uint_as_float(qv.z & 0xffff0000u);
-                            x[6] = __uint_as_float(qv.w << 16); x[7] = __uint_as_float(qv.w & 0xffff0000u);
-                        } else {
-                            // fp32 staging row: 32 floats = 128 bytes, 128-byte swizzle
-                            const unsigned char* rowF = st + C::kATileBytes + C::kBTileBytes + t * 128;
-                            const float4 f0 = *reinterpret_cast<const float4*>(rowF + (((2 * c) ^ (t & 7)) * 16));
-                            const float4 f1 = *reinterpret_cast<const float4*>(rowF + (((2 * c + 1) ^ (t & 7)) * 16));
-                            x[0] = f0.x; x[1] = f0.y; x[2] = f0.z; x[3] = f0.w;
-                            x[4] = f1.x; x[5] = f1.y; x[6] = f1.z; x[7] = f1.w;
+                    for (int r = 0; r < kRows; ++r) {
+                        const int t = t0 + r * kGT;
+                        const float lb = lbs[r];
+                        unsigned char* rowA = st + t * (C::BK * 2);
+                        // one tile row = BK bf16 = BK/8 16-byte chunks; the swizzle permutes chunks
+                        // within the row, so chunk c of the row sits at c ^ ((t >> sh) & mask)
+                        constexpr int kChunks = C::BK / 8;
+                        const int sw = (C::kASwizzle == 128) ? (t & 7) : ((t >> 1) & 3);
+#pragma unroll
+                        for (int cc = 0; cc < kChunks; ++cc) {
+                            const int c = cc;
+                            const int pc = c ^ sw;
+                            float x[8];
+                            if (C::kAMode == A_SOFTMAX_BF16) {
+                                const uint4 qv = *reinterpret_cast<const uint4*>(rowA + pc * 16);
+                                x[0] = __uint_as_float(qv.x << 16); x[1] = __uint_as_float(qv.x & 0xffff0000u);
+                                x[2] = __uint_as_float(qv.y << 16); x[3] = __uint_as_float(qv.y & 0xffff0000u);
+                                x[4] = __uint_as_float(qv.z << 16); x[5] = __uint_as_float(qv.z & 0xffff0000u);
+                                x[6] = __uint_as_float(qv.w << 16); x[7] = __uint_as_float(qv.w & 0xffff0000u);
+                            } else {
+                                // fp32 staging row: 32 floats = 128 bytes, 128-byte swizzle
+                                const unsigned char* rowF = st + C::kATileBytes + C::kBTileBytes + t * 128;
+                                const float4 f0 = *reinterpret_cast<const float4*>(rowF + (((2 * c) ^ (t & 7)) * 16));
+                                const float4 f1 = *reinterpret_cast<const float4*>(rowF + (((2 * c + 1) ^ (t & 7)) * 16));
+                                x[0] = f0.x; x[1] = f0.y; x[2] = f0.z; x[3] = f0.w;
+                                x[4] = f1.x; x[5] = f1.y; x[6] = f1.z; x[7] = f1.w;
+                            }
+                            float pz[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) pz[j] = ex2(fmaf(x[j], kx, -lb));
+                            if (tail) {
+#pragma unroll
+                                for (int j = 0; j < 8; ++j)
+                                    if (kbase + c * 8 + j >= a.K) pz[j] = 0.f;
+                            }
+                            *reinterpret_cast<uint4*>(rowA + pc * 16) =
+                                make_uint4(pack_bf16x2(pz[0], pz[1]), pack_bf16x2(pz[2], pz[3]),
+                                           pack_bf16x2(pz[4], pz[5]), pack_bf16x2(pz[6], pz[7]));
                         }
-                        float pz[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) pz[j] = ex2(fmaf(x[j], kx, -lb));
-                        if (tail) {
-#pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                if (kbase + c * 8 + j >= a.K) pz[j] = 0.f;
-                        }
-                        *reinterpret_cast<uint4*>(rowA + pc * 16) =
-                            make_uint4(pack_bf16x2(pz[0], pz[1]), pack_bf16x2(pz[2], pz[3]),
-                                       pack_bf16x2(pz[4], pz[5]), pack_bf16x2(pz[6], pz[7]));
-                    }
+                    }  // rows
                     dg::fence_proxy_async_smem();  // make the generic-proxy writes visible to tcgen05
                     if (PAIR) {
                         __syncwarp();

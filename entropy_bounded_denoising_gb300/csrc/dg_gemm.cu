@@ -566,9 +566,24 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                                 x[0] = f0.x; x[1] = f0.y; x[2] = f0.z; x[3] = f0.w;
                                 x[4] = f1.x; x[5] = f1.y; x[6] = f1.z; x[7] = f1.w;
                             }
+                            // exponent arguments two at a time (fma.rn.f32x2: the same single
+                            // rounding per element as fmaf)
                             float pz[8];
+                            {
+                                uint64_t kk, bb;
+                                asm("mov.b64 %0, {%1, %1};" : "=l"(kk) : "f"(kx));
+                                asm("mov.b64 %0, {%1, %1};" : "=l"(bb) : "f"(-lb));
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) pz[j] = ex2(fmaf(x[j], kx, -lb));
+                                for (int j = 0; j < 8; j += 2) {
+                                    uint64_t xx, rr;
+                                    asm("mov.b64 %0, {%1, %2};" : "=l"(xx) : "f"(x[j]), "f"(x[j + 1]));
+                                    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rr) : "l"(xx), "l"(kk), "l"(bb));
+                                    float lo, hi;
+                                    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(rr));
+                                    pz[j] = ex2(lo);
+                                    pz[j + 1] = ex2(hi);
+                                }
+                            }
                             if (tail) {
 #pragma unroll
                                 for (int j = 0; j < 8; ++j)

@@ -110,3 +110,32 @@ def test_self_cond_logits(dtype, V, ld, d, h, L):
         ref = oracle.self_cond_rows(hx[c], np.full(L, p["temperature"][c], np.float64), *bits, V=V)
         err = delta_rel_err(got[c], ref)
         assert err.max() <= DELTA_RTOL, (c, err.max())
+
+
+@pytest.mark.parametrize("n,L,V,d,h", [(3, 256, 32768, 1024, 2048), (1, 200, 5003, 192, 320)])
+def test_feedback_is_deterministic(n, L, V, d, h):
+    """The feedback depends only on its inputs: two runs give bit-identical delta_emb (the
+    split-K partials are added in slice order by one thread per column; no float atomics).
+    A race in the GEMM engine's pipeline would show here as a bit difference."""
+    rng = np.random.default_rng(n + L)
+    ld = (V + 7) // 8 * 8  # rows 16-byte aligned
+    x = synth.logits(n, L, V, seed=n * 7 + L, step=1, scale=(0.5, 12.0), spike_frac=0.1, ld=ld, device=DEV)
+    (E, Wg, Wu, Wd), _ = _weights(V, d, h, seed=3)
+    E, Wg, Wu, Wd = (t.to(DEV) for t in (E, Wg, Wu, Wd))
+    p = {"temperature": rng.uniform(0.5, 1.5, n).astype(np.float32), "beta": np.full(n, 8.0, np.float32),
+         "tau": np.full(n, 0.3, np.float32), "k": np.full(n, 2, np.int32), "max_steps": np.full(n, 64, np.int32),
+         "min_accept": np.ones(n, np.int32), "step": np.ones(n, np.int32),
+         "request_id": np.arange(n, dtype=np.uint32), "flags": np.full(n, dg.DG_ACTIVE | dg.DG_SELF_COND, np.uint32)}
+    pt = dg.params_tensor(p, DEV)
+    b = StepBuffers.make(n, L, DEV)
+    run_step(x, pt, 5, b, V=V)
+    ws = torch.empty(dg.dg_self_cond_workspace_bytes(n, L, d, h), dtype=torch.uint8, device=DEV)
+    outs = []
+    for _ in range(2):
+        delta = torch.full((n, L, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+        dg.dg_self_cond_logits(x, b.lse, pt, b.converged, E, Wg, Wu, Wd, delta, ws, V=V)
+        torch.cuda.synchronize()
+        outs.append(delta.view(torch.int16).cpu())
+    assert dg.dg_get_device_status() == 0
+    assert torch.equal(outs[0], outs[1])
+    assert torch.isfinite(outs[0].view(torch.bfloat16).float()).all()

@@ -62,7 +62,50 @@ struct GemmArgs {
     int32_t m_valid;        // valid output rows (plain GEMMs)
     float* partial;         // [items][BM * BN] when splits > 1
     unsigned* status;
+    // dyn_splits = 1: the k-slices are chosen on the device from the active m-tiles (the host
+    // only knows an upper bound when a plan lists the rows), the same way in the GEMM and its
+    // fix-up, from these values of the host's plan
+    int32_t dyn_splits;
+    int32_t cm_plan;        // CTAs per cluster
+    int32_t clusters;       // concurrent clusters
+    int32_t min_slice;      // k-blocks
+    int64_t max_slots;      // partial tiles the workspace holds
+    int32_t split_below;    // split only below this round efficiency (percent)
 };
+
+// k-slices: the fewest that keep the rounds at least 95 % full, with slices of at least
+// `min_slice` k-blocks so that the partial tiles stay cheap next to the MMA work.  Round
+// efficiencies items / (rounds * P) are compared as exact fractions (integer arithmetic:
+// host and device agree, and GB300's slow FP64 stays out of every CTA's prologue).
+__host__ __device__ inline int choose_splits(int64_t T, int k_blocks, int P, int min_slice) {
+    int best = 1;
+    int64_t best_num = 0, best_den = 1;
+    for (int s = 1; s <= 32; ++s) {
+        if (s > 1 && k_blocks / s < min_slice) break;
+        const int64_t items = T * s;  // < 2^31 for every supported shape: 32-bit division
+        const int64_t den = (int64_t)(((uint32_t)items + (uint32_t)P - 1u) / (uint32_t)P) * P;
+        if (items * best_den > best_num * den) {
+            best_num = items;
+            best_den = den;
+            best = s;
+        }
+        if (items * 100 >= den * 95) break;
+    }
+    return best;
+}
+
+// The k-slices for `mt` m-tiles (`per_split` work groups per slice): per the plan's rule
+// (round efficiency below split_below percent, within max_slots partial tiles).
+__host__ __device__ inline int plan_splits(int64_t per_split, int64_t mt, int n_tiles, int k_blocks, int clusters,
+                                           int min_slice, int64_t max_slots, int split_below) {
+    if (per_split <= 0 || clusters <= 0) return 1;
+    const int64_t den1 = (int64_t)(((uint32_t)per_split + (uint32_t)clusters - 1u) / (uint32_t)clusters) * clusters;
+    int splits = per_split * 100 < (int64_t)split_below * den1
+                     ? choose_splits(per_split, k_blocks, clusters, min_slice < 1 ? 1 : min_slice)
+                     : 1;
+    while (splits > 1 && mt * n_tiles * splits > max_slots) --splits;
+    return splits;
+}
 
 // PAIR_: the CTA pair of a 2-CTA cluster computes one 256-row tile with cta_group::2 MMAs;
 // each CTA then holds half of every 256-column B slab (for the gate/up tile: the first CTA
@@ -128,11 +171,18 @@ DG_DEVINL int active_m_tiles(const GemmArgs& a) {
 // Work is cut into groups of `cm` consecutive m-tiles sharing one (k-slice, n-tile); the cm
 // CTAs of a cluster run a group together (rank r takes m-tile mg * cm + r) so that they can
 // share the B tile.  Groups are ordered (k-slice, n-tile, m-group), m fastest.
-DG_DEVINL int64_t group_count(const GemmArgs& a, int mt, int cm) {
-    return (int64_t)a.splits * a.n_tiles * ((mt + cm - 1) / cm);
+DG_DEVINL int64_t group_count(const GemmArgs& a, int mt, int cm, int splits) {
+    return (int64_t)splits * a.n_tiles * ((mt + cm - 1) / cm);
 }
 
-DG_DEVINL Item decode(const GemmArgs& a, int mt, int cm, int rank, int64_t G) {
+// The launch's k-slices for `mt` active m-tiles.
+DG_DEVINL int active_splits(const GemmArgs& a, int mt) {
+    if (!a.dyn_splits) return a.splits;
+    const int64_t per_split = (int64_t)a.n_tiles * ((mt + a.cm_plan - 1) / a.cm_plan);
+    return plan_splits(per_split, mt, a.n_tiles, a.k_blocks, a.clusters, a.min_slice, a.max_slots, a.split_below);
+}
+
+DG_DEVINL Item decode(const GemmArgs& a, int mt, int cm, int rank, int64_t G, int splits) {
     const int64_t mgc = (mt + cm - 1) / cm;
     const int64_t per_s = (int64_t)a.n_tiles * mgc;
     const int s = (int)(G / per_s);
@@ -142,8 +192,8 @@ DG_DEVINL Item decode(const GemmArgs& a, int mt, int cm, int rank, int64_t G) {
     it.m = (int)(rem % mgc) * cm + rank;
     it.valid = it.m < mt;
     it.m_load = it.valid ? it.m : mt - 1;
-    it.kb_lo = (int)((int64_t)s * a.k_blocks / a.splits);
-    it.kb_hi = (int)((int64_t)(s + 1) * a.k_blocks / a.splits);
+    it.kb_lo = (int)((int64_t)s * a.k_blocks / splits);
+    it.kb_hi = (int)((int64_t)(s + 1) * a.k_blocks / splits);
     it.w = (int64_t)s * mt * a.n_tiles + (int64_t)it.n * mt + it.m;
     return it;
 }
@@ -186,6 +236,7 @@ struct __align__(8) GemmShared {
     uint64_t acce[2];
     uint32_t tmem_base;
     int abort_flag;
+    int splits;  // k-slices of this launch
 };
 
 DG_DEVINL bool aborted(const GemmShared& sh) { return *(volatile const int*)&sh.abort_flag != 0; }
@@ -304,7 +355,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     dg::pdl_wait();
     dg::pdl_release();
     const int mt = active_m_tiles(a);
-    const int64_t n_groups = mt > 0 ? group_count(a, mt, cm) : 0;
+    if (threadIdx.x == 0) sh.splits = active_splits(a, mt);  // once per CTA, shared
+    __syncthreads();
+    const int splits = sh.splits;
+    const int64_t n_groups = mt > 0 ? group_count(a, mt, cm, splits) : 0;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -314,7 +368,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (C::kBMode == B_KMAJOR_GATEUP) dg::prefetch_tmap(&tmB1);
             uint32_t it = 0;
             for (int64_t G = cid; G < n_groups && !aborted(sh); G += ncl) {
-                const Item im = decode(a, mt, cm, rank, G);
+                const Item im = decode(a, mt, cm, rank, G, splits);
                 int cz = 0, crow = 0;
                 if (C::kXform) {
                     cz = canvas_of(a, im.m_load);
@@ -383,7 +437,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int64_t G = cid; G < n_groups && ok && !aborted(sh); G += ncl) {
-                const Item im = decode(a, mt, cm, rank, G);
+                const Item im = decode(a, mt, cm, rank, G, splits);
                 for (int kb = im.kb_lo; kb < im.kb_hi; ++kb, ++it) {
                     const int s = (int)(it % C::STAGES);
                     if (!dg::mbar_wait(&sh.full[s], (it / C::STAGES) & 1u)) { ok = false; break; }
@@ -399,7 +453,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             constexpr uint32_t idesc = (C::kBMode == B_MNMAJOR) ? idesc_mn : idesc_k;
             uint32_t it = 0, acc_it = 0;
             for (int64_t G = cid; G < n_groups && !aborted(sh); G += ncl, ++acc_it) {
-                const Item im = decode(a, mt, cm, rank, G);
+                const Item im = decode(a, mt, cm, rank, G, splits);
                 const int ab = (int)(acc_it % C::kNAcc);
                 const uint32_t aph = (acc_it / C::kNAcc) & 1u;
                 if (!dg::mbar_wait(&sh.acce[ab], aph ^ 1u)) {
@@ -463,7 +517,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const int row = q * 32 + lane;
         uint32_t acc_it = 0;
         for (int64_t G = cid; G < n_groups && !aborted_warp(sh); G += ncl, ++acc_it) {
-            const Item im = decode(a, mt, cm, rank, G);
+            const Item im = decode(a, mt, cm, rank, G, splits);
             const int ab = (int)(acc_it % C::kNAcc);
             const uint32_t aph = (acc_it / C::kNAcc) & 1u;
             if (!dg::mbar_wait_warp(&sh.accf[ab], aph, 256)) { do_abort(sh, a.status); break; }
@@ -471,7 +525,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * C::kAccCols);
             if (!im.valid) {
                 // padding member of the group: nothing to store
-            } else if (a.splits > 1) {
+            } else if (splits > 1) {
                 float* dst = a.partial + (size_t)im.w * (BM * C::BN) + (size_t)row * C::BN;
                 for (int ch = 0; ch < C::BN / 32; ++ch) {
                     float v[32];
@@ -518,7 +572,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             const int t0 = xt % kGT;
             uint32_t it = 0;
             for (int64_t G = cid; G < n_groups && !aborted_warp(sh); G += ncl) {
-                const Item im = decode(a, mt, cm, rank, G);
+                const Item im = decode(a, mt, cm, rank, G, splits);
                 const int cz = canvas_of(a, im.m_load);
                 const dg_canvas_params pr = a.params[cz];
                 const float kx = kLog2e / pr.temperature;
@@ -627,6 +681,11 @@ __global__ void __launch_bounds__(256) k_fixup(const GemmArgs a) {
     dg::pdl_wait();
     dg::pdl_release();
     const int mt = active_m_tiles(a);
+    __shared__ int splits_sh;
+    if (threadIdx.x == 0) splits_sh = active_splits(a, mt);  // once per CTA, shared
+    __syncthreads();
+    const int splits = splits_sh;
+    if (splits <= 1) return;  // the device's plan did not split K: nothing to add
     const int64_t T = (int64_t)mt * a.n_tiles;
     const int64_t t = blockIdx.x;
     if (t >= T) return;
@@ -642,18 +701,18 @@ __global__ void __launch_bounds__(256) k_fixup(const GemmArgs a) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), up = make_float4(0.f, 0.f, 0.f, 0.f);
         // kU slices' loads in flight at once, added in slice order (read once: streaming loads)
         constexpr int kU = 8;
-        for (int s0 = 0; s0 < a.splits; s0 += kU) {
+        for (int s0 = 0; s0 < splits; s0 += kU) {
             float4 v[kU], u[kU];
 #pragma unroll
             for (int j = 0; j < kU; ++j) {
-                if (s0 + j >= a.splits) continue;
+                if (s0 + j >= splits) continue;
                 const float* src = a.partial + (size_t)((s0 + j) * T + t) * (BM * BN) + (size_t)row * BN + col;
                 v[j] = __ldcs(reinterpret_cast<const float4*>(src));
                 if (gu) u[j] = __ldcs(reinterpret_cast<const float4*>(src + BN / 2));
             }
 #pragma unroll
             for (int j = 0; j < kU; ++j) {
-                if (s0 + j >= a.splits) continue;
+                if (s0 + j >= splits) continue;
                 acc.x += v[j].x;
                 acc.y += v[j].y;
                 acc.z += v[j].z;
@@ -777,29 +836,13 @@ using DownSingle = Cfg<A_TMA, B_KMAJOR, 256, 64, 4>;  // plain GEMMs (K-major B)
 constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// k-slices: the fewest that keep the rounds at least 95 % full, with slices of at least
-// `min_slice` k-blocks so that the partial tiles stay cheap next to the MMA work.
-int choose_splits(int64_t T, int k_blocks, int P, int min_slice) {
-    int best = 1;
-    double best_eff = 0.0;
-    for (int s = 1; s <= 32; ++s) {
-        if (s > 1 && k_blocks / s < min_slice) break;
-        const int64_t items = T * s;
-        const int64_t rounds = (items + P - 1) / P;
-        const double eff = (double)items / (double)(rounds * P);
-        if (eff > best_eff + 1e-9) {
-            best_eff = eff;
-            best = s;
-        }
-        if (eff >= 0.95) break;
-    }
-    return best;
-}
-
 struct LaunchPlan {
     int cm;        // CTAs per cluster
     int clusters;  // concurrent clusters (persistent grid = clusters * cm CTAs)
-    int splits;    // k-slices
+    int splits;    // k-slices (for the host's m-tile count)
+    int min_slice;
+    int64_t max_slots;
+    int split_below;  // percent
 };
 
 // Cluster size, persistent grid and k-slices for a GEMM.  The N-major B tile (embedding rows)
@@ -810,7 +853,7 @@ struct LaunchPlan {
 // least `min_slice` k-blocks, and only when the unsplit work would fill less than
 // `split_below` of the clusters' last round.
 template <class C>
-bool plan_gemm(const GemmArgs& a, int64_t max_slots, LaunchPlan* pl, int min_slice = 256, double split_below = 1.01) {
+bool plan_gemm(const GemmArgs& a, int64_t max_slots, LaunchPlan* pl, int min_slice = 256, int split_below = 101) {
     auto kern = k_gemm<C>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
         return false;
@@ -842,10 +885,11 @@ bool plan_gemm(const GemmArgs& a, int64_t max_slots, LaunchPlan* pl, int min_sli
     }
     if (cm == 1) clusters = P;
     const int64_t per_split = (int64_t)a.n_tiles * ((a.m_tiles + cm - 1) / cm);
-    const int64_t rounds1 = (per_split + clusters - 1) / clusters;
-    const double eff1 = (double)per_split / (double)(rounds1 * clusters);
-    int splits = eff1 < split_below ? choose_splits(per_split, a.k_blocks, clusters, std::max(1, min_slice)) : 1;
-    while (splits > 1 && (int64_t)a.m_tiles * a.n_tiles * splits > max_slots) --splits;
+    const int splits = plan_splits(per_split, a.m_tiles, a.n_tiles, a.k_blocks, clusters, min_slice, max_slots,
+                                   split_below);
+    pl->min_slice = min_slice;
+    pl->max_slots = max_slots;
+    pl->split_below = split_below;
     pl->cm = cm;
     pl->clusters = clusters;
     pl->splits = splits;
@@ -864,7 +908,10 @@ dg_status launch_gemm(const void* tmA, const void* tmB0, const void* tmB1, const
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // the kernel waits after its prologue
     attr[1].val.programmaticStreamSerializationAllowed = 1;
-    const int64_t groups = (int64_t)a.splits * a.n_tiles * ((a.m_tiles + pl.cm - 1) / pl.cm);
+    // with the k-slices chosen on the device the work may exceed the host's count: the full
+    // persistent grid (CTAs without work leave after their prologue)
+    const int64_t groups = a.dyn_splits ? (int64_t)pl.clusters
+                                        : (int64_t)a.splits * a.n_tiles * ((a.m_tiles + pl.cm - 1) / pl.cm);
     const int64_t ncl = std::max<int64_t>(1, std::min<int64_t>(pl.clusters, groups));
     cfg.gridDim = dim3((unsigned)(ncl * pl.cm), 1, 1);
     cfg.blockDim = dim3(C::kThreads, 1, 1);
@@ -876,7 +923,7 @@ dg_status launch_gemm(const void* tmA, const void* tmB0, const void* tmB1, const
                                        *static_cast<const CUtensorMap*>(tmB0), *static_cast<const CUtensorMap*>(tmB1), a);
     dghost::count_launch();
     if (e != cudaSuccess) return DG_ERR_CUDA;
-    if (a.splits > 1) {
+    if (a.splits > 1 || a.dyn_splits) {  // a device plan that does not split leaves the fix-up idle
         const int64_t T = (int64_t)a.m_tiles * a.n_tiles;
         // spread each tile over enough CTAs to fill the GPU a few times
         const int P = dghost::sm_count();
@@ -890,10 +937,17 @@ dg_status launch_gemm(const void* tmA, const void* tmB0, const void* tmB1, const
 // Plan, then launch, with the planned k-slices.
 template <class C>
 dg_status plan_and_launch(const void* tmA, const void* tmB0, const void* tmB1, GemmArgs a, int64_t max_slots,
-                          cudaStream_t stream, int min_slice = 256, double split_below = 1.01) {
+                          cudaStream_t stream, int min_slice = 256, int split_below = 101) {
     LaunchPlan pl;
     if (!plan_gemm<C>(a, max_slots, &pl, min_slice, split_below)) return DG_ERR_CUDA;
     a.splits = pl.splits;
+    if (a.dyn_splits) {  // the device re-plans for the m-tiles actually active
+        a.cm_plan = pl.cm;
+        a.clusters = pl.clusters;
+        a.min_slice = pl.min_slice;
+        a.max_slots = pl.max_slots;
+        a.split_below = pl.split_below;
+    }
     return launch_gemm<C>(tmA, tmB0, tmB1, a, pl, stream);
 }
 
@@ -984,7 +1038,7 @@ dg_status run_mlp(const uint16_t* pe, uint16_t* hmid, int64_t rows, int32_t d, i
     g.partial = partial;
     g.status = dghost::status_word();
     const int64_t mlp_slots = partial ? 2 * pe_slots : 0;
-    dg_status s = plan_and_launch<GateUp>(t1.a, t1.b0, t1.b1, g, mlp_slots, stream, kMinSliceK / 64, 0.6);
+    dg_status s = plan_and_launch<GateUp>(t1.a, t1.b0, t1.b1, g, mlp_slots, stream, kMinSliceK / 64, 60);
     if (s != DG_OK) return s;
 
     if (!tmap_2d(t2.a, 0, hmid, h, rows, h, 64, BM, 128)) return DG_ERR_CUDA;
@@ -999,7 +1053,7 @@ dg_status run_mlp(const uint16_t* pe, uint16_t* hmid, int64_t rows, int32_t d, i
     q.n_valid = d;
     q.m_valid = m_valid_rows;
     (void)P;
-    return plan_and_launch<Down>(t2.a, t2.b0, t2.b0, q, mlp_slots, stream, kMinSliceK / 64, 0.6);
+    return plan_and_launch<Down>(t2.a, t2.b0, t2.b0, q, mlp_slots, stream, kMinSliceK / 64, 60);
 }
 
 dg_status check_weights(int64_t V, int32_t d, int32_t h, const uint16_t* E, const uint16_t* Wg, const uint16_t* Wu,
@@ -1106,6 +1160,7 @@ dg_status dg_self_cond_pe(const void* logits, dg_dtype dtype, int64_t ld, const 
     g.m_valid = (int32_t)lay.rows;
     g.partial = reinterpret_cast<float*>(ws + lay.partial);
     g.status = dghost::status_word();
+    g.dyn_splits = 1;  // the plan lists the canvases with feedback: the device knows how many
     const int64_t max_slots = pe_partial_slots(n_canvas, L, d, P);
     return dtype == DG_BF16 ? plan_and_launch<PEbf16>(tm.a, tm.b0, tm.b0, g, max_slots, st, kMinSliceK / bk)
                             : plan_and_launch<PEfp32>(tm.a, tm.b0, tm.b0, g, max_slots, st, kMinSliceK / bk);

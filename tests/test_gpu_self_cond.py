@@ -139,3 +139,34 @@ def test_feedback_is_deterministic(n, L, V, d, h):
     assert dg.dg_get_device_status() == 0
     assert torch.equal(outs[0], outs[1])
     assert torch.isfinite(outs[0].view(torch.bfloat16).float()).all()
+
+
+def test_feedback_with_few_active_canvases_replans_on_device():
+    """Six canvases of which only one has feedback on: the host plans P.E's k-slices for
+    twelve m-tiles, the device for the two that are active (a different split of K); the
+    feedback rows match the oracle and every other canvas's rows are zero."""
+    n, L, V, d, h = 6, 256, 32768, 1024, 2048
+    x = synth.logits(n, L, V, seed=61, step=1, scale=(0.5, 12.0), spike_frac=0.1, device=DEV)
+    (E, Wg, Wu, Wd), bits = _weights(V, d, h, seed=4)
+    E, Wg, Wu, Wd = (t.to(DEV) for t in (E, Wg, Wu, Wd))
+    p = {"temperature": np.full(n, 0.9, np.float32), "beta": np.full(n, 8.0, np.float32),
+         "tau": np.full(n, 0.3, np.float32), "k": np.full(n, 2, np.int32), "max_steps": np.full(n, 64, np.int32),
+         "min_accept": np.ones(n, np.int32), "step": np.ones(n, np.int32),
+         "request_id": np.arange(n, dtype=np.uint32), "flags": np.full(n, dg.DG_ACTIVE, np.uint32)}
+    p["flags"][2] |= dg.DG_SELF_COND
+    pt = dg.params_tensor(p, DEV)
+    b = StepBuffers.make(n, L, DEV)
+    run_step(x, pt, 9, b)
+    ws = torch.empty(dg.dg_self_cond_workspace_bytes(n, L, d, h), dtype=torch.uint8, device=DEV)
+    delta = torch.full((n, L, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    dg.dg_clear_device_status()
+    dg.dg_self_cond_logits(x, b.lse, pt, b.converged, E, Wg, Wu, Wd, delta, ws)
+    torch.cuda.synchronize()
+    assert dg.dg_get_device_status() == 0
+    dh = delta.float().cpu().numpy()
+    for c in range(n):
+        if c != 2:
+            assert (dh[c] == 0).all(), c
+    rows = [0, 77, 255]
+    ref = oracle.self_cond_rows(synth.host_logits(x[2, rows]), np.full(len(rows), 0.9), *bits, V=V)
+    assert delta_rel_err(dh[2, rows], ref).max() <= DELTA_RTOL

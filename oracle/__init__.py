@@ -74,6 +74,9 @@ def _load():
         lib.orc_bf16_round.restype = ctypes.c_uint16
         lib.orc_embed_canvas.argtypes = [P, i64, i64, P, i32, P, ctypes.c_float, P]
         lib.orc_commit.argtypes = [P, P, P, i64, i32, P, P, P, P]
+        lib.orc_bf16_round_f64.argtypes = [dbl]
+        lib.orc_bf16_round_f64.restype = ctypes.c_uint16
+        lib.orc_lm_head_logits.argtypes = [P, i64, i32, i64, P, i64, i64, P, i64, P, P, ctypes.c_int]
         lib.orc_max_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -317,3 +320,28 @@ def commit(converged, active, argmax, tokens, prev_argmax, stable_count) -> dict
     committed = np.zeros(n, np.uint8)
     lib.orc_commit(_ptr(cv), _ptr(ac), _ptr(am), n, L, _ptr(tok), _ptr(prev), _ptr(st), _ptr(committed))
     return {"tokens": tok, "prev_argmax": prev, "stable_count": st, "committed": committed}
+
+
+# ---------------------------------------------------------------- LM head
+def bf16_round_f64(x: float) -> int:
+    """The bf16 bit pattern nearest to a double (ties to even), rounded once."""
+    return int(_load().orc_bf16_round_f64(float(x)))
+
+
+def lm_head_logits(hidden_bf16, W_bf16, V: int | None = None, ld: int | None = None,
+                   exact: bool = False, n_threads: int = 0):
+    """logits = bf16(hidden . W^T): hidden [rows, d] and W [V, d] as bf16 bit patterns.
+    Returns the logits as bf16 bits [rows, ld] (columns past V are 0); with exact=True also
+    the unrounded fp64 dot products and sum_j |h_j W_vj|, each [rows, V]."""
+    lib = _load()
+    h = _c(hidden_bf16, np.uint16)
+    W = _c(W_bf16, np.uint16)
+    rows, d = h.shape
+    V = W.shape[0] if V is None else V
+    assert W.shape[1] == d and W.shape[0] >= V
+    ld = V if ld is None else ld
+    out = np.zeros((rows, ld), np.uint16)
+    ex = np.zeros((rows, V), np.float64) if exact else None
+    ab = np.zeros((rows, V), np.float64) if exact else None
+    lib.orc_lm_head_logits(_ptr(h), rows, d, d, _ptr(W), V, d, _ptr(out), ld, _ptr(ex), _ptr(ab), int(n_threads))
+    return (out, ex, ab) if exact else out

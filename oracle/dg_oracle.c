@@ -585,6 +585,69 @@ void orc_commit(const uint8_t* converged, const uint8_t* active, const int32_t* 
     }
 }
 
+/* ------------------------------------------------------------------------------- */
+/* LM head: the logits the denoise step reads are the model's output over the canvas */
+/* [DG], section "엔트로피 기반 디노이징" (each step runs the model on the canvas and   */
+/* reads the per-position distributions).  Reading (the pages do not describe the    */
+/* output layer): a plain linear map of the last hidden states,                      */
+/*   logits[r][v] = sum_j hidden[r][j] W[v][j],   W = [V][d] (row = vocabulary entry; */
+/* the input embedding table when the model ties the two, as the Gemma family does), */
+/* with no bias and no soft-capping.  The logits are stored as bf16, so their        */
+/* definition fixes the rounding: the dot product, rounded once to the nearest bf16, */
+/* ties to even.  The dot product is summed in fp64 (exact for small-integer          */
+/* operands; otherwise within d 2^-53 sum_j |hidden[r][j] W[v][j]|).                  */
+/* ------------------------------------------------------------------------------- */
+/* The bf16 bit pattern nearest to x (ties to even), from x itself: no intermediate   */
+/* fp32 rounding.  bf16 keeps 8 significant bits down to 2^-126 and a fixed quantum   */
+/* of 2^-133 below; magnitudes that round past (2 - 2^-7) 2^127 become infinite.      */
+uint16_t orc_bf16_round_f64(double x)
+{
+    if (isnan(x)) return (uint16_t)0x7fc0u;
+    uint16_t sign = signbit(x) ? (uint16_t)0x8000u : (uint16_t)0u;
+    double a = fabs(x);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return (uint16_t)(sign | 0x7f80u);
+    int e;
+    (void)frexp(a, &e);            /* a = m 2^e with m in [0.5, 1) */
+    int q = e - 8;                 /* exponent of the quantum at a's binade */
+    if (q < -133) q = -133;
+    /* nearbyint rounds to nearest, ties to even (the default rounding mode) */
+    double r = ldexp(nearbyint(ldexp(a, -q)), q);
+    if (r > 0x1.fep127) return (uint16_t)(sign | 0x7f80u);
+    float f = (float)r;            /* exact: r has at most 8 significant bits */
+    uint32_t b;
+    memcpy(&b, &f, sizeof b);
+    return (uint16_t)(sign | (uint16_t)(b >> 16));
+}
+
+/* logits (bf16 bits) [n_rows][ld] from hidden [n_rows][ldh] and W [V][ldw], both bf16 */
+/* bits; optionally the unrounded dot products `exact` and sum_j |h_j W_vj| `abssum`  */
+/* ([n_rows][V] each, may be NULL).                                                   */
+void orc_lm_head_logits(const uint16_t* hidden, int64_t n_rows, int32_t d, int64_t ldh,
+                        const uint16_t* W, int64_t V, int64_t ldw, uint16_t* logits, int64_t ld,
+                        double* exact, double* abssum, int n_threads)
+{
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+    #pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        for (int64_t v = 0; v < V; ++v) {
+            double s = 0.0, sa = 0.0;
+            for (int32_t j = 0; j < d; ++j) {
+                double t = orc_bf16(hidden[r * ldh + j]) * orc_bf16(W[v * ldw + j]);
+                s += t;
+                sa += fabs(t);
+            }
+            logits[r * ld + v] = orc_bf16_round_f64(s);
+            if (exact) exact[r * V + v] = s;
+            if (abssum) abssum[r * V + v] = sa;
+        }
+    }
+}
+
 int orc_max_threads(void)
 {
 #ifdef _OPENMP

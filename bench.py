@@ -520,6 +520,27 @@ def run_ours(args):
             "note": "timed alone, not part of the step; alg_bytes: embed = E rows gathered + feedback + "
                     "output; choice_probs = 4 slots x (token + probability + logit) + lse; commit = argmax + tokens",
         }
+        # The LM head fused with the step's statistics (logits = hidden . E^T with the head tied
+        # to the embedding table, stored once; entropy / lse / argmax from the GEMM's epilogue),
+        # against the same work unfused: the LM head alone, then dg_denoise_step on its logits.
+        hid = synth.hidden_states(n, L, d, seed=wl.seed + 7, kind="normal", device=dev)
+        xl = torch.empty((n, L, V), dtype=torch.bfloat16, device=dev)
+        lws = torch.empty(dg.dg_lm_head_workspace_bytes(n, L, V), dtype=torch.uint8, device=dev)
+        t_lm = _time(lambda: dg.dg_lm_head_denoise_step(hid, E, params, seed, xl, canvas, prev, stable, acc, am, smp,
+                                                        ent, lse, conv, workspace=lws, stream=stream), reps=10)
+        t_lm_logits = _time(lambda: dg.dg_lm_head_logits(hid, E, params, xl, lws, stream=stream), reps=10)
+        t_dn_xl = _time(lambda: dg.dg_denoise_step(xl, params, seed, canvas, prev, stable, acc, am, smp, ent, lse,
+                                                   conv, workspace=dws, stream=stream), reps=10)
+        lm_flops = 2.0 * n * L * V * d
+        around["lm_head_step"] = {
+            "ms": t_lm, "tflops": lm_flops / (t_lm * 1e-3) / 1e12,
+            "frac_tc": lm_flops / (t_lm * 1e-3) / 1e12 / peak_tc,
+            "unfused_ms": t_lm_logits + t_dn_xl, "lm_head_logits_ms": t_lm_logits,
+            "denoise_on_its_logits_ms": t_dn_xl,
+            "note": "dg_lm_head_denoise_step (hidden [n, L, d] x E^T -> bf16 logits + step), timed alone; "
+                    "frac_tc: 2 N V d flops against the sustained bf16 peak; unfused = dg_lm_head_logits "
+                    "then dg_denoise_step"}
+        del xl, lws, hid
         torch.cuda.synchronize()
         if dg.dg_get_device_status():
             raise RuntimeError("device status set by the rows around the step")

@@ -58,6 +58,10 @@ def load(path: str | None = None):
         "dg_denoise_stats": (st, [P, ctypes.c_int, i64, i64, i32, i64, P, u64] + [P] * 11 + [P, sz, P]),
         "dg_denoise_samples": (st, [P, ctypes.c_int, i64, i64, i32, i64, P, u64, P, P, P, sz, P]),
         "dg_accept_from_entropy": (st, [P, P, P, i64, i32, i64, P, u64] + [P] * 7 + [P]),
+        "dg_lm_head_workspace_bytes": (sz, [i64, i32, i64]),
+        "dg_lm_head_logits": (st, [P, i64, P, i64, i64, i32, i64, i32, P, P, i64, P, sz, P]),
+        "dg_lm_head_denoise_step": (st, [P, i64, P, i64, i64, i32, i64, i32, P, u64, P, i64]
+                                    + [P] * 11 + [P, sz, P]),
         "dg_canvas_init": (st, [P, i64, i32, i64, P, u64, P]),
         "dg_advance_params": (st, [P, P, i64, P]),
         "dg_self_cond_workspace_bytes": (sz, [i64, i32, i32, i32]),
@@ -92,7 +96,8 @@ def load(path: str | None = None):
 def exported_symbols() -> list[str]:
     lib = load()
     return [n for n in ("dg_denoise_workspace_bytes", "dg_denoise_step", "dg_denoise_stats",
-                        "dg_denoise_samples", "dg_accept_from_entropy",
+                        "dg_denoise_samples", "dg_accept_from_entropy", "dg_lm_head_workspace_bytes",
+                        "dg_lm_head_logits", "dg_lm_head_denoise_step",
                         "dg_canvas_init", "dg_advance_params", "dg_self_cond_workspace_bytes",
                         "dg_self_cond_logits", "dg_self_cond_prepare", "dg_self_cond_pe",
                         "dg_self_cond_mlp", "dg_self_cond_probs_workspace_bytes",
@@ -243,6 +248,49 @@ def dg_accept_from_entropy(entropy, sample, argmax, n_canvas, L, V, params, seed
                                        _p(converged), _p(mean_entropy), _p(n_accept), _s(stream))
     if check:
         _check("dg_accept_from_entropy", rc)
+    return rc
+
+
+def dg_lm_head_workspace_bytes(n_canvas: int, L: int, V: int) -> int:
+    return int(load().dg_lm_head_workspace_bytes(n_canvas, L, V))
+
+
+def _lm_dims(hidden, W_lm, logits, V):
+    n, L, ldh = hidden.shape
+    d = W_lm.shape[1] if W_lm.dim() == 2 else None
+    if hidden.stride(2) != 1 or W_lm.stride(1) != 1 or logits.stride(2) != 1:
+        raise ValueError("rows must be contiguous")
+    V = W_lm.shape[0] if V is None else V
+    return n, L, V, d, hidden.stride(1), W_lm.stride(0), logits.stride(1)
+
+
+def dg_lm_head_logits(hidden, W_lm, params, logits, workspace=None, *, V=None, stream=None,
+                      check=True) -> int:
+    """logits[n, L, ld] = bf16(hidden[n, L, d] . W_lm[V, d]^T) for the active canvases."""
+    n, L, V, d, ldh, ldw, ld = _lm_dims(hidden, W_lm, logits, V)
+    if workspace is None:
+        workspace = torch.empty(dg_lm_head_workspace_bytes(n, L, V), dtype=torch.uint8, device=hidden.device)
+    rc = load().dg_lm_head_logits(_p(hidden), ldh, _p(W_lm), ldw, n, L, V, d, _p(params), _p(logits), ld,
+                                  _p(workspace), workspace.numel(), _s(stream))
+    if check:
+        _check("dg_lm_head_logits", rc)
+    return rc
+
+
+def dg_lm_head_denoise_step(hidden, W_lm, params, seed, logits, canvas, prev_argmax, stable_count,
+                            accept_mask, argmax, sample, entropy, lse, converged, mean_entropy=None,
+                            n_accept=None, workspace=None, *, V=None, stream=None, check=True) -> int:
+    """The LM head (logits stored into ``logits``) and one denoising step on its logits."""
+    n, L, V, d, ldh, ldw, ld = _lm_dims(hidden, W_lm, logits, V)
+    if workspace is None:
+        workspace = torch.empty(dg_lm_head_workspace_bytes(n, L, V), dtype=torch.uint8, device=hidden.device)
+    rc = load().dg_lm_head_denoise_step(_p(hidden), ldh, _p(W_lm), ldw, n, L, V, d, _p(params),
+                                        int(seed) & 0xFFFFFFFFFFFFFFFF, _p(logits), ld, _p(canvas),
+                                        _p(prev_argmax), _p(stable_count), _p(accept_mask), _p(argmax),
+                                        _p(sample), _p(entropy), _p(lse), _p(converged), _p(mean_entropy),
+                                        _p(n_accept), _p(workspace), workspace.numel(), _s(stream))
+    if check:
+        _check("dg_lm_head_denoise_step", rc)
     return rc
 
 

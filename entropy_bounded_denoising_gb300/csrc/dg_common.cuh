@@ -396,6 +396,14 @@ inline dg_status cuda_status(cudaError_t err) { return err == cudaSuccess ? DG_O
 // Encode a tiled tensor map (driver entry point fetched once).  Returns false on failure.
 bool encode_tmap(void* tmap, int dtype_code, int rank, void* base, const uint64_t* dims,
                  const uint64_t* strides_bytes, const uint32_t* box, int swizzle_bytes);
+// LM head (dg_gemm.cu): logits = bf16(hidden . W^T) for the active canvases' rows, [n][L][ld]
+// bf16; with `stats` non-null also each row's softmax state per kLmTileCols-column tile, as
+// 5 arrays (max, count, r, t, first column of the max) of n * L floats per tile, tile after
+// tile.  `plan` needs n + 1 ints.  Enqueues 2 kernels on `stream`.
+constexpr int kLmTileCols = 256;
+dg_status lm_head_gemm(const uint16_t* hidden, int64_t ldh, const uint16_t* W, int64_t ldw, int64_t n, int32_t L,
+                       int64_t V, int32_t d, const dg_canvas_params* params, uint16_t* logits, int64_t ld,
+                       int32_t* plan, float* stats, cudaStream_t stream);
 // Programmatic dependent launch on (build with -DDG_NO_PDL for plain stream order).
 #ifdef DG_NO_PDL
 constexpr bool kPdl = false;

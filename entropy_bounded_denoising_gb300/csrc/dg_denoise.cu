@@ -85,6 +85,7 @@ struct DeferredWs {
     unsigned long long* key;  // [n * L]: best (score, entry) of the row so far, see score_key
     int32_t* done;   // [n * L]: chunks of the row searched so far
     float* row_max;  // [n * L] by row: written by the statistics pass
+    int32_t all_deferred;  // 1: every canvas is sampled by the deferred pass (DG_SAMPLE_ALL ignored)
 };
 
 template <int DT>
@@ -842,7 +843,7 @@ __global__ void __launch_bounds__(1024) k2_accept(
     // ws.count null (the acceptance hook): no deferred sampling.  Else accepted positions of
     // a canvas without DG_SAMPLE_ALL are listed for the deferred sampling pass, which writes
     // their sample and token
-    const bool deferred = ws.count && !(p.flags & DG_SAMPLE_ALL);
+    const bool deferred = ws.count && (ws.all_deferred || !(p.flags & DG_SAMPLE_ALL));
     const bool valid = i < L;
     const int64_t q = c * L + i;
     const float H = valid ? entropy[q] : 0.f;
@@ -954,6 +955,85 @@ __global__ void k_philox_words(uint64_t seed, uint32_t request_id, uint32_t step
 }
 
 // ------------------------------------------------------------------------------------
+// LM head: each row's statistics from the softmax states the GEMM epilogue recorded per
+// 256-column tile (same quantities as RowState, records [tile][5][R]).  One CTA per 32
+// consecutive rows (lane = row, so every load is 128 contiguous bytes); its 32 warps take the
+// tiles in 32 contiguous ranges and are merged in warp order, so the result does not depend
+// on timing.  Writes what k1_row_stats writes for a canvas without DG_SAMPLE_ALL (sample -1,
+// the row's maximum for the deferred sampler) and clears the list of accepted rows.
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) k_lm_stats_merge(
+    const float* __restrict__ rec, int64_t R, int32_t n_tiles, int32_t L, const dg_canvas_params* __restrict__ params,
+    int32_t* __restrict__ argmax_out, int32_t* __restrict__ sample_out, float* __restrict__ entropy_out,
+    float* __restrict__ lse_out, DeferredWs ws, unsigned* status) {
+    __shared__ RowState part[32][33];
+    __shared__ int part_bad[32][33];
+    dg::pdl_wait();
+    dg::pdl_release();
+    if (ws.count && blockIdx.x == 0 && threadIdx.x == 0) *ws.count = 0;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t row = (int64_t)blockIdx.x * 32 + lane;
+    const int64_t canvas = row < R ? row / L : 0;
+    const dg_canvas_params p = params[canvas];
+    const bool t_ok = p.temperature > 0.f && isfinite(p.temperature);
+    const bool use = row < R && (p.flags & DG_ACTIVE) && t_ok;
+    const float invT = use ? 1.0f / p.temperature : 1.f;
+    const float k2 = kLog2e * invT;
+    RowState st{-INFINITY, 0.f, 0.f, 0.f, 0x7fffffff};
+    bool bad = false;
+    if (use) {
+        const int t0 = (int)((int64_t)warp * n_tiles / 32), t1 = (int)((int64_t)(warp + 1) * n_tiles / 32);
+        constexpr int kB = 4;  // records in flight per thread
+        for (int t = t0; t < t1; t += kB) {
+            float f[kB][5];
+#pragma unroll
+            for (int b = 0; b < kB; ++b) {
+                if (t + b < t1) {
+                    const float* q = rec + (int64_t)(t + b) * 5 * R + row;
+#pragma unroll
+                    for (int k = 0; k < 5; ++k) f[b][k] = __ldcs(q + k * R);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kB; ++b) {
+                if (t + b < t1) {
+                    if (f[b][1] != f[b][1]) {
+                        bad = true;
+                    } else {
+                        st = merge(st, RowState{f[b][0], f[b][1], f[b][2], f[b][3], __float_as_int(f[b][4])}, k2);
+                    }
+                }
+            }
+        }
+    }
+    part[warp][lane] = st;
+    part_bad[warp][lane] = bad ? 1 : 0;
+    __syncthreads();
+    if (warp != 0) return;
+    if (row < R && (p.flags & DG_ACTIVE) && !t_ok) {
+        if (row % L == 0) dg::raise_status(status, DG_DEV_BAD_PARAM);
+        return;
+    }
+    if (!use) return;
+    RowState rs = part[0][lane];
+    for (int w = 1; w < 32; ++w) {
+        rs = merge(rs, part[w][lane], k2);
+        bad |= part_bad[w][lane] != 0;
+    }
+    const bool empty = rs.m == -INFINITY;
+    const bool row_bad = bad || rs.m == INFINITY || !isfinite(rs.r) || !isfinite(rs.t);
+    const float sum = rs.c + rs.r;
+    const float lns = (rs.c == 1.f) ? log1pf(rs.r) : logf(rs.c) + log1pf(rs.r / rs.c);
+    entropy_out[row] = lns - rs.t * kLn2 / sum;
+    lse_out[row] = rs.m * invT + lns;
+    argmax_out[row] = empty ? 0 : rs.idx;
+    sample_out[row] = -1;
+    ws.row_max[row] = (empty || row_bad) ? __int_as_float(0x7fc00000) : rs.m;
+    if (row_bad) dg::raise_status(status, DG_DEV_NAN_INF_ROW);
+    if (empty) dg::raise_status(status, DG_DEV_EMPTY_ROW);
+}
+
+// ------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -1036,7 +1116,41 @@ DeferredWs carve_ws(void* workspace, int64_t rows) {
     ws.key = reinterpret_cast<unsigned long long*>(b + 256 + 8 * rows);
     ws.done = reinterpret_cast<int32_t*>(b + 256 + 16 * rows);
     ws.row_max = reinterpret_cast<float*>(b + 256 + 20 * rows);
+    ws.all_deferred = 0;
     return ws;
+}
+
+// LM-head workspace: the deferred-sampling workspace, the list of active canvases, then the
+// per-tile softmax states (5 floats per row and 256-column tile).
+struct LmLayout {
+    size_t plan, rec, total;
+    int32_t n_tiles;
+};
+
+LmLayout lm_layout(int64_t n, int32_t L, int64_t V) {
+    const int64_t rows = n * (int64_t)L;
+    LmLayout l;
+    l.n_tiles = (int32_t)((V + dghost::kLmTileCols - 1) / dghost::kLmTileCols);
+    l.plan = (denoise_ws_bytes(rows) + 255) / 256 * 256;
+    l.rec = l.plan + ((size_t)(n + 1) * 4 + 255) / 256 * 256;
+    l.total = l.rec + ((size_t)rows * l.n_tiles * 5 * 4 + 255) / 256 * 256;
+    return l;
+}
+
+// Shapes, strides and alignment shared by the LM-head entry points.
+dg_status lm_head_check(const void* hidden, int64_t ldh, const void* W, int64_t ldw, int64_t n, int32_t L, int64_t V,
+                        int32_t d, const void* params, const void* logits, int64_t ld, const void* workspace,
+                        size_t workspace_bytes) {
+    dg_status s = check_canvas_dims(n, L, V);
+    if (s != DG_OK) return s;
+    if (d < 8 || d > 65536 || (d % 8) || ldh < d || ldw < d || ld < V || V >= (1LL << 30)) return DG_ERR_INVALID_ARG;
+    if (n == 0) return DG_OK;
+    if (!hidden || !W || !params || !logits) return DG_ERR_INVALID_ARG;
+    if (!aligned16(hidden) || !aligned16(W) || !aligned16(logits) || (ldh % 8) || (ldw % 8) || (ld % 8))
+        return DG_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < lm_layout(n, L, V).total) return DG_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DG_ERR_ALIGNMENT;
+    return DG_OK;
 }
 
 }  // namespace
@@ -1115,6 +1229,56 @@ dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld, int64_
     // alone on its stream: three CTAs per SM hide more of the load latency
     return denoise_samples(logits, dtype, ld, n_canvas, L, V, params, seed, canvas, sample, workspace,
                            workspace_bytes, 3, (cudaStream_t)stream);
+}
+
+size_t dg_lm_head_workspace_bytes(int64_t n_canvas, int32_t L, int64_t V) {
+    if (n_canvas < 0 || L < 0 || V < 0) return 0;
+    return lm_layout(n_canvas, L, V).total;
+}
+
+dg_status dg_lm_head_logits(const uint16_t* hidden, int64_t ldh, const uint16_t* W_lm, int64_t ldw, int64_t n_canvas,
+                            int32_t L, int64_t V, int32_t d, const dg_canvas_params* params, uint16_t* logits,
+                            int64_t ld, void* workspace, size_t workspace_bytes, dg_stream_t stream) {
+    const dg_status s = lm_head_check(hidden, ldh, W_lm, ldw, n_canvas, L, V, d, params, logits, ld, workspace,
+                                      workspace_bytes);
+    if (s != DG_OK || n_canvas == 0) return s;
+    const LmLayout lay = lm_layout(n_canvas, L, V);
+    unsigned char* b = static_cast<unsigned char*>(workspace);
+    return dghost::lm_head_gemm(hidden, ldh, W_lm, ldw, n_canvas, L, V, d, params, logits, ld,
+                                reinterpret_cast<int32_t*>(b + lay.plan), nullptr, (cudaStream_t)stream);
+}
+
+dg_status dg_lm_head_denoise_step(const uint16_t* hidden, int64_t ldh, const uint16_t* W_lm, int64_t ldw,
+                                  int64_t n_canvas, int32_t L, int64_t V, int32_t d, const dg_canvas_params* params,
+                                  uint64_t seed, uint16_t* logits, int64_t ld, int32_t* canvas, int32_t* prev_argmax,
+                                  int32_t* stable_count, uint8_t* accept_mask, int32_t* argmax, int32_t* sample,
+                                  float* entropy, float* lse, uint8_t* converged, float* mean_entropy,
+                                  int32_t* n_accept, void* workspace, size_t workspace_bytes, dg_stream_t stream) {
+    dg_status s = lm_head_check(hidden, ldh, W_lm, ldw, n_canvas, L, V, d, params, logits, ld, workspace,
+                                workspace_bytes);
+    if (s != DG_OK || n_canvas == 0) return s;
+    if (!canvas || !prev_argmax || !stable_count || !accept_mask || !argmax || !sample || !entropy || !lse ||
+        !converged)
+        return DG_ERR_INVALID_ARG;
+    const LmLayout lay = lm_layout(n_canvas, L, V);
+    unsigned char* b = static_cast<unsigned char*>(workspace);
+    const int64_t R = n_canvas * (int64_t)L;
+    float* rec = reinterpret_cast<float*>(b + lay.rec);
+    cudaStream_t st = (cudaStream_t)stream;
+    s = dghost::lm_head_gemm(hidden, ldh, W_lm, ldw, n_canvas, L, V, d, params, logits, ld,
+                             reinterpret_cast<int32_t*>(b + lay.plan), rec, st);
+    if (s != DG_OK) return s;
+    DeferredWs ws = carve_ws(workspace, R);
+    ws.all_deferred = 1;
+    const cudaError_t e = dghost::launch_pdl(k_lm_stats_merge, dim3((unsigned)((R + 31) / 32)), dim3(1024), 0, st, rec,
+                                             R, lay.n_tiles, L, params, argmax, sample, entropy, lse, ws,
+                                             dghost::status_word());
+    dghost::count_launch();
+    if (e != cudaSuccess) return DG_ERR_CUDA;
+    s = launch_k2(entropy, sample, argmax, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
+                  accept_mask, converged, mean_entropy, n_accept, ws, st);
+    if (s != DG_OK) return s;
+    return launch_kd<0>(logits, ld, n_canvas, L, V, params, seed, ws, sample, canvas, 3, st);
 }
 
 dg_status dg_accept_from_entropy(const float* entropy, const int32_t* sample, const int32_t* argmax,

@@ -40,9 +40,11 @@ namespace {
 constexpr int BM = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum AMode { A_TMA = 0, A_SOFTMAX_BF16 = 1, A_SOFTMAX_FP32 = 2 };
+// A_TMA_CANVAS: plain bf16 A rows per canvas ([n][L][ld], 3D map), as the LM head reads the
+// hidden states of the listed canvases
+enum AMode { A_TMA = 0, A_SOFTMAX_BF16 = 1, A_SOFTMAX_FP32 = 2, A_TMA_CANVAS = 3 };
 enum BMode { B_KMAJOR = 0, B_MNMAJOR = 1, B_KMAJOR_GATEUP = 2 };
-enum Epi { EPI_F32 = 0, EPI_BF16 = 1, EPI_GELU_GATEUP = 2, EPI_SCATTER_BF16 = 3 };
+enum Epi { EPI_F32 = 0, EPI_BF16 = 1, EPI_GELU_GATEUP = 2, EPI_SCATTER_BF16 = 3, EPI_LOGIT_STATS = 4 };
 
 struct GemmArgs {
     int32_t m_tiles;        // m-tiles when plan == nullptr; upper bound otherwise
@@ -71,6 +73,9 @@ struct GemmArgs {
     int32_t min_slice;      // k-blocks
     int64_t max_slots;      // partial tiles the workspace holds
     int32_t split_below;    // split only below this round efficiency (percent)
+    // EPI_LOGIT_STATS: per (tile column block, row) softmax states, [n_tiles][5][stats_rows]
+    float* stats;
+    int64_t stats_rows;
 };
 
 // k-slices: the fewest that keep the rounds at least 95 % full, with slices of at least
@@ -118,7 +123,7 @@ struct Cfg {
     static constexpr int BN = BN_;
     static constexpr int BK = BK_;
     static constexpr int STAGES = STAGES_;
-    static constexpr bool kXform = AM != A_TMA;
+    static constexpr bool kXform = AM == A_SOFTMAX_BF16 || AM == A_SOFTMAX_FP32;
     static constexpr int kAccCols = BN;                      // fp32 accumulator columns
     static constexpr int kNAcc = (BN <= 256) ? 2 : 1;        // double-buffered when it fits
     static constexpr int kTmemCols = kAccCols * kNAcc;       // 256 or 512
@@ -300,6 +305,95 @@ DG_DEVINL void epi_store(const GemmArgs& a, int epi, int m, int n_tile, int row,
     }
 }
 
+// ------------------------------------------------------------------ LM-head epilogue
+// EPI_LOGIT_STATS: one row's part of the logits over one tile of BN columns.  The fp32
+// accumulator is rounded to bf16 (the stored logits: 16-byte stores into the caller's
+// [n][L][ld] rows), and the softmax state of exactly those stored values is recorded for the
+// row: the maximum m, the count c of entries equal to it, r = sum over the others of
+// 2^((x - m) k2), t = sum of 2^((x - m) k2) (x - m) k2 (k2 = log2(e) / T), and the first
+// column holding m.  -inf entries are left out of the state; a NaN or +inf marks the record
+// (c = NaN).  The records of a row merge in any order to the row's statistics.
+constexpr float kStatsMinExponent = -256.f;  // 2^-256 is 0 in fp32: keeps t finite
+
+template <int BN>
+DG_DEVINL void logit_stats_tile(const GemmArgs& a, int m, int n_tile, int row, uint32_t tbase) {
+    const int pos = (m % a.tpc) * BM + row;
+    const bool live = pos < a.L;  // the canvas's last tile may hold padding rows
+    const int cz = canvas_of(a, m);
+    const int64_t r = (int64_t)cz * a.L + pos;
+    const float k2 = kLog2e / a.params[cz].temperature;
+    uint16_t* orow = static_cast<uint16_t*>(a.out) + r * a.ldo;
+    float M = -INFINITY, cnt = 0.f, rs = 0.f, ts = 0.f;
+    int idx = 0x7fffffff;
+    bool bad = false;
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 32; ++ch) {
+        float v[32];
+        dg::tmem_ld32(tbase + ch * 32, v);  // whole warp
+        const int c0 = n_tile * BN + ch * 32;
+        if (!live || c0 >= a.n_valid) continue;
+        const int nv = min(32, a.n_valid - c0);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        uint16_t* o = orow + c0;
+        if (nv == 32) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) *reinterpret_cast<uint4*>(o + 2 * i) = make_uint4(pk[i], pk[i + 1], pk[i + 2], pk[i + 3]);
+        } else {
+            for (int i = 0; i < nv; ++i) o[i] = (uint16_t)((i & 1) ? (pk[i >> 1] >> 16) : (pk[i >> 1] & 0xFFFFu));
+        }
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            x[2 * i] = __uint_as_float(pk[i] << 16);
+            x[2 * i + 1] = __uint_as_float(pk[i] & 0xffff0000u);
+        }
+        float cm = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (j < nv) {
+                bad |= (x[j] != x[j]) || (x[j] == INFINITY);
+                cm = fmaxf(cm, x[j]);
+            }
+        }
+        if (cm > M) {  // a new maximum: the entries so far move below it
+            if (cnt > 0.f || rs > 0.f) {
+                const float d = (M - cm) * k2, al = ex2(d), sum = cnt + rs;
+                ts = al * (ts + d * sum);
+                rs = al * sum;
+                cnt = 0.f;
+            }
+            M = cm;
+            idx = 0x7fffffff;
+        }
+        if (cm == -INFINITY) continue;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (j < nv && x[j] > -INFINITY) {
+                if (x[j] == M) {
+                    cnt += 1.f;
+                    idx = min(idx, c0 + j);
+                } else if (x[j] == x[j]) {
+                    const float d = fmaxf((x[j] - M) * k2, kStatsMinExponent);
+                    const float e = ex2(d);
+                    rs += e;
+                    ts = fmaf(e, d, ts);
+                }
+            }
+        }
+    }
+    if (live) {
+        const int64_t R = a.stats_rows;
+        float* st = a.stats + (int64_t)n_tile * 5 * R + r;
+        st[0] = M;
+        st[R] = bad ? __int_as_float(0x7fc00000) : cnt;
+        st[2 * R] = rs;
+        st[3 * R] = ts;
+        st[4 * R] = __int_as_float(idx);
+    }
+}
+
 // ------------------------------------------------------------------ the GEMM kernel
 // Launched as clusters of cm = gridDim.x / (clusters) CTAs (cm = 1, 2 or 4).  With cm > 1
 // (N-major B only) every CTA loads BN/64/cm of the B tile's 64-column atoms and multicasts
@@ -370,7 +464,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             for (int64_t G = cid; G < n_groups && !aborted(sh); G += ncl) {
                 const Item im = decode(a, mt, cm, rank, G, splits);
                 int cz = 0, crow = 0;
-                if (C::kXform) {
+                if (C::kXform || C::kAMode == A_TMA_CANVAS) {
                     cz = canvas_of(a, im.m_load);
                     crow = (im.m_load % a.tpc) * BM;
                 }
@@ -386,7 +480,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     const int k0 = kb * C::BK;
                     if (C::kAMode == A_TMA) {
                         dg::tma_load_2d(sA, &tmA, k0, im.m_load * BM, &sh.full[s]);
-                    } else if (C::kAMode == A_SOFTMAX_BF16) {
+                    } else if (C::kAMode == A_SOFTMAX_BF16 || C::kAMode == A_TMA_CANVAS) {
                         dg::tma_load_3d(sA, &tmA, k0, crow, cz, &sh.full[s]);
                     } else {
                         // fp32 logits: BK = 32 columns = one 128-byte swizzle row per tile row
@@ -534,6 +628,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     for (int i = 0; i < 32; i += 4)
                         *reinterpret_cast<float4*>(dst + ch * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
                 }
+            } else if (a.epi == EPI_LOGIT_STATS) {
+                logit_stats_tile<C::BN>(a, im.m, im.n, row, tbase);
             } else if (a.epi == EPI_GELU_GATEUP) {
                 for (int ch = 0; ch < C::BN / 64; ++ch) {
                     float g[32], u[32];
@@ -769,10 +865,11 @@ DG_DEVINL bool self_cond_on(const dg_canvas_params& p, const uint8_t* converged,
            !(converged && converged[c]) && p.temperature > 0.f;
 }
 
-// Compact list of the canvases whose feedback is computed this step (original order): per
-// chunk of blockDim.x canvases, warp ballots, an exclusive prefix over the warps' counts.
+// Compact list of canvases in original order: those whose feedback is computed this step
+// (mode 0) or the active ones (mode 1, the LM head's rows).  Per chunk of blockDim.x
+// canvases, warp ballots, an exclusive prefix over the warps' counts.
 __global__ void k_plan(const dg_canvas_params* __restrict__ params, const uint8_t* __restrict__ converged,
-                       int64_t n, int32_t* __restrict__ plan) {
+                       int64_t n, int32_t* __restrict__ plan, int mode) {
     dg::pdl_wait();
     dg::pdl_release();
     __shared__ int warp_base[32];
@@ -781,7 +878,8 @@ __global__ void k_plan(const dg_canvas_params* __restrict__ params, const uint8_
     int count = 0;  // canvases listed before this chunk (same in every thread)
     for (int64_t base = 0; base < n; base += blockDim.x) {
         const int64_t c = base + threadIdx.x;
-        const bool on = c < n && self_cond_on(params[c], converged, c);
+        const bool on = c < n && (mode == 0 ? self_cond_on(params[c], converged, c)
+                                            : (params[c].flags & DG_ACTIVE) != 0u);
         const unsigned ballot = __ballot_sync(0xffffffffu, on);
         if (lane == 0) warp_base[warp] = __popc(ballot);
         __syncthreads();
@@ -832,6 +930,8 @@ using PEprob = Cfg<A_TMA, B_MNMAJOR, 512, 32, 5>;
 using GateUp = Cfg<A_TMA, B_KMAJOR_GATEUP, 256, 64, DG_MLP_STAGES, true>;
 using Down = Cfg<A_TMA, B_KMAJOR, 256, 64, DG_MLP_STAGES, true>;
 using DownSingle = Cfg<A_TMA, B_KMAJOR, 256, 64, 4>;  // plain GEMMs (K-major B) on one CTA per tile
+// LM head: hidden rows of the listed canvases (3D map) times W_lm [V][d] (K-major), CTA pairs
+using LmHead = Cfg<A_TMA_CANVAS, B_KMAJOR, 256, 64, DG_MLP_STAGES, true>;
 
 constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -1067,6 +1167,50 @@ dg_status check_weights(int64_t V, int32_t d, int32_t h, const uint16_t* E, cons
 
 }  // namespace
 
+// LM head: logits = bf16(hidden . W^T) for the rows of the active canvases, on CTA pairs
+// (tcgen05, cta_group::2; 256 x 256 tiles, K = d never split).  With `stats` the epilogue also
+// records each row's softmax state per 256-column tile (EPI_LOGIT_STATS).  `plan` holds
+// n + 1 ints (the list of active canvases, written here first).
+dg_status dghost::lm_head_gemm(const uint16_t* hidden, int64_t ldh, const uint16_t* W, int64_t ldw, int64_t n,
+                               int32_t L, int64_t V, int32_t d, const dg_canvas_params* params, uint16_t* logits,
+                               int64_t ld, int32_t* plan, float* stats, cudaStream_t stream) {
+    cudaError_t e = dghost::launch_pdl(k_plan, dim3(1), dim3(1024), 0, stream, params,
+                                       static_cast<const uint8_t*>(nullptr), n, plan, 1);
+    dghost::count_launch();
+    if (e != cudaSuccess) return DG_ERR_CUDA;
+    TMaps tm;
+    {
+        uint64_t dims[3] = {(uint64_t)d, (uint64_t)L, (uint64_t)n};
+        uint64_t strides[2] = {(uint64_t)(ldh * 2), (uint64_t)(ldh * 2 * L)};
+        uint32_t box[3] = {64, (uint32_t)BM, 1};
+        if (!dghost::encode_tmap(tm.a, 0, 3, const_cast<uint16_t*>(hidden), dims, strides, box, 128))
+            return DG_ERR_CUDA;
+    }
+    if (!tmap_2d(tm.b0, 0, W, d, V, ldw, 64, kLmTileCols / 2, 128)) return DG_ERR_CUDA;
+    const int tpc = (L + BM - 1) / BM;
+    GemmArgs g{};
+    g.m_tiles = (int32_t)(n * tpc);
+    g.plan = plan;
+    g.tpc = tpc;
+    g.n_tiles = (int32_t)((V + kLmTileCols - 1) / kLmTileCols);
+    g.k_blocks = (d + 63) / 64;
+    g.splits = 1;
+    g.K = d;
+    g.L = L;
+    g.params = params;
+    g.epi = stats ? EPI_LOGIT_STATS : EPI_SCATTER_BF16;
+    g.out = logits;
+    g.ldo = ld;
+    g.n_valid = (int32_t)V;
+    g.m_valid = (int32_t)(n * tpc * BM);
+    g.status = dghost::status_word();
+    g.stats = stats;
+    g.stats_rows = n * (int64_t)L;
+    LaunchPlan pl;
+    if (!plan_gemm<LmHead>(g, 0, &pl)) return DG_ERR_CUDA;  // no partial slots: K is never split
+    return launch_gemm<LmHead>(tm.a, tm.b0, tm.b0, g, pl, stream);
+}
+
 extern "C" {
 
 size_t dg_self_cond_workspace_bytes(int64_t n_canvas, int32_t L, int32_t d, int32_t h) {
@@ -1107,7 +1251,7 @@ dg_status dg_self_cond_prepare(const dg_canvas_params* params, const uint8_t* co
     if (s != DG_OK) return s;
     cudaStream_t st = (cudaStream_t)stream;
     int32_t* plan = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + lay.plan);
-    cudaError_t e = dghost::launch_pdl(k_plan, dim3(1), dim3(1024), 0, st, params, converged, n_canvas, plan);
+    cudaError_t e = dghost::launch_pdl(k_plan, dim3(1), dim3(1024), 0, st, params, converged, n_canvas, plan, 0);
     dghost::count_launch();
     if (e != cudaSuccess) return DG_ERR_CUDA;
     // about four CTAs per SM over all canvases (most of them exit at once when feedback is on)

@@ -13,7 +13,10 @@ workloads this library is measured on):
   * optionally a fraction of positions is made near one-hot by setting one random token
     to (row max + 20) after the step's logits are formed;
   * computed in fp32 and rounded to bf16 (or kept fp32);
-  * E, W_gate, W_up, W_down ~ N(0, 0.02^2), rounded to bf16.
+  * E, W_gate, W_up, W_down ~ N(0, 0.02^2), rounded to bf16;
+  * for the LM head, hidden states h_i = s_i z / (0.02 sqrt(d)) with z ~ N(0, 1), so that
+    hidden . E^T has the same per-position spread s_i; or small-integer operands (k / 8,
+    |k| <= 12 for hidden, <= 4 for W) whose dot products fp32 sums exactly.
 Every draw comes from a torch generator seeded from (seed, purpose, canvas), so the bytes
 do not depend on how canvases are chunked; CPU and CUDA generators give different (each
 reproducible) streams, and a test always hands the same bytes to both sides.
@@ -21,6 +24,7 @@ reproducible) streams, and a test always hands the same bytes to both sides.
 from __future__ import annotations
 
 import dataclasses
+import math
 
 import numpy as np
 import torch
@@ -28,7 +32,7 @@ import torch
 ACTIVE, READ_ONLY, SELF_COND, SAMPLE_ALL = 1, 2, 4, 8
 
 # purposes for seeding (arbitrary distinct constants)
-_P_BASE, _P_SCALE, _P_NOISE, _P_SPIKE, _P_WEIGHT, _P_PARAMS = 11, 23, 37, 41, 53, 67
+_P_BASE, _P_SCALE, _P_NOISE, _P_SPIKE, _P_WEIGHT, _P_PARAMS, _P_HIDDEN = 11, 23, 37, 41, 53, 67, 79
 
 
 def _gen(device, *parts: int) -> torch.Generator:
@@ -112,6 +116,36 @@ def weights(V: int, d: int, h: int, *, seed: int, device="cpu"):
         t = torch.randn(shape, generator=_gen(device, seed, _P_WEIGHT, purpose), device=device)
         return t.mul_(0.02).to(torch.bfloat16)
     return w((V, d), 1), w((h, d), 2), w((h, d), 3), w((d, h), 4)
+
+
+def hidden_states(n: int, L: int, d: int, *, seed: int, scale=(0.5, 12.0), kind: str = "normal",
+                  ld: int | None = None, device="cpu") -> torch.Tensor:
+    """Last hidden states [n, L, ld] bf16 for the LM head (columns past d are 0).
+
+    kind "normal": s_i z / (0.02 sqrt(d)), z ~ N(0, 1), s_i ~ U[scale] per position (with
+    N(0, 0.02^2) weights the logits spread like the logits workload's); kind "int": k m_i / 8
+    with k uniform in [-4, 4] and m_i in {1, 2, 3} per position."""
+    ld = d if ld is None else ld
+    assert ld >= d and kind in ("normal", "int")
+    out = torch.zeros((n, L, ld), dtype=torch.bfloat16, device=device)
+    for c in range(n):
+        g = _gen(device, seed, _P_HIDDEN, c)
+        if kind == "normal":
+            z = torch.randn((L, d), generator=g, device=device)
+            s = torch.empty((L, 1), device=device).uniform_(scale[0], scale[1],
+                                                            generator=_gen(device, seed, _P_SCALE, c))
+            out[c, :, :d] = (z * s / (0.02 * math.sqrt(d))).to(torch.bfloat16)
+        else:
+            k = torch.randint(-4, 5, (L, d), generator=g, device=device).float()
+            m = torch.randint(1, 4, (L, 1), generator=g, device=device).float()
+            out[c, :, :d] = (k * m / 8.0).to(torch.bfloat16)
+    return out
+
+
+def lm_head_weights_int(V: int, d: int, *, seed: int, device="cpu") -> torch.Tensor:
+    """W_lm [V, d] bf16 with entries k / 8, k uniform in [-4, 4]."""
+    k = torch.randint(-4, 5, (V, d), generator=_gen(device, seed, _P_WEIGHT, 5), device=device).float()
+    return (k / 8.0).to(torch.bfloat16)
 
 
 def canvas_params(wl: Workload, step: int = 0):

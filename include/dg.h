@@ -224,6 +224,56 @@ DG_API dg_status dg_advance_params(dg_canvas_params* params, const uint8_t* conv
                             int64_t n_canvas, dg_stream_t stream);
 
 /* ------------------------------------------------------------------------------------ */
+/* LM head fused with the step's statistics.  The logits the denoise step reads are the   */
+/* model's output over the canvas [DG "엔트로피 기반 디노이징"]; the pages do not describe  */
+/* the output layer, and the reading taken is a plain linear map of the last hidden        */
+/* states, logits = bf16(hidden . W_lm^T), no bias, no soft-capping (W_lm is the input    */
+/* embedding table when the model ties them).  Computed on the tensor cores (tcgen05,      */
+/* bf16 operands, fp32 accumulation, one rounding to bf16 per logit); the statistics are   */
+/* taken from the stored bf16 logits in the GEMM's epilogue, so the logits are not read    */
+/* back for them.                                                                          */
+/* ------------------------------------------------------------------------------------ */
+
+/* Workspace for dg_lm_head_logits / dg_lm_head_denoise_step (bytes): the deferred-sampling
+ * list of dg_denoise_workspace_bytes, the list of active canvases, and 20 bytes per position
+ * and 256 columns of V (each row's softmax state per tile). */
+DG_API size_t dg_lm_head_workspace_bytes(int64_t n_canvas, int32_t L, int64_t V);
+
+/* logits = bf16(hidden . W_lm^T) for every position of every DG_ACTIVE canvas; the rows of
+ * other canvases are not written.
+ *   hidden  (device) [n_canvas][L][ldh] bf16: last hidden states; ldh >= d, ldh % 8 == 0.
+ *   W_lm    (device) [V][ldw] bf16: output projection (row v = token v); ldw >= d, % 8 == 0.
+ *   logits  (device, out) [n_canvas][L][ld] bf16; ld >= V, ld % 8 == 0.  Columns V..ld-1
+ *           are not written.
+ *   params  (device) [n_canvas]: only DG_ACTIVE is read.
+ *   workspace (device) >= dg_lm_head_workspace_bytes(), 16-byte aligned, no initial contents.
+ * All device pointers 16-byte aligned.  Limits: 8 <= d <= 65536, d % 8 == 0, V < 2^30;
+ * n_canvas and L as dg_denoise_step.  Errors: DG_ERR_INVALID_ARG, DG_ERR_ALIGNMENT,
+ * DG_ERR_WORKSPACE, DG_ERR_CUDA.  Enqueues 2 kernels. */
+DG_API dg_status dg_lm_head_logits(const uint16_t* hidden, int64_t ldh, const uint16_t* W_lm,
+                                   int64_t ldw, int64_t n_canvas, int32_t L, int64_t V, int32_t d,
+                                   const dg_canvas_params* params, uint16_t* logits, int64_t ld,
+                                   void* workspace, size_t workspace_bytes, dg_stream_t stream);
+
+/* dg_lm_head_logits, then one denoising step on those logits: the outputs of
+ * dg_denoise_step (same meaning, same arguments after params) for the logits it stores,
+ * which the self-conditioning calls can then read with the lse written here.  Every
+ * canvas is sampled at its accepted positions only (DG_SAMPLE_ALL has no effect: sample
+ * is -1 at the other positions).  Launches: active-canvas list, the LM-head GEMM with the
+ * statistics epilogue, a merge of the per-tile states (fixed order: results do not depend
+ * on timing), acceptance / renoise / convergence, the samples of the accepted positions.
+ * Same limits and errors as dg_lm_head_logits and dg_denoise_step. */
+DG_API dg_status dg_lm_head_denoise_step(const uint16_t* hidden, int64_t ldh, const uint16_t* W_lm,
+                                         int64_t ldw, int64_t n_canvas, int32_t L, int64_t V,
+                                         int32_t d, const dg_canvas_params* params, uint64_t seed,
+                                         uint16_t* logits, int64_t ld, int32_t* canvas,
+                                         int32_t* prev_argmax, int32_t* stable_count,
+                                         uint8_t* accept_mask, int32_t* argmax, int32_t* sample,
+                                         float* entropy, float* lse, uint8_t* converged,
+                                         float* mean_entropy, int32_t* n_accept,
+                                         void* workspace, size_t workspace_bytes, dg_stream_t stream);
+
+/* ------------------------------------------------------------------------------------ */
 /* Self-conditioning [DG "자기 조건화"]:                                                  */
 /*   pe    = P . E,  P = softmax(logits / T) per position, E the token embedding table;  */
 /*   delta = W_down (gelu_tanh(W_gate pe) * (W_up pe)), no bias (gated MLP).            */

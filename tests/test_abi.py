@@ -73,6 +73,37 @@ def test_host_validation_without_gpu():
     assert lib.dg_advance_params(None, None, -1, None) == dg.DG_ERR_INVALID_ARG
 
 
+def test_lm_head_validation_without_gpu():
+    lib = dg.load()
+    # workspace: deferred list (256 + 24 per position), canvas list, 20 bytes per position and tile
+    assert dg.dg_lm_head_workspace_bytes(2, 16, 1000) == 1024 + 256 + 32 * 4 * 20
+    assert dg.dg_lm_head_workspace_bytes(8, 256, 262144) == \
+        (256 + 24 * 2048 + 255) // 256 * 256 + 256 + 2048 * 1024 * 20
+    ws = dg.dg_lm_head_workspace_bytes(1, 16, 64)
+
+    def call(h=16, ldh=64, W=16, ldw=64, n=1, L=16, V=64, d=64, logits=16, ld=64, w=256, wb=None):
+        return lib.dg_lm_head_logits(h, ldh, W, ldw, n, L, V, d, 16, logits, ld, w, ws if wb is None else wb, None)
+
+    assert call(d=60, ldh=60, ldw=60) == dg.DG_ERR_INVALID_ARG      # d % 8
+    assert call(ldh=32) == dg.DG_ERR_INVALID_ARG                    # ldh < d
+    assert call(ld=56) == dg.DG_ERR_INVALID_ARG                     # ld < V
+    assert call(V=1 << 30, ld=1 << 30) == dg.DG_ERR_INVALID_ARG     # V >= 2^30
+    assert call(L=0) == dg.DG_ERR_INVALID_ARG
+    assert call(h=None) == dg.DG_ERR_INVALID_ARG
+    assert call(h=24) == dg.DG_ERR_ALIGNMENT
+    assert call(ldw=68) == dg.DG_ERR_ALIGNMENT
+    assert call(ld=68) == dg.DG_ERR_ALIGNMENT
+    assert call(wb=ws - 1) == dg.DG_ERR_WORKSPACE
+    assert call(w=None) == dg.DG_ERR_WORKSPACE
+    assert call(w=264) == dg.DG_ERR_ALIGNMENT
+    assert call(n=0) == dg.DG_OK
+    step = lib.dg_lm_head_denoise_step
+    args = [16, 64, 16, 64, 1, 16, 64, 64, 16, 0, 16, 64]
+    assert step(*args, *([16] * 11), 256, ws - 1, None) == dg.DG_ERR_WORKSPACE
+    assert step(*args, None, *([16] * 10), 256, ws, None) == dg.DG_ERR_INVALID_ARG   # canvas
+    assert step(*args[:4], 0, *args[5:], *([None] * 11), None, 0, None) == dg.DG_OK
+
+
 def test_params_record_layout():
     import numpy as np
     p = {"temperature": np.float32([0.5]), "beta": np.float32([2.0]), "tau": np.float32([0.25]),

@@ -137,8 +137,10 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def _workload_arith(wl, n_sc_rows, n_read_rows):
-    """Algorithmic bytes and tensor-core FLOPs of one step."""
+def _workload_arith(wl, n_sc_rows, n_read_rows, from_hidden=False):
+    """Algorithmic bytes and tensor-core FLOPs of one step.  From hidden states the step
+    reads the hidden rows instead of the logits and adds the LM head's contraction (its
+    weights are the embedding table, already counted); the logits are an intermediate."""
     N = wl.n * wl.L
     logits_b = 2 * n_read_rows * wl.V
     e_b = 2 * wl.V * wl.d
@@ -146,8 +148,10 @@ def _workload_arith(wl, n_sc_rows, n_read_rows):
     out_b = 17 * N + 2 * N * wl.d
     pe_flops = 2.0 * n_sc_rows * wl.V * wl.d
     mlp_flops = 6.0 * n_sc_rows * wl.d * wl.h
-    return {"bytes": logits_b + e_b + w_b + out_b, "logits_bytes": logits_b, "pe_flops": pe_flops,
-            "mlp_flops": mlp_flops, "tc_flops": pe_flops + mlp_flops}
+    lm_flops = 2.0 * n_read_rows * wl.V * wl.d if from_hidden else 0.0
+    in_b = 2 * n_read_rows * wl.d if from_hidden else logits_b
+    return {"bytes": in_b + e_b + w_b + out_b, "logits_bytes": logits_b, "pe_flops": pe_flops,
+            "mlp_flops": mlp_flops, "lm_flops": lm_flops, "tc_flops": pe_flops + mlp_flops + lm_flops}
 
 
 def _profile_traffic(kernel_tag: str):
@@ -263,9 +267,11 @@ def run_reference(args):
     return 0
 
 
-def _config(wl):
+def _config(wl, from_hidden=False):
+    src = ("from bf16 hidden states: LM head (tied to E) fused with the step's statistics"
+           if from_hidden else f"{wl.dtype} logits")
     return {"workload": (f"{wl.name}: {wl.n} canvases x {wl.L} positions, V={wl.V}, d={wl.d}, h={wl.h}, "
-                         f"{wl.dtype} logits"),
+                         f"{src}"),
             "n_canvas": wl.n, "L": wl.L, "V": wl.V, "d": wl.d, "h": wl.h,
             "l2": "no flush: each step reads inputs larger than L2 (logits + embedding table)",
             "parallelism": "replicas (canvases independent, no exchange step)"}
@@ -314,6 +320,15 @@ def run_ours(args):
     wsp = torch.empty(dg.dg_self_cond_workspace_bytes(n, L, d, h), dtype=torch.uint8, device=dev)
     dws = torch.empty(dg.dg_denoise_workspace_bytes(n, L, V, dg.DG_BF16 if wl.dtype == "bf16" else dg.DG_FP32),
                       dtype=torch.uint8, device=dev)
+    # --from-hidden: the step starts from the last hidden states; the LM head (tied to E) writes
+    # the logits the feedback reads and the step's statistics come from its epilogue
+    fh = args.from_hidden
+    if fh:
+        hid = synth.hidden_states(n, L, d, seed=wl.seed + 1000 * rank, kind="normal", device=dev)
+        xs = torch.empty((n, L, V), dtype=torch.bfloat16, device=dev)
+        lws = torch.empty(dg.dg_lm_head_workspace_bytes(n, L, V), dtype=torch.uint8, device=dev)
+    else:
+        xs = x
     # --graph captures the step once as a CUDA graph (on a side stream, as capture requires)
     # and times its replays; otherwise every step is enqueued call by call.
     stream = torch.cuda.Stream(device=dev) if args.graph else torch.cuda.current_stream()
@@ -323,12 +338,16 @@ def run_ours(args):
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        dg.dg_denoise_step(x, params, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv, workspace=dws,
-                           stream=stream)
+        if fh:
+            dg.dg_lm_head_denoise_step(hid, E, params, seed, xs, canvas, prev, stable, acc, am, smp, ent, lse,
+                                       conv, workspace=lws, stream=stream)
+        else:
+            dg.dg_denoise_step(x, params, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv, workspace=dws,
+                               stream=stream)
         dg.dg_self_cond_prepare(params, conv, n, L, d, h, delta, wsp, stream=stream)
         if ev:
             ev[1].record(stream)
-        dg.dg_self_cond_pe(x, lse, params, E, h, wsp, stream=stream)
+        dg.dg_self_cond_pe(xs, lse, params, E, h, wsp, stream=stream)
         if ev:
             ev[2].record(stream)
         dg.dg_self_cond_mlp(n, L, Wg, Wu, Wd, delta, wsp, stream=stream)
@@ -400,7 +419,7 @@ def run_ours(args):
     t_dn = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     t_pe = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
     t_mlp = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
-    ar = _workload_arith(wl, n_sc_rows, n_read_rows)
+    ar = _workload_arith(wl, n_sc_rows, n_read_rows, from_hidden=fh)
     pk = _peaks()
     peak_tc = pk["bf16_tflops_sustained"]
     pe_tflops = ar["pe_flops"] / (t_pe * 1e-3) / 1e12 if t_pe > 0 else 0.0
@@ -410,8 +429,9 @@ def run_ours(args):
     # ---------------------------------------------------------------- e2e: host buffers
     e2e = None
     if not args.no_e2e:
-        xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-        xh.copy_(x)
+        xin = hid if fh else x
+        xh = torch.empty(xin.shape, dtype=xin.dtype, pin_memory=True)
+        xh.copy_(xin)
         out_canvas = torch.empty((n, L), dtype=torch.int32, pin_memory=True)
         out_conv = torch.empty((n,), dtype=torch.uint8, pin_memory=True)
         out_delta = torch.empty((n, L, d), dtype=torch.bfloat16, pin_memory=True)
@@ -421,7 +441,7 @@ def run_ours(args):
         # second stream (into the other of two device buffers) while step k computes; every
         # step's copy in and result copy out lie inside the timed region.
         copy_stream = torch.cuda.Stream(device=dev)
-        xdev = [torch.empty_like(x), torch.empty_like(x)]
+        xdev = [torch.empty_like(xin), torch.empty_like(xin)]
         h2d_done = [torch.cuda.Event(), torch.cuda.Event()]
         buf_free = [torch.cuda.Event(), torch.cuda.Event()]
 
@@ -435,9 +455,14 @@ def run_ours(args):
         def e2e_compute(k):
             b = k % 2
             stream.wait_event(h2d_done[b])
-            dg.dg_denoise_step(xdev[b], params, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv,
-                               workspace=dws, stream=stream)
-            dg.dg_self_cond_logits(xdev[b], lse, params, conv, E, Wg, Wu, Wd, delta, wsp, stream=stream)
+            if fh:
+                dg.dg_lm_head_denoise_step(xdev[b], E, params, seed, xs, canvas, prev, stable, acc, am, smp, ent,
+                                           lse, conv, workspace=lws, stream=stream)
+                dg.dg_self_cond_logits(xs, lse, params, conv, E, Wg, Wu, Wd, delta, wsp, stream=stream)
+            else:
+                dg.dg_denoise_step(xdev[b], params, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv,
+                                   workspace=dws, stream=stream)
+                dg.dg_self_cond_logits(xdev[b], lse, params, conv, E, Wg, Wu, Wd, delta, wsp, stream=stream)
             buf_free[b].record(stream)
             out_canvas.copy_(canvas, non_blocking=True)
             out_conv.copy_(conv, non_blocking=True)
@@ -471,7 +496,7 @@ def run_ours(args):
     # single-pass-read choice probabilities (4 slots per position) and the commit, each
     # against the HBM roofline of its algorithmic bytes.
     around = None
-    if not args.no_extras:
+    if not args.no_extras and not fh:
         rng = np.random.default_rng(5)
         emb = torch.empty((n * L, d), dtype=torch.bfloat16, device=dev)
         C = 4
@@ -547,7 +572,7 @@ def run_ours(args):
 
     # ---------------------------------------------------------------- CPU baseline (oracle)
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not fh:
         import oracle
         oracle.build()
         threads = oracle.max_threads()
@@ -565,7 +590,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(_config(wl), launch=("CUDA graph replays of the captured step" if graph is not None
+        "config": dict(_config(wl, fh), launch=("CUDA graph replays of the captured step" if graph is not None
                                             else "eager: every call enqueued each step")),
         "roofline": {"bound": "tensor", "achieved": pe_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                      "frac": pe_tflops / peak_tc, "traffic": traffic,
@@ -574,8 +599,10 @@ def run_ours(args):
         "step_roofline": {"t_roof_ms": t_roof * 1e3, "frac": (t_roof * 1e3) / ms_step,
                           "alg_bytes": ar["bytes"], "tc_flops": ar["tc_flops"],
                           "hbm_peak_gbs": pk["hbm_gbs"], "tc_peak_tflops": peak_tc},
-        "kernels_ms": {"denoise_and_prepare": t_dn, "pe": t_pe, "mlp": t_mlp,
-                       "denoise_hbm_frac": (ar["logits_bytes"] / (t_dn * 1e-3)) / (pk["hbm_gbs"] * 1e9),
+        "kernels_ms": {("lm_head_denoise_and_prepare" if fh else "denoise_and_prepare"): t_dn, "pe": t_pe,
+                       "mlp": t_mlp,
+                       "denoise_hbm_frac": (None if fh else (ar["logits_bytes"] / (t_dn * 1e-3)) / (pk["hbm_gbs"] * 1e9)),
+                       "lm_head_tflops": (ar["lm_flops"] / (t_dn * 1e-3) / 1e12) if fh else None,
                        "mlp_tflops": ar["mlp_flops"] / (t_mlp * 1e-3) / 1e12 if t_mlp > 0 else 0.0},
         "steps_per_s": 1e3 / ms_step, "self_cond_rows": n_sc_rows, "converged_canvases": n_conv,
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clk.summary(),
@@ -706,6 +733,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip timing the rows around the step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--from-hidden", action="store_true",
+                    help="start each step from hidden states: the LM head fused with the step's statistics")
     ap.add_argument("--graph", action="store_true", help="time replays of the step captured as a CUDA graph")
     ap.add_argument("--loop", action="store_true",
                     help="time the workload's whole denoising loop (e.g. --workload sweep) instead of repeated steps")

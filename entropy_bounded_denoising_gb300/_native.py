@@ -260,6 +260,8 @@ def _lm_dims(hidden, W_lm, logits, V):
     d = W_lm.shape[1] if W_lm.dim() == 2 else None
     if hidden.stride(2) != 1 or W_lm.stride(1) != 1 or logits.stride(2) != 1:
         raise ValueError("rows must be contiguous")
+    if hidden.stride(0) != L * hidden.stride(1) or logits.stride(0) != L * logits.stride(1):
+        raise ValueError("canvases must follow each other at L row strides")
     V = W_lm.shape[0] if V is None else V
     return n, L, V, d, hidden.stride(1), W_lm.stride(0), logits.stride(1)
 

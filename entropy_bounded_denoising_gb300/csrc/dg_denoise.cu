@@ -694,7 +694,7 @@ template <int DT>
 __global__ void __launch_bounds__(kDWarps * 32, 3) k1_sample_listed(
     const unsigned char* __restrict__ logits, int64_t ld_bytes, int64_t V, int32_t L,
     const dg_canvas_params* __restrict__ params, uint64_t seed, DeferredWs ws, int32_t* __restrict__ sample_out,
-    int32_t* __restrict__ canvas_out) {
+    int32_t* __restrict__ canvas_out, int64_t rows) {
     constexpr int VN = Vec<DT>::N;
     constexpr int ES = DT == 0 ? 2 : 4;
     constexpr int GPV = VN / 4;
@@ -718,10 +718,11 @@ __global__ void __launch_bounds__(kDWarps * 32, 3) k1_sample_listed(
         const int chunk = (int)(it - (int64_t)w * cpr);
         const int2 e = ws.entry[w];
         const int64_t row = e.x;
+        const bool in_range = (uint64_t)row < (uint64_t)rows;  // entries come from K2; checked anyway
         const float m = __int_as_float(e.y);
-        const int64_t canvas = row / L;
+        const int64_t canvas = in_range ? row / L : 0;
         const dg_canvas_params p = params[canvas];
-        const bool ok = isfinite(m);  // else a NaN / inf / empty row (flagged by the statistics pass)
+        const bool ok = in_range && isfinite(m);  // else a NaN / inf / empty row (flagged by the statistics pass)
         float best = -INFINITY;
         int bidx = 0x7fffffff;
         if (ok) {
@@ -801,7 +802,7 @@ __global__ void __launch_bounds__(kDWarps * 32, 3) k1_sample_listed(
         if (lane == 0) {
             if (ok && best > -INFINITY) atomicMax(ws.key + w, score_key(best, bidx));
             __threadfence();
-            if (atomicAdd(ws.done + w, 1) == cpr - 1) {
+            if (atomicAdd(ws.done + w, 1) == cpr - 1 && in_range) {
                 // every chunk of the row is in: its winner is the position's sample and token
                 __threadfence();
                 const unsigned long long k = atomicMax(ws.key + w, 0ull);
@@ -846,7 +847,10 @@ __global__ void __launch_bounds__(1024) k2_accept(
     const bool deferred = ws.count && (ws.all_deferred || !(p.flags & DG_SAMPLE_ALL));
     const bool valid = i < L;
     const int64_t q = c * L + i;
-    const float H = valid ? entropy[q] : 0.f;
+    // a NaN entropy (a row flagged by the statistics pass) ranks after every number, so the
+    // ranks stay a permutation and every reserved slot of the sampler's list is written
+    const float H0 = valid ? entropy[q] : 0.f;
+    const float H = (H0 == H0) ? H0 : INFINITY;
     const int32_t am = valid ? argmax[q] : 0;
     if (valid) sH[i] = H;
     if (i == 0) sCut = L;
@@ -1086,7 +1090,7 @@ dg_status launch_kd(const void* logits, int64_t ld, int64_t n, int32_t L, int64_
     const int64_t ld_bytes = ld * (DT == 0 ? 2 : 4);
     const cudaError_t e = dghost::launch_pdl(k1_sample_listed<DT>, dim3(grid), dim3(kDWarps * 32), 0, stream,
                                              static_cast<const unsigned char*>(logits), ld_bytes, V, L, params, seed,
-                                             ws, sample, canvas);
+                                             ws, sample, canvas, n * (int64_t)L);
     dghost::count_launch();
     return dghost::cuda_status(e);
 }

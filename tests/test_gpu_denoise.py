@@ -184,14 +184,19 @@ def test_batch_composition_does_not_change_rows():
         assert np.array_equal(outs[0][k][2], s[k][0]), k
 
 
-def test_nan_and_empty_rows_set_status():
+@pytest.mark.parametrize("deferred", [False, True])
+def test_nan_and_empty_rows_set_status(deferred):
+    """NaN, +inf and all -inf rows raise their status bits and leave the valid rows alone.
+    Deferred (no DG_SAMPLE_ALL) with a budget larger than any finite sum: the flagged rows'
+    NaN entropies rank after the valid ones, so every slot of the sampler's list is filled."""
     n, L, V = 1, 5, 64
     x = torch.zeros((n, L, V), dtype=torch.float32)
     x[0, 1, 5] = float("nan")
     x[0, 2, :] = float("-inf")
     x[0, 3, 7] = float("inf")
     x[0, 4, 10:20] = float("-inf")      # some -inf entries are fine
-    p = _params(n, np.random.default_rng(9), temperature=1.0, flags=dg.DG_ACTIVE | dg.DG_SAMPLE_ALL)
+    flags = dg.DG_ACTIVE if deferred else dg.DG_ACTIVE | dg.DG_SAMPLE_ALL
+    p = _params(n, np.random.default_rng(9), temperature=1.0, flags=flags, beta=1e30)
     b = StepBuffers.make(n, L, DEV)
     dg.dg_clear_device_status()
     run_step(x.to(DEV), dg.params_tensor(p, DEV), 1, b)

@@ -226,3 +226,41 @@ def test_lm_head_batched_full_size():
         if g["accept"][c, i] and g["sample"][c, i] != st["sample"]:
             gap = (st["score1"] - st["score2"]) / max(abs(st["score1"]), 1.0)
             assert gap < BOUNDARY, (c, i)
+
+
+def test_lm_head_strided_operands_and_bad_rows():
+    """Row strides past d (hidden [.., d + 8], W [.., d + 16]); a canvas with T = 0 (status
+    DG_DEV_BAD_PARAM, its statistics and decisions left untouched, its logits still written);
+    a NaN in one hidden row (status DG_DEV_NAN_INF_ROW).  The other canvas matches the oracle."""
+    n, L, V, d = 3, 64, 777, 96
+    hb_full = synth.hidden_states(n, L, d + 8, seed=31, kind="int", device=DEV)
+    hidden = hb_full[:, :, :d]
+    Wf = synth.lm_head_weights_int(V, d + 16, seed=32, device=DEV)
+    W = Wf[:, :d]
+    rng = np.random.default_rng(33)
+    p = _params(n, rng, ("normal", "normal", "normal"))
+    p["temperature"][1] = 0.0
+    hidden[2, 5, 3] = float("nan")
+    canvas0 = rng.integers(0, V, (n, L)).astype(np.int32)
+    prev0, stable0 = np.full((n, L), -1, np.int32), np.zeros(n, np.int32)
+    b, logits, _ = _run(hidden, W, p, V, 784, canvas0, prev0, stable0)
+    st = dg.dg_get_device_status()
+    assert st & dg.DG_DEV_BAD_PARAM and st & dg.DG_DEV_NAN_INF_ROW
+    g = b.host()
+    got = synth.bf16_bits(logits)
+    hbits, wbits = synth.bf16_bits(hidden.contiguous()), synth.bf16_bits(W.contiguous())
+    for c in (0, 1):
+        assert np.array_equal(got[c, :, :V], oracle.lm_head_logits(hbits[c], wbits)), c
+    assert np.isnan((got[2, 5, :V].astype(np.uint32) << 16).view(np.float32)).all()
+    # the canvas with T = 0: nothing but its logits written
+    assert (g["entropy"][1] == -1.0).all() and (g["argmax"][1] == -7).all()
+    assert (g["canvas"][1] == canvas0[1]).all() and g["converged"][1] == 7
+    ref = np.zeros((1, L, 784), np.uint16)
+    ref[0] = oracle.lm_head_logits(hbits[0], wbits, ld=784)
+    pc = {k: np.asarray(v)[:1].copy() for k, v in p.items()}
+    o = oracle.denoise_step(ref, pc, SEED, canvas0[:1], prev0[:1], stable0[:1], ld=784, V=V)
+    rep = compare_step({k: v[:1] for k, v in g.items()}, o, pc, V, SEED, canvas0[:1], prev0[:1], stable0[:1])
+    print(rep)
+    # the NaN row is flagged; the rest of its canvas keeps finite statistics
+    rows = np.arange(L) != 5
+    assert np.isfinite(g["entropy"][2][rows]).all()

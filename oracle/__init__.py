@@ -77,6 +77,9 @@ def _load():
         lib.orc_bf16_round_f64.argtypes = [dbl]
         lib.orc_bf16_round_f64.restype = ctypes.c_uint16
         lib.orc_lm_head_logits.argtypes = [P, i64, i32, i64, P, i64, i64, P, i64, P, P, ctypes.c_int]
+        lib.orc_attn_allowed.argtypes = [ctypes.c_int, i64, i64, i64, i64]
+        lib.orc_attn_allowed.restype = ctypes.c_int
+        lib.orc_attention.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i64, dbl, P, P, ctypes.c_int]
         lib.orc_max_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -345,3 +348,33 @@ def lm_head_logits(hidden_bf16, W_bf16, V: int | None = None, ld: int | None = N
     ab = np.zeros((rows, V), np.float64) if exact else None
     lib.orc_lm_head_logits(_ptr(h), rows, d, d, _ptr(W), V, d, _ptr(out), ld, _ptr(ex), _ptr(ab), int(n_threads))
     return (out, ex, ab) if exact else out
+
+
+# ---------------------------------------------------------------- attention
+def attn_allowed(causal: bool, window: int, pos: int, j: int, kv_len: int) -> bool:
+    """Whether query position `pos` may attend to key j (window < 0: no window)."""
+    return bool(_load().orc_attn_allowed(int(bool(causal)), int(window), int(pos), int(j), int(kv_len)))
+
+
+def attention(q_bf16, k_bf16, v_bf16, cu_q, cu_kv, causal, window: int = -1, scale: float | None = None,
+              n_threads: int = 0):
+    """Attention with per-sequence causality and an optional symmetric window (fp64).
+    q [total_q, Hq, D], k / v [total_kv, Hkv, D] as bf16 bit patterns; cu_q / cu_kv [n + 1]
+    int32 offsets; causal [n] flags.  Returns (o [total_q, Hq, D], lse [total_q, Hq])."""
+    lib = _load()
+    q = _c(q_bf16, np.uint16)
+    k = _c(k_bf16, np.uint16)
+    v = _c(v_bf16, np.uint16)
+    total_q, Hq, D = q.shape
+    Hkv = k.shape[1]
+    assert k.shape == v.shape and k.shape[2] == D and Hq % Hkv == 0
+    cq = _c(cu_q, np.int32)
+    ck = _c(cu_kv, np.int32)
+    cz = _c(causal, np.uint8)
+    n = cz.shape[0]
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    o = np.zeros((total_q, Hq, D), np.float64)
+    lse = np.zeros((total_q, Hq), np.float64)
+    lib.orc_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(cq), _ptr(ck), _ptr(cz), n, Hq, Hkv, D, int(window),
+                      scale, _ptr(o), _ptr(lse), int(n_threads))
+    return o, lse

@@ -648,6 +648,86 @@ void orc_lm_head_logits(const uint16_t* hidden, int64_t n_rows, int32_t d, int64
     }
 }
 
+/* ------------------------------------------------------------------------------- */
+/* Attention with per-sequence causality and a symmetric window [DG], sections        */
+/* "시퀀스별로 동적으로 바뀌는 인과 어텐션" (per-sequence dynamic causal attention) and  */
+/* "슬라이딩 윈도우 어텐션도 대칭으로" (the sliding window made symmetric).  A batch     */
+/* mixes requests: a causal one (prefill or commit pass) lets query i see keys j <= its */
+/* own position; a bidirectional one (a denoising canvas) lets every query see every   */
+/* key of its sequence, context and canvas alike.  With a window W >= 0 a causal query */
+/* sees keys in [pos - W, pos] and a bidirectional one keys in [pos - W, pos + W].      */
+/* Reading (the pages give only the figures): a sequence's queries are its last q_len  */
+/* tokens, so query i sits at position kv_len - q_len + i; scores are scale * q . k    */
+/* (no soft-capping); one key/value head serves Hq / Hkv consecutive query heads.      */
+/*   o[i][h] = sum_j softmax_j(scale q_i . k_j over the allowed j) v_j,               */
+/*   lse[i][h] = log sum_j exp(scale q_i . k_j) over the allowed j.                   */
+/* q [total_q][Hq][D], k and v [total_kv][Hkv][D] as bf16 bits; o and lse in fp64.     */
+/* A query with no allowed key gets o = 0 and lse = -inf.                             */
+/* ------------------------------------------------------------------------------- */
+int orc_attn_allowed(int causal, int64_t window, int64_t pos, int64_t j, int64_t kv_len)
+{
+    if (j < 0 || j >= kv_len) return 0;
+    if (causal && j > pos) return 0;
+    if (window >= 0) {
+        if (j < pos - window) return 0;
+        if (!causal && j > pos + window) return 0;
+    }
+    return 1;
+}
+
+void orc_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* cu_q,
+                   const int32_t* cu_kv, const uint8_t* causal, int32_t n_seq, int32_t Hq, int32_t Hkv,
+                   int32_t D, int64_t window, double scale, double* o, double* lse, int n_threads)
+{
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+    int32_t group = Hq / Hkv;
+    for (int32_t s = 0; s < n_seq; ++s) {
+        int64_t q0 = cu_q[s], q_len = cu_q[s + 1] - cu_q[s];
+        int64_t k0 = cu_kv[s], kv_len = cu_kv[s + 1] - cu_kv[s];
+        #pragma omp parallel for collapse(2) schedule(dynamic, 4)
+        for (int64_t i = 0; i < q_len; ++i) {
+            for (int32_t h = 0; h < Hq; ++h) {
+                int64_t pos = kv_len - q_len + i;
+                int32_t hk = h / group;
+                const uint16_t* qi = q + ((q0 + i) * Hq + h) * D;
+                double* oi = o + ((q0 + i) * Hq + h) * D;
+                double* sc = (double*)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1));
+                double m = -INFINITY;
+                for (int64_t j = 0; j < kv_len; ++j) {
+                    sc[j] = -INFINITY;
+                    if (!orc_attn_allowed(causal[s], window, pos, j, kv_len)) continue;
+                    const uint16_t* kj = k + ((k0 + j) * Hkv + hk) * D;
+                    double dot = 0.0;
+                    for (int32_t c = 0; c < D; ++c) dot += orc_bf16(qi[c]) * orc_bf16(kj[c]);
+                    sc[j] = scale * dot;
+                    if (sc[j] > m) m = sc[j];
+                }
+                for (int32_t c = 0; c < D; ++c) oi[c] = 0.0;
+                if (m == -INFINITY) {
+                    lse[(q0 + i) * Hq + h] = -INFINITY;
+                    free(sc);
+                    continue;
+                }
+                double sum = 0.0;
+                for (int64_t j = 0; j < kv_len; ++j) {
+                    if (sc[j] == -INFINITY) continue;
+                    double w = exp(sc[j] - m);
+                    sum += w;
+                    const uint16_t* vj = v + ((k0 + j) * Hkv + hk) * D;
+                    for (int32_t c = 0; c < D; ++c) oi[c] += w * orc_bf16(vj[c]);
+                }
+                for (int32_t c = 0; c < D; ++c) oi[c] /= sum;
+                lse[(q0 + i) * Hq + h] = m + log(sum);
+                free(sc);
+            }
+        }
+    }
+}
+
 int orc_max_threads(void)
 {
 #ifdef _OPENMP

@@ -566,6 +566,44 @@ def run_ours(args):
                     "frac_tc: 2 N V d flops against the sustained bf16 peak; unfused = dg_lm_head_logits "
                     "then dg_denoise_step"}
         del xl, lws, hid
+
+        # Attention with per-sequence causality (timed alone): 8 denoising canvases of 256
+        # after 2048 context tokens (bidirectional) and 4 causal prefills of 1024, 16 query
+        # heads over 8 key/value heads, D = 128, without a window and with W = 512.
+        seqs = [(256, 2304, 0)] * 8 + [(1024, 1024, 1)] * 4
+        cu_q = np.cumsum([0] + [a[0] for a in seqs]).astype(np.int32)
+        cu_kv = np.cumsum([0] + [a[1] for a in seqs]).astype(np.int32)
+        cz = np.array([a[2] for a in seqs], np.uint8)
+        Hq, Hkv, Dh = 16, 8, 128
+        aq, ak, av = synth.attention_inputs(int(cu_q[-1]), int(cu_kv[-1]), Hq, Hkv, Dh, seed=9, device=dev)
+        ao = torch.empty_like(aq)
+        dq, dkv, dcz = (torch.from_numpy(t).to(dev) for t in (cu_q, cu_kv, cz))
+        attn = {}
+        for W in (-1, 512):
+            pairs = 0
+            tiles = tiles_all = 0
+            for ql, kl, c in seqs:
+                pos = np.arange(kl - ql, kl)
+                lo = np.maximum(0, pos - W) if W >= 0 else np.zeros_like(pos)
+                hi = pos if c else (np.minimum(kl - 1, pos + W) if W >= 0 else np.full_like(pos, kl - 1))
+                pairs += int((hi - lo + 1).sum())
+                for t0 in range(0, ql, 128):
+                    p0, p1 = pos[t0], pos[min(ql, t0 + 128) - 1]
+                    jl = max(0, p0 - W) if W >= 0 else 0
+                    jh = p1 if c else (min(kl - 1, p1 + W) if W >= 0 else kl - 1)
+                    tiles += jh // 128 - jl // 128 + 1
+                    tiles_all += (kl + 127) // 128
+            ms = _time(lambda: dg.dg_attention(aq, ak, av, ao, dq, dkv, dcz, 1024, window=W, stream=stream), reps=20)
+            alg = 4.0 * pairs * Dh * Hq
+            exe = 4.0 * tiles * 128 * 128 * Dh * Hq
+            attn["window_%d" % W if W >= 0 else "no_window"] = {
+                "ms": ms, "tflops_allowed": alg / (ms * 1e-3) / 1e12, "tflops_executed": exe / (ms * 1e-3) / 1e12,
+                "frac_tc_executed": exe / (ms * 1e-3) / 1e12 / peak_tc, "tiles_visited": tiles,
+                "tiles_skipped_frac": 1.0 - tiles / tiles_all}
+        attn["note"] = ("dg_attention timed alone; allowed = 4 D flops per allowed (query, key) pair per head, "
+                        "executed = the visited 128 x 128 tiles; frac against the sustained bf16 peak")
+        around["attention"] = attn
+        del aq, ak, av, ao
         torch.cuda.synchronize()
         if dg.dg_get_device_status():
             raise RuntimeError("device status set by the rows around the step")

@@ -1,0 +1,445 @@
+// dg_attn.cu -- attention with per-sequence causality and a symmetric sliding window, on the
+// tensor cores (tcgen05 + TMEM + TMA, sm_103a).
+//
+// Method (DiffusionGemma vLLM page, sections "시퀀스별로 동적으로 바뀌는 인과 어텐션"
+// (per-sequence dynamic causal attention) and "슬라이딩 윈도우 어텐션도 대칭으로" (the sliding
+// window made symmetric)): one batch mixes causal requests (prefill and commit passes: query i
+// sees keys up to its own position) and bidirectional ones (a denoising canvas: every query
+// sees every key of its sequence, context and canvas); attention runs tile by tile and a tile
+// holding only masked entries is skipped, saving its MMAs and its K/V reads.  With a window W
+// a causal query keeps [pos - W, pos] and a canvas query [pos - W, pos + W].  A sequence's
+// queries are its last q_len tokens (query i sits at kv_len - q_len + i); that and the score
+// scale * q.k without soft-capping are readings, the pages give only the figures.
+//
+// One CTA per (128-query tile, query head, sequence); one pass with an online softmax:
+//   warp 0      TMA producer: the Q tile once, then K and V tiles (128 keys) in a 2-stage ring;
+//   warp 1      MMA issuer (one elected thread): S = Q K^T into one of two TMEM buffers while the
+//               softmax works on the other, O += P V into a third;
+//   warps 2..5  softmax, one query row per thread (its TMEM lane): the row of S, the mask on
+//               tiles that are not wholly allowed, P = 2^(x - m) in bf16 into shared memory for
+//               the P V MMA, the row sum.  The reference m only moves when a row's maximum grows
+//               by more than 8 (in log2 units), so P < 2^8 and most tiles leave O alone; when it
+//               moves, the row of O is rescaled in TMEM (tcgen05.ld, multiply, tcgen05.st)
+//               between two P V MMAs.  At the end O / l goes out in bf16 with the row's lse.
+// Only key tiles holding an allowed key for some query of the tile are visited.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <math.h>
+
+#include <algorithm>
+
+#include "dg_common.cuh"
+
+namespace {
+
+constexpr int kTile = 128;      // queries per CTA and keys per tile
+constexpr int kHead = 128;      // head dimension D
+constexpr int kSub = 64;        // columns per 128-byte swizzle atom
+constexpr uint32_t kSubBytes = kTile * kSub * 2;   // 16 KB: one 128 x 64 bf16 atom block
+constexpr uint32_t kTileBytes = 2 * kSubBytes;     // 32 KB: 128 x 128 bf16
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleAbove = 8.f;  // log2 units: P stays below 2^8 between rescales
+
+struct AttnArgs {
+    const int32_t* cu_q;    // [n + 1] query offsets
+    const int32_t* cu_kv;   // [n + 1] key offsets
+    const uint8_t* causal;  // [n]
+    uint16_t* o;            // [total_q][Hq][D] bf16
+    float* lse;             // [total_q][Hq] or null
+    int32_t Hq, Hkv, window;
+    int64_t total_q, total_kv;
+    float scale_log2;       // scale * log2(e)
+    unsigned* status;
+};
+
+struct __align__(8) AttnShared {
+    uint64_t qfull;
+    uint64_t kvfull[2];
+    uint64_t kvempty[2];
+    uint64_t sfull[2];
+    uint64_t sempty[2];
+    uint64_t pfull;
+    uint64_t pvdone;
+    uint64_t mmadone;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// shared memory: Q | K[2] | V[2] | P, each 32 KB and 1024-aligned, then the barriers
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kTileBytes;
+constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;
+constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;
+constexpr uint32_t kOffBar = kOffP + kTileBytes;
+constexpr size_t kAttnSmem = 1024 + kOffBar + sizeof(AttnShared) + 64;
+static_assert(kAttnSmem <= 232448, "fits the opt-in shared memory of an SM");
+
+// Whether the query at position pos may see key j of a sequence of kv_len keys.
+DG_DEVINL bool allowed(bool causal, int window, int pos, int j, int kv_len) {
+    if (j >= kv_len) return false;
+    if (causal && j > pos) return false;
+    if (window >= 0) {
+        if (j < pos - window) return false;
+        if (!causal && j > pos + window) return false;
+    }
+    return true;
+}
+
+// The key tiles a query tile visits, and whether a key tile is allowed for all its queries.
+struct TileRange {
+    int q0, ql, k0, kl;   // sequence offsets and lengths
+    int pmin, pmax;       // positions of the tile's first and last real query
+    int jt_lo, nt;        // first key tile and count
+    bool causal;
+};
+
+DG_DEVINL TileRange tile_range(const AttnArgs& a, int s, int t) {
+    TileRange r;
+    r.q0 = a.cu_q[s];
+    r.ql = a.cu_q[s + 1] - r.q0;
+    r.k0 = a.cu_kv[s];
+    r.kl = a.cu_kv[s + 1] - r.k0;
+    r.causal = a.causal[s] != 0;
+    const int off = r.kl - r.ql;
+    r.pmin = off + t * kTile;
+    r.pmax = off + min(r.ql, t * kTile + kTile) - 1;
+    const int W = a.window;
+    const int jlo = W >= 0 ? max(0, r.pmin - W) : 0;
+    const int jhi = r.causal ? r.pmax : (W >= 0 ? min(r.kl - 1, r.pmax + W) : r.kl - 1);
+    r.jt_lo = jlo / kTile;
+    r.nt = jhi >= jlo ? jhi / kTile - r.jt_lo + 1 : 0;
+    return r;
+}
+
+DG_DEVINL bool tile_full(const TileRange& r, int window, int jt) {
+    const int j0 = jt * kTile, j1 = j0 + kTile - 1;
+    if (j1 >= r.kl) return false;
+    if (r.causal && j1 > r.pmin) return false;
+    if (window >= 0) {
+        if (j0 < r.pmax - window) return false;
+        if (!r.causal && j1 > r.pmin + window) return false;
+    }
+    return true;
+}
+
+DG_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t v;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(v) : "f"(hi), "f"(lo));
+    return v;
+}
+
+DG_DEVINL float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+DG_DEVINL bool aborted(const AttnShared& sh) { return *(volatile const int*)&sh.abort_flag != 0; }
+
+DG_DEVINL void do_abort(AttnShared& sh, unsigned* status) {
+    *(volatile int*)&sh.abort_flag = 1;
+    dg::raise_status(status, DG_DEV_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ the kernel
+__global__ void __launch_bounds__(192, 1)
+    k_attention(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+    extern __shared__ __align__(1024) unsigned char attn_smem_raw[];
+    unsigned char* smem =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(attn_smem_raw) + 1023) & ~uintptr_t(1023));
+    AttnShared& sh = *reinterpret_cast<AttnShared*>(smem + kOffBar);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+    const TileRange r = tile_range(a, s, t);
+    if (threadIdx.x == 0 && t == (int)gridDim.x - 1 && r.ql > (int)gridDim.x * kTile)
+        dg::raise_status(a.status, DG_DEV_BAD_PARAM);  // max_q_len below this sequence's queries
+    if (t * kTile >= r.ql) return;  // the whole CTA: past the sequence's queries
+    // offsets inside the buffers, and the queries the sequence's last tokens
+    if (r.q0 < 0 || r.k0 < 0 || (int64_t)r.q0 + r.ql > a.total_q || (int64_t)r.k0 + r.kl > a.total_kv ||
+        r.ql > r.kl || r.nt <= 0) {
+        if (threadIdx.x == 0) dg::raise_status(a.status, DG_DEV_BAD_PARAM);
+        return;
+    }
+    const int hk = h / (a.Hq / a.Hkv);
+
+    if (threadIdx.x == 0) {
+        dg::mbar_init(&sh.qfull, 1);
+        for (int i = 0; i < 2; ++i) {
+            dg::mbar_init(&sh.kvfull[i], 1);
+            dg::mbar_init(&sh.kvempty[i], 1);
+            dg::mbar_init(&sh.sfull[i], 1);
+            dg::mbar_init(&sh.sempty[i], 4);  // one arrival per softmax warp
+        }
+        dg::mbar_init(&sh.pfull, 4);
+        dg::mbar_init(&sh.pvdone, 1);
+        dg::mbar_init(&sh.mmadone, 1);
+        sh.abort_flag = 0;
+        dg::fence_mbar_init();
+    }
+    if (warp == 1) {
+        dg::tmem_alloc(&sh.tmem_base, 512);  // S buffers at columns 0 and 128, O at 256
+        dg::tmem_relinquish();
+    }
+    dg::tc_fence_before();
+    __syncthreads();
+    dg::tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+    const uint32_t sQ = dg::smem_u32(smem + kOffQ);
+    const uint32_t sP = dg::smem_u32(smem + kOffP);
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            dg::prefetch_tmap(&tmQ);
+            dg::prefetch_tmap(&tmK);
+            dg::prefetch_tmap(&tmV);
+            const int qrow = r.q0 + t * kTile;
+            dg::mbar_arrive_expect_tx(&sh.qfull, kTileBytes);
+            dg::tma_load_2d(smem + kOffQ, &tmQ, h * kHead, qrow, &sh.qfull);
+            dg::tma_load_2d(smem + kOffQ + kSubBytes, &tmQ, h * kHead + kSub, qrow, &sh.qfull);
+            int issued[2] = {0, 0};
+            for (int i = 0; i < r.nt && !aborted(sh); ++i) {
+                const int st = i & 1;
+                if (!dg::mbar_wait(&sh.kvempty[st], (((uint32_t)i >> 1) & 1u) ^ 1u)) {
+                    do_abort(sh, a.status);
+                    break;
+                }
+                dg::mbar_arrive_expect_tx(&sh.kvfull[st], 2 * kTileBytes);
+                const int krow = r.k0 + (r.jt_lo + i) * kTile;
+                unsigned char* sk = smem + kOffK + st * kTileBytes;
+                unsigned char* sv = smem + kOffV + st * kTileBytes;
+                dg::tma_load_2d(sk, &tmK, hk * kHead, krow, &sh.kvfull[st]);
+                dg::tma_load_2d(sk + kSubBytes, &tmK, hk * kHead + kSub, krow, &sh.kvfull[st]);
+                dg::tma_load_2d(sv, &tmV, hk * kHead, krow, &sh.kvfull[st]);
+                dg::tma_load_2d(sv + kSubBytes, &tmV, hk * kHead + kSub, krow, &sh.kvfull[st]);
+                ++issued[st];
+            }
+            if (aborted(sh)) {  // never leave with a copy still landing in shared memory
+                (void)dg::mbar_wait(&sh.qfull, 0);
+                for (int st = 0; st < 2; ++st)
+                    if (issued[st] > 0) (void)dg::mbar_wait(&sh.kvfull[st], (uint32_t)(issued[st] - 1) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = dg::instr_desc(kTile, kTile, false);  // S = Q K^T: K tile K-major
+            constexpr uint32_t idO = dg::instr_desc(kTile, kHead, true);   // O += P V: V rows are N-major
+            bool ok = dg::mbar_wait(&sh.qfull, 0);
+            for (int i = 0; ok && i <= r.nt && !aborted(sh); ++i) {
+                if (i < r.nt) {  // S_i into buffer i % 2
+                    const int st = i & 1;
+                    const uint32_t ph = ((uint32_t)i >> 1) & 1u;
+                    if (!dg::mbar_wait(&sh.kvfull[st], ph) || !dg::mbar_wait(&sh.sempty[st], ph ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    dg::tc_fence_after();
+                    const uint32_t sK = dg::smem_u32(smem + kOffK + st * kTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kHead / 16; ++kk) {
+                        const uint32_t off = (uint32_t)(kk >> 2) * kSubBytes + (uint32_t)(kk & 3) * 32u;
+                        dg::tc_mma_f16(tmem + (uint32_t)(st * kTile), dg::smem_desc(sQ + off, 16, 1024, 128),
+                                       dg::smem_desc(sK + off, 16, 1024, 128), idS, kk > 0 ? 1u : 0u);
+                    }
+                    dg::tc_commit(&sh.sfull[st]);
+                }
+                if (i >= 1) {  // O += P_{i-1} V_{i-1} once the softmax has written P
+                    const int j = i - 1, st = j & 1;
+                    if (!dg::mbar_wait(&sh.pfull, (uint32_t)j & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    dg::tc_fence_after();
+                    const uint32_t sV = dg::smem_u32(smem + kOffV + st * kTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                        // A: P rows, keys in two 64-wide atoms; B: 16 V rows (keys) x 128 columns
+                        // (two 64-column atoms, kSubBytes apart)
+                        const uint32_t offp = (uint32_t)(kk >> 2) * kSubBytes + (uint32_t)(kk & 3) * 32u;
+                        dg::tc_mma_f16(tmem + 256u, dg::smem_desc(sP + offp, 16, 1024, 128),
+                                       dg::smem_desc(sV + (uint32_t)kk * 16u * 128u, kSubBytes, 1024, 128), idO,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    dg::tc_commit(&sh.pvdone);
+                    dg::tc_commit(&sh.kvempty[st]);
+                }
+            }
+            if (!ok) do_abort(sh, a.status);
+            // every MMA issued above has completed before the tensor memory is released
+            dg::tc_commit(&sh.mmadone);
+            (void)dg::mbar_wait(&sh.mmadone, 0);
+        }
+    } else {
+        // ------------------------------------------------ softmax (warps 2..5), one row per thread
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const int pos = r.kl - r.ql + t * kTile + row;
+        const bool row_valid = t * kTile + row < r.ql;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int i = 0; i < r.nt; ++i) {
+            const int sb = i & 1;
+            if (!dg::mbar_wait_warp(&sh.sfull[sb], ((uint32_t)i >> 1) & 1u)) {
+                ok = false;
+                break;
+            }
+            dg::tc_fence_after();
+            float x[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) dg::tmem_ld32(tmem + lane_base + (uint32_t)(sb * kTile + c * 32), x[c]);
+            dg::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) dg::mbar_arrive(&sh.sempty[sb]);  // S buffer free for S_{i+2}
+            const int jt = r.jt_lo + i;
+            const bool full = tile_full(r, a.window, jt);
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    float v = x[c][e] * a.scale_log2;
+                    if (!full && !allowed(r.causal, a.window, pos, jt * kTile + c * 32 + e, r.kl)) v = -INFINITY;
+                    x[c][e] = v;
+                    tmax = fmaxf(tmax, v);
+                }
+            }
+            // P V of the previous tile must be done before P or O is touched
+            if (i > 0) {
+                if (!dg::mbar_wait_warp(&sh.pvdone, (uint32_t)(i - 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                dg::tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, tmax > m_ref + kRescaleAbove)) {  // m_ref = -inf: any finite max
+                const float m_new = fmaxf(m_ref, tmax);
+                const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_ref - m_new);
+                l *= alpha;
+                if (i > 0) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float o[32];
+                        const uint32_t ta = tmem + lane_base + 256u + (uint32_t)(c * 32);
+                        dg::tmem_ld32(ta, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                        dg::tmem_st32(ta, o);
+                    }
+                    dg::tmem_st_wait();
+                }
+                m_ref = m_new;
+            }
+            // P = 2^(x - m_ref) in bf16, 8 keys per 16-byte chunk, swizzled like a TMA tile
+            unsigned char* prow = smem + kOffP + (uint32_t)row * 128u;
+            float sum = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) {
+                const int c = ch >> 2, e0 = (ch & 3) * 8;
+                float p[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float v = x[c][e0 + e];
+                    p[e] = (v == -INFINITY) ? 0.f : ex2(v - m_ref);
+                    sum += p[e];
+                }
+                const uint32_t off = (uint32_t)(ch >> 3) * kSubBytes + (uint32_t)(((ch & 7) ^ (row & 7)) << 4);
+                *reinterpret_cast<uint4*>(prow + off) = make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
+                                                                   pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
+            }
+            l += sum;
+            dg::fence_proxy_async_smem();  // the generic-proxy stores, visible to the MMA
+            dg::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) dg::mbar_arrive(&sh.pfull);
+        }
+        if (ok && !dg::mbar_wait_warp(&sh.pvdone, (uint32_t)(r.nt - 1) & 1u)) ok = false;
+        if (ok) {
+            dg::tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const int64_t qi = (int64_t)r.q0 + t * kTile + row;
+            uint16_t* orow = a.o + (qi * a.Hq + h) * kHead;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float o[32];
+                dg::tmem_ld32(tmem + lane_base + 256u + (uint32_t)(c * 32), o);
+                if (row_valid) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8)
+                        *reinterpret_cast<uint4*>(orow + c * 32 + e) =
+                            make_uint4(pack_bf16x2(o[e] * inv, o[e + 1] * inv), pack_bf16x2(o[e + 2] * inv, o[e + 3] * inv),
+                                       pack_bf16x2(o[e + 4] * inv, o[e + 5] * inv), pack_bf16x2(o[e + 6] * inv, o[e + 7] * inv));
+                }
+            }
+            if (row_valid && a.lse) a.lse[qi * a.Hq + h] = (m_ref + log2f(l)) * kLn2;
+        } else {
+            do_abort(sh, a.status);
+        }
+    }
+
+    dg::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        dg::tc_fence_after();
+        dg::tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ host side
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// [rows][heads * D] bf16 with 128 x 64 boxes (one 128-byte swizzle atom of 128 rows).
+bool tmap_heads(CUtensorMap* tm, const void* base, int64_t rows, int32_t heads) {
+    uint64_t dims[2] = {(uint64_t)heads * kHead, (uint64_t)rows};
+    uint64_t strides[1] = {(uint64_t)heads * kHead * 2};
+    uint32_t box[2] = {(uint32_t)kSub, (uint32_t)kTile};
+    return dghost::encode_tmap(tm, 0, 2, const_cast<void*>(base), dims, strides, box, 128);
+}
+
+}  // namespace
+
+extern "C" dg_status dg_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse,
+                                  const int32_t* cu_q, const int32_t* cu_kv, const uint8_t* causal, int32_t n_seq,
+                                  int32_t max_q_len, int64_t total_q, int64_t total_kv, int32_t Hq, int32_t Hkv,
+                                  int32_t D, int32_t window, float scale, dg_stream_t stream) {
+    if (n_seq < 0 || n_seq > 65535 || Hq < 1 || Hq > 65535 || Hkv < 1 || Hq % Hkv != 0 || window < -1 ||
+        !(scale == scale) || scale == INFINITY || scale == -INFINITY)
+        return DG_ERR_INVALID_ARG;
+    if (D != kHead) return DG_ERR_UNSUPPORTED;
+    if (n_seq == 0) return DG_OK;
+    if (max_q_len < 1 || max_q_len > (1 << 30) || total_q < 1 || total_kv < 1 || total_q >= (1LL << 31) ||
+        total_kv >= (1LL << 31))
+        return DG_ERR_INVALID_ARG;
+    if (!q || !k || !v || !o || !cu_q || !cu_kv || !causal) return DG_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return DG_ERR_ALIGNMENT;
+    CUtensorMap tq, tk, tv;
+    if (!tmap_heads(&tq, q, total_q, Hq) || !tmap_heads(&tk, k, total_kv, Hkv) || !tmap_heads(&tv, v, total_kv, Hkv))
+        return DG_ERR_CUDA;
+    if (cudaFuncSetAttribute(k_attention, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttnSmem) != cudaSuccess)
+        return DG_ERR_CUDA;
+    AttnArgs a;
+    a.cu_q = cu_q;
+    a.cu_kv = cu_kv;
+    a.causal = causal;
+    a.o = o;
+    a.lse = lse;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.window = window;
+    a.total_q = total_q;
+    a.total_kv = total_kv;
+    a.scale_log2 = scale * kLog2e;
+    a.status = dghost::status_word();
+    const dim3 grid((unsigned)((max_q_len + kTile - 1) / kTile), (unsigned)Hq, (unsigned)n_seq);
+    k_attention<<<grid, 192, kAttnSmem, (cudaStream_t)stream>>>(tq, tk, tv, a);
+    dghost::count_launch();
+    return dghost::cuda_status(cudaGetLastError());
+}

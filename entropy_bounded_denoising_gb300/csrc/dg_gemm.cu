@@ -143,22 +143,8 @@ struct Cfg {
 };
 
 // ------------------------------------------------------------------ descriptors
-// Shared-memory matrix descriptor (tcgen05): start >> 4 in bits 0..13, leading byte offset
-// >> 4 in 16..29, stride byte offset >> 4 in 32..45, version 1 in 46..47, layout in 61..63
-// (2 = 128-byte swizzle, 4 = 64-byte swizzle).
-DG_DEVINL uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, int swizzle_bytes) {
-    const uint64_t layout = swizzle_bytes == 128 ? 2ull : 4ull;
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (layout << 61);
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulator (bit 4), bf16 A (bits 7..9 = 1) and
-// B (bits 10..12 = 1), A K-major (bit 15 = 0), B major in bit 16, N >> 3 in 17..22,
-// M >> 4 in 24..28.
-__host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
-}
+using dg::instr_desc;
+using dg::smem_desc;
 
 // ------------------------------------------------------------------ scheduling
 struct Item {

@@ -16,7 +16,9 @@ workloads this library is measured on):
   * E, W_gate, W_up, W_down ~ N(0, 0.02^2), rounded to bf16;
   * for the LM head, hidden states h_i = s_i z / (0.02 sqrt(d)) with z ~ N(0, 1), so that
     hidden . E^T has the same per-position spread s_i; or small-integer operands (k / 8,
-    |k| <= 12 for hidden, <= 4 for W) whose dot products fp32 sums exactly.
+    |k| <= 12 for hidden, <= 4 for W) whose dot products fp32 sums exactly;
+  * for attention, q ~ N(0, s_t^2) per token with s_t ~ U[0.5, 4] (scores from flat to peaked
+    at the scale 1/sqrt(D)), k and v ~ N(0, 1), all bf16.
 Every draw comes from a torch generator seeded from (seed, purpose, canvas), so the bytes
 do not depend on how canvases are chunked; CPU and CUDA generators give different (each
 reproducible) streams, and a test always hands the same bytes to both sides.
@@ -32,7 +34,7 @@ import torch
 ACTIVE, READ_ONLY, SELF_COND, SAMPLE_ALL = 1, 2, 4, 8
 
 # purposes for seeding (arbitrary distinct constants)
-_P_BASE, _P_SCALE, _P_NOISE, _P_SPIKE, _P_WEIGHT, _P_PARAMS, _P_HIDDEN = 11, 23, 37, 41, 53, 67, 79
+_P_BASE, _P_SCALE, _P_NOISE, _P_SPIKE, _P_WEIGHT, _P_PARAMS, _P_HIDDEN, _P_ATTN = 11, 23, 37, 41, 53, 67, 79, 83
 
 
 def _gen(device, *parts: int) -> torch.Generator:
@@ -146,6 +148,16 @@ def lm_head_weights_int(V: int, d: int, *, seed: int, device="cpu") -> torch.Ten
     """W_lm [V, d] bf16 with entries k / 8, k uniform in [-4, 4]."""
     k = torch.randint(-4, 5, (V, d), generator=_gen(device, seed, _P_WEIGHT, 5), device=device).float()
     return (k / 8.0).to(torch.bfloat16)
+
+
+def attention_inputs(total_q: int, total_kv: int, Hq: int, Hkv: int, D: int, *, seed: int, device="cpu"):
+    """q [total_q, Hq, D], k and v [total_kv, Hkv, D] in bf16 (see the module recipe)."""
+    g = _gen(device, seed, _P_ATTN, 0)
+    s = torch.empty((total_q, 1, 1), device=device).uniform_(0.5, 4.0, generator=g)
+    q = (torch.randn((total_q, Hq, D), generator=g, device=device) * s).to(torch.bfloat16)
+    k = torch.randn((total_kv, Hkv, D), generator=g, device=device).to(torch.bfloat16)
+    v = torch.randn((total_kv, Hkv, D), generator=g, device=device).to(torch.bfloat16)
+    return q, k, v
 
 
 def canvas_params(wl: Workload, step: int = 0):

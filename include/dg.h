@@ -274,6 +274,35 @@ DG_API dg_status dg_lm_head_denoise_step(const uint16_t* hidden, int64_t ldh, co
                                          void* workspace, size_t workspace_bytes, dg_stream_t stream);
 
 /* ------------------------------------------------------------------------------------ */
+/* Attention with per-sequence causality [DG "시퀀스별로 동적으로 바뀌는 인과 어텐션",       */
+/* "슬라이딩 윈도우 어텐션도 대칭으로"]: one batch mixes causal requests (prefill / commit   */
+/* passes) and bidirectional ones (a denoising canvas, which sees its context and the whole */
+/* canvas); key tiles that hold no allowed key are skipped (neither loaded nor multiplied). */
+/* ------------------------------------------------------------------------------------ */
+
+/* o[i][h] = softmax over the allowed keys j of (scale * q[i][h] . k[j][h']) applied to v,
+ * h' = h / (Hq / Hkv), for every query of n_seq sequences.  Sequence s owns queries
+ * cu_q[s] .. cu_q[s+1]-1 and keys cu_kv[s] .. cu_kv[s+1]-1; its queries are its last
+ * q_len = cu_q[s+1] - cu_q[s] tokens, so query i sits at position kv_len - q_len + i.  Key j
+ * is allowed when j < kv_len and, for causal[s] != 0, j <= position; with window >= 0 also
+ * j >= position - window and, for a bidirectional sequence, j <= position + window.
+ *   q    (device) [total_q][Hq][D] bf16;  k, v (device) [total_kv][Hkv][D] bf16.
+ *   o    (device, out) [total_q][Hq][D] bf16.
+ *   lse  (device, out, may be NULL) [total_q][Hq] float: log sum exp of the allowed scores.
+ *   cu_q, cu_kv (device) [n_seq + 1] int32 offsets (non-decreasing); causal (device) [n_seq].
+ *   max_q_len: at least every sequence's q_len (a smaller one leaves queries out and raises
+ *   DG_DEV_BAD_PARAM); a sequence with q_len > kv_len or offsets outside [0, total_q] /
+ *   [0, total_kv] raises DG_DEV_BAD_PARAM and is skipped (its rows of o are not written).
+ * D must be 128 (else DG_ERR_UNSUPPORTED); Hq a multiple of Hkv; window >= -1 (-1: none);
+ * total_q, total_kv < 2^31; q, k, v, o 16-byte aligned.  Computed on the tensor cores
+ * (tcgen05, bf16 operands, fp32 accumulation and softmax, one pass).  One kernel launch. */
+DG_API dg_status dg_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
+                              float* lse, const int32_t* cu_q, const int32_t* cu_kv,
+                              const uint8_t* causal, int32_t n_seq, int32_t max_q_len,
+                              int64_t total_q, int64_t total_kv, int32_t Hq, int32_t Hkv, int32_t D,
+                              int32_t window, float scale, dg_stream_t stream);
+
+/* ------------------------------------------------------------------------------------ */
 /* Self-conditioning [DG "자기 조건화"]:                                                  */
 /*   pe    = P . E,  P = softmax(logits / T) per position, E the token embedding table;  */
 /*   delta = W_down (gelu_tanh(W_gate pe) * (W_up pe)), no bias (gated MLP).            */

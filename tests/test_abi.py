@@ -104,6 +104,23 @@ def test_lm_head_validation_without_gpu():
     assert step(*args[:4], 0, *args[5:], *([None] * 11), None, 0, None) == dg.DG_OK
 
 
+def test_attention_validation_without_gpu():
+    lib = dg.load()
+
+    def call(q=16, k=16, v=16, o=16, n=1, mq=4, tq=4, tk=8, Hq=2, Hkv=1, D=128, W=-1, scale=0.1):
+        return lib.dg_attention(q, k, v, o, None, 16, 16, 16, n, mq, tq, tk, Hq, Hkv, D, W, scale, None)
+
+    assert call(D=64) == dg.DG_ERR_UNSUPPORTED
+    assert call(Hq=3, Hkv=2) == dg.DG_ERR_INVALID_ARG
+    assert call(W=-2) == dg.DG_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == dg.DG_ERR_INVALID_ARG
+    assert call(mq=0) == dg.DG_ERR_INVALID_ARG
+    assert call(tk=0) == dg.DG_ERR_INVALID_ARG
+    assert call(q=None) == dg.DG_ERR_INVALID_ARG
+    assert call(o=24) == dg.DG_ERR_ALIGNMENT
+    assert call(n=0, q=None) == dg.DG_OK
+
+
 def test_params_record_layout():
     import numpy as np
     p = {"temperature": np.float32([0.5]), "beta": np.float32([2.0]), "tau": np.float32([0.25]),

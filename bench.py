@@ -588,7 +588,7 @@ def run_ours(args):
                 hi = pos if c else (np.minimum(kl - 1, pos + W) if W >= 0 else np.full_like(pos, kl - 1))
                 pairs += int((hi - lo + 1).sum())
                 for t0 in range(0, ql, 128):
-                    p0, p1 = pos[t0], pos[min(ql, t0 + 128) - 1]
+                    p0, p1 = int(pos[t0]), int(pos[min(ql, t0 + 128) - 1])
                     jl = max(0, p0 - W) if W >= 0 else 0
                     jh = p1 if c else (min(kl - 1, p1 + W) if W >= 0 else kl - 1)
                     tiles += jh // 128 - jl // 128 + 1
@@ -598,7 +598,7 @@ def run_ours(args):
             exe = 4.0 * tiles * 128 * 128 * Dh * Hq
             attn["window_%d" % W if W >= 0 else "no_window"] = {
                 "ms": ms, "tflops_allowed": alg / (ms * 1e-3) / 1e12, "tflops_executed": exe / (ms * 1e-3) / 1e12,
-                "frac_tc_executed": exe / (ms * 1e-3) / 1e12 / peak_tc, "tiles_visited": tiles,
+                "frac_tc_executed": exe / (ms * 1e-3) / 1e12 / peak_tc, "tiles_visited": int(tiles),
                 "tiles_skipped_frac": 1.0 - tiles / tiles_all}
         attn["note"] = ("dg_attention timed alone; allowed = 4 D flops per allowed (query, key) pair per head, "
                         "executed = the visited 128 x 128 tiles; frac against the sustained bf16 peak")

@@ -15,9 +15,10 @@
 //   warp 0      TMA producer: the Q tile once, then K and V tiles (128 keys) in a 2-stage ring;
 //   warp 1      MMA issuer (one elected thread): S = Q K^T into one of two TMEM buffers while the
 //               softmax works on the other, O += P V into a third;
-//   warps 2..5  softmax, one query row per thread (its TMEM lane): the row of S, the mask on
-//               tiles that are not wholly allowed, P = 2^(x - m) in bf16 into shared memory for
-//               the P V MMA, the row sum.  The reference m only moves when a row's maximum grows
+//   warps 2..9  softmax, two warps per TMEM lane quarter, each thread one query row (its TMEM
+//               lane) and 64 of its 128 columns: the row of S, the mask on tiles that are not
+//               wholly allowed, the row maximum shared with the other half through shared
+//               memory, P = 2^(x - m) in bf16 into shared memory for the P V MMA, the row sum.  The reference m only moves when a row's maximum grows
 //               by more than 8 (in log2 units), so P < 2^8 and most tiles leave O alone; when it
 //               moves, the row of O is rescaled in TMEM (tcgen05.ld, multiply, tcgen05.st)
 //               between two P V MMAs.  At the end O / l goes out in bf16 with the row's lse.
@@ -63,8 +64,11 @@ struct __align__(8) AttnShared {
     uint64_t pfull;
     uint64_t pvdone;
     uint64_t mmadone;
+    uint64_t xbar[4];         // per lane quarter: both halves have posted their row values
     uint32_t tmem_base;
     int abort_flag;
+    float xmax[2][2][kTile];  // [tile parity][column half][row]: the halves' row maxima
+    float xsum[2][kTile];     // [column half][row]: the halves' row sums, at the end
 };
 
 // shared memory: Q | K[2] | V[2] | P, each 32 KB and 1024-aligned, then the barriers
@@ -136,6 +140,46 @@ DG_DEVINL float ex2(float x) {
     return y;
 }
 
+// Barrier waits on the per-tile critical path: polled without a suspend-time hint (a
+// suspended thread wakes late next to this loop's ~1 us per tile), still bounded.
+#ifndef DG_ATTN_HINT_NS
+#define DG_ATTN_HINT_NS 0
+#endif
+DG_DEVINL bool attn_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+#if DG_ATTN_HINT_NS > 0
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(dg::smem_u32(bar)), "r"(parity), "r"((uint32_t)DG_ATTN_HINT_NS)
+        : "memory");
+#else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(dg::smem_u32(bar)), "r"(parity)
+        : "memory");
+#endif
+    return ok != 0;
+}
+
+DG_DEVINL bool attn_wait(uint64_t* bar, uint32_t parity) {
+    for (uint32_t i = 0; i < 4u * dg::kWaitPolls; ++i)
+        if (attn_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// Whole warp: lane 0 polls, then the warp synchronises.
+DG_DEVINL bool attn_wait_warp(uint64_t* bar, uint32_t parity) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = attn_wait(bar, parity) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
 DG_DEVINL bool aborted(const AttnShared& sh) { return *(volatile const int*)&sh.abort_flag != 0; }
 
 DG_DEVINL void do_abort(AttnShared& sh, unsigned* status) {
@@ -144,7 +188,10 @@ DG_DEVINL void do_abort(AttnShared& sh, unsigned* status) {
 }
 
 // ------------------------------------------------------------------ the kernel
-__global__ void __launch_bounds__(192, 1)
+constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quarter, 64 columns each
+constexpr int kThreads = 64 + 32 * kSoftmaxWarps;
+
+__global__ void __launch_bounds__(kThreads, 1)
     k_attention(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
     extern __shared__ __align__(1024) unsigned char attn_smem_raw[];
@@ -171,11 +218,12 @@ __global__ void __launch_bounds__(192, 1)
             dg::mbar_init(&sh.kvfull[i], 1);
             dg::mbar_init(&sh.kvempty[i], 1);
             dg::mbar_init(&sh.sfull[i], 1);
-            dg::mbar_init(&sh.sempty[i], 4);  // one arrival per softmax warp
+            dg::mbar_init(&sh.sempty[i], kSoftmaxWarps);  // one arrival per softmax warp
         }
-        dg::mbar_init(&sh.pfull, 4);
+        dg::mbar_init(&sh.pfull, kSoftmaxWarps);
         dg::mbar_init(&sh.pvdone, 1);
         dg::mbar_init(&sh.mmadone, 1);
+        for (int i = 0; i < 4; ++i) dg::mbar_init(&sh.xbar[i], 2);  // one arrival per half's warp
         sh.abort_flag = 0;
         dg::fence_mbar_init();
     }
@@ -203,7 +251,7 @@ __global__ void __launch_bounds__(192, 1)
             int issued[2] = {0, 0};
             for (int i = 0; i < r.nt && !aborted(sh); ++i) {
                 const int st = i & 1;
-                if (!dg::mbar_wait(&sh.kvempty[st], (((uint32_t)i >> 1) & 1u) ^ 1u)) {
+                if (!attn_wait(&sh.kvempty[st], (((uint32_t)i >> 1) & 1u) ^ 1u)) {
                     do_abort(sh, a.status);
                     break;
                 }
@@ -218,9 +266,9 @@ __global__ void __launch_bounds__(192, 1)
                 ++issued[st];
             }
             if (aborted(sh)) {  // never leave with a copy still landing in shared memory
-                (void)dg::mbar_wait(&sh.qfull, 0);
+                (void)attn_wait(&sh.qfull, 0);
                 for (int st = 0; st < 2; ++st)
-                    if (issued[st] > 0) (void)dg::mbar_wait(&sh.kvfull[st], (uint32_t)(issued[st] - 1) & 1u);
+                    if (issued[st] > 0) (void)attn_wait(&sh.kvfull[st], (uint32_t)(issued[st] - 1) & 1u);
             }
         }
     } else if (warp == 1) {
@@ -228,12 +276,12 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             constexpr uint32_t idS = dg::instr_desc(kTile, kTile, false);  // S = Q K^T: K tile K-major
             constexpr uint32_t idO = dg::instr_desc(kTile, kHead, true);   // O += P V: V rows are N-major
-            bool ok = dg::mbar_wait(&sh.qfull, 0);
+            bool ok = attn_wait(&sh.qfull, 0);
             for (int i = 0; ok && i <= r.nt && !aborted(sh); ++i) {
                 if (i < r.nt) {  // S_i into buffer i % 2
                     const int st = i & 1;
                     const uint32_t ph = ((uint32_t)i >> 1) & 1u;
-                    if (!dg::mbar_wait(&sh.kvfull[st], ph) || !dg::mbar_wait(&sh.sempty[st], ph ^ 1u)) {
+                    if (!attn_wait(&sh.kvfull[st], ph) || !attn_wait(&sh.sempty[st], ph ^ 1u)) {
                         ok = false;
                         break;
                     }
@@ -249,7 +297,7 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 if (i >= 1) {  // O += P_{i-1} V_{i-1} once the softmax has written P
                     const int j = i - 1, st = j & 1;
-                    if (!dg::mbar_wait(&sh.pfull, (uint32_t)j & 1u)) {
+                    if (!attn_wait(&sh.pfull, (uint32_t)j & 1u)) {
                         ok = false;
                         break;
                     }
@@ -271,60 +319,84 @@ __global__ void __launch_bounds__(192, 1)
             if (!ok) do_abort(sh, a.status);
             // every MMA issued above has completed before the tensor memory is released
             dg::tc_commit(&sh.mmadone);
-            (void)dg::mbar_wait(&sh.mmadone, 0);
+            (void)attn_wait(&sh.mmadone, 0);
         }
     } else {
-        // ------------------------------------------------ softmax (warps 2..5), one row per thread
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // ------------------------------------------------ softmax (warps 2..9): one query row and
+        // 64 of the 128 columns per thread; the two warps of a lane quarter share row maxima
+        const int q = warp & 3;                 // TMEM lane quarter this warp may access
+        const int half = (warp - 2) >> 2;       // columns [64 half, 64 half + 64) of S, P and O
         const int row = q * 32 + lane;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int pos = r.kl - r.ql + t * kTile + row;
         const bool row_valid = t * kTile + row < r.ql;
+        const uint32_t col0 = (uint32_t)(half * 64);
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int i = 0; i < r.nt; ++i) {
             const int sb = i & 1;
-            if (!dg::mbar_wait_warp(&sh.sfull[sb], ((uint32_t)i >> 1) & 1u)) {
+            if (!attn_wait_warp(&sh.sfull[sb], ((uint32_t)i >> 1) & 1u)) {
                 ok = false;
                 break;
             }
             dg::tc_fence_after();
-            float x[4][32];
+            float x[2][32];
+            {
+                uint32_t raw[2][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) dg::tmem_ld32(tmem + lane_base + (uint32_t)(sb * kTile + c * 32), x[c]);
+                for (int c = 0; c < 2; ++c)
+                    dg::tmem_ld32_nowait(tmem + lane_base + (uint32_t)(sb * kTile) + col0 + (uint32_t)(c * 32), raw[c]);
+                dg::tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[c][e] = __uint_as_float(raw[c][e]);
+            }
             dg::tc_fence_before();
             __syncwarp();
             if (lane == 0) dg::mbar_arrive(&sh.sempty[sb]);  // S buffer free for S_{i+2}
             const int jt = r.jt_lo + i;
             const bool full = tile_full(r, a.window, jt);
+            const int j0 = jt * kTile + (int)col0;
             float tmax = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     float v = x[c][e] * a.scale_log2;
-                    if (!full && !allowed(r.causal, a.window, pos, jt * kTile + c * 32 + e, r.kl)) v = -INFINITY;
+                    if (!full && !allowed(r.causal, a.window, pos, j0 + c * 32 + e, r.kl)) v = -INFINITY;
                     x[c][e] = v;
                     tmax = fmaxf(tmax, v);
                 }
             }
+            // the row's maximum over both halves (entries alternate by tile: a half writes tile
+            // i + 2's entry only after both have arrived for tile i + 1, i.e. after the read)
+            sh.xmax[i & 1][half][row] = tmax;
+            __syncwarp();
+            if (lane == 0) dg::mbar_arrive(&sh.xbar[q]);
+            if (!attn_wait_warp(&sh.xbar[q], (uint32_t)i & 1u)) {  // one phase per tile
+                ok = false;
+                break;
+            }
+            tmax = fmaxf(tmax, sh.xmax[i & 1][half ^ 1][row]);
             // P V of the previous tile must be done before P or O is touched
             if (i > 0) {
-                if (!dg::mbar_wait_warp(&sh.pvdone, (uint32_t)(i - 1) & 1u)) {
+                if (!attn_wait_warp(&sh.pvdone, (uint32_t)(i - 1) & 1u)) {
                     ok = false;
                     break;
                 }
                 dg::tc_fence_after();
             }
+            // both halves see the same maxima, so they decide alike (warp-uniform per quarter)
             if (__any_sync(0xffffffffu, tmax > m_ref + kRescaleAbove)) {  // m_ref = -inf: any finite max
                 const float m_new = fmaxf(m_ref, tmax);
                 const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_ref - m_new);
                 l *= alpha;
                 if (i > 0) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 2; ++c) {
                         float o[32];
-                        const uint32_t ta = tmem + lane_base + 256u + (uint32_t)(c * 32);
+                        const uint32_t ta = tmem + lane_base + 256u + col0 + (uint32_t)(c * 32);
                         dg::tmem_ld32(ta, o);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] *= alpha;
@@ -334,11 +406,11 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 m_ref = m_new;
             }
-            // P = 2^(x - m_ref) in bf16, 8 keys per 16-byte chunk, swizzled like a TMA tile
-            unsigned char* prow = smem + kOffP + (uint32_t)row * 128u;
+            // P = 2^(x - m_ref) in bf16: this half's 64 keys are one swizzled 64-wide sub-tile
+            unsigned char* prow = smem + kOffP + (uint32_t)half * kSubBytes + (uint32_t)row * 128u;
             float sum = 0.f;
 #pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
+            for (int ch = 0; ch < 8; ++ch) {
                 const int c = ch >> 2, e0 = (ch & 3) * 8;
                 float p[8];
 #pragma unroll
@@ -347,9 +419,9 @@ __global__ void __launch_bounds__(192, 1)
                     p[e] = (v == -INFINITY) ? 0.f : ex2(v - m_ref);
                     sum += p[e];
                 }
-                const uint32_t off = (uint32_t)(ch >> 3) * kSubBytes + (uint32_t)(((ch & 7) ^ (row & 7)) << 4);
-                *reinterpret_cast<uint4*>(prow + off) = make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
-                                                                   pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
+                *reinterpret_cast<uint4*>(prow + (uint32_t)((ch ^ (row & 7)) << 4)) =
+                    make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
+                               pack_bf16x2(p[6], p[7]));
             }
             l += sum;
             dg::fence_proxy_async_smem();  // the generic-proxy stores, visible to the MMA
@@ -357,16 +429,23 @@ __global__ void __launch_bounds__(192, 1)
             __syncwarp();
             if (lane == 0) dg::mbar_arrive(&sh.pfull);
         }
-        if (ok && !dg::mbar_wait_warp(&sh.pvdone, (uint32_t)(r.nt - 1) & 1u)) ok = false;
+        if (ok && !attn_wait_warp(&sh.pvdone, (uint32_t)(r.nt - 1) & 1u)) ok = false;
+        if (ok) {  // the row sum over both halves: the exchange's phase nt
+            sh.xsum[half][row] = l;
+            __syncwarp();
+            if (lane == 0) dg::mbar_arrive(&sh.xbar[q]);
+            ok = attn_wait_warp(&sh.xbar[q], (uint32_t)r.nt & 1u);
+        }
         if (ok) {
             dg::tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float lt = l + sh.xsum[half ^ 1][row];
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
             const int64_t qi = (int64_t)r.q0 + t * kTile + row;
-            uint16_t* orow = a.o + (qi * a.Hq + h) * kHead;
+            uint16_t* orow = a.o + (qi * a.Hq + h) * kHead + col0;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 float o[32];
-                dg::tmem_ld32(tmem + lane_base + 256u + (uint32_t)(c * 32), o);
+                dg::tmem_ld32(tmem + lane_base + 256u + col0 + (uint32_t)(c * 32), o);
                 if (row_valid) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8)
@@ -375,7 +454,7 @@ __global__ void __launch_bounds__(192, 1)
                                        pack_bf16x2(o[e + 4] * inv, o[e + 5] * inv), pack_bf16x2(o[e + 6] * inv, o[e + 7] * inv));
                 }
             }
-            if (row_valid && a.lse) a.lse[qi * a.Hq + h] = (m_ref + log2f(l)) * kLn2;
+            if (row_valid && half == 0 && a.lse) a.lse[qi * a.Hq + h] = (m_ref + log2f(lt)) * kLn2;
         } else {
             do_abort(sh, a.status);
         }
@@ -439,7 +518,7 @@ extern "C" dg_status dg_attention(const uint16_t* q, const uint16_t* k, const ui
     a.scale_log2 = scale * kLog2e;
     a.status = dghost::status_word();
     const dim3 grid((unsigned)((max_q_len + kTile - 1) / kTile), (unsigned)Hq, (unsigned)n_seq);
-    k_attention<<<grid, 192, kAttnSmem, (cudaStream_t)stream>>>(tq, tk, tv, a);
+    k_attention<<<grid, kThreads, kAttnSmem, (cudaStream_t)stream>>>(tq, tk, tv, a);
     dghost::count_launch();
     return dghost::cuda_status(cudaGetLastError());
 }

@@ -14,11 +14,12 @@
 // One CTA per (128-query tile, query head, sequence); one pass with an online softmax:
 //   warp 0      TMA producer: the Q tile once, then K and V tiles (128 keys) in a 2-stage ring;
 //   warp 1      MMA issuer (one elected thread): S = Q K^T into one of two TMEM buffers while the
-//               softmax works on the other, O += P V into a third;
+//               softmax works on the other, O += P V into a third with P read from tensor memory;
 //   warps 2..9  softmax, two warps per TMEM lane quarter, each thread one query row (its TMEM
 //               lane) and 64 of its 128 columns: the row of S, the mask on tiles that are not
 //               wholly allowed, the row maximum shared with the other half through shared
-//               memory, P = 2^(x - m) in bf16 into shared memory for the P V MMA, the row sum.  The reference m only moves when a row's maximum grows
+//               memory, P = 2^(x - m) as bf16 pairs into one of two TMEM buffers (tcgen05.st)
+//               for the P V MMA, the row sum; only a rescale of O waits for the last P V.  The reference m only moves when a row's maximum grows
 //               by more than 8 (in log2 units), so P < 2^8 and most tiles leave O alone; when it
 //               moves, the row of O is rescaled in TMEM (tcgen05.ld, multiply, tcgen05.st)
 //               between two P V MMAs.  At the end O / l goes out in bf16 with the row's lse.
@@ -62,7 +63,7 @@ struct __align__(8) AttnShared {
     uint64_t sfull[2];
     uint64_t sempty[2];
     uint64_t pfull;
-    uint64_t pvdone;
+    uint64_t pvdone[2];       // P V of the tiles using P buffer 0 / 1 done
     uint64_t mmadone;
     uint64_t xbar[4];         // per lane quarter: both halves have posted their row values
     uint32_t tmem_base;
@@ -71,12 +72,13 @@ struct __align__(8) AttnShared {
     float xsum[2][kTile];     // [column half][row]: the halves' row sums, at the end
 };
 
-// shared memory: Q | K[2] | V[2] | P, each 32 KB and 1024-aligned, then the barriers
+// shared memory: Q | K[2] | V[2], each 32 KB and 1024-aligned, then the barriers
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTileBytes;
 constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;
-constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;
-constexpr uint32_t kOffBar = kOffP + kTileBytes;
+constexpr uint32_t kOffBar = kOffV + 2 * kTileBytes;
+// tensor memory columns: S buffers, O, P buffers (bf16 pairs: 64 columns for 128 keys)
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 constexpr size_t kAttnSmem = 1024 + kOffBar + sizeof(AttnShared) + 64;
 static_assert(kAttnSmem <= 232448, "fits the opt-in shared memory of an SM");
 
@@ -221,14 +223,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             dg::mbar_init(&sh.sempty[i], kSoftmaxWarps);  // one arrival per softmax warp
         }
         dg::mbar_init(&sh.pfull, kSoftmaxWarps);
-        dg::mbar_init(&sh.pvdone, 1);
+        dg::mbar_init(&sh.pvdone[0], 1);
+        dg::mbar_init(&sh.pvdone[1], 1);
         dg::mbar_init(&sh.mmadone, 1);
         for (int i = 0; i < 4; ++i) dg::mbar_init(&sh.xbar[i], 2);  // one arrival per half's warp
         sh.abort_flag = 0;
         dg::fence_mbar_init();
     }
     if (warp == 1) {
-        dg::tmem_alloc(&sh.tmem_base, 512);  // S buffers at columns 0 and 128, O at 256
+        dg::tmem_alloc(&sh.tmem_base, 512);  // S at 0 and 128, O at 256, P at 384 and 448
         dg::tmem_relinquish();
     }
     dg::tc_fence_before();
@@ -236,7 +239,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     dg::tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
     const uint32_t sQ = dg::smem_u32(smem + kOffQ);
-    const uint32_t sP = dg::smem_u32(smem + kOffP);
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kHead / 16; ++kk) {
                         const uint32_t off = (uint32_t)(kk >> 2) * kSubBytes + (uint32_t)(kk & 3) * 32u;
-                        dg::tc_mma_f16(tmem + (uint32_t)(st * kTile), dg::smem_desc(sQ + off, 16, 1024, 128),
+                        dg::tc_mma_f16(tmem + kColS + (uint32_t)(st * kTile), dg::smem_desc(sQ + off, 16, 1024, 128),
                                        dg::smem_desc(sK + off, 16, 1024, 128), idS, kk > 0 ? 1u : 0u);
                     }
                     dg::tc_commit(&sh.sfull[st]);
@@ -305,14 +307,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sV = dg::smem_u32(smem + kOffV + st * kTileBytes);
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk) {
-                        // A: P rows, keys in two 64-wide atoms; B: 16 V rows (keys) x 128 columns
-                        // (two 64-column atoms, kSubBytes apart)
-                        const uint32_t offp = (uint32_t)(kk >> 2) * kSubBytes + (uint32_t)(kk & 3) * 32u;
-                        dg::tc_mma_f16(tmem + 256u, dg::smem_desc(sP + offp, 16, 1024, 128),
-                                       dg::smem_desc(sV + (uint32_t)kk * 16u * 128u, kSubBytes, 1024, 128), idO,
-                                       (j > 0 || kk > 0) ? 1u : 0u);
+                        // A: P in tensor memory, 16 keys = 8 columns per step; B: 16 V rows (keys)
+                        // x 128 columns (two 64-column atoms, kSubBytes apart)
+                        dg::tc_mma_f16_ts(tmem + kColO, tmem + kColP + (uint32_t)(st * 64 + kk * 8),
+                                          dg::smem_desc(sV + (uint32_t)kk * 16u * 128u, kSubBytes, 1024, 128), idO,
+                                          (j > 0 || kk > 0) ? 1u : 0u);
                     }
-                    dg::tc_commit(&sh.pvdone);
+                    dg::tc_commit(&sh.pvdone[st]);
                     dg::tc_commit(&sh.kvempty[st]);
                 }
             }
@@ -345,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t raw[2][32];
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
-                    dg::tmem_ld32_nowait(tmem + lane_base + (uint32_t)(sb * kTile) + col0 + (uint32_t)(c * 32), raw[c]);
+                    dg::tmem_ld32_nowait(tmem + lane_base + kColS + (uint32_t)(sb * kTile) + col0 + (uint32_t)(c * 32),
+                                         raw[c]);
                 dg::tmem_ld_wait();
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
@@ -379,16 +381,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tmax = fmaxf(tmax, sh.xmax[i & 1][half ^ 1][row]);
-            // P V of the previous tile must be done before P or O is touched
-            if (i > 0) {
-                if (!attn_wait_warp(&sh.pvdone, (uint32_t)(i - 1) & 1u)) {
+            // both halves see the same maxima, so they decide alike (warp-uniform per quarter)
+            const bool rescale = __any_sync(0xffffffffu, tmax > m_ref + kRescaleAbove);  // m_ref = -inf: any finite max
+            // before P buffer i % 2 is rewritten, the P V that read it (tile i - 2) must be done;
+            // before O is rescaled, the last P V (tile i - 1), which implies the one before
+            if (i > 0 && (rescale || i > 1)) {
+                const int j = rescale ? i - 1 : i - 2;
+                if (!attn_wait_warp(&sh.pvdone[j & 1], ((uint32_t)j >> 1) & 1u)) {
                     ok = false;
                     break;
                 }
                 dg::tc_fence_after();
             }
-            // both halves see the same maxima, so they decide alike (warp-uniform per quarter)
-            if (__any_sync(0xffffffffu, tmax > m_ref + kRescaleAbove)) {  // m_ref = -inf: any finite max
+            if (rescale) {
                 const float m_new = fmaxf(m_ref, tmax);
                 const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_ref - m_new);
                 l *= alpha;
@@ -396,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         float o[32];
-                        const uint32_t ta = tmem + lane_base + 256u + col0 + (uint32_t)(c * 32);
+                        const uint32_t ta = tmem + lane_base + kColO + col0 + (uint32_t)(c * 32);
                         dg::tmem_ld32(ta, o);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] *= alpha;
@@ -406,30 +411,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 m_ref = m_new;
             }
-            // P = 2^(x - m_ref) in bf16: this half's 64 keys are one swizzled 64-wide sub-tile
-            unsigned char* prow = smem + kOffP + (uint32_t)half * kSubBytes + (uint32_t)row * 128u;
+            // P = 2^(x - m_ref) in bf16 pairs into P buffer i % 2 (this half's 64 keys are its
+            // 32 columns) for the P V MMA, which reads A from tensor memory
             float sum = 0.f;
+            uint32_t pk[32];
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const int c = ch >> 2, e0 = (ch & 3) * 8;
-                float p[8];
+            for (int c = 0; c < 2; ++c) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float v = x[c][e0 + e];
-                    p[e] = (v == -INFINITY) ? 0.f : ex2(v - m_ref);
-                    sum += p[e];
+                for (int e = 0; e < 32; e += 2) {
+                    const float v0 = x[c][e], v1 = x[c][e + 1];
+                    const float p0 = (v0 == -INFINITY) ? 0.f : ex2(v0 - m_ref);
+                    const float p1 = (v1 == -INFINITY) ? 0.f : ex2(v1 - m_ref);
+                    sum += p0 + p1;
+                    pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
                 }
-                *reinterpret_cast<uint4*>(prow + (uint32_t)((ch ^ (row & 7)) << 4)) =
-                    make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
-                               pack_bf16x2(p[6], p[7]));
             }
+            dg::tmem_st32u(tmem + lane_base + kColP + (uint32_t)(sb * 64) + (uint32_t)(half * 32), pk);
+            dg::tmem_st_wait();
             l += sum;
-            dg::fence_proxy_async_smem();  // the generic-proxy stores, visible to the MMA
             dg::tc_fence_before();
             __syncwarp();
             if (lane == 0) dg::mbar_arrive(&sh.pfull);
         }
-        if (ok && !attn_wait_warp(&sh.pvdone, (uint32_t)(r.nt - 1) & 1u)) ok = false;
+        if (ok && !attn_wait_warp(&sh.pvdone[(r.nt - 1) & 1], ((uint32_t)(r.nt - 1) >> 1) & 1u)) ok = false;
         if (ok) {  // the row sum over both halves: the exchange's phase nt
             sh.xsum[half][row] = l;
             __syncwarp();
@@ -445,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 float o[32];
-                dg::tmem_ld32(tmem + lane_base + 256u + col0 + (uint32_t)(c * 32), o);
+                dg::tmem_ld32(tmem + lane_base + kColO + col0 + (uint32_t)(c * 32), o);
                 if (row_valid) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8)

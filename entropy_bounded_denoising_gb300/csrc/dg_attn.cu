@@ -15,9 +15,9 @@
 //   warp 0      TMA producer: the Q tile once, then K and V tiles (128 keys) in a 2-stage ring;
 //   warp 1      MMA issuer (one elected thread): S = Q K^T into one of two TMEM buffers while the
 //               softmax works on the other, O += P V into a third with P read from tensor memory;
-//   warps 2..9  softmax, two warps per TMEM lane quarter, each thread one query row (its TMEM
-//               lane) and 64 of its 128 columns: the row of S, the mask on tiles that are not
-//               wholly allowed, the row maximum shared with the other half through shared
+//   warps 2..    softmax, kParts warps per TMEM lane quarter, each thread one query row (its
+//               TMEM lane) and 128 / kParts of its columns: the row of S, the mask on tiles that
+//               are not wholly allowed, the row maximum shared among the parts through shared
 //               memory, P = 2^(x - m) as bf16 pairs into one of two TMEM buffers (tcgen05.st)
 //               for the P V MMA, the row sum; only a rescale of O waits for the last P V.  The reference m only moves when a row's maximum grows
 //               by more than 8 (in log2 units), so P < 2^8 and most tiles leave O alone; when it
@@ -65,11 +65,11 @@ struct __align__(8) AttnShared {
     uint64_t pfull;
     uint64_t pvdone[2];       // P V of the tiles using P buffer 0 / 1 done
     uint64_t mmadone;
-    uint64_t xbar[4];         // per lane quarter: both halves have posted their row values
+    uint64_t xbar[4];         // per lane quarter: every column part has posted its row values
     uint32_t tmem_base;
     int abort_flag;
-    float xmax[2][2][kTile];  // [tile parity][column half][row]: the halves' row maxima
-    float xsum[2][kTile];     // [column half][row]: the halves' row sums, at the end
+    float xmax[2][4][kTile];  // [tile parity][column part][row]: the parts' row maxima
+    float xsum[4][kTile];     // [column part][row]: the parts' row sums, at the end
 };
 
 // shared memory: Q | K[2] | V[2], each 32 KB and 1024-aligned, then the barriers
@@ -142,10 +142,11 @@ DG_DEVINL float ex2(float x) {
     return y;
 }
 
-// Barrier waits on the per-tile critical path: polled without a suspend-time hint (a
-// suspended thread wakes late next to this loop's ~1 us per tile), still bounded.
+// Barrier waits on the per-tile critical path: a 200 ns suspend-time hint (measured against
+// none, which lets a polling lane take issue slots from the other softmax warp, and 1000 ns,
+// which wakes late next to this loop's ~2 us per tile); bounded.
 #ifndef DG_ATTN_HINT_NS
-#define DG_ATTN_HINT_NS 0
+#define DG_ATTN_HINT_NS 200
 #endif
 DG_DEVINL bool attn_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
@@ -190,8 +191,15 @@ DG_DEVINL void do_abort(AttnShared& sh, unsigned* status) {
 }
 
 // ------------------------------------------------------------------ the kernel
-constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quarter, 64 columns each
+#ifndef DG_ATTN_PARTS
+#define DG_ATTN_PARTS 2
+#endif
+constexpr int kParts = DG_ATTN_PARTS;           // softmax warps per TMEM lane quarter
+constexpr int kCols = kTile / kParts;           // columns of S (and of O) per softmax thread
+constexpr int kChunks = kCols / 32;
+constexpr int kSoftmaxWarps = 4 * kParts;
 constexpr int kThreads = 64 + 32 * kSoftmaxWarps;
+static_assert(kParts == 2 || kParts == 4, "64 or 32 columns per softmax thread");
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_attention(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -226,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         dg::mbar_init(&sh.pvdone[0], 1);
         dg::mbar_init(&sh.pvdone[1], 1);
         dg::mbar_init(&sh.mmadone, 1);
-        for (int i = 0; i < 4; ++i) dg::mbar_init(&sh.xbar[i], 2);  // one arrival per half's warp
+        for (int i = 0; i < 4; ++i) dg::mbar_init(&sh.xbar[i], kParts);  // one arrival per part's warp
         sh.abort_flag = 0;
         dg::fence_mbar_init();
     }
@@ -323,15 +331,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             (void)attn_wait(&sh.mmadone, 0);
         }
     } else {
-        // ------------------------------------------------ softmax (warps 2..9): one query row and
-        // 64 of the 128 columns per thread; the two warps of a lane quarter share row maxima
+        // ------------------------------------------------ softmax: one query row and kCols of the
+        // 128 columns per thread; the kParts warps of a lane quarter share row maxima
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
-        const int half = (warp - 2) >> 2;       // columns [64 half, 64 half + 64) of S, P and O
+        const int part = (warp - 2) >> 2;       // columns [kCols part, kCols (part + 1)) of S and O
         const int row = q * 32 + lane;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int pos = r.kl - r.ql + t * kTile + row;
         const bool row_valid = t * kTile + row < r.ql;
-        const uint32_t col0 = (uint32_t)(half * 64);
+        const uint32_t col0 = (uint32_t)(part * kCols);
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int i = 0; i < r.nt; ++i) {
@@ -341,16 +349,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             dg::tc_fence_after();
-            float x[2][32];
+            float x[kChunks][32];
             {
-                uint32_t raw[2][32];
+                uint32_t raw[kChunks][32];
 #pragma unroll
-                for (int c = 0; c < 2; ++c)
+                for (int c = 0; c < kChunks; ++c)
                     dg::tmem_ld32_nowait(tmem + lane_base + kColS + (uint32_t)(sb * kTile) + col0 + (uint32_t)(c * 32),
                                          raw[c]);
                 dg::tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 2; ++c)
+                for (int c = 0; c < kChunks; ++c)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) x[c][e] = __uint_as_float(raw[c][e]);
             }
@@ -362,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j0 = jt * kTile + (int)col0;
             float tmax = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     float v = x[c][e] * a.scale_log2;
@@ -371,17 +379,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmax = fmaxf(tmax, v);
                 }
             }
-            // the row's maximum over both halves (entries alternate by tile: a half writes tile
-            // i + 2's entry only after both have arrived for tile i + 1, i.e. after the read)
-            sh.xmax[i & 1][half][row] = tmax;
+            // the row's maximum over all parts (entries alternate by tile: a part writes tile
+            // i + 2's entry only after all have arrived for tile i + 1, i.e. after the reads)
+            sh.xmax[i & 1][part][row] = tmax;
             __syncwarp();
             if (lane == 0) dg::mbar_arrive(&sh.xbar[q]);
             if (!attn_wait_warp(&sh.xbar[q], (uint32_t)i & 1u)) {  // one phase per tile
                 ok = false;
                 break;
             }
-            tmax = fmaxf(tmax, sh.xmax[i & 1][half ^ 1][row]);
-            // both halves see the same maxima, so they decide alike (warp-uniform per quarter)
+#pragma unroll
+            for (int o = 1; o < kParts; ++o) tmax = fmaxf(tmax, sh.xmax[i & 1][(part + o) % kParts][row]);
+            // every part sees the same maxima, so they decide alike (warp-uniform per quarter)
             const bool rescale = __any_sync(0xffffffffu, tmax > m_ref + kRescaleAbove);  // m_ref = -inf: any finite max
             // before P buffer i % 2 is rewritten, the P V that read it (tile i - 2) must be done;
             // before O is rescaled, the last P V (tile i - 1), which implies the one before
@@ -399,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l *= alpha;
                 if (i > 0) {
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
+                    for (int c = 0; c < kChunks; ++c) {
                         float o[32];
                         const uint32_t ta = tmem + lane_base + kColO + col0 + (uint32_t)(c * 32);
                         dg::tmem_ld32(ta, o);
@@ -411,12 +420,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 m_ref = m_new;
             }
-            // P = 2^(x - m_ref) in bf16 pairs into P buffer i % 2 (this half's 64 keys are its
-            // 32 columns) for the P V MMA, which reads A from tensor memory
+            // P = 2^(x - m_ref) in bf16 pairs into P buffer i % 2 (this part's kCols keys are
+            // its kCols / 2 columns) for the P V MMA, which reads A from tensor memory
             float sum = 0.f;
-            uint32_t pk[32];
+            uint32_t pk[kCols / 2];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     const float v0 = x[c][e], v1 = x[c][e + 1];
@@ -426,7 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
                 }
             }
-            dg::tmem_st32u(tmem + lane_base + kColP + (uint32_t)(sb * 64) + (uint32_t)(half * 32), pk);
+            const uint32_t pa = tmem + lane_base + kColP + (uint32_t)(sb * 64) + (uint32_t)(part * (kCols / 2));
+            if constexpr (kCols == 64) dg::tmem_st32u(pa, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+            else dg::tmem_st16u(pa, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
             dg::tmem_st_wait();
             l += sum;
             dg::tc_fence_before();
@@ -434,20 +445,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) dg::mbar_arrive(&sh.pfull);
         }
         if (ok && !attn_wait_warp(&sh.pvdone[(r.nt - 1) & 1], ((uint32_t)(r.nt - 1) >> 1) & 1u)) ok = false;
-        if (ok) {  // the row sum over both halves: the exchange's phase nt
-            sh.xsum[half][row] = l;
+        if (ok) {  // the row sum over all parts: the exchange's phase nt
+            sh.xsum[part][row] = l;
             __syncwarp();
             if (lane == 0) dg::mbar_arrive(&sh.xbar[q]);
             ok = attn_wait_warp(&sh.xbar[q], (uint32_t)r.nt & 1u);
         }
         if (ok) {
             dg::tc_fence_after();
-            const float lt = l + sh.xsum[half ^ 1][row];
+            float lt = l;
+#pragma unroll
+            for (int o = 1; o < kParts; ++o) lt += sh.xsum[(part + o) % kParts][row];
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
             const int64_t qi = (int64_t)r.q0 + t * kTile + row;
             uint16_t* orow = a.o + (qi * a.Hq + h) * kHead + col0;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kChunks; ++c) {
                 float o[32];
                 dg::tmem_ld32(tmem + lane_base + kColO + col0 + (uint32_t)(c * 32), o);
                 if (row_valid) {
@@ -458,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        pack_bf16x2(o[e + 4] * inv, o[e + 5] * inv), pack_bf16x2(o[e + 6] * inv, o[e + 7] * inv));
                 }
             }
-            if (row_valid && half == 0 && a.lse) a.lse[qi * a.Hq + h] = (m_ref + log2f(lt)) * kLn2;
+            if (row_valid && part == 0 && a.lse) a.lse[qi * a.Hq + h] = (m_ref + log2f(lt)) * kLn2;
         } else {
             do_abort(sh, a.status);
         }

@@ -11,18 +11,20 @@
 // queries are its last q_len tokens (query i sits at kv_len - q_len + i); that and the score
 // scale * q.k without soft-capping are readings, the pages give only the figures.
 //
-// One CTA per (128-query tile, query head, sequence); one pass with an online softmax:
-//   warp 0      TMA producer: the Q tile once, then K and V tiles (128 keys) in a 2-stage ring;
-//   warp 1      MMA issuer (one elected thread): S = Q K^T into one of two TMEM buffers while the
-//               softmax works on the other, O += P V into a third with P read from tensor memory;
-//   warps 2..    softmax, kParts warps per TMEM lane quarter, each thread one query row (its
-//               TMEM lane) and 128 / kParts of its columns: the row of S, the mask on tiles that
-//               are not wholly allowed, the row maximum shared among the parts through shared
-//               memory, P = 2^(x - m) as bf16 pairs into one of two TMEM buffers (tcgen05.st)
-//               for the P V MMA, the row sum; only a rescale of O waits for the last P V.  The reference m only moves when a row's maximum grows
-//               by more than 8 (in log2 units), so P < 2^8 and most tiles leave O alone; when it
-//               moves, the row of O is rescaled in TMEM (tcgen05.ld, multiply, tcgen05.st)
-//               between two P V MMAs.  At the end O / l goes out in bf16 with the row's lse.
+// One CTA per (128-query tile, query head, sequence), two CTAs per SM (each 256 TMEM columns
+// and under half the shared memory, so one CTA's barrier waits are the other's issue slots);
+// one pass with an online softmax:
+//   warp 0      TMA producers: the Q tile once, then K and V tiles (64 keys) in two 2-stage
+//               rings (a K buffer frees when its S MMA is done, a V buffer after its P V);
+//   warp 1      MMA issuer (one elected thread): S = Q K^T (128 x 64) into TMEM, issued as soon
+//               as the softmax has read the previous S, and O += P V with P read from TMEM;
+//   warps 2..5  softmax, one query row per thread (its TMEM lane), all 64 columns of a tile:
+//               the row of S, the mask on tiles that are not wholly allowed, P = 2^(x - m) as
+//               bf16 pairs into one of two TMEM buffers (tcgen05.st) for the P V MMA, the row
+//               sum.  The reference m only moves when a row's maximum grows by more than 8 (in
+//               log2 units), so P < 2^8 and most tiles leave O alone; when it moves, the row of
+//               O is rescaled in TMEM (tcgen05.ld, multiply, tcgen05.st) after the last P V.
+//               At the end O / l goes out in bf16 with the row's lse.
 // Only key tiles holding an allowed key for some query of the tile are visited.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -35,11 +37,14 @@
 
 namespace {
 
-constexpr int kTile = 128;      // queries per CTA and keys per tile
+constexpr int kTile = 128;      // queries per CTA
+constexpr int kKeys = 64;       // keys per tile
 constexpr int kHead = 128;      // head dimension D
 constexpr int kSub = 64;        // columns per 128-byte swizzle atom
-constexpr uint32_t kSubBytes = kTile * kSub * 2;   // 16 KB: one 128 x 64 bf16 atom block
-constexpr uint32_t kTileBytes = 2 * kSubBytes;     // 32 KB: 128 x 128 bf16
+constexpr uint32_t kQSub = kTile * kSub * 2;       // 16 KB: 128 rows x 64 columns of Q
+constexpr uint32_t kQBytes = 2 * kQSub;            // the Q tile, D = 128
+constexpr uint32_t kKSub = kKeys * kSub * 2;       // 8 KB: 64 rows x 64 columns of K or V
+constexpr uint32_t kKVBytes = 2 * kKSub;           // one K (or V) tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleAbove = 8.f;  // log2 units: P stays below 2^8 between rescales
@@ -58,29 +63,30 @@ struct AttnArgs {
 
 struct __align__(8) AttnShared {
     uint64_t qfull;
-    uint64_t kvfull[2];
-    uint64_t kvempty[2];
-    uint64_t sfull[2];
-    uint64_t sempty[2];
+    uint64_t kfull[2];        // K and V tiles in separate rings: a K buffer is free as soon as
+    uint64_t kempty[2];       // its S MMA is done, long before the V buffer of the same tile
+    uint64_t vfull[2];
+    uint64_t vempty[2];
+    uint64_t sfull;
+    uint64_t sempty;
     uint64_t pfull;
     uint64_t pvdone[2];       // P V of the tiles using P buffer 0 / 1 done
     uint64_t mmadone;
-    uint64_t xbar[4];         // per lane quarter: every column part has posted its row values
     uint32_t tmem_base;
     int abort_flag;
-    float xmax[2][4][kTile];  // [tile parity][column part][row]: the parts' row maxima
-    float xsum[4][kTile];     // [column part][row]: the parts' row sums, at the end
 };
 
-// shared memory: Q | K[2] | V[2], each 32 KB and 1024-aligned, then the barriers
+// shared memory: Q | K[2] | V[2] (1024-aligned blocks), then the barriers
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTileBytes;
-constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;
-constexpr uint32_t kOffBar = kOffV + 2 * kTileBytes;
-// tensor memory columns: S buffers, O, P buffers (bf16 pairs: 64 columns for 128 keys)
-constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+constexpr uint32_t kOffK = kOffQ + kQBytes;
+constexpr uint32_t kOffV = kOffK + 2 * kKVBytes;
+constexpr uint32_t kOffBar = kOffV + 2 * kKVBytes;
 constexpr size_t kAttnSmem = 1024 + kOffBar + sizeof(AttnShared) + 64;
-static_assert(kAttnSmem <= 232448, "fits the opt-in shared memory of an SM");
+static_assert(2 * (kAttnSmem + 1024) <= 232448, "two CTAs fit the shared memory of an SM");
+// tensor memory columns (256 per CTA): S, O, P buffers (bf16 pairs: 32 columns for 64 keys)
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0, kColO = 64, kColP = 192;
+constexpr int kThreads = 192;
 
 // Whether the query at position pos may see key j of a sequence of kv_len keys.
 DG_DEVINL bool allowed(bool causal, int window, int pos, int j, int kv_len) {
@@ -114,13 +120,13 @@ DG_DEVINL TileRange tile_range(const AttnArgs& a, int s, int t) {
     const int W = a.window;
     const int jlo = W >= 0 ? max(0, r.pmin - W) : 0;
     const int jhi = r.causal ? r.pmax : (W >= 0 ? min(r.kl - 1, r.pmax + W) : r.kl - 1);
-    r.jt_lo = jlo / kTile;
-    r.nt = jhi >= jlo ? jhi / kTile - r.jt_lo + 1 : 0;
+    r.jt_lo = jlo / kKeys;
+    r.nt = jhi >= jlo ? jhi / kKeys - r.jt_lo + 1 : 0;
     return r;
 }
 
 DG_DEVINL bool tile_full(const TileRange& r, int window, int jt) {
-    const int j0 = jt * kTile, j1 = j0 + kTile - 1;
+    const int j0 = jt * kKeys, j1 = j0 + kKeys - 1;
     if (j1 >= r.kl) return false;
     if (r.causal && j1 > r.pmin) return false;
     if (window >= 0) {
@@ -191,17 +197,7 @@ DG_DEVINL void do_abort(AttnShared& sh, unsigned* status) {
 }
 
 // ------------------------------------------------------------------ the kernel
-#ifndef DG_ATTN_PARTS
-#define DG_ATTN_PARTS 2
-#endif
-constexpr int kParts = DG_ATTN_PARTS;           // softmax warps per TMEM lane quarter
-constexpr int kCols = kTile / kParts;           // columns of S (and of O) per softmax thread
-constexpr int kChunks = kCols / 32;
-constexpr int kSoftmaxWarps = 4 * kParts;
-constexpr int kThreads = 64 + 32 * kSoftmaxWarps;
-static_assert(kParts == 2 || kParts == 4, "64 or 32 columns per softmax thread");
-
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     k_attention(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
     extern __shared__ __align__(1024) unsigned char attn_smem_raw[];
@@ -225,21 +221,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         dg::mbar_init(&sh.qfull, 1);
         for (int i = 0; i < 2; ++i) {
-            dg::mbar_init(&sh.kvfull[i], 1);
-            dg::mbar_init(&sh.kvempty[i], 1);
-            dg::mbar_init(&sh.sfull[i], 1);
-            dg::mbar_init(&sh.sempty[i], kSoftmaxWarps);  // one arrival per softmax warp
+            dg::mbar_init(&sh.kfull[i], 1);
+            dg::mbar_init(&sh.kempty[i], 1);
+            dg::mbar_init(&sh.vfull[i], 1);
+            dg::mbar_init(&sh.vempty[i], 1);
+            dg::mbar_init(&sh.pvdone[i], 1);
         }
-        dg::mbar_init(&sh.pfull, kSoftmaxWarps);
-        dg::mbar_init(&sh.pvdone[0], 1);
-        dg::mbar_init(&sh.pvdone[1], 1);
+        dg::mbar_init(&sh.sfull, 1);
+        dg::mbar_init(&sh.sempty, 4);  // one arrival per softmax warp
+        dg::mbar_init(&sh.pfull, 4);
         dg::mbar_init(&sh.mmadone, 1);
-        for (int i = 0; i < 4; ++i) dg::mbar_init(&sh.xbar[i], kParts);  // one arrival per part's warp
         sh.abort_flag = 0;
         dg::fence_mbar_init();
     }
     if (warp == 1) {
-        dg::tmem_alloc(&sh.tmem_base, 512);  // S at 0 and 128, O at 256, P at 384 and 448
+        dg::tmem_alloc(&sh.tmem_base, kTmemCols);
         dg::tmem_relinquish();
     }
     dg::tc_fence_before();
@@ -249,80 +245,88 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = dg::smem_u32(smem + kOffQ);
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            dg::prefetch_tmap(&tmQ);
-            dg::prefetch_tmap(&tmK);
-            dg::prefetch_tmap(&tmV);
-            const int qrow = r.q0 + t * kTile;
-            dg::mbar_arrive_expect_tx(&sh.qfull, kTileBytes);
-            dg::tma_load_2d(smem + kOffQ, &tmQ, h * kHead, qrow, &sh.qfull);
-            dg::tma_load_2d(smem + kOffQ + kSubBytes, &tmQ, h * kHead + kSub, qrow, &sh.qfull);
+        // ------------------------------------------------ TMA producers: lane 0 Q and the K ring,
+        // lane 1 the V ring
+        if (lane < 2) {
+            const bool is_k = lane == 0;
+            const CUtensorMap* tm = is_k ? &tmK : &tmV;
+            uint64_t* full = is_k ? sh.kfull : sh.vfull;
+            uint64_t* empty = is_k ? sh.kempty : sh.vempty;
+            unsigned char* ring = smem + (is_k ? kOffK : kOffV);
+            if (is_k) {
+                dg::prefetch_tmap(&tmQ);
+                dg::prefetch_tmap(&tmK);
+                const int qrow = r.q0 + t * kTile;
+                dg::mbar_arrive_expect_tx(&sh.qfull, kQBytes);
+                dg::tma_load_2d(smem + kOffQ, &tmQ, h * kHead, qrow, &sh.qfull);
+                dg::tma_load_2d(smem + kOffQ + kQSub, &tmQ, h * kHead + kSub, qrow, &sh.qfull);
+            } else {
+                dg::prefetch_tmap(&tmV);
+            }
             int issued[2] = {0, 0};
             for (int i = 0; i < r.nt && !aborted(sh); ++i) {
                 const int st = i & 1;
-                if (!attn_wait(&sh.kvempty[st], (((uint32_t)i >> 1) & 1u) ^ 1u)) {
+                if (!attn_wait(&empty[st], (((uint32_t)i >> 1) & 1u) ^ 1u)) {
                     do_abort(sh, a.status);
                     break;
                 }
-                dg::mbar_arrive_expect_tx(&sh.kvfull[st], 2 * kTileBytes);
-                const int krow = r.k0 + (r.jt_lo + i) * kTile;
-                unsigned char* sk = smem + kOffK + st * kTileBytes;
-                unsigned char* sv = smem + kOffV + st * kTileBytes;
-                dg::tma_load_2d(sk, &tmK, hk * kHead, krow, &sh.kvfull[st]);
-                dg::tma_load_2d(sk + kSubBytes, &tmK, hk * kHead + kSub, krow, &sh.kvfull[st]);
-                dg::tma_load_2d(sv, &tmV, hk * kHead, krow, &sh.kvfull[st]);
-                dg::tma_load_2d(sv + kSubBytes, &tmV, hk * kHead + kSub, krow, &sh.kvfull[st]);
+                dg::mbar_arrive_expect_tx(&full[st], kKVBytes);
+                const int krow = r.k0 + (r.jt_lo + i) * kKeys;
+                unsigned char* dst = ring + st * kKVBytes;
+                dg::tma_load_2d(dst, tm, hk * kHead, krow, &full[st]);
+                dg::tma_load_2d(dst + kKSub, tm, hk * kHead + kSub, krow, &full[st]);
                 ++issued[st];
             }
             if (aborted(sh)) {  // never leave with a copy still landing in shared memory
-                (void)attn_wait(&sh.qfull, 0);
+                if (is_k) (void)attn_wait(&sh.qfull, 0);
                 for (int st = 0; st < 2; ++st)
-                    if (issued[st] > 0) (void)attn_wait(&sh.kvfull[st], (uint32_t)(issued[st] - 1) & 1u);
+                    if (issued[st] > 0) (void)attn_wait(&full[st], (uint32_t)(issued[st] - 1) & 1u);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idS = dg::instr_desc(kTile, kTile, false);  // S = Q K^T: K tile K-major
+            constexpr uint32_t idS = dg::instr_desc(kTile, kKeys, false);  // S = Q K^T: K tile K-major
             constexpr uint32_t idO = dg::instr_desc(kTile, kHead, true);   // O += P V: V rows are N-major
             bool ok = attn_wait(&sh.qfull, 0);
             for (int i = 0; ok && i <= r.nt && !aborted(sh); ++i) {
-                if (i < r.nt) {  // S_i into buffer i % 2
+                if (i < r.nt) {  // S_i, once the softmax has read S_{i-1}
                     const int st = i & 1;
-                    const uint32_t ph = ((uint32_t)i >> 1) & 1u;
-                    if (!attn_wait(&sh.kvfull[st], ph) || !attn_wait(&sh.sempty[st], ph ^ 1u)) {
+                    if (!attn_wait(&sh.kfull[st], ((uint32_t)i >> 1) & 1u) ||
+                        !attn_wait(&sh.sempty, ((uint32_t)i & 1u) ^ 1u)) {
                         ok = false;
                         break;
                     }
                     dg::tc_fence_after();
-                    const uint32_t sK = dg::smem_u32(smem + kOffK + st * kTileBytes);
+                    const uint32_t sK = dg::smem_u32(smem + kOffK + st * kKVBytes);
 #pragma unroll
                     for (int kk = 0; kk < kHead / 16; ++kk) {
-                        const uint32_t off = (uint32_t)(kk >> 2) * kSubBytes + (uint32_t)(kk & 3) * 32u;
-                        dg::tc_mma_f16(tmem + kColS + (uint32_t)(st * kTile), dg::smem_desc(sQ + off, 16, 1024, 128),
-                                       dg::smem_desc(sK + off, 16, 1024, 128), idS, kk > 0 ? 1u : 0u);
+                        const uint32_t offq = (uint32_t)(kk >> 2) * kQSub + (uint32_t)(kk & 3) * 32u;
+                        const uint32_t offk = (uint32_t)(kk >> 2) * kKSub + (uint32_t)(kk & 3) * 32u;
+                        dg::tc_mma_f16(tmem + kColS, dg::smem_desc(sQ + offq, 16, 1024, 128),
+                                       dg::smem_desc(sK + offk, 16, 1024, 128), idS, kk > 0 ? 1u : 0u);
                     }
-                    dg::tc_commit(&sh.sfull[st]);
+                    dg::tc_commit(&sh.sfull);
+                    dg::tc_commit(&sh.kempty[st]);  // the K buffer, once S_i has read it
                 }
                 if (i >= 1) {  // O += P_{i-1} V_{i-1} once the softmax has written P
                     const int j = i - 1, st = j & 1;
-                    if (!attn_wait(&sh.pfull, (uint32_t)j & 1u)) {
+                    if (!attn_wait(&sh.pfull, (uint32_t)j & 1u) || !attn_wait(&sh.vfull[st], ((uint32_t)j >> 1) & 1u)) {
                         ok = false;
                         break;
                     }
                     dg::tc_fence_after();
-                    const uint32_t sV = dg::smem_u32(smem + kOffV + st * kTileBytes);
+                    const uint32_t sV = dg::smem_u32(smem + kOffV + st * kKVBytes);
 #pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                    for (int kk = 0; kk < kKeys / 16; ++kk) {
                         // A: P in tensor memory, 16 keys = 8 columns per step; B: 16 V rows (keys)
-                        // x 128 columns (two 64-column atoms, kSubBytes apart)
-                        dg::tc_mma_f16_ts(tmem + kColO, tmem + kColP + (uint32_t)(st * 64 + kk * 8),
-                                          dg::smem_desc(sV + (uint32_t)kk * 16u * 128u, kSubBytes, 1024, 128), idO,
+                        // x 128 columns (two 64-column atoms, kKSub apart)
+                        dg::tc_mma_f16_ts(tmem + kColO, tmem + kColP + (uint32_t)(st * 32 + kk * 8),
+                                          dg::smem_desc(sV + (uint32_t)kk * 16u * 128u, kKSub, 1024, 128), idO,
                                           (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     dg::tc_commit(&sh.pvdone[st]);
-                    dg::tc_commit(&sh.kvempty[st]);
+                    dg::tc_commit(&sh.vempty[st]);
                 }
             }
             if (!ok) do_abort(sh, a.status);
@@ -331,46 +335,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             (void)attn_wait(&sh.mmadone, 0);
         }
     } else {
-        // ------------------------------------------------ softmax: one query row and kCols of the
-        // 128 columns per thread; the kParts warps of a lane quarter share row maxima
-        const int q = warp & 3;                 // TMEM lane quarter this warp may access
-        const int part = (warp - 2) >> 2;       // columns [kCols part, kCols (part + 1)) of S and O
+        // ------------------------------------------------ softmax (warps 2..5), one row per thread
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int pos = r.kl - r.ql + t * kTile + row;
         const bool row_valid = t * kTile + row < r.ql;
-        const uint32_t col0 = (uint32_t)(part * kCols);
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int i = 0; i < r.nt; ++i) {
-            const int sb = i & 1;
-            if (!attn_wait_warp(&sh.sfull[sb], ((uint32_t)i >> 1) & 1u)) {
+            if (!attn_wait_warp(&sh.sfull, (uint32_t)i & 1u)) {
                 ok = false;
                 break;
             }
             dg::tc_fence_after();
-            float x[kChunks][32];
+            float x[2][32];
             {
-                uint32_t raw[kChunks][32];
+                uint32_t raw[2][32];
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c)
-                    dg::tmem_ld32_nowait(tmem + lane_base + kColS + (uint32_t)(sb * kTile) + col0 + (uint32_t)(c * 32),
-                                         raw[c]);
+                for (int c = 0; c < 2; ++c) dg::tmem_ld32_nowait(tmem + lane_base + kColS + (uint32_t)(c * 32), raw[c]);
                 dg::tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c)
+                for (int c = 0; c < 2; ++c)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) x[c][e] = __uint_as_float(raw[c][e]);
             }
             dg::tc_fence_before();
             __syncwarp();
-            if (lane == 0) dg::mbar_arrive(&sh.sempty[sb]);  // S buffer free for S_{i+2}
+            if (lane == 0) dg::mbar_arrive(&sh.sempty);  // S free for S_{i+1}
             const int jt = r.jt_lo + i;
             const bool full = tile_full(r, a.window, jt);
-            const int j0 = jt * kTile + (int)col0;
+            const int j0 = jt * kKeys;
             float tmax = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
+            for (int c = 0; c < 2; ++c) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     float v = x[c][e] * a.scale_log2;
@@ -379,18 +377,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmax = fmaxf(tmax, v);
                 }
             }
-            // the row's maximum over all parts (entries alternate by tile: a part writes tile
-            // i + 2's entry only after all have arrived for tile i + 1, i.e. after the reads)
-            sh.xmax[i & 1][part][row] = tmax;
-            __syncwarp();
-            if (lane == 0) dg::mbar_arrive(&sh.xbar[q]);
-            if (!attn_wait_warp(&sh.xbar[q], (uint32_t)i & 1u)) {  // one phase per tile
-                ok = false;
-                break;
-            }
-#pragma unroll
-            for (int o = 1; o < kParts; ++o) tmax = fmaxf(tmax, sh.xmax[i & 1][(part + o) % kParts][row]);
-            // every part sees the same maxima, so they decide alike (warp-uniform per quarter)
             const bool rescale = __any_sync(0xffffffffu, tmax > m_ref + kRescaleAbove);  // m_ref = -inf: any finite max
             // before P buffer i % 2 is rewritten, the P V that read it (tile i - 2) must be done;
             // before O is rescaled, the last P V (tile i - 1), which implies the one before
@@ -408,9 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l *= alpha;
                 if (i > 0) {
 #pragma unroll
-                    for (int c = 0; c < kChunks; ++c) {
+                    for (int c = 0; c < kHead / 32; ++c) {
                         float o[32];
-                        const uint32_t ta = tmem + lane_base + kColO + col0 + (uint32_t)(c * 32);
+                        const uint32_t ta = tmem + lane_base + kColO + (uint32_t)(c * 32);
                         dg::tmem_ld32(ta, o);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] *= alpha;
@@ -420,12 +406,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 m_ref = m_new;
             }
-            // P = 2^(x - m_ref) in bf16 pairs into P buffer i % 2 (this part's kCols keys are
-            // its kCols / 2 columns) for the P V MMA, which reads A from tensor memory
+            // P = 2^(x - m_ref) in bf16 pairs into P buffer i % 2 for the P V MMA
             float sum = 0.f;
-            uint32_t pk[kCols / 2];
+            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
+            for (int c = 0; c < 2; ++c) {
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     const float v0 = x[c][e], v1 = x[c][e + 1];
@@ -435,9 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
                 }
             }
-            const uint32_t pa = tmem + lane_base + kColP + (uint32_t)(sb * 64) + (uint32_t)(part * (kCols / 2));
-            if constexpr (kCols == 64) dg::tmem_st32u(pa, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-            else dg::tmem_st16u(pa, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+            dg::tmem_st32u(tmem + lane_base + kColP + (uint32_t)((i & 1) * 32), pk);
             dg::tmem_st_wait();
             l += sum;
             dg::tc_fence_before();
@@ -445,24 +428,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) dg::mbar_arrive(&sh.pfull);
         }
         if (ok && !attn_wait_warp(&sh.pvdone[(r.nt - 1) & 1], ((uint32_t)(r.nt - 1) >> 1) & 1u)) ok = false;
-        if (ok) {  // the row sum over all parts: the exchange's phase nt
-            sh.xsum[part][row] = l;
-            __syncwarp();
-            if (lane == 0) dg::mbar_arrive(&sh.xbar[q]);
-            ok = attn_wait_warp(&sh.xbar[q], (uint32_t)r.nt & 1u);
-        }
         if (ok) {
             dg::tc_fence_after();
-            float lt = l;
-#pragma unroll
-            for (int o = 1; o < kParts; ++o) lt += sh.xsum[(part + o) % kParts][row];
-            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
             const int64_t qi = (int64_t)r.q0 + t * kTile + row;
-            uint16_t* orow = a.o + (qi * a.Hq + h) * kHead + col0;
+            uint16_t* orow = a.o + (qi * a.Hq + h) * kHead;
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
+            for (int c = 0; c < kHead / 32; ++c) {
                 float o[32];
-                dg::tmem_ld32(tmem + lane_base + kColO + col0 + (uint32_t)(c * 32), o);
+                dg::tmem_ld32(tmem + lane_base + kColO + (uint32_t)(c * 32), o);
                 if (row_valid) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8)
@@ -471,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        pack_bf16x2(o[e + 4] * inv, o[e + 5] * inv), pack_bf16x2(o[e + 6] * inv, o[e + 7] * inv));
                 }
             }
-            if (row_valid && part == 0 && a.lse) a.lse[qi * a.Hq + h] = (m_ref + log2f(lt)) * kLn2;
+            if (row_valid && a.lse) a.lse[qi * a.Hq + h] = (m_ref + log2f(l)) * kLn2;
         } else {
             do_abort(sh, a.status);
         }
@@ -481,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         dg::tc_fence_after();
-        dg::tmem_dealloc(tmem, 512);
+        dg::tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -492,11 +466,11 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// [rows][heads * D] bf16 with 128 x 64 boxes (one 128-byte swizzle atom of 128 rows).
-bool tmap_heads(CUtensorMap* tm, const void* base, int64_t rows, int32_t heads) {
+// [rows][heads * D] bf16 with boxes of 64 columns (one 128-byte swizzle atom) x box_rows.
+bool tmap_heads(CUtensorMap* tm, const void* base, int64_t rows, int32_t heads, uint32_t box_rows) {
     uint64_t dims[2] = {(uint64_t)heads * kHead, (uint64_t)rows};
     uint64_t strides[1] = {(uint64_t)heads * kHead * 2};
-    uint32_t box[2] = {(uint32_t)kSub, (uint32_t)kTile};
+    uint32_t box[2] = {(uint32_t)kSub, box_rows};
     return dghost::encode_tmap(tm, 0, 2, const_cast<void*>(base), dims, strides, box, 128);
 }
 
@@ -517,7 +491,8 @@ extern "C" dg_status dg_attention(const uint16_t* q, const uint16_t* k, const ui
     if (!q || !k || !v || !o || !cu_q || !cu_kv || !causal) return DG_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return DG_ERR_ALIGNMENT;
     CUtensorMap tq, tk, tv;
-    if (!tmap_heads(&tq, q, total_q, Hq) || !tmap_heads(&tk, k, total_kv, Hkv) || !tmap_heads(&tv, v, total_kv, Hkv))
+    if (!tmap_heads(&tq, q, total_q, Hq, kTile) || !tmap_heads(&tk, k, total_kv, Hkv, kKeys) ||
+        !tmap_heads(&tv, v, total_kv, Hkv, kKeys))
         return DG_ERR_CUDA;
     if (cudaFuncSetAttribute(k_attention, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttnSmem) != cudaSuccess)
         return DG_ERR_CUDA;

@@ -47,7 +47,10 @@ constexpr uint32_t kKSub = kKeys * kSub * 2;       // 8 KB: 64 rows x 64 columns
 constexpr uint32_t kKVBytes = 2 * kKSub;           // one K (or V) tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleAbove = 8.f;  // log2 units: P stays below 2^8 between rescales
+#ifndef DG_ATTN_RESCALE_LOG2
+#define DG_ATTN_RESCALE_LOG2 8
+#endif
+constexpr float kRescaleAbove = DG_ATTN_RESCALE_LOG2;  // log2 units: P < 2^this between rescales
 
 struct AttnArgs {
     const int32_t* cu_q;    // [n + 1] query offsets
@@ -146,6 +149,24 @@ DG_DEVINL float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Packed fp32 pairs (one rounding per element, as the scalar forms).
+DG_DEVINL uint64_t f2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+DG_DEVINL void f2_split(uint64_t v, float& a, float& b) { asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v)); }
+DG_DEVINL uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+DG_DEVINL uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
 }
 
 // Barrier waits on the per-tile critical path: a 200 ns suspend-time hint (measured against
@@ -364,19 +385,23 @@ __global__ void __launch_bounds__(kThreads, 2)
             __syncwarp();
             if (lane == 0) dg::mbar_arrive(&sh.sempty);  // S free for S_{i+1}
             const int jt = r.jt_lo + i;
-            const bool full = tile_full(r, a.window, jt);
             const int j0 = jt * kKeys;
-            float tmax = -INFINITY;
+            if (!tile_full(r, a.window, jt)) {  // masked entries: -inf, which 2^x maps to 0
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < 2; ++c)
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float v = x[c][e] * a.scale_log2;
-                    if (!full && !allowed(r.causal, a.window, pos, j0 + c * 32 + e, r.kl)) v = -INFINITY;
-                    x[c][e] = v;
-                    tmax = fmaxf(tmax, v);
-                }
+                    for (int e = 0; e < 32; ++e)
+                        if (!allowed(r.causal, a.window, pos, j0 + c * 32 + e, r.kl)) x[c][e] = -INFINITY;
             }
+            // the tile's row maximum of the raw scores (a tree: independent steps), in log2 units
+            float mx[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) mx[e] = fmaxf(fmaxf(x[0][2 * e], x[0][2 * e + 1]), fmaxf(x[1][2 * e], x[1][2 * e + 1]));
+#pragma unroll
+            for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
+            const float tmax = mx[0] * a.scale_log2;  // -inf stays -inf (scale > 0)
             const bool rescale = __any_sync(0xffffffffu, tmax > m_ref + kRescaleAbove);  // m_ref = -inf: any finite max
             // before P buffer i % 2 is rewritten, the P V that read it (tile i - 2) must be done;
             // before O is rescaled, the last P V (tile i - 1), which implies the one before
@@ -406,20 +431,27 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 m_ref = m_new;
             }
-            // P = 2^(x - m_ref) in bf16 pairs into P buffer i % 2 for the P V MMA
-            float sum = 0.f;
+            // P = 2^(s c - m_ref) in bf16 pairs into P buffer i % 2 for the P V MMA; the exponent
+            // in one packed fma per pair (a row with no allowed key yet keeps m_ref = -inf: its
+            // entries are all -inf and the offset 0 keeps them so)
+            const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            const uint64_t cc = f2(a.scale_log2, a.scale_log2), mm = f2(neg_m, neg_m);
+            uint64_t acc = f2(0.f, 0.f);
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const float v0 = x[c][e], v1 = x[c][e + 1];
-                    const float p0 = (v0 == -INFINITY) ? 0.f : ex2(v0 - m_ref);
-                    const float p1 = (v1 == -INFINITY) ? 0.f : ex2(v1 - m_ref);
-                    sum += p0 + p1;
+                    float z0, z1;
+                    f2_split(f2_fma(f2(x[c][e], x[c][e + 1]), cc, mm), z0, z1);
+                    const float p0 = ex2(z0), p1 = ex2(z1);
+                    acc = f2_add(acc, f2(p0, p1));
                     pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
                 }
             }
+            float sa, sb;
+            f2_split(acc, sa, sb);
+            const float sum = sa + sb;
             dg::tmem_st32u(tmem + lane_base + kColP + (uint32_t)((i & 1) * 32), pk);
             dg::tmem_st_wait();
             l += sum;

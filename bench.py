@@ -567,43 +567,7 @@ def run_ours(args):
                     "then dg_denoise_step"}
         del xl, lws, hid
 
-        # Attention with per-sequence causality (timed alone): 8 denoising canvases of 256
-        # after 2048 context tokens (bidirectional) and 4 causal prefills of 1024, 16 query
-        # heads over 8 key/value heads, D = 128, without a window and with W = 512.
-        seqs = [(256, 2304, 0)] * 8 + [(1024, 1024, 1)] * 4
-        cu_q = np.cumsum([0] + [a[0] for a in seqs]).astype(np.int32)
-        cu_kv = np.cumsum([0] + [a[1] for a in seqs]).astype(np.int32)
-        cz = np.array([a[2] for a in seqs], np.uint8)
-        Hq, Hkv, Dh = 16, 8, 128
-        aq, ak, av = synth.attention_inputs(int(cu_q[-1]), int(cu_kv[-1]), Hq, Hkv, Dh, seed=9, device=dev)
-        ao = torch.empty_like(aq)
-        dq, dkv, dcz = (torch.from_numpy(t).to(dev) for t in (cu_q, cu_kv, cz))
-        attn = {}
-        for W in (-1, 512):
-            pairs = 0
-            tiles = tiles_all = 0
-            for ql, kl, c in seqs:
-                pos = np.arange(kl - ql, kl)
-                lo = np.maximum(0, pos - W) if W >= 0 else np.zeros_like(pos)
-                hi = pos if c else (np.minimum(kl - 1, pos + W) if W >= 0 else np.full_like(pos, kl - 1))
-                pairs += int((hi - lo + 1).sum())
-                for t0 in range(0, ql, 128):
-                    p0, p1 = int(pos[t0]), int(pos[min(ql, t0 + 128) - 1])
-                    jl = max(0, p0 - W) if W >= 0 else 0
-                    jh = p1 if c else (min(kl - 1, p1 + W) if W >= 0 else kl - 1)
-                    tiles += jh // 128 - jl // 128 + 1
-                    tiles_all += (kl + 127) // 128
-            ms = _time(lambda: dg.dg_attention(aq, ak, av, ao, dq, dkv, dcz, 1024, window=W, stream=stream), reps=20)
-            alg = 4.0 * pairs * Dh * Hq
-            exe = 4.0 * tiles * 128 * 128 * Dh * Hq
-            attn["window_%d" % W if W >= 0 else "no_window"] = {
-                "ms": ms, "tflops_allowed": alg / (ms * 1e-3) / 1e12, "tflops_executed": exe / (ms * 1e-3) / 1e12,
-                "frac_tc_executed": exe / (ms * 1e-3) / 1e12 / peak_tc, "tiles_visited": int(tiles),
-                "tiles_skipped_frac": 1.0 - tiles / tiles_all}
-        attn["note"] = ("dg_attention timed alone; allowed = 4 D flops per allowed (query, key) pair per head, "
-                        "executed = the visited 128 x 128 tiles; frac against the sustained bf16 peak")
-        around["attention"] = attn
-        del aq, ak, av, ao
+        around["attention"] = _attention_rows(dg, synth, dev, stream, _time, peak_tc)
         torch.cuda.synchronize()
         if dg.dg_get_device_status():
             raise RuntimeError("device status set by the rows around the step")
@@ -649,6 +613,78 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if ws > 1:
         tdist.destroy_process_group()
+    return 0
+
+
+def _attention_rows(dg, synth, dev, stream, time_fn, peak_tc):
+    """dg_attention timed alone on a denoising batch: 8 canvases of 256 after 2048 context
+    tokens (bidirectional) and 4 causal prefills of 1024, 16 query heads over 8 key/value
+    heads, D = 128, without a window and with W = 512."""
+    import torch
+    seqs = [(256, 2304, 0)] * 8 + [(1024, 1024, 1)] * 4
+    cu_q = np.cumsum([0] + [a[0] for a in seqs]).astype(np.int32)
+    cu_kv = np.cumsum([0] + [a[1] for a in seqs]).astype(np.int32)
+    cz = np.array([a[2] for a in seqs], np.uint8)
+    Hq, Hkv, Dh, TQ, TK = 16, 8, 128, 128, 64   # 128-query tiles over 64-key tiles
+    aq, ak, av = synth.attention_inputs(int(cu_q[-1]), int(cu_kv[-1]), Hq, Hkv, Dh, seed=9, device=dev)
+    ao = torch.empty_like(aq)
+    dq, dkv, dcz = (torch.from_numpy(t).to(dev) for t in (cu_q, cu_kv, cz))
+    attn = {}
+    for W in (-1, 512):
+        pairs = 0
+        tiles = tiles_all = 0
+        for ql, kl, c in seqs:
+            pos = np.arange(kl - ql, kl)
+            lo = np.maximum(0, pos - W) if W >= 0 else np.zeros_like(pos)
+            hi = pos if c else (np.minimum(kl - 1, pos + W) if W >= 0 else np.full_like(pos, kl - 1))
+            pairs += int((hi - lo + 1).sum())
+            for t0 in range(0, ql, TQ):
+                p0, p1 = int(pos[t0]), int(pos[min(ql, t0 + TQ) - 1])
+                jl = max(0, p0 - W) if W >= 0 else 0
+                jh = p1 if c else (min(kl - 1, p1 + W) if W >= 0 else kl - 1)
+                tiles += jh // TK - jl // TK + 1
+                tiles_all += (kl + TK - 1) // TK
+        ms = time_fn(lambda: dg.dg_attention(aq, ak, av, ao, dq, dkv, dcz, 1024, window=W, stream=stream), reps=20)
+        alg = 4.0 * pairs * Dh * Hq
+        exe = 4.0 * tiles * TQ * TK * Dh * Hq
+        attn["window_%d" % W if W >= 0 else "no_window"] = {
+            "ms": ms, "tflops_allowed": alg / (ms * 1e-3) / 1e12, "tflops_executed": exe / (ms * 1e-3) / 1e12,
+            "frac_tc_executed": exe / (ms * 1e-3) / 1e12 / peak_tc, "tiles_visited": int(tiles),
+            "tiles_skipped_frac": 1.0 - tiles / tiles_all}
+    attn["note"] = ("dg_attention timed alone; allowed = 4 D flops per allowed (query, key) pair per head, "
+                    "executed = the visited 128 x 64 tiles; frac against the sustained bf16 peak")
+    del aq, ak, av, ao
+    return attn
+
+
+def run_attention(args):
+    """--attention: dg_attention alone (the rows above), one JSON line; a small command to
+    profile the attention kernel on."""
+    import torch
+    import entropy_bounded_denoising_gb300 as dg
+    from entropy_bounded_denoising_gb300 import synth, build
+    build.build()
+    dg.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+
+    def _time(fn, reps=20):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    pk = _peaks()
+    rows = _attention_rows(dg, synth, dev, stream, _time, pk["bf16_tflops_sustained"])
+    if dg.dg_get_device_status():
+        raise RuntimeError("device status set by dg_attention")
+    print(json.dumps({"metric": "attention TFLOP/s (executed tiles) on a denoising batch", "rows": rows,
+                      "gpu_launches_per_call": 1}), flush=True)
     return 0
 
 
@@ -774,6 +810,8 @@ def main():
     ap.add_argument("--from-hidden", action="store_true",
                     help="start each step from hidden states: the LM head fused with the step's statistics")
     ap.add_argument("--graph", action="store_true", help="time replays of the step captured as a CUDA graph")
+    ap.add_argument("--attention", action="store_true",
+                    help="time only the attention kernel on a denoising batch (one JSON line)")
     ap.add_argument("--loop", action="store_true",
                     help="time the workload's whole denoising loop (e.g. --workload sweep) instead of repeated steps")
     args = ap.parse_args()
@@ -781,6 +819,8 @@ def main():
         return run_reference(args)
     if args.loop:
         return run_loop(args)
+    if args.attention:
+        return run_attention(args)
     return run_ours(args)
 
 

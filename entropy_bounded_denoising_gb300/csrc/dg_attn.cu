@@ -91,17 +91,6 @@ constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0, kColO = 64, kColP = 192;
 constexpr int kThreads = 192;
 
-// Whether the query at position pos may see key j of a sequence of kv_len keys.
-DG_DEVINL bool allowed(bool causal, int window, int pos, int j, int kv_len) {
-    if (j >= kv_len) return false;
-    if (causal && j > pos) return false;
-    if (window >= 0) {
-        if (j < pos - window) return false;
-        if (!causal && j > pos + window) return false;
-    }
-    return true;
-}
-
 // The key tiles a query tile visits, and whether a key tile is allowed for all its queries.
 struct TileRange {
     int q0, ql, k0, kl;   // sequence offsets and lengths
@@ -120,21 +109,21 @@ DG_DEVINL TileRange tile_range(const AttnArgs& a, int s, int t) {
     const int off = r.kl - r.ql;
     r.pmin = off + t * kTile;
     r.pmax = off + min(r.ql, t * kTile + kTile) - 1;
-    const int W = a.window;
-    const int jlo = W >= 0 ? max(0, r.pmin - W) : 0;
-    const int jhi = r.causal ? r.pmax : (W >= 0 ? min(r.kl - 1, r.pmax + W) : r.kl - 1);
+    const int64_t W = a.window;
+    const int jlo = W >= 0 ? (int)max((int64_t)0, (int64_t)r.pmin - W) : 0;
+    const int jhi = r.causal ? r.pmax : (W >= 0 ? (int)min((int64_t)r.kl - 1, (int64_t)r.pmax + W) : r.kl - 1);
     r.jt_lo = jlo / kKeys;
     r.nt = jhi >= jlo ? jhi / kKeys - r.jt_lo + 1 : 0;
     return r;
 }
 
 DG_DEVINL bool tile_full(const TileRange& r, int window, int jt) {
-    const int j0 = jt * kKeys, j1 = j0 + kKeys - 1;
+    const int64_t j0 = (int64_t)jt * kKeys, j1 = j0 + kKeys - 1;
     if (j1 >= r.kl) return false;
     if (r.causal && j1 > r.pmin) return false;
     if (window >= 0) {
-        if (j0 < r.pmax - window) return false;
-        if (!r.causal && j1 > r.pmin + window) return false;
+        if (j0 < (int64_t)r.pmax - window) return false;
+        if (!r.causal && j1 > (int64_t)r.pmin + window) return false;
     }
     return true;
 }
@@ -386,12 +375,21 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (lane == 0) dg::mbar_arrive(&sh.sempty);  // S free for S_{i+1}
             const int jt = r.jt_lo + i;
             const int j0 = jt * kKeys;
-            if (!tile_full(r, a.window, jt)) {  // masked entries: -inf, which 2^x maps to 0
+            if (!tile_full(r, a.window, jt)) {
+                // masked entries: -inf, which 2^x maps to 0.  The keys a query at position pos may
+                // see form one range: j < kv_len, j <= pos if causal, and with a window W also
+                // j >= pos - W and (bidirectional) j <= pos + W; the mask is two compares per entry
+                const int64_t W = a.window;
+                const int lo = (int)max((int64_t)-1, (W >= 0 ? (int64_t)pos - W : 0) - j0);
+                const int hi = (int)min((int64_t)kKeys,
+                                        min((int64_t)r.kl - 1, r.causal ? (int64_t)pos : (W >= 0 ? (int64_t)pos + W : (int64_t)r.kl - 1)) - j0);
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (!allowed(r.causal, a.window, pos, j0 + c * 32 + e, r.kl)) x[c][e] = -INFINITY;
+                    for (int e = 0; e < 32; ++e) {
+                        const int k = c * 32 + e;
+                        x[c][e] = (k >= lo && k <= hi) ? x[c][e] : -INFINITY;
+                    }
             }
             // the tile's row maximum of the raw scores (a tree: independent steps), in log2 units
             float mx[16];

@@ -138,3 +138,13 @@ def _one_query(qi, kk, vv, pos, causal, window):
     o, lse = oracle.attention(qi, kk[keys], vv[keys], np.array([0, 1], np.int32),
                               np.array([0, len(keys)], np.int32), np.array([0], np.uint8))
     return o[0], lse[0]
+
+
+def test_attention_window_wider_than_every_sequence_is_no_window():
+    """A window at least as long as every sequence allows what no window allows: the outputs
+    are bit-identical (the range arithmetic is 64-bit, so a window near 2^31 cannot wrap)."""
+    q, k, v, cu_q, cu_kv, causal = _batch(SEQS, 4, 2, seed=8)
+    o1, l1 = _run(q, k, v, cu_q, cu_kv, causal, -1)
+    o2, l2 = _run(q, k, v, cu_q, cu_kv, causal, 2 ** 31 - 1)
+    assert dg.dg_get_device_status() == 0
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)

@@ -76,7 +76,9 @@ def load(path: str | None = None):
         "dg_gemm_bf16": (st, [P, i64, P, i64, ctypes.c_int, P, i64, i64, i64, i64, P, sz, P]),
         "dg_gemm_bf16_noalloc": (st, [P, i64, P, i64, ctypes.c_int, P, i64, i64, i64, i64, P]),
         "dg_choice_probs": (st, [P, ctypes.c_int, i64, P, P, i64, i32, i64, P, i32, P, P]),
-        "dg_attention": (st, [P, P, P, P, P, P, P, P, i32, i32, i64, i64, i32, i32, i32, i32, ctypes.c_float, P]),
+        "dg_attention_workspace_bytes": (sz, [i32, i32]),
+        "dg_attention": (st, [P, P, P, P, P, P, P, P, i32, i32, i64, i64, i32, i32, i32, i32, ctypes.c_float,
+                              P, sz, P]),
         "dg_embed_canvas": (st, [P, i64, i64, P, i32, P, ctypes.c_float, P, P]),
         "dg_commit": (st, [P, P, P, i64, i32, P, P, P, P, P]),
         "dg_philox_words": (st, [u64, u32, u32, u32, u32, u32, i64, P, P]),
@@ -104,6 +106,7 @@ def exported_symbols() -> list[str]:
                         "dg_self_cond_mlp", "dg_self_cond_probs_workspace_bytes",
                         "dg_self_cond_probs", "dg_gemm_workspace_bytes", "dg_gemm_bf16",
                         "dg_gemm_bf16_noalloc", "dg_choice_probs", "dg_embed_canvas", "dg_commit", "dg_attention",
+                        "dg_attention_workspace_bytes",
                         "dg_philox_words", "dg_get_device_status", "dg_clear_device_status",
                         "dg_status_string", "dg_version", "dg_launch_count") if hasattr(lib, n)]
 
@@ -323,8 +326,12 @@ def dg_choice_probs(logits, lse, params, choices, probs, *, V=None, stream=None,
     return rc
 
 
+def dg_attention_workspace_bytes(n_seq: int, max_q_len: int) -> int:
+    return int(load().dg_attention_workspace_bytes(n_seq, max_q_len))
+
+
 def dg_attention(q, k, v, o, cu_q, cu_kv, causal, max_q_len: int, *, lse=None, window: int = -1,
-                 scale: float | None = None, stream=None, check=True) -> int:
+                 scale: float | None = None, workspace=None, stream=None, check=True) -> int:
     """o = attention over the allowed keys (per-sequence causality, optional symmetric window);
     q [total_q, Hq, D], k / v [total_kv, Hkv, D], o like q (bf16); cu_q / cu_kv [n + 1] int32 and
     causal [n] uint8 on the device."""
@@ -335,8 +342,12 @@ def dg_attention(q, k, v, o, cu_q, cu_kv, causal, max_q_len: int, *, lse=None, w
             raise ValueError("q, k, v and o must be contiguous")
     n = causal.numel()
     scale = 1.0 / float(D) ** 0.5 if scale is None else float(scale)
+    if workspace is None:
+        workspace = torch.empty(max(1, dg_attention_workspace_bytes(n, int(max_q_len))), dtype=torch.uint8,
+                                device=q.device)
     rc = load().dg_attention(_p(q), _p(k), _p(v), _p(o), _p(lse), _p(cu_q), _p(cu_kv), _p(causal), n,
-                             int(max_q_len), total_q, total_kv, Hq, Hkv, D, int(window), scale, _s(stream))
+                             int(max_q_len), total_q, total_kv, Hq, Hkv, D, int(window), scale, _p(workspace),
+                             workspace.numel(), _s(stream))
     if check:
         _check("dg_attention", rc)
     return rc

@@ -66,6 +66,8 @@ struct AttnArgs {
 
 struct __align__(8) AttnShared {
     uint64_t qfull;
+    uint64_t qempty;          // the Q tile has been read by the item's last S MMA
+    uint64_t oempty;          // the softmax has read O out for the item (the next may overwrite it)
     uint64_t kfull[2];        // K and V tiles in separate rings: a K buffer is free as soon as
     uint64_t kempty[2];       // its S MMA is done, long before the V buffer of the same tile
     uint64_t vfull[2];
@@ -206,30 +208,91 @@ DG_DEVINL void do_abort(AttnShared& sh, unsigned* status) {
     dg::raise_status(status, DG_DEV_TIMEOUT);
 }
 
+// ------------------------------------------------------------------ the plan
+// Work items are (sequence, 128-query tile) pairs with at least one query.  One CTA lists them
+// by decreasing cost (key tiles visited; a counting sort over kCostBuckets), so that the
+// persistent CTAs, which take items round robin, start with the longest.  A sequence whose
+// offsets or lengths are out of range, or that has more queries than max_q_tiles tiles hold,
+// raises DG_DEV_BAD_PARAM and is left out (wholly, or its tiles past max_q_tiles).
+constexpr int kCostBuckets = 1024;
+constexpr int kPlanHeader = 4;  // ints before the items: the item count, padding
+
+__global__ void __launch_bounds__(1024) k_attn_plan(const AttnArgs a, int32_t n_seq, int32_t max_q_tiles,
+                                                    int32_t* __restrict__ plan) {
+    __shared__ int count[kCostBuckets];
+    __shared__ int warp_sum[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int b = tid; b < kCostBuckets; b += blockDim.x) count[b] = 0;
+    __syncthreads();
+    const int64_t pairs = (int64_t)n_seq * max_q_tiles;
+    auto item_key = [&](int64_t f, int& key) -> bool {  // false: no item (past the queries or bad)
+        const int s = (int)(f / max_q_tiles), t = (int)(f % max_q_tiles);
+        const TileRange r = tile_range(a, s, t);
+        const bool bad = r.q0 < 0 || r.k0 < 0 || r.ql < 0 || (int64_t)r.q0 + r.ql > a.total_q ||
+                         (int64_t)r.k0 + r.kl > a.total_kv || r.ql > r.kl;
+        if (t == 0 && (bad || r.ql > max_q_tiles * kTile)) dg::raise_status(a.status, DG_DEV_BAD_PARAM);
+        if (bad || t * kTile >= r.ql || r.nt <= 0) return false;
+        key = kCostBuckets - 1 - min(r.nt, kCostBuckets - 1);  // longest first
+        return true;
+    };
+    for (int64_t f = tid; f < pairs; f += blockDim.x) {
+        int key;
+        if (item_key(f, key)) atomicAdd(&count[key], 1);
+    }
+    __syncthreads();
+    // exclusive prefix over the buckets (one per thread): warp scans, then the warp totals
+    const int c = tid < kCostBuckets ? count[tid] : 0;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int v = warp_sum[lane];
+        int wi = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        warp_sum[lane] = wi - v;
+        if (lane == 31) plan[0] = wi;
+    }
+    __syncthreads();
+    if (tid < kCostBuckets) count[tid] = warp_sum[warp] + incl - c;
+    __syncthreads();
+    int2* items = reinterpret_cast<int2*>(plan + kPlanHeader);
+    for (int64_t f = tid; f < pairs; f += blockDim.x) {
+        int key;
+        if (item_key(f, key)) items[atomicAdd(&count[key], 1)] = make_int2((int)(f / max_q_tiles), (int)(f % max_q_tiles));
+    }
+}
+
 // ------------------------------------------------------------------ the kernel
+// Persistent: CTA b takes work w = b, b + gridDim.x, ... of n_items * Hq (item w / Hq, head
+// w % Hq).  Every ring, buffer and barrier phase is counted over the CTA's whole run (g: its
+// key tiles so far, k: its items so far), so the next item's Q and K / V loads and its first
+// S MMA overlap the current item's last tiles and its epilogue.
 __global__ void __launch_bounds__(kThreads, 2)
     k_attention(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+                const __grid_constant__ CUtensorMap tmV, const AttnArgs a, const int32_t* __restrict__ plan) {
     extern __shared__ __align__(1024) unsigned char attn_smem_raw[];
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(attn_smem_raw) + 1023) & ~uintptr_t(1023));
     AttnShared& sh = *reinterpret_cast<AttnShared*>(smem + kOffBar);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
-    const TileRange r = tile_range(a, s, t);
-    if (threadIdx.x == 0 && t == (int)gridDim.x - 1 && r.ql > (int)gridDim.x * kTile)
-        dg::raise_status(a.status, DG_DEV_BAD_PARAM);  // max_q_len below this sequence's queries
-    if (t * kTile >= r.ql) return;  // the whole CTA: past the sequence's queries
-    // offsets inside the buffers, and the queries the sequence's last tokens
-    if (r.q0 < 0 || r.k0 < 0 || (int64_t)r.q0 + r.ql > a.total_q || (int64_t)r.k0 + r.kl > a.total_kv ||
-        r.ql > r.kl || r.nt <= 0) {
-        if (threadIdx.x == 0) dg::raise_status(a.status, DG_DEV_BAD_PARAM);
-        return;
-    }
-    const int hk = h / (a.Hq / a.Hkv);
+    const int64_t n_work = (int64_t)plan[0] * a.Hq;
+    if ((int64_t)blockIdx.x >= n_work) return;  // the whole CTA: no work
+    const int2* items = reinterpret_cast<const int2*>(plan + kPlanHeader);
+    const int group = a.Hq / a.Hkv;
 
     if (threadIdx.x == 0) {
         dg::mbar_init(&sh.qfull, 1);
+        dg::mbar_init(&sh.qempty, 1);
+        dg::mbar_init(&sh.oempty, 4);  // one arrival per softmax warp
         for (int i = 0; i < 2; ++i) {
             dg::mbar_init(&sh.kfull[i], 1);
             dg::mbar_init(&sh.kempty[i], 1);
@@ -238,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             dg::mbar_init(&sh.pvdone[i], 1);
         }
         dg::mbar_init(&sh.sfull, 1);
-        dg::mbar_init(&sh.sempty, 4);  // one arrival per softmax warp
+        dg::mbar_init(&sh.sempty, 4);
         dg::mbar_init(&sh.pfull, 4);
         dg::mbar_init(&sh.mmadone, 1);
         sh.abort_flag = 0;
@@ -255,40 +318,56 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t sQ = dg::smem_u32(smem + kOffQ);
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producers: lane 0 Q and the K ring,
-        // lane 1 the V ring
-        if (lane < 2) {
+        // ------------------------------------------------ TMA producers: lane 0 the K ring, lane 1
+        // the V ring, lane 2 the Q tile of each item (once the last item's last S has read it)
+        if (lane == 2) {
+            dg::prefetch_tmap(&tmQ);
+            uint32_t kq = 0;
+            bool ok = true;
+            for (int64_t w = blockIdx.x; w < n_work && !aborted(sh); w += gridDim.x, ++kq) {
+                const int2 it = items[w / a.Hq];
+                const int h = (int)(w % a.Hq);
+                if (!attn_wait(&sh.qempty, (kq & 1u) ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                const int qrow = a.cu_q[it.x] + it.y * kTile;
+                dg::mbar_arrive_expect_tx(&sh.qfull, kQBytes);
+                dg::tma_load_2d(smem + kOffQ, &tmQ, h * kHead, qrow, &sh.qfull);
+                dg::tma_load_2d(smem + kOffQ + kQSub, &tmQ, h * kHead + kSub, qrow, &sh.qfull);
+            }
+            if (!ok) do_abort(sh, a.status);
+            if (aborted(sh) && kq > 0) (void)attn_wait(&sh.qfull, (kq - 1u) & 1u);  // the last Q copy landed
+        } else if (lane < 2) {
             const bool is_k = lane == 0;
             const CUtensorMap* tm = is_k ? &tmK : &tmV;
             uint64_t* full = is_k ? sh.kfull : sh.vfull;
             uint64_t* empty = is_k ? sh.kempty : sh.vempty;
             unsigned char* ring = smem + (is_k ? kOffK : kOffV);
-            if (is_k) {
-                dg::prefetch_tmap(&tmQ);
-                dg::prefetch_tmap(&tmK);
-                const int qrow = r.q0 + t * kTile;
-                dg::mbar_arrive_expect_tx(&sh.qfull, kQBytes);
-                dg::tma_load_2d(smem + kOffQ, &tmQ, h * kHead, qrow, &sh.qfull);
-                dg::tma_load_2d(smem + kOffQ + kQSub, &tmQ, h * kHead + kSub, qrow, &sh.qfull);
-            } else {
-                dg::prefetch_tmap(&tmV);
-            }
+            dg::prefetch_tmap(tm);
+            uint32_t g = 0;
             int issued[2] = {0, 0};
-            for (int i = 0; i < r.nt && !aborted(sh); ++i) {
-                const int st = i & 1;
-                if (!attn_wait(&empty[st], (((uint32_t)i >> 1) & 1u) ^ 1u)) {
-                    do_abort(sh, a.status);
-                    break;
+            bool ok = true;
+            for (int64_t w = blockIdx.x; w < n_work && ok && !aborted(sh); w += gridDim.x) {
+                const int2 it = items[w / a.Hq];
+                const int hk = (int)(w % a.Hq) / group;
+                const TileRange r = tile_range(a, it.x, it.y);
+                for (int i = 0; i < r.nt; ++i, ++g) {
+                    const int st = (int)(g & 1u);
+                    if (!attn_wait(&empty[st], ((g >> 1) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    dg::mbar_arrive_expect_tx(&full[st], kKVBytes);
+                    const int krow = r.k0 + (r.jt_lo + i) * kKeys;
+                    unsigned char* dst = ring + st * kKVBytes;
+                    dg::tma_load_2d(dst, tm, hk * kHead, krow, &full[st]);
+                    dg::tma_load_2d(dst + kKSub, tm, hk * kHead + kSub, krow, &full[st]);
+                    ++issued[st];
                 }
-                dg::mbar_arrive_expect_tx(&full[st], kKVBytes);
-                const int krow = r.k0 + (r.jt_lo + i) * kKeys;
-                unsigned char* dst = ring + st * kKVBytes;
-                dg::tma_load_2d(dst, tm, hk * kHead, krow, &full[st]);
-                dg::tma_load_2d(dst + kKSub, tm, hk * kHead + kSub, krow, &full[st]);
-                ++issued[st];
             }
+            if (!ok) do_abort(sh, a.status);
             if (aborted(sh)) {  // never leave with a copy still landing in shared memory
-                if (is_k) (void)attn_wait(&sh.qfull, 0);
                 for (int st = 0; st < 2; ++st)
                     if (issued[st] > 0) (void)attn_wait(&full[st], (uint32_t)(issued[st] - 1) & 1u);
             }
@@ -298,46 +377,60 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) {
             constexpr uint32_t idS = dg::instr_desc(kTile, kKeys, false);  // S = Q K^T: K tile K-major
             constexpr uint32_t idO = dg::instr_desc(kTile, kHead, true);   // O += P V: V rows are N-major
-            bool ok = attn_wait(&sh.qfull, 0);
-            for (int i = 0; ok && i <= r.nt && !aborted(sh); ++i) {
-                if (i < r.nt) {  // S_i, once the softmax has read S_{i-1}
-                    const int st = i & 1;
-                    if (!attn_wait(&sh.kfull[st], ((uint32_t)i >> 1) & 1u) ||
-                        !attn_wait(&sh.sempty, ((uint32_t)i & 1u) ^ 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    dg::tc_fence_after();
-                    const uint32_t sK = dg::smem_u32(smem + kOffK + st * kKVBytes);
-#pragma unroll
-                    for (int kk = 0; kk < kHead / 16; ++kk) {
-                        const uint32_t offq = (uint32_t)(kk >> 2) * kQSub + (uint32_t)(kk & 3) * 32u;
-                        const uint32_t offk = (uint32_t)(kk >> 2) * kKSub + (uint32_t)(kk & 3) * 32u;
-                        dg::tc_mma_f16(tmem + kColS, dg::smem_desc(sQ + offq, 16, 1024, 128),
-                                       dg::smem_desc(sK + offk, 16, 1024, 128), idS, kk > 0 ? 1u : 0u);
-                    }
-                    dg::tc_commit(&sh.sfull);
-                    dg::tc_commit(&sh.kempty[st]);  // the K buffer, once S_i has read it
+            uint32_t g = 0, kq = 0;
+            bool ok = true;
+            for (int64_t w = blockIdx.x; w < n_work && ok && !aborted(sh); w += gridDim.x, ++kq) {
+                const int2 it = items[w / a.Hq];
+                const TileRange r = tile_range(a, it.x, it.y);
+                if (!attn_wait(&sh.qfull, kq & 1u)) {
+                    ok = false;
+                    break;
                 }
-                if (i >= 1) {  // O += P_{i-1} V_{i-1} once the softmax has written P
-                    const int j = i - 1, st = j & 1;
-                    if (!attn_wait(&sh.pfull, (uint32_t)j & 1u) || !attn_wait(&sh.vfull[st], ((uint32_t)j >> 1) & 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    dg::tc_fence_after();
-                    const uint32_t sV = dg::smem_u32(smem + kOffV + st * kKVBytes);
+                for (int i = 0; i <= r.nt; ++i) {
+                    if (i < r.nt) {  // S of tile g + i, once the softmax has read the previous S
+                        const uint32_t gs = g + (uint32_t)i;
+                        const int st = (int)(gs & 1u);
+                        if (!attn_wait(&sh.kfull[st], (gs >> 1) & 1u) || !attn_wait(&sh.sempty, (gs & 1u) ^ 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        dg::tc_fence_after();
+                        const uint32_t sK = dg::smem_u32(smem + kOffK + st * kKVBytes);
 #pragma unroll
-                    for (int kk = 0; kk < kKeys / 16; ++kk) {
-                        // A: P in tensor memory, 16 keys = 8 columns per step; B: 16 V rows (keys)
-                        // x 128 columns (two 64-column atoms, kKSub apart)
-                        dg::tc_mma_f16_ts(tmem + kColO, tmem + kColP + (uint32_t)(st * 32 + kk * 8),
-                                          dg::smem_desc(sV + (uint32_t)kk * 16u * 128u, kKSub, 1024, 128), idO,
-                                          (j > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kHead / 16; ++kk) {
+                            const uint32_t offq = (uint32_t)(kk >> 2) * kQSub + (uint32_t)(kk & 3) * 32u;
+                            const uint32_t offk = (uint32_t)(kk >> 2) * kKSub + (uint32_t)(kk & 3) * 32u;
+                            dg::tc_mma_f16(tmem + kColS, dg::smem_desc(sQ + offq, 16, 1024, 128),
+                                           dg::smem_desc(sK + offk, 16, 1024, 128), idS, kk > 0 ? 1u : 0u);
+                        }
+                        dg::tc_commit(&sh.sfull);
+                        dg::tc_commit(&sh.kempty[st]);              // the K buffer, once S has read it
+                        if (i == r.nt - 1) dg::tc_commit(&sh.qempty);  // the Q buffer, after the item's last S
                     }
-                    dg::tc_commit(&sh.pvdone[st]);
-                    dg::tc_commit(&sh.vempty[st]);
+                    if (i >= 1) {  // O += P V of tile g + i - 1 once the softmax has written P
+                        const int j = i - 1;
+                        const uint32_t gp = g + (uint32_t)j;
+                        const int st = (int)(gp & 1u);
+                        if (!attn_wait(&sh.pfull, gp & 1u) || !attn_wait(&sh.vfull[st], (gp >> 1) & 1u) ||
+                            (j == 0 && !attn_wait(&sh.oempty, (kq & 1u) ^ 1u))) {  // the last item's O read out
+                            ok = false;
+                            break;
+                        }
+                        dg::tc_fence_after();
+                        const uint32_t sV = dg::smem_u32(smem + kOffV + st * kKVBytes);
+#pragma unroll
+                        for (int kk = 0; kk < kKeys / 16; ++kk) {
+                            // A: P in tensor memory, 16 keys = 8 columns per step; B: 16 V rows (keys)
+                            // x 128 columns (two 64-column atoms, kKSub apart)
+                            dg::tc_mma_f16_ts(tmem + kColO, tmem + kColP + (uint32_t)(st * 32 + kk * 8),
+                                              dg::smem_desc(sV + (uint32_t)kk * 16u * 128u, kKSub, 1024, 128), idO,
+                                              (j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        dg::tc_commit(&sh.pvdone[st]);
+                        dg::tc_commit(&sh.vempty[st]);
+                    }
                 }
+                g += (uint32_t)r.nt;
             }
             if (!ok) do_abort(sh, a.status);
             // every MMA issued above has completed before the tensor memory is released
@@ -349,116 +442,127 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        const int pos = r.kl - r.ql + t * kTile + row;
-        const bool row_valid = t * kTile + row < r.ql;
-        float m_ref = -INFINITY, l = 0.f;
+        uint32_t g = 0, kq = 0;
         bool ok = true;
-        for (int i = 0; i < r.nt; ++i) {
-            if (!attn_wait_warp(&sh.sfull, (uint32_t)i & 1u)) {
-                ok = false;
-                break;
-            }
-            dg::tc_fence_after();
-            float x[2][32];
-            {
-                uint32_t raw[2][32];
-#pragma unroll
-                for (int c = 0; c < 2; ++c) dg::tmem_ld32_nowait(tmem + lane_base + kColS + (uint32_t)(c * 32), raw[c]);
-                dg::tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) x[c][e] = __uint_as_float(raw[c][e]);
-            }
-            dg::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) dg::mbar_arrive(&sh.sempty);  // S free for S_{i+1}
-            const int jt = r.jt_lo + i;
-            const int j0 = jt * kKeys;
-            if (!tile_full(r, a.window, jt)) {
-                // masked entries: -inf, which 2^x maps to 0.  The keys a query at position pos may
-                // see form one range: j < kv_len, j <= pos if causal, and with a window W also
-                // j >= pos - W and (bidirectional) j <= pos + W; the mask is two compares per entry
-                const int64_t W = a.window;
-                const int lo = (int)max((int64_t)-1, (W >= 0 ? (int64_t)pos - W : 0) - j0);
-                const int hi = (int)min((int64_t)kKeys,
-                                        min((int64_t)r.kl - 1, r.causal ? (int64_t)pos : (W >= 0 ? (int64_t)pos + W : (int64_t)r.kl - 1)) - j0);
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int k = c * 32 + e;
-                        x[c][e] = (k >= lo && k <= hi) ? x[c][e] : -INFINITY;
-                    }
-            }
-            // the tile's row maximum of the raw scores (a tree: independent steps), in log2 units
-            float mx[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) mx[e] = fmaxf(fmaxf(x[0][2 * e], x[0][2 * e + 1]), fmaxf(x[1][2 * e], x[1][2 * e + 1]));
-#pragma unroll
-            for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-                for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
-            const float tmax = mx[0] * a.scale_log2;  // -inf stays -inf (scale > 0)
-            const bool rescale = __any_sync(0xffffffffu, tmax > m_ref + kRescaleAbove);  // m_ref = -inf: any finite max
-            // before P buffer i % 2 is rewritten, the P V that read it (tile i - 2) must be done;
-            // before O is rescaled, the last P V (tile i - 1), which implies the one before
-            if (i > 0 && (rescale || i > 1)) {
-                const int j = rescale ? i - 1 : i - 2;
-                if (!attn_wait_warp(&sh.pvdone[j & 1], ((uint32_t)j >> 1) & 1u)) {
+        for (int64_t w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++kq) {
+            const int2 it = items[w / a.Hq];
+            const int h = (int)(w % a.Hq);
+            const TileRange r = tile_range(a, it.x, it.y);
+            const int t = it.y;
+            const int pos = r.kl - r.ql + t * kTile + row;
+            const bool row_valid = t * kTile + row < r.ql;
+            float m_ref = -INFINITY, l = 0.f;
+            for (int i = 0; i < r.nt; ++i) {
+                const uint32_t gi = g + (uint32_t)i;
+                if (!attn_wait_warp(&sh.sfull, gi & 1u)) {
                     ok = false;
                     break;
                 }
                 dg::tc_fence_after();
-            }
-            if (rescale) {
-                const float m_new = fmaxf(m_ref, tmax);
-                const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_ref - m_new);
-                l *= alpha;
-                if (i > 0) {
+                float x[2][32];
+                {
+                    uint32_t raw[2][32];
 #pragma unroll
-                    for (int c = 0; c < kHead / 32; ++c) {
-                        float o[32];
-                        const uint32_t ta = tmem + lane_base + kColO + (uint32_t)(c * 32);
-                        dg::tmem_ld32(ta, o);
+                    for (int c = 0; c < 2; ++c) dg::tmem_ld32_nowait(tmem + lane_base + kColS + (uint32_t)(c * 32), raw[c]);
+                    dg::tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                        dg::tmem_st32(ta, o);
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) x[c][e] = __uint_as_float(raw[c][e]);
+                }
+                dg::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) dg::mbar_arrive(&sh.sempty);  // S free for the next tile's S
+                const int jt = r.jt_lo + i;
+                const int j0 = jt * kKeys;
+                if (!tile_full(r, a.window, jt)) {
+                    // masked entries: -inf, which 2^x maps to 0.  The keys a query at position pos may
+                    // see form one range: j < kv_len, j <= pos if causal, and with a window W also
+                    // j >= pos - W and (bidirectional) j <= pos + W; the mask is two compares per entry
+                    const int64_t W = a.window;
+                    const int lo = (int)max((int64_t)-1, (W >= 0 ? (int64_t)pos - W : 0) - j0);
+                    const int hi = (int)min((int64_t)kKeys,
+                                            min((int64_t)r.kl - 1, r.causal ? (int64_t)pos : (W >= 0 ? (int64_t)pos + W : (int64_t)r.kl - 1)) - j0);
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int kx = c * 32 + e;
+                            x[c][e] = (kx >= lo && kx <= hi) ? x[c][e] : -INFINITY;
+                        }
+                }
+                // the tile's row maximum of the raw scores (a tree: independent steps), in log2 units
+                float mx[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) mx[e] = fmaxf(fmaxf(x[0][2 * e], x[0][2 * e + 1]), fmaxf(x[1][2 * e], x[1][2 * e + 1]));
+#pragma unroll
+                for (int wd = 8; wd >= 1; wd >>= 1)
+#pragma unroll
+                    for (int e = 0; e < wd; ++e) mx[e] = fmaxf(mx[e], mx[e + wd]);
+                const float tmax = mx[0] * a.scale_log2;  // -inf stays -inf (scale > 0)
+                const bool rescale = __any_sync(0xffffffffu, tmax > m_ref + kRescaleAbove);  // m_ref = -inf: any finite max
+                // O is rescaled only after this item's last P V (which implies the one before);
+                // otherwise P buffer gi % 2 must have been read by the P V two tiles back, which may
+                // be the previous item's
+                if ((rescale && i > 0) || gi > 1) {
+                    const uint32_t gj = (rescale && i > 0) ? gi - 1 : gi - 2;
+                    if (!attn_wait_warp(&sh.pvdone[gj & 1u], (gj >> 1) & 1u)) {
+                        ok = false;
+                        break;
                     }
-                    dg::tmem_st_wait();
+                    dg::tc_fence_after();
                 }
-                m_ref = m_new;
-            }
-            // P = 2^(s c - m_ref) in bf16 pairs into P buffer i % 2 for the P V MMA; the exponent
-            // in one packed fma per pair (a row with no allowed key yet keeps m_ref = -inf: its
-            // entries are all -inf and the offset 0 keeps them so)
-            const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            const uint64_t cc = f2(a.scale_log2, a.scale_log2), mm = f2(neg_m, neg_m);
-            uint64_t acc = f2(0.f, 0.f);
-            uint32_t pk[32];
+                if (rescale) {
+                    const float m_new = fmaxf(m_ref, tmax);
+                    const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_ref - m_new);
+                    l *= alpha;
+                    if (i > 0) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+                        for (int c = 0; c < kHead / 32; ++c) {
+                            float o[32];
+                            const uint32_t ta = tmem + lane_base + kColO + (uint32_t)(c * 32);
+                            dg::tmem_ld32(ta, o);
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float z0, z1;
-                    f2_split(f2_fma(f2(x[c][e], x[c][e + 1]), cc, mm), z0, z1);
-                    const float p0 = ex2(z0), p1 = ex2(z1);
-                    acc = f2_add(acc, f2(p0, p1));
-                    pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
+                            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                            dg::tmem_st32(ta, o);
+                        }
+                        dg::tmem_st_wait();
+                    }
+                    m_ref = m_new;
                 }
+                // P = 2^(s c - m_ref) in bf16 pairs into P buffer gi % 2 for the P V MMA; the exponent
+                // in one packed fma per pair (a row with no allowed key yet keeps m_ref = -inf: its
+                // entries are all -inf and the offset 0 keeps them so)
+                const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                const uint64_t cc = f2(a.scale_log2, a.scale_log2), mm = f2(neg_m, neg_m);
+                uint64_t acc = f2(0.f, 0.f);
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float z0, z1;
+                        f2_split(f2_fma(f2(x[c][e], x[c][e + 1]), cc, mm), z0, z1);
+                        const float p0 = ex2(z0), p1 = ex2(z1);
+                        acc = f2_add(acc, f2(p0, p1));
+                        pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
+                    }
+                }
+                float sa, sb;
+                f2_split(acc, sa, sb);
+                dg::tmem_st32u(tmem + lane_base + kColP + (gi & 1u) * 32u, pk);
+                dg::tmem_st_wait();
+                l += sa + sb;
+                dg::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) dg::mbar_arrive(&sh.pfull);
             }
-            float sa, sb;
-            f2_split(acc, sa, sb);
-            const float sum = sa + sb;
-            dg::tmem_st32u(tmem + lane_base + kColP + (uint32_t)((i & 1) * 32), pk);
-            dg::tmem_st_wait();
-            l += sum;
-            dg::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) dg::mbar_arrive(&sh.pfull);
-        }
-        if (ok && !attn_wait_warp(&sh.pvdone[(r.nt - 1) & 1], ((uint32_t)(r.nt - 1) >> 1) & 1u)) ok = false;
-        if (ok) {
+            if (!ok) break;
+            const uint32_t gl = g + (uint32_t)r.nt - 1u;  // the item's last P V
+            if (!attn_wait_warp(&sh.pvdone[gl & 1u], (gl >> 1) & 1u)) {
+                ok = false;
+                break;
+            }
             dg::tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int64_t qi = (int64_t)r.q0 + t * kTile + row;
@@ -476,9 +580,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
             if (row_valid && a.lse) a.lse[qi * a.Hq + h] = (m_ref + log2f(l)) * kLn2;
-        } else {
-            do_abort(sh, a.status);
+            dg::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) dg::mbar_arrive(&sh.oempty);  // O read out: the next item may overwrite it
+            g += (uint32_t)r.nt;
         }
+        if (!ok) do_abort(sh, a.status);
     }
 
     dg::tc_fence_before();
@@ -504,12 +611,23 @@ bool tmap_heads(CUtensorMap* tm, const void* base, int64_t rows, int32_t heads, 
     return dghost::encode_tmap(tm, 0, 2, const_cast<void*>(base), dims, strides, box, 128);
 }
 
+// Plan: a header and one (sequence, query tile) entry per possible item.
+size_t plan_bytes(int64_t n_seq, int64_t max_q_tiles) {
+    return ((size_t)kPlanHeader * 4 + (size_t)n_seq * (size_t)max_q_tiles * 8 + 255) / 256 * 256;
+}
+
 }  // namespace
+
+extern "C" size_t dg_attention_workspace_bytes(int32_t n_seq, int32_t max_q_len) {
+    if (n_seq < 0 || max_q_len < 1) return 0;
+    return plan_bytes(n_seq, (max_q_len + kTile - 1) / kTile);
+}
 
 extern "C" dg_status dg_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse,
                                   const int32_t* cu_q, const int32_t* cu_kv, const uint8_t* causal, int32_t n_seq,
                                   int32_t max_q_len, int64_t total_q, int64_t total_kv, int32_t Hq, int32_t Hkv,
-                                  int32_t D, int32_t window, float scale, dg_stream_t stream) {
+                                  int32_t D, int32_t window, float scale, void* workspace, size_t workspace_bytes,
+                                  dg_stream_t stream) {
     if (n_seq < 0 || n_seq > 65535 || Hq < 1 || Hq > 65535 || Hkv < 1 || Hq % Hkv != 0 || window < -1 ||
         !(scale == scale) || scale == INFINITY || scale == -INFINITY)
         return DG_ERR_INVALID_ARG;
@@ -520,6 +638,11 @@ extern "C" dg_status dg_attention(const uint16_t* q, const uint16_t* k, const ui
         return DG_ERR_INVALID_ARG;
     if (!q || !k || !v || !o || !cu_q || !cu_kv || !causal) return DG_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return DG_ERR_ALIGNMENT;
+    const int32_t max_q_tiles = (max_q_len + kTile - 1) / kTile;
+    if (!workspace || workspace_bytes < plan_bytes(n_seq, max_q_tiles)) return DG_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DG_ERR_ALIGNMENT;
+    const int P = dghost::sm_count();
+    if (P <= 0) return DG_ERR_CUDA;
     CUtensorMap tq, tk, tv;
     if (!tmap_heads(&tq, q, total_q, Hq, kTile) || !tmap_heads(&tk, k, total_kv, Hkv, kKeys) ||
         !tmap_heads(&tv, v, total_kv, Hkv, kKeys))
@@ -539,8 +662,15 @@ extern "C" dg_status dg_attention(const uint16_t* q, const uint16_t* k, const ui
     a.total_kv = total_kv;
     a.scale_log2 = scale * kLog2e;
     a.status = dghost::status_word();
-    const dim3 grid((unsigned)((max_q_len + kTile - 1) / kTile), (unsigned)Hq, (unsigned)n_seq);
-    k_attention<<<grid, kThreads, kAttnSmem, (cudaStream_t)stream>>>(tq, tk, tv, a);
+    int32_t* plan = static_cast<int32_t*>(workspace);
+    cudaStream_t st = (cudaStream_t)stream;
+    k_attn_plan<<<1, 1024, 0, st>>>(a, n_seq, max_q_tiles, plan);
+    dghost::count_launch();
+    if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+    // two persistent CTAs per SM, or fewer when there is less work (the device knows exactly)
+    const int64_t work_bound = (int64_t)n_seq * max_q_tiles * Hq;
+    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(2LL * P, work_bound));
+    k_attention<<<grid, kThreads, kAttnSmem, st>>>(tq, tk, tv, a, plan);
     dghost::count_launch();
     return dghost::cuda_status(cudaGetLastError());
 }

@@ -290,17 +290,23 @@ DG_API dg_status dg_lm_head_denoise_step(const uint16_t* hidden, int64_t ldh, co
  *   o    (device, out) [total_q][Hq][D] bf16.
  *   lse  (device, out, may be NULL) [total_q][Hq] float: log sum exp of the allowed scores.
  *   cu_q, cu_kv (device) [n_seq + 1] int32 offsets (non-decreasing); causal (device) [n_seq].
- *   max_q_len: at least every sequence's q_len (a smaller one leaves queries out and raises
- *   DG_DEV_BAD_PARAM); a sequence with q_len > kv_len or offsets outside [0, total_q] /
- *   [0, total_kv] raises DG_DEV_BAD_PARAM and is skipped (its rows of o are not written).
+ *   max_q_len: at least every sequence's q_len (a smaller one leaves the queries past it out
+ *   and raises DG_DEV_BAD_PARAM); a sequence with q_len > kv_len or offsets outside
+ *   [0, total_q] / [0, total_kv] raises DG_DEV_BAD_PARAM and is skipped (its rows of o are not
+ *   written).
+ *   workspace (device) >= dg_attention_workspace_bytes(n_seq, max_q_len), 16-byte aligned,
+ *   no initial contents: the list of (sequence, query tile) items, longest first.
  * D must be 128 (else DG_ERR_UNSUPPORTED); Hq a multiple of Hkv; window >= -1 (-1: none);
  * total_q, total_kv < 2^31; q, k, v, o 16-byte aligned.  Computed on the tensor cores
- * (tcgen05, bf16 operands, fp32 accumulation and softmax, one pass).  One kernel launch. */
+ * (tcgen05, bf16 operands, fp32 accumulation and softmax, one pass) by two persistent CTAs
+ * per SM that take the listed items in turn.  Two kernel launches (the list, the attention). */
+DG_API size_t dg_attention_workspace_bytes(int32_t n_seq, int32_t max_q_len);
 DG_API dg_status dg_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
                               float* lse, const int32_t* cu_q, const int32_t* cu_kv,
                               const uint8_t* causal, int32_t n_seq, int32_t max_q_len,
                               int64_t total_q, int64_t total_kv, int32_t Hq, int32_t Hkv, int32_t D,
-                              int32_t window, float scale, dg_stream_t stream);
+                              int32_t window, float scale, void* workspace, size_t workspace_bytes,
+                              dg_stream_t stream);
 
 /* ------------------------------------------------------------------------------------ */
 /* Self-conditioning [DG "자기 조건화"]:                                                  */

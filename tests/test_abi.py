@@ -107,8 +107,11 @@ def test_lm_head_validation_without_gpu():
 def test_attention_validation_without_gpu():
     lib = dg.load()
 
-    def call(q=16, k=16, v=16, o=16, n=1, mq=4, tq=4, tk=8, Hq=2, Hkv=1, D=128, W=-1, scale=0.1):
-        return lib.dg_attention(q, k, v, o, None, 16, 16, 16, n, mq, tq, tk, Hq, Hkv, D, W, scale, None)
+    assert dg.dg_attention_workspace_bytes(3, 300) == 256      # 16 + 3 x 3 x 8 bytes, rounded
+    assert dg.dg_attention_workspace_bytes(100, 1024) == (16 + 100 * 8 * 8 + 255) // 256 * 256
+
+    def call(q=16, k=16, v=16, o=16, n=1, mq=4, tq=4, tk=8, Hq=2, Hkv=1, D=128, W=-1, scale=0.1, ws=256, wsb=256):
+        return lib.dg_attention(q, k, v, o, None, 16, 16, 16, n, mq, tq, tk, Hq, Hkv, D, W, scale, ws, wsb, None)
 
     assert call(D=64) == dg.DG_ERR_UNSUPPORTED
     assert call(Hq=3, Hkv=2) == dg.DG_ERR_INVALID_ARG
@@ -118,6 +121,9 @@ def test_attention_validation_without_gpu():
     assert call(tk=0) == dg.DG_ERR_INVALID_ARG
     assert call(q=None) == dg.DG_ERR_INVALID_ARG
     assert call(o=24) == dg.DG_ERR_ALIGNMENT
+    assert call(ws=None) == dg.DG_ERR_WORKSPACE
+    assert call(wsb=0) == dg.DG_ERR_WORKSPACE
+    assert call(ws=264) == dg.DG_ERR_ALIGNMENT
     assert call(n=0, q=None) == dg.DG_OK
 
 

@@ -619,6 +619,25 @@ def run_ours(args):
     return 0
 
 
+def attention_counts(seqs, W, TQ=128, TK=64):
+    """(allowed (query, key) pairs, key tiles visited, key tiles in all) for sequences given as
+    (q_len, kv_len, causal): a query tile visits every TK-key tile from the first key any of
+    its queries may see to the last."""
+    pairs = tiles = tiles_all = 0
+    for ql, kl, c in seqs:
+        pos = np.arange(kl - ql, kl)
+        lo = np.maximum(0, pos - W) if W >= 0 else np.zeros_like(pos)
+        hi = pos if c else (np.minimum(kl - 1, pos + W) if W >= 0 else np.full_like(pos, kl - 1))
+        pairs += int((hi - lo + 1).sum())
+        for t0 in range(0, ql, TQ):
+            p0, p1 = int(pos[t0]), int(pos[min(ql, t0 + TQ) - 1])
+            jl = max(0, p0 - W) if W >= 0 else 0
+            jh = p1 if c else (min(kl - 1, p1 + W) if W >= 0 else kl - 1)
+            tiles += jh // TK - jl // TK + 1
+            tiles_all += (kl + TK - 1) // TK
+    return pairs, tiles, tiles_all
+
+
 def _attention_rows(dg, synth, dev, stream, time_fn, peak_tc):
     """dg_attention timed alone on a denoising batch: 8 canvases of 256 after 2048 context
     tokens (bidirectional) and 4 causal prefills of 1024, 16 query heads over 8 key/value
@@ -635,19 +654,7 @@ def _attention_rows(dg, synth, dev, stream, time_fn, peak_tc):
     aws = torch.empty(dg.dg_attention_workspace_bytes(len(seqs), 1024), dtype=torch.uint8, device=dev)
     attn = {}
     for W in (-1, 512):
-        pairs = 0
-        tiles = tiles_all = 0
-        for ql, kl, c in seqs:
-            pos = np.arange(kl - ql, kl)
-            lo = np.maximum(0, pos - W) if W >= 0 else np.zeros_like(pos)
-            hi = pos if c else (np.minimum(kl - 1, pos + W) if W >= 0 else np.full_like(pos, kl - 1))
-            pairs += int((hi - lo + 1).sum())
-            for t0 in range(0, ql, TQ):
-                p0, p1 = int(pos[t0]), int(pos[min(ql, t0 + TQ) - 1])
-                jl = max(0, p0 - W) if W >= 0 else 0
-                jh = p1 if c else (min(kl - 1, p1 + W) if W >= 0 else kl - 1)
-                tiles += jh // TK - jl // TK + 1
-                tiles_all += (kl + TK - 1) // TK
+        pairs, tiles, tiles_all = attention_counts(seqs, W, TQ, TK)
         ms = time_fn(lambda: dg.dg_attention(aq, ak, av, ao, dq, dkv, dcz, 1024, window=W, workspace=aws,
                                              stream=stream), reps=20)
         alg = 4.0 * pairs * Dh * Hq

@@ -11,9 +11,10 @@
 // queries are its last q_len tokens (query i sits at kv_len - q_len + i); that and the score
 // scale * q.k without soft-capping are readings, the pages give only the figures.
 //
-// One CTA per (128-query tile, query head, sequence), two CTAs per SM (each 256 TMEM columns
-// and under half the shared memory, so one CTA's barrier waits are the other's issue slots);
-// one pass with an online softmax:
+// Work items are (sequence, 128-query tile, query head); a plan kernel lists the items longest
+// first and two persistent CTAs per SM take them in turn (each 256 TMEM columns and under half
+// the shared memory, so one CTA's barrier waits are the other's issue slots); one pass with an
+// online softmax per item:
 //   warp 0      TMA producers: the Q tile once, then K and V tiles (64 keys) in two 2-stage
 //               rings (a K buffer frees when its S MMA is done, a V buffer after its P V);
 //   warp 1      MMA issuer (one elected thread): S = Q K^T (128 x 64) into TMEM, issued as soon

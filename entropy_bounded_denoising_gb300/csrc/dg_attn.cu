@@ -40,12 +40,9 @@ namespace {
 
 constexpr int kTile = 128;      // queries per CTA
 constexpr int kKeys = 64;       // keys per tile
-constexpr int kHead = 128;      // head dimension D
 constexpr int kSub = 64;        // columns per 128-byte swizzle atom
 constexpr uint32_t kQSub = kTile * kSub * 2;       // 16 KB: 128 rows x 64 columns of Q
-constexpr uint32_t kQBytes = 2 * kQSub;            // the Q tile, D = 128
 constexpr uint32_t kKSub = kKeys * kSub * 2;       // 8 KB: 64 rows x 64 columns of K or V
-constexpr uint32_t kKVBytes = 2 * kKSub;           // one K (or V) tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 #ifndef DG_ATTN_RESCALE_LOG2
@@ -82,16 +79,26 @@ struct __align__(8) AttnShared {
     int abort_flag;
 };
 
-// shared memory: Q | K[2] | V[2] (1024-aligned blocks), then the barriers
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kQBytes;
-constexpr uint32_t kOffV = kOffK + 2 * kKVBytes;
-constexpr uint32_t kOffBar = kOffV + 2 * kKVBytes;
-constexpr size_t kAttnSmem = 1024 + kOffBar + sizeof(AttnShared) + 64;
-static_assert(2 * (kAttnSmem + 1024) <= 232448, "two CTAs fit the shared memory of an SM");
-// tensor memory columns (256 per CTA): S, O, P buffers (bf16 pairs: 32 columns for 64 keys)
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0, kColO = 64, kColP = 192;
+// Per head dimension D (64, 128 or 256): shared memory Q | K[2] | V[2] (1024-aligned blocks of
+// D / 64 swizzle atoms each), then the barriers; tensor memory columns S (64), O (D), the two P
+// buffers (bf16 pairs: 32 columns for 64 keys each), rounded up to a power of two.  Two CTAs
+// share an SM while both fit (D = 64, 128), else one (D = 256).
+template <int D>
+struct AttnCfg {
+    static_assert(D == 64 || D == 128 || D == 256, "head dimension 64, 128 or 256");
+    static constexpr int kHead = D;
+    static constexpr uint32_t kQBytes = (D / kSub) * kQSub;     // the Q tile
+    static constexpr uint32_t kKVBytes = (D / kSub) * kKSub;    // one K (or V) tile
+    static constexpr uint32_t kOffQ = 0;
+    static constexpr uint32_t kOffK = kOffQ + kQBytes;
+    static constexpr uint32_t kOffV = kOffK + 2 * kKVBytes;
+    static constexpr uint32_t kOffBar = kOffV + 2 * kKVBytes;
+    static constexpr size_t kSmem = 1024 + kOffBar + sizeof(AttnShared) + 64;
+    static constexpr uint32_t kColS = 0, kColO = 64, kColP = 64 + D;
+    static constexpr uint32_t kTmemCols = (kColP + 64 <= 256) ? 256 : 512;
+    static constexpr int kCtasPerSm = (2 * (kSmem + 1024) <= 232448 && 2 * kTmemCols <= 512) ? 2 : 1;
+    static_assert(kSmem <= 232448, "fits the opt-in shared memory of an SM");
+};
 constexpr int kThreads = 192;
 
 // The key tiles a query tile visits, and whether a key tile is allowed for all its queries.
@@ -277,9 +284,15 @@ __global__ void __launch_bounds__(1024) k_attn_plan(const AttnArgs a, int32_t n_
 // w % Hq).  Every ring, buffer and barrier phase is counted over the CTA's whole run (g: its
 // key tiles so far, k: its items so far), so the next item's Q and K / V loads and its first
 // S MMA overlap the current item's last tiles and its epilogue.
-__global__ void __launch_bounds__(kThreads, 2)
+template <int D>
+__global__ void __launch_bounds__(kThreads, AttnCfg<D>::kCtasPerSm)
     k_attention(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const AttnArgs a, const int32_t* __restrict__ plan) {
+    using C = AttnCfg<D>;
+    constexpr int kHead = D;
+    constexpr uint32_t kQBytes = C::kQBytes, kKVBytes = C::kKVBytes;
+    constexpr uint32_t kOffQ = C::kOffQ, kOffK = C::kOffK, kOffV = C::kOffV, kOffBar = C::kOffBar;
+    constexpr uint32_t kColS = C::kColS, kColO = C::kColO, kColP = C::kColP, kTmemCols = C::kTmemCols;
     extern __shared__ __align__(1024) unsigned char attn_smem_raw[];
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(attn_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -334,8 +347,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 const int qrow = a.cu_q[it.x] + it.y * kTile;
                 dg::mbar_arrive_expect_tx(&sh.qfull, kQBytes);
-                dg::tma_load_2d(smem + kOffQ, &tmQ, h * kHead, qrow, &sh.qfull);
-                dg::tma_load_2d(smem + kOffQ + kQSub, &tmQ, h * kHead + kSub, qrow, &sh.qfull);
+#pragma unroll
+                for (int c = 0; c < kHead / kSub; ++c)
+                    dg::tma_load_2d(smem + kOffQ + c * kQSub, &tmQ, h * kHead + c * kSub, qrow, &sh.qfull);
             }
             if (!ok) do_abort(sh, a.status);
             if (aborted(sh) && kq > 0) (void)attn_wait(&sh.qfull, (kq - 1u) & 1u);  // the last Q copy landed
@@ -362,8 +376,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                     dg::mbar_arrive_expect_tx(&full[st], kKVBytes);
                     const int krow = r.k0 + (r.jt_lo + i) * kKeys;
                     unsigned char* dst = ring + st * kKVBytes;
-                    dg::tma_load_2d(dst, tm, hk * kHead, krow, &full[st]);
-                    dg::tma_load_2d(dst + kKSub, tm, hk * kHead + kSub, krow, &full[st]);
+#pragma unroll
+                    for (int c = 0; c < kHead / kSub; ++c)
+                        dg::tma_load_2d(dst + c * kKSub, tm, hk * kHead + c * kSub, krow, &full[st]);
                     ++issued[st];
                 }
             }
@@ -422,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                         for (int kk = 0; kk < kKeys / 16; ++kk) {
                             // A: P in tensor memory, 16 keys = 8 columns per step; B: 16 V rows (keys)
-                            // x 128 columns (two 64-column atoms, kKSub apart)
+                            // x D columns (D / 64 atoms of 64 columns, kKSub apart)
                             dg::tc_mma_f16_ts(tmem + kColO, tmem + kColP + (uint32_t)(st * 32 + kk * 8),
                                               dg::smem_desc(sV + (uint32_t)kk * 16u * 128u, kKSub, 1024, 128), idO,
                                               (j > 0 || kk > 0) ? 1u : 0u);
@@ -605,9 +620,9 @@ namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // [rows][heads * D] bf16 with boxes of 64 columns (one 128-byte swizzle atom) x box_rows.
-bool tmap_heads(CUtensorMap* tm, const void* base, int64_t rows, int32_t heads, uint32_t box_rows) {
-    uint64_t dims[2] = {(uint64_t)heads * kHead, (uint64_t)rows};
-    uint64_t strides[1] = {(uint64_t)heads * kHead * 2};
+bool tmap_heads(CUtensorMap* tm, const void* base, int64_t rows, int32_t heads, int32_t D, uint32_t box_rows) {
+    uint64_t dims[2] = {(uint64_t)heads * D, (uint64_t)rows};
+    uint64_t strides[1] = {(uint64_t)heads * D * 2};
     uint32_t box[2] = {(uint32_t)kSub, box_rows};
     return dghost::encode_tmap(tm, 0, 2, const_cast<void*>(base), dims, strides, box, 128);
 }
@@ -632,7 +647,7 @@ extern "C" dg_status dg_attention(const uint16_t* q, const uint16_t* k, const ui
     if (n_seq < 0 || n_seq > 65535 || Hq < 1 || Hq > 65535 || Hkv < 1 || Hq % Hkv != 0 || window < -1 ||
         !(scale == scale) || scale == INFINITY || scale == -INFINITY)
         return DG_ERR_INVALID_ARG;
-    if (D != kHead) return DG_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128 && D != 256) return DG_ERR_UNSUPPORTED;
     if (n_seq == 0) return DG_OK;
     if (max_q_len < 1 || max_q_len > (1 << 30) || total_q < 1 || total_kv < 1 || total_q >= (1LL << 31) ||
         total_kv >= (1LL << 31))
@@ -645,10 +660,8 @@ extern "C" dg_status dg_attention(const uint16_t* q, const uint16_t* k, const ui
     const int P = dghost::sm_count();
     if (P <= 0) return DG_ERR_CUDA;
     CUtensorMap tq, tk, tv;
-    if (!tmap_heads(&tq, q, total_q, Hq, kTile) || !tmap_heads(&tk, k, total_kv, Hkv, kKeys) ||
-        !tmap_heads(&tv, v, total_kv, Hkv, kKeys))
-        return DG_ERR_CUDA;
-    if (cudaFuncSetAttribute(k_attention, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttnSmem) != cudaSuccess)
+    if (!tmap_heads(&tq, q, total_q, Hq, D, kTile) || !tmap_heads(&tk, k, total_kv, Hkv, D, kKeys) ||
+        !tmap_heads(&tv, v, total_kv, Hkv, D, kKeys))
         return DG_ERR_CUDA;
     AttnArgs a;
     a.cu_q = cu_q;
@@ -668,10 +681,18 @@ extern "C" dg_status dg_attention(const uint16_t* q, const uint16_t* k, const ui
     k_attn_plan<<<1, 1024, 0, st>>>(a, n_seq, max_q_tiles, plan);
     dghost::count_launch();
     if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
-    // two persistent CTAs per SM, or fewer when there is less work (the device knows exactly)
+    // persistent CTAs (two or one per SM by D), fewer when there is less work (the device knows
+    // exactly how much)
     const int64_t work_bound = (int64_t)n_seq * max_q_tiles * Hq;
-    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(2LL * P, work_bound));
-    k_attention<<<grid, kThreads, kAttnSmem, st>>>(tq, tk, tv, a, plan);
-    dghost::count_launch();
-    return dghost::cuda_status(cudaGetLastError());
+    auto launch = [&](auto kern, size_t smem, int per_sm) -> dg_status {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return DG_ERR_CUDA;
+        const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>((int64_t)per_sm * P, work_bound));
+        kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, a, plan);
+        dghost::count_launch();
+        return dghost::cuda_status(cudaGetLastError());
+    };
+    if (D == 64) return launch(k_attention<64>, AttnCfg<64>::kSmem, AttnCfg<64>::kCtasPerSm);
+    if (D == 128) return launch(k_attention<128>, AttnCfg<128>::kSmem, AttnCfg<128>::kCtasPerSm);
+    return launch(k_attention<256>, AttnCfg<256>::kSmem, AttnCfg<256>::kCtasPerSm);
 }

@@ -296,10 +296,10 @@ DG_API dg_status dg_lm_head_denoise_step(const uint16_t* hidden, int64_t ldh, co
  *   written).
  *   workspace (device) >= dg_attention_workspace_bytes(n_seq, max_q_len), 16-byte aligned,
  *   no initial contents: the list of (sequence, query tile) items, longest first.
- * D must be 128 (else DG_ERR_UNSUPPORTED); Hq a multiple of Hkv; window >= -1 (-1: none);
+ * D must be 64, 128 or 256 (else DG_ERR_UNSUPPORTED); Hq a multiple of Hkv; window >= -1 (-1: none);
  * total_q, total_kv < 2^31; q, k, v, o 16-byte aligned.  Computed on the tensor cores
- * (tcgen05, bf16 operands, fp32 accumulation and softmax, one pass) by two persistent CTAs
- * per SM that take the listed items in turn.  Two kernel launches (the list, the attention). */
+ * (tcgen05, bf16 operands, fp32 accumulation and softmax, one pass) by persistent CTAs (two
+ * per SM for D = 64 and 128, one for D = 256) that take the listed items in turn.  Two kernel launches (the list, the attention). */
 DG_API size_t dg_attention_workspace_bytes(int32_t n_seq, int32_t max_q_len);
 DG_API dg_status dg_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
                               float* lse, const int32_t* cu_q, const int32_t* cu_kv,

@@ -113,7 +113,8 @@ def test_attention_validation_without_gpu():
     def call(q=16, k=16, v=16, o=16, n=1, mq=4, tq=4, tk=8, Hq=2, Hkv=1, D=128, W=-1, scale=0.1, ws=256, wsb=256):
         return lib.dg_attention(q, k, v, o, None, 16, 16, 16, n, mq, tq, tk, Hq, Hkv, D, W, scale, ws, wsb, None)
 
-    assert call(D=64) == dg.DG_ERR_UNSUPPORTED
+    assert call(D=96) == dg.DG_ERR_UNSUPPORTED
+    assert call(D=512) == dg.DG_ERR_UNSUPPORTED
     assert call(Hq=3, Hkv=2) == dg.DG_ERR_INVALID_ARG
     assert call(W=-2) == dg.DG_ERR_INVALID_ARG
     assert call(scale=float("nan")) == dg.DG_ERR_INVALID_ARG

@@ -25,11 +25,11 @@ D = 128
 SEQS = [(300, 300, 1), (256, 1256, 0), (256, 1256, 1), (5, 5, 1), (17, 40, 0), (128, 128, 0), (1, 1, 0)]
 
 
-def _batch(seqs, Hq, Hkv, seed):
+def _batch(seqs, Hq, Hkv, seed, d=D):
     cu_q = np.cumsum([0] + [s[0] for s in seqs]).astype(np.int32)
     cu_kv = np.cumsum([0] + [s[1] for s in seqs]).astype(np.int32)
     causal = np.array([s[2] for s in seqs], np.uint8)
-    q, k, v = synth.attention_inputs(int(cu_q[-1]), int(cu_kv[-1]), Hq, Hkv, D, seed=seed, device=DEV)
+    q, k, v = synth.attention_inputs(int(cu_q[-1]), int(cu_kv[-1]), Hq, Hkv, d, seed=seed, device=DEV)
     return q, k, v, cu_q, cu_kv, causal
 
 
@@ -148,3 +148,21 @@ def test_attention_window_wider_than_every_sequence_is_no_window():
     o2, l2 = _run(q, k, v, cu_q, cu_kv, causal, 2 ** 31 - 1)
     assert dg.dg_get_device_status() == 0
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("d", [64, 256])
+@pytest.mark.parametrize("window", [-1, 200])
+def test_attention_other_head_dimensions(d, window):
+    """Head dimensions 64 (two CTAs per SM, 192 TMEM columns) and 256 (one CTA per SM, 384)."""
+    q, k, v, cu_q, cu_kv, causal = _batch(SEQS, 4, 2, seed=d + window, d=d)
+    o, lse = _run(q, k, v, cu_q, cu_kv, causal, window)
+    assert dg.dg_get_device_status() == 0
+    print(f"D={d}: max scaled error {_check(o, lse, q, k, v, cu_q, cu_kv, causal, window):.2e}")
+    if window == -1:   # a window of 0 on the causal sequences: the own value row, bit for bit
+        o0, _ = _run(q, k, v, cu_q, cu_kv, causal, 0)
+        ob, vb = synth.bf16_bits(o0), synth.bf16_bits(v)
+        for s_, (ql, kl, cz) in enumerate(SEQS):
+            if cz:
+                j = cu_kv[s_] + kl - ql + np.arange(ql)
+                for h in range(4):
+                    assert np.array_equal(ob[cu_q[s_]:cu_q[s_] + ql, h], vb[j, h // 2]), (s_, h)

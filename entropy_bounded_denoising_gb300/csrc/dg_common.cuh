@@ -214,9 +214,9 @@ DG_DEVINL void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// Returns false when the bound expired.
-DG_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitPolls; ++i)
+// Returns false when the bound expired (`polls` polls; the kernels use kWaitPolls).
+DG_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t polls = kWaitPolls) {
+    for (uint32_t i = 0; i < polls; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
@@ -225,11 +225,11 @@ DG_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity) {
 // barrier guards for the other lanes).  Keeps 31 lanes from hammering shared memory.
 // Must be called by all 32 lanes, converged.  `sleep_ns` > 0 backs off between polls for
 // waits that are off the critical path.
-DG_DEVINL bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t sleep_ns = 0) {
+DG_DEVINL bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t sleep_ns = 0, uint32_t polls = kWaitPolls) {
     int ok = 1;
     if ((threadIdx.x & 31) == 0) {
         ok = 0;
-        for (uint32_t i = 0; i < kWaitPolls; ++i) {
+        for (uint32_t i = 0; i < polls; ++i) {
             if (mbar_try_wait(bar, parity)) {
                 ok = 1;
                 break;
@@ -257,16 +257,6 @@ DG_DEVINL void tma_load_2d(void* dst, const void* tmap, int32_t c0, int32_t c1, 
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
         "[%4];" ::"r"(smem_u32(dst)),
         "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Multicast: the box lands at the same shared-memory offset in every CTA of `mask`, and each
-// of those CTAs' mbarrier at `bar`'s offset receives the byte count.
-DG_DEVINL void tma_load_2d_mc(void* dst, const void* tmap, int32_t c0, int32_t c1, uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
-        "[%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask)
         : "memory");
 }
 
@@ -364,15 +354,6 @@ DG_DEVINL void tc_commit_pair_mc(uint64_t* bar, uint16_t mask) {
 DG_DEVINL void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
-}
-
-// As tc_commit, arriving on the mbarrier at `bar`'s offset in every CTA of `mask`.
-DG_DEVINL void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
 }
 
 // tmem_ld32 without its wait: several loads can be in flight before one tmem_ld_wait (the

@@ -381,9 +381,9 @@ DG_DEVINL void logit_stats_tile(const GemmArgs& a, int m, int n_tile, int row, u
 }
 
 // ------------------------------------------------------------------ the GEMM kernel
-// Launched as clusters of cm = gridDim.x / (clusters) CTAs (cm = 1, 2 or 4).  With cm > 1
-// (N-major B only) every CTA loads BN/64/cm of the B tile's 64-column atoms and multicasts
-// them to the whole cluster, and a stage is refilled only once all cm CTAs' MMAs have read it.
+// Launched as clusters of cm CTAs: cm = 2 for the CTA-pair configurations (cta_group::2
+// MMAs over the pair's 256 rows), cm = 1 otherwise.  Every CTA loads its own operand tiles
+// with plain TMA copies; CTAs that share a tile find it in L2.
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             // (without a transform: the second CTA's relay, once its own stage has landed)
             dg::mbar_init(&sh.xform[s], PAIR ? (C::kXform ? 2 * (C::kXformWarps / DG_XFORM_GROUPS) : 1)
                                               : (C::kXform ? C::kXformThreads / DG_XFORM_GROUPS : 1));
-            dg::mbar_init(&sh.empty[s], PAIR ? 1u : (uint32_t)cm);  // one release per CTA of the cluster
+            dg::mbar_init(&sh.empty[s], 1);  // released by the (pair's) MMA commit
         }
         for (int i = 0; i < C::kNAcc; ++i) {
             dg::mbar_init(&sh.accf[i], 1);
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
     }
     dg::tc_fence_before();
-    cluster.sync();  // peers' barriers are initialised before any multicast lands
+    cluster.sync();  // the peer's barriers are initialised before any pair commit or arrival lands
     dg::tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
     // the prologue above overlaps the previous kernel; its outputs (plan, lse, A, B) are read below
@@ -473,8 +473,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                         dg::tma_load_3d(sF, &tmA, k0, crow, cz, &sh.full[s]);
                     }
                     if (C::kBMode == B_MNMAJOR) {
-                        // [K][N] embedding rows: one 64-column (128-byte) atom column per load; with
-                        // a cluster each CTA fetches every cm-th atom for all of its peers
+                        // [K][N] embedding rows: one 64-column (128-byte) atom column per load
                         if (PAIR) {
                             // this CTA's half of each 256-column slab h: atoms 2h, 2h + 1
 #pragma unroll
@@ -483,14 +482,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                                 for (int at = 0; at < 2; ++at)
                                     dg::tma_load_2d(sB + (2 * h + at) * (C::BK * 128), &tmB0,
                                                     im.n * C::BN + h * 256 + rank * 128 + at * 64, k0, &sh.full[s]);
-                        } else if (cm == 1) {
+                        } else {
 #pragma unroll
                             for (int j = 0; j < C::BN / 64; ++j)
                                 dg::tma_load_2d(sB + j * (C::BK * 128), &tmB0, im.n * C::BN + j * 64, k0, &sh.full[s]);
-                        } else {
-                            for (int j = rank; j < C::BN / 64; j += cm)
-                                dg::tma_load_2d_mc(sB + j * (C::BK * 128), &tmB0, im.n * C::BN + j * 64, k0,
-                                                   &sh.full[s], mask);
                         }
                     } else if (C::kBMode == B_KMAJOR) {
                         // pair: this CTA's half of the tile's rows (box of BN / 2 rows)
@@ -581,10 +576,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                             dg::tc_mma_f16(dacc, ad, bd, idesc, accum);
                         }
                     }
-                    // frees the stage (in every CTA of the cluster) once these MMAs have read it
+                    // frees the stage (in both CTAs of a pair) once these MMAs have read it
                     if constexpr (PAIR) dg::tc_commit_pair_mc(&sh.empty[s], mask);
-                    else if (cm == 1) dg::tc_commit(&sh.empty[s]);
-                    else dg::tc_commit_mc(&sh.empty[s], mask);
+                    else dg::tc_commit(&sh.empty[s]);
                 }
                 if (!ok) { do_abort(sh, a.status); break; }
                 if constexpr (PAIR) dg::tc_commit_pair_mc(&sh.accf[ab], mask);  // both CTAs' accumulators complete
@@ -744,7 +738,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
 
     dg::tc_fence_before();
-    // no CTA leaves while a peer may still multicast into it or release its stages
+    // no CTA of a pair leaves while its peer may still signal its barriers
     cluster.sync();
     if (warp == 1) {
         dg::tc_fence_after();
@@ -912,7 +906,7 @@ __global__ void k_zero_rows(const dg_canvas_params* __restrict__ params, const u
 #endif
 using PEbf16 = Cfg<A_SOFTMAX_BF16, B_MNMAJOR, 512, 32, DG_PE_STAGES, true>;
 using PEfp32 = Cfg<A_SOFTMAX_FP32, B_MNMAJOR, 512, 32, 5, true>;
-using PEprob = Cfg<A_TMA, B_MNMAJOR, 512, 32, 5>;
+using PEprob = Cfg<A_TMA, B_MNMAJOR, 512, 32, DG_PE_STAGES, true>;  // plain N-major B: CTA pairs
 using GateUp = Cfg<A_TMA, B_KMAJOR_GATEUP, 256, 64, DG_MLP_STAGES, true>;
 using Down = Cfg<A_TMA, B_KMAJOR, 256, 64, DG_MLP_STAGES, true>;
 using DownSingle = Cfg<A_TMA, B_KMAJOR, 256, 64, 4>;  // plain GEMMs (K-major B) on one CTA per tile
@@ -931,13 +925,11 @@ struct LaunchPlan {
     int split_below;  // percent
 };
 
-// Cluster size, persistent grid and k-slices for a GEMM.  The N-major B tile (embedding rows)
-// is shared by the 2 CTAs of a cluster on neighbouring m-tiles (pairs fill the GPCs better
-// than 4-CTA clusters, and measured as fast); the 4-CTA form stays available and is used
-// only while the GPU keeps at least 90 % of its SMs busy with it.  The k-slices are then
-// chosen for the number of clusters, within `max_slots` partial tiles, with slices of at
-// least `min_slice` k-blocks, and only when the unsplit work would fill less than
-// `split_below` of the clusters' last round.
+// Cluster size, persistent grid and k-slices for a GEMM.  Pair configurations run as 2-CTA
+// clusters (as many as fit at once), the others one CTA per cluster on every SM.  The
+// k-slices are then chosen for the number of clusters, within `max_slots` partial tiles,
+// with slices of at least `min_slice` k-blocks, and only when the unsplit work would fill
+// less than `split_below` of the clusters' last round.
 template <class C>
 bool plan_gemm(const GemmArgs& a, int64_t max_slots, LaunchPlan* pl, int min_slice = 256, int split_below = 101) {
     auto kern = k_gemm<C>;
@@ -954,22 +946,16 @@ bool plan_gemm(const GemmArgs& a, int64_t max_slots, LaunchPlan* pl, int min_sli
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int cm = 1;
-    if (C::kPair || (C::kBMode == B_MNMAJOR && a.m_tiles >= 2)) cm = 2;
+    const int cm = C::kPair ? 2 : 1;
     int clusters = P;
-    while (cm > 1) {
-        attr[0].val.clusterDim.x = (unsigned)cm;
-        cfg.gridDim = dim3((unsigned)((P / cm) * cm), 1, 1);
+    if (C::kPair) {
+        attr[0].val.clusterDim.x = 2u;
+        cfg.gridDim = dim3((unsigned)((P / 2) * 2), 1, 1);
         int nc = 0;
-        if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess) nc = 0;
-        if (C::kPair && nc <= 0) return false;  // a pair kernel runs only as 2-CTA clusters
-        if (nc > 0 && (cm < 4 || nc * 4 >= (P * 9) / 10)) {
-            clusters = nc;
-            break;
-        }
-        cm /= 2;
+        if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess || nc <= 0)
+            return false;  // a pair kernel runs only as 2-CTA clusters
+        clusters = nc;
     }
-    if (cm == 1) clusters = P;
     const int64_t per_split = (int64_t)a.n_tiles * ((a.m_tiles + cm - 1) / cm);
     const int splits = plan_splits(per_split, a.m_tiles, a.n_tiles, a.k_blocks, clusters, min_slice, max_slots,
                                    split_below);

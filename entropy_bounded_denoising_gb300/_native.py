@@ -84,6 +84,7 @@ def load(path: str | None = None):
         "dg_philox_words": (st, [u64, u32, u32, u32, u32, u32, i64, P, P]),
         "dg_get_device_status": (st, [P, ctypes.POINTER(u32)]),
         "dg_clear_device_status": (st, [P]),
+        "dg_probe_bounded_wait": (st, [u32, P, P]),
         "dg_status_string": (ctypes.c_char_p, [st]),
         "dg_version": (i32, []),
         "dg_launch_count": (u64, []),
@@ -108,6 +109,7 @@ def exported_symbols() -> list[str]:
                         "dg_gemm_bf16_noalloc", "dg_choice_probs", "dg_embed_canvas", "dg_commit", "dg_attention",
                         "dg_attention_workspace_bytes",
                         "dg_philox_words", "dg_get_device_status", "dg_clear_device_status",
+                        "dg_probe_bounded_wait",
                         "dg_status_string", "dg_version", "dg_launch_count") if hasattr(lib, n)]
 
 
@@ -498,3 +500,10 @@ def dg_get_device_status(stream=None) -> int:
 
 def dg_clear_device_status(stream=None) -> None:
     _check("dg_clear_device_status", load().dg_clear_device_status(_s(stream)))
+
+
+def dg_probe_bounded_wait(polls, result, stream=None, check=True) -> int:
+    rc = load().dg_probe_bounded_wait(int(polls), _p(result), _s(stream))
+    if check:
+        _check("dg_probe_bounded_wait", rc)
+    return rc

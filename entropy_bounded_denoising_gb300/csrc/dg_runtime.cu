@@ -92,7 +92,47 @@ bool encode_tmap(void* tmap, int dtype_code, int rank, void* base, const uint64_
 
 }  // namespace dghost
 
+namespace {
+// The bounded waits of the kernels, run on shared-memory barriers of one warp: `never` gets
+// no arrival (its waits must expire and raise DG_DEV_TIMEOUT, as in a kernel), `done` gets
+// its one arrival before the wait (which must then succeed).
+__global__ void k_probe_bounded_wait(unsigned* status, uint32_t polls, uint32_t* result) {
+    __shared__ __align__(8) uint64_t never, done;
+    if (threadIdx.x == 0) {
+        dg::mbar_init(&never, 1);
+        dg::mbar_init(&done, 1);
+        dg::fence_mbar_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0) dg::mbar_arrive(&done);
+    __syncwarp();
+    uint32_t single = 1;
+    if (threadIdx.x == 0) {
+        single = dg::mbar_wait(&never, 0, polls) ? 1u : 0u;
+        if (!single) dg::raise_status(status, DG_DEV_TIMEOUT);
+    }
+    const bool warp_ok = dg::mbar_wait_warp(&never, 0, 0, polls);
+    const bool done_ok = dg::mbar_wait_warp(&done, 0, 0, polls);
+    if (threadIdx.x == 0) {
+        if (!warp_ok) dg::raise_status(status, DG_DEV_TIMEOUT);
+        result[0] = single;
+        result[1] = warp_ok ? 1u : 0u;
+        result[2] = done_ok ? 1u : 0u;
+    }
+}
+}  // namespace
+
 extern "C" {
+
+dg_status dg_probe_bounded_wait(uint32_t polls, uint32_t* result, dg_stream_t stream) {
+    if (polls < 1 || polls > 65536 || !result) return DG_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(result) & 3u) return DG_ERR_ALIGNMENT;
+    unsigned* st = dghost::status_word();
+    if (!st) return DG_ERR_CUDA;
+    k_probe_bounded_wait<<<1, 32, 0, (cudaStream_t)stream>>>(st, polls, result);
+    dghost::count_launch();
+    return dghost::cuda_status(cudaGetLastError());
+}
 
 dg_status dg_get_device_status(dg_stream_t stream, uint32_t* status) {
     if (!status) return DG_ERR_INVALID_ARG;

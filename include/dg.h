@@ -474,6 +474,20 @@ DG_API dg_status dg_get_device_status(dg_stream_t stream, uint32_t* status);
 /* Synchronises `stream` and clears the status word of the current device. */
 DG_API dg_status dg_clear_device_status(dg_stream_t stream);
 
+/* Diagnostic hook (the method's pages have no counterpart; this checks the library's own
+ * failure handling).  Runs the bounded mbarrier waits that every kernel of the library uses
+ * (one thread polling, and a whole warp with one lane polling) on a shared-memory barrier
+ * that never receives an arrival, with a limit of `polls` polls (1..65536, each at most
+ * about a microsecond) instead of the kernels' 2^22, in one warp of one CTA on `stream`.
+ * The expired waits return and raise DG_DEV_TIMEOUT in the status word, exactly as an
+ * expired wait inside a kernel does; no copy or MMA is in flight, so nothing else unwinds.
+ *   result (device, out) uint32 [3], 4-byte aligned: [0] the single-thread wait (0 =
+ *   expired), [1] the whole-warp wait (0 = expired), [2] a wait on a barrier that did
+ *   receive its arrival (1 = completed).
+ * Returns DG_ERR_INVALID_ARG for polls outside 1..65536 or a null result (nothing
+ * launched). */
+DG_API dg_status dg_probe_bounded_wait(uint32_t polls, uint32_t* result, dg_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 DG_API const char* dg_status_string(dg_status status);
 

@@ -4,15 +4,18 @@
   oracle each running their own loop from the same initial state (the canvas is renoised
   from the same counters on both sides; logits are precomputed per step), every step
   compared; self-conditioning compared on every row (tiny) or sampled rows (single).
-* batched (8x256, V=262144, d=4096, h=16384): one step plus self-conditioning; two whole
-  canvases and sampled feedback rows against the oracle.
+* batched (8x256, V=262144, d=4096, h=16384): one step plus self-conditioning; every
+  canvas against the oracle, and 32 feedback rows: two in each of the 16 row tiles of 128,
+  so both CTAs of every CTA pair and every k-slice's partial tile are covered.
 * sweep (64x256, V=262144): the full loop until every canvas converges or hits the step
   cap, in the launch configuration the benchmark uses; two canvases followed by the oracle
-  over every step, feedback rows sampled at the first self-conditioned step.
+  over every step, feedback rows at the first two steps and the last.
 * ragged (32x256, V=152064, d=3584, h=18944): one step with converged (masked), read-only
-  and normal canvases at mixed temperatures; sampled canvases of every role.
-Decision outputs are bit-exact except counted boundary positions (1e-6 relative);
-entropies within 1e-5 relative; feedback rows within 2e-2 relative (bf16 tensor cores)."""
+  and normal canvases at mixed temperatures; every canvas against the oracle, two feedback
+  rows per canvas with feedback.
+Decision outputs are bit-exact except positions on a decision boundary (1e-6 relative);
+entropies within 1e-5 relative; feedback rows within 2e-2 relative per row and per component
+(helpers.delta_elem_excess: bf16 tensor cores, fp32 accumulation)."""
 import numpy as np
 import pytest
 import torch
@@ -21,7 +24,7 @@ import entropy_bounded_denoising_gb300 as dg
 from entropy_bounded_denoising_gb300 import synth
 import oracle
 
-from helpers import DELTA_RTOL, StepBuffers, compare_step, delta_rel_err, run_step
+from helpers import StepBuffers, check_delta, compare_step, run_step
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -96,8 +99,7 @@ def _loop(wl, sc_from_step, check_rows_per_step):
                     assert (dh[c] == 0).all()
                     continue
                 ref = oracle.self_cond_rows(hx[c][rows], np.full(len(rows), float(p["temperature"][c])), *bits, V=V)
-                err = delta_rel_err(dh[c][rows], ref)
-                assert err.max() <= DELTA_RTOL, (t, c, err.max())
+                check_delta(dh[c][rows], ref, (t, c))
         active &= ~o["converged"].astype(bool)
         steps += 1
         print(f"step {t}: {rep}")
@@ -116,7 +118,7 @@ def test_single_full_loop():
     assert 1 <= steps <= wl.steps
 
 
-def _one_step(wl, check_canvases, sc_rows, params):
+def _one_step(wl, sc_rows, params):
     n, L, V = wl.n, wl.L, wl.V
     x = synth.logits(n, L, V, seed=wl.seed, step=1, scale=wl.scale, spike_frac=wl.spike_frac, device=DEV)
     wts, bits = _weights(wl, DEV)
@@ -131,19 +133,29 @@ def _one_step(wl, check_canvases, sc_rows, params):
     assert dg.dg_get_device_status() == 0
     g = b.host()
     dh = delta.float().cpu().numpy()
-    for c in check_canvases:
-        hx = synth.host_logits(x[c:c + 1])
-        pc = _subset(params, [c])
-        o = oracle.denoise_step(hx, pc, SEED, canvas0[c:c + 1], np.full((1, L), -1, np.int32), np.zeros(1, np.int32))
-        gc = {k: v[c:c + 1] for k, v in g.items()}
-        rep = compare_step(gc, o, pc, V, SEED, canvas0[c:c + 1], np.full((1, L), -1, np.int32), np.zeros(1, np.int32))
-        print(f"canvas {c} (flags {params['flags'][c]}): {rep}")
-    for (c, i) in sc_rows:
-        hx = synth.host_logits(x[c, i:i + 1])
-        ref = oracle.self_cond_rows(hx, np.array([float(params["temperature"][c])]), *bits, V=V)
-        err = delta_rel_err(dh[c, i:i + 1], ref)
-        assert err.max() <= DELTA_RTOL, (c, i, err.max())
+    # every canvas against the oracle in one call (its rows run in parallel on the host)
+    hx = synth.host_logits(x)
+    prev0, stable0 = np.full((n, L), -1, np.int32), np.zeros(n, np.int32)
+    o = oracle.denoise_step(hx, params, SEED, canvas0, prev0, stable0)
+    rep = compare_step(g, o, params, V, SEED, canvas0, prev0, stable0)
+    print(f"{n} canvases: {rep}")
+    if sc_rows:
+        cs = np.array([c for c, _ in sc_rows])
+        ii = np.array([i for _, i in sc_rows])
+        ref = oracle.self_cond_rows(hx[cs, ii], params["temperature"][cs].astype(np.float64), *bits, V=V)
+        check_delta(dh[cs, ii], ref, "feedback rows")
     return g, dh, canvas0
+
+
+def _rows_per_tile(canvases, L, per_tile, seed):
+    """`per_tile` positions in each 128-row tile of each canvas (the GEMMs' M tiles)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for c in canvases:
+        for t0 in range(0, L, 128):
+            for i in rng.choice(np.arange(t0, min(L, t0 + 128)), per_tile, replace=False):
+                out.append((int(c), int(i)))
+    return out
 
 
 @pytest.mark.parametrize("sample_all", [False, True])
@@ -152,7 +164,8 @@ def test_batched_full_size(sample_all):
     p = synth.canvas_params(wl, step=1)
     if sample_all:
         p["flags"] |= dg.DG_SAMPLE_ALL
-    g, dh, _ = _one_step(wl, check_canvases=[0, 5], sc_rows=[(0, 3), (5, 200), (7, 255)], params=p)
+    rows = _rows_per_tile(range(wl.n), wl.L, 2, seed=11) + [(0, 0), (7, 255)]
+    g, dh, _ = _one_step(wl, sc_rows=rows, params=p)
     assert (g["converged"] == 0).all() and np.isfinite(dh).all()
     drawn = g["sample"] >= 0
     assert drawn.all() if sample_all else np.array_equal(drawn, g["accept"] == 1)
@@ -165,8 +178,8 @@ def test_ragged_full_size():
     conv = [c for c in range(wl.n) if flags[c] == 0]
     ro = [c for c in range(wl.n) if flags[c] & dg.DG_READ_ONLY]
     normal = [c for c in range(wl.n) if (flags[c] & dg.DG_SELF_COND)]
-    g, dh, canvas0 = _one_step(wl, check_canvases=[normal[0], normal[-1], ro[0]],
-                               sc_rows=[(normal[0], 0), (normal[-1], 129)], params=p)
+    rows = _rows_per_tile(normal, wl.L, 1, seed=12)   # two per canvas, one in each row tile
+    g, dh, canvas0 = _one_step(wl, sc_rows=rows, params=p)
     for c in conv:   # masked canvases: never read, nothing written, no feedback
         assert (g["canvas"][c] == canvas0[c]).all() and (g["argmax"][c] == -7).all()
         assert (dh[c] == 0).all()
@@ -213,11 +226,15 @@ def test_sweep_full_loop():
             o = oracle.denoise_step(hx, pf, SEED, o_canvas, o_prev, o_stable)
             rep = compare_step(g, o, pf, V, SEED, g_in["canvas"], g_in["prev"], g_in["stable"], g_in=g_in)
             print(f"step {t}: {rep}")
-            if t == 0:
+            if t in (0, 1, wl.steps - 1):
                 dh = delta.float().cpu().numpy()
                 for j, c in enumerate(follow):
-                    ref = oracle.self_cond_rows(hx[j, [17]], np.array([float(pf["temperature"][j])]), *bits, V=V)
-                    assert delta_rel_err(dh[c, [17]], ref).max() <= DELTA_RTOL
+                    if o["converged"][j]:
+                        assert (dh[c] == 0).all()
+                        continue
+                    rr = [17, 128 + (t * 37) % 128]   # one row in each of the canvas's two row tiles
+                    ref = oracle.self_cond_rows(hx[j, rr], np.full(2, float(pf["temperature"][j])), *bits, V=V)
+                    check_delta(dh[c, rr], ref, (t, c))
             o_canvas, o_prev, o_stable = o["canvas"], o["prev_argmax"], o["stable_count"]
             o_active &= ~o["converged"].astype(bool)
         dg.dg_advance_params(pt, b.converged, n)

@@ -418,13 +418,24 @@ def test_read_only_and_inactive():
     assert out["entropy"][1].sum() == 0 and out["converged"][1] == 0
 
 
-def test_canvas_init_tokens():
+def _check_canvas_init(canvas_init, random_token):
+    """The Prefill case's canvas: uniform tokens of the init stream (2), position by position,
+    for active canvases only -- not the renoise stream's tokens."""
     n, L, V = 2, 300, 7
-    p = _params(n, step=[0, 0])
+    p = _params(n, step=[0, 3])
     p["flags"] = np.array([oracle.ACTIVE, 0], np.uint32)
-    c = oracle.canvas_init(n, L, V, p, seed=77)
+    c = canvas_init(n, L, V, p, 77)
     assert c[0].min() >= 0 and c[0].max() < V and (c[1] == 0).all()
     assert scipy.stats.chisquare(np.bincount(c[0], minlength=V)).pvalue > 1e-4
+    req, step = int(p["request_id"][0]), int(p["step"][0])
+    init = [random_token(77, req, step, i, oracle.STREAM_INIT, V) for i in range(L)]
+    renoise = [random_token(77, req, step, i, oracle.STREAM_RENOISE, V) for i in range(L)]
+    assert np.sum(np.array(init) != np.array(renoise)) > L // 2   # the streams differ
+    assert list(c[0]) == init
+
+
+def test_canvas_init_tokens():
+    _check_canvas_init(lambda n, L, V, p, seed: oracle.canvas_init(n, L, V, p, seed), oracle.random_token)
 
 
 # ----------------------------------------------------------------------------- self-conditioning
@@ -457,14 +468,73 @@ def test_pe_one_hot_uniform_linear():
     np.testing.assert_allclose(pe[2], P[2] @ Ef, rtol=1e-12, atol=1e-18)   # library matmul
 
 
+def _check_gelu(gelu):
+    """GELU in its tanh form (Hendrycks & Gimpel) against the exact GELU x * Phi(x):
+    * the tanh form is built to agree with x Phi(x) to second order at 0, so
+      (gelu(x) - x / 2) / x^2 -> 1 / sqrt(2 pi) (this fixes the tanh argument's scale);
+    * with the published cubic coefficient its largest distance from x Phi(x) is 4.73e-4
+      (over all x); the pin allows 4.8e-4 (a cubic coefficient of 0.04 or 0.05 gives
+      2.9e-3 / 3.0e-3, a scale of 0.8 gives 6.4e-4);
+    * gelu(x) - gelu(-x) = x, gelu(0) = 0, and the tails tend to x and 0."""
+    assert gelu(0.0) == 0.0
+    xs = np.linspace(-8.0, 8.0, 16001)
+    exact = 0.5 * xs * (1.0 + scipy.special.erf(xs / math.sqrt(2.0)))   # x * Phi(x)
+    got = np.array([gelu(float(x)) for x in xs])
+    assert np.abs(got - exact).max() < 4.8e-4
+    for x in (1e-4, -1e-4, 3e-5):
+        assert abs((gelu(x) - 0.5 * x) / (x * x) - 1.0 / math.sqrt(2.0 * math.pi)) < 1e-6
+    for x in (0.3, 1.7, 4.0):
+        assert abs(gelu(x) - gelu(-x) - x) < 1e-15 * max(1.0, x)
+    assert gelu(30.0) == pytest.approx(30.0)
+    assert abs(gelu(-30.0)) < 1e-12
+
+
 def test_gelu_tanh_properties():
-    assert oracle.gelu_tanh(0.0) == 0.0
-    for x in np.linspace(-6, 6, 121):
-        exact = 0.5 * x * (1.0 + scipy.special.erf(x / math.sqrt(2.0)))   # x * Phi(x)
-        assert abs(oracle.gelu_tanh(float(x)) - exact) < 1e-3
-    assert oracle.gelu_tanh(30.0) == pytest.approx(30.0)
-    assert abs(oracle.gelu_tanh(-30.0)) < 1e-12
-    assert oracle.gelu_tanh(1.0) > 0.8 and oracle.gelu_tanh(-1.0) < 0
+    _check_gelu(oracle.gelu_tanh)
+
+
+def _mutant_oracle(tmp_path, old, new):
+    """A copy of the oracle compiled with one planted mistake (the text `old` of its C
+    source replaced by `new`), loaded on its own: the product oracle is never touched."""
+    import ctypes
+    import subprocess
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "dg_oracle.c")).read()
+    assert src.count(old) == 1, old
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-fPIC", "-shared", "-std=gnu11", "-o", str(so), str(path), "-lm"], check=True)
+    lib = ctypes.CDLL(str(so))
+    lib.orc_gelu_tanh.argtypes = [ctypes.c_double]
+    lib.orc_gelu_tanh.restype = ctypes.c_double
+    lib.orc_random_token.argtypes = [ctypes.c_uint64] + [ctypes.c_uint32] * 5
+    lib.orc_random_token.restype = ctypes.c_uint32
+    P = ctypes.c_void_p
+    lib.orc_canvas_init.argtypes = [P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64, P, P, P, ctypes.c_uint64]
+
+    def canvas_init(n, L, V, p, seed):
+        out = np.zeros((n, L), np.int32)
+        st = np.ascontiguousarray(p["step"], np.int32)
+        rq = np.ascontiguousarray(p["request_id"], np.uint32)
+        fl = np.ascontiguousarray(p["flags"], np.uint32)
+        lib.orc_canvas_init(out.ctypes.data, n, L, V, st.ctypes.data, rq.ctypes.data, fl.ctypes.data, seed)
+        return out
+    return lib, canvas_init
+
+
+@pytest.mark.parametrize("old,new", [("const double k = sqrt(2.0 / M_PI);", "const double k = 0.8;"),
+                                     ("0.044715 * z * z * z", "0.04 * z * z * z")])
+def test_planted_gelu_mistakes_fail_the_pin(tmp_path, old, new):
+    lib, _ = _mutant_oracle(tmp_path, old, new)
+    with pytest.raises(AssertionError):
+        _check_gelu(lib.orc_gelu_tanh)
+
+
+def test_planted_canvas_init_stream_fails_the_pin(tmp_path):
+    lib, canvas_init = _mutant_oracle(tmp_path, "(uint32_t)i, ORC_STREAM_INIT, (uint32_t)V);",
+                                      "(uint32_t)i, ORC_STREAM_RENOISE, (uint32_t)V);")
+    with pytest.raises(AssertionError):
+        _check_canvas_init(canvas_init, oracle.random_token)
 
 
 def test_gated_mlp_closed_forms():

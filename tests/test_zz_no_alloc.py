@@ -3,10 +3,13 @@
 implicit synchronisation are not allowed).  Its split-K partial tiles live in a fixed
 8 MiB array inside the library instead of a caller workspace.
 
-Checked through the C ABI against dg_gemm_bf16 (which takes a workspace) on two calls in
-a row with different inputs, so a stale partial tile left by the first call would show in
-the second; plus the host-side rejection of problems that need more scratch than the array
-holds.  This file runs last so that a stop-at-first-failure run has done every other test."""
+Checked through the C ABI on two calls in a row with different inputs: bit for bit
+against dg_gemm_bf16 (which takes a workspace and plans the same k-slices, so it adds the
+same partial tiles in the same order), so a stale partial tile left by the first call would
+show in the second; and against an fp32 torch matmul of the same bf16 inputs within the
+GEMM engine tests' tolerance.  Plus the host-side rejection of problems that need more
+scratch than the array holds.  This file runs last so that a stop-at-first-failure run has
+done every other test."""
 import numpy as np
 import pytest
 import torch
@@ -39,7 +42,9 @@ def test_noalloc_matches_workspace_gemm_twice(M, N, K, mn_major):
         torch.cuda.synchronize()
         assert dg.dg_get_device_status() == 0
         assert torch.isfinite(got).all(), call
-        err = (got - ref).abs().max().item() / ref.abs().max().item()
+        assert torch.equal(got, ref), (call, (got - ref).abs().max().item())
+        exact = A.float() @ (B.float() if mn_major else B.float().T)
+        err = (got - exact).abs().max().item() / exact.abs().max().item()
         assert err <= REL_TOL, (call, err)
 
 

@@ -40,3 +40,16 @@ def test_step_arithmetic_from_logits_and_from_hidden():
     assert b["tc_flops"] == a["tc_flops"] + 2.0 * N * wl.V * wl.d      # the LM head
     # from hidden states the step reads the hidden rows instead of the logits
     assert a["bytes"] - b["bytes"] == 2 * N * wl.V - 2 * N * wl.d
+
+
+def test_peak_follows_the_timed_window():
+    pk = {"bf16_tflops": 1891.2, "bf16_tflops_sustained": 1692.7, "hbm_gbs": 6788.6}
+    # a 67 ms window at full clock (the round-end bench line): the burst figure
+    assert bench.choose_tc_peak(pk, 0.067, 2070.0, 2070.0) == (1891.2, "burst")
+    # a short window is a burst whatever the sampled clock
+    assert bench.choose_tc_peak(pk, 0.5, 1600.0, 2070.0) == (1891.2, "burst")
+    # seconds under the power cap: the sustained figure
+    assert bench.choose_tc_peak(pk, 1.1, 1680.0, 2070.0) == (1692.7, "sustained")
+    # seconds at full clock (within 3 %): still the burst figure
+    assert bench.choose_tc_peak(pk, 3.0, 2020.0, 2070.0) == (1891.2, "burst")
+    assert bench.choose_tc_peak(pk, 3.0, None, None) == (1692.7, "sustained")

@@ -184,6 +184,40 @@ def test_batch_composition_does_not_change_rows():
         assert np.array_equal(outs[0][k][2], s[k][0]), k
 
 
+@pytest.mark.parametrize("sample_all", [False, True])
+@pytest.mark.parametrize("pieces", [1, 2, 3, 4, 5, 8, 9])
+def test_step_rows_split_over_clusters(pieces, sample_all):
+    """Rows of 2-3 16 KB pieces are streamed by 2 CTAs of a cluster, rows of 4-8 by 4, and the
+    parts merged in rank order; 1 and 9 pieces stay on one CTA.  V = 8192 k - 3 puts a ragged
+    end in the last CTA's last piece; spiked rows put the maximum in any CTA's part.  Against
+    the oracle, and with NaN / +inf logits in the last part and an all -inf row (status bits
+    from whichever CTA saw them)."""
+    rng = np.random.default_rng(pieces * 10 + sample_all)
+    V = 8192 * pieces - 3
+    ld = V + 3  # rows 16-byte aligned
+    n, L = 3, 96
+    x = synth.logits(n, L, V, seed=pieces, step=1, scale=(0.5, 12.0), spike_frac=0.3, ld=ld)
+    p = _params(n, rng)
+    if sample_all:
+        p["flags"] |= dg.DG_SAMPLE_ALL
+    _check_case(x, p, 0x5EED + pieces, V, canvas0=rng.integers(0, V, (n, L)).astype(np.int32))
+    # flagged rows: a NaN near the row's end, +inf near its start, a row of -inf
+    y = synth.logits(1, 4, V, seed=pieces + 1, step=0, scale=(1.0, 2.0), ld=ld).float()
+    y[0, 1, V - 2] = float("nan")
+    y[0, 2, 3] = float("inf")
+    y[0, 3, :] = float("-inf")
+    q = _params(1, rng, temperature=1.0, flags=dg.DG_ACTIVE | dg.DG_SAMPLE_ALL)
+    b = StepBuffers.make(1, 4, DEV)
+    dg.dg_clear_device_status()
+    run_step(y.to(torch.bfloat16).to(DEV), dg.params_tensor(q, DEV), 3, b, V=V)
+    st = dg.dg_get_device_status()
+    assert st & dg.DG_DEV_NAN_INF_ROW and st & dg.DG_DEV_EMPTY_ROW and not st & dg.DG_DEV_TIMEOUT
+    dg.dg_clear_device_status()
+    o = oracle.row_stats(synth.host_logits(y.to(torch.bfloat16))[0, 0, :V], T=1.0, seed=3,
+                         request_id=int(q["request_id"][0]), step=int(q["step"][0]), position=0)
+    assert int(b.argmax[0, 0]) == o["argmax"] and int(b.sample[0, 0]) == o["sample"]
+
+
 @pytest.mark.parametrize("deferred", [False, True])
 def test_nan_and_empty_rows_set_status(deferred):
     """NaN, +inf and all -inf rows raise their status bits and leave the valid rows alone.

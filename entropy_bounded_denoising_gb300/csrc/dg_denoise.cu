@@ -36,11 +36,7 @@
 #include <algorithm>
 #include <type_traits>
 
-#include <cooperative_groups.h>
-
 #include "dg_common.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace {
 
@@ -107,11 +103,6 @@ struct K1Shared {
     // a queued group outlives the ring slot it came from
     int q_e0[kK1Warps][kQueue];
     uint32_t q_x[kK1Warps][kQueue][kQW];
-    // a row split over a cluster: this CTA's part, read by the cluster's first CTA
-    RowState part_state;
-    float part_best;
-    int part_bidx;
-    int part_flags;  // 1: a NaN / inf logit, 2: a bounded wait expired
 };
 
 DG_DEVINL float ex2(float x) {
@@ -365,10 +356,7 @@ DG_DEVINL void draw_queued(const int* q_e0, const uint32_t (*q_x)[QW], int qh, i
 }
 
 // ------------------------------------------------------------------------------------
-// K1: per-position statistics and Gumbel-max sample.  grid (L * split, n): a row is streamed by
-// a cluster of `split` CTAs (1, 2 or 4, fixed by V alone, so that a row's reduction order
-// never depends on its batch), each over a contiguous range of the row's 16 KB pieces; the
-// cluster's first CTA merges the parts through distributed shared memory in rank order.
+// K1: per-position statistics and Gumbel-max sample.  grid (L, n), one CTA per position.
 // Each consumer warp takes kVecPerLane 16-byte vectors per lane of every piece, in two
 // passes over shared memory: (1) vector maxima, candidate groups into the warp's queue;
 // (2) the exponential sums against the warp's running max, which only grows between
@@ -392,15 +380,13 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
     Shared& sh = *reinterpret_cast<Shared*>(k1_smem);
     unsigned char* ring = k1_smem + ((sizeof(Shared) + 127) / 128) * 128;
 
-    const int split = (int)(gridDim.x / (unsigned)L);  // CTAs per row (the cluster size)
-    const int pos = (int)blockIdx.x / split;
-    const int part = (int)blockIdx.x % split;           // this CTA's rank in the row's cluster
+    const int pos = blockIdx.x;
     const int64_t canvas = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     dg::pdl_wait();
     dg::pdl_release();
-    if (ws.count && blockIdx.x == 0 && canvas == 0 && tid == 0) *ws.count = 0;
+    if (ws.count && pos == 0 && canvas == 0 && tid == 0) *ws.count = 0;
     const dg_canvas_params p = params[canvas];
     if (!(p.flags & DG_ACTIVE)) return;
     if (!(p.temperature > 0.f) || !isfinite(p.temperature)) {
@@ -415,7 +401,6 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
     const uint32_t bytes = (uint32_t)(V * ES);
     const uint32_t bulk = bytes & ~15u;
     const int npieces = (int)((bytes + kPieceBytes - 1) / kPieceBytes);
-    const int q_lo = part * npieces / split, q_hi = (part + 1) * npieces / split;  // this CTA's pieces
 
     if (tid == 0) {
         for (int i = 0; i < kSlots; ++i) {
@@ -432,10 +417,9 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
     if (warp == kK1Warps) {
         // ---------------- producer: keep the ring full
         if (lane == 0) {
-            for (int q = q_lo; q < q_hi; ++q) {
-                const int qi = q - q_lo;
-                const int sl = qi % kSlots;
-                if (qi >= kSlots && !dg::mbar_wait(&sh.empty[sl], (uint32_t)((qi / kSlots) - 1) & 1u)) {
+            for (int q = 0; q < npieces; ++q) {
+                const int sl = q % kSlots;
+                if (q >= kSlots && !dg::mbar_wait(&sh.empty[sl], (uint32_t)((q / kSlots) - 1) & 1u)) {
                     sh.timeout = 1;
                     break;
                 }
@@ -466,10 +450,9 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
         uint32_t(*q_x)[QW] = sh.q_x[warp];
         int qh = 0, qn = 0;  // warp-uniform queue head and length, kept across pieces
         const unsigned lt = (1u << lane) - 1u;
-        for (int q = q_lo; q < q_hi; ++q) {
-            const int qi = q - q_lo;
-            const int sl = qi % kSlots;
-            if (!__all_sync(0xffffffffu, dg::mbar_wait(&sh.full[sl], (uint32_t)(qi / kSlots) & 1u))) {
+        for (int q = 0; q < npieces; ++q) {
+            const int sl = q % kSlots;
+            if (!__all_sync(0xffffffffu, dg::mbar_wait(&sh.full[sl], (uint32_t)(q / kSlots) & 1u))) {
                 sh.timeout = 1;
                 break;
             }
@@ -662,9 +645,8 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
         }
     }
     __syncthreads();
-    // the CTA's state: the warps' states merged in warp order, its sample candidate the best of
-    // the warps' own winners
     if (warp == 0) {
+        // the sample: the best of the warps' own winners
         float b = -INFINITY;
         int bi = 0x7fffffff;
         if (lane < kK1Warps) {
@@ -675,50 +657,21 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
         if (lane == 0) {
             RowState rs = sh.warp_state[0];
             for (int w = 1; w < kK1Warps; ++w) rs = merge(rs, sh.warp_state[w], k2);
-            sh.part_state = rs;
-            sh.part_best = b;
-            sh.part_bidx = bi;
-            sh.part_flags = (sh.bad ? 1 : 0) | (sh.timeout ? 2 : 0);
+            const bool empty = rs.m == -INFINITY;
+            const bool row_bad = sh.bad || rs.m == INFINITY || !isfinite(rs.r) || !isfinite(rs.t);
+            // H = log(c + r) - t ln2 / (c + r), with log1p where a single entry holds the max
+            const float s = rs.c + rs.r;
+            const float lns = (rs.c == 1.f) ? log1pf(rs.r) : logf(rs.c) + log1pf(rs.r / rs.c);
+            const float H = lns - rs.t * kLn2 / s;
+            entropy_out[row] = H;
+            lse_out[row] = rs.m * invT + lns;
+            argmax_out[row] = empty ? 0 : rs.idx;
+            sample_out[row] = (do_sample && !empty && !row_bad) ? bi : -1;
+            if (ws.row_max) ws.row_max[row] = (empty || row_bad) ? __int_as_float(0x7fc00000) : rs.m;
+            if (row_bad) dg::raise_status(status, DG_DEV_NAN_INF_ROW);
+            if (empty) dg::raise_status(status, DG_DEV_EMPTY_ROW);
+            if (sh.timeout) dg::raise_status(status, DG_DEV_TIMEOUT);
         }
-    }
-    if (split > 1) {
-        // every part is in shared memory before the first CTA reads them; no CTA leaves
-        // before it has
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();
-        if (part == 0 && tid == 0) {
-            for (int r = 1; r < split; ++r) {
-                const Shared* other = cluster.map_shared_rank(&sh, r);
-                sh.part_state = merge(sh.part_state, other->part_state, k2);
-                if (better(other->part_best, other->part_bidx, sh.part_best, sh.part_bidx)) {
-                    sh.part_best = other->part_best;
-                    sh.part_bidx = other->part_bidx;
-                }
-                sh.part_flags |= other->part_flags;
-            }
-        }
-        cluster.sync();
-        if (part != 0) return;
-    } else {
-        __syncthreads();
-    }
-    if (tid == 0) {
-        const RowState rs = sh.part_state;
-        const int bi = sh.part_bidx;
-        const bool empty = rs.m == -INFINITY;
-        const bool row_bad = (sh.part_flags & 1) || rs.m == INFINITY || !isfinite(rs.r) || !isfinite(rs.t);
-        // H = log(c + r) - t ln2 / (c + r), with log1p where a single entry holds the max
-        const float s = rs.c + rs.r;
-        const float lns = (rs.c == 1.f) ? log1pf(rs.r) : logf(rs.c) + log1pf(rs.r / rs.c);
-        const float H = lns - rs.t * kLn2 / s;
-        entropy_out[row] = H;
-        lse_out[row] = rs.m * invT + lns;
-        argmax_out[row] = empty ? 0 : rs.idx;
-        sample_out[row] = (do_sample && !empty && !row_bad) ? bi : -1;
-        if (ws.row_max) ws.row_max[row] = (empty || row_bad) ? __int_as_float(0x7fc00000) : rs.m;
-        if (row_bad) dg::raise_status(status, DG_DEV_NAN_INF_ROW);
-        if (empty) dg::raise_status(status, DG_DEV_EMPTY_ROW);
-        if (sh.part_flags & 2) dg::raise_status(status, DG_DEV_TIMEOUT);
     }
 }
 
@@ -1104,21 +1057,6 @@ template <int DT>
 size_t k1_smem_bytes() { return ((sizeof(K1Shared<DT>) + 127) / 128) * 128 + (size_t)kSlots * kPieceBytes; }
 
 // Statistics of every active row (+ samples of DG_SAMPLE_ALL canvases); clears the list.
-// CTAs per row of K1, from the row's length alone (so that a row's reduction order, and with
-// it every result, is the same in any batch): rows of 2-3 pieces go to 2 CTAs, rows of 4-8
-// pieces (64-128 KB of bf16 logits) to 4, longer rows to one CTA, which keeps them streaming
-// long enough to hide the ring's fill and the merge.
-#ifndef DG_K1_SPLIT_MAX
-#define DG_K1_SPLIT_MAX 4
-#endif
-int k1_split(int64_t V, int es) {
-    const int64_t np = (V * es + kPieceBytes - 1) / kPieceBytes;
-    int s = 1;
-    if (np >= 4 && np <= 8) s = 4;
-    else if (np >= 2 && np <= 3) s = 2;
-    return s < DG_K1_SPLIT_MAX ? s : DG_K1_SPLIT_MAX;
-}
-
 template <int DT>
 dg_status launch_k1(const void* logits, int64_t ld, int64_t n, int32_t L, int64_t V,
                     const dg_canvas_params* params, uint64_t seed, int32_t* argmax, int32_t* sample, float* entropy,
@@ -1128,23 +1066,9 @@ dg_status launch_k1(const void* logits, int64_t ld, int64_t n, int32_t L, int64_
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DG_ERR_CUDA;
     const int64_t ld_bytes = ld * (DT == 0 ? 2 : 4);
-    const int split = k1_split(V, DT == 0 ? 2 : 4);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(L * split), (unsigned)n, 1);
-    cfg.blockDim = dim3(kK1Threads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;  // the CTAs of a row form a cluster
-    attr[0].val.clusterDim.x = (unsigned)split;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = dghost::kPdl ? 2 : 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<const unsigned char*>(logits), ld_bytes, V, L,
-                                             params, seed, argmax, sample, entropy, lse, ws, dghost::status_word());
+    const cudaError_t e = dghost::launch_pdl(kern, dim3((unsigned)L, (unsigned)n, 1), dim3(kK1Threads), smem, stream,
+                                             static_cast<const unsigned char*>(logits), ld_bytes, V, L, params, seed,
+                                             argmax, sample, entropy, lse, ws, dghost::status_word());
     dghost::count_launch();
     return dghost::cuda_status(e);
 }

@@ -186,12 +186,11 @@ def test_batch_composition_does_not_change_rows():
 
 @pytest.mark.parametrize("sample_all", [False, True])
 @pytest.mark.parametrize("pieces", [1, 2, 3, 4, 5, 8, 9])
-def test_step_rows_split_over_clusters(pieces, sample_all):
-    """Rows of 2-3 16 KB pieces are streamed by 2 CTAs of a cluster, rows of 4-8 by 4, and the
-    parts merged in rank order; 1 and 9 pieces stay on one CTA.  V = 8192 k - 3 puts a ragged
-    end in the last CTA's last piece; spiked rows put the maximum in any CTA's part.  Against
-    the oracle, and with NaN / +inf logits in the last part and an all -inf row (status bits
-    from whichever CTA saw them)."""
+def test_step_rows_of_many_pieces_with_ragged_ends(pieces, sample_all):
+    """Rows of 1-9 16 KB pieces streamed through one CTA's ring.  V = 8192 k - 3 puts a
+    ragged end in the last piece; spiked rows put the maximum in any piece.  Against the
+    oracle, and with NaN / +inf logits near the row's two ends and an all -inf row (their
+    status bits raised, the valid row's argmax and sample still the oracle's)."""
     rng = np.random.default_rng(pieces * 10 + sample_all)
     V = 8192 * pieces - 3
     ld = V + 3  # rows 16-byte aligned

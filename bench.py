@@ -566,6 +566,19 @@ def run_ours(args):
             "note": "timed alone, not part of the step; alg_bytes: embed = E rows gathered + feedback + "
                     "output; choice_probs = 4 slots x (token + probability + logit) + lse; commit = argmax + tokens",
         }
+        # Read-only canvases (single-pass reads): the step with the choice gather fused into
+        # its statistics pass, against the step followed by the separate gather.
+        p_ro = dict(p)
+        p_ro["flags"] = p["flags"] | dg.DG_READ_ONLY
+        params_ro = dg.params_tensor(p_ro, dev)
+        t_ro = _time(_denoise(params_ro), reps=20)
+        t_ro_fused = _time(lambda: dg.dg_denoise_step_choices(x, params_ro, seed, canvas, prev, stable, acc, am, smp,
+                                                              ent, lse, conv, choices, probs, workspace=dws,
+                                                              stream=stream), reps=20)
+        around["read_only_step_choices"] = {
+            "fused_ms": t_ro_fused, "unfused_ms": t_ro + around["choice_probs"]["ms"], "step_alone_ms": t_ro,
+            "note": f"every canvas DG_READ_ONLY with {C} choices per position: dg_denoise_step_choices against "
+                    "dg_denoise_step then dg_choice_probs"}
         # The LM head fused with the step's statistics (logits = hidden . E^T with the head tied
         # to the embedding table, stored once; entropy / lse / argmax from the GEMM's epilogue),
         # against the same work unfused: the LM head alone, then dg_denoise_step on its logits.

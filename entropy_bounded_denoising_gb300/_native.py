@@ -57,6 +57,8 @@ def load(path: str | None = None):
         "dg_denoise_step": (st, [P, ctypes.c_int, i64, i64, i32, i64, P, u64] + [P] * 11 + [P, sz, P]),
         "dg_denoise_stats": (st, [P, ctypes.c_int, i64, i64, i32, i64, P, u64] + [P] * 11 + [P, sz, P]),
         "dg_denoise_samples": (st, [P, ctypes.c_int, i64, i64, i32, i64, P, u64, P, P, P, sz, P]),
+        "dg_denoise_step_choices": (st, [P, ctypes.c_int, i64, i64, i32, i64, P, u64] + [P] * 11
+                                    + [P, i32, P] + [P, sz, P]),
         "dg_accept_from_entropy": (st, [P, P, P, i64, i32, i64, P, u64] + [P] * 7 + [P]),
         "dg_lm_head_workspace_bytes": (sz, [i64, i32, i64]),
         "dg_lm_head_logits": (st, [P, i64, P, i64, i64, i32, i64, i32, P, P, i64, P, sz, P]),
@@ -100,7 +102,7 @@ def load(path: str | None = None):
 def exported_symbols() -> list[str]:
     lib = load()
     return [n for n in ("dg_denoise_workspace_bytes", "dg_denoise_step", "dg_denoise_stats",
-                        "dg_denoise_samples", "dg_accept_from_entropy", "dg_lm_head_workspace_bytes",
+                        "dg_denoise_samples", "dg_denoise_step_choices", "dg_accept_from_entropy", "dg_lm_head_workspace_bytes",
                         "dg_lm_head_logits", "dg_lm_head_denoise_step",
                         "dg_canvas_init", "dg_advance_params", "dg_self_cond_workspace_bytes",
                         "dg_self_cond_logits", "dg_self_cond_prepare", "dg_self_cond_pe",
@@ -218,6 +220,25 @@ def dg_denoise_step(logits, params, seed, canvas, prev_argmax, stable_count, acc
     return _denoise_full("dg_denoise_step", logits, params, seed, canvas, prev_argmax, stable_count,
                          accept_mask, argmax, sample, entropy, lse, converged, mean_entropy, n_accept,
                          workspace, n_canvas, L, V, ld, stream, check)
+
+
+def dg_denoise_step_choices(logits, params, seed, canvas, prev_argmax, stable_count, accept_mask,
+                            argmax, sample, entropy, lse, converged, choices, probs, mean_entropy=None,
+                            n_accept=None, workspace=None, *, n_canvas=None, L=None, V=None, ld=None,
+                            stream=None, check=True) -> int:
+    """dg_denoise_step plus probs[c, i, k] = exp(logits[c, i, choices[c, i, k]] / T - lse[c, i])
+    gathered in the statistics pass; choices [n, L, C] int32, probs [n, L, C] float32."""
+    n_canvas, L, V, ld = _denoise_dims(logits, n_canvas, L, V, ld)
+    workspace, ws_bytes = _denoise_ws(workspace, logits, n_canvas, L, V)
+    C = choices.shape[-1]
+    rc = load().dg_denoise_step_choices(_p(logits), _dtype_code(logits), ld, n_canvas, L, V, _p(params),
+                                        int(seed) & 0xFFFFFFFFFFFFFFFF, _p(canvas), _p(prev_argmax),
+                                        _p(stable_count), _p(accept_mask), _p(argmax), _p(sample),
+                                        _p(entropy), _p(lse), _p(converged), _p(mean_entropy), _p(n_accept),
+                                        _p(choices), C, _p(probs), _p(workspace), ws_bytes, _s(stream))
+    if check:
+        _check("dg_denoise_step_choices", rc)
+    return rc
 
 
 def dg_denoise_stats(logits, params, seed, canvas, prev_argmax, stable_count, accept_mask, argmax,

@@ -88,6 +88,14 @@ struct DeferredWs {
     int32_t all_deferred;  // 1: every canvas is sampled by the deferred pass (DG_SAMPLE_ALL ignored)
 };
 
+// Optional single-pass-read output of the statistics pass: per active position, the
+// probabilities of C caller-given tokens under the position's own softmax(logits / T).
+struct ChoiceOut {
+    const int32_t* choices;  // [rows][C]; a token outside [0, V) gives probability 0
+    float* probs;            // [rows][C]; null: nothing gathered
+    int32_t C;
+};
+
 template <int DT>
 struct K1Shared {
     static constexpr int kQW = DT == 0 ? 2 : 4;  // words per queued group (4 bf16 or 4 fp32)
@@ -369,7 +377,7 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
     const unsigned char* __restrict__ logits, int64_t ld_bytes, int64_t V, int32_t L,
     const dg_canvas_params* __restrict__ params, uint64_t seed, int32_t* __restrict__ argmax_out,
     int32_t* __restrict__ sample_out, float* __restrict__ entropy_out, float* __restrict__ lse_out,
-    DeferredWs ws, unsigned* status) {
+    DeferredWs ws, ChoiceOut co, unsigned* status) {
     constexpr int VN = Vec<DT>::N;
     constexpr int ES = DT == 0 ? 2 : 4;
     constexpr int GPV = VN / 4;                    // Philox blocks per 16-byte vector
@@ -654,6 +662,7 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
             bi = sh.warp_bidx[lane];
         }
         warp_best(b, bi);
+        float lse = 0.f;
         if (lane == 0) {
             RowState rs = sh.warp_state[0];
             for (int w = 1; w < kK1Warps; ++w) rs = merge(rs, sh.warp_state[w], k2);
@@ -663,14 +672,32 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
             const float s = rs.c + rs.r;
             const float lns = (rs.c == 1.f) ? log1pf(rs.r) : logf(rs.c) + log1pf(rs.r / rs.c);
             const float H = lns - rs.t * kLn2 / s;
+            lse = rs.m * invT + lns;
             entropy_out[row] = H;
-            lse_out[row] = rs.m * invT + lns;
+            lse_out[row] = lse;
             argmax_out[row] = empty ? 0 : rs.idx;
             sample_out[row] = (do_sample && !empty && !row_bad) ? bi : -1;
             if (ws.row_max) ws.row_max[row] = (empty || row_bad) ? __int_as_float(0x7fc00000) : rs.m;
             if (row_bad) dg::raise_status(status, DG_DEV_NAN_INF_ROW);
             if (empty) dg::raise_status(status, DG_DEV_EMPTY_ROW);
             if (sh.timeout) dg::raise_status(status, DG_DEV_TIMEOUT);
+        }
+        if (co.probs) {
+            // choice probabilities from the lse just formed; the chosen logits come from the
+            // row that was streamed a moment ago (L2)
+            lse = __shfl_sync(0xffffffffu, lse, 0);
+            const int32_t* ch = co.choices + row * co.C;
+            float* pr = co.probs + row * co.C;
+            for (int k = lane; k < co.C; k += 32) {
+                const int32_t tok = ch[k];
+                float out = 0.f;
+                if (tok >= 0 && (int64_t)tok < V) {
+                    const float x = DT == 0 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(src)[tok] << 16)
+                                            : reinterpret_cast<const float*>(src)[tok];
+                    out = expf(x * invT - lse);
+                }
+                pr[k] = out;
+            }
         }
     }
 }
@@ -824,7 +851,7 @@ __global__ void __launch_bounds__(1024) k2_accept(
     int32_t* __restrict__ prev_argmax, int32_t* __restrict__ stable_count, uint8_t* __restrict__ accept_mask,
     uint8_t* __restrict__ converged, float* __restrict__ mean_entropy, int32_t* __restrict__ n_accept,
     DeferredWs ws, unsigned* status) {
-    __shared__ float sH[1024];
+    __shared__ __align__(16) float sH[1024];
     __shared__ double sSorted[1024];
     __shared__ double sWarp[32];
     __shared__ int sCut;
@@ -852,16 +879,25 @@ __global__ void __launch_bounds__(1024) k2_accept(
     const float H0 = valid ? entropy[q] : 0.f;
     const float H = (H0 == H0) ? H0 : INFINITY;
     const int32_t am = valid ? argmax[q] : 0;
+    const int L4 = (L + 3) & ~3;  // <= blockDim.x
+    // +inf pads the entropies to whole quads; a pad never ranks before a position (its index
+    // is larger and no entropy exceeds +inf)
     if (valid) sH[i] = H;
+    else if (i < L4) sH[i] = INFINITY;
     if (i == 0) sCut = L;
     __syncthreads();
 
-    // rank in (entropy, position) order
+    // rank in (entropy, position) order, four entropies per shared-memory read
     int rk = 0;
     if (valid) {
-        for (int j = 0; j < L; ++j) {
-            const float hj = sH[j];
-            rk += (hj < H) || (hj == H && j < i);
+        const float4* h4 = reinterpret_cast<const float4*>(sH);
+#pragma unroll 4
+        for (int j = 0; j < L4; j += 4) {
+            const float4 hv = h4[j >> 2];
+            rk += (hv.x < H) || (hv.x == H && j < i);
+            rk += (hv.y < H) || (hv.y == H && j + 1 < i);
+            rk += (hv.z < H) || (hv.z == H && j + 2 < i);
+            rk += (hv.w < H) || (hv.w == H && j + 3 < i);
         }
         sSorted[rk] = (double)H;
     }
@@ -1060,7 +1096,7 @@ size_t k1_smem_bytes() { return ((sizeof(K1Shared<DT>) + 127) / 128) * 128 + (si
 template <int DT>
 dg_status launch_k1(const void* logits, int64_t ld, int64_t n, int32_t L, int64_t V,
                     const dg_canvas_params* params, uint64_t seed, int32_t* argmax, int32_t* sample, float* entropy,
-                    float* lse, const DeferredWs& ws, cudaStream_t stream) {
+                    float* lse, const DeferredWs& ws, const ChoiceOut& co, cudaStream_t stream) {
     auto kern = k1_row_stats<DT>;
     const size_t smem = k1_smem_bytes<DT>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -1068,7 +1104,7 @@ dg_status launch_k1(const void* logits, int64_t ld, int64_t n, int32_t L, int64_
     const int64_t ld_bytes = ld * (DT == 0 ? 2 : 4);
     const cudaError_t e = dghost::launch_pdl(kern, dim3((unsigned)L, (unsigned)n, 1), dim3(kK1Threads), smem, stream,
                                              static_cast<const unsigned char*>(logits), ld_bytes, V, L, params, seed,
-                                             argmax, sample, entropy, lse, ws, dghost::status_word());
+                                             argmax, sample, entropy, lse, ws, co, dghost::status_word());
     dghost::count_launch();
     return dghost::cuda_status(e);
 }
@@ -1166,11 +1202,12 @@ size_t dg_denoise_workspace_bytes(int64_t n_canvas, int32_t L, int64_t, dg_dtype
     return (denoise_ws_bytes(n_canvas * (int64_t)L) + 255) / 256 * 256;
 }
 
-dg_status dg_denoise_stats(const void* logits, dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L, int64_t V,
-                           const dg_canvas_params* params, uint64_t seed, int32_t* canvas, int32_t* prev_argmax,
-                           int32_t* stable_count, uint8_t* accept_mask, int32_t* argmax, int32_t* sample,
-                           float* entropy, float* lse, uint8_t* converged, float* mean_entropy, int32_t* n_accept,
-                           void* workspace, size_t workspace_bytes, dg_stream_t stream) {
+static dg_status denoise_stats(const void* logits, dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L,
+                               int64_t V, const dg_canvas_params* params, uint64_t seed, int32_t* canvas,
+                               int32_t* prev_argmax, int32_t* stable_count, uint8_t* accept_mask, int32_t* argmax,
+                               int32_t* sample, float* entropy, float* lse, uint8_t* converged, float* mean_entropy,
+                               int32_t* n_accept, const ChoiceOut& co, void* workspace, size_t workspace_bytes,
+                               dg_stream_t stream) {
     if (dtype != DG_BF16 && dtype != DG_FP32) return DG_ERR_INVALID_ARG;
     dg_status s = check_canvas_dims(n_canvas, L, V);
     if (s != DG_OK) return s;
@@ -1186,11 +1223,22 @@ dg_status dg_denoise_stats(const void* logits, dg_dtype dtype, int64_t ld, int64
     if ((reinterpret_cast<uintptr_t>(workspace) & 7u) != 0) return DG_ERR_ALIGNMENT;
     const DeferredWs ws = carve_ws(workspace, n_canvas * (int64_t)L);
     cudaStream_t st = (cudaStream_t)stream;
-    s = dtype == DG_BF16 ? launch_k1<0>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, ws, st)
-                         : launch_k1<1>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, ws, st);
+    s = dtype == DG_BF16
+            ? launch_k1<0>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, ws, co, st)
+            : launch_k1<1>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, ws, co, st);
     if (s != DG_OK) return s;
     return launch_k2(entropy, sample, argmax, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
                      accept_mask, converged, mean_entropy, n_accept, ws, st);
+}
+
+dg_status dg_denoise_stats(const void* logits, dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L, int64_t V,
+                           const dg_canvas_params* params, uint64_t seed, int32_t* canvas, int32_t* prev_argmax,
+                           int32_t* stable_count, uint8_t* accept_mask, int32_t* argmax, int32_t* sample,
+                           float* entropy, float* lse, uint8_t* converged, float* mean_entropy, int32_t* n_accept,
+                           void* workspace, size_t workspace_bytes, dg_stream_t stream) {
+    return denoise_stats(logits, dtype, ld, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
+                         accept_mask, argmax, sample, entropy, lse, converged, mean_entropy, n_accept, ChoiceOut{},
+                         workspace, workspace_bytes, stream);
 }
 
 static dg_status denoise_samples(const void* logits, dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L,
@@ -1226,11 +1274,27 @@ dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld, int64_
                           int32_t* stable_count, uint8_t* accept_mask, int32_t* argmax, int32_t* sample,
                           float* entropy, float* lse, uint8_t* converged, float* mean_entropy, int32_t* n_accept,
                           void* workspace, size_t workspace_bytes, dg_stream_t stream) {
-    dg_status s = dg_denoise_stats(logits, dtype, ld, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
-                                   accept_mask, argmax, sample, entropy, lse, converged, mean_entropy, n_accept,
-                                   workspace, workspace_bytes, stream);
+    dg_status s = denoise_stats(logits, dtype, ld, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
+                                accept_mask, argmax, sample, entropy, lse, converged, mean_entropy, n_accept,
+                                ChoiceOut{}, workspace, workspace_bytes, stream);
     if (s != DG_OK || n_canvas == 0) return s;
     // alone on its stream: three CTAs per SM hide more of the load latency
+    return denoise_samples(logits, dtype, ld, n_canvas, L, V, params, seed, canvas, sample, workspace,
+                           workspace_bytes, 3, (cudaStream_t)stream);
+}
+
+dg_status dg_denoise_step_choices(const void* logits, dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L,
+                                  int64_t V, const dg_canvas_params* params, uint64_t seed, int32_t* canvas,
+                                  int32_t* prev_argmax, int32_t* stable_count, uint8_t* accept_mask, int32_t* argmax,
+                                  int32_t* sample, float* entropy, float* lse, uint8_t* converged,
+                                  float* mean_entropy, int32_t* n_accept, const int32_t* choices, int32_t C,
+                                  float* probs, void* workspace, size_t workspace_bytes, dg_stream_t stream) {
+    if (C < 1 || C > 1024) return DG_ERR_INVALID_ARG;
+    if (n_canvas > 0 && (!choices || !probs)) return DG_ERR_INVALID_ARG;
+    dg_status s = denoise_stats(logits, dtype, ld, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
+                                accept_mask, argmax, sample, entropy, lse, converged, mean_entropy, n_accept,
+                                ChoiceOut{choices, probs, C}, workspace, workspace_bytes, stream);
+    if (s != DG_OK || n_canvas == 0) return s;
     return denoise_samples(logits, dtype, ld, n_canvas, L, V, params, seed, canvas, sample, workspace,
                            workspace_bytes, 3, (cudaStream_t)stream);
 }

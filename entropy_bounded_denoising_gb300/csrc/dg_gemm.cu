@@ -600,13 +600,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (!im.valid) {
                 // padding member of the group: nothing to store
             } else if (splits > 1) {
-                float* dst = a.partial + (size_t)im.w * (BM * C::BN) + (size_t)row * C::BN;
+                // partial tile in column-quad order [BN / 4][BM][4]: the warp's 32 rows store
+                // 512 contiguous bytes per instruction instead of 16 bytes in each of 32 rows
+                float* dst = a.partial + (size_t)im.w * (BM * C::BN) + (size_t)row * 4;
                 for (int ch = 0; ch < C::BN / 32; ++ch) {
                     float v[32];
                     dg::tmem_ld32(tbase + ch * 32, v);
 #pragma unroll
                     for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4*>(dst + ch * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                        *reinterpret_cast<float4*>(dst + (size_t)((ch * 32 + i) / 4) * (BM * 4)) =
+                            make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
                 }
             } else if (a.epi == EPI_LOGIT_STATS) {
                 logit_stats_tile<C::BN>(a, im.m, im.n, row, tbase);
@@ -749,9 +752,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
 // ------------------------------------------------------------------ split-K fix-up
 // Adds the k-slice partials of each tile in slice order and applies the epilogue.  Every
-// thread owns 4 consecutive output columns of a row (float4 loads, coalesced across the warp)
-// and the tiles are spread over gridDim.y CTAs each.  For the gate/up epilogue the output
-// columns are the tile's first BN/2 (gate) columns, each paired with the up column BN/2 later.
+// thread owns 4 consecutive output columns of a row; consecutive threads take consecutive
+// rows of one column quad, which are adjacent in the partial tiles' [BN / 4][BM][4] order
+// (float4 loads, coalesced across the warp), and the tiles are spread over gridDim.y CTAs
+// each.  For the gate/up epilogue the output columns are the tile's first BN/2 (gate)
+// columns, each paired with the up column BN/2 later.
 template <int BN>
 __global__ void __launch_bounds__(256) k_fixup(const GemmArgs a) {
     dg::pdl_wait();
@@ -772,8 +777,9 @@ __global__ void __launch_bounds__(256) k_fixup(const GemmArgs a) {
     const int per_cta = (quads + gridDim.y - 1) / gridDim.y;
     const int q0 = blockIdx.y * per_cta, q1 = min(quads, q0 + per_cta);
     for (int qd = q0 + threadIdx.x; qd < q1; qd += blockDim.x) {
-        const int row = qd / (out_cols / 4);
-        const int col = (qd % (out_cols / 4)) * 4;
+        const int row = qd % BM;
+        const int cq = qd / BM;  // column quad
+        const int col = cq * 4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), up = make_float4(0.f, 0.f, 0.f, 0.f);
         // kU slices' loads in flight at once, added in slice order (read once: streaming loads)
         constexpr int kU = 8;
@@ -782,9 +788,9 @@ __global__ void __launch_bounds__(256) k_fixup(const GemmArgs a) {
 #pragma unroll
             for (int j = 0; j < kU; ++j) {
                 if (s0 + j >= splits) continue;
-                const float* src = a.partial + (size_t)((s0 + j) * T + t) * (BM * BN) + (size_t)row * BN + col;
+                const float* src = a.partial + (size_t)((s0 + j) * T + t) * (BM * BN) + ((size_t)cq * BM + row) * 4;
                 v[j] = __ldcs(reinterpret_cast<const float4*>(src));
-                if (gu) u[j] = __ldcs(reinterpret_cast<const float4*>(src + BN / 2));
+                if (gu) u[j] = __ldcs(reinterpret_cast<const float4*>(src + (size_t)(BN / 8) * BM * 4));
             }
 #pragma unroll
             for (int j = 0; j < kU; ++j) {
@@ -848,10 +854,9 @@ DG_DEVINL bool self_cond_on(const dg_canvas_params& p, const uint8_t* converged,
 // Compact list of canvases in original order: those whose feedback is computed this step
 // (mode 0) or the active ones (mode 1, the LM head's rows).  Per chunk of blockDim.x
 // canvases, warp ballots, an exclusive prefix over the warps' counts.
-__global__ void k_plan(const dg_canvas_params* __restrict__ params, const uint8_t* __restrict__ converged,
-                       int64_t n, int32_t* __restrict__ plan, int mode) {
-    dg::pdl_wait();
-    dg::pdl_release();
+// Called by every thread of one block.
+DG_DEVINL void plan_list(const dg_canvas_params* __restrict__ params, const uint8_t* __restrict__ converged,
+                         int64_t n, int32_t* __restrict__ plan, int mode) {
     __shared__ int warp_base[32];
     __shared__ int total;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -882,12 +887,22 @@ __global__ void k_plan(const dg_canvas_params* __restrict__ params, const uint8_
     if (threadIdx.x == 0) plan[0] = count;
 }
 
-// Zero the feedback rows of canvases that get none this step: grid (CTAs per canvas, canvases),
-// 16-byte stores (d is a multiple of 8 and delta_emb 16-byte aligned).
-__global__ void k_zero_rows(const dg_canvas_params* __restrict__ params, const uint8_t* __restrict__ converged,
-                            int32_t L, int32_t d, uint16_t* __restrict__ delta) {
+__global__ void k_plan(const dg_canvas_params* __restrict__ params, const uint8_t* __restrict__ converged,
+                       int64_t n, int32_t* __restrict__ plan, int mode) {
     dg::pdl_wait();
     dg::pdl_release();
+    plan_list(params, converged, n, plan, mode);
+}
+
+// The feedback plan (block (0, 0), as k_plan mode 0) and the zeroing of the feedback rows of
+// canvases that get none this step: grid (CTAs per canvas, canvases), 16-byte stores (d is a
+// multiple of 8 and delta_emb 16-byte aligned).
+__global__ void k_zero_rows(const dg_canvas_params* __restrict__ params, const uint8_t* __restrict__ converged,
+                            int64_t n, int32_t L, int32_t d, uint16_t* __restrict__ delta,
+                            int32_t* __restrict__ plan) {
+    dg::pdl_wait();
+    dg::pdl_release();
+    if (blockIdx.x == 0 && blockIdx.y == 0) plan_list(params, converged, n, plan, 0);
     const int64_t c = blockIdx.y;
     if (self_cond_on(params[c], converged, c)) return;
     const int64_t vecs = (int64_t)L * d / 8;
@@ -1223,15 +1238,13 @@ dg_status dg_self_cond_prepare(const dg_canvas_params* params, const uint8_t* co
     if (s != DG_OK) return s;
     cudaStream_t st = (cudaStream_t)stream;
     int32_t* plan = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + lay.plan);
-    cudaError_t e = dghost::launch_pdl(k_plan, dim3(1), dim3(1024), 0, st, params, converged, n_canvas, plan, 0);
-    dghost::count_launch();
-    if (e != cudaSuccess) return DG_ERR_CUDA;
     // about four CTAs per SM over all canvases (most of them exit at once when feedback is on)
     const int P = std::max(1, dghost::sm_count());
     const int64_t per_canvas = std::max<int64_t>(1, std::min<int64_t>(((int64_t)L * d / 8 + 255) / 256,
                                                                       (4LL * P + n_canvas - 1) / n_canvas));
     dim3 grid((unsigned)per_canvas, (unsigned)n_canvas);
-    e = dghost::launch_pdl(k_zero_rows, grid, dim3(256), 0, st, params, converged, L, d, delta_emb);
+    const cudaError_t e = dghost::launch_pdl(k_zero_rows, grid, dim3(256), 0, st, params, converged, n_canvas, L, d,
+                                             delta_emb, plan);
     dghost::count_launch();
     return dghost::cuda_status(e);
 }

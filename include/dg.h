@@ -200,6 +200,30 @@ DG_API dg_status dg_denoise_samples(const void* logits, dg_dtype dtype, int64_t 
                                     int32_t* canvas, int32_t* sample,
                                     void* workspace, size_t workspace_bytes, dg_stream_t stream);
 
+/* dg_denoise_step with the single-pass-read gather fused into the statistics pass [SPR,
+ * "답의 내용은 몰라도 답을 담을 자리는 안다": one pass over a read-only request's logits
+ * returns the probabilities of its fixed answer tokens].  Besides every output of
+ * dg_denoise_step, for every position of every DG_ACTIVE canvas and every slot k < C:
+ *   probs[c][i][k] = exp(logits[c][i][tok] / T - lse[c][i]),  tok = choices[c][i][k],
+ * with the lse this call writes; the CTA that streams the row gathers its C logits as soon as
+ * its lse is known, so the logits are not read a second time.  The values are those of
+ * dg_choice_probs on this call's lse (bit for bit).  A slot with a token outside [0, V)
+ * gives 0 (use -1 for unused slots); inactive canvases leave probs untouched.  Read-only
+ * canvases (DG_READ_ONLY) are the intended users, but every active canvas is served.
+ *   choices (device) [n_canvas][L][C] int32.
+ *   probs   (device, out) [n_canvas][L][C] float.
+ * Other arguments, limits and errors are those of dg_denoise_step; in addition
+ * DG_ERR_INVALID_ARG for C outside [1, 1024] or null choices / probs. */
+DG_API dg_status dg_denoise_step_choices(const void* logits, dg_dtype dtype, int64_t ld,
+                                         int64_t n_canvas, int32_t L, int64_t V,
+                                         const dg_canvas_params* params, uint64_t seed,
+                                         int32_t* canvas, int32_t* prev_argmax, int32_t* stable_count,
+                                         uint8_t* accept_mask, int32_t* argmax, int32_t* sample,
+                                         float* entropy, float* lse, uint8_t* converged,
+                                         float* mean_entropy, int32_t* n_accept,
+                                         const int32_t* choices, int32_t C, float* probs,
+                                         void* workspace, size_t workspace_bytes, dg_stream_t stream);
+
 /* The per-canvas half of the step (acceptance, renoise, convergence) on caller-given
  * per-position entropy, sample and argmax, all (device) [n_canvas][L].  Same semantics and
  * outputs as dg_denoise_step, except that every accepted position takes the given sample

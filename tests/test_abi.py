@@ -58,6 +58,15 @@ def test_host_validation_without_gpu():
     assert lib.dg_denoise_samples(16, 0, 8, 1, 16, 8, 16, 0, None, 16, 256, 768, None) == dg.DG_ERR_INVALID_ARG
     assert lib.dg_denoise_samples(16, 0, 8, 1, 16, 8, 16, 0, 16, 16, 256, 640, None) == dg.DG_ERR_WORKSPACE
     assert lib.dg_denoise_samples(18, 0, 8, 1, 16, 8, 16, 0, 16, 16, 256, 768, None) == dg.DG_ERR_ALIGNMENT
+    # the step with the fused choice gather: C within 1..1024, choices and probs given, then
+    # the step's own checks
+    assert lib.dg_denoise_step_choices(16, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), 16, 0, 16, 256, 768, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_denoise_step_choices(16, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), 16, 1025, 16, 256, 768, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_denoise_step_choices(16, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), None, 4, 16, 256, 768, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_denoise_step_choices(16, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), 16, 4, None, 256, 768, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_denoise_step_choices(18, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), 16, 4, 16, 256, 768, None) == dg.DG_ERR_ALIGNMENT
+    assert lib.dg_denoise_step_choices(16, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), 16, 4, 16, None, 0, None) == dg.DG_ERR_WORKSPACE
+    assert lib.dg_denoise_step_choices(None, 0, 8, 0, 16, 8, None, 0, *([None] * 11), None, 4, None, None, 0, None) == dg.DG_OK
     # the bounded-wait probe: poll limits outside 1..65536, a null or misaligned result
     assert lib.dg_probe_bounded_wait(0, 16, None) == dg.DG_ERR_INVALID_ARG
     assert lib.dg_probe_bounded_wait(65537, 16, None) == dg.DG_ERR_INVALID_ARG

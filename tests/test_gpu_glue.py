@@ -3,6 +3,9 @@
 * dg_choice_probs: p = exp(x_tok / T - lse) with the step's own lse from dg_denoise_step;
   relative tolerance 2e-7 |x/T| + 1.5e-6 |lse| + 1e-6 (fp32 scaling and exp, plus the lse's
   own 1e-6 relative bar), absolute 1e-37 for underflow.
+* dg_denoise_step_choices (the same gather fused into the statistics pass): the step's outputs
+  equal to dg_denoise_step's, the probabilities bit-equal to dg_choice_probs, and the same
+  oracle tolerance.
 * dg_embed_canvas: bit-exact (the output is a rounded bf16 pattern fixed by its definition).
 * dg_commit: exact.
 Small ragged cases on every element, the batched workload's full size on sampled rows."""
@@ -98,6 +101,96 @@ def test_choice_probs_batched_full_size():
         hx = synth.host_logits(x[c, i:i + 1])
         ref = oracle.choice_probs(hx, [1.0], choices[c, i:i + 1], V=V)
         y = _logit_values(hx)[0][choices[c, i]]
+        _check_probs(got[c, i:i + 1], ref, y[None, :], np.array([[lse[c, i]]]))
+
+
+def _run_choices(xd, pt, seed, b, choices, probs, V):
+    n, L, ld = xd.shape
+    dg.dg_denoise_step_choices(xd, pt, seed, b.canvas, b.prev, b.stable, b.accept, b.argmax, b.sample,
+                               b.entropy, b.lse, b.converged, choices, probs, b.mean_entropy, b.n_accept,
+                               V=V, ld=ld)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("V,ld,C", [(5003, 5008, 6), (40000, 40000, 33), (2, 8, 1)])
+def test_step_with_fused_choices(dtype, V, ld, C):
+    """dg_denoise_step_choices: every step output equal to dg_denoise_step's on the same
+    inputs, the probabilities bit-equal to dg_choice_probs on the step's lse and within the
+    oracle tolerance; read-only, normal (deferred and DG_SAMPLE_ALL) and inactive canvases in
+    one batch; C = 33 spans two rounds of a warp's lanes."""
+    rng = np.random.default_rng(V + C)
+    n, L = 4, 70
+    x = synth.logits(n, L, V, seed=V + 1, step=1, scale=(0.5, 12.0), spike_frac=0.2, dtype=dtype, ld=ld)
+    p = _params(n, rng)
+    p["flags"] = np.array([dg.DG_ACTIVE | dg.DG_READ_ONLY, dg.DG_ACTIVE, 0,
+                           dg.DG_ACTIVE | dg.DG_SAMPLE_ALL], np.uint32)
+    p["max_steps"][:] = 8
+    pt = dg.params_tensor(p, DEV)
+    xd = x.to(DEV)
+    choices = rng.integers(0, V, (n, L, C)).astype(np.int32)
+    if C >= 3:
+        choices[:, :, 0] = -1
+        choices[:, :, 1] = V
+    ch = torch.from_numpy(choices).to(DEV)
+    canvas0 = rng.integers(0, V, (n, L)).astype(np.int32)
+    a = StepBuffers.make(n, L, DEV, canvas=canvas0)
+    b = StepBuffers.make(n, L, DEV, canvas=canvas0)
+    probs = torch.full((n, L, C), -5.0, dtype=torch.float32, device=DEV)
+    _run_choices(xd, pt, 9, a, ch, probs, V)
+    run_step(xd, pt, 9, b, V=V)
+    ref_g = torch.full((n, L, C), -5.0, dtype=torch.float32, device=DEV)
+    dg.dg_choice_probs(xd, b.lse, pt, ch, ref_g, V=V)
+    torch.cuda.synchronize()
+    assert dg.dg_get_device_status() == 0
+    ha, hb = a.host(), b.host()
+    for k in ha:
+        assert np.array_equal(ha[k], hb[k]), k
+    got = probs.cpu().numpy()
+    assert np.array_equal(got, ref_g.cpu().numpy())
+    assert (got[2] == -5.0).all()
+    hx = synth.host_logits(x)
+    for c in (0, 1, 3):
+        T = float(p["temperature"][c])
+        ref = oracle.choice_probs(hx[c], np.full(L, T), choices[c], V=V)
+        y = np.take_along_axis(_logit_values(hx[c]), np.clip(choices[c], 0, V - 1), axis=1) / T
+        _check_probs(got[c], ref, y, ha["lse"][c][:, None])
+        if C >= 3:
+            assert (got[c][:, :2] == 0).all()
+
+
+def test_step_with_fused_choices_batched_full_size():
+    """The batched workload (8 x 256, V = 262144) as read-only canvases with 4 choices per
+    position, one of them the argmax: probabilities bit-equal to dg_choice_probs everywhere,
+    against the oracle on sampled rows, and the argmax slot the largest."""
+    wl = synth.WORKLOADS["batched"]
+    n, L, V = wl.n, wl.L, wl.V
+    rng = np.random.default_rng(12)
+    x = synth.logits(n, L, V, seed=wl.seed, step=1, scale=wl.scale, spike_frac=wl.spike_frac, device=DEV)
+    p = _params(n, rng)
+    pt = dg.params_tensor(p, DEV)
+    C = 4
+    b = StepBuffers.make(n, L, DEV)
+    run_step(x, pt, 5, b)
+    choices = rng.integers(0, V, (n, L, C)).astype(np.int32)
+    choices[:, :, 3] = b.argmax.cpu().numpy()
+    ch = torch.from_numpy(choices).to(DEV)
+    a = StepBuffers.make(n, L, DEV)
+    probs = torch.zeros((n, L, C), dtype=torch.float32, device=DEV)
+    _run_choices(x, pt, 5, a, ch, probs, V)
+    ref_g = torch.zeros((n, L, C), dtype=torch.float32, device=DEV)
+    dg.dg_choice_probs(x, a.lse, pt, ch, ref_g)
+    torch.cuda.synchronize()
+    assert dg.dg_get_device_status() == 0
+    assert torch.equal(a.lse, b.lse) and torch.equal(a.entropy, b.entropy)
+    got = probs.cpu().numpy()
+    assert np.array_equal(got, ref_g.cpu().numpy())
+    assert (got[:, :, 3] >= got[:, :, :3].max(axis=2)).all()
+    lse = a.lse.cpu().numpy()
+    for (c, i) in [(0, 0), (2, 131), (5, 64), (7, 255)]:
+        T = float(p["temperature"][c])
+        hx = synth.host_logits(x[c, i:i + 1])
+        ref = oracle.choice_probs(hx, [T], choices[c, i:i + 1], V=V)
+        y = _logit_values(hx)[0][choices[c, i]] / T
         _check_probs(got[c, i:i + 1], ref, y[None, :], np.array([[lse[c, i]]]))
 
 

@@ -445,7 +445,8 @@ def run_ours(args):
     peak_alone = pk["bf16_tflops"]   # rows timed alone, in short bursts
     pe_tflops = ar["pe_flops"] / (t_pe * 1e-3) / 1e12 if t_pe > 0 else 0.0
     t_roof = max(ar["bytes"] / (pk["hbm_gbs"] * 1e9), ar["tc_flops"] / (peak_tc * 1e12))
-    traffic = _profile_traffic("pe_gemm_batched")
+    # the committed capture is of the batched workload's P.E launch: no figure for the others
+    traffic = _profile_traffic("pe_gemm_batched") if wl.name == "batched" else None
 
     # ---------------------------------------------------------------- e2e: host buffers
     e2e = None

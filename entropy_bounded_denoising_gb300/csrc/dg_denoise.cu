@@ -861,6 +861,14 @@ __global__ void __launch_bounds__(1024) k2_accept(
     const int i = threadIdx.x, lane = i & 31, warp = i >> 5, nwarps = blockDim.x >> 5;
     dg::pdl_wait();
     dg::pdl_release();
+    const bool valid = i < L;
+    const int64_t q = c * L + i;
+    // the per-position loads (and the canvas's stable count) go out with the parameter load:
+    // in range whatever the parameters say, unused for an inactive canvas
+    const float H0 = valid ? entropy[q] : 0.f;
+    const int32_t am = valid ? argmax[q] : 0;
+    const int32_t pam = valid ? prev_argmax[q] : 0;
+    const int32_t st0 = i == 0 ? stable_count[c] : 0;
     const dg_canvas_params p = params[c];
     if (!(p.flags & DG_ACTIVE)) return;
     if (!dg::canvas_params_ok(p, L)) {
@@ -872,13 +880,9 @@ __global__ void __launch_bounds__(1024) k2_accept(
     // a canvas without DG_SAMPLE_ALL are listed for the deferred sampling pass, which writes
     // their sample and token
     const bool deferred = ws.count && (ws.all_deferred || !(p.flags & DG_SAMPLE_ALL));
-    const bool valid = i < L;
-    const int64_t q = c * L + i;
     // a NaN entropy (a row flagged by the statistics pass) ranks after every number, so the
     // ranks stay a permutation and every reserved slot of the sampler's list is written
-    const float H0 = valid ? entropy[q] : 0.f;
     const float H = (H0 == H0) ? H0 : INFINITY;
-    const int32_t am = valid ? argmax[q] : 0;
     const int L4 = (L + 3) & ~3;  // <= blockDim.x
     // +inf pads the entropies to whole quads; a pad never ranks before a position (its index
     // is larger and no entropy exceeds +inf)
@@ -933,7 +937,7 @@ __global__ void __launch_bounds__(1024) k2_accept(
     if (read_only) nacc = 0;
 
     if (i == 0 && deferred && nacc > 0) sBase = atomicAdd(ws.count, nacc);
-    const bool same = __syncthreads_and(!valid || am == prev_argmax[q]) != 0;
+    const bool same = __syncthreads_and(!valid || am == pam) != 0;
     if (valid) {
         const bool acc = rk < nacc;
         if (deferred && acc) {  // accepted ranks are 0..nacc-1
@@ -953,7 +957,7 @@ __global__ void __launch_bounds__(1024) k2_accept(
         prev_argmax[q] = am;
     }
     if (i == 0) {
-        const int32_t st = same ? stable_count[c] + 1 : 0;
+        const int32_t st = same ? st0 + 1 : 0;
         const double Hbar = Hsum / (double)L;
         bool conv = (st >= p.k && Hbar < (double)p.tau) || (p.step + 1 >= p.max_steps);
         if (read_only) conv = true;

@@ -46,6 +46,8 @@ enum AMode { A_TMA = 0, A_SOFTMAX_BF16 = 1, A_SOFTMAX_FP32 = 2, A_TMA_CANVAS = 3
 enum BMode { B_KMAJOR = 0, B_MNMAJOR = 1, B_KMAJOR_GATEUP = 2 };
 enum Epi { EPI_F32 = 0, EPI_BF16 = 1, EPI_GELU_GATEUP = 2, EPI_SCATTER_BF16 = 3, EPI_LOGIT_STATS = 4 };
 
+constexpr int kSplitTab = 256;
+
 struct GemmArgs {
     int32_t m_tiles;        // m-tiles when plan == nullptr; upper bound otherwise
     const int32_t* plan;    // plan[0] = active canvases, plan[1..] = their ids (or nullptr)
@@ -73,6 +75,9 @@ struct GemmArgs {
     int32_t min_slice;      // k-blocks
     int64_t max_slots;      // partial tiles the workspace holds
     int32_t split_below;    // split only below this round efficiency (percent)
+    // the same rule tabulated by the host for plans listing j <= kSplitTab canvases
+    // (split_tab[j]); larger plans evaluate it on the device
+    uint8_t split_tab[260];
     // EPI_LOGIT_STATS: per (tile column block, row) softmax states, [n_tiles][5][stats_rows]
     float* stats;
     int64_t stats_rows;
@@ -166,9 +171,11 @@ DG_DEVINL int64_t group_count(const GemmArgs& a, int mt, int cm, int splits) {
     return (int64_t)splits * a.n_tiles * ((mt + cm - 1) / cm);
 }
 
-// The launch's k-slices for `mt` active m-tiles.
+// The launch's k-slices for `mt` active m-tiles.  The rule's loop of integer divisions takes
+// microseconds on one thread, so plans of up to kSplitTab canvases read the host's table.
 DG_DEVINL int active_splits(const GemmArgs& a, int mt) {
     if (!a.dyn_splits) return a.splits;
+    if (a.plan && mt % a.tpc == 0 && mt / a.tpc <= kSplitTab) return a.split_tab[mt / a.tpc];
     const int64_t per_split = (int64_t)a.n_tiles * ((mt + a.cm_plan - 1) / a.cm_plan);
     return plan_splits(per_split, mt, a.n_tiles, a.k_blocks, a.clusters, a.min_slice, a.max_slots, a.split_below);
 }
@@ -206,9 +213,18 @@ DG_DEVINL float ex2(float x) {
     return y;
 }
 
+// GELU, tanh form: 0.5 z (1 + tanh y), y = sqrt(2 / pi) (z + 0.044715 z^3), evaluated as
+// z * sigmoid(2 y) = z / (1 + 2^(-2 y log2 e)) (the same function, since 1 + tanh y =
+// 2 / (1 + e^(-2 y))): one exponential and one reciprocal, about 1e-6 relative, far inside the
+// bf16 rounding of the hidden layer.  Large |z|: the exponential saturates to 0 or inf and the
+// result to z or -0.
 DG_DEVINL float gelu_tanh(float z) {
-    const float k = 0.7978845608028654f;  // sqrt(2 / pi)
-    return 0.5f * z * (1.f + tanhf(k * (z + 0.044715f * z * z * z)));
+    const float k2 = -2.f * 0.7978845608028654f * 1.4426950408889634f;  // -2 sqrt(2 / pi) log2 e
+    float e, r;
+    const float t = k2 * (z + 0.044715f * z * z * z);
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(t));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+    return z * r;
 }
 
 // Groups of softmax-transform threads that take the P.E stages in turn (2: measured fastest
@@ -757,8 +773,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 // (float4 loads, coalesced across the warp), and the tiles are spread over gridDim.y CTAs
 // each.  For the gate/up epilogue the output columns are the tile's first BN/2 (gate)
 // columns, each paired with the up column BN/2 later.
-template <int BN>
-__global__ void __launch_bounds__(256) k_fixup(const GemmArgs a) {
+template <int BN, bool GU>
+__global__ void __launch_bounds__(256, GU ? 1 : 4) k_fixup(const GemmArgs a) {
     dg::pdl_wait();
     dg::pdl_release();
     const int mt = active_m_tiles(a);
@@ -771,7 +787,7 @@ __global__ void __launch_bounds__(256) k_fixup(const GemmArgs a) {
     const int64_t t = blockIdx.x;
     if (t >= T) return;
     const int n = (int)(t / mt), m = (int)(t % mt);
-    const bool gu = a.epi == EPI_GELU_GATEUP;
+    constexpr bool gu = GU;  // a.epi == EPI_GELU_GATEUP
     const int out_cols = gu ? BN / 2 : BN;
     const int quads = BM * out_cols / 4;
     const int per_cta = (quads + gridDim.y - 1) / gridDim.y;
@@ -1012,10 +1028,15 @@ dg_status launch_gemm(const void* tmA, const void* tmB0, const void* tmB1, const
     if (e != cudaSuccess) return DG_ERR_CUDA;
     if (a.splits > 1 || a.dyn_splits) {  // a device plan that does not split leaves the fix-up idle
         const int64_t T = (int64_t)a.m_tiles * a.n_tiles;
-        // spread each tile over enough CTAs to fill the GPU a few times
+        // spread each tile over enough CTAs to give the GPU about 8 per SM, each thread at
+        // least one column quad (its partial loads in flight are what hides the latency)
         const int P = dghost::sm_count();
-        const unsigned per_tile = (unsigned)std::max<int64_t>(1, std::min<int64_t>(16, (4LL * P + T - 1) / T));
-        e = dghost::launch_pdl(k_fixup<C::BN>, dim3((unsigned)T, per_tile, 1), dim3(256), 0, stream, a);
+        const bool gu = a.epi == EPI_GELU_GATEUP;
+        const int64_t quads = (int64_t)BM * (gu ? C::BN / 2 : C::BN) / 4;
+        const unsigned per_tile = (unsigned)std::max<int64_t>(
+            1, std::min<int64_t>(std::min<int64_t>(64, quads / 256), (8LL * P + T - 1) / T));
+        e = gu ? dghost::launch_pdl(k_fixup<C::BN, true>, dim3((unsigned)T, per_tile, 1), dim3(256), 0, stream, a)
+               : dghost::launch_pdl(k_fixup<C::BN, false>, dim3((unsigned)T, per_tile, 1), dim3(256), 0, stream, a);
         dghost::count_launch();
     }
     return dghost::cuda_status(e);
@@ -1034,6 +1055,14 @@ dg_status plan_and_launch(const void* tmA, const void* tmB0, const void* tmB1, G
         a.min_slice = pl.min_slice;
         a.max_slots = pl.max_slots;
         a.split_below = pl.split_below;
+        // j listed canvases: j * tpc active m-tiles (the plan lists whole canvases)
+        const int64_t jmax = std::min<int64_t>(kSplitTab, a.tpc > 0 ? a.m_tiles / a.tpc : 0);
+        for (int64_t j = 0; j <= jmax; ++j) {
+            const int64_t mt = j * a.tpc;
+            const int64_t per_split = (int64_t)a.n_tiles * ((mt + pl.cm - 1) / pl.cm);
+            a.split_tab[j] = (uint8_t)plan_splits(per_split, mt, a.n_tiles, a.k_blocks, pl.clusters, pl.min_slice,
+                                                  pl.max_slots, pl.split_below);
+        }
     }
     return launch_gemm<C>(tmA, tmB0, tmB1, a, pl, stream);
 }

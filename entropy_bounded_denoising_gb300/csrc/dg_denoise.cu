@@ -25,9 +25,9 @@
 // A sample is kept only at an accepted position (a rejected one is renoised in the same
 // step), so canvases without DG_SAMPLE_ALL skip the search in the statistics pass; the
 // acceptance kernel lists their accepted rows (with each row's maximum, recorded by the
-// statistics pass), and a third kernel searches those rows in 16 KB chunks, one warp per
-// chunk, reading global memory directly: few rows are left, so the work is cut finer than a
-// row to keep every SM busy.
+// statistics pass), and a third kernel searches those rows in chunks of up to 16 KB, the
+// warps taking groups of consecutive chunks in a grid-stride loop, reading global memory
+// directly: few rows are left, so the work is cut finer than a row to keep every SM busy.
 // The reduction order depends only on V, so a row's result does not depend on its batch.
 #include <cuda_runtime.h>
 
@@ -47,6 +47,7 @@ constexpr uint32_t kChunkBytes = 16384;            // deferred sampling: largest
 constexpr uint32_t kChunkMin = 2048;               // and smallest (one batch of loads per lane)
 constexpr int kDWarps = 8;                         // deferred sampling: warps per CTA
 constexpr int kDBatch = 4;                         // 16-byte loads in flight per lane
+constexpr int64_t kRunsMaxRows = 512;              // deferred sampling: contiguous runs up to this many rows
 constexpr uint32_t kPieceBytes = 16384;            // bytes per slot
 constexpr int kVecPerLane = (int)(kPieceBytes / 16) / (kK1Warps * 32);  // 16-byte vectors per lane per piece
 constexpr int kDrawPerLane = 1;                    // queued groups drawn per lane per round
@@ -704,20 +705,27 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
 
 // ------------------------------------------------------------------------------------
 // Deferred sampling: the Gumbel-max samples of the listed accepted rows.  Work items are
-// (list entry, chunk of its row), taken one per warp in a grid-stride loop; chunks are 16 KB,
+// (list entry, chunk of its row), taken in groups of consecutive items by the warps in a
+// grid-stride loop (a warp streams each row's part of its group as one segment and publishes
+// once per segment); chunks are 16 KB,
 // or shorter (down to 2 KB) when the listed rows are too few to give every warp two; a lane
 // loads kDBatch 16-byte vectors at a time straight from global memory and draws the noise
 // only for 4-entry groups whose largest y + G_max reaches the bound m / T - kGumbelLow (m
-// the row's largest logit) or the warp's best so far.  A chunk's winner joins the row's
-// 64-bit key by atomicMax (order-independent, so the result is deterministic); the warp that
-// completes the row's last chunk writes its sample and token.
+// the row's largest logit) or the warp's best so far.  A segment's winner joins the row's
+// 64-bit key by atomicMax (order-independent, so the result is deterministic) and its chunks
+// are added to the row's count; the warp that brings the count to the row's chunks writes
+// its sample and token.
 // ------------------------------------------------------------------------------------
 // Order-preserving key of (score, entry): larger score first, then the smaller entry.
 DG_DEVINL unsigned long long score_key(float score, int idx) {
     return ((unsigned long long)float_key(score) << 32) | (unsigned long long)(0xffffffffu - (uint32_t)idx);
 }
 
-template <int DT>
+// kRuns: each warp takes one contiguous run of the items (for short lists, where a warp
+// gets at most a few chunks: a second chunk of the same row then costs no second
+// publication); else one chunk per step of a grid-stride loop, so that the warps read one
+// compact window of the list at a time (measured: contiguous runs are slower on long lists).
+template <int DT, bool kRuns>
 __global__ void __launch_bounds__(kDWarps * 32, 3) k1_sample_listed(
     const unsigned char* __restrict__ logits, int64_t ld_bytes, int64_t V, int32_t L,
     const dg_canvas_params* __restrict__ params, uint64_t seed, DeferredWs ws, int32_t* __restrict__ sample_out,
@@ -740,9 +748,10 @@ __global__ void __launch_bounds__(kDWarps * 32, 3) k1_sample_listed(
     const int kChunkElems = (int)(chunk_bytes / ES);
     const int cpr = (int)((row_bytes + chunk_bytes - 1) / chunk_bytes);  // chunks per row
     const int64_t items = (int64_t)count * cpr;
-    for (int64_t it = gw; it < items; it += nw) {
-        const int w = (int)(it / cpr);
-        const int chunk = (int)(it - (int64_t)w * cpr);
+    // One row segment: chunks [c_lo, c_hi) of list entry w, searched and published (the
+    // winner into the row's key, the chunks into its count; the warp that completes the count
+    // writes the sample and token).
+    auto segment = [&](int w, int c_lo, int c_hi) {
         const int2 e = ws.entry[w];
         const int64_t row = e.x;
         const bool in_range = (uint64_t)row < (uint64_t)rows;  // entries come from K2; checked anyway
@@ -760,9 +769,9 @@ __global__ void __launch_bounds__(kDWarps * 32, 3) k1_sample_listed(
             const dg::PhiloxPre pre = dg::philox_pre((uint32_t)pos, (uint32_t)p.step,
                                                      dg::ctr_word3(seed, dg::kStreamGumbel), (uint32_t)seed,
                                                      p.request_id);
-            const uint4* src = reinterpret_cast<const uint4*>(logits + row * ld_bytes + (int64_t)chunk * chunk_bytes);
-            const int e_lo = chunk * kChunkElems;
-            const int n_el = (int)min((int64_t)kChunkElems, V - e_lo);
+            const int e_lo = c_lo * kChunkElems;
+            const uint4* src = reinterpret_cast<const uint4*>(logits + row * ld_bytes + (int64_t)e_lo * ES);
+            const int n_el = (int)min((int64_t)(c_hi - c_lo) * kChunkElems, V - e_lo);
             const int nvec = (n_el + VN - 1) / VN;
             float x_thr = (bound - kGumbelMax - kCandidateSlack) * p.temperature;
             uint32_t thr2 = DT == 0 ? bf16_floor2(x_thr) : 0u;
@@ -785,7 +794,7 @@ __global__ void __launch_bounds__(kDWarps * 32, 3) k1_sample_listed(
                     const int j = b0 + k * 32 + lane;
                     if (j >= nvec) continue;
                     const uint4 v = cur[k];
-                    const int valid = n_el - j * VN;  // entries of this vector inside the row
+                    const int valid = n_el - j * VN;  // entries of this vector inside the segment
                     bool cand[GPV];
                     if (DT == 0 && valid >= VN) {
                         // whole vector: packed test of each 4-entry group's max
@@ -829,7 +838,8 @@ __global__ void __launch_bounds__(kDWarps * 32, 3) k1_sample_listed(
         if (lane == 0) {
             if (ok && best > -INFINITY) atomicMax(ws.key + w, score_key(best, bidx));
             __threadfence();
-            if (atomicAdd(ws.done + w, 1) == cpr - 1 && in_range) {
+            const int nc = c_hi - c_lo;
+            if (atomicAdd(ws.done + w, nc) == cpr - nc && in_range) {
                 // every chunk of the row is in: its winner is the position's sample and token
                 __threadfence();
                 const unsigned long long k = atomicMax(ws.key + w, 0ull);
@@ -839,6 +849,22 @@ __global__ void __launch_bounds__(kDWarps * 32, 3) k1_sample_listed(
             }
         }
         __syncwarp();
+    };
+    if constexpr (!kRuns) {
+        for (int64_t it = gw; it < items; it += nw) {
+            const int w = (int)(it / cpr);
+            const int c = (int)(it - (int64_t)w * cpr);
+            segment(w, c, c + 1);
+        }
+    } else {
+        const int64_t per = (items + nw - 1) / nw;
+        for (int64_t it = gw * per, it1 = min(items, gw * per + per); it < it1;) {
+            const int w = (int)(it / cpr);
+            const int c_lo = (int)(it - (int64_t)w * cpr);
+            const int c_hi = (int)min((int64_t)cpr, (int64_t)c_lo + (it1 - it));
+            it += c_hi - c_lo;
+            segment(w, c_lo, c_hi);
+        }
     }
 }
 
@@ -1128,7 +1154,9 @@ dg_status launch_kd(const void* logits, int64_t ld, int64_t n, int32_t L, int64_
     const unsigned grid =
         (unsigned)std::max<int64_t>(1, std::min<int64_t>((int64_t)ctas_per_sm * sms, (max_items + kDWarps - 1) / kDWarps));
     const int64_t ld_bytes = ld * (DT == 0 ? 2 : 4);
-    const cudaError_t e = dghost::launch_pdl(k1_sample_listed<DT>, dim3(grid), dim3(kDWarps * 32), 0, stream,
+    // few rows (a single request): contiguous runs per warp; else single chunks
+    auto kern = n * (int64_t)L <= kRunsMaxRows ? k1_sample_listed<DT, true> : k1_sample_listed<DT, false>;
+    const cudaError_t e = dghost::launch_pdl(kern, dim3(grid), dim3(kDWarps * 32), 0, stream,
                                              static_cast<const unsigned char*>(logits), ld_bytes, V, L, params, seed,
                                              ws, sample, canvas, n * (int64_t)L);
     dghost::count_launch();

@@ -352,25 +352,46 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=dev) if args.graph else torch.cuda.current_stream()
     stream.wait_stream(torch.cuda.current_stream())
     seed = 0x5EED0000 + rank
+    # Small batches (a single request) run the overlapped schedule: the acceptance and the
+    # deferred samples on a second stream while the feedback GEMMs, which need only the
+    # step's lse, start at once; the rows of canvases that converged are zeroed afterwards
+    # (bit-identical outputs, tests/test_gpu_schedule.py).  Larger batches keep every launch
+    # on one stream (measured faster: the second stream's sampler slows P.E more than it saves).
+    overlap = not fh and n * L <= 512
+    side = torch.cuda.Stream(device=dev) if overlap else None
+    ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
 
-    def step(ev=None):
+    def step_calls(xin, ev=None):
         if ev:
             ev[0].record(stream)
         if fh:
             dg.dg_lm_head_denoise_step(hid, E, params, seed, xs, canvas, prev, stable, acc, am, smp, ent, lse,
                                        conv, workspace=lws, stream=stream)
+        elif overlap:
+            dg.dg_denoise_row_stats(xin, params, seed, am, smp, ent, lse, dws, stream=stream)
+            ev_fork.record(stream)
+            side.wait_event(ev_fork)
+            dg.dg_denoise_accept(ent, smp, am, params, seed, canvas, prev, stable, acc, conv, dws, V=V, stream=side)
+            dg.dg_denoise_samples(xin, params, seed, canvas, smp, dws, stream=side)
+            ev_join.record(side)
         else:
-            dg.dg_denoise_step(x, params, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv, workspace=dws,
-                               stream=stream)
-        dg.dg_self_cond_prepare(params, conv, n, L, d, h, delta, wsp, stream=stream)
+            dg.dg_denoise_step(xin, params, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv,
+                               workspace=dws, stream=stream)
+        dg.dg_self_cond_prepare(params, None if overlap else conv, n, L, d, h, delta, wsp, stream=stream)
         if ev:
             ev[1].record(stream)
-        dg.dg_self_cond_pe(xs, lse, params, E, h, wsp, stream=stream)
+        dg.dg_self_cond_pe(xs if fh else xin, lse, params, E, h, wsp, stream=stream)
         if ev:
             ev[2].record(stream)
         dg.dg_self_cond_mlp(n, L, Wg, Wu, Wd, delta, wsp, stream=stream)
+        if overlap:
+            stream.wait_event(ev_join)
+            dg.dg_self_cond_zero_converged(params, conv, delta, stream=stream)
         if ev:
             ev[3].record(stream)
+
+    def step(ev=None):
+        step_calls(x, ev)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -482,9 +503,7 @@ def run_ours(args):
                                            lse, conv, workspace=lws, stream=stream)
                 dg.dg_self_cond_logits(xs, lse, params, conv, E, Wg, Wu, Wd, delta, wsp, stream=stream)
             else:
-                dg.dg_denoise_step(xdev[b], params, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv,
-                                   workspace=dws, stream=stream)
-                dg.dg_self_cond_logits(xdev[b], lse, params, conv, E, Wg, Wu, Wd, delta, wsp, stream=stream)
+                step_calls(xdev[b])
             buf_free[b].record(stream)
             out_canvas.copy_(canvas, non_blocking=True)
             out_conv.copy_(conv, non_blocking=True)
@@ -630,8 +649,9 @@ def run_ours(args):
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": _config(wl, fh),
-        "launch": ("CUDA graph replays of the captured step" if graph is not None
-                   else "eager: every call enqueued each step"),
+        "launch": (("CUDA graph replays of the captured step" if graph is not None
+                    else "eager: every call enqueued each step")
+                   + ("; acceptance and samples on a second stream beside the feedback GEMMs" if overlap else "")),
         "roofline": {"bound": "tensor", "achieved": pe_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                      "frac": pe_tflops / peak_tc, "traffic": traffic,
                      "kernel": "P.E contraction (k_gemm softmax-A, N-major B) + split-K fix-up",

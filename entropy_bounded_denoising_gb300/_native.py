@@ -57,6 +57,9 @@ def load(path: str | None = None):
         "dg_denoise_step": (st, [P, ctypes.c_int, i64, i64, i32, i64, P, u64] + [P] * 11 + [P, sz, P]),
         "dg_denoise_stats": (st, [P, ctypes.c_int, i64, i64, i32, i64, P, u64] + [P] * 11 + [P, sz, P]),
         "dg_denoise_samples": (st, [P, ctypes.c_int, i64, i64, i32, i64, P, u64, P, P, P, sz, P]),
+        "dg_denoise_row_stats": (st, [P, ctypes.c_int, i64, i64, i32, i64, P, u64, P, P, P, P, P, sz, P]),
+        "dg_denoise_accept": (st, [P, P, P, i64, i32, i64, P, u64] + [P] * 7 + [P, sz, P]),
+        "dg_self_cond_zero_converged": (st, [P, P, i64, i32, i32, P, P]),
         "dg_denoise_step_choices": (st, [P, ctypes.c_int, i64, i64, i32, i64, P, u64] + [P] * 11
                                     + [P, i32, P] + [P, sz, P]),
         "dg_accept_from_entropy": (st, [P, P, P, i64, i32, i64, P, u64] + [P] * 7 + [P]),
@@ -102,7 +105,8 @@ def load(path: str | None = None):
 def exported_symbols() -> list[str]:
     lib = load()
     return [n for n in ("dg_denoise_workspace_bytes", "dg_denoise_step", "dg_denoise_stats",
-                        "dg_denoise_samples", "dg_denoise_step_choices", "dg_accept_from_entropy", "dg_lm_head_workspace_bytes",
+                        "dg_denoise_samples", "dg_denoise_step_choices", "dg_denoise_row_stats", "dg_denoise_accept",
+                        "dg_self_cond_zero_converged", "dg_accept_from_entropy", "dg_lm_head_workspace_bytes",
                         "dg_lm_head_logits", "dg_lm_head_denoise_step",
                         "dg_canvas_init", "dg_advance_params", "dg_self_cond_workspace_bytes",
                         "dg_self_cond_logits", "dg_self_cond_prepare", "dg_self_cond_pe",
@@ -252,6 +256,35 @@ def dg_denoise_stats(logits, params, seed, canvas, prev_argmax, stable_count, ac
     return _denoise_full("dg_denoise_stats", logits, params, seed, canvas, prev_argmax, stable_count,
                          accept_mask, argmax, sample, entropy, lse, converged, mean_entropy, n_accept,
                          workspace, n_canvas, L, V, ld, stream, check)
+
+
+def dg_denoise_row_stats(logits, params, seed, argmax, sample, entropy, lse, workspace, *, n_canvas=None,
+                         L=None, V=None, ld=None, stream=None, check=True) -> int:
+    """K1 alone: per-position statistics (and DG_SAMPLE_ALL samples) into the given buffers;
+    the workspace then goes to dg_denoise_accept and dg_denoise_samples."""
+    n_canvas, L, V, ld = _denoise_dims(logits, n_canvas, L, V, ld)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = load().dg_denoise_row_stats(_p(logits), _dtype_code(logits), ld, n_canvas, L, V, _p(params),
+                                     int(seed) & 0xFFFFFFFFFFFFFFFF, _p(argmax), _p(sample), _p(entropy),
+                                     _p(lse), _p(workspace), ws_bytes, _s(stream))
+    if check:
+        _check("dg_denoise_row_stats", rc)
+    return rc
+
+
+def dg_denoise_accept(entropy, sample, argmax, params, seed, canvas, prev_argmax, stable_count, accept_mask,
+                      converged, workspace, *, V, mean_entropy=None, n_accept=None, stream=None,
+                      check=True) -> int:
+    """Acceptance, renoise, convergence and the sampler's list after dg_denoise_row_stats."""
+    n_canvas, L = entropy.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = load().dg_denoise_accept(_p(entropy), _p(sample), _p(argmax), n_canvas, L, V, _p(params),
+                                  int(seed) & 0xFFFFFFFFFFFFFFFF, _p(canvas), _p(prev_argmax), _p(stable_count),
+                                  _p(accept_mask), _p(converged), _p(mean_entropy), _p(n_accept),
+                                  _p(workspace), ws_bytes, _s(stream))
+    if check:
+        _check("dg_denoise_accept", rc)
+    return rc
 
 
 def dg_denoise_samples(logits, params, seed, canvas, sample, workspace, *, n_canvas=None, L=None,
@@ -454,6 +487,15 @@ def dg_self_cond_mlp(n_canvas, L, W_gate, W_up, W_down, delta_emb, workspace, st
                                  _p(workspace), ws_bytes, _s(stream))
     if check:
         _check("dg_self_cond_mlp", rc)
+    return rc
+
+
+def dg_self_cond_zero_converged(params, converged, delta_emb, stream=None, check=True) -> int:
+    """Zero the feedback rows of canvases that got feedback and converged (delta_emb [n, L, d])."""
+    n_canvas, L, d = delta_emb.shape
+    rc = load().dg_self_cond_zero_converged(_p(params), _p(converged), n_canvas, L, d, _p(delta_emb), _s(stream))
+    if check:
+        _check("dg_self_cond_zero_converged", rc)
     return rc
 
 

@@ -45,7 +45,8 @@ constexpr int kK1Threads = (kK1Warps + 1) * 32;    // + one producer warp
 constexpr int kSlots = 4;                          // ring of shared-memory slots
 constexpr uint32_t kChunkBytes = 16384;            // deferred sampling: largest bytes of a row per warp item
 constexpr uint32_t kChunkMin = 2048;               // and smallest (one batch of loads per lane)
-constexpr int kDWarps = 8;                         // deferred sampling: warps per CTA
+constexpr int kDWarps = 8;                         // deferred sampling: warps per CTA in line
+constexpr int kSideWarps = 3;                      // and per CTA beside a GEMM on another stream
 constexpr int kDBatch = 4;                         // 16-byte loads in flight per lane
 constexpr int64_t kRunsMaxRows = 512;              // deferred sampling: contiguous runs up to this many rows
 constexpr uint32_t kPieceBytes = 16384;            // bytes per slot
@@ -725,8 +726,10 @@ DG_DEVINL unsigned long long score_key(float score, int idx) {
 // gets at most a few chunks: a second chunk of the same row then costs no second
 // publication); else one chunk per step of a grid-stride loop, so that the warps read one
 // compact window of the list at a time (measured: contiguous runs are slower on long lists).
-template <int DT, bool kRuns>
-__global__ void __launch_bounds__(kDWarps * 32, 3) k1_sample_listed(
+// kW warps per CTA: 8 in line (3 CTAs per SM), 3 beside a GEMM on another stream (96 threads
+// x 80 registers fit next to a P.E CTA's 448 x 128 in an SM's 64 K registers).
+template <int DT, bool kRuns, int kW>
+__global__ void __launch_bounds__(kW * 32, kW == kDWarps ? 3 : 8) k1_sample_listed(
     const unsigned char* __restrict__ logits, int64_t ld_bytes, int64_t V, int32_t L,
     const dg_canvas_params* __restrict__ params, uint64_t seed, DeferredWs ws, int32_t* __restrict__ sample_out,
     int32_t* __restrict__ canvas_out, int64_t rows) {
@@ -735,8 +738,8 @@ __global__ void __launch_bounds__(kDWarps * 32, 3) k1_sample_listed(
     constexpr int GPV = VN / 4;
     static_assert(kChunkMin % (32 * kDBatch * 16) == 0 && kChunkBytes % kChunkMin == 0, "whole batches per chunk");
     const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * kDWarps + (threadIdx.x >> 5);
-    const int64_t nw = (int64_t)gridDim.x * kDWarps;
+    const int64_t gw = (int64_t)blockIdx.x * kW + (threadIdx.x >> 5);
+    const int64_t nw = (int64_t)gridDim.x * kW;
     dg::pdl_wait();
     dg::pdl_release();
     const int count = *ws.count;
@@ -871,14 +874,19 @@ __global__ void __launch_bounds__(kDWarps * 32, 3) k1_sample_listed(
 // ------------------------------------------------------------------------------------
 // K2: acceptance, renoise and convergence for one canvas per CTA (blockDim = 32 * ceil(L/32)).
 // ------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) k2_accept(
+// kMaxT: 256 (up to 256 positions; 32 registers, so that the CTA fits beside a GEMM CTA on
+// another stream) or 1024.  late_release: let the next launch on the stream start only when
+// this grid completes (so that a sampler launched after it cannot take an SM that a GEMM on
+// another stream is about to need).
+template <int kMaxT>
+__global__ void __launch_bounds__(kMaxT, kMaxT <= 256 ? 8 : 1) k2_accept(
     const float* __restrict__ entropy, const int32_t* __restrict__ sample, const int32_t* __restrict__ argmax,
     int32_t L, int64_t V, const dg_canvas_params* __restrict__ params, uint64_t seed, int32_t* __restrict__ canvas,
     int32_t* __restrict__ prev_argmax, int32_t* __restrict__ stable_count, uint8_t* __restrict__ accept_mask,
     uint8_t* __restrict__ converged, float* __restrict__ mean_entropy, int32_t* __restrict__ n_accept,
-    DeferredWs ws, unsigned* status) {
-    __shared__ __align__(16) float sH[1024];
-    __shared__ double sSorted[1024];
+    DeferredWs ws, int late_release, unsigned* status) {
+    __shared__ __align__(16) float sH[kMaxT];
+    __shared__ double sSorted[kMaxT];
     __shared__ double sWarp[32];
     __shared__ int sCut;
     __shared__ int sBase;
@@ -886,7 +894,7 @@ __global__ void __launch_bounds__(1024) k2_accept(
     const int64_t c = blockIdx.x;
     const int i = threadIdx.x, lane = i & 31, warp = i >> 5, nwarps = blockDim.x >> 5;
     dg::pdl_wait();
-    dg::pdl_release();
+    if (!late_release) dg::pdl_release();
     const bool valid = i < L;
     const int64_t q = c * L + i;
     // the per-position loads (and the canvas's stable count) go out with the parameter load:
@@ -1139,24 +1147,28 @@ dg_status launch_k1(const void* logits, int64_t ld, int64_t n, int32_t L, int64_
     return dghost::cuda_status(e);
 }
 
-// Samples and tokens of the listed accepted rows: ctas_per_sm CTAs of kDWarps warps per SM,
-// one warp per 16 KB chunk (the list length is only known on the device).
+// Samples and tokens of the listed accepted rows (the list length is only known on the
+// device): in line, 3 CTAs of kDWarps warps per SM; beside (for another stream), one CTA of
+// kSideWarps warps per SM, small enough to share an SM with a GEMM CTA.
 template <int DT>
 dg_status launch_kd(const void* logits, int64_t ld, int64_t n, int32_t L, int64_t V,
                     const dg_canvas_params* params, uint64_t seed, const DeferredWs& ws, int32_t* sample,
-                    int32_t* canvas, int ctas_per_sm, cudaStream_t stream) {
+                    int32_t* canvas, bool beside, cudaStream_t stream) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return DG_ERR_CUDA;
     const int64_t cpr = (V * (DT == 0 ? 2 : 4) + kChunkBytes - 1) / kChunkBytes;
     const int64_t max_items = n * (int64_t)L * cpr;
-    const unsigned grid =
-        (unsigned)std::max<int64_t>(1, std::min<int64_t>((int64_t)ctas_per_sm * sms, (max_items + kDWarps - 1) / kDWarps));
+    const int warps = beside ? kSideWarps : kDWarps;
+    const unsigned grid = (unsigned)std::max<int64_t>(
+        1, std::min<int64_t>((int64_t)(beside ? 1 : 3) * sms, (max_items + warps - 1) / warps));
     const int64_t ld_bytes = ld * (DT == 0 ? 2 : 4);
     // few rows (a single request): contiguous runs per warp; else single chunks
-    auto kern = n * (int64_t)L <= kRunsMaxRows ? k1_sample_listed<DT, true> : k1_sample_listed<DT, false>;
-    const cudaError_t e = dghost::launch_pdl(kern, dim3(grid), dim3(kDWarps * 32), 0, stream,
+    const bool runs = n * (int64_t)L <= kRunsMaxRows;
+    auto kern = beside ? (runs ? k1_sample_listed<DT, true, kSideWarps> : k1_sample_listed<DT, false, kSideWarps>)
+                       : (runs ? k1_sample_listed<DT, true, kDWarps> : k1_sample_listed<DT, false, kDWarps>);
+    const cudaError_t e = dghost::launch_pdl(kern, dim3(grid), dim3(warps * 32), 0, stream,
                                              static_cast<const unsigned char*>(logits), ld_bytes, V, L, params, seed,
                                              ws, sample, canvas, n * (int64_t)L);
     dghost::count_launch();
@@ -1166,12 +1178,13 @@ dg_status launch_kd(const void* logits, int64_t ld, int64_t n, int32_t L, int64_
 dg_status launch_k2(const float* entropy, const int32_t* sample, const int32_t* argmax, int64_t n, int32_t L,
                     int64_t V, const dg_canvas_params* params, uint64_t seed, int32_t* canvas, int32_t* prev_argmax,
                     int32_t* stable_count, uint8_t* accept_mask, uint8_t* converged, float* mean_entropy,
-                    int32_t* n_accept, const DeferredWs& ws, cudaStream_t stream) {
+                    int32_t* n_accept, const DeferredWs& ws, cudaStream_t stream, bool late_release = false) {
     const unsigned threads = (unsigned)((L + 31) / 32 * 32);
-    const cudaError_t e = dghost::launch_pdl(k2_accept, dim3((unsigned)n), dim3(threads), 0, stream, entropy, sample,
+    auto kern = threads <= 256 ? k2_accept<256> : k2_accept<1024>;
+    const cudaError_t e = dghost::launch_pdl(kern, dim3((unsigned)n), dim3(threads), 0, stream, entropy, sample,
                                              argmax, L, V, params, seed, canvas, prev_argmax, stable_count,
                                              accept_mask, converged, mean_entropy, n_accept, ws,
-                                             dghost::status_word());
+                                             late_release ? 1 : 0, dghost::status_word());
     dghost::count_launch();
     return dghost::cuda_status(e);
 }
@@ -1273,9 +1286,49 @@ dg_status dg_denoise_stats(const void* logits, dg_dtype dtype, int64_t ld, int64
                          workspace, workspace_bytes, stream);
 }
 
+dg_status dg_denoise_row_stats(const void* logits, dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L, int64_t V,
+                               const dg_canvas_params* params, uint64_t seed, int32_t* argmax, int32_t* sample,
+                               float* entropy, float* lse, void* workspace, size_t workspace_bytes,
+                               dg_stream_t stream) {
+    if (dtype != DG_BF16 && dtype != DG_FP32) return DG_ERR_INVALID_ARG;
+    dg_status s = check_canvas_dims(n_canvas, L, V);
+    if (s != DG_OK) return s;
+    if (ld < V) return DG_ERR_INVALID_ARG;
+    if (n_canvas == 0) return DG_OK;
+    if (!logits || !params || !argmax || !sample || !entropy || !lse) return DG_ERR_INVALID_ARG;
+    const int64_t es = dtype == DG_BF16 ? 2 : 4;
+    if (!aligned16(logits) || (ld * es) % 16 != 0) return DG_ERR_ALIGNMENT;
+    if (!k1_supported(dtype, V)) return DG_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < dg_denoise_workspace_bytes(n_canvas, L, V, dtype)) return DG_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 7u) != 0) return DG_ERR_ALIGNMENT;
+    const DeferredWs ws = carve_ws(workspace, n_canvas * (int64_t)L);
+    cudaStream_t st = (cudaStream_t)stream;
+    return dtype == DG_BF16
+               ? launch_k1<0>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, ws, ChoiceOut{}, st)
+               : launch_k1<1>(logits, ld, n_canvas, L, V, params, seed, argmax, sample, entropy, lse, ws, ChoiceOut{}, st);
+}
+
+dg_status dg_denoise_accept(const float* entropy, const int32_t* sample, const int32_t* argmax, int64_t n_canvas,
+                            int32_t L, int64_t V, const dg_canvas_params* params, uint64_t seed, int32_t* canvas,
+                            int32_t* prev_argmax, int32_t* stable_count, uint8_t* accept_mask, uint8_t* converged,
+                            float* mean_entropy, int32_t* n_accept, void* workspace, size_t workspace_bytes,
+                            dg_stream_t stream) {
+    dg_status s = check_canvas_dims(n_canvas, L, V);
+    if (s != DG_OK) return s;
+    if (n_canvas == 0) return DG_OK;
+    if (!entropy || !sample || !argmax || !params || !canvas || !prev_argmax || !stable_count || !accept_mask ||
+        !converged)
+        return DG_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < dg_denoise_workspace_bytes(n_canvas, L, V, DG_BF16)) return DG_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 7u) != 0) return DG_ERR_ALIGNMENT;
+    const DeferredWs ws = carve_ws(workspace, n_canvas * (int64_t)L);
+    return launch_k2(entropy, sample, argmax, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
+                     accept_mask, converged, mean_entropy, n_accept, ws, (cudaStream_t)stream, true);
+}
+
 static dg_status denoise_samples(const void* logits, dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L,
                                  int64_t V, const dg_canvas_params* params, uint64_t seed, int32_t* canvas,
-                                 int32_t* sample, void* workspace, size_t workspace_bytes, int ctas_per_sm,
+                                 int32_t* sample, void* workspace, size_t workspace_bytes, bool beside,
                                  cudaStream_t st) {
     if (dtype != DG_BF16 && dtype != DG_FP32) return DG_ERR_INVALID_ARG;
     dg_status s = check_canvas_dims(n_canvas, L, V);
@@ -1290,15 +1343,15 @@ static dg_status denoise_samples(const void* logits, dg_dtype dtype, int64_t ld,
     if ((reinterpret_cast<uintptr_t>(workspace) & 7u) != 0) return DG_ERR_ALIGNMENT;
     const DeferredWs ws = carve_ws(workspace, n_canvas * (int64_t)L);
     return dtype == DG_BF16
-               ? launch_kd<0>(logits, ld, n_canvas, L, V, params, seed, ws, sample, canvas, ctas_per_sm, st)
-               : launch_kd<1>(logits, ld, n_canvas, L, V, params, seed, ws, sample, canvas, ctas_per_sm, st);
+               ? launch_kd<0>(logits, ld, n_canvas, L, V, params, seed, ws, sample, canvas, beside, st)
+               : launch_kd<1>(logits, ld, n_canvas, L, V, params, seed, ws, sample, canvas, beside, st);
 }
 
 dg_status dg_denoise_samples(const void* logits, dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L, int64_t V,
                              const dg_canvas_params* params, uint64_t seed, int32_t* canvas, int32_t* sample,
                              void* workspace, size_t workspace_bytes, dg_stream_t stream) {
     return denoise_samples(logits, dtype, ld, n_canvas, L, V, params, seed, canvas, sample, workspace,
-                           workspace_bytes, 1, (cudaStream_t)stream);
+                           workspace_bytes, true, (cudaStream_t)stream);
 }
 
 dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L, int64_t V,
@@ -1310,9 +1363,9 @@ dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld, int64_
                                 accept_mask, argmax, sample, entropy, lse, converged, mean_entropy, n_accept,
                                 ChoiceOut{}, workspace, workspace_bytes, stream);
     if (s != DG_OK || n_canvas == 0) return s;
-    // alone on its stream: three CTAs per SM hide more of the load latency
+    // alone on its stream: three CTAs of 8 warps per SM hide more of the load latency
     return denoise_samples(logits, dtype, ld, n_canvas, L, V, params, seed, canvas, sample, workspace,
-                           workspace_bytes, 3, (cudaStream_t)stream);
+                           workspace_bytes, false, (cudaStream_t)stream);
 }
 
 dg_status dg_denoise_step_choices(const void* logits, dg_dtype dtype, int64_t ld, int64_t n_canvas, int32_t L,
@@ -1328,7 +1381,7 @@ dg_status dg_denoise_step_choices(const void* logits, dg_dtype dtype, int64_t ld
                                 ChoiceOut{choices, probs, C}, workspace, workspace_bytes, stream);
     if (s != DG_OK || n_canvas == 0) return s;
     return denoise_samples(logits, dtype, ld, n_canvas, L, V, params, seed, canvas, sample, workspace,
-                           workspace_bytes, 3, (cudaStream_t)stream);
+                           workspace_bytes, false, (cudaStream_t)stream);
 }
 
 size_t dg_lm_head_workspace_bytes(int64_t n_canvas, int32_t L, int64_t V) {
@@ -1378,7 +1431,7 @@ dg_status dg_lm_head_denoise_step(const uint16_t* hidden, int64_t ldh, const uin
     s = launch_k2(entropy, sample, argmax, n_canvas, L, V, params, seed, canvas, prev_argmax, stable_count,
                   accept_mask, converged, mean_entropy, n_accept, ws, st);
     if (s != DG_OK) return s;
-    return launch_kd<0>(logits, ld, n_canvas, L, V, params, seed, ws, sample, canvas, 3, st);
+    return launch_kd<0>(logits, ld, n_canvas, L, V, params, seed, ws, sample, canvas, false, st);
 }
 
 dg_status dg_accept_from_entropy(const float* entropy, const int32_t* sample, const int32_t* argmax,

@@ -927,6 +927,21 @@ __global__ void k_zero_rows(const dg_canvas_params* __restrict__ params, const u
         row[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
+// The feedback rows of canvases that got feedback although they converged this step (the
+// feedback was computed before the convergence was known): zeroed, as if planned without
+// them.  Grid (CTAs per canvas, canvases).
+__global__ void k_zero_converged(const dg_canvas_params* __restrict__ params, const uint8_t* __restrict__ converged,
+                                 int32_t L, int32_t d, uint16_t* __restrict__ delta) {
+    dg::pdl_wait();
+    dg::pdl_release();
+    const int64_t c = blockIdx.y;
+    if (!self_cond_on(params[c], nullptr, c) || !converged[c]) return;
+    const int64_t vecs = (int64_t)L * d / 8;
+    uint4* row = reinterpret_cast<uint4*>(delta + c * (int64_t)L * d);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < vecs; i += (int64_t)gridDim.x * blockDim.x)
+        row[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // ------------------------------------------------------------------ host side
 // Pipeline depths (shared-memory stages) of the self-conditioning GEMMs.
 #ifndef DG_PE_STAGES
@@ -1274,6 +1289,22 @@ dg_status dg_self_cond_prepare(const dg_canvas_params* params, const uint8_t* co
     dim3 grid((unsigned)per_canvas, (unsigned)n_canvas);
     const cudaError_t e = dghost::launch_pdl(k_zero_rows, grid, dim3(256), 0, st, params, converged, n_canvas, L, d,
                                              delta_emb, plan);
+    dghost::count_launch();
+    return dghost::cuda_status(e);
+}
+
+dg_status dg_self_cond_zero_converged(const dg_canvas_params* params, const uint8_t* converged, int64_t n_canvas,
+                                      int32_t L, int32_t d, uint16_t* delta_emb, dg_stream_t stream) {
+    if (n_canvas < 0 || n_canvas > 65535 || L < 1 || L > 1024 || d < 8 || d > 65536 || (d % 8))
+        return DG_ERR_INVALID_ARG;
+    if (n_canvas == 0) return DG_OK;
+    if (!params || !converged || !delta_emb) return DG_ERR_INVALID_ARG;
+    if (!aligned16(delta_emb)) return DG_ERR_ALIGNMENT;
+    const int P = std::max(1, dghost::sm_count());
+    const int64_t per_canvas = std::max<int64_t>(1, std::min<int64_t>(((int64_t)L * d / 8 + 255) / 256,
+                                                                      (4LL * P + n_canvas - 1) / n_canvas));
+    const cudaError_t e = dghost::launch_pdl(k_zero_converged, dim3((unsigned)per_canvas, (unsigned)n_canvas),
+                                             dim3(256), 0, (cudaStream_t)stream, params, converged, L, d, delta_emb);
     dghost::count_launch();
     return dghost::cuda_status(e);
 }

@@ -178,9 +178,10 @@ DG_API dg_status dg_denoise_step(const void* logits, dg_dtype dtype, int64_t ld,
  *                       DG_SAMPLE_ALL in the workspace (their sample and canvas entries are
  *                       written by dg_denoise_samples);
  *   dg_denoise_samples: the Gumbel-max samples of the listed positions, written to sample
- *                       and canvas.  It launches at most one CTA per SM (of 256 threads and
- *                       80 registers, no shared memory), so that it can share SMs with a
- *                       GEMM running on another stream.
+ *                       and canvas.  It launches at most one CTA per SM (of 96 threads and
+ *                       at most 80 registers, no shared memory), so that it can share SMs
+ *                       with a GEMM running on another stream (a P.E CTA of 448 threads x
+ *                       128 registers leaves room for it).
  * dg_denoise_samples must follow dg_denoise_stats of the same step (an event on the stats'
  * stream when it runs on another stream), with the same logits, params, seed, sizes and
  * workspace, and complete before the canvas or the workspace is used again (by the caller or
@@ -223,6 +224,34 @@ DG_API dg_status dg_denoise_step_choices(const void* logits, dg_dtype dtype, int
                                          float* mean_entropy, int32_t* n_accept,
                                          const int32_t* choices, int32_t C, float* probs,
                                          void* workspace, size_t workspace_bytes, dg_stream_t stream);
+
+/* dg_denoise_stats in two calls, so that the acceptance (and then dg_denoise_samples) can run
+ * on another stream while the self-conditioning feedback, which needs only lse, starts:
+ *   dg_denoise_row_stats: per-position entropy, lse, argmax (and the samples of DG_SAMPLE_ALL
+ *                         canvases; -1 elsewhere), each row's maximum recorded in the
+ *                         workspace and the workspace's list cleared;
+ *   dg_denoise_accept:    acceptance, renoise, convergence and the list of accepted positions
+ *                         (exactly the second half of dg_denoise_stats, on the outputs of
+ *                         dg_denoise_row_stats and the same workspace).  The next launch on its
+ *                         stream starts only when it completes; up to 256 positions its CTAs
+ *                         use 256 threads and at most 32 registers, so that each fits on an
+ *                         SM beside a feedback GEMM CTA.
+ * In order (dg_denoise_row_stats, dg_denoise_accept, dg_denoise_samples, with the same
+ * logits, params, seed, sizes and workspace) they produce exactly dg_denoise_step's outputs.
+ * Arguments, limits and errors are those of dg_denoise_step (dg_denoise_accept checks the
+ * workspace size as for bf16 logits, which is the same for every dtype). */
+DG_API dg_status dg_denoise_row_stats(const void* logits, dg_dtype dtype, int64_t ld,
+                                      int64_t n_canvas, int32_t L, int64_t V,
+                                      const dg_canvas_params* params, uint64_t seed,
+                                      int32_t* argmax, int32_t* sample, float* entropy, float* lse,
+                                      void* workspace, size_t workspace_bytes, dg_stream_t stream);
+DG_API dg_status dg_denoise_accept(const float* entropy, const int32_t* sample, const int32_t* argmax,
+                                   int64_t n_canvas, int32_t L, int64_t V,
+                                   const dg_canvas_params* params, uint64_t seed,
+                                   int32_t* canvas, int32_t* prev_argmax, int32_t* stable_count,
+                                   uint8_t* accept_mask, uint8_t* converged,
+                                   float* mean_entropy, int32_t* n_accept,
+                                   void* workspace, size_t workspace_bytes, dg_stream_t stream);
 
 /* The per-canvas half of the step (acceptance, renoise, convergence) on caller-given
  * per-position entropy, sample and argmax, all (device) [n_canvas][L].  Same semantics and
@@ -385,6 +414,20 @@ DG_API dg_status dg_self_cond_mlp(int64_t n_canvas, int32_t L, int32_t d, int32_
                                   const uint16_t* W_gate, const uint16_t* W_up,
                                   const uint16_t* W_down, uint16_t* delta_emb, void* workspace,
                                   size_t workspace_bytes, dg_stream_t stream);
+
+/* For a feedback started before the step's convergence was known (dg_self_cond_prepare with
+ * converged = NULL, while dg_denoise_accept runs on another stream): zeroes the delta_emb
+ * rows of every canvas that got feedback (DG_ACTIVE and DG_SELF_COND, not DG_READ_ONLY) and
+ * has converged[c] = 1, which makes delta_emb exactly what dg_self_cond_logits with that
+ * converged array writes.  Call it on the feedback's stream after dg_self_cond_mlp, once the
+ * converged array is complete (an event from the acceptance's stream).
+ *   params (device) [n_canvas]; converged (device) [n_canvas] uint8;
+ *   delta_emb (device, in/out) bf16 [n_canvas][L][d], 16-byte aligned.
+ * Limits: L <= 1024, d a multiple of 8 in [8, 65536], n_canvas <= 65535 (0 launches nothing).
+ * Errors: DG_ERR_INVALID_ARG, DG_ERR_ALIGNMENT, DG_ERR_CUDA. */
+DG_API dg_status dg_self_cond_zero_converged(const dg_canvas_params* params, const uint8_t* converged,
+                                             int64_t n_canvas, int32_t L, int32_t d,
+                                             uint16_t* delta_emb, dg_stream_t stream);
 
 /* Workspace for dg_self_cond_probs. */
 DG_API size_t dg_self_cond_probs_workspace_bytes(int64_t n_rows, int32_t d, int32_t h);

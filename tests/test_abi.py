@@ -67,6 +67,19 @@ def test_host_validation_without_gpu():
     assert lib.dg_denoise_step_choices(18, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), 16, 4, 16, 256, 768, None) == dg.DG_ERR_ALIGNMENT
     assert lib.dg_denoise_step_choices(16, 0, 8, 1, 16, 8, 16, 0, *([16] * 11), 16, 4, 16, None, 0, None) == dg.DG_ERR_WORKSPACE
     assert lib.dg_denoise_step_choices(None, 0, 8, 0, 16, 8, None, 0, *([None] * 11), None, 4, None, None, 0, None) == dg.DG_OK
+    # the staged statistics / acceptance calls and the converged-row zeroing
+    assert lib.dg_denoise_row_stats(16, 0, 8, 1, 16, 8, 16, 0, 16, 16, 16, None, 256, 768, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_denoise_row_stats(18, 0, 8, 1, 16, 8, 16, 0, 16, 16, 16, 16, 256, 768, None) == dg.DG_ERR_ALIGNMENT
+    assert lib.dg_denoise_row_stats(16, 0, 8, 1, 16, 8, 16, 0, 16, 16, 16, 16, 256, 640, None) == dg.DG_ERR_WORKSPACE
+    assert lib.dg_denoise_row_stats(None, 0, 8, 0, 16, 8, None, 0, None, None, None, None, None, 0, None) == dg.DG_OK
+    assert lib.dg_denoise_accept(16, 16, 16, 1, 16, 8, 16, 0, *([16] * 4), None, None, None, 256, 768, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_denoise_accept(16, 16, 16, 1, 16, 8, 16, 0, *([16] * 5), None, None, 256, 640, None) == dg.DG_ERR_WORKSPACE
+    assert lib.dg_denoise_accept(16, 16, 16, 1, 16, 8, 16, 0, *([16] * 5), None, None, 260, 768, None) == dg.DG_ERR_ALIGNMENT
+    assert lib.dg_denoise_accept(16, 16, 16, 1, 2000, 8, 16, 0, *([16] * 5), None, None, 256, 768, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_self_cond_zero_converged(16, 16, 1, 16, 12, 16, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_self_cond_zero_converged(16, None, 1, 16, 16, 16, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_self_cond_zero_converged(16, 16, 1, 16, 16, 18, None) == dg.DG_ERR_ALIGNMENT
+    assert lib.dg_self_cond_zero_converged(None, None, 0, 16, 16, None, None) == dg.DG_OK
     # the bounded-wait probe: poll limits outside 1..65536, a null or misaligned result
     assert lib.dg_probe_bounded_wait(0, 16, None) == dg.DG_ERR_INVALID_ARG
     assert lib.dg_probe_bounded_wait(65537, 16, None) == dg.DG_ERR_INVALID_ARG

@@ -352,10 +352,10 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=dev) if args.graph else torch.cuda.current_stream()
     stream.wait_stream(torch.cuda.current_stream())
     seed = 0x5EED0000 + rank
-    # Small batches (a single request) run the overlapped schedule: the acceptance and the
-    # deferred samples on a second stream while the feedback GEMMs, which need only the
-    # step's lse, start at once; the rows of canvases that converged are zeroed afterwards
-    # (bit-identical outputs, tests/test_gpu_schedule.py).  Larger batches keep every launch
+    # Small batches (a single request) run the overlapped schedule: the feedback, which needs
+    # only the step's lse, starts right after the statistics pass; the acceptance and the
+    # deferred samples run on a second stream beside the MLP GEMMs; the rows of canvases that
+    # converged are zeroed at the end (bit-identical outputs, tests/test_gpu_schedule.py).  Larger batches keep every launch
     # on one stream (measured faster: the second stream's sampler slows P.E more than it saves).
     overlap = not fh and n * L <= 512
     side = torch.cuda.Stream(device=dev) if overlap else None
@@ -369,11 +369,6 @@ def run_ours(args):
                                        conv, workspace=lws, stream=stream)
         elif overlap:
             dg.dg_denoise_row_stats(xin, params, seed, am, smp, ent, lse, dws, stream=stream)
-            ev_fork.record(stream)
-            side.wait_event(ev_fork)
-            dg.dg_denoise_accept(ent, smp, am, params, seed, canvas, prev, stable, acc, conv, dws, V=V, stream=side)
-            dg.dg_denoise_samples(xin, params, seed, canvas, smp, dws, stream=side)
-            ev_join.record(side)
         else:
             dg.dg_denoise_step(xin, params, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv,
                                workspace=dws, stream=stream)
@@ -381,6 +376,14 @@ def run_ours(args):
         if ev:
             ev[1].record(stream)
         dg.dg_self_cond_pe(xs if fh else xin, lse, params, E, h, wsp, stream=stream)
+        if overlap:
+            # forked once P.E is done: the acceptance and the samples then share the SMs with
+            # the MLP GEMMs (which leave some idle) instead of taking an SM that P.E needs
+            ev_fork.record(stream)
+            side.wait_event(ev_fork)
+            dg.dg_denoise_accept(ent, smp, am, params, seed, canvas, prev, stable, acc, conv, dws, V=V, stream=side)
+            dg.dg_denoise_samples(xin, params, seed, canvas, smp, dws, stream=side)
+            ev_join.record(side)
         if ev:
             ev[2].record(stream)
         dg.dg_self_cond_mlp(n, L, Wg, Wu, Wd, delta, wsp, stream=stream)

@@ -180,18 +180,23 @@ DG_DEVINL int active_splits(const GemmArgs& a, int mt) {
     return plan_splits(per_split, mt, a.n_tiles, a.k_blocks, a.clusters, a.min_slice, a.max_slots, a.split_below);
 }
 
+// Group counts stay far below 2^32 (k-slices x n-tiles x m-groups), so the indices are split
+// in 32-bit arithmetic: a 64-bit division is a long emulated sequence, paid by every warp role
+// before its first item.
 DG_DEVINL Item decode(const GemmArgs& a, int mt, int cm, int rank, int64_t G, int splits) {
-    const int64_t mgc = (mt + cm - 1) / cm;
-    const int64_t per_s = (int64_t)a.n_tiles * mgc;
-    const int s = (int)(G / per_s);
-    const int64_t rem = G % per_s;
+    const uint32_t mgc = (uint32_t)((mt + cm - 1) / cm);
+    const uint32_t per_s = (uint32_t)a.n_tiles * mgc;
+    const uint32_t g = (uint32_t)G;
+    const int s = (int)(g / per_s);
+    const uint32_t rem = g - (uint32_t)s * per_s;
     Item it;
     it.n = (int)(rem / mgc);
-    it.m = (int)(rem % mgc) * cm + rank;
+    it.m = (int)(rem - (uint32_t)it.n * mgc) * cm + rank;
     it.valid = it.m < mt;
     it.m_load = it.valid ? it.m : mt - 1;
-    it.kb_lo = (int)((int64_t)s * a.k_blocks / splits);
-    it.kb_hi = (int)((int64_t)(s + 1) * a.k_blocks / splits);
+    // (s + 1) * k_blocks <= 33 * 2^26 < 2^32: unsigned 32-bit
+    it.kb_lo = (int)((uint32_t)s * (uint32_t)a.k_blocks / (uint32_t)splits);
+    it.kb_hi = (int)((uint32_t)(s + 1) * (uint32_t)a.k_blocks / (uint32_t)splits);
     it.w = (int64_t)s * mt * a.n_tiles + (int64_t)it.n * mt + it.m;
     return it;
 }
@@ -786,7 +791,7 @@ __global__ void __launch_bounds__(256, GU ? 1 : 4) k_fixup(const GemmArgs a) {
     const int64_t T = (int64_t)mt * a.n_tiles;
     const int64_t t = blockIdx.x;
     if (t >= T) return;
-    const int n = (int)(t / mt), m = (int)(t % mt);
+    const int n = (int)((uint32_t)t / (uint32_t)mt), m = (int)((uint32_t)t - (uint32_t)n * (uint32_t)mt);
     constexpr bool gu = GU;  // a.epi == EPI_GELU_GATEUP
     const int out_cols = gu ? BN / 2 : BN;
     const int quads = BM * out_cols / 4;

@@ -1,10 +1,10 @@
 """The overlapped launch schedule of one step against the in-line one, through the C ABI.
 
 In line: dg_denoise_step, then dg_self_cond_logits with the step's converged flags.
-Overlapped (what the benchmark runs for small batches): dg_denoise_row_stats on the main
-stream; dg_denoise_accept and dg_denoise_samples on a second stream; meanwhile
-dg_self_cond_prepare with converged = NULL, dg_self_cond_pe and dg_self_cond_mlp on the main
-stream; then, after an event from the second stream, dg_self_cond_zero_converged.  Every
+Overlapped (what the benchmark runs for small batches): on the main stream
+dg_denoise_row_stats, dg_self_cond_prepare with converged = NULL and dg_self_cond_pe; then
+dg_denoise_accept and dg_denoise_samples on a second stream while dg_self_cond_mlp runs on the
+main one; then, after an event from the second stream, dg_self_cond_zero_converged.  Every
 output (canvas, state, statistics, samples, acceptance, convergence and the feedback rows)
 must be bit-identical: the schedule moves launches, not arithmetic.  Cases: a mixed batch
 (feedback, a canvas converging this step, read-only, inactive and DG_SAMPLE_ALL canvases;
@@ -32,15 +32,15 @@ def _run(x, pt, seed, b, delta, ws_d, ws_s, weights, V, overlapped, main, side):
         dg.dg_self_cond_logits(x, b.lse, pt, b.converged, E, Wg, Wu, Wd, delta, ws_s, V=V, stream=main)
         return
     dg.dg_denoise_row_stats(x, pt, seed, b.argmax, b.sample, b.entropy, b.lse, ws_d, V=V, stream=main)
-    stats_done, accept_done = torch.cuda.Event(), torch.cuda.Event()
-    stats_done.record(main)
-    side.wait_event(stats_done)
+    fork, accept_done = torch.cuda.Event(), torch.cuda.Event()
+    dg.dg_self_cond_prepare(pt, None, n, L, delta.shape[2], h, delta, ws_s, stream=main)
+    dg.dg_self_cond_pe(x, b.lse, pt, E, h, ws_s, V=V, stream=main)
+    fork.record(main)
+    side.wait_event(fork)
     dg.dg_denoise_accept(b.entropy, b.sample, b.argmax, pt, seed, b.canvas, b.prev, b.stable, b.accept,
                          b.converged, ws_d, V=V, mean_entropy=b.mean_entropy, n_accept=b.n_accept, stream=side)
     dg.dg_denoise_samples(x, pt, seed, b.canvas, b.sample, ws_d, V=V, stream=side)
     accept_done.record(side)
-    dg.dg_self_cond_prepare(pt, None, n, L, delta.shape[2], h, delta, ws_s, stream=main)
-    dg.dg_self_cond_pe(x, b.lse, pt, E, h, ws_s, V=V, stream=main)
     dg.dg_self_cond_mlp(n, L, Wg, Wu, Wd, delta, ws_s, stream=main)
     main.wait_event(accept_done)
     dg.dg_self_cond_zero_converged(pt, b.converged, delta, stream=main)

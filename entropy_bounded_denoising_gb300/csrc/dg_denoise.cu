@@ -743,14 +743,18 @@ __global__ void __launch_bounds__(kW * 32, kW == kDWarps ? 3 : 8) k1_sample_list
     dg::pdl_wait();
     dg::pdl_release();
     const int count = *ws.count;
-    // chunk size: every warp computes the same one from the list length
-    const int64_t row_bytes = V * ES;
-    const int64_t want = ((int64_t)count * row_bytes) / (2 * nw);
+    // chunk size: every warp computes the same one from the list length (in float: the size
+    // only cuts the work, the result does not depend on it; 64-bit divisions are long
+    // emulated sequences)
+    const int64_t row_bytes = V * ES;  // < 2^31
+    const float want = (float)count * (float)row_bytes / (float)(2 * nw);
     const uint32_t chunk_bytes =
-        (uint32_t)min((int64_t)kChunkBytes, max((int64_t)kChunkMin, (want + kChunkMin - 1) / kChunkMin * kChunkMin));
+        want >= (float)kChunkBytes ? kChunkBytes
+                                   : max(kChunkMin, ((uint32_t)want + kChunkMin - 1) / kChunkMin * kChunkMin);
     const int kChunkElems = (int)(chunk_bytes / ES);
-    const int cpr = (int)((row_bytes + chunk_bytes - 1) / chunk_bytes);  // chunks per row
+    const int cpr = (int)(((uint32_t)row_bytes + chunk_bytes - 1) / chunk_bytes);  // chunks per row
     const int64_t items = (int64_t)count * cpr;
+    const bool items32 = items <= 0xffffffffLL;  // item indices split in 32-bit arithmetic
     // One row segment: chunks [c_lo, c_hi) of list entry w, searched and published (the
     // winner into the row's key, the chunks into its count; the warp that completes the count
     // writes the sample and token).
@@ -759,7 +763,7 @@ __global__ void __launch_bounds__(kW * 32, kW == kDWarps ? 3 : 8) k1_sample_list
         const int64_t row = e.x;
         const bool in_range = (uint64_t)row < (uint64_t)rows;  // entries come from K2; checked anyway
         const float m = __int_as_float(e.y);
-        const int64_t canvas = in_range ? row / L : 0;
+        const int64_t canvas = in_range ? (int64_t)((uint32_t)row / (uint32_t)L) : 0;  // row < n L < 2^26
         const dg_canvas_params p = params[canvas];
         const bool ok = in_range && isfinite(m);  // else a NaN / inf / empty row (flagged by the statistics pass)
         float best = -INFINITY;
@@ -853,16 +857,19 @@ __global__ void __launch_bounds__(kW * 32, kW == kDWarps ? 3 : 8) k1_sample_list
         }
         __syncwarp();
     };
+    auto row_of = [&](int64_t it) {
+        return items32 ? (int)((uint32_t)it / (uint32_t)cpr) : (int)(it / cpr);
+    };
     if constexpr (!kRuns) {
         for (int64_t it = gw; it < items; it += nw) {
-            const int w = (int)(it / cpr);
+            const int w = row_of(it);
             const int c = (int)(it - (int64_t)w * cpr);
             segment(w, c, c + 1);
         }
     } else {
         const int64_t per = (items + nw - 1) / nw;
         for (int64_t it = gw * per, it1 = min(items, gw * per + per); it < it1;) {
-            const int w = (int)(it / cpr);
+            const int w = row_of(it);
             const int c_lo = (int)(it - (int64_t)w * cpr);
             const int c_hi = (int)min((int64_t)cpr, (int64_t)c_lo + (it1 - it));
             it += c_hi - c_lo;

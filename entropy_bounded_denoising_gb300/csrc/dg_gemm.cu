@@ -75,6 +75,9 @@ struct GemmArgs {
     int32_t min_slice;      // k-blocks
     int64_t max_slots;      // partial tiles the workspace holds
     int32_t split_below;    // split only below this round efficiency (percent)
+    // P.E: a counter of work items whose loads the CTAs' producers have issued (zeroed by
+    // the plan launch), used to keep the clusters' items in step (see pace_wait); null: none
+    unsigned* pace;
     // the same rule tabulated by the host for plans listing j <= kSplitTab canvases
     // (split_tab[j]); larger plans evaluate it on the device
     uint8_t split_tab[260];
@@ -199,6 +202,23 @@ DG_DEVINL Item decode(const GemmArgs& a, int mt, int cm, int rank, int64_t G, in
     it.kb_hi = (int)((uint32_t)(s + 1) * (uint32_t)a.k_blocks / (uint32_t)splits);
     it.w = (int64_t)s * mt * a.n_tiles + (int64_t)it.n * mt + it.m;
     return it;
+}
+
+// Keeps the clusters of a persistent P.E launch in step: before loading its item j, a CTA's
+// producer waits until every CTA has issued the loads of its item j - 1 (items go round-robin,
+// so if any cluster has an item j every cluster had items 0 .. j - 1).  Items of one round
+// share their logits and embedding k-blocks through L2 only while the clusters stream them at
+// about the same time; left alone, they drift apart over a launch and most re-reads miss.
+// Only the timing depends on it: an expired wait raises DG_DEV_TIMEOUT and goes on.
+#ifndef DG_PE_PACE
+#define DG_PE_PACE 1
+#endif
+DG_DEVINL void pace_wait(const unsigned* ctr, unsigned target, unsigned* status) {
+    for (uint32_t i = 0; i < (1u << 20); ++i) {
+        if (*(volatile const unsigned*)ctr >= target) return;
+        __nanosleep(128);
+    }
+    dg::raise_status(status, DG_DEV_TIMEOUT);
 }
 
 DG_DEVINL int canvas_of(const GemmArgs& a, int m) {
@@ -468,8 +488,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             dg::prefetch_tmap(&tmB0);
             if (C::kBMode == B_KMAJOR_GATEUP) dg::prefetch_tmap(&tmB1);
             uint32_t it = 0;
-            for (int64_t G = cid; G < n_groups && !aborted(sh); G += ncl) {
+            const bool pace = DG_PE_PACE && C::kXform && a.pace != nullptr;
+            unsigned item_no = 0;
+            for (int64_t G = cid; G < n_groups && !aborted(sh); G += ncl, ++item_no) {
                 const Item im = decode(a, mt, cm, rank, G, splits);
+                if (pace && item_no > 0) pace_wait(a.pace, item_no * gridDim.x, a.status);
                 int cz = 0, crow = 0;
                 if (C::kXform || C::kAMode == A_TMA_CANVAS) {
                     cz = canvas_of(a, im.m_load);
@@ -520,6 +543,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                         dg::tma_load_2d(sB + (C::BN / 2) * C::BK * 2, &tmB1, k0, im.n * (C::BN / 2), &sh.full[s]);
                     }
                 }
+                if (pace) atomicAdd(a.pace, 1u);
             }
             // never leave with a copy still landing in this CTA's shared memory
             if (aborted(sh)) {
@@ -915,15 +939,18 @@ __global__ void k_plan(const dg_canvas_params* __restrict__ params, const uint8_
     plan_list(params, converged, n, plan, mode);
 }
 
-// The feedback plan (block (0, 0), as k_plan mode 0) and the zeroing of the feedback rows of
-// canvases that get none this step: grid (CTAs per canvas, canvases), 16-byte stores (d is a
-// multiple of 8 and delta_emb 16-byte aligned).
+// The feedback plan (block (0, 0), as k_plan mode 0; it also zeroes P.E's pacing counter) and
+// the zeroing of the feedback rows of canvases that get none this step: grid (CTAs per canvas,
+// canvases), 16-byte stores (d is a multiple of 8 and delta_emb 16-byte aligned).
 __global__ void k_zero_rows(const dg_canvas_params* __restrict__ params, const uint8_t* __restrict__ converged,
                             int64_t n, int32_t L, int32_t d, uint16_t* __restrict__ delta,
-                            int32_t* __restrict__ plan) {
+                            int32_t* __restrict__ plan, unsigned* __restrict__ pace) {
     dg::pdl_wait();
     dg::pdl_release();
-    if (blockIdx.x == 0 && blockIdx.y == 0) plan_list(params, converged, n, plan, 0);
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+        if (threadIdx.x == 0) *pace = 0u;
+        plan_list(params, converged, n, plan, 0);
+    }
     const int64_t c = blockIdx.y;
     if (self_cond_on(params[c], converged, c)) return;
     const int64_t vecs = (int64_t)L * d / 8;
@@ -1114,7 +1141,7 @@ bool tmap_logits(void* tm, int dt, const void* base, int64_t V, int32_t L, int64
 }
 
 struct SelfCondLayout {
-    size_t plan, pe, hmid, partial, total;
+    size_t plan, pace, pe, hmid, partial, total;
     int64_t rows;  // compact rows (n * L_pad)
 };
 
@@ -1123,7 +1150,8 @@ SelfCondLayout self_cond_layout(int64_t n, int32_t L, int32_t d, int32_t h, int 
     const int tpc = (L + BM - 1) / BM;
     l.rows = n * tpc * BM;
     l.plan = 0;
-    l.pe = align256(sizeof(int32_t) * (size_t)(n + 1));
+    l.pace = align256(sizeof(int32_t) * (size_t)(n + 1));
+    l.pe = l.pace + 256;
     l.hmid = l.pe + align256((size_t)l.rows * d * 2);
     l.partial = l.hmid + align256((size_t)l.rows * h * 2);
     // partial slots for the P.E GEMM (the only one that splits K)
@@ -1292,8 +1320,9 @@ dg_status dg_self_cond_prepare(const dg_canvas_params* params, const uint8_t* co
     const int64_t per_canvas = std::max<int64_t>(1, std::min<int64_t>(((int64_t)L * d / 8 + 255) / 256,
                                                                       (4LL * P + n_canvas - 1) / n_canvas));
     dim3 grid((unsigned)per_canvas, (unsigned)n_canvas);
+    unsigned* pace = reinterpret_cast<unsigned*>(static_cast<unsigned char*>(workspace) + lay.pace);
     const cudaError_t e = dghost::launch_pdl(k_zero_rows, grid, dim3(256), 0, st, params, converged, n_canvas, L, d,
-                                             delta_emb, plan);
+                                             delta_emb, plan, pace);
     dghost::count_launch();
     return dghost::cuda_status(e);
 }
@@ -1355,6 +1384,7 @@ dg_status dg_self_cond_pe(const void* logits, dg_dtype dtype, int64_t ld, const 
     g.partial = reinterpret_cast<float*>(ws + lay.partial);
     g.status = dghost::status_word();
     g.dyn_splits = 1;  // the plan lists the canvases with feedback: the device knows how many
+    g.pace = reinterpret_cast<unsigned*>(ws + lay.pace);
     const int64_t max_slots = pe_partial_slots(n_canvas, L, d, P);
     return dtype == DG_BF16 ? plan_and_launch<PEbf16>(tm.a, tm.b0, tm.b0, g, max_slots, st, kMinSliceK / bk)
                             : plan_and_launch<PEfp32>(tm.a, tm.b0, tm.b0, g, max_slots, st, kMinSliceK / bk);

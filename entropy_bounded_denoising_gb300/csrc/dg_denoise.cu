@@ -524,21 +524,25 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
                 (void)m2;
                 const uint64_t mm = f2(st.m, st.m), kk = f2(k2, k2);
                 uint64_t racc[2] = {0ull, 0ull}, tacc[2] = {0ull, 0ull};  // pairs of partial sums
-                auto vec2 = [&](int v) {
+                // TIE: the vector may hold entries equal to the running max (counted in c).  Only a
+                // lane whose own maximum over this piece equals it can hold one, so a piece without
+                // such a lane (a warp vote) skips the per-vector test.
+                auto vec2 = [&](int v, auto tie_tag) {
+                    constexpr bool TIE = decltype(tie_tag)::value;
                     const int j = (v * kK1Warps + warp) * 32 + lane;
                     const bool in = FULL || j < nvec;
                     const uint4 w = load_raw<DT, FULL>(slot, j, nvec, n_el);
-                    bool cand[GPV], tie;
+                    bool cand[GPV], tie = false;
                     if constexpr (DT == 0) {
                         const uint32_t g0 = bmax2(w.x, w.y), g1 = bmax2(w.z, w.w);
                         cand[0] = SAMPLE && in && bge2_any(g0, thr2);
                         cand[GPV - 1] = SAMPLE && in && bge2_any(g1, thr2);
-                        tie = beq2_any(bmax2(g0, g1), m2);
+                        if (TIE) tie = beq2_any(bmax2(g0, g1), m2);
                     } else {
                         const float vmax = max_nan(max_nan(__uint_as_float(w.x), __uint_as_float(w.y)),
                                                    max_nan(__uint_as_float(w.z), __uint_as_float(w.w)));
                         cand[0] = SAMPLE && in && vmax >= x_thr;
-                        tie = vmax == st.m;
+                        if (TIE) tie = vmax == st.m;
                     }
                     if (in) {
                         float x[VN];
@@ -613,10 +617,13 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
                 };
                 if constexpr (SAMPLE) {
 #pragma unroll 1
-                    for (int v = 0; v < kVecPerLane; ++v) vec2(v);  // rolled: one copy of the draw code
+                    for (int v = 0; v < kVecPerLane; ++v) vec2(v, std::true_type{});  // rolled: one copy of the draw code
+                } else if (FULL && !__any_sync(0xffffffffu, lane_max == st.m)) {
+#pragma unroll
+                    for (int v = 0; v < kVecPerLane; ++v) vec2(v, std::false_type{});
                 } else {
 #pragma unroll
-                    for (int v = 0; v < kVecPerLane; ++v) vec2(v);
+                    for (int v = 0; v < kVecPerLane; ++v) vec2(v, std::true_type{});
                 }
                 if (DT == 0) {
                     st.r += (f2_lo(racc[0]) + f2_hi(racc[0])) + (f2_lo(racc[1]) + f2_hi(racc[1]));

@@ -163,6 +163,16 @@ DG_DEVINL uint32_t bf16_floor2(float t) {
     return h | (h << 16);
 }
 
+// (lo - m, hi - m) for a bf16 pair, each with the mixed-precision subtract (bf16 operand, fp32
+// result): the bf16 value widens exactly and, with m itself a bf16 value, the difference is
+// exact in fp32 -- the same result as unpacking first, without the unpacking instructions.
+DG_DEVINL void bf16x2_sub_f32(uint32_t w, float m, float& lo, float& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tsub.rn.f32.bf16 %0, l, %3;\n\t"
+        "sub.rn.f32.bf16 %1, h, %3;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w), "f"(m));
+}
+
 // Packed fp32 pairs (sm_100 f32x2 arithmetic, round to nearest like the scalar forms).
 DG_DEVINL uint64_t f2(float a, float b) {
     uint64_t r;
@@ -567,7 +577,9 @@ __global__ void __launch_bounds__(kK1Threads, 3) k1_row_stats(
                                                     bmax2(w.z, kBf16NegFloor2), bmax2(w.w, kBf16NegFloor2)};
         #pragma unroll
                             for (int k = 0; k < 4; ++k) {
-                                const uint64_t d2 = f2_mul(f2_sub(f2(bf_lo(fw[k]), bf_hi(fw[k])), mm), kk);
+                                float dl, dh;
+                                bf16x2_sub_f32(fw[k], st.m, dl, dh);
+                                const uint64_t d2 = f2_mul(f2(dl, dh), kk);
                                 const uint64_t e2 = f2(ex2(f2_lo(d2)), ex2(f2_hi(d2)));
                                 racc[k & 1] = f2_add(racc[k & 1], e2);
                                 tacc[k & 1] = f2_fma(e2, d2, tacc[k & 1]);

@@ -169,3 +169,41 @@ def test_feedback_with_few_active_canvases_replans_on_device():
     rows = [0, 77, 255]
     ref = oracle.self_cond_rows(synth.host_logits(x[2, rows]), np.full(len(rows), 0.9), *bits, V=V)
     check_delta(dh[2, rows], ref)
+
+
+def test_feedback_plan_beyond_the_host_table():
+    """More than 256 canvases with feedback: the k-slice count is then evaluated on the device
+    (the host tabulates it only up to 256 listed canvases).  300 canvases of 8 positions
+    (each its own 128-row m-tile), all with feedback, against the oracle on sampled rows; and a
+    second call with 200 of them listed (the table) on the same inputs, checked the same way."""
+    n, L, V, d, h = 300, 8, 4096, 256, 512
+    x = synth.logits(n, L, V, seed=71, step=1, scale=(0.5, 12.0), spike_frac=0.1, device=DEV)
+    (E, Wg, Wu, Wd), bits = _weights(V, d, h, seed=5)
+    E, Wg, Wu, Wd = (t.to(DEV) for t in (E, Wg, Wu, Wd))
+    T = np.linspace(0.6, 1.4, n).astype(np.float32)
+    p = {"temperature": T, "beta": np.full(n, 4.0, np.float32), "tau": np.full(n, 0.3, np.float32),
+         "k": np.full(n, 2, np.int32), "max_steps": np.full(n, 64, np.int32), "min_accept": np.ones(n, np.int32),
+         "step": np.ones(n, np.int32), "request_id": np.arange(n, dtype=np.uint32),
+         "flags": np.full(n, dg.DG_ACTIVE | dg.DG_SELF_COND, np.uint32)}
+    ws = torch.empty(dg.dg_self_cond_workspace_bytes(n, L, d, h), dtype=torch.uint8, device=DEV)
+    hx = synth.host_logits(x)
+    for listed in (n, 200):
+        q = dict(p)
+        q["flags"] = p["flags"].copy()
+        q["flags"][listed:] = dg.DG_ACTIVE
+        pt = dg.params_tensor(q, DEV)
+        b = StepBuffers.make(n, L, DEV)
+        run_step(x, pt, 9, b)
+        delta = torch.full((n, L, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+        dg.dg_clear_device_status()
+        dg.dg_self_cond_logits(x, b.lse, pt, b.converged, E, Wg, Wu, Wd, delta, ws)
+        torch.cuda.synchronize()
+        assert dg.dg_get_device_status() == 0
+        dh = delta.float().cpu().numpy()
+        assert np.isfinite(dh).all()
+        if listed < n:
+            assert (dh[listed:] == 0).all()
+        for c in (0, 137, listed - 1):
+            ref = oracle.self_cond_rows(hx[c], np.full(L, float(T[c]), np.float64), *bits, V=V)
+            check_delta(dh[c], ref, (listed, c))
+

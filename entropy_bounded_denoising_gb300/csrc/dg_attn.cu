@@ -12,9 +12,9 @@
 // scale * q.k without soft-capping are readings, the pages give only the figures.
 //
 // Work items are (sequence, 128-query tile, query head); a plan kernel lists the items longest
-// first and two persistent CTAs per SM take them in turn (each 256 TMEM columns and under half
-// the shared memory, so one CTA's barrier waits are the other's issue slots); one pass with an
-// online softmax per item:
+// first and two persistent CTAs per SM take them from a counter as they free up (each 256 TMEM
+// columns and under half the shared memory, so one CTA's barrier waits are the other's issue
+// slots); one pass with an online softmax per item:
 //   warp 0      TMA producers: the Q tile once, then K and V tiles (64 keys) in two 2-stage
 //               rings (a K buffer frees when its S MMA is done, a V buffer after its P V);
 //   warp 1      MMA issuer (one elected thread): S = Q K^T (128 x 64) into TMEM, issued as soon
@@ -72,9 +72,14 @@ struct __align__(8) AttnShared {
     uint64_t vempty[2];
     uint64_t sfull;
     uint64_t sempty;
-    uint64_t pfull;
+    uint64_t pfull[2];        // P buffer b written by the four softmax warps (one barrier per buffer:
+                              // with one for both, a warp a tile ahead could complete the phase of
+                              // a tile whose P another warp is still writing)
     uint64_t pvdone[2];       // P V of the tiles using P buffer 0 / 1 done
     uint64_t mmadone;
+    uint64_t wfull[4];        // the item queue: slot k % 4 holds the CTA's k-th work index
+    uint64_t wempty[4];       // (-1: no more), taken by its 7 readers
+    int64_t item_w[4];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -211,6 +216,39 @@ DG_DEVINL bool attn_wait_warp(uint64_t* bar, uint32_t parity) {
 
 DG_DEVINL bool aborted(const AttnShared& sh) { return *(volatile const int*)&sh.abort_flag != 0; }
 
+// Which items a CTA works.  When they all cost the same, CTA b takes b, b + grid, ...: with two
+// CTAs per SM that spreads the last round over distinct SMs (claiming from a counter lets both
+// CTAs of an SM, which finish together, take the last items together).  When they differ, the
+// CTA's Q producer claims the next work index from a launch-wide counter once the Q buffer
+// frees (later claims balance better: a CTA holds at most the item it is computing and the
+// claimed one, and CTAs that finish early take more; the items are ordered longest first) and
+// publishes it in the CTA's item queue, where the K and V producers, the MMA issuer and the
+// four softmax warps read it in turn.
+constexpr int kQueueReaders = 7;
+
+DG_DEVINL int64_t take_item(AttnShared& sh, uint32_t k, bool& ok) {
+    const int slot = (int)(k & 3u);
+    if (!attn_wait(&sh.wfull[slot], (k >> 2) & 1u)) {
+        ok = false;
+        return -1;
+    }
+    const int64_t w = *(volatile int64_t*)&sh.item_w[slot];
+    dg::mbar_arrive(&sh.wempty[slot]);
+    return w;
+}
+
+DG_DEVINL int64_t take_item_warp(AttnShared& sh, uint32_t k, bool& ok) {
+    const int slot = (int)(k & 3u);
+    if (!attn_wait_warp(&sh.wfull[slot], (k >> 2) & 1u)) {
+        ok = false;
+        return -1;
+    }
+    const int64_t w = *(volatile int64_t*)&sh.item_w[slot];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) dg::mbar_arrive(&sh.wempty[slot]);
+    return w;
+}
+
 DG_DEVINL void do_abort(AttnShared& sh, unsigned* status) {
     *(volatile int*)&sh.abort_flag = 1;
     dg::raise_status(status, DG_DEV_TIMEOUT);
@@ -219,11 +257,11 @@ DG_DEVINL void do_abort(AttnShared& sh, unsigned* status) {
 // ------------------------------------------------------------------ the plan
 // Work items are (sequence, 128-query tile) pairs with at least one query.  One CTA lists them
 // by decreasing cost (key tiles visited; a counting sort over kCostBuckets), so that the
-// persistent CTAs, which take items round robin, start with the longest.  A sequence whose
+// persistent CTAs, which take items in that order, start with the longest.  A sequence whose
 // offsets or lengths are out of range, or that has more queries than max_q_tiles tiles hold,
 // raises DG_DEV_BAD_PARAM and is left out (wholly, or its tiles past max_q_tiles).
 constexpr int kCostBuckets = 1024;
-constexpr int kPlanHeader = 4;  // ints before the items: the item count, padding
+constexpr int kPlanHeader = 4;  // ints before the items: the item count, a one-cost flag, a 64-bit work counter
 
 __global__ void __launch_bounds__(1024) k_attn_plan(const AttnArgs a, int32_t n_seq, int32_t max_q_tiles,
                                                     int32_t* __restrict__ plan) {
@@ -231,6 +269,7 @@ __global__ void __launch_bounds__(1024) k_attn_plan(const AttnArgs a, int32_t n_
     __shared__ int warp_sum[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int b = tid; b < kCostBuckets; b += blockDim.x) count[b] = 0;
+    if (tid == 0) *reinterpret_cast<unsigned long long*>(plan + 2) = 0ull;  // the attention kernel's work counter
     __syncthreads();
     const int64_t pairs = (int64_t)n_seq * max_q_tiles;
     auto item_key = [&](int64_t f, int& key) -> bool {  // false: no item (past the queries or bad)
@@ -250,6 +289,10 @@ __global__ void __launch_bounds__(1024) k_attn_plan(const AttnArgs a, int32_t n_
     __syncthreads();
     // exclusive prefix over the buckets (one per thread): warp scans, then the warp totals
     const int c = tid < kCostBuckets ? count[tid] : 0;
+    // items of one cost: the kernel's CTAs take them round robin (balanced per SM), else from
+    // the counter (list scheduling, longest first)
+    const int n_costs = __syncthreads_count(c > 0);
+    if (tid == 0) plan[1] = n_costs <= 1 ? 1 : 0;
     int incl = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -280,10 +323,11 @@ __global__ void __launch_bounds__(1024) k_attn_plan(const AttnArgs a, int32_t n_
 }
 
 // ------------------------------------------------------------------ the kernel
-// Persistent: CTA b takes work w = b, b + gridDim.x, ... of n_items * Hq (item w / Hq, head
-// w % Hq).  Every ring, buffer and barrier phase is counted over the CTA's whole run (g: its
-// key tiles so far, k: its items so far), so the next item's Q and K / V loads and its first
-// S MMA overlap the current item's last tiles and its epilogue.
+// Persistent: the CTAs take work indices w of n_items * Hq (item w / Hq, head w % Hq) from a
+// counter, in the plan's order (longest first), through the item queue above.  Every ring,
+// buffer and barrier phase is counted over the CTA's whole run (g: its key tiles so far, k: its
+// items so far), so the next item's Q and K / V loads and its first S MMA overlap the current
+// item's last tiles and its epilogue.
 template <int D>
 __global__ void __launch_bounds__(kThreads, AttnCfg<D>::kCtasPerSm)
     k_attention(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -302,6 +346,11 @@ __global__ void __launch_bounds__(kThreads, AttnCfg<D>::kCtasPerSm)
     if ((int64_t)blockIdx.x >= n_work) return;  // the whole CTA: no work
     const int2* items = reinterpret_cast<const int2*>(plan + kPlanHeader);
     const int group = a.Hq / a.Hkv;
+    const bool round_robin = plan[1] != 0;
+    auto rr_item = [&](uint32_t k) -> int64_t {
+        const int64_t w = (int64_t)blockIdx.x + (int64_t)k * gridDim.x;
+        return w < n_work ? w : -1;
+    };
 
     if (threadIdx.x == 0) {
         dg::mbar_init(&sh.qfull, 1);
@@ -316,8 +365,13 @@ __global__ void __launch_bounds__(kThreads, AttnCfg<D>::kCtasPerSm)
         }
         dg::mbar_init(&sh.sfull, 1);
         dg::mbar_init(&sh.sempty, 4);
-        dg::mbar_init(&sh.pfull, 4);
+        dg::mbar_init(&sh.pfull[0], 4);
+        dg::mbar_init(&sh.pfull[1], 4);
         dg::mbar_init(&sh.mmadone, 1);
+        for (int i = 0; i < 4; ++i) {
+            dg::mbar_init(&sh.wfull[i], 1);
+            dg::mbar_init(&sh.wempty[i], kQueueReaders);
+        }
         sh.abort_flag = 0;
         dg::fence_mbar_init();
     }
@@ -336,15 +390,28 @@ __global__ void __launch_bounds__(kThreads, AttnCfg<D>::kCtasPerSm)
         // the V ring, lane 2 the Q tile of each item (once the last item's last S has read it)
         if (lane == 2) {
             dg::prefetch_tmap(&tmQ);
+            unsigned long long* counter = reinterpret_cast<unsigned long long*>(const_cast<int32_t*>(plan) + 2);
             uint32_t kq = 0;
             bool ok = true;
-            for (int64_t w = blockIdx.x; w < n_work && !aborted(sh); w += gridDim.x, ++kq) {
-                const int2 it = items[w / a.Hq];
-                const int h = (int)(w % a.Hq);
-                if (!attn_wait(&sh.qempty, (kq & 1u) ^ 1u)) {
+            for (;; ++kq) {
+                const int slot = (int)(kq & 3u);
+                if (!attn_wait(&sh.qempty, (kq & 1u) ^ 1u) ||
+                    (!round_robin && !attn_wait(&sh.wempty[slot], ((kq >> 2) & 1u) ^ 1u))) {
                     ok = false;
                     break;
                 }
+                int64_t w;
+                if (round_robin) {
+                    w = rr_item(kq);
+                } else {
+                    w = (int64_t)atomicAdd(counter, 1ull);
+                    if (w >= n_work || aborted(sh)) w = -1;
+                    sh.item_w[slot] = w;
+                    dg::mbar_arrive(&sh.wfull[slot]);  // releases the index to the readers
+                }
+                if (w < 0 || aborted(sh)) break;
+                const int2 it = items[w / a.Hq];
+                const int h = (int)(w % a.Hq);
                 const int qrow = a.cu_q[it.x] + it.y * kTile;
                 dg::mbar_arrive_expect_tx(&sh.qfull, kQBytes);
 #pragma unroll
@@ -363,7 +430,9 @@ __global__ void __launch_bounds__(kThreads, AttnCfg<D>::kCtasPerSm)
             uint32_t g = 0;
             int issued[2] = {0, 0};
             bool ok = true;
-            for (int64_t w = blockIdx.x; w < n_work && ok && !aborted(sh); w += gridDim.x) {
+            for (uint32_t k = 0; ok && !aborted(sh); ++k) {
+                const int64_t w = round_robin ? rr_item(k) : take_item(sh, k, ok);
+                if (w < 0) break;
                 const int2 it = items[w / a.Hq];
                 const int hk = (int)(w % a.Hq) / group;
                 const TileRange r = tile_range(a, it.x, it.y);
@@ -395,7 +464,9 @@ __global__ void __launch_bounds__(kThreads, AttnCfg<D>::kCtasPerSm)
             constexpr uint32_t idO = dg::instr_desc(kTile, kHead, true);   // O += P V: V rows are N-major
             uint32_t g = 0, kq = 0;
             bool ok = true;
-            for (int64_t w = blockIdx.x; w < n_work && ok && !aborted(sh); w += gridDim.x, ++kq) {
+            for (; ok && !aborted(sh); ++kq) {
+                const int64_t w = round_robin ? rr_item(kq) : take_item(sh, kq, ok);
+                if (w < 0) break;
                 const int2 it = items[w / a.Hq];
                 const TileRange r = tile_range(a, it.x, it.y);
                 if (!attn_wait(&sh.qfull, kq & 1u)) {
@@ -427,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, AttnCfg<D>::kCtasPerSm)
                         const int j = i - 1;
                         const uint32_t gp = g + (uint32_t)j;
                         const int st = (int)(gp & 1u);
-                        if (!attn_wait(&sh.pfull, gp & 1u) || !attn_wait(&sh.vfull[st], (gp >> 1) & 1u) ||
+                        if (!attn_wait(&sh.pfull[st], (gp >> 1) & 1u) || !attn_wait(&sh.vfull[st], (gp >> 1) & 1u) ||
                             (j == 0 && !attn_wait(&sh.oempty, (kq & 1u) ^ 1u))) {  // the last item's O read out
                             ok = false;
                             break;
@@ -460,7 +531,9 @@ __global__ void __launch_bounds__(kThreads, AttnCfg<D>::kCtasPerSm)
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         uint32_t g = 0, kq = 0;
         bool ok = true;
-        for (int64_t w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++kq) {
+        for (; ok; ++kq) {
+            const int64_t w = round_robin ? rr_item(kq) : take_item_warp(sh, kq, ok);
+            if (w < 0) break;
             const int2 it = items[w / a.Hq];
             const int h = (int)(w % a.Hq);
             const TileRange r = tile_range(a, it.x, it.y);
@@ -480,7 +553,8 @@ __global__ void __launch_bounds__(kThreads, AttnCfg<D>::kCtasPerSm)
                     uint32_t raw[2][32];
 #pragma unroll
                     for (int c = 0; c < 2; ++c) dg::tmem_ld32_nowait(tmem + lane_base + kColS + (uint32_t)(c * 32), raw[c]);
-                    dg::tmem_ld_wait();
+                    dg::tmem_ld_wait_dep(raw[0]);
+                    dg::tmem_ld_wait_dep(raw[1]);  // (returns at once: no load is left in flight)
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -541,8 +615,8 @@ __global__ void __launch_bounds__(kThreads, AttnCfg<D>::kCtasPerSm)
 #pragma unroll
                             for (int e = 0; e < 32; ++e) o[e] *= alpha;
                             dg::tmem_st32(ta, o);
+                            dg::tmem_st_wait();  // before the next chunk's load may reuse the registers
                         }
-                        dg::tmem_st_wait();
                     }
                     m_ref = m_new;
                 }
@@ -571,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, AttnCfg<D>::kCtasPerSm)
                 l += sa + sb;
                 dg::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) dg::mbar_arrive(&sh.pfull);
+                if (lane == 0) dg::mbar_arrive(&sh.pfull[gi & 1u]);
             }
             if (!ok) break;
             const uint32_t gl = g + (uint32_t)r.nt - 1u;  // the item's last P V

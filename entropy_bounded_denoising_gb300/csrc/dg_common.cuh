@@ -372,6 +372,20 @@ DG_DEVINL void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
 
 DG_DEVINL void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// The wait with the registers a tmem_ld32_nowait wrote passed through it: they are undefined
+// until the wait, and an operand dependency is what keeps the compiler from scheduling a use of
+// them before it (a plain volatile asm orders memory and other asm, not register arithmetic).
+DG_DEVINL void tmem_ld_wait_dep(uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.wait::ld.sync.aligned;"
+        : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+          "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+          "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+          "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+        :
+        : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets lane (base + t).
 DG_DEVINL void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
@@ -384,13 +398,14 @@ DG_DEVINL void tmem_ld32(uint32_t taddr, float (&v)[32]) {
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
         : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    tmem_ld_wait_dep(r);
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // The same direction: 32 lanes x 32 consecutive columns from registers (whole warp); the
-// caller waits with tmem_st_wait before anything reads the columns.
+// caller waits with tmem_st_wait before anything reads the columns, and before the source
+// registers can be written again (the store is asynchronous).
 DG_DEVINL void tmem_st32(uint32_t taddr, const float (&v)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "

@@ -308,3 +308,29 @@ def test_split_step_on_two_streams_matches_one_call():
         for k in h1:
             assert np.array_equal(h1[k], h2[k]), (t, k)
         assert (h2["sample"][0][h2["accept"][0] == 1] >= 0).all()
+
+
+def test_whole_step_hand_worked_5x4x8():
+    """The CUDA step over three steps against the hand-worked whole-step fixture (the same
+    values the oracle is pinned to; tests/golden/step_worked_5x4x8.json says how each was
+    worked out): entropies 0, ln 2, 2 ln 2 and lse = 0.5/T + ln|support| within fp32
+    rounding, everything else exact."""
+    from test_oracle_pins import _worked_step, check_worked_step, worked_step_inputs
+    g = _worked_step()
+    x, p, canvas = worked_step_inputs(g)
+    n, L = canvas.shape
+    xd = torch.from_numpy(x).to(DEV)
+    b = StepBuffers.make(n, L, DEV, canvas)
+    dg.dg_clear_device_status()
+    for t in range(g["steps"]):
+        p["step"][:] = t
+        before = b.canvas.cpu().numpy().copy()
+        run_step(xd, dg.params_tensor(p, DEV), g["seed"], b)
+        torch.cuda.synchronize()
+        h = b.host()
+        out = {"canvas": h["canvas"], "prev_argmax": h["prev"], "stable_count": h["stable"],
+               "accept_mask": h["accept"], "argmax": h["argmax"], "entropy": h["entropy"].astype(np.float64),
+               "lse": h["lse"].astype(np.float64), "converged": h["converged"],
+               "mean_entropy": h["mean_entropy"].astype(np.float64), "n_accept": h["n_accept"]}
+        check_worked_step(g, t, out, before, ent_tol=2e-6, lse_rel=1e-6)
+    assert dg.dg_get_device_status() == 0

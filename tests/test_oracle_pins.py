@@ -8,6 +8,7 @@ entropy-bound rule, the convergence rule), "자기 조건화" (self-conditioning
 "DiffusionGemmaModelState와 DiffusionSampler" (Gumbel-max candidate, renoise, argmax canvas);
 Salmon et al., SC'11, for Philox-4x32.
 """
+import ctypes
 import itertools
 import json
 import math
@@ -293,6 +294,89 @@ def test_acceptance_hand_worked_4x8():
                 assert out["canvas"][0, i] == out["sample"][0, i]
 
 
+def _worked_step():
+    with open(os.path.join(GOLDEN, "step_worked_5x4x8.json")) as f:
+        return json.load(f)
+
+
+def _contract_token(seed, request_id, step, position, V):
+    """A renoise token by the random-number contract, restated here from its definition: the
+    Philox-4x32-10 block (pinned above as the published bijection) at counter (0, position,
+    step, 1 | seed bits 32..55 << 8) and key (low word of seed, request_id); the token is the
+    integer part of (w0:w1) * V / 2^64 in exact integer arithmetic."""
+    w = oracle.philox4x32([0, position, step, 1 | (((seed >> 32) & 0xFFFFFF) << 8)],
+                          [seed & 0xFFFFFFFF, request_id])
+    return ((int(w[0]) << 32) | int(w[1])) * V >> 64
+
+
+def worked_step_inputs(g):
+    """Logits [n, L, V] (fp32), parameters and initial state of the hand-worked whole step."""
+    n, L, V = len(g["canvases"]), g["L"], g["V"]
+    x = np.full((n, L, V), NEG_INF, np.float32)
+    for c, cv in enumerate(g["canvases"]):
+        for i, sup in enumerate(cv["supports"]):
+            x[c, i, sup] = 0.5
+    flag = {"active": oracle.ACTIVE, "read_only": oracle.READ_ONLY}
+    p = {"temperature": np.array([cv["temperature"] for cv in g["canvases"]], np.float32),
+         "beta": np.array([cv["beta"] for cv in g["canvases"]], np.float32),
+         "tau": np.array([cv["tau"] for cv in g["canvases"]], np.float32),
+         "k": np.array([cv["k"] for cv in g["canvases"]], np.int32),
+         "max_steps": np.array([cv["max_steps"] for cv in g["canvases"]], np.int32),
+         "min_accept": np.array([cv["min_accept"] for cv in g["canvases"]], np.int32),
+         "step": np.zeros(n, np.int32),
+         "request_id": np.array([cv["request_id"] for cv in g["canvases"]], np.uint32),
+         "flags": np.array([sum(flag[f] for f in cv["flags"]) for cv in g["canvases"]], np.uint32)}
+    return x, p, np.array(g["initial_canvas"], np.int32)
+
+
+def check_worked_step(g, t, out, canvas_before, ent_tol, lse_rel):
+    """The outputs of step t against the hand-worked values (out: canvas, prev_argmax,
+    stable_count, accept_mask, argmax, entropy, lse, converged, mean_entropy, n_accept)."""
+    ln2 = math.log(2)
+    for c, cv in enumerate(g["canvases"]):
+        if cv.get("inactive"):
+            assert np.array_equal(out["canvas"][c], canvas_before[c]), (t, c)
+            assert (out["prev_argmax"][c] == -1).all() and out["stable_count"][c] == 0, (t, c)
+            continue
+        ctx = (t, c, cv["what"][:40])
+        H = np.array(cv["entropy_in_ln2"], np.float64) * ln2
+        assert np.all(np.abs(out["entropy"][c] - H) <= ent_tol), (ctx, out["entropy"][c])
+        lse = 0.5 / cv["temperature"] + np.log([len(s) for s in cv["supports"]])
+        assert np.all(np.abs(out["lse"][c] - lse) <= lse_rel * np.maximum(np.abs(lse), 1.0)), (ctx, out["lse"][c])
+        assert out["argmax"][c].tolist() == cv["argmax"], ctx
+        assert out["prev_argmax"][c].tolist() == cv["argmax"], ctx
+        assert abs(out["mean_entropy"][c] - cv["mean_entropy_in_ln2"] * ln2) <= ent_tol, ctx
+        assert sorted(np.nonzero(out["accept_mask"][c])[0].tolist()) == cv["accepted"], ctx
+        assert int(out["n_accept"][c]) == len(cv["accepted"]), ctx
+        read_only = "read_only" in cv["flags"]
+        for i in range(g["L"]):
+            if read_only:
+                want = canvas_before[c, i]
+            elif i in cv["accepted"]:
+                want = cv["supports"][i][0]          # a one-token support: its sample
+            else:
+                want = _contract_token(g["seed"], cv["request_id"], t, i, g["V"])
+            assert out["canvas"][c, i] == want, (ctx, i)
+        assert int(out["stable_count"][c]) == cv["stable_count"][t], ctx
+        assert int(out["converged"][c]) == cv["converged"][t], ctx
+
+
+def test_whole_step_hand_worked_5x4x8():
+    """The composed step (statistics, acceptance, canvas update, convergence) over three
+    steps against values worked out by hand from the method's rules (the fixture's source
+    says which): five canvases covering acceptance by the budget, the step cap, read-only,
+    inactive and nothing-accepted canvases."""
+    g = _worked_step()
+    x, p, canvas = worked_step_inputs(g)
+    n, L = canvas.shape
+    prev, stable = np.full((n, L), -1, np.int32), np.zeros(n, np.int32)
+    for t in range(g["steps"]):
+        p["step"][:] = t
+        out = oracle.denoise_step(x, p, g["seed"], canvas, prev, stable)
+        check_worked_step(g, t, out, canvas, ent_tol=1e-15, lse_rel=1e-15)
+        canvas, prev, stable = out["canvas"], out["prev_argmax"], out["stable_count"]
+
+
 def test_acceptance_entropy_only_cases():
     for case in _golden()["entropy_only_cases"]:
         r = oracle.accept(case["H"], case["beta"], case["min_accept"])
@@ -535,6 +619,35 @@ def test_planted_canvas_init_stream_fails_the_pin(tmp_path):
                                       "(uint32_t)i, ORC_STREAM_RENOISE, (uint32_t)V);")
     with pytest.raises(AssertionError):
         _check_canvas_init(canvas_init, oracle.random_token)
+
+
+@pytest.mark.parametrize("old,new", [
+    # a rejected position renoised with the next position's draw
+    ("(uint32_t)step[c], (uint32_t)i, ORC_STREAM_RENOISE, (uint32_t)V);",
+     "(uint32_t)step[c], (uint32_t)i + 1u, ORC_STREAM_RENOISE, (uint32_t)V);"),
+    # either convergence condition instead of both
+    ("(st >= k[c] && Hbar < (double)tau[c])", "(st >= k[c] || Hbar < (double)tau[c])"),
+    # the stable count not reset when the argmax canvas changes
+    ("int32_t st = same ? stable_count[c] + 1 : 0;", "int32_t st = stable_count[c] + 1;"),
+    # the step cap one step late
+    ("(step[c] + 1 >= max_steps[c])", "(step[c] >= max_steps[c])"),
+])
+def test_planted_step_mistakes_fail_the_worked_step(tmp_path, monkeypatch, old, new):
+    lib, _ = _mutant_oracle(tmp_path, old, new)
+    P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    lib.orc_denoise_step.argtypes = [P, ctypes.c_int, i64, i64, i32, i64] + [P] * 9 + [ctypes.c_uint64] + [P] * 15 + [ctypes.c_int]
+    lib.orc_philox4x32.argtypes = [P, P, ctypes.c_int, P]
+    monkeypatch.setattr(oracle, "_lib", lib)   # the wrapper calls the mutant; restored after the test
+    g = _worked_step()
+    x, p, canvas = worked_step_inputs(g)
+    n, L = canvas.shape
+    prev, stable = np.full((n, L), -1, np.int32), np.zeros(n, np.int32)
+    with pytest.raises(AssertionError):
+        for t in range(g["steps"]):
+            p["step"][:] = t
+            out = oracle.denoise_step(x, p, g["seed"], canvas, prev, stable)
+            check_worked_step(g, t, out, canvas, ent_tol=1e-15, lse_rel=1e-15)
+            canvas, prev, stable = out["canvas"], out["prev_argmax"], out["stable_count"]
 
 
 def test_gated_mlp_closed_forms():

@@ -12,9 +12,10 @@
 // scale * q.k without soft-capping are readings, the pages give only the figures.
 //
 // Work items are (sequence, 128-query tile, query head); a plan kernel lists the items longest
-// first and two persistent CTAs per SM take them from a counter as they free up (each 256 TMEM
-// columns and under half the shared memory, so one CTA's barrier waits are the other's issue
-// slots); one pass with an online softmax per item:
+// first and two persistent CTAs per SM take them, from a counter as they free up when the items
+// differ in cost, round robin when they do not (each CTA 256 TMEM columns and under half the
+// shared memory, so one CTA's barrier waits are the other's issue slots); one pass with an
+// online softmax per item:
 //   warp 0      TMA producers: the Q tile once, then K and V tiles (64 keys) in two 2-stage
 //               rings (a K buffer frees when its S MMA is done, a V buffer after its P V);
 //   warp 1      MMA issuer (one elected thread): S = Q K^T (128 x 64) into TMEM, issued as soon
@@ -323,8 +324,9 @@ __global__ void __launch_bounds__(1024) k_attn_plan(const AttnArgs a, int32_t n_
 }
 
 // ------------------------------------------------------------------ the kernel
-// Persistent: the CTAs take work indices w of n_items * Hq (item w / Hq, head w % Hq) from a
-// counter, in the plan's order (longest first), through the item queue above.  Every ring,
+// Persistent: the CTAs take work indices w of n_items * Hq (item w / Hq, head w % Hq) in the
+// plan's order (longest first), round robin or from the counter through the item queue (see
+// above).  Every ring,
 // buffer and barrier phase is counted over the CTA's whole run (g: its key tiles so far, k: its
 // items so far), so the next item's Q and K / V loads and its first S MMA overlap the current
 // item's last tiles and its epilogue.

@@ -368,11 +368,16 @@ def run_ours(args):
             dg.dg_lm_head_denoise_step(hid, E, params, seed, xs, canvas, prev, stable, acc, am, smp, ent, lse,
                                        conv, workspace=lws, stream=stream)
         elif overlap:
+            # the feedback plan needs no statistics: first, so that P.E follows the statistics
+            # pass directly (its CTAs take the SMs the pass leaves free and bring their first
+            # embedding tiles into L2 while it runs)
+            dg.dg_self_cond_prepare(params, None, n, L, d, h, delta, wsp, stream=stream)
             dg.dg_denoise_row_stats(xin, params, seed, am, smp, ent, lse, dws, stream=stream)
         else:
             dg.dg_denoise_step(xin, params, seed, canvas, prev, stable, acc, am, smp, ent, lse, conv,
                                workspace=dws, stream=stream)
-        dg.dg_self_cond_prepare(params, None if overlap else conv, n, L, d, h, delta, wsp, stream=stream)
+        if not overlap:
+            dg.dg_self_cond_prepare(params, conv, n, L, d, h, delta, wsp, stream=stream)
         if ev:
             ev[1].record(stream)
         dg.dg_self_cond_pe(xs if fh else xin, lse, params, E, h, wsp, stream=stream)

@@ -2,7 +2,7 @@
 
 In line: dg_denoise_step, then dg_self_cond_logits with the step's converged flags.
 Overlapped (what the benchmark runs for small batches): on the main stream
-dg_denoise_row_stats, dg_self_cond_prepare with converged = NULL and dg_self_cond_pe; then
+dg_self_cond_prepare with converged = NULL, dg_denoise_row_stats and dg_self_cond_pe; then
 dg_denoise_accept and dg_denoise_samples on a second stream while dg_self_cond_mlp runs on the
 main one; then, after an event from the second stream, dg_self_cond_zero_converged.  Every
 output (canvas, state, statistics, samples, acceptance, convergence and the feedback rows)
@@ -31,9 +31,9 @@ def _run(x, pt, seed, b, delta, ws_d, ws_s, weights, V, overlapped, main, side):
                            b.converged, b.mean_entropy, b.n_accept, workspace=ws_d, V=V, stream=main)
         dg.dg_self_cond_logits(x, b.lse, pt, b.converged, E, Wg, Wu, Wd, delta, ws_s, V=V, stream=main)
         return
+    dg.dg_self_cond_prepare(pt, None, n, L, delta.shape[2], h, delta, ws_s, stream=main)
     dg.dg_denoise_row_stats(x, pt, seed, b.argmax, b.sample, b.entropy, b.lse, ws_d, V=V, stream=main)
     fork, accept_done = torch.cuda.Event(), torch.cuda.Event()
-    dg.dg_self_cond_prepare(pt, None, n, L, delta.shape[2], h, delta, ws_s, stream=main)
     dg.dg_self_cond_pe(x, b.lse, pt, E, h, ws_s, V=V, stream=main)
     fork.record(main)
     side.wait_event(fork)

@@ -326,10 +326,9 @@ __global__ void __launch_bounds__(1024) k_attn_plan(const AttnArgs a, int32_t n_
 // ------------------------------------------------------------------ the kernel
 // Persistent: the CTAs take work indices w of n_items * Hq (item w / Hq, head w % Hq) in the
 // plan's order (longest first), round robin or from the counter through the item queue (see
-// above).  Every ring,
-// buffer and barrier phase is counted over the CTA's whole run (g: its key tiles so far, k: its
-// items so far), so the next item's Q and K / V loads and its first S MMA overlap the current
-// item's last tiles and its epilogue.
+// above).  Every ring, buffer and barrier phase is counted over the CTA's whole run (g: its key
+// tiles so far, k: its items so far), so the next item's Q and K / V loads and its first S MMA
+// overlap the current item's last tiles and its epilogue.
 template <int D>
 __global__ void __launch_bounds__(kThreads, AttnCfg<D>::kCtasPerSm)
     k_attention(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
